@@ -1,0 +1,218 @@
+"""CPU oracle for the lattice-PIR database scan (ctypes wrapper over oracle.c).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package; the product library
+and its Python binding never do.  The oracle shares no code with the CUDA path.
+
+Every function restates a definition from the pages (see oracle.c):
+  * VIPIR (CSDN translation), sections 2.2-2.5, 4.1-4.3: RNS primes, the
+    negacyclic NTT, the INT8 x INT32 scan mod 2^32;
+  * GPIR (arXiv 2604.04696), section 2: RowSel as point-wise GEMMs
+    M_out[p,m,n] = sum_k M_in0[p,m,k] * M_in1[p,k,n] mod q.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+_u32p = ctypes.POINTER(ctypes.c_uint32)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc into liboracle.so (portable flags only)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread",
+                               "-o", tmp, _SRC])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        L.orc_powmod.restype = ctypes.c_uint32
+        L.orc_powmod.argtypes = [ctypes.c_uint32, ctypes.c_uint64, ctypes.c_uint32]
+        L.orc_invmod.restype = ctypes.c_uint32
+        L.orc_invmod.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+        L.orc_is_prime.restype = ctypes.c_int
+        L.orc_is_prime.argtypes = [ctypes.c_uint32]
+        L.orc_primes.restype = ctypes.c_int
+        L.orc_primes.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, _u32p]
+        L.orc_min_psi.restype = ctypes.c_uint32
+        L.orc_min_psi.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+        L.orc_bitrev.restype = ctypes.c_uint32
+        L.orc_bitrev.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+        for name in ("orc_ntt_direct", "orc_intt_direct"):
+            f = getattr(L, name)
+            f.restype = None
+            f.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p]
+        for name in ("orc_ntt_iter", "orc_intt_iter"):
+            f = getattr(L, name)
+            f.restype = None
+            f.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, _u32p]
+        L.orc_negacyclic_mul.restype = None
+        L.orc_negacyclic_mul.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, _u32p]
+        L.orc_ntt_polys.restype = None
+        L.orc_ntt_polys.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint64,
+                                    _u32p, _u32p, ctypes.c_int, ctypes.c_int]
+        L.orc_encode_records.restype = None
+        L.orc_encode_records.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p,
+                                         ctypes.c_uint64, _u32p, _u32p, ctypes.c_int]
+        L.orc_rowsel.restype = None
+        L.orc_rowsel.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, ctypes.c_uint32,
+                                 ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint32,
+                                 _u32p, _u32p, ctypes.c_int]
+        L.orc_scalar_scan.restype = None
+        L.orc_scalar_scan.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32, _u8p,
+                                      _u32p, _u32p, ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _p32(a: np.ndarray):
+    assert a.dtype == np.uint32 and a.flags["C_CONTIGUOUS"], (a.dtype, a.flags)
+    return a.ctypes.data_as(_u32p)
+
+
+def _p8(a: np.ndarray):
+    assert a.dtype == np.uint8 and a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(_u8p)
+
+
+# --------------------------------------------------------------- parameters
+def is_prime(q: int) -> bool:
+    return bool(lib().orc_is_prime(q))
+
+
+def primes(N: int, count: int, bound: int = 1 << 29) -> list[int]:
+    """The `count` largest primes < bound with q = 1 mod 2N, descending."""
+    out = np.zeros(count, dtype=np.uint32)
+    n = lib().orc_primes(N, count, bound, _p32(out))
+    return [int(x) for x in out[:n]]
+
+
+def min_psi(q: int, N: int) -> int:
+    """Smallest g with g^N = -1 mod q (a primitive 2N-th root of unity)."""
+    return int(lib().orc_min_psi(q, N))
+
+
+def powmod(b: int, e: int, q: int) -> int:
+    return int(lib().orc_powmod(b, e, q))
+
+
+def invmod(a: int, q: int) -> int:
+    return int(lib().orc_invmod(a, q))
+
+
+def bitrev(x: int, bits: int) -> int:
+    return int(lib().orc_bitrev(x, bits))
+
+
+# --------------------------------------------------------------- NTT
+def ntt_direct(a: np.ndarray, q: int, psi: int) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.uint32)
+    out = np.empty_like(a)
+    lib().orc_ntt_direct(q, psi, a.size, _p32(a), _p32(out))
+    return out
+
+
+def intt_direct(a: np.ndarray, q: int, psi: int) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.uint32)
+    out = np.empty_like(a)
+    lib().orc_intt_direct(q, psi, a.size, _p32(a), _p32(out))
+    return out
+
+
+def ntt_iter(a: np.ndarray, q: int, psi: int) -> np.ndarray:
+    out = np.array(a, dtype=np.uint32, copy=True, order="C")
+    lib().orc_ntt_iter(q, psi, out.size, _p32(out))
+    return out
+
+
+def intt_iter(a: np.ndarray, q: int, psi: int) -> np.ndarray:
+    out = np.array(a, dtype=np.uint32, copy=True, order="C")
+    lib().orc_intt_iter(q, psi, out.size, _p32(out))
+    return out
+
+
+def negacyclic_mul(a: np.ndarray, b: np.ndarray, q: int) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.uint32)
+    b = np.ascontiguousarray(b, dtype=np.uint32)
+    c = np.empty_like(a)
+    lib().orc_negacyclic_mul(q, a.size, _p32(a), _p32(b), _p32(c))
+    return c
+
+
+def ntt_polys(polys: np.ndarray, qs, psis, inverse: bool = False, threads: int | None = None) -> np.ndarray:
+    """Transform an array [..., L, N] of RNS polynomials (row l uses qs[l])."""
+    polys = np.ascontiguousarray(polys, dtype=np.uint32)
+    L, N = polys.shape[-2], polys.shape[-1]
+    cnt = polys.size // (L * N)
+    q = np.asarray(qs, dtype=np.uint32)
+    ps = np.asarray(psis, dtype=np.uint32)
+    out = np.empty_like(polys)
+    lib().orc_ntt_polys(N, L, _p32(q), _p32(ps), cnt, _p32(polys), _p32(out), int(inverse),
+                        threads or default_threads())
+    return out
+
+
+def encode_records(raw: np.ndarray, qs, psis, threads: int | None = None) -> np.ndarray:
+    """raw [..., N] coefficients in [0, 2^16) -> NTT form [..., L, N]."""
+    raw = np.ascontiguousarray(raw, dtype=np.uint32)
+    N = raw.shape[-1]
+    cnt = raw.size // N
+    L = len(qs)
+    q = np.asarray(qs, dtype=np.uint32)
+    ps = np.asarray(psis, dtype=np.uint32)
+    out = np.empty(raw.shape[:-1] + (L, N), dtype=np.uint32)
+    lib().orc_encode_records(N, L, _p32(q), _p32(ps), cnt, _p32(raw), _p32(out),
+                             threads or default_threads())
+    return out
+
+
+# --------------------------------------------------------------- RowSel
+def rowsel(db: np.ndarray, query: np.ndarray, qs, cols=None, threads: int | None = None) -> np.ndarray:
+    """db [D0][D1][L][N], query [B][D0][2][L][N] -> out [B][len(cols)][2][L][N]."""
+    db = np.ascontiguousarray(db, dtype=np.uint32)
+    query = np.ascontiguousarray(query, dtype=np.uint32)
+    D0, D1, L, N = db.shape
+    B = query.shape[0]
+    assert query.shape == (B, D0, 2, L, N), (query.shape, db.shape)
+    if cols is None:
+        cols = np.arange(D1, dtype=np.uint32)
+    cols = np.ascontiguousarray(cols, dtype=np.uint32)
+    q = np.asarray(qs, dtype=np.uint32)
+    out = np.empty((B, cols.size, 2, L, N), dtype=np.uint32)
+    lib().orc_rowsel(N, L, _p32(q), D0, D1, B, _p32(db), _p32(query), cols.size, _p32(cols),
+                     _p32(out), threads or default_threads())
+    return out
+
+
+# --------------------------------------------------------------- scalar scan
+def scalar_scan(db_rows: np.ndarray, Q: np.ndarray, threads: int | None = None) -> np.ndarray:
+    """db_rows [R'][C] uint8, Q [C][B] uint32 -> [R'][B] uint32 (mod 2^32)."""
+    db_rows = np.ascontiguousarray(db_rows, dtype=np.uint8)
+    Q = np.ascontiguousarray(Q, dtype=np.uint32)
+    R, C = db_rows.shape
+    assert Q.shape[0] == C
+    B = Q.shape[1]
+    out = np.empty((R, B), dtype=np.uint32)
+    lib().orc_scalar_scan(R, C, B, _p8(db_rows), _p32(Q), _p32(out), threads or default_threads())
+    return out

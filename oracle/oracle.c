@@ -1,0 +1,443 @@
+/*
+ * oracle.c — CPU oracle for the lattice-PIR database scan.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load this code.  The product library never
+ * calls it, and the two share no source, header, table or constant generator.
+ *
+ * Plain, slow, obviously-correct C.  Every function restates one definition
+ * from the pages it is checked against:
+ *
+ *   [VIPIR]  "VIPIR: a general GPU framework for integrating PIR protocols"
+ *            (CSDN translation), sections 2.2-2.5 and 4.1-4.3.
+ *   [GPIR]   "GPIR: Enabling Practical Private Information Retrieval with
+ *            GPUs" (arXiv 2604.04696), the RowSel paragraphs of section 2
+ *            (the M_out[p,m,n] formulation).
+ *
+ * Readings of points the pages leave open are stated at each function and
+ * listed in the design notes.  Integer arithmetic only; no lazy reduction,
+ * no blocking, no reordering beyond the definitions.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <pthread.h>
+
+typedef unsigned __int128 u128;
+
+/* ------------------------------------------------------------------ */
+/* Modular arithmetic on residues < q < 2^32 (plain % reductions).      */
+/* ------------------------------------------------------------------ */
+
+static uint32_t mulmod(uint32_t a, uint32_t b, uint32_t q)
+{
+    return (uint32_t)(((uint64_t)a * (uint64_t)b) % q);
+}
+
+uint32_t orc_powmod(uint32_t base, uint64_t e, uint32_t q)
+{
+    uint32_t r = 1 % q;
+    uint32_t b = base % q;
+    while (e) {
+        if (e & 1) r = mulmod(r, b, q);
+        b = mulmod(b, b, q);
+        e >>= 1;
+    }
+    return r;
+}
+
+/* Inverse by Fermat's little theorem (q prime). */
+uint32_t orc_invmod(uint32_t a, uint32_t q)
+{
+    return orc_powmod(a, (uint64_t)q - 2, q);
+}
+
+/* Primality by trial division. */
+int orc_is_prime(uint32_t q)
+{
+    if (q < 2) return 0;
+    if (q % 2 == 0) return q == 2;
+    for (uint64_t d = 3; d * d <= q; d += 2)
+        if (q % d == 0) return 0;
+    return 1;
+}
+
+/*
+ * RNS primes: the `count` largest primes below `bound` with q = 1 (mod 2N),
+ * in descending order.  [VIPIR 2.3]: q = q0*q1*q2, each q_i < 2^32 and one row
+ * of the 3 x N residue matrix; [VIPIR 4.2]: q_i < 2^29 for lazy reduction.
+ * q = 1 (mod 2N) is what makes a negacyclic NTT of length N exist mod q_i.
+ * Returns the number found.
+ */
+int orc_primes(uint32_t N, uint32_t count, uint32_t bound, uint32_t *out)
+{
+    uint64_t twoN = 2ull * N;
+    if (bound < twoN + 2) return 0;
+    /* largest x < bound with x = 1 (mod 2N) */
+    uint64_t x = ((uint64_t)(bound - 2) / twoN) * twoN + 1;
+    int found = 0;
+    while (found < (int)count && x > twoN) {
+        if (orc_is_prime((uint32_t)x)) out[found++] = (uint32_t)x;
+        x -= twoN;
+    }
+    return found;
+}
+
+/*
+ * psi: the smallest g in [2, q) with g^N = -1 (mod q).  Any such g has
+ * multiplicative order exactly 2N (its order divides 2N but not N, and 2N is
+ * a power of two), so it is a primitive 2N-th root of unity.
+ * Reading: the pages do not say which root; the smallest one is taken.
+ */
+uint32_t orc_min_psi(uint32_t q, uint32_t N)
+{
+    for (uint32_t g = 2; g < q; g++)
+        if (orc_powmod(g, N, q) == q - 1) return g;
+    return 0;
+}
+
+uint32_t orc_bitrev(uint32_t x, uint32_t bits)
+{
+    uint32_t r = 0;
+    for (uint32_t i = 0; i < bits; i++) {
+        r = (r << 1) | (x & 1);
+        x >>= 1;
+    }
+    return r;
+}
+
+static uint32_t log2u(uint32_t N)
+{
+    uint32_t b = 0;
+    while ((1u << b) < N) b++;
+    return b;
+}
+
+/* ------------------------------------------------------------------ */
+/* Negacyclic NTT over Z_q[X]/(X^N+1)   [VIPIR 2.3]                     */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Forward transform, straight from the definition (O(N^2)):
+ *     out[j] = sum_t a[t] * psi^((2*brv(j)+1)*t)  mod q.
+ * out[j] is the value of a(X) at the root psi^(2*brv(j)+1) of X^N+1, so the
+ * transform maps a product in Z_q[X]/(X^N+1) to a point-wise product.
+ * Reading: output in bit-reversed order of the odd roots (the pages are
+ * silent on the order).
+ */
+void orc_ntt_direct(uint32_t q, uint32_t psi, uint32_t N, const uint32_t *a, uint32_t *out)
+{
+    uint32_t bits = log2u(N);
+    for (uint32_t j = 0; j < N; j++) {
+        uint32_t root = orc_powmod(psi, 2ull * orc_bitrev(j, bits) + 1, q);
+        uint32_t w = 1 % q;            /* root^t */
+        uint64_t acc = 0;
+        for (uint32_t t = 0; t < N; t++) {
+            acc = (acc + mulmod(a[t], w, q)) % q;
+            w = mulmod(w, root, q);
+        }
+        out[j] = (uint32_t)acc;
+    }
+}
+
+/*
+ * Inverse transform, from the definition:
+ *     a[t] = N^-1 * sum_j in[j] * psi^(-(2*brv(j)+1)*t)  mod q.
+ */
+void orc_intt_direct(uint32_t q, uint32_t psi, uint32_t N, const uint32_t *in, uint32_t *out)
+{
+    uint32_t bits = log2u(N);
+    uint32_t psi_inv = orc_invmod(psi, q);
+    uint32_t n_inv = orc_invmod(N % q, q);
+    for (uint32_t t = 0; t < N; t++) {
+        uint64_t acc = 0;
+        for (uint32_t j = 0; j < N; j++) {
+            uint64_t e = (2ull * orc_bitrev(j, bits) + 1) * (uint64_t)t;
+            acc = (acc + mulmod(in[j], orc_powmod(psi_inv, e % (2ull * N), q), q)) % q;
+        }
+        out[t] = mulmod((uint32_t)acc, n_inv, q);
+    }
+}
+
+/*
+ * Textbook iterative forward transform (O(N log N)), same result as
+ * orc_ntt_direct:
+ *   1. twist:      b[t] = a[t] * psi^t            (turns negacyclic into cyclic)
+ *   2. cyclic DFT  B[u] = sum_t b[t] * w^(u*t), w = psi^2, by the radix-2
+ *      decimation-in-time Cooley-Tukey recursion on bit-reversed input;
+ *   3. reorder:    out[j] = B[brv(j)]
+ * since psi^((2*brv(j)+1)*t) = psi^t * w^(brv(j)*t).
+ * In place on a[0..N).
+ */
+void orc_ntt_iter(uint32_t q, uint32_t psi, uint32_t N, uint32_t *a)
+{
+    uint32_t bits = log2u(N);
+    uint32_t *tmp = (uint32_t *)malloc(sizeof(uint32_t) * N);
+    /* 1. twist */
+    uint32_t p = 1 % q;
+    for (uint32_t t = 0; t < N; t++) {
+        a[t] = mulmod(a[t] % q, p, q);
+        p = mulmod(p, psi, q);
+    }
+    /* 2a. bit-reverse permutation of the input */
+    for (uint32_t t = 0; t < N; t++) tmp[orc_bitrev(t, bits)] = a[t];
+    /* 2b. DIT butterflies, natural-order output */
+    uint32_t w = mulmod(psi, psi, q);
+    for (uint32_t len = 2; len <= N; len <<= 1) {
+        uint32_t wlen = orc_powmod(w, N / len, q);   /* primitive len-th root */
+        for (uint32_t i = 0; i < N; i += len) {
+            uint32_t wj = 1 % q;
+            for (uint32_t j = 0; j < len / 2; j++) {
+                uint32_t u = tmp[i + j];
+                uint32_t v = mulmod(tmp[i + j + len / 2], wj, q);
+                tmp[i + j] = (uint32_t)(((uint64_t)u + v) % q);
+                tmp[i + j + len / 2] = (uint32_t)(((uint64_t)u + q - v) % q);
+                wj = mulmod(wj, wlen, q);
+            }
+        }
+    }
+    /* 3. bit-reversed output order */
+    for (uint32_t j = 0; j < N; j++) a[j] = tmp[orc_bitrev(j, bits)];
+    free(tmp);
+}
+
+/*
+ * Textbook iterative inverse: undo step 3, inverse cyclic DFT with w^-1 and
+ * the factor N^-1, then undo the twist with psi^-t.  In place.
+ */
+void orc_intt_iter(uint32_t q, uint32_t psi, uint32_t N, uint32_t *a)
+{
+    uint32_t bits = log2u(N);
+    uint32_t *B = (uint32_t *)malloc(sizeof(uint32_t) * N);
+    uint32_t *tmp = (uint32_t *)malloc(sizeof(uint32_t) * N);
+    for (uint32_t j = 0; j < N; j++) B[orc_bitrev(j, bits)] = a[j] % q;
+    for (uint32_t t = 0; t < N; t++) tmp[orc_bitrev(t, bits)] = B[t];
+    uint32_t psi_inv = orc_invmod(psi, q);
+    uint32_t winv = mulmod(psi_inv, psi_inv, q);
+    for (uint32_t len = 2; len <= N; len <<= 1) {
+        uint32_t wlen = orc_powmod(winv, N / len, q);
+        for (uint32_t i = 0; i < N; i += len) {
+            uint32_t wj = 1 % q;
+            for (uint32_t j = 0; j < len / 2; j++) {
+                uint32_t u = tmp[i + j];
+                uint32_t v = mulmod(tmp[i + j + len / 2], wj, q);
+                tmp[i + j] = (uint32_t)(((uint64_t)u + v) % q);
+                tmp[i + j + len / 2] = (uint32_t)(((uint64_t)u + q - v) % q);
+                wj = mulmod(wj, wlen, q);
+            }
+        }
+    }
+    uint32_t n_inv = orc_invmod(N % q, q);
+    uint32_t p = 1 % q;
+    for (uint32_t t = 0; t < N; t++) {
+        a[t] = mulmod(mulmod(tmp[t], n_inv, q), p, q);
+        p = mulmod(p, psi_inv, q);
+    }
+    free(B);
+    free(tmp);
+}
+
+/*
+ * Schoolbook product in Z_q[X]/(X^N+1):
+ *     c[t] = sum_{u+v=t} a[u]*b[v] - sum_{u+v=t+N} a[u]*b[v]  mod q
+ * (X^N = -1 folds the upper half back with a minus sign).
+ */
+void orc_negacyclic_mul(uint32_t q, uint32_t N, const uint32_t *a, const uint32_t *b, uint32_t *c)
+{
+    for (uint32_t t = 0; t < N; t++) {
+        uint64_t pos = 0, neg = 0;
+        for (uint32_t u = 0; u < N; u++) {
+            uint32_t prod = mulmod(a[u] % q, b[(t + N - u) % N] % q, q);
+            if (u <= t) pos = (pos + prod) % q;    /* v = t - u */
+            else        neg = (neg + prod) % q;    /* v = t + N - u */
+        }
+        c[t] = (uint32_t)((pos + q - neg) % q);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Batched helpers (threads over independent polynomials)              */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    uint32_t N, L;
+    const uint32_t *q, *psi;
+    uint64_t row0, row1;      /* rows [row0,row1) of the [cnt][L][N] array */
+    const uint32_t *in;
+    uint32_t *out;
+    int inverse;
+} ntt_job;
+
+static void *ntt_worker(void *arg)
+{
+    ntt_job *j = (ntt_job *)arg;
+    for (uint64_t r = j->row0; r < j->row1; r++) {
+        uint32_t l = (uint32_t)(r % j->L);
+        uint32_t *dst = j->out + r * j->N;
+        if (dst != j->in + r * j->N) memcpy(dst, j->in + r * j->N, sizeof(uint32_t) * j->N);
+        if (j->inverse) orc_intt_iter(j->q[l], j->psi[l], j->N, dst);
+        else            orc_ntt_iter(j->q[l], j->psi[l], j->N, dst);
+    }
+    return NULL;
+}
+
+static int clamp_threads(int nthreads, uint64_t work)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((uint64_t)nthreads > work) nthreads = (int)(work ? work : 1);
+    return nthreads;
+}
+
+/*
+ * Transform cnt polynomials in RNS form, laid out [cnt][L][N] (row r uses
+ * prime r % L).  in may equal out.
+ */
+void orc_ntt_polys(uint32_t N, uint32_t L, const uint32_t *q, const uint32_t *psi,
+                   uint64_t cnt, const uint32_t *in, uint32_t *out, int inverse, int nthreads)
+{
+    uint64_t rows = cnt * L;
+    nthreads = clamp_threads(nthreads, rows);
+    pthread_t th[256];
+    ntt_job jobs[256];
+    for (int i = 0; i < nthreads; i++) {
+        jobs[i] = (ntt_job){N, L, q, psi, rows * i / nthreads, rows * (i + 1) / nthreads, in, out, inverse};
+        pthread_create(&th[i], NULL, ntt_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; i++) pthread_join(th[i], NULL);
+}
+
+/*
+ * DB encoding of plaintext records [VIPIR 2.4; GPIR section 2]: each record
+ * is a polynomial with coefficients in [0, 2^16); it is lifted to R_q (a
+ * coefficient below every q_i is its own residue, so the lift copies it into
+ * each of the L RNS rows) and brought to the evaluation domain by the forward
+ * NTT.  raw is [cnt][N]; out is [cnt][L][N].
+ * Reading: no scaling of the plaintext (a BFV plaintext-ciphertext product
+ * multiplies by the plaintext as is).
+ */
+void orc_encode_records(uint32_t N, uint32_t L, const uint32_t *q, const uint32_t *psi,
+                        uint64_t cnt, const uint32_t *raw, uint32_t *out, int nthreads)
+{
+    for (uint64_t r = 0; r < cnt; r++)
+        for (uint32_t l = 0; l < L; l++)
+            for (uint32_t t = 0; t < N; t++)
+                out[(r * L + l) * N + t] = raw[r * N + t] % q[l];
+    orc_ntt_polys(N, L, q, psi, cnt, out, out, 0, nthreads);
+}
+
+/* ------------------------------------------------------------------ */
+/* RowSel  [GPIR section 2]                                             */
+/* ------------------------------------------------------------------ */
+
+/*
+ * M_out[p,m,n] = sum_k M_in0[p,m,k] * M_in1[p,k,n]  mod q_{l(p)}
+ *
+ * with p = l*N + j an evaluation point (prime l, NTT slot j), m = 2b + c
+ * (query b, ciphertext polynomial c in {0,1}), k < D0 a DB row and n < D1 a
+ * DB column:
+ *     M_in0[p, 2b+c, k] = query[b][k][c][l][j]      (the D0 query ciphertexts)
+ *     M_in1[p, k, n]    = db[k][n][l][j]            (NTT of record (k,n))
+ *     M_out[p, 2b+c, n] -> out[b][i][c][l][j]       (D1 result ciphertexts)
+ * The sum is exact in 128 bits and reduced once.
+ *
+ * Layouts (uint32, all residues < q_l):
+ *   db    [D0][D1][L][N]
+ *   query [B][D0][2][L][N]
+ *   out   [B][ncols][2][L][N], where output column i is DB column cols[i].
+ * Threads split the output columns.
+ * Reading: the pages' "4N" points are L*N residues per polynomial here.
+ */
+typedef struct {
+    uint32_t N, L, D0, D1, B;
+    const uint32_t *q, *db, *query, *cols;
+    uint32_t ncols, i0, i1;
+    uint32_t *out;
+} rowsel_job;
+
+static void *rowsel_worker(void *arg)
+{
+    rowsel_job *J = (rowsel_job *)arg;
+    uint64_t P = (uint64_t)J->L * J->N;
+    for (uint32_t i = J->i0; i < J->i1; i++) {
+        uint32_t n = J->cols[i];
+        for (uint32_t b = 0; b < J->B; b++)
+            for (uint32_t c = 0; c < 2; c++)
+                for (uint64_t p = 0; p < P; p++) {
+                    uint32_t q = J->q[p / J->N];
+                    u128 acc = 0;
+                    for (uint32_t k = 0; k < J->D0; k++) {
+                        uint64_t in0 = J->query[(((uint64_t)b * J->D0 + k) * 2 + c) * P + p];
+                        uint64_t in1 = J->db[((uint64_t)k * J->D1 + n) * P + p];
+                        acc += (u128)(in0 * in1);
+                    }
+                    J->out[(((uint64_t)b * J->ncols + i) * 2 + c) * P + p] = (uint32_t)(acc % q);
+                }
+    }
+    return NULL;
+}
+
+void orc_rowsel(uint32_t N, uint32_t L, const uint32_t *q, uint32_t D0, uint32_t D1, uint32_t B,
+                const uint32_t *db, const uint32_t *query, uint32_t ncols, const uint32_t *cols,
+                uint32_t *out, int nthreads)
+{
+    nthreads = clamp_threads(nthreads, ncols);
+    pthread_t th[256];
+    rowsel_job jobs[256];
+    for (int t = 0; t < nthreads; t++) {
+        jobs[t] = (rowsel_job){N, L, D0, D1, B, q, db, query, cols, ncols,
+                               (uint32_t)((uint64_t)ncols * t / nthreads),
+                               (uint32_t)((uint64_t)ncols * (t + 1) / nthreads), out};
+        pthread_create(&th[t], NULL, rowsel_worker, &jobs[t]);
+    }
+    for (int t = 0; t < nthreads; t++) pthread_join(th[t], NULL);
+}
+
+/* ------------------------------------------------------------------ */
+/* Scalar-HE scan  [VIPIR 2.5, 4.1]                                     */
+/* ------------------------------------------------------------------ */
+
+/*
+ * out[r][b] = sum_c db[r][c] * Q[c][b]  mod 2^32
+ * The DB GEMM of SimplePIR-style folding: a D1 x B x D0 GEMM of a byte DB by
+ * 32-bit query words, where arithmetic mod 2^32 is plain wrap-around
+ * ("the modular reduction is free").  uint32 arithmetic wraps by definition.
+ * db rows are given as a list: db_rows is [nrows][C] (row i of it is DB row
+ * rows[i]); out is [nrows][B].  Q is [C][B].  Threads split the rows.
+ * Reading: DB bytes are unsigned, in [0, 256).
+ */
+typedef struct {
+    uint64_t C;
+    uint32_t B;
+    const uint8_t *db_rows;
+    const uint32_t *Q;
+    uint32_t *out;
+    uint64_t i0, i1;
+} scalar_job;
+
+static void *scalar_worker(void *arg)
+{
+    scalar_job *J = (scalar_job *)arg;
+    for (uint64_t i = J->i0; i < J->i1; i++) {
+        for (uint32_t b = 0; b < J->B; b++) {
+            uint32_t acc = 0;
+            for (uint64_t c = 0; c < J->C; c++)
+                acc += (uint32_t)J->db_rows[i * J->C + c] * J->Q[c * J->B + b];
+            J->out[i * J->B + b] = acc;
+        }
+    }
+    return NULL;
+}
+
+void orc_scalar_scan(uint64_t nrows, uint64_t C, uint32_t B, const uint8_t *db_rows,
+                     const uint32_t *Q, uint32_t *out, int nthreads)
+{
+    nthreads = clamp_threads(nthreads, nrows);
+    pthread_t th[256];
+    scalar_job jobs[256];
+    for (int t = 0; t < nthreads; t++) {
+        jobs[t] = (scalar_job){C, B, db_rows, Q, out, nrows * t / nthreads, nrows * (t + 1) / nthreads};
+        pthread_create(&th[t], NULL, scalar_worker, &jobs[t]);
+    }
+    for (int t = 0; t < nthreads; t++) pthread_join(th[t], NULL);
+}
