@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Benchmark of the lattice-PIR database scan on GB300.
+
+Default workload: the 64 GiB RowSel query pipeline (N = 4096, 3 RNS primes
+below 2^29, D0 = 1024 x D1 = 1365 records, one query): forward NTT of the
+query (2048 polynomials), the RowSel scan of the NTT-domain DB, inverse NTT of
+the 2730 result polynomials.  One step = one query batch through all three
+kernels; the encoded DB stays resident in HBM (encoded once, untimed).
+
+Prints ONE JSON line (rank 0):
+  value     DB GB/s scanned (logical DB bytes / step time), device-resident
+            inputs, CUDA events on the launching stream, max over ranks;
+  e2e       the same metric through the public API with the query coming
+            from pinned host memory and the result going back to it;
+  roofline  the RowSel kernel's algorithmic bytes / its average launch time
+            against the measured HBM copy bandwidth;
+  cpu_baseline  the oracle (plain C, all host cores) on a bounded sample.
+
+--impl reference runs the oracle itself as the reference arm (each step a
+bounded sample of the same workload on the host cores).
+Multi-GPU (torchrun): every rank runs an independent replica (the scan does
+not exchange data); value aggregates all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+GIB = 1 << 30
+WORKLOADS = {
+    # name: ring, DB grid, batch, query domain
+    "rowsel_64g": dict(N=4096, L=3, D0=1024, D1=1365, B=1, domain="coeff",
+                       desc="RowSel 64 GiB NTT-form DB: N=4096, 3 RNS primes <2^29, D0=1024 x D1=1365 records, "
+                            "B=1 query; step = NTT(query, 2048 polys) + RowSel scan + INTT(2730 result polys)"),
+    "rowsel_6g": dict(N=4096, L=3, D0=256, D1=512, B=1, domain="ntt",
+                      desc="RowSel 6 GiB: N=4096, 3 primes, D0=256 x D1=512, B=1, NTT-domain query"),
+    "rowsel_24g_b16": dict(N=4096, L=3, D0=512, D1=1024, B=16, domain="ntt",
+                           desc="RowSel 24 GiB: N=4096, 3 primes, D0=512 x D1=1024, B=16 queries, NTT-domain"),
+}
+METRIC = "DB GB/s scanned & queries/s (RowSel, 64 GiB DB), % of GB300 HBM roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="rowsel_64g", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle baseline budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def profile_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary of `kernel`, if any."""
+    path = os.path.join(ROOT, "profiles", "%s.md" % kernel)
+    try:
+        for line in open(path):
+            if line.startswith("traffic_bytes_per_launch:"):
+                v = line.split(":", 1)[1].strip()
+                return None if v in ("", "null") else float(v)
+    except OSError:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.f.name)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle (CPU) leg
+def oracle_rowsel_sample(cfg, budget_s: float):
+    """Time the oracle RowSel on a bounded sample: all D0 rows and B queries, a
+    subset of evaluation points (prime 0) and DB columns.  Returns
+    (GB/s, threads, description, seconds)."""
+    import oracle
+    import synth
+    N, D0, B = cfg["N"], cfg["D0"], cfg["B"]
+    q0 = oracle.primes(N, 1)[0]
+    threads = oracle.default_threads()
+    npts = 1024
+
+    def run(ncols):
+        db = synth.residues(11, (D0, ncols, 1, npts), [q0], tid=synth.T_EXTRA)
+        qu = synth.residues(12, (B, D0, 2, 1, npts), [q0], tid=synth.T_EXTRA)
+        t = time.perf_counter()
+        oracle.rowsel(db, qu, [q0], threads=threads)
+        return time.perf_counter() - t
+
+    t1 = run(threads)
+    ncols = threads * max(1, min(64, int(budget_s / max(t1, 1e-3))))
+    ncols = min(ncols, cfg["D1"])
+    dt = run(ncols)
+    nbytes = D0 * ncols * npts * 4
+    desc = ("oracle RowSel on %d of %d DB columns x %d of %d evaluation points, all %d rows, B=%d"
+            % (ncols, cfg["D1"], npts, cfg["L"] * N, D0, B))
+    return nbytes / dt / 1e9, threads, desc, dt, (ncols, npts)
+
+
+def run_reference(args, cfg):
+    """Reference arm: the oracle as it stands, timed on the host cores."""
+    import oracle
+    import synth
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    N, D0, B = cfg["N"], cfg["D0"], cfg["B"]
+    q0 = oracle.primes(N, 1)[0]
+    threads = oracle.default_threads()
+    npts = 256
+    total_budget = 120.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    db1 = synth.residues(11, (D0, threads, 1, npts), [q0], tid=synth.T_EXTRA)
+    qu = synth.residues(12, (B, D0, 2, 1, npts), [q0], tid=synth.T_EXTRA)
+    t = time.perf_counter()
+    oracle.rowsel(db1, qu, [q0], threads=threads)
+    t1 = time.perf_counter() - t
+    ncols = min(cfg["D1"], max(1, threads * max(1, int(per_step / max(t1, 1e-4)))))
+    db = synth.residues(11, (D0, ncols, 1, npts), [q0], tid=synth.T_EXTRA)
+    for _ in range(args.warmup):
+        oracle.rowsel(db, qu, [q0], threads=threads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.rowsel(db, qu, [q0], threads=threads)
+    dt = (time.perf_counter() - t) / max(1, args.steps)
+    nbytes = D0 * ncols * npts * 4
+    value = nbytes / dt / 1e9
+    sample = ("oracle RowSel per step: %d of %d DB columns x %d of %d evaluation points, all %d rows, B=%d"
+              % (ncols, cfg["D1"], npts, cfg["L"] * N, D0, B))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u32", "data": "synthetic (seeded SplitMix64 residues)",
+        "config": {"workload": args.workload, "desc": cfg["desc"]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "queries_per_s": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU leg
+def device_db(ctx, D0, D1, seed):
+    """Seeded raw records generated on the device, encoded in row chunks."""
+    import torch
+    import synth
+    import synth.device as sd
+    from lattice_he_database_gb300 import pir
+    N = ctx.N
+    db = torch.empty(pir.pir_db_bytes(ctx, D0, D1) // 4, dtype=torch.int32, device="cuda")
+    rows = max(1, min(D0, (1 << 30) // (D1 * N * 4)))
+    raw = torch.empty(rows * D1 * N, dtype=torch.int32, device="cuda")
+    for k0 in range(0, D0, rows):
+        kc = min(rows, D0 - k0)
+        r = raw[: kc * D1 * N]
+        sd.fill_coeffs(r, seed, synth.T_DB_COEFF, idx0=k0 * D1 * N)
+        pir.pir_db_encode(ctx, r, k0, kc, D0, D1, db)
+    torch.cuda.synchronize()
+    del raw
+    return db
+
+
+def run_ours(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    import synth.device as sd
+    from lattice_he_database_gb300 import pir
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+
+    N, L, D0, D1, B = cfg["N"], cfg["L"], cfg["D0"], cfg["D1"], cfg["B"]
+    qs = pir.pir_primes(N, L)
+    ctx = pir.pir_ctx_create(N, qs, local)
+    P = L * N
+    db = device_db(ctx, D0, D1, seed=7)
+    stream = torch.cuda.Stream()
+    srv = pir.RowselServer(ctx, db, D0, D1, B, stream=stream)
+    sd.fill_residues(srv.q_coef, 7, synth.T_QUERY, N, qs)
+    torch.cuda.synchronize()
+
+    logical_db = P * D0 * D1 * 4
+    q_bytes = B * D0 * 2 * P * 4
+    o_bytes = B * D1 * 2 * P * 4
+    coeff = cfg["domain"] == "coeff"
+
+    def step(ev=None):
+        if coeff:
+            pir.pir_ntt_fwd(ctx, srv.q_coef, srv.q_ntt, B * D0 * 2, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        pir.pir_rowsel(ctx, db, D0, D1, srv.q_ntt if coeff else srv.q_coef, B, srv.o_ntt, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if coeff:
+            pir.pir_ntt_inv(ctx, srv.o_ntt, srv.o_coef, B * D1 * 2, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(kev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    rowsel_ms = float(np.mean([a.elapsed_time(b) for a, b in kev]))
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    status = pir.pir_status(ctx)
+    if status:
+        raise RuntimeError("device status word set: %d" % status)
+
+    # ---- end to end through the public API: pinned host query in, result out
+    q_host = torch.empty(srv.q_words, dtype=torch.int32, pin_memory=True)
+    q_host.copy_(srv.q_coef.cpu())
+    o_host = torch.empty(srv.o_words, dtype=torch.int32, pin_memory=True)
+    ke = max(1, min(args.e2e_steps, args.steps))
+    result_buf = srv.o_coef if coeff else srv.o_ntt
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            srv.q_coef.copy_(q_host, non_blocking=True)
+            step()
+            o_host.copy_(result_buf, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / ke
+
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    algo_bytes = logical_db + q_bytes + o_bytes       # the RowSel kernel's algorithmic bytes per launch
+    achieved = algo_bytes / (rowsel_ms * 1e-3) / 1e9
+
+    result = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            gbs, threads, desc, secs, _ = oracle_rowsel_sample(cfg, args.cpu_seconds)
+            cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
+                   "seconds": round(secs, 2)}
+        value = world * logical_db * args.steps / (ms_total * 1e-3) / 1e9
+        result = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u32",
+            "data": "synthetic: seeded SplitMix64 DB coefficients U[0,2^16), query residues U[0,q_i)",
+            "config": {"workload": args.workload, "desc": cfg["desc"], "logical_db_bytes": logical_db,
+                       "encoded_db_bytes": pir.pir_db_bytes(ctx, D0, D1), "B": B,
+                       "l2": "inputs larger than L2 (DB %.1f GiB >> 129 MB L2), no flush" % (logical_db / GIB),
+                       "parallelism": "replicas x%d" % world},
+            "queries_per_s": world * B * args.steps / (ms_total * 1e-3),
+            "kernel_ms": {"rowsel": rowsel_ms},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": profile_traffic("rowsel_kernel_rowsel_64g"),
+                         "kernel": "rowsel_kernel", "peak_source": "%s hbm_gbs (copy)" % peak_kind,
+                         "algorithmic_bytes_per_launch": algo_bytes},
+            "clocks": clk,
+            "e2e": {"value": logical_db / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": q_bytes, "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * (3 if coeff else 1),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(result), flush=True)
+    ctx.close()
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def main():
+    args = parse()
+    cfg = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+/*
+ * pir.h — C ABI of the GB300 (sm_103a) server-side scan of lattice-based
+ * single-server PIR.
+ *
+ * Two scans are provided:
+ *
+ *  - RowSel, the first-dimension fold of the OnionPIR family.  Every DB record
+ *    is a plaintext polynomial in R_q = Z_q[X]/(X^N+1), q held in RNS
+ *    (q_i < 2^29, q_i = 1 mod 2N).  DB and query are in the evaluation
+ *    (NTT) domain, where the fold becomes L*N independent point-wise GEMMs
+ *        M_out[p,m,n] = sum_k M_in0[p,m,k] * M_in1[p,k,n]  mod q_{l(p)}
+ *    (GPIR, arXiv 2604.04696, section 2, the RowSel formulation; VIPIR,
+ *    sections 2.3 and 4.2).
+ *
+ *  - the scalar-HE scan, the first fold of the SimplePIR family: a byte DB
+ *    times a matrix of 32-bit query words, mod 2^32 (VIPIR, sections 2.5
+ *    and 4.1).
+ *
+ * Conventions for every call:
+ *  - All buffers are owned and allocated by the caller; pointers marked
+ *    "device" must be device memory of the context's GPU, 16-byte aligned.
+ *    The library allocates device memory only in pir_ctx_create (its
+ *    twiddle tables and a status word) and frees it in pir_ctx_destroy.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and returns before it completes.  Inputs must stay valid and
+ *    unmodified until the stream reaches the work.
+ *  - Return value: PIR_OK (0) or a negative PIR_ERR_* code.  Arguments are
+ *    validated on the host before anything is enqueued; a failed call
+ *    enqueues nothing.  Nothing is thrown across the ABI.
+ *  - Residues are uint32 values in [0, q_l).  Input values are not range
+ *    checked on the device; residues >= q_l give unspecified (but memory-safe)
+ *    results.
+ *  - Device-side waits are bounded.  A kernel that gives up sets a bit in the
+ *    context's status word (pir_status) instead of hanging.
+ */
+#ifndef PIR_H
+#define PIR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PIR_OK 0
+#define PIR_ERR_ARG (-1)          /* invalid argument (size, pointer, parameters) */
+#define PIR_ERR_CUDA (-2)         /* a CUDA runtime/driver call or launch failed */
+#define PIR_ERR_UNSUPPORTED (-3)  /* valid but outside what this build supports */
+#define PIR_ERR_ALLOC (-4)        /* pir_ctx_create could not allocate its tables */
+
+/* Bits of the device status word (pir_status). */
+#define PIR_STATUS_TIMEOUT 1u     /* a bounded device wait ran out */
+
+#define PIR_MAX_RNS 4
+#define PIR_SLAB 128              /* width (uint32 words) of one DB column slab */
+
+typedef struct pir_ctx pir_ctx;
+
+/*
+ * pir_params_check — validate ring parameters on the host (no GPU needed).
+ * N: ring degree, a power of two in [16, 4096] (VIPIR 2.2 uses N = 2^12).
+ * L: number of RNS primes, 1..4 (VIPIR 2.3 uses #RNS = 3).
+ * q: host array of L distinct primes with q_i < 2^29 and q_i = 1 (mod 2N)
+ *    (VIPIR 4.2: primes below 2^29 for 64-bit lazy accumulation).
+ * Returns PIR_OK or PIR_ERR_ARG.
+ */
+int pir_params_check(uint32_t N, uint32_t L, const uint32_t *q);
+
+/*
+ * pir_primes — the L largest primes q < 2^29 with q = 1 (mod 2N), in
+ * descending order, written to q (host, L entries).  Host only.  These are
+ * the RNS primes of the workloads (VIPIR 2.3: q = q0*q1*q2 ~ 2^87 with
+ * #RNS = 3; VIPIR 4.2: q_i < 2^29).
+ * Errors: PIR_ERR_ARG (N not a power of two in [16, 4096], L not in 1..4,
+ * q NULL).
+ */
+int pir_primes(uint32_t N, uint32_t L, uint32_t *q);
+
+/*
+ * pir_ctx_create — build a context for ring degree N and RNS primes q[0..L)
+ * on CUDA device `device`: validates the parameters (as pir_params_check),
+ * selects for each q_i the smallest primitive 2N-th root of unity psi_i, and
+ * uploads its twiddle tables.  *out receives the context (NULL on error).
+ * Errors: PIR_ERR_ARG, PIR_ERR_CUDA, PIR_ERR_ALLOC.
+ */
+int pir_ctx_create(pir_ctx **out, uint32_t N, uint32_t L, const uint32_t *q, int device);
+
+/* pir_ctx_destroy — free the context's device tables (synchronises the device). */
+void pir_ctx_destroy(pir_ctx *ctx);
+
+/*
+ * pir_ctx_psi — copy the L roots psi_i chosen by the context into psi (host).
+ * The NTT-domain convention below depends on them.
+ */
+int pir_ctx_psi(const pir_ctx *ctx, uint32_t *psi);
+
+/*
+ * pir_ntt_fwd — forward negacyclic NTT of cnt RNS polynomials
+ * (VIPIR 2.3: the per-row transform that turns a product in R_q into a
+ * point-wise product mod q_i; VIPIR 4.3: one kernel per N = 2^12 transform).
+ *   in, out : device, [cnt][L][N] uint32; row l of each polynomial holds
+ *             residues mod q_l.  in == out (in place) is allowed; otherwise
+ *             the buffers must not overlap.
+ *   Output convention: out[j] = sum_t in[t] * psi^((2*brv(j)+1)*t) mod q_l,
+ *   brv = log2(N)-bit reversal; outputs are canonical residues in [0, q_l).
+ * Errors: PIR_ERR_ARG (NULL/unaligned pointer, cnt*L*N overflow), PIR_ERR_CUDA.
+ * cnt = 0 is a no-op.
+ */
+int pir_ntt_fwd(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream);
+
+/*
+ * pir_ntt_inv — inverse of pir_ntt_fwd including the factor N^-1:
+ *   out[t] = N^-1 * sum_j in[j] * psi^(-(2*brv(j)+1)*t) mod q_l.
+ * Same layout, aliasing rules and errors as pir_ntt_fwd.
+ */
+int pir_ntt_inv(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream);
+
+/*
+ * pir_db_bytes — bytes of the encoded RowSel DB for a D0 x D1 grid of records
+ * (GPIR section 2: DB[i][j], i < D0, j < D1), i.e. L*N*D0*D1p*4 with
+ * D1p = D1 rounded up to a multiple of 4.  Returns 0 for invalid sizes.
+ *
+ * Encoded layout ("column slabs", k/n-contiguous per evaluation point):
+ *   evaluation point p = l*N + j (prime l, NTT slot j), record (k, n);
+ *   columns are cut into slabs of PIR_SLAB = 128 columns, s = n / 128; the
+ *   last slab is W_last = D1p - 128*(S-1) wide, S = ceil(D1/128).  Word
+ *       db[ p*D0*D1p + s*D0*128 + k*W_s + (n - 128*s) ]
+ *   holds NTT(record(k,n))[l][j], where W_s = 128 for s < S-1, W_last for
+ *   the last slab.  Each (p, slab) is one contiguous D0 x W_s block.
+ *   Padding columns n in [D1, D1p) hold 0.
+ */
+uint64_t pir_db_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t D1);
+
+/*
+ * pir_db_encode — offline DB encoding (VIPIR 2.4: lift of the plaintext to
+ * R_q and NTT; GPIR section 2: DB records as NTT-domain vectors), for DB rows
+ * k0 .. k0+kcnt-1 of a D0 x D1 DB.
+ *   raw : device, [kcnt][D1][N] uint32 plaintext coefficients (each is
+ *         lifted to R_q as its residue mod q_l; the workloads use [0, 2^16)).
+ *   db  : device, pir_db_bytes(ctx, D0, D1) bytes, layout above.  Only the
+ *         words of rows k0..k0+kcnt-1 (including their padding columns) are
+ *         written, so the DB can be encoded in row chunks.
+ * Errors: PIR_ERR_ARG (k0+kcnt > D0, zero sizes, NULL/unaligned), PIR_ERR_CUDA.
+ */
+int pir_db_encode(pir_ctx *ctx, const uint32_t *raw, uint32_t k0, uint32_t kcnt,
+                  uint32_t D0, uint32_t D1, uint32_t *db, void *stream);
+
+/*
+ * pir_rowsel — the RowSel scan (GPIR section 2):
+ *   out[b][n][c][l][j] = sum_{k<D0} query[b][k][c][l][j] * DB(k,n)[l][j]  mod q_l
+ * i.e. M_out[p, m=2b+c, n] = sum_k M_in0[p,m,k] * M_in1[p,k,n] with p = l*N+j:
+ * B queries, each D0 BFV ciphertexts (2 polynomials, NTT form), fold a
+ * D0 x D1 DB into D1 ciphertexts per query.
+ *   db    : device, encoded by pir_db_encode for the same ctx, D0, D1.
+ *   query : device, [B][D0][2][L][N] uint32 residues (NTT form).
+ *   out   : device, [B][D1][2][L][N] uint32 (NTT form, canonical residues).
+ * The DB is read from HBM once per pass; a pass covers as many queries as
+ * fit the on-chip query buffer (all B for B*D0 <= 8192), larger batches take
+ * ceil(B / per-pass) passes.
+ * Errors: PIR_ERR_ARG (zero sizes, NULL/unaligned, overflow), PIR_ERR_CUDA,
+ * PIR_ERR_UNSUPPORTED (D0 > 16384).
+ */
+int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1,
+               const uint32_t *query, uint32_t B, uint32_t *out, void *stream);
+
+/*
+ * pir_scalar_workspace_bytes — device workspace pir_scalar_scan needs for a
+ * C x B query matrix (0 for invalid sizes).
+ */
+uint64_t pir_scalar_workspace_bytes(uint64_t C, uint32_t B);
+
+/*
+ * pir_scalar_scan — scalar-HE DB fold (VIPIR 2.5 and 4.1):
+ *   out[r][b] = sum_{c<C} db[r][c] * Q[c][b]  mod 2^32
+ * computed on the tensor cores with the 4-way byte split of Q
+ * (Q = sum_i 2^(8i) Q_i, VIPIR 4.1).
+ *   db  : device, [R][C] uint8 row-major (bytes are unsigned).
+ *   Q   : device, [C][B] uint32.
+ *   out : device, [R][B] uint32.
+ *   workspace : device, >= pir_scalar_workspace_bytes(C, B) bytes, 128-byte
+ *               aligned; scratch for the split query, contents undefined
+ *               after the call.
+ * Requirements: R % 128 == 0, C % 128 == 0, B == 64.
+ * Errors: PIR_ERR_ARG, PIR_ERR_UNSUPPORTED (shape outside the requirements),
+ * PIR_ERR_CUDA.
+ */
+int pir_scalar_scan(pir_ctx *ctx, const uint8_t *db, uint64_t R, uint64_t C,
+                    const uint32_t *Q, uint32_t B, uint32_t *out,
+                    void *workspace, uint64_t workspace_bytes, void *stream);
+
+/*
+ * pir_status — read the context's device status word (PIR_STATUS_* bits set
+ * by kernels whose bounded waits ran out) into *flags; clear it if `clear`.
+ * Synchronises the context's device.
+ */
+int pir_status(pir_ctx *ctx, uint32_t *flags, int clear);
+
+/* pir_strerror — static description of a return code. */
+const char *pir_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PIR_H */

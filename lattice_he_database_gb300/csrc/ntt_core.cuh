@@ -1,0 +1,150 @@
+// ntt_core.cuh — negacyclic NTT of rows held in shared memory.
+//
+// VIPIR section 2.3: the NTT of each row of the L x N residue matrix turns a
+// product in Z_q[X]/(X^N+1) into a point-wise product mod q_i; section 4.3:
+// for N = 2^12 the whole transform fits on chip, so one kernel does it.
+//
+// Forward: in-place Cooley-Tukey on natural-order input with twiddles
+// psi^brv(m+i), giving out[j] = sum_t a[t] psi^((2 brv(j)+1) t) (bit-reversed
+// order).  Inverse: Gentleman-Sande with psi^-brv(m+i), natural-order output,
+// then the factor N^-1.  Butterflies use Shoup products with Harvey's lazy
+// ranges: forward values live in [0, 4q), inverse values in [0, 2q); q < 2^29
+// keeps 4q below 2^32.
+//
+// Stages are processed three at a time in registers: a thread loads 8
+// elements spaced by the smallest butterfly distance of the round, runs the
+// three butterfly levels, and writes them back; rounds are separated by
+// __syncthreads.
+#pragma once
+
+#include "common.cuh"
+
+// Forward CT butterfly, Harvey form: x, y in [0, 4q) -> [0, 4q).
+__device__ __forceinline__ void ct_bfly(uint32_t &x, uint32_t &y, uint32_t w, uint32_t wp, uint32_t q,
+                                        uint32_t q2) {
+    uint32_t a = x >= q2 ? x - q2 : x;          // [0, 2q)
+    uint32_t t = shoup_mul(y, w, wp, q);         // [0, 2q)
+    x = a + t;                                   // [0, 4q)
+    y = a - t + q2;                              // (0, 4q)
+}
+
+// Inverse GS butterfly, Harvey form: x, y in [0, 2q) -> [0, 2q).
+__device__ __forceinline__ void gs_bfly(uint32_t &x, uint32_t &y, uint32_t w, uint32_t wp, uint32_t q,
+                                        uint32_t q2) {
+    uint32_t u = x + y;
+    u = u >= q2 ? u - q2 : u;                    // [0, 2q)
+    uint32_t v = x - y + q2;                     // (0, 4q)
+    x = u;
+    y = shoup_mul(v, w, wp, q);                  // [0, 2q)
+}
+
+// One forward round of R stages (s0 .. s0+R-1) on a group of G = 2^R
+// elements e_i = g + i*tlow, where tlow = N >> (s0+R) is the butterfly
+// distance of the last stage and `high` the group's index bits above the
+// round's R bits (so e = (high << (log2 tlow + R)) | (i << log2 tlow) | low).
+template <int R>
+__device__ __forceinline__ void fwd_round_group(uint32_t *row, uint32_t g, uint32_t tlow, uint32_t s0,
+                                                uint32_t high, const uint32_t *__restrict__ W,
+                                                const uint32_t *__restrict__ Wp, uint32_t q) {
+    constexpr int G = 1 << R;
+    uint32_t x[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) x[i] = row[g + i * tlow];
+    const uint32_t q2 = 2 * q;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int d = G >> (r + 1);
+        const uint32_t m = 1u << (s0 + r);
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            if (i & d) continue;
+            uint32_t blk = (high << r) | (uint32_t)(i >> (R - r));
+            uint32_t w = __ldg(W + m + blk), wp = __ldg(Wp + m + blk);
+            ct_bfly(x[i], x[i + d], w, wp, q, q2);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < G; ++i) row[g + i * tlow] = x[i];
+}
+
+// One inverse round of R stages s_hi, s_hi-1, .., s_hi-R+1 on a group of
+// G = 2^R elements e_i = g + i*tlow, tlow = N >> (s_hi+1) the distance of the
+// first (smallest) stage.
+template <int R>
+__device__ __forceinline__ void inv_round_group(uint32_t *row, uint32_t g, uint32_t tlow, uint32_t s_hi,
+                                                uint32_t high, const uint32_t *__restrict__ W,
+                                                const uint32_t *__restrict__ Wp, uint32_t q) {
+    constexpr int G = 1 << R;
+    uint32_t x[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) x[i] = row[g + i * tlow];
+    const uint32_t q2 = 2 * q;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int d = 1 << r;
+        const uint32_t m = 1u << (s_hi - r);
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            if (i & d) continue;
+            uint32_t blk = (high << (R - 1 - r)) | (uint32_t)(i >> (r + 1));
+            uint32_t w = __ldg(W + m + blk), wp = __ldg(Wp + m + blk);
+            gs_bfly(x[i], x[i + d], w, wp, q, q2);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < G; ++i) row[g + i * tlow] = x[i];
+}
+
+// Transform `nrows` rows of length N held contiguously in shared memory
+// (row r at sm + r*N, using prime prime_of(r)), cooperatively by all threads
+// of the block.  Leaves forward results in [0, 4q) and inverse results in
+// [0, 2q) *without* the N^-1 factor; callers finish the reduction.
+template <bool FWD, typename PrimeOf>
+__device__ void ntt_rows_smem(uint32_t *sm, uint32_t nrows, const RnsParams &P, PrimeOf prime_of) {
+    const uint32_t N = P.N, logN = P.logN;
+    const uint32_t nthr = blockDim.x, tid = threadIdx.x;
+    uint32_t done = 0;  // stages completed
+    while (done < logN) {
+        const uint32_t R = (logN - done) >= 3 ? 3 : (logN - done);
+        const uint32_t G = 1u << R;
+        const uint32_t groups_per_row = N >> R;
+        // forward: stages s0 = done .. done+R-1; inverse: s_hi = logN-1-done .. down
+        const uint32_t log_tlow = FWD ? (logN - done - R) : done;
+        const uint32_t tlow = 1u << log_tlow;
+        for (uint32_t v = tid; v < nrows * groups_per_row; v += nthr) {
+            const uint32_t r = v / groups_per_row, vv = v - r * groups_per_row;
+            const uint32_t l = prime_of(r);
+            const uint32_t q = P.q[l];
+            const uint32_t *W = P.tw + (size_t)l * 4 * N + (FWD ? TW_FWD : TW_INV) * N;
+            const uint32_t *Wp = P.tw + (size_t)l * 4 * N + (FWD ? TW_FWD_SHOUP : TW_INV_SHOUP) * N;
+            const uint32_t low = vv & (tlow - 1), high = vv >> log_tlow;
+            const uint32_t g = (high << (log_tlow + R)) | low;
+            uint32_t *row = sm + (size_t)r * N;
+            if (FWD) {
+                if (R == 3) fwd_round_group<3>(row, g, tlow, done, high, W, Wp, q);
+                else if (R == 2) fwd_round_group<2>(row, g, tlow, done, high, W, Wp, q);
+                else fwd_round_group<1>(row, g, tlow, done, high, W, Wp, q);
+            } else {
+                const uint32_t s_hi = logN - 1 - done;
+                if (R == 3) inv_round_group<3>(row, g, tlow, s_hi, high, W, Wp, q);
+                else if (R == 2) inv_round_group<2>(row, g, tlow, s_hi, high, W, Wp, q);
+                else inv_round_group<1>(row, g, tlow, s_hi, high, W, Wp, q);
+            }
+        }
+        (void)G;
+        __syncthreads();
+        done += R;
+    }
+}
+
+// Final reductions.
+__device__ __forceinline__ uint32_t fwd_final(uint32_t x, uint32_t q) {  // [0,4q) -> [0,q)
+    x = x >= 2 * q ? x - 2 * q : x;
+    return x >= q ? x - q : x;
+}
+
+__device__ __forceinline__ uint32_t inv_final(uint32_t x, uint32_t ninv, uint32_t ninv_shoup,
+                                              uint32_t q) {  // [0,2q) * N^-1 -> [0,q)
+    uint32_t y = shoup_mul(x, ninv, ninv_shoup, q);
+    return y >= q ? y - q : y;
+}

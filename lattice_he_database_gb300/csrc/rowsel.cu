@@ -1,0 +1,330 @@
+// rowsel.cu — the RowSel scan of the OnionPIR family on GB300.
+//
+// GPIR (arXiv 2604.04696) section 2: RowSel is L*N independent point-wise
+// GEMMs  M_out[p,m,n] = sum_k M_in0[p,m,k] * M_in1[p,k,n]  (p: evaluation
+// point, m: ciphertext polynomial, k < D0 DB row, n < D1 DB column), and GEMM
+// kernels want the DB contiguous along k/n per point rather than p-major.
+// VIPIR section 4.2: with primes below 2^29 and 64-bit accumulators the
+// modular reduction can be deferred across many multiply-adds.
+//
+// Design (one GPU, HBM-bound for small B):
+//  * The DB is pre-encoded (encode.cu) so that every (p, column slab) is one
+//    contiguous D0 x W_s block, W_s <= 128 words.  A unit of work is one such
+//    block; units are split into equal contiguous ranges, one per CTA of a
+//    persistent grid, so each CTA streams its own region of HBM exactly once.
+//  * A producer warp moves the block through a 4-stage shared-memory ring
+//    with 1-D bulk async copies (cp.async.bulk, L2 evict-first) of 32 rows
+//    each, signalling mbarriers; 8 consumer warps compute from shared memory.
+//  * The query slice M_in0[p, :, :] (2B x D0 words) is gathered into shared
+//    memory when a CTA moves to a new point p.
+//  * Thread tile: 4 consecutive columns x MT ciphertext polynomials; warps
+//    split the polynomials (msplit) and the rows of each chunk (ksplit).
+//    Products of residues < 2^29 are accumulated with 32x32->64-bit
+//    multiply-adds; every <= 48 products the accumulator is folded
+//    (lo + hi * (2^32 mod q)); one Barrett reduction per output at the end,
+//    plus a sum of the ksplit partial residues.
+//  * Device waits are bounded; on a timeout the kernel raises
+//    PIR_STATUS_TIMEOUT, stops issuing copies, drains those in flight and
+//    runs the remaining control flow without waiting, so it always ends.
+#include <cstring>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int KC = 32;                         // DB rows per ring stage
+constexpr int NST = 4;                         // ring stages
+constexpr int NWC = 8;                         // consumer warps
+constexpr int NTHREADS = (NWC + 1) * 32;       // + one producer warp
+constexpr uint32_t STAGE_WORDS = KC * PIR_SLAB;  // 16 KiB
+constexpr uint32_t IN0_MAX_BYTES = 128 * 1024;
+constexpr uint32_t FOLD_LIMIT = 48;            // products between folds
+
+struct RowselArgs {
+    const uint32_t *db;
+    const uint32_t *query;
+    uint32_t *out;
+    uint32_t *status;
+    uint32_t N, L, D0, D1, D1p, S, Wlast;
+    uint32_t B, b0, Mv, Mp, msplit, ksplit, nchunks;
+    uint64_t P, units;
+    uint32_t q[PIR_MAX_RNS], r32[PIR_MAX_RNS];
+    uint64_t mu[PIR_MAX_RNS];
+};
+
+__device__ __forceinline__ uint32_t slab_width(const RowselArgs &A, uint32_t s) {
+    return s == A.S - 1 ? A.Wlast : PIR_SLAB;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant__ RowselArgs A) {
+    extern __shared__ __align__(128) uint32_t smw[];
+    uint32_t *ring = smw;                                    // NST * STAGE_WORDS
+    uint32_t *in0s = ring + NST * STAGE_WORDS;               // D0 * Mp   (k-major)
+    uint32_t *red = in0s + (size_t)A.D0 * A.Mp;              // ksplit * Mp * 128
+    uint64_t *bars = reinterpret_cast<uint64_t *>(red + (A.ksplit > 1 ? A.ksplit * A.Mp * PIR_SLAB : 0));
+    uint64_t *full = bars, *empty = bars + NST;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t u0 = (uint64_t)blockIdx.x * A.units / gridDim.x;
+    const uint64_t u1 = (uint64_t)(blockIdx.x + 1) * A.units / gridDim.x;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, NWC);
+        }
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ producer
+    if (warp == NWC) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            uint32_t stage = 0, phase = 0;
+            uint64_t issued = 0;
+            for (uint64_t u = u0; u < u1 && !abort_flag; ++u) {
+                const uint64_t p = u / A.S;
+                const uint32_t s = (uint32_t)(u - p * A.S);
+                const uint32_t Ws = slab_width(A, s);
+                const uint32_t *src = A.db + p * A.D0 * A.D1p + (uint64_t)s * A.D0 * PIR_SLAB;
+                for (uint32_t c = 0; c < A.nchunks; ++c) {
+                    const uint32_t rows = min((uint32_t)KC, A.D0 - c * KC);
+                    const uint32_t bytes = rows * Ws * 4;
+                    if (!mbar_wait(empty + stage, phase ^ 1, A.status)) {
+                        abort_flag = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full + stage, bytes);
+                    bulk_g2s(ring + stage * STAGE_WORDS, src + (uint64_t)c * KC * Ws, bytes, full + stage, pol);
+                    ++issued;
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
+                }
+            }
+            // The copies still in flight target this CTA's shared memory:
+            // wait (bounded) for the last min(issued, NST) of them to land.
+            const uint32_t pend = issued < (uint64_t)NST ? (uint32_t)issued : (uint32_t)NST;
+            for (uint32_t i = 0; i < pend; ++i) {
+                if (stage == 0) { stage = NST - 1; phase ^= 1; } else { --stage; }
+                mbar_wait(full + stage, phase, A.status);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers
+    const uint32_t ctid = threadIdx.x;  // 0 .. NWC*32-1
+    const uint32_t ms = warp % A.msplit, ks = warp / A.msplit;
+    uint32_t stage = 0, phase = 0;
+    uint64_t cur_p = ~0ull;
+
+    for (uint64_t u = u0; u < u1; ++u) {
+        const uint64_t p = u / A.S;
+        const uint32_t s = (uint32_t)(u - p * A.S);
+        const uint32_t Ws = slab_width(A, s);
+        const uint32_t l = (uint32_t)(p / A.N);
+        const uint32_t q = A.q[l], r32 = A.r32[l];
+        const uint64_t mu = A.mu[l];
+
+        if (p != cur_p) {  // gather M_in0[p, m, k] = query[b][k][c][p], m = 2b + c
+            named_barrier(1, NWC * 32);
+            const uint32_t tot = A.D0 * A.Mp;
+            for (uint32_t idx = ctid; idx < tot; idx += NWC * 32) {
+                const uint32_t k = idx / A.Mp, m = idx - k * A.Mp;
+                uint32_t v = 0;
+                if (m < A.Mv) {
+                    const uint64_t b = A.b0 + (m >> 1);
+                    v = A.query[((b * A.D0 + k) * 2 + (m & 1)) * A.P + p];
+                }
+                in0s[idx] = v;
+            }
+            named_barrier(1, NWC * 32);
+            cur_p = p;
+        }
+
+        uint64_t acc[MT][4];
+#pragma unroll
+        for (int i = 0; i < MT; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0;
+        uint32_t cnt = 0;
+        const bool active = 4u * lane < Ws;
+        const uint32_t *a_base = in0s + ms * MT;
+
+        for (uint32_t c = 0; c < A.nchunks; ++c) {
+            const uint32_t rows = min((uint32_t)KC, A.D0 - c * KC);
+            bool ok = !abort_flag;
+            if (ok && !mbar_wait(full + stage, phase, A.status)) {
+                abort_flag = 1;
+                ok = false;
+            }
+            const uint32_t per = rows > ks ? (rows - ks + A.ksplit - 1) / A.ksplit : 0;
+            if (cnt + per > FOLD_LIMIT) {
+#pragma unroll
+                for (int i = 0; i < MT; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fold64(acc[i][j], r32);
+                cnt = 0;
+            }
+            cnt += per;
+            if (ok && active) {
+                const uint32_t *st = ring + stage * STAGE_WORDS + 4 * lane;
+                const uint32_t *ak = a_base + (size_t)c * KC * A.Mp;
+#pragma unroll(MT == 2 ? 4 : 2)
+                for (uint32_t r = ks; r < rows; r += A.ksplit) {
+                    const uint4 d = *reinterpret_cast<const uint4 *>(st + r * Ws);
+                    uint32_t a[MT];
+                    if constexpr (MT == 2) {
+                        const uint2 v = *reinterpret_cast<const uint2 *>(ak + r * A.Mp);
+                        a[0] = v.x;
+                        a[1] = v.y;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < MT; i += 4) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(ak + r * A.Mp + i);
+                            a[i] = v.x;
+                            a[i + 1] = v.y;
+                            a[i + 2] = v.z;
+                            a[i + 3] = v.w;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) {
+                        acc[i][0] += (uint64_t)a[i] * d.x;
+                        acc[i][1] += (uint64_t)a[i] * d.y;
+                        acc[i][2] += (uint64_t)a[i] * d.z;
+                        acc[i][3] += (uint64_t)a[i] * d.w;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + stage);
+            if (++stage == NST) { stage = 0; phase ^= 1; }
+        }
+
+        // ---- unit epilogue: one reduction per output, then the write
+        const uint32_t nbase = s * PIR_SLAB;
+        if (A.ksplit == 1) {
+            if (active) {
+#pragma unroll
+                for (int i = 0; i < MT; ++i) {
+                    const uint32_t m = ms * MT + i;
+                    if (m >= A.Mv) continue;
+                    const uint64_t b = A.b0 + (m >> 1);
+                    const uint32_t cc = m & 1;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t n = nbase + 4 * lane + j;
+                        if (n < A.D1) A.out[((b * A.D1 + n) * 2 + cc) * A.P + p] = barrett64(acc[i][j], q, mu);
+                    }
+                }
+            }
+        } else {
+            named_barrier(1, NWC * 32);  // previous unit's readers of `red` are done
+            if (active) {
+#pragma unroll
+                for (int i = 0; i < MT; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        red[(ks * A.Mp + ms * MT + i) * PIR_SLAB + 4 * lane + j] = barrett64(acc[i][j], q, mu);
+            }
+            named_barrier(1, NWC * 32);
+            const uint32_t tot = A.Mv * Ws;
+            for (uint32_t idx = ctid; idx < tot; idx += NWC * 32) {
+                const uint32_t m = idx / Ws, col = idx - m * Ws;
+                const uint32_t n = nbase + col;
+                if (n >= A.D1) continue;
+                uint32_t sum = 0;  // < ksplit * q < 2^32
+                for (uint32_t kk = 0; kk < A.ksplit; ++kk) sum += red[(kk * A.Mp + m) * PIR_SLAB + col];
+                const uint64_t b = A.b0 + (m >> 1);
+                A.out[((b * A.D1 + n) * 2 + (m & 1)) * A.P + p] = sum % q;
+            }
+        }
+    }
+}
+
+template <int MT>
+int launch_pass(pir_ctx *ctx, RowselArgs &A, cudaStream_t st) {
+    const size_t smem = (size_t)NST * STAGE_WORDS * 4 + (size_t)A.D0 * A.Mp * 4 +
+                        (A.ksplit > 1 ? (size_t)A.ksplit * A.Mp * PIR_SLAB * 4 : 0) + 2 * NST * sizeof(uint64_t);
+    static bool attr_set[64] = {};
+    if (ctx->device < 64 && !attr_set[ctx->device]) {
+        if (cudaFuncSetAttribute(rowsel_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024) !=
+            cudaSuccess)
+            return PIR_ERR_CUDA;
+        attr_set[ctx->device] = true;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rowsel_kernel<MT>, NTHREADS, smem) != cudaSuccess ||
+        per_sm < 1)
+        return PIR_ERR_CUDA;
+    const uint64_t cap = (uint64_t)ctx->num_sms * per_sm;
+    const uint64_t grid = A.units < cap ? A.units : cap;
+    rowsel_kernel<MT><<<(unsigned)grid, NTHREADS, smem, st>>>(A);
+    return launch_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *query,
+                          uint32_t B, uint32_t *out, void *stream) {
+    if (!ctx || !db || !query || !out) return PIR_ERR_ARG;
+    if (!aligned16(db) || !aligned16(query) || !aligned16(out)) return PIR_ERR_ARG;
+    if (D0 == 0 || D1 == 0 || B == 0) return PIR_ERR_ARG;
+    if (D0 > 16384) return PIR_ERR_UNSUPPORTED;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
+
+    RowselArgs A;
+    memset(&A, 0, sizeof(A));
+    A.db = db;
+    A.query = query;
+    A.out = out;
+    A.status = ctx->d_status;
+    A.N = ctx->N;
+    A.L = ctx->L;
+    A.D0 = D0;
+    A.D1 = D1;
+    A.D1p = (D1 + 3) / 4 * 4;
+    A.S = (D1 + PIR_SLAB - 1) / PIR_SLAB;
+    A.Wlast = A.D1p - PIR_SLAB * (A.S - 1);
+    A.B = B;
+    A.P = (uint64_t)ctx->L * ctx->N;
+    A.units = A.P * A.S;
+    A.nchunks = (D0 + KC - 1) / KC;
+    for (uint32_t l = 0; l < ctx->L; ++l) {
+        A.q[l] = ctx->q[l];
+        A.r32[l] = ctx->r32[l];
+        A.mu[l] = ctx->mu[l];
+    }
+    // Polynomials per pass: the padded count Mp must be MT * msplit with
+    // msplit | NWC, and the query slice D0 * Mp words must fit on chip.
+    uint32_t mp_cap = 32;
+    while (mp_cap > 2 && (uint64_t)D0 * mp_cap * 4 > IN0_MAX_BYTES) mp_cap >>= 1;
+    if ((uint64_t)D0 * mp_cap * 4 > IN0_MAX_BYTES) return PIR_ERR_UNSUPPORTED;
+    const uint32_t b_per_pass = mp_cap / 2;
+    cudaStream_t st = (cudaStream_t)stream;
+    for (uint32_t b0 = 0; b0 < B; b0 += b_per_pass) {
+        const uint32_t nb = min(b_per_pass, B - b0);
+        A.b0 = b0;
+        A.Mv = 2 * nb;
+        int rc;
+        if (A.Mv <= 2) {
+            A.Mp = 2;
+            A.msplit = 1;
+            A.ksplit = NWC;
+            rc = launch_pass<2>(ctx, A, st);
+        } else {
+            uint32_t mp = 4;
+            while (mp < A.Mv) mp <<= 1;
+            A.Mp = mp;
+            A.msplit = mp / 4;
+            A.ksplit = NWC / A.msplit;
+            rc = launch_pass<4>(ctx, A, st);
+        }
+        if (rc) return rc;
+    }
+    return PIR_OK;
+}

@@ -1,0 +1,267 @@
+"""Thin Python binding of libpir.so (include/pir.h).
+
+Argument marshalling only: every step of the scan runs in the library's CUDA
+kernels.  Functions carry the C names; tensors are torch CUDA tensors (used as
+plain device buffers), streams are torch.cuda.Stream objects or None for the
+current stream.  A non-zero return code raises PirError.  The library must
+have been built (``lattice_he_database_gb300.build.build()``); there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+PIR_OK = 0
+PIR_ERR_ARG = -1
+PIR_ERR_CUDA = -2
+PIR_ERR_UNSUPPORTED = -3
+PIR_ERR_ALLOC = -4
+PIR_STATUS_TIMEOUT = 1
+PIR_SLAB = 128
+
+
+class PirError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (what, pir_strerror(code) if _lib else "?", code))
+
+
+_lib = None
+_u32p = ctypes.POINTER(ctypes.c_uint32)
+_vp = ctypes.c_void_p
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpir.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError("libpir.so not built: run lattice_he_database_gb300.build.build()")
+        L = ctypes.CDLL(_build.LIB)
+        L.pir_params_check.restype = ctypes.c_int
+        L.pir_params_check.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p]
+        L.pir_primes.restype = ctypes.c_int
+        L.pir_primes.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p]
+        L.pir_ctx_create.restype = ctypes.c_int
+        L.pir_ctx_create.argtypes = [ctypes.POINTER(_vp), ctypes.c_uint32, ctypes.c_uint32, _u32p, ctypes.c_int]
+        L.pir_ctx_destroy.restype = None
+        L.pir_ctx_destroy.argtypes = [_vp]
+        L.pir_ctx_psi.restype = ctypes.c_int
+        L.pir_ctx_psi.argtypes = [_vp, _u32p]
+        for name in ("pir_ntt_fwd", "pir_ntt_inv"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [_vp, _vp, _vp, ctypes.c_uint64, _vp]
+        L.pir_db_bytes.restype = ctypes.c_uint64
+        L.pir_db_bytes.argtypes = [_vp, ctypes.c_uint32, ctypes.c_uint32]
+        L.pir_db_encode.restype = ctypes.c_int
+        L.pir_db_encode.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                                    _vp, _vp]
+        L.pir_rowsel.restype = ctypes.c_int
+        L.pir_rowsel.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, ctypes.c_uint32, _vp, _vp]
+        L.pir_scalar_workspace_bytes.restype = ctypes.c_uint64
+        L.pir_scalar_workspace_bytes.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
+        L.pir_scalar_scan.restype = ctypes.c_int
+        L.pir_scalar_scan.argtypes = [_vp, _vp, ctypes.c_uint64, ctypes.c_uint64, _vp, ctypes.c_uint32, _vp,
+                                      _vp, ctypes.c_uint64, _vp]
+        L.pir_status.restype = ctypes.c_int
+        L.pir_status.argtypes = [_vp, _u32p, ctypes.c_int]
+        L.pir_strerror.restype = ctypes.c_char_p
+        L.pir_strerror.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def pir_strerror(code: int) -> str:
+    return lib().pir_strerror(code).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != PIR_OK:
+        raise PirError(rc, what)
+
+
+def _qarr(qs):
+    arr = (ctypes.c_uint32 * max(1, len(qs)))(*[int(q) for q in qs])
+    return arr
+
+
+def _dev_ptr(t: torch.Tensor, itemsize: int, what: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    if t.element_size() != itemsize:
+        raise ValueError("%s must have %d-byte elements" % (what, itemsize))
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---------------------------------------------------------------- context
+def pir_params_check(N: int, qs) -> int:
+    return lib().pir_params_check(N, len(qs), _qarr(qs))
+
+
+def pir_primes(N: int, L: int) -> list[int]:
+    """The L largest primes < 2^29 with q = 1 mod 2N (descending)."""
+    out = (ctypes.c_uint32 * max(1, L))()
+    _check(lib().pir_primes(N, L, out), "pir_primes")
+    return [int(v) for v in out[:L]]
+
+
+class Ctx:
+    """Owning handle of a pir_ctx (destroyed on close/GC)."""
+
+    def __init__(self, handle: int, N: int, qs, device: int):
+        self.handle = handle
+        self.N = N
+        self.qs = [int(q) for q in qs]
+        self.L = len(self.qs)
+        self.device = device
+
+    def close(self):
+        if self.handle:
+            lib().pir_ctx_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def _as_parameter_(self):
+        return _vp(self.handle)
+
+
+def pir_ctx_create(N: int, qs, device: int = 0) -> Ctx:
+    h = _vp()
+    _check(lib().pir_ctx_create(ctypes.byref(h), N, len(qs), _qarr(qs), device), "pir_ctx_create")
+    return Ctx(h.value, N, qs, device)
+
+
+def pir_ctx_destroy(ctx: Ctx):
+    ctx.close()
+
+
+def pir_ctx_psi(ctx: Ctx) -> list[int]:
+    out = (ctypes.c_uint32 * ctx.L)()
+    _check(lib().pir_ctx_psi(ctx, out), "pir_ctx_psi")
+    return [int(v) for v in out]
+
+
+def pir_status(ctx: Ctx, clear: bool = True) -> int:
+    flags = ctypes.c_uint32(0)
+    _check(lib().pir_status(ctx, ctypes.byref(flags), int(clear)), "pir_status")
+    return int(flags.value)
+
+
+# ---------------------------------------------------------------- NTT
+def pir_ntt_fwd(ctx: Ctx, inp: torch.Tensor, out: torch.Tensor, cnt: int, stream=None):
+    _check(lib().pir_ntt_fwd(ctx, _dev_ptr(inp, 4, "in"), _dev_ptr(out, 4, "out"), cnt, _stream(stream)),
+           "pir_ntt_fwd")
+
+
+def pir_ntt_inv(ctx: Ctx, inp: torch.Tensor, out: torch.Tensor, cnt: int, stream=None):
+    _check(lib().pir_ntt_inv(ctx, _dev_ptr(inp, 4, "in"), _dev_ptr(out, 4, "out"), cnt, _stream(stream)),
+           "pir_ntt_inv")
+
+
+# ---------------------------------------------------------------- RowSel
+def pir_db_bytes(ctx: Ctx, D0: int, D1: int) -> int:
+    return int(lib().pir_db_bytes(ctx, D0, D1))
+
+
+def pir_db_encode(ctx: Ctx, raw: torch.Tensor, k0: int, kcnt: int, D0: int, D1: int, db: torch.Tensor,
+                  stream=None):
+    _check(lib().pir_db_encode(ctx, _dev_ptr(raw, 4, "raw"), k0, kcnt, D0, D1, _dev_ptr(db, 4, "db"),
+                               _stream(stream)), "pir_db_encode")
+
+
+def pir_rowsel(ctx: Ctx, db: torch.Tensor, D0: int, D1: int, query: torch.Tensor, B: int, out: torch.Tensor,
+               stream=None):
+    _check(lib().pir_rowsel(ctx, _dev_ptr(db, 4, "db"), D0, D1, _dev_ptr(query, 4, "query"), B,
+                            _dev_ptr(out, 4, "out"), _stream(stream)), "pir_rowsel")
+
+
+# ---------------------------------------------------------------- scalar scan
+def pir_scalar_workspace_bytes(C: int, B: int) -> int:
+    return int(lib().pir_scalar_workspace_bytes(C, B))
+
+
+def pir_scalar_scan(ctx: Ctx, db: torch.Tensor, R: int, C: int, Q: torch.Tensor, B: int, out: torch.Tensor,
+                    workspace: torch.Tensor, stream=None):
+    ws = _dev_ptr(workspace, workspace.element_size(), "workspace")
+    _check(lib().pir_scalar_scan(ctx, _dev_ptr(db, 1, "db"), R, C, _dev_ptr(Q, 4, "Q"), B, _dev_ptr(out, 4, "out"),
+                                 ws, workspace.numel() * workspace.element_size(), _stream(stream)),
+           "pir_scalar_scan")
+
+
+# ---------------------------------------------------------------- helpers
+def empty_u32(n, device="cuda") -> torch.Tensor:
+    """A flat device buffer of n uint32 words (int32 storage)."""
+    return torch.empty(int(n), dtype=torch.int32, device=device)
+
+
+def db_layout_offset(N: int, L: int, D0: int, D1: int, p, k, n):
+    """Word offset of (evaluation point p, DB row k, DB column n) in the encoded DB
+    (numpy/int arrays broadcast).  Mirrors the layout documented in pir.h."""
+    import numpy as np
+    D1p = (D1 + 3) // 4 * 4
+    S = (D1 + PIR_SLAB - 1) // PIR_SLAB
+    Wl = D1p - PIR_SLAB * (S - 1)
+    p = np.asarray(p, dtype=np.int64)
+    k = np.asarray(k, dtype=np.int64)
+    n = np.asarray(n, dtype=np.int64)
+    s = n // PIR_SLAB
+    Ws = np.where(s == S - 1, Wl, PIR_SLAB)
+    return p * D0 * D1p + s * D0 * PIR_SLAB + k * Ws + (n - PIR_SLAB * s)
+
+
+class RowselServer:
+    """RowSel serving path: an encoded DB resident in HBM, answering query
+    batches given in coefficient form (host or device), through the C ABI:
+    forward NTT of the query, the scan, inverse NTT of the result."""
+
+    def __init__(self, ctx: Ctx, db: torch.Tensor, D0: int, D1: int, B: int, stream=None):
+        self.ctx, self.db, self.D0, self.D1, self.B = ctx, db, D0, D1, B
+        P = ctx.L * ctx.N
+        self.q_words = B * D0 * 2 * P
+        self.o_words = B * D1 * 2 * P
+        dev = db.device
+        self.q_coef = empty_u32(self.q_words, dev)
+        self.q_ntt = empty_u32(self.q_words, dev)
+        self.o_ntt = empty_u32(self.o_words, dev)
+        self.o_coef = empty_u32(self.o_words, dev)
+        self.stream = stream or torch.cuda.current_stream(dev)
+        self.launches_per_answer = 3
+
+    def answer_device(self, q_coef: torch.Tensor | None = None):
+        """Device-resident query (coefficient form) -> device result (coefficient form)."""
+        q = self.q_coef if q_coef is None else q_coef
+        c = self.ctx
+        pir_ntt_fwd(c, q, self.q_ntt, self.B * self.D0 * 2, self.stream)
+        pir_rowsel(c, self.db, self.D0, self.D1, self.q_ntt, self.B, self.o_ntt, self.stream)
+        pir_ntt_inv(c, self.o_ntt, self.o_coef, self.B * self.D1 * 2, self.stream)
+        return self.o_coef
+
+    def answer_host(self, q_host: torch.Tensor, o_host: torch.Tensor):
+        """Pinned host query in, pinned host result out (copies on the same stream)."""
+        with torch.cuda.stream(self.stream):
+            self.q_coef.copy_(q_host, non_blocking=True)
+            self.answer_device()
+            o_host.copy_(self.o_coef, non_blocking=True)
+        return o_host

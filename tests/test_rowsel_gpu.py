@@ -1,0 +1,184 @@
+"""GPU parity: DB encoding and the RowSel scan against the oracle (bit-exact).
+
+Small shapes are compared element by element (several column slabs, ragged
+row chunks and column tails, multi-pass batches).  The full-size workloads
+(6 GiB, 24 GiB with B = 16, 64 GiB with the query NTT and output INTT) are
+checked on sampled DB columns, all evaluation points, all queries.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.helpers import (CONFIGS, ensure_built, gather_db_device, make_device_db, oracle_db_columns, to_dev,
+                           to_host_u32)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pir():
+    ensure_built()
+    from lattice_he_database_gb300 import pir as p
+    return p
+
+
+def _small_case(pir, N, L, D0, D1, B, seed):
+    qs = oracle.primes(N, L)
+    psis = [oracle.min_psi(q, N) for q in qs]
+    ctx = pir.pir_ctx_create(N, qs)
+    raw = synth.coeffs(seed, (D0, D1, N))
+    db_t = pir.empty_u32(pir.pir_db_bytes(ctx, D0, D1) // 4)
+    db_t.fill_(-1)  # poison: every word must be written
+    pir.pir_db_encode(ctx, to_dev(raw), 0, D0, D0, D1, db_t)
+    query = synth.residues(seed + 1, (B, D0, 2, L, N), qs)
+    return ctx, qs, psis, raw, db_t, query
+
+
+@pytest.mark.parametrize("N,L,D0,D1,B", [
+    (64, 2, 3, 5, 1),        # single slab, ragged width
+    (64, 3, 33, 130, 1),     # 2 slabs (128 + 4), ragged row chunk (32 + 1)
+    (256, 2, 70, 257, 2),    # 3 slabs, 3 chunks
+    (16, 1, 5, 128, 3),      # exact slab, odd B
+    (64, 2, 40, 200, 5),     # padded polynomial count (M = 10 -> 16)
+    (16, 2, 9, 44, 16),      # M = 32
+    (16, 2, 9, 44, 17),      # two passes (16 + 1)
+])
+def test_encode_and_rowsel_small(pir, N, L, D0, D1, B):
+    ctx, qs, psis, raw, db_t, query = _small_case(pir, N, L, D0, D1, B, seed=N + D0 + D1 + B)
+    # the encoded DB holds NTT(record) at its documented position
+    enc = oracle.encode_records(raw, qs, psis)               # [D0][D1][L][N]
+    ks, ns = np.meshgrid(np.arange(D0), np.arange(D1), indexing="ij")
+    got_db = gather_db_device(db_t, N, L, D0, D1, ks.reshape(-1), ns.reshape(-1))
+    assert np.array_equal(got_db, enc.reshape(D0 * D1, L * N))
+    D1p = (D1 + 3) // 4 * 4
+    if D1p > D1:  # padding columns are zero
+        kp, npd = np.meshgrid(np.arange(D0), np.arange(D1, D1p), indexing="ij")
+        assert (gather_db_device(db_t, N, L, D0, D1, kp.reshape(-1), npd.reshape(-1)) == 0).all()
+    out = pir.empty_u32(B * D1 * 2 * L * N)
+    out.fill_(-1)
+    pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(query), B, out)
+    got = to_host_u32(out).reshape(B, D1, 2, L, N)
+    assert np.array_equal(got, oracle.rowsel(enc, query, qs))
+    assert pir.pir_status(ctx) == 0
+
+
+def test_rowsel_one_hot_returns_record(pir):
+    """Selection invariant: a one-hot query returns DB[i*][n] exactly after the INTT."""
+    N, L, D0, D1 = 4096, 3, 40, 131
+    qs = oracle.primes(N, L)
+    ctx = pir.pir_ctx_create(N, qs)
+    raw = synth.coeffs(5, (D0, D1, N))
+    db_t = pir.empty_u32(pir.pir_db_bytes(ctx, D0, D1) // 4)
+    pir.pir_db_encode(ctx, to_dev(raw), 0, D0, D0, D1, db_t)
+    for istar in (0, 17, D0 - 1):
+        q = np.zeros((1, D0, 2, L, N), np.uint32)
+        q[0, istar, 0] = 1       # the constant polynomial 1: all ones in NTT form
+        out = pir.empty_u32(D1 * 2 * L * N)
+        pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(q), 1, out)
+        pir.pir_ntt_inv(ctx, out, out, D1 * 2)
+        got = to_host_u32(out).reshape(D1, 2, L, N)
+        for l in range(L):
+            assert np.array_equal(got[:, 0, l], raw[istar])
+        assert (got[:, 1] == 0).all()
+    assert pir.pir_status(ctx) == 0
+
+
+def test_rowsel_max_residues(pir):
+    """All residues q-1 (largest products, longest lazy chains): out = D0 mod q."""
+    N, L, D0, D1, B = 64, 3, 1000, 9, 2
+    qs = oracle.primes(N, L)
+    ctx = pir.pir_ctx_create(N, qs)
+    P = L * N
+    D1p = (D1 + 3) // 4 * 4
+    # an encoded DB with every word q_l - 1 (written directly in the layout)
+    words = np.empty((P, D0 * D1p), np.uint32)
+    for l in range(L):
+        words[l * N:(l + 1) * N] = qs[l] - 1
+    db_t = to_dev(words.reshape(-1))
+    query = np.broadcast_to(np.array(qs, np.uint32).reshape(1, 1, 1, L, 1) - 1, (B, D0, 2, L, N)).copy()
+    out = pir.empty_u32(B * D1 * 2 * P)
+    pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(query), B, out)
+    got = to_host_u32(out).reshape(B, D1, 2, L, N)
+    for l in range(L):
+        assert (got[..., l, :] == D0 % qs[l]).all()
+    assert pir.pir_status(ctx) == 0
+
+
+def test_rowsel_rejects_bad_arguments(pir):
+    qs = oracle.primes(64, 2)
+    ctx = pir.pir_ctx_create(64, qs)
+    db = pir.empty_u32(pir.pir_db_bytes(ctx, 4, 4) // 4)
+    q = pir.empty_u32(4 * 2 * 2 * 64)
+    out = pir.empty_u32(4 * 2 * 2 * 64)
+    for args in [(0, 4, 1), (4, 0, 1), (4, 4, 0)]:
+        with pytest.raises(pir.PirError):
+            pir.pir_rowsel(ctx, db, args[0], args[1], q, args[2], out)
+    with pytest.raises(pir.PirError):
+        pir.pir_rowsel(ctx, db, 4, 4, q[1:], 1, out)
+    with pytest.raises(pir.PirError):
+        pir.pir_db_encode(ctx, q, 3, 2, 4, 4, db)   # k0 + kcnt > D0
+
+
+# ------------------------------------------------------------------ full-size workloads
+def _full_size(pir, name, sample_cols):
+    import torch
+    import synth.device as sd
+    cfg = CONFIGS[name]
+    N, L, D0, D1, B = cfg["N"], cfg["L"], cfg["D0"], cfg["D1"], cfg["B"]
+    qs = oracle.primes(N, L)
+    psis = [oracle.min_psi(q, N) for q in qs]
+    ctx = pir.pir_ctx_create(N, qs)
+    seed = 7
+    db_t = make_device_db(ctx, D0, D1, seed)
+    P = L * N
+    qwords = B * D0 * 2 * P
+    q_t = torch.empty(qwords, dtype=torch.int32, device="cuda")
+    sd.fill_residues(q_t, seed, synth.T_QUERY, N, qs)
+    query = to_host_u32(q_t).reshape(B, D0, 2, L, N)
+    out = pir.empty_u32(B * D1 * 2 * P)
+    if cfg["query_domain"] == "coeff":
+        # the serving path: NTT(query) -> RowSel -> INTT(result)
+        srv = pir.RowselServer(ctx, db_t, D0, D1, B)
+        res = srv.answer_device(q_t)
+        q_ntt_gpu = to_host_u32(srv.q_ntt).reshape(query.shape)
+        q_ntt = oracle.ntt_polys(query, qs, psis)
+        assert np.array_equal(q_ntt_gpu, q_ntt)
+        out_ntt = to_host_u32(srv.o_ntt).reshape(B, D1, 2, L, N)
+        out_coef = to_host_u32(res).reshape(B, D1, 2, L, N)
+    else:
+        q_ntt = query
+        pir.pir_rowsel(ctx, db_t, D0, D1, q_t, B, out)
+        out_ntt = to_host_u32(out).reshape(B, D1, 2, L, N)
+        out_coef = None
+    assert pir.pir_status(ctx) == 0
+    cols = np.array(sample_cols, np.uint32)
+    # the DB words of the sampled columns (a few rows) match the oracle encoding
+    enc = oracle_db_columns(qs, psis, N, D0, D1, seed, cols)    # [D0][ncols][L][N]
+    for k in (0, D0 - 1):
+        got = gather_db_device(db_t, N, L, D0, D1, [k] * len(cols), cols)
+        assert np.array_equal(got, enc[k].reshape(len(cols), P))
+    want = oracle.rowsel(enc, q_ntt, qs, cols=np.arange(len(cols)))   # [B][ncols][2][L][N]
+    assert np.array_equal(out_ntt[:, cols.astype(np.int64)], want)
+    if out_coef is not None:
+        want_coef = oracle.ntt_polys(want, qs, psis, inverse=True)
+        assert np.array_equal(out_coef[:, cols.astype(np.int64)], want_coef)
+    del db_t
+    torch.cuda.empty_cache()
+
+
+def test_full_tiny_exact(pir):
+    """16 x 16 records, 2 primes: every output compared."""
+    _full_size(pir, "tiny", sample_cols=list(range(16)))
+
+
+def test_full_rowsel_6g(pir):
+    _full_size(pir, "rowsel_6g", sample_cols=[0, 127, 128, 300, 511])
+
+
+def test_full_rowsel_24g_b16(pir):
+    _full_size(pir, "rowsel_24g_b16", sample_cols=[0, 513, 1023])
+
+
+def test_full_rowsel_64g_with_ntt(pir):
+    _full_size(pir, "rowsel_64g", sample_cols=[0, 1279, 1280, 1364])
