@@ -47,6 +47,10 @@ WORKLOADS = {
                       desc="RowSel 6 GiB: N=4096, 3 primes, D0=256 x D1=512, B=1, NTT-domain query"),
     "rowsel_24g_b16": dict(N=4096, L=3, D0=512, D1=1024, B=16, domain="ntt",
                            desc="RowSel 24 GiB: N=4096, 3 primes, D0=512 x D1=1024, B=16 queries, NTT-domain"),
+    # small case of the 64 GiB pipeline for profiler captures (3 GiB, 2 column slabs)
+    "rowsel_3g_prof": dict(N=4096, L=3, D0=256, D1=256, B=1, domain="coeff",
+                           desc="RowSel 3 GiB profiling case: N=4096, 3 primes, D0=256 x D1=256, B=1, "
+                                "NTT + RowSel + INTT"),
 }
 METRIC = "DB GB/s scanned & queries/s (RowSel, 64 GiB DB), % of GB300 HBM roofline"
 
@@ -61,6 +65,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiler runs)")
     return ap.parse_args()
 
 
@@ -313,7 +318,7 @@ def run_ours(args, cfg):
     q_host = torch.empty(srv.q_words, dtype=torch.int32, pin_memory=True)
     q_host.copy_(srv.q_coef.cpu())
     o_host = torch.empty(srv.o_words, dtype=torch.int32, pin_memory=True)
-    ke = max(1, min(args.e2e_steps, args.steps))
+    ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
     result_buf = srv.o_coef if coeff else srv.o_ntt
 
     def e2e_step():
@@ -322,17 +327,19 @@ def run_ours(args, cfg):
             step()
             o_host.copy_(result_buf, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(ke):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / ke
+    e2e_ms = None
+    if ke:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / ke
 
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
@@ -363,8 +370,9 @@ def run_ours(args, cfg):
                          "kernel": "rowsel_kernel", "peak_source": "%s hbm_gbs (copy)" % peak_kind,
                          "algorithmic_bytes_per_launch": algo_bytes},
             "clocks": clk,
-            "e2e": {"value": logical_db / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                    "h2d_bytes_per_step": q_bytes, "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms},
+            "e2e": None if e2e_ms is None else {
+                "value": logical_db / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": q_bytes,
+                "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms},
             "gpu_launches": args.steps * (3 if coeff else 1),
             "cpu_baseline": cpu,
         }

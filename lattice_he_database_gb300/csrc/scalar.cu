@@ -1,15 +1,430 @@
-// scalar.cu — scalar-HE scan (placeholder until the tensor-core kernel lands).
+// scalar.cu — scalar-HE DB scan (SimplePIR-family first fold) on tcgen05.
+//
+// VIPIR section 2.5: the online server work of SimplePIR with B batched
+// queries is a D1 x B x D0 GEMM of a byte DB by 32-bit query words, mod 2^32
+// (the reduction is free).  VIPIR section 4.1: run it on tensor cores by
+// splitting each 32-bit word into four bytes, Q = sum_i 2^(8i) Q_i, so that
+//     DB * Q = sum_i 2^(8i) (DB * Q_i)   mod 2^32.
+//
+// GB300 (sm_103a) has no integer tensor-core MMA (tcgen05 kind::i8 is not
+// available on this target), so the byte products run on the fp16 path
+// (kind::f16) where they are still exact:
+//  * Q's bytes are re-expressed as balanced base-256 digits d_i in
+//    [-128, 127] (Q = sum_i 256^i d_i mod 2^32), stored as fp16 (exact);
+//  * DB bytes 0..255 are exact fp16 values;
+//  * every product is an integer of magnitude <= 255*128 = 32640, so a sum
+//    of 512 of them stays below 2^24 and is exact in the fp32 accumulator.
+// The accumulator is therefore drained every 512 columns of the DB (a
+// "chunk"): the four digit planes are converted to integers and folded into
+// 32-bit running sums as  acc += S_0 + (S_1 << 8) + (S_2 << 16) + (S_3 << 24)
+// with wrap-around, which is exactly the byte-split identity mod 2^32.
+//
+// Kernel structure (one CTA per SM, persistent over 128-row DB tiles):
+//   warp 0      TMA producer: the 128 x 64-byte DB tile (tensor map) and the
+//               matching 256 x 64 fp16 digit tile (1-D bulk copy of a block
+//               pre-swizzled by the prep kernel) into a 3-stage ring;
+//   warp 1      TMEM allocator and the single MMA-issuing thread:
+//               4 x tcgen05.mma (M=128, N=256, K=16) per stage into one of
+//               two 256-column fp32 accumulators (double buffered so that a
+//               drain overlaps the next chunk's MMAs);
+//   warps 2-5   converters: DB bytes -> fp16 in the 128B-swizzled K-major
+//               layout the MMA reads;
+//   warps 6-9   epilogue: tcgen05.ld of a drained accumulator, integer
+//               conversion and the shifted accumulation; one row per thread;
+//               the 64 running sums per row are written at the end of a tile.
+// All mbarrier waits are bounded (PIR_STATUS_TIMEOUT); TMEM is always freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <cstring>
+
 #include "common.cuh"
 
+namespace {
+
+constexpr int SC_NS = 3;                      // pipeline stages
+constexpr int SC_KB = 64;                     // DB bytes (K elements) per stage
+constexpr int SC_TM = 128;                    // DB rows per tile (MMA M)
+constexpr int SC_BQ = 64;                     // queries per pass (digit planes hold 4 x 64 rows)
+constexpr int SC_N = 4 * SC_BQ;               // MMA N = 256
+constexpr int SC_CHUNK_STAGES = 8;            // stages per accumulator chunk: 512 K elements
+constexpr uint32_t SC_A_BYTES = SC_TM * 128;  // fp16 A tile: 128 rows x 64 halves
+constexpr uint32_t SC_B_BYTES = SC_N * 128;   // fp16 B tile: 256 rows x 64 halves
+constexpr uint32_t SC_U8_BYTES = SC_TM * SC_KB;
+constexpr uint32_t SC_STAGE_BYTES = SC_A_BYTES + SC_B_BYTES + SC_U8_BYTES;
+constexpr int SC_THREADS = 320;
+constexpr uint32_t SC_TMEM_COLS = 512;
+
+// Byte offset of (row, 16-byte chunk j) in a K-major tile with the 128-byte
+// swizzle: rows of 128 B, 8-row groups of 1 KiB, chunk index XOR (row % 8).
+__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t j) {
+    return (row >> 3) * 1024u + (row & 7u) * 128u + ((j ^ (row & 7u)) << 4);
+}
+
+// ---------------------------------------------------------------- digit prep
+// ws block kb (64 DB columns) = 256 rows (plane i, query b -> row 64 i + b)
+// x 64 fp16 digits, 128B-swizzled, 32 KiB.
+__global__ void __launch_bounds__(256) digits_kernel(const uint32_t *__restrict__ Q, uint32_t C, uint32_t B,
+                                                     uint8_t *__restrict__ ws) {
+    __shared__ uint32_t tile[64][SC_BQ + 1];
+    const uint32_t kb = blockIdx.x;
+    for (uint32_t i = threadIdx.x; i < 64 * SC_BQ; i += blockDim.x) {
+        const uint32_t k = i / SC_BQ, b = i % SC_BQ;
+        tile[k][b] = b < B ? Q[(uint64_t)(kb * 64 + k) * B + b] : 0u;
+    }
+    __syncthreads();
+    uint8_t *blk = ws + (uint64_t)kb * SC_B_BYTES;
+    for (uint32_t t = threadIdx.x; t < SC_N * 8; t += blockDim.x) {
+        const uint32_t n = t >> 3, j = t & 7;         // row n = 64*plane + b, chunk j = k 8j..8j+7
+        const uint32_t plane = n / SC_BQ, b = n % SC_BQ;
+        __align__(16) __half h[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            uint64_t y = tile[8 * j + e][b];
+            int d = 0;
+            for (uint32_t i = 0; i <= plane; ++i) {   // balanced base-256 digits, low first
+                const int lo = (int)(y & 0xFFu);
+                d = lo >= 128 ? lo - 256 : lo;
+                y = (y - (uint64_t)(int64_t)d) >> 8;
+            }
+            h[e] = __int2half_rn(d);
+        }
+        *reinterpret_cast<uint4 *>(blk + sw128_offset(n, j)) = *reinterpret_cast<const uint4 *>(h);
+    }
+}
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    // start>>4 | LBO (unused for swizzled K-major) | SBO 1024>>4 | version 1 | SWIZZLE_128B
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// kind::f16, A = B = F16, D = F32, K-major A and B, N = 256, M = 128
+constexpr uint32_t SC_IDESC = (1u << 4) | ((uint32_t)(SC_N >> 3) << 17) | ((uint32_t)(SC_TM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+        "l"(adesc), "l"(bdesc), "r"(SC_IDESC), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+struct ScalarArgs {
+    const uint8_t *ws;   // digit blocks
+    uint32_t *out;
+    uint32_t *status;
+    uint64_t R;
+    uint32_t C, B, ntiles, nkb;
+};
+
+__global__ void __launch_bounds__(SC_THREADS, 1)
+    scalar_kernel(const __grid_constant__ CUtensorMap dbmap, const __grid_constant__ ScalarArgs A) {
+    extern __shared__ uint8_t smraw[];
+    // 1 KiB alignment for the swizzle atoms
+    const uint32_t base_s = smem_u32(smraw);
+    uint8_t *sm = smraw + (((base_s + 1023u) & ~1023u) - base_s);
+    uint8_t *stA = sm;                                   // [NS][A]
+    uint8_t *stB = stA + SC_NS * SC_A_BYTES;             // [NS][B]
+    uint8_t *stU = stB + SC_NS * SC_B_BYTES;             // [NS][U8]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stU + SC_NS * SC_U8_BYTES);
+    uint64_t *full = bars, *conv = bars + SC_NS, *empty = bars + 2 * SC_NS;
+    uint64_t *accf = bars + 3 * SC_NS, *acce = accf + 2, *done = acce + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SC_NS; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(conv + s, 4);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf + b, 1);
+            mbar_init(acce + b, 4);
+        }
+        mbar_init(done, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(SC_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t nchunks = (A.nkb + SC_CHUNK_STAGES - 1) / SC_CHUNK_STAGES;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_db = policy_evict_first(), pol_q = policy_evict_last();
+            uint32_t it = 0;
+            for (uint32_t t = blockIdx.x; t < A.ntiles; t += gridDim.x) {
+                for (uint32_t kb = 0; kb < A.nkb; ++kb, ++it) {
+                    const uint32_t s = it % SC_NS, ph = (it / SC_NS) & 1;
+                    if (abort_flag || !mbar_wait(empty + s, ph ^ 1, A.status)) {
+                        abort_flag = 1;
+                        continue;
+                    }
+                    mbar_arrive_expect_tx(full + s, SC_U8_BYTES + SC_B_BYTES);
+                    tma_load_2d(stU + s * SC_U8_BYTES, &dbmap, (int)(kb * SC_KB), (int)(t * SC_TM), full + s, pol_db);
+                    bulk_g2s(stB + s * SC_B_BYTES, A.ws + (uint64_t)kb * SC_B_BYTES, SC_B_BYTES, full + s, pol_q);
+                }
+            }
+            // copies in flight land in this CTA's shared memory: wait for the last ones
+            for (uint32_t i = 0; i < SC_NS && i < it; ++i) {
+                const uint32_t j = it - 1 - i;
+                mbar_wait(full + j % SC_NS, (j / SC_NS) & 1, A.status);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, g = 0;
+            for (uint32_t t = blockIdx.x; t < A.ntiles; t += gridDim.x) {
+                for (uint32_t ch = 0; ch < nchunks; ++ch, ++g) {
+                    const uint32_t buf = g & 1, use = (g >> 1) & 1;
+                    bool ok = !abort_flag && mbar_wait(acce + buf, use ^ 1, A.status);
+                    if (!ok) abort_flag = 1;
+                    tc_fence_after();
+                    const uint32_t d = tmem + buf * SC_N;
+                    const uint32_t kb_end = min(A.nkb, (ch + 1) * SC_CHUNK_STAGES);
+                    for (uint32_t kb = ch * SC_CHUNK_STAGES; kb < kb_end; ++kb, ++it) {
+                        const uint32_t s = it % SC_NS, ph = (it / SC_NS) & 1;
+                        if (!abort_flag && !mbar_wait(conv + s, ph, A.status)) abort_flag = 1;
+                        if (abort_flag) continue;
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(stA + s * SC_A_BYTES), b0 = smem_u32(stB + s * SC_B_BYTES);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)   // K = 16 fp16 = 32 bytes per MMA
+                            mma_f16(d, sdesc_sw128(a0 + 32 * k), sdesc_sw128(b0 + 32 * k),
+                                    (kb > ch * SC_CHUNK_STAGES || k > 0) ? 1u : 0u);
+                        mma_commit(empty + s);        // stage reusable once these MMAs finish
+                    }
+                    if (!abort_flag) mma_commit(accf + buf);  // chunk complete -> epilogue
+                }
+            }
+            // all issued MMAs complete before TMEM is released
+            mma_commit(done);
+            mbar_wait(done, 0, A.status);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------ converters: bytes -> fp16, swizzled
+        const uint32_t ct = threadIdx.x - 64;  // 0..127
+        uint32_t it = 0;
+        for (uint32_t t = blockIdx.x; t < A.ntiles; t += gridDim.x) {
+            for (uint32_t kb = 0; kb < A.nkb; ++kb, ++it) {
+                const uint32_t s = it % SC_NS, ph = (it / SC_NS) & 1;
+                if (!abort_flag && !mbar_wait(full + s, ph, A.status)) abort_flag = 1;
+                if (!abort_flag) {
+                    const uint8_t *u = stU + s * SC_U8_BYTES;
+                    uint8_t *a = stA + s * SC_A_BYTES;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t q = ct + 128 * i;          // 16-byte piece: row q/4, part q%4
+                        const uint32_t row = q >> 2, part = q & 3;
+                        const uint4 w = *reinterpret_cast<const uint4 *>(u + row * SC_KB + part * 16);
+                        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+                        uint32_t h[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            // 0x64xx is the fp16 value 1024 + x: subtract 1024 exactly
+                            const uint32_t lo = __byte_perm(ws4[e], 0x64646464u, 0x5140);
+                            const uint32_t hi = __byte_perm(ws4[e], 0x64646464u, 0x7362);
+                            const __half2 c = __floats2half2_rn(1024.f, 1024.f);
+                            __half2 l2 = __hsub2(*reinterpret_cast<const __half2 *>(&lo), c);
+                            __half2 h2 = __hsub2(*reinterpret_cast<const __half2 *>(&hi), c);
+                            h[2 * e] = *reinterpret_cast<uint32_t *>(&l2);
+                            h[2 * e + 1] = *reinterpret_cast<uint32_t *>(&h2);
+                        }
+                        *reinterpret_cast<uint4 *>(a + sw128_offset(row, 2 * part)) = make_uint4(h[0], h[1], h[2], h[3]);
+                        *reinterpret_cast<uint4 *>(a + sw128_offset(row, 2 * part + 1)) =
+                            make_uint4(h[4], h[5], h[6], h[7]);
+                    }
+                    fence_proxy_async();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(conv + s);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue: drain, convert, accumulate
+        const uint32_t quad = warp & 3;               // TMEM lane quadrant of this warp
+        const uint32_t row_in_tile = quad * 32 + lane;
+        uint32_t g = 0;
+        for (uint32_t t = blockIdx.x; t < A.ntiles; t += gridDim.x) {
+            uint32_t acc[SC_BQ];
+#pragma unroll
+            for (int b = 0; b < SC_BQ; ++b) acc[b] = 0;
+            for (uint32_t ch = 0; ch < nchunks; ++ch, ++g) {
+                const uint32_t buf = g & 1, use = (g >> 1) & 1;
+                if (!abort_flag && !mbar_wait(accf + buf, use, A.status)) abort_flag = 1;
+                tc_fence_after();
+                if (!abort_flag) {
+                    const uint32_t taddr = tmem + ((quad * 32u) << 16) + buf * SC_N;
+#pragma unroll
+                    for (int plane = 0; plane < 4; ++plane) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t v[32];
+                            tmem_ld32(taddr + plane * SC_BQ + half * 32, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int s = __float2int_rn(__uint_as_float(v[j]));
+                                acc[half * 32 + j] += (uint32_t)s << (8 * plane);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce + buf);
+            }
+            const uint64_t r = (uint64_t)t * SC_TM + row_in_tile;
+            if (r < A.R && !abort_flag) {
+                uint32_t *o = A.out + r * A.B;
+                if (A.B == SC_BQ) {
+#pragma unroll
+                    for (int b = 0; b < SC_BQ; b += 4)
+                        *reinterpret_cast<uint4 *>(o + b) = make_uint4(acc[b], acc[b + 1], acc[b + 2], acc[b + 3]);
+                } else {
+#pragma unroll
+                    for (int b = 0; b < SC_BQ; ++b)
+                        if ((uint32_t)b < A.B) o[b] = acc[b];
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(SC_TMEM_COLS)
+                     : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_tiled() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+size_t scalar_smem_bytes() { return 1024 + (size_t)SC_NS * SC_STAGE_BYTES + 256; }
+
+}  // namespace
+
 extern "C" uint64_t pir_scalar_workspace_bytes(uint64_t C, uint32_t B) {
-    if (C == 0 || B == 0) return 0;
-    return C * (uint64_t)B * 4 * 2;
+    if (C == 0 || B == 0 || C % SC_KB) return 0;
+    return (C / SC_KB) * (uint64_t)SC_B_BYTES;
 }
 
 extern "C" int pir_scalar_scan(pir_ctx *ctx, const uint8_t *db, uint64_t R, uint64_t C, const uint32_t *Q,
                                uint32_t B, uint32_t *out, void *workspace, uint64_t workspace_bytes,
                                void *stream) {
-    (void)ctx; (void)db; (void)R; (void)C; (void)Q; (void)B; (void)out; (void)workspace;
-    (void)workspace_bytes; (void)stream;
-    return PIR_ERR_UNSUPPORTED;
+    if (!ctx || !db || !Q || !out || !workspace) return PIR_ERR_ARG;
+    if (!aligned16(db) || !aligned16(Q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 127))
+        return PIR_ERR_ARG;
+    if (R == 0 || C == 0 || B == 0) return PIR_ERR_ARG;
+    if (C % SC_KB || B > SC_BQ || C > (1ull << 31) || R > (1ull << 31)) return PIR_ERR_UNSUPPORTED;
+    if (workspace_bytes < pir_scalar_workspace_bytes(C, B)) return PIR_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
+    auto encode = get_encode_tiled();
+    if (!encode) return PIR_ERR_CUDA;
+
+    CUtensorMap map;
+    memset(&map, 0, sizeof(map));
+    const cuuint64_t gdim[2] = {C, R};
+    const cuuint64_t gstride[1] = {C};
+    const cuuint32_t box[2] = {SC_KB, SC_TM};
+    const cuuint32_t estride[2] = {1, 1};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(db), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PIR_ERR_ARG;
+
+    cudaStream_t st = (cudaStream_t)stream;
+    const uint32_t nkb = (uint32_t)(C / SC_KB);
+    digits_kernel<<<nkb, 256, 0, st>>>(Q, (uint32_t)C, B, reinterpret_cast<uint8_t *>(workspace));
+    if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
+
+    const size_t smem = scalar_smem_bytes();
+    static bool attr_set[64] = {};
+    if (ctx->device < 64 && !attr_set[ctx->device]) {
+        if (cudaFuncSetAttribute(scalar_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return PIR_ERR_CUDA;
+        attr_set[ctx->device] = true;
+    }
+    ScalarArgs a;
+    a.ws = reinterpret_cast<const uint8_t *>(workspace);
+    a.out = out;
+    a.status = ctx->d_status;
+    a.R = R;
+    a.C = (uint32_t)C;
+    a.B = B;
+    a.ntiles = (uint32_t)((R + SC_TM - 1) / SC_TM);
+    a.nkb = nkb;
+    const uint32_t grid = a.ntiles < (uint32_t)ctx->num_sms ? a.ntiles : (uint32_t)ctx->num_sms;
+    scalar_kernel<<<grid, SC_THREADS, smem, st>>>(map, a);
+    return launch_status(cudaGetLastError());
 }

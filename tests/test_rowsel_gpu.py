@@ -45,7 +45,7 @@ def _small_case(pir, N, L, D0, D1, B, seed):
     (16, 2, 9, 44, 17),      # two passes (16 + 1)
 ])
 def test_encode_and_rowsel_small(pir, N, L, D0, D1, B):
-    ctx, qs, psis, raw, db_t, query = _small_case(pir, N, L, D0, D1, B, seed=N + D0 + D1 + B)
+    ctx, qs, psis, raw, db_t, query = _small_case(pir, N, L, D0, D1, B, seed=(N + D0 + D1 + B) % 251)
     # the encoded DB holds NTT(record) at its documented position
     enc = oracle.encode_records(raw, qs, psis)               # [D0][D1][L][N]
     ks, ns = np.meshgrid(np.arange(D0), np.arange(D1), indexing="ij")
