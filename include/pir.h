@@ -189,6 +189,27 @@ int pir_scalar_scan(pir_ctx *ctx, const uint8_t *db, uint64_t R, uint64_t C,
                     void *workspace, uint64_t workspace_bytes, void *stream);
 
 /*
+ * pir_scalar_scan_noalloc — pir_scalar_scan for callers that cannot allocate
+ * device memory at call time (a framework allocator owns the device pool,
+ * the caller only receives its input and output buffers, or a cudaMalloc
+ * and its implicit synchronisation are not acceptable on the call path).
+ * The pages have no counterpart; this is a deployment variant.
+ *   Same arguments, layouts, results and errors as pir_scalar_scan, minus the
+ *   workspace: the split query is staged in a static device array of
+ *   8 MiB that the library reserves on every GPU where it is loaded, so
+ *   C <= 16384 (larger C returns PIR_ERR_UNSUPPORTED).  No device memory is
+ *   allocated or freed by this call.
+ *   The first call on a device looks up the array's device address (one
+ *   runtime query, no allocation); make that first call before any stream
+ *   capture.  All calls share the array and it keeps the last call's
+ *   contents; each call rewrites what it reads, so nothing needs clearing,
+ *   but calls that overlap on the GPU (different streams, no ordering
+ *   between them) race on it and give undefined results.
+ */
+int pir_scalar_scan_noalloc(pir_ctx *ctx, const uint8_t *db, uint64_t R, uint64_t C,
+                            const uint32_t *Q, uint32_t B, uint32_t *out, void *stream);
+
+/*
  * pir_status — read the context's device status word (PIR_STATUS_* bits set
  * by kernels whose bounded waits ran out) into *flags; clear it if `clear`.
  * Synchronises the context's device.

@@ -428,3 +428,47 @@ extern "C" int pir_scalar_scan(pir_ctx *ctx, const uint8_t *db, uint64_t R, uint
     scalar_kernel<<<grid, SC_THREADS, smem, st>>>(map, a);
     return launch_status(cudaGetLastError());
 }
+
+// ---------------------------------------------------------------- allocation-free variant
+//
+// Some callers cannot allocate device memory when they run the scan: code
+// that runs while a framework's caching allocator owns the whole device pool,
+// plugin or serving paths that are handed only the input and output buffers,
+// and latency-critical loops where a cudaMalloc (which may synchronise the
+// device) is not acceptable.  For them the split-query scratch lives in a
+// fixed static device array instead of a caller-provided workspace.
+//
+// Limit: the array holds the digit blocks for at most kNoAllocMaxC DB
+// columns (C * 512 bytes; 8 MiB for 16384 columns).  Every GPU on which the
+// library is loaded keeps this array until the process exits.
+#include <atomic>
+
+namespace {
+
+constexpr uint64_t kNoAllocMaxC = 16384;
+constexpr uint64_t kNoAllocScratchBytes = kNoAllocMaxC / SC_KB * SC_B_BYTES;  // 8 MiB
+
+static __device__ __align__(256) uint8_t g_scalar_scratch[kNoAllocScratchBytes];
+
+// Device address of g_scalar_scratch, looked up once per device.
+std::atomic<void *> g_scratch_addr[64];
+
+}  // namespace
+
+extern "C" int pir_scalar_scan_noalloc(pir_ctx *ctx, const uint8_t *db, uint64_t R, uint64_t C, const uint32_t *Q,
+                                       uint32_t B, uint32_t *out, void *stream) {
+    if (!ctx || ctx->device < 0 || ctx->device >= 64) return PIR_ERR_ARG;
+    if (C > kNoAllocMaxC) return PIR_ERR_UNSUPPORTED;  // beyond the static scratch
+    // Make the context's device current before touching its copy of the array.
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
+    void *scratch = g_scratch_addr[ctx->device].load(std::memory_order_acquire);
+    if (!scratch) {
+        // One-time set-up per device: the symbol's host-side name is only a
+        // stand-in, so ask the runtime for the device address.
+        if (cudaGetSymbolAddress(&scratch, g_scalar_scratch) != cudaSuccess || !scratch) return PIR_ERR_CUDA;
+        g_scratch_addr[ctx->device].store(scratch, std::memory_order_release);
+    }
+    // The digit kernel rewrites every scratch block the scan reads, so stale
+    // contents from an earlier call never leak into this one.
+    return pir_scalar_scan(ctx, db, R, C, Q, B, out, scratch, kNoAllocScratchBytes, stream);
+}

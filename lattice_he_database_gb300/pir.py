@@ -210,6 +210,18 @@ def pir_scalar_scan(ctx: Ctx, db: torch.Tensor, R: int, C: int, Q: torch.Tensor,
            "pir_scalar_scan")
 
 
+def pir_scalar_scan_noalloc(ctx: Ctx, db: torch.Tensor, R: int, C: int, Q: torch.Tensor, B: int,
+                            out: torch.Tensor, stream=None):
+    """pir_scalar_scan without a workspace argument: the library stages the
+    split query in its own static device array (C <= 16384), allocating
+    nothing.  For callers that cannot allocate device memory per call."""
+    f = lib().pir_scalar_scan_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [_vp, _vp, ctypes.c_uint64, ctypes.c_uint64, _vp, ctypes.c_uint32, _vp, _vp]
+    _check(f(ctx, _dev_ptr(db, 1, "db"), R, C, _dev_ptr(Q, 4, "Q"), B, _dev_ptr(out, 4, "out"), _stream(stream)),
+           "pir_scalar_scan_noalloc")
+
+
 # ---------------------------------------------------------------- helpers
 def empty_u32(n, device="cuda") -> torch.Tensor:
     """A flat device buffer of n uint32 words (int32 storage)."""
