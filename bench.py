@@ -47,6 +47,11 @@ WORKLOADS = {
                       desc="RowSel 6 GiB: N=4096, 3 primes, D0=256 x D1=512, B=1, NTT-domain query"),
     "rowsel_24g_b16": dict(N=4096, L=3, D0=512, D1=1024, B=16, domain="ntt",
                            desc="RowSel 24 GiB: N=4096, 3 primes, D0=512 x D1=1024, B=16 queries, NTT-domain"),
+    # scalar-HE scan: byte DB x 64 query words mod 2^32 (tcgen05 fp16 path)
+    "scalar_16g": dict(kind="scalar", R=131072, C=131072, B=64,
+                       desc="Scalar-HE scan: DB 131072 x 131072 uint8 (16 GiB) x Q 131072 x 64 uint32, mod 2^32"),
+    "scalar_2g_prof": dict(kind="scalar", R=16384, C=131072, B=64,
+                           desc="Scalar-HE scan profiling case: DB 16384 x 131072 uint8 (2 GiB), B=64"),
     # small case of the 64 GiB pipeline for profiler captures (3 GiB, 2 column slabs)
     "rowsel_3g_prof": dict(N=4096, L=3, D0=256, D1=256, B=1, domain="coeff",
                            desc="RowSel 3 GiB profiling case: N=4096, 3 primes, D0=256 x D1=256, B=1, "
@@ -148,32 +153,80 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- oracle (CPU) leg
-def oracle_rowsel_sample(cfg, budget_s: float):
-    """Time the oracle RowSel on a bounded sample: all D0 rows and B queries, a
-    subset of evaluation points (prime 0) and DB columns.  Returns
-    (GB/s, threads, description, seconds)."""
+ORACLE_POINTS = 1024   # evaluation points per oracle sample (of L*N = 12288)
+
+
+def _oracle_rowsel_inputs(cfg, ncols):
     import oracle
     import synth
     N, D0, B = cfg["N"], cfg["D0"], cfg["B"]
     q0 = oracle.primes(N, 1)[0]
+    db = synth.residues(11, (D0, ncols, 1, ORACLE_POINTS), [q0], tid=synth.T_EXTRA)
+    qu = synth.residues(12, (B, D0, 2, 1, ORACLE_POINTS), [q0], tid=synth.T_EXTRA)
+    return q0, db, qu
+
+
+def oracle_rowsel_calibrate(cfg, seconds: float):
+    """Columns per oracle call so that one call takes about `seconds` on all host cores."""
+    import oracle
     threads = oracle.default_threads()
-    npts = 1024
+    q0, db, qu = _oracle_rowsel_inputs(cfg, threads)
+    t = time.perf_counter()
+    oracle.rowsel(db, qu, [q0], threads=threads)
+    t1 = time.perf_counter() - t
+    ncols = threads * max(1, int(seconds / max(t1, 1e-4)))
+    return min(ncols, cfg["D1"]), threads
 
-    def run(ncols):
-        db = synth.residues(11, (D0, ncols, 1, npts), [q0], tid=synth.T_EXTRA)
-        qu = synth.residues(12, (B, D0, 2, 1, npts), [q0], tid=synth.T_EXTRA)
-        t = time.perf_counter()
-        oracle.rowsel(db, qu, [q0], threads=threads)
-        return time.perf_counter() - t
 
-    t1 = run(threads)
-    ncols = threads * max(1, min(64, int(budget_s / max(t1, 1e-3))))
-    ncols = min(ncols, cfg["D1"])
-    dt = run(ncols)
-    nbytes = D0 * ncols * npts * 4
+def oracle_rowsel_sample(cfg, budget_s: float):
+    """Time the oracle RowSel on a bounded sample: all D0 rows and B queries,
+    ORACLE_POINTS evaluation points (prime 0) and a calibrated number of DB
+    columns.  Returns (GB/s, threads, description, seconds)."""
+    import oracle
+    ncols, threads = oracle_rowsel_calibrate(cfg, budget_s)
+    q0, db, qu = _oracle_rowsel_inputs(cfg, ncols)
+    t = time.perf_counter()
+    oracle.rowsel(db, qu, [q0], threads=threads)
+    dt = time.perf_counter() - t
+    nbytes = cfg["D0"] * ncols * ORACLE_POINTS * 4
     desc = ("oracle RowSel on %d of %d DB columns x %d of %d evaluation points, all %d rows, B=%d"
-            % (ncols, cfg["D1"], npts, cfg["L"] * N, D0, B))
-    return nbytes / dt / 1e9, threads, desc, dt, (ncols, npts)
+            % (ncols, cfg["D1"], ORACLE_POINTS, cfg["L"] * cfg["N"], cfg["D0"], cfg["B"]))
+    return nbytes / dt / 1e9, threads, desc, dt
+
+
+def run_reference_scalar(args, cfg):
+    """Reference arm for the scalar scan: the oracle on a bounded row sample."""
+    import oracle
+    import synth
+    R, C, B = cfg["R"], cfg["C"], cfg["B"]
+    threads = oracle.default_threads()
+    Q = synth.words(7, (C, B))
+    rows = threads
+    db = synth.db_bytes(7, (rows, C))
+    t = time.perf_counter()
+    oracle.scalar_scan(db, Q, threads=threads)
+    t1 = time.perf_counter() - t
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    rows = max(threads, threads * int(per_step / max(t1, 1e-4)))
+    rows = min(rows, R)
+    db = synth.db_bytes(7, (rows, C))
+    for _ in range(args.warmup):
+        oracle.scalar_scan(db, Q, threads=threads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.scalar_scan(db, Q, threads=threads)
+    dt = (time.perf_counter() - t) / max(1, args.steps)
+    value = rows * C / dt / 1e9
+    sample = "oracle scalar scan per step: %d of %d DB rows x %d columns, B=%d" % (rows, R, C, B)
+    line = {
+        "impl": "reference", "metric": "scalar-HE scan: DB GB/s scanned", "value": value, "unit": "GB/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8 x u32",
+        "data": "synthetic", "config": {"workload": args.workload, "desc": cfg["desc"]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
 
 
 def run_reference(args, cfg):
@@ -183,29 +236,22 @@ def run_reference(args, cfg):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    N, D0, B = cfg["N"], cfg["D0"], cfg["B"]
-    q0 = oracle.primes(N, 1)[0]
-    threads = oracle.default_threads()
-    npts = 256
-    total_budget = 120.0
-    per_step = total_budget / max(1, args.steps + args.warmup)
-    db1 = synth.residues(11, (D0, threads, 1, npts), [q0], tid=synth.T_EXTRA)
-    qu = synth.residues(12, (B, D0, 2, 1, npts), [q0], tid=synth.T_EXTRA)
-    t = time.perf_counter()
-    oracle.rowsel(db1, qu, [q0], threads=threads)
-    t1 = time.perf_counter() - t
-    ncols = min(cfg["D1"], max(1, threads * max(1, int(per_step / max(t1, 1e-4)))))
-    db = synth.residues(11, (D0, ncols, 1, npts), [q0], tid=synth.T_EXTRA)
+    if cfg.get("kind") == "scalar":
+        return run_reference_scalar(args, cfg)
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    ncols, threads = oracle_rowsel_calibrate(cfg, per_step)
+    q0, db, qu = _oracle_rowsel_inputs(cfg, ncols)
     for _ in range(args.warmup):
         oracle.rowsel(db, qu, [q0], threads=threads)
     t = time.perf_counter()
     for _ in range(args.steps):
         oracle.rowsel(db, qu, [q0], threads=threads)
     dt = (time.perf_counter() - t) / max(1, args.steps)
-    nbytes = D0 * ncols * npts * 4
+    N, D0, B = cfg["N"], cfg["D0"], cfg["B"]
+    nbytes = D0 * ncols * ORACLE_POINTS * 4
     value = nbytes / dt / 1e9
     sample = ("oracle RowSel per step: %d of %d DB columns x %d of %d evaluation points, all %d rows, B=%d"
-              % (ncols, cfg["D1"], npts, cfg["L"] * N, D0, B))
+              % (ncols, cfg["D1"], ORACLE_POINTS, cfg["L"] * N, D0, B))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -219,6 +265,81 @@ def run_reference(args, cfg):
 
 
 # ---------------------------------------------------------------- GPU leg
+def kernel_rooflines(coeff, q_bytes, o_bytes, ntt_fwd_ms, ntt_inv_ms, hbm_peak):
+    """HBM fractions of the NTT kernels of the step (read + write of every residue)."""
+    if not coeff:
+        return None
+    out = {}
+    for name, nbytes, ms in (("ntt_fwd", 2 * q_bytes, ntt_fwd_ms), ("ntt_inv", 2 * o_bytes, ntt_inv_ms)):
+        ach = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                     "algorithmic_bytes_per_launch": nbytes}
+    return out
+
+
+def run_scalar(args, cfg):
+    """Scalar-HE scan: one step = digit split of Q + the tensor-core scan."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    import synth.device as sd
+    from lattice_he_database_gb300 import pir
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    R, C, B = cfg["R"], cfg["C"], cfg["B"]
+    ctx = pir.pir_ctx_create(4096, pir.pir_primes(4096, 1), local)
+    db = torch.empty(R * C, dtype=torch.uint8, device="cuda")
+    sd.fill_bytes(db, 7, synth.T_SCALAR_DB)
+    Q = torch.empty(C * B, dtype=torch.int32, device="cuda")
+    sd.fill_words(Q, 7, synth.T_SCALAR_Q)
+    out = torch.empty(R * B, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pir.pir_scalar_workspace_bytes(C, B), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        pir.pir_scalar_scan(ctx, db, R, C, Q, B, out, ws, stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        pir.pir_scalar_scan(ctx, db, R, C, Q, B, out, ws, stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    if pir.pir_status(ctx):
+        raise RuntimeError("device status word set")
+    peaks, kind = measured_peaks()
+    db_bytes = R * C
+    flops = 2.0 * R * C * 4 * 64        # fp16 multiply-adds on 4 digit planes x 64 query slots
+    tf = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "scalar-HE scan: DB GB/s scanned", "value": db_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8 x u32 (fp16 digits, fp32 accumulate)",
+        "data": "synthetic: seeded SplitMix64 bytes U[0,256), words U[0,2^32)",
+        "config": {"workload": args.workload, "desc": cfg["desc"], "R": R, "C": C, "B": B,
+                   "l2": "inputs larger than L2 (DB %.1f GiB), no flush" % (db_bytes / GIB)},
+        "queries_per_s": B * 1e3 / ms,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
+                     "frac": tf / float(peaks["bf16_tflops"]), "traffic": None, "kernel": "scalar_kernel",
+                     "peak_source": "%s bf16_tflops (fp16 dense rate is the same)" % kind,
+                     "hbm_frac": db_bytes / (ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"])},
+        "clocks": clk, "gpu_launches": 2 * args.steps, "e2e": None, "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    return line
+
+
 def device_db(ctx, D0, D1, seed):
     """Seeded raw records generated on the device, encoded in row chunks."""
     import torch
@@ -270,15 +391,19 @@ def run_ours(args, cfg):
     coeff = cfg["domain"] == "coeff"
 
     def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
         if coeff:
             pir.pir_ntt_fwd(ctx, srv.q_coef, srv.q_ntt, B * D0 * 2, stream)
         if ev is not None:
-            ev[0].record(stream)
+            ev[1].record(stream)
         pir.pir_rowsel(ctx, db, D0, D1, srv.q_ntt if coeff else srv.q_coef, B, srv.o_ntt, stream)
         if ev is not None:
-            ev[1].record(stream)
+            ev[2].record(stream)
         if coeff:
             pir.pir_ntt_inv(ctx, srv.o_ntt, srv.o_coef, B * D1 * 2, stream)
+        if ev is not None:
+            ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -289,7 +414,7 @@ def run_ours(args, cfg):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -304,7 +429,9 @@ def run_ours(args, cfg):
         dist.barrier()
     clk = clocks.stop()
     ms_total = t0.elapsed_time(t1)
-    rowsel_ms = float(np.mean([a.elapsed_time(b) for a, b in kev]))
+    ntt_fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in kev]))
+    rowsel_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in kev]))
+    ntt_inv_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in kev]))
     if world > 1:
         t = torch.tensor([ms_total], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -341,6 +468,18 @@ def run_ours(args, cfg):
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / ke
 
+    # read-only HBM probe over the same buffer (a library reduction, for context)
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        db.sum(dtype=torch.int64)
+        p0.record(stream)
+        for _ in range(3):
+            db.sum(dtype=torch.int64)
+        p1.record(stream)
+    torch.cuda.synchronize()
+    read_probe_gbs = 3 * db.numel() * 4 / (p0.elapsed_time(p1) * 1e-3) / 1e9
+
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     algo_bytes = logical_db + q_bytes + o_bytes       # the RowSel kernel's algorithmic bytes per launch
@@ -350,7 +489,7 @@ def run_ours(args, cfg):
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            gbs, threads, desc, secs, _ = oracle_rowsel_sample(cfg, args.cpu_seconds)
+            gbs, threads, desc, secs = oracle_rowsel_sample(cfg, args.cpu_seconds)
             cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
                    "seconds": round(secs, 2)}
         value = world * logical_db * args.steps / (ms_total * 1e-3) / 1e9
@@ -364,11 +503,13 @@ def run_ours(args, cfg):
                        "l2": "inputs larger than L2 (DB %.1f GiB >> 129 MB L2), no flush" % (logical_db / GIB),
                        "parallelism": "replicas x%d" % world},
             "queries_per_s": world * B * args.steps / (ms_total * 1e-3),
-            "kernel_ms": {"rowsel": rowsel_ms},
+            "kernel_ms": {"ntt_fwd": ntt_fwd_ms, "rowsel": rowsel_ms, "ntt_inv": ntt_inv_ms},
+            "kernels": kernel_rooflines(coeff, q_bytes, o_bytes, ntt_fwd_ms, ntt_inv_ms, hbm_peak),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": profile_traffic("rowsel_kernel_rowsel_64g"),
                          "kernel": "rowsel_kernel", "peak_source": "%s hbm_gbs (copy)" % peak_kind,
-                         "algorithmic_bytes_per_launch": algo_bytes},
+                         "algorithmic_bytes_per_launch": algo_bytes,
+                         "frac_of_read_probe": achieved / read_probe_gbs, "read_probe_gbs": read_probe_gbs},
             "clocks": clk,
             "e2e": None if e2e_ms is None else {
                 "value": logical_db / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": q_bytes,
@@ -389,6 +530,8 @@ def main():
     cfg = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, cfg)
+    elif cfg.get("kind") == "scalar":
+        run_scalar(args, cfg)
     else:
         run_ours(args, cfg)
 
