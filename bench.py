@@ -468,18 +468,6 @@ def run_ours(args, cfg):
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / ke
 
-    # read-only HBM probe over the same buffer (a library reduction, for context)
-    p0 = torch.cuda.Event(enable_timing=True)
-    p1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        db.sum(dtype=torch.int64)
-        p0.record(stream)
-        for _ in range(3):
-            db.sum(dtype=torch.int64)
-        p1.record(stream)
-    torch.cuda.synchronize()
-    read_probe_gbs = 3 * db.numel() * 4 / (p0.elapsed_time(p1) * 1e-3) / 1e9
-
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     algo_bytes = logical_db + q_bytes + o_bytes       # the RowSel kernel's algorithmic bytes per launch
@@ -508,8 +496,7 @@ def run_ours(args, cfg):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": profile_traffic("rowsel_kernel_rowsel_64g"),
                          "kernel": "rowsel_kernel", "peak_source": "%s hbm_gbs (copy)" % peak_kind,
-                         "algorithmic_bytes_per_launch": algo_bytes,
-                         "frac_of_read_probe": achieved / read_probe_gbs, "read_probe_gbs": read_probe_gbs},
+                         "algorithmic_bytes_per_launch": algo_bytes},
             "clocks": clk,
             "e2e": None if e2e_ms is None else {
                 "value": logical_db / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": q_bytes,

@@ -10,27 +10,30 @@
 namespace {
 
 constexpr int kNttThreads = 512;
+constexpr uint32_t kMaxRowsPerCta = 4096 / 16;  // rows per CTA for the smallest ring (N = 16)
 
 template <bool FWD>
 __global__ void __launch_bounds__(kNttThreads) ntt_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                           uint64_t rows, uint32_t rpc,
                                                           const __grid_constant__ RnsParams P) {
     extern __shared__ __align__(16) uint32_t sm[];
-    const uint32_t N = P.N, L = P.L;
+    __shared__ uint8_t row_prime[kMaxRowsPerCta];
+    const uint32_t N = P.N, L = P.L, logN = P.logN;
     const uint64_t row0 = (uint64_t)blockIdx.x * rpc;
     const uint32_t nrows = (uint32_t)((rows - row0) < rpc ? (rows - row0) : rpc);
     const uint32_t nwords = nrows * N;  // multiple of 16
     const uint4 *src = reinterpret_cast<const uint4 *>(in + row0 * N);
     uint4 *s4 = reinterpret_cast<uint4 *>(sm);
     for (uint32_t i = threadIdx.x; i < nwords / 4; i += blockDim.x) s4[i] = src[i];
+    if (threadIdx.x < nrows) row_prime[threadIdx.x] = (uint8_t)((row0 + threadIdx.x) % L);
     __syncthreads();
 
-    auto prime_of = [&](uint32_t r) -> uint32_t { return (uint32_t)((row0 + r) % L); };
+    auto prime_of = [&](uint32_t r) -> uint32_t { return row_prime[r]; };
     ntt_rows_smem<FWD>(sm, nrows, P, prime_of);
 
     uint4 *dst = reinterpret_cast<uint4 *>(out + row0 * N);
     for (uint32_t i = threadIdx.x; i < nwords / 4; i += blockDim.x) {
-        const uint32_t l = prime_of((i * 4) / N);
+        const uint32_t l = row_prime[(i * 4) >> logN];
         const uint32_t q = P.q[l];
         uint4 v = s4[i];
         if (FWD) {

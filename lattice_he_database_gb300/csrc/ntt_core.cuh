@@ -106,13 +106,12 @@ __device__ void ntt_rows_smem(uint32_t *sm, uint32_t nrows, const RnsParams &P, 
     uint32_t done = 0;  // stages completed
     while (done < logN) {
         const uint32_t R = (logN - done) >= 3 ? 3 : (logN - done);
-        const uint32_t G = 1u << R;
-        const uint32_t groups_per_row = N >> R;
+        const uint32_t lg = logN - R;  // log2(groups per row)
         // forward: stages s0 = done .. done+R-1; inverse: s_hi = logN-1-done .. down
         const uint32_t log_tlow = FWD ? (logN - done - R) : done;
         const uint32_t tlow = 1u << log_tlow;
-        for (uint32_t v = tid; v < nrows * groups_per_row; v += nthr) {
-            const uint32_t r = v / groups_per_row, vv = v - r * groups_per_row;
+        for (uint32_t v = tid; v < (nrows << lg); v += nthr) {
+            const uint32_t r = v >> lg, vv = v & ((1u << lg) - 1);
             const uint32_t l = prime_of(r);
             const uint32_t q = P.q[l];
             const uint32_t *W = P.tw + (size_t)l * 4 * N + (FWD ? TW_FWD : TW_INV) * N;
@@ -131,7 +130,6 @@ __device__ void ntt_rows_smem(uint32_t *sm, uint32_t nrows, const RnsParams &P, 
                 else inv_round_group<1>(row, g, tlow, s_hi, high, W, Wp, q);
             }
         }
-        (void)G;
         __syncthreads();
         done += R;
     }
