@@ -397,7 +397,7 @@ def run_ours(args, cfg):
             pir.pir_ntt_fwd(ctx, srv.q_coef, srv.q_ntt, B * D0 * 2, stream)
         if ev is not None:
             ev[1].record(stream)
-        pir.pir_rowsel(ctx, db, D0, D1, srv.q_ntt if coeff else srv.q_coef, B, srv.o_ntt, stream)
+        pir.pir_rowsel(ctx, db, D0, D1, srv.q_ntt if coeff else srv.q_coef, B, srv.o_ntt, srv.ws, stream)
         if ev is not None:
             ev[2].record(stream)
         if coeff:

@@ -146,6 +146,14 @@ int pir_db_encode(pir_ctx *ctx, const uint32_t *raw, uint32_t k0, uint32_t kcnt,
                   uint32_t D0, uint32_t D1, uint32_t *db, void *stream);
 
 /*
+ * pir_rowsel_workspace_bytes — device workspace pir_rowsel needs for D0 DB
+ * rows and B queries: one pass's query in point-major order,
+ * L*N * roundup(D0*Mp, 4) words, Mp = the pass's polynomial count (2B for
+ * one query, padded to a power of two, at most 32).  0 for invalid sizes.
+ */
+uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t B);
+
+/*
  * pir_rowsel — the RowSel scan (GPIR section 2):
  *   out[b][n][c][l][j] = sum_{k<D0} query[b][k][c][l][j] * DB(k,n)[l][j]  mod q_l
  * i.e. M_out[p, m=2b+c, n] = sum_k M_in0[p,m,k] * M_in1[p,k,n] with p = l*N+j:
@@ -154,14 +162,19 @@ int pir_db_encode(pir_ctx *ctx, const uint32_t *raw, uint32_t k0, uint32_t kcnt,
  *   db    : device, encoded by pir_db_encode for the same ctx, D0, D1.
  *   query : device, [B][D0][2][L][N] uint32 residues (NTT form).
  *   out   : device, [B][D1][2][L][N] uint32 (NTT form, canonical residues).
+ *   workspace : device, >= pir_rowsel_workspace_bytes(ctx, D0, B) bytes,
+ *               16-byte aligned; holds the query transposed to point-major
+ *               order (GPIR's NTT-to-GEMM layout change); contents undefined
+ *               after the call.
  * The DB is read from HBM once per pass; a pass covers as many queries as
- * fit the on-chip query buffer (all B for B*D0 <= 8192), larger batches take
- * ceil(B / per-pass) passes.
- * Errors: PIR_ERR_ARG (zero sizes, NULL/unaligned, overflow), PIR_ERR_CUDA,
- * PIR_ERR_UNSUPPORTED (D0 > 16384).
+ * fit the on-chip query buffer (16 queries for D0 <= 896, fewer for larger
+ * D0); larger batches take ceil(B / per-pass) passes.
+ * Errors: PIR_ERR_ARG (zero sizes, NULL/unaligned, workspace too small),
+ * PIR_ERR_CUDA, PIR_ERR_UNSUPPORTED (D0 > 14336).
  */
 int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1,
-               const uint32_t *query, uint32_t B, uint32_t *out, void *stream);
+               const uint32_t *query, uint32_t B, uint32_t *out,
+               void *workspace, uint64_t workspace_bytes, void *stream);
 
 /*
  * pir_scalar_workspace_bytes — device workspace pir_scalar_scan needs for a

@@ -12,15 +12,18 @@
 //    contiguous D0 x W_s block, W_s <= 128 words.  A unit of work is one such
 //    block; units are split into equal contiguous ranges, one per CTA of a
 //    persistent grid, so each CTA streams its own region of HBM exactly once.
-//  * A producer warp moves the block through a 4-stage shared-memory ring
-//    with 1-D bulk async copies (cp.async.bulk, L2 evict-first) of 32 rows
-//    each, signalling mbarriers; 8 consumer warps compute from shared memory.
-//  * The query slice M_in0[p, :, :] (2B x D0 words) is gathered into shared
-//    memory when a CTA moves to a new point p.
+//  * A producer warp moves the block through a 3-stage shared-memory ring
+//    with 1-D bulk async copies (cp.async.bulk, L2 evict-first) of 64 rows
+//    (32 KiB) each, signalling mbarriers; 8 consumer warps compute from
+//    shared memory.
+//  * The query is first transposed (GPIR's NTT-to-GEMM layout change) into
+//    a workspace qT[p][k][m], so that the slice M_in0[p, :, :] of a point
+//    is one contiguous block; the producer bulk-copies it into shared
+//    memory ahead of the point's DB chunks (double-buffered when it fits).
 //  * Thread tile: 4 consecutive columns x MT ciphertext polynomials; warps
 //    split the polynomials (msplit) and the rows of each chunk (ksplit).
 //    Products of residues < 2^29 are accumulated with 32x32->64-bit
-//    multiply-adds; every <= 48 products the accumulator is folded
+//    multiply-adds; at least every 48 products the accumulator is folded
 //    (lo + hi * (2^32 mod q)); one Barrett reduction per output at the end,
 //    plus a sum of the ksplit partial residues.
 //  * Device waits are bounded; on a timeout the kernel raises
@@ -32,21 +35,23 @@
 
 namespace {
 
-constexpr int KC = 32;                         // DB rows per ring stage
-constexpr int NST = 4;                         // ring stages
+constexpr int KC = 64;                         // DB rows per ring stage
+constexpr int NST = 3;                         // ring stages
 constexpr int NWC = 8;                         // consumer warps
 constexpr int NTHREADS = (NWC + 1) * 32;       // + one producer warp
-constexpr uint32_t STAGE_WORDS = KC * PIR_SLAB;  // 16 KiB
-constexpr uint32_t IN0_MAX_BYTES = 128 * 1024;
+constexpr uint32_t STAGE_WORDS = KC * PIR_SLAB;  // 32 KiB
+constexpr uint32_t IN0_MAX_BYTES = 112 * 1024;  // one query slice; the ring takes 96 KiB
 constexpr uint32_t FOLD_LIMIT = 48;            // products between folds
+static_assert(KC / 2 <= 32, "a chunk must add at most 32 products per accumulator (ksplit >= 2)");
 
 struct RowselArgs {
     const uint32_t *db;
-    const uint32_t *query;
+    const uint32_t *qT;      // transposed query [P][PS] (PS >= D0*Mp, multiple of 4)
     uint32_t *out;
     uint32_t *status;
     uint32_t N, L, D0, D1, D1p, S, Wlast;
     uint32_t B, b0, Mv, Mp, msplit, ksplit, nchunks;
+    uint32_t PS, nb;         // query slice stride (words) and number of slice buffers (1 or 2)
     uint64_t P, units;
     uint32_t q[PIR_MAX_RNS], r32[PIR_MAX_RNS];
     uint64_t mu[PIR_MAX_RNS];
@@ -56,24 +61,60 @@ __device__ __forceinline__ uint32_t slab_width(const RowselArgs &A, uint32_t s) 
     return s == A.S - 1 ? A.Wlast : PIR_SLAB;
 }
 
+// Transpose of the query into qT[p][k][m] (m = 2b + c relative to the pass's
+// first query b0; polynomials m >= Mv of the padded count are zero).  One
+// CTA moves a tile of 32 points x 32 (k, m) rows through shared memory so
+// that both the reads (along p) and the writes (along (k, m)) are coalesced.
+__global__ void __launch_bounds__(256) transpose_query_kernel(const uint32_t *__restrict__ query,
+                                                              uint32_t *__restrict__ qT, uint64_t P,
+                                                              uint32_t D0, uint32_t Mp, uint32_t Mv,
+                                                              uint32_t b0, uint32_t PS) {
+    __shared__ uint32_t tile[32][33];
+    const uint64_t p0 = (uint64_t)blockIdx.x * 32;
+    const uint32_t r0 = blockIdx.y * 32;
+    const uint32_t rows = D0 * Mp;
+    const uint32_t tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    for (uint32_t i = ty; i < 32; i += 8) {
+        const uint32_t r = r0 + i;
+        const uint64_t p = p0 + tx;
+        uint32_t v = 0;
+        if (r < rows && p < P) {
+            const uint32_t k = r / Mp, m = r - k * Mp;
+            if (m < Mv) v = query[(((uint64_t)(b0 + (m >> 1)) * D0 + k) * 2 + (m & 1)) * P + p];
+        }
+        tile[i][tx] = v;
+    }
+    __syncthreads();
+    for (uint32_t j = ty; j < 32; j += 8) {
+        const uint64_t p = p0 + j;
+        const uint32_t r = r0 + tx;
+        if (p < P && r < PS) qT[p * PS + r] = r < rows ? tile[tx][j] : 0u;
+    }
+}
+
 template <int MT>
 __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant__ RowselArgs A) {
     extern __shared__ __align__(128) uint32_t smw[];
     uint32_t *ring = smw;                                    // NST * STAGE_WORDS
-    uint32_t *in0s = ring + NST * STAGE_WORDS;               // D0 * Mp   (k-major)
-    uint32_t *red = in0s + (size_t)A.D0 * A.Mp;              // ksplit * Mp * 128
+    uint32_t *in0s = ring + NST * STAGE_WORDS;               // nb * PS   (k-major query slices)
+    uint32_t *red = in0s + (size_t)A.nb * A.PS;              // ksplit * Mp * 128
     uint64_t *bars = reinterpret_cast<uint64_t *>(red + (A.ksplit > 1 ? A.ksplit * A.Mp * PIR_SLAB : 0));
-    uint64_t *full = bars, *empty = bars + NST;
+    uint64_t *full = bars, *empty = bars + NST, *qfull = bars + 2 * NST, *qempty = qfull + 2;
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t u0 = (uint64_t)blockIdx.x * A.units / gridDim.x;
     const uint64_t u1 = (uint64_t)(blockIdx.x + 1) * A.units / gridDim.x;
+    const uint32_t qbytes = A.PS * 4;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) {
             mbar_init(full + i, 1);
             mbar_init(empty + i, NWC);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(qfull + i, 1);
+            mbar_init(qempty + i, NWC);
         }
         abort_flag = 0;
         fence_mbar_init();
@@ -84,11 +125,22 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
     if (warp == NWC) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            uint32_t stage = 0, phase = 0;
-            uint64_t issued = 0;
+            uint32_t stage = 0, phase = 0, pc = 0;
+            uint64_t issued = 0, cur_p = ~0ull;
             for (uint64_t u = u0; u < u1 && !abort_flag; ++u) {
                 const uint64_t p = u / A.S;
                 const uint32_t s = (uint32_t)(u - p * A.S);
+                if (p != cur_p) {  // the point's query slice goes first (consumers need it first)
+                    const uint32_t slot = pc % A.nb, use = (pc / A.nb) & 1;
+                    if (!mbar_wait(qempty + slot, use ^ 1, A.status)) {
+                        abort_flag = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(qfull + slot, qbytes);
+                    bulk_g2s(in0s + (size_t)slot * A.PS, A.qT + p * A.PS, qbytes, qfull + slot, pol);
+                    ++pc;
+                    cur_p = p;
+                }
                 const uint32_t Ws = slab_width(A, s);
                 const uint32_t *src = A.db + p * A.D0 * A.D1p + (uint64_t)s * A.D0 * PIR_SLAB;
                 for (uint32_t c = 0; c < A.nchunks; ++c) {
@@ -105,11 +157,16 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
                 }
             }
             // The copies still in flight target this CTA's shared memory:
-            // wait (bounded) for the last min(issued, NST) of them to land.
+            // wait (bounded) for the last ring copies and query slices to land.
             const uint32_t pend = issued < (uint64_t)NST ? (uint32_t)issued : (uint32_t)NST;
             for (uint32_t i = 0; i < pend; ++i) {
                 if (stage == 0) { stage = NST - 1; phase ^= 1; } else { --stage; }
                 mbar_wait(full + stage, phase, A.status);
+            }
+            const uint32_t qpend = pc < A.nb ? pc : A.nb;
+            for (uint32_t i = 0; i < qpend; ++i) {
+                const uint32_t j = pc - 1 - i;
+                mbar_wait(qfull + j % A.nb, (j / A.nb) & 1, A.status);
             }
         }
         return;
@@ -118,7 +175,7 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
     // ------------------------------------------------------------ consumers
     const uint32_t ctid = threadIdx.x;  // 0 .. NWC*32-1
     const uint32_t ms = warp % A.msplit, ks = warp / A.msplit;
-    uint32_t stage = 0, phase = 0;
+    uint32_t stage = 0, phase = 0, pc = 0, qslot = 0;
     uint64_t cur_p = ~0ull;
 
     for (uint64_t u = u0; u < u1; ++u) {
@@ -129,19 +186,14 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
         const uint32_t q = A.q[l], r32 = A.r32[l];
         const uint64_t mu = A.mu[l];
 
-        if (p != cur_p) {  // gather M_in0[p, m, k] = query[b][k][c][p], m = 2b + c
-            named_barrier(1, NWC * 32);
-            const uint32_t tot = A.D0 * A.Mp;
-            for (uint32_t idx = ctid; idx < tot; idx += NWC * 32) {
-                const uint32_t k = idx / A.Mp, m = idx - k * A.Mp;
-                uint32_t v = 0;
-                if (m < A.Mv) {
-                    const uint64_t b = A.b0 + (m >> 1);
-                    v = A.query[((b * A.D0 + k) * 2 + (m & 1)) * A.P + p];
-                }
-                in0s[idx] = v;
+        if (p != cur_p) {  // release the previous point's slice, wait for this one
+            if (cur_p != ~0ull) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qempty + qslot);
             }
-            named_barrier(1, NWC * 32);
+            qslot = pc % A.nb;
+            if (!abort_flag && !mbar_wait(qfull + qslot, (pc / A.nb) & 1, A.status)) abort_flag = 1;
+            ++pc;
             cur_p = p;
         }
 
@@ -152,7 +204,7 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
             for (int j = 0; j < 4; ++j) acc[i][j] = 0;
         uint32_t cnt = 0;
         const bool active = 4u * lane < Ws;
-        const uint32_t *a_base = in0s + ms * MT;
+        const uint32_t *a_base = in0s + (size_t)qslot * A.PS + ms * MT;
 
         for (uint32_t c = 0; c < A.nchunks; ++c) {
             const uint32_t rows = min((uint32_t)KC, A.D0 - c * KC);
@@ -161,6 +213,8 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
                 abort_flag = 1;
                 ok = false;
             }
+            // KC / ksplit <= 32 (host guarantees ksplit >= 2), so a fold is
+            // never more than FOLD_LIMIT (48) products away
             const uint32_t per = rows > ks ? (rows - ks + A.ksplit - 1) / A.ksplit : 0;
             if (cnt + per > FOLD_LIMIT) {
 #pragma unroll
@@ -173,7 +227,7 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
             if (ok && active) {
                 const uint32_t *st = ring + stage * STAGE_WORDS + 4 * lane;
                 const uint32_t *ak = a_base + (size_t)c * KC * A.Mp;
-#pragma unroll(MT == 2 ? 4 : 2)
+#pragma unroll(MT == 8 ? 1 : (MT == 2 ? 4 : 2))
                 for (uint32_t r = ks; r < rows; r += A.ksplit) {
                     const uint4 d = *reinterpret_cast<const uint4 *>(st + r * Ws);
                     uint32_t a[MT];
@@ -246,13 +300,23 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
     }
 }
 
+size_t rowsel_smem(const RowselArgs &A, uint32_t nb) {
+    return (size_t)NST * STAGE_WORDS * 4 + (size_t)nb * A.PS * 4 +
+           (A.ksplit > 1 ? (size_t)A.ksplit * A.Mp * PIR_SLAB * 4 : 0) + (2 * NST + 4) * sizeof(uint64_t);
+}
+
 template <int MT>
 int launch_pass(pir_ctx *ctx, RowselArgs &A, cudaStream_t st) {
-    const size_t smem = (size_t)NST * STAGE_WORDS * 4 + (size_t)A.D0 * A.Mp * 4 +
-                        (A.ksplit > 1 ? (size_t)A.ksplit * A.Mp * PIR_SLAB * 4 : 0) + 2 * NST * sizeof(uint64_t);
+    // Double-buffer the query slices when that still leaves room for two
+    // CTAs per SM, or when one CTA per SM is the outcome either way.
+    constexpr size_t kTwoPerSm = 113 * 1024, kMax = 220 * 1024;  // 228 KiB per SM, 1 KiB reserved per CTA
+    const size_t s1 = rowsel_smem(A, 1), s2 = rowsel_smem(A, 2);
+    A.nb = (s2 <= kTwoPerSm || (s1 > kTwoPerSm && s2 <= kMax)) ? 2 : 1;
+    const size_t smem = rowsel_smem(A, A.nb);
+    if (smem > kMax) return PIR_ERR_UNSUPPORTED;
     static bool attr_set[64] = {};
     if (ctx->device < 64 && !attr_set[ctx->device]) {
-        if (cudaFuncSetAttribute(rowsel_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024) !=
+        if (cudaFuncSetAttribute(rowsel_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMax) !=
             cudaSuccess)
             return PIR_ERR_CUDA;
         attr_set[ctx->device] = true;
@@ -267,20 +331,45 @@ int launch_pass(pir_ctx *ctx, RowselArgs &A, cudaStream_t st) {
     return launch_status(cudaGetLastError());
 }
 
+// Polynomials per pass: the padded count Mp must be MT * msplit with
+// msplit | NWC, and one query slice D0 * Mp words must fit on chip.
+uint32_t mp_capacity(uint32_t D0) {
+    uint32_t cap = 32;
+    while (cap > 2 && (uint64_t)D0 * cap * 4 > IN0_MAX_BYTES) cap >>= 1;
+    return (uint64_t)D0 * cap * 4 > IN0_MAX_BYTES ? 0 : cap;
+}
+
+uint32_t padded_mp(uint32_t Mv) {
+    if (Mv <= 2) return 2;
+    uint32_t mp = 4;
+    while (mp < Mv) mp <<= 1;
+    return mp;
+}
+
 }  // namespace
 
+extern "C" uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t B) {
+    if (!ctx || D0 == 0 || B == 0 || D0 > 14336) return 0;
+    const uint32_t cap = mp_capacity(D0);
+    if (!cap) return 0;
+    const uint32_t mp = padded_mp(2 * (B < cap / 2 ? B : cap / 2));
+    const uint64_t ps = ((uint64_t)D0 * mp + 3) / 4 * 4;
+    return (uint64_t)ctx->L * ctx->N * ps * 4;
+}
+
 extern "C" int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *query,
-                          uint32_t B, uint32_t *out, void *stream) {
-    if (!ctx || !db || !query || !out) return PIR_ERR_ARG;
-    if (!aligned16(db) || !aligned16(query) || !aligned16(out)) return PIR_ERR_ARG;
+                          uint32_t B, uint32_t *out, void *workspace, uint64_t workspace_bytes, void *stream) {
+    if (!ctx || !db || !query || !out || !workspace) return PIR_ERR_ARG;
+    if (!aligned16(db) || !aligned16(query) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
     if (D0 == 0 || D1 == 0 || B == 0) return PIR_ERR_ARG;
-    if (D0 > 16384) return PIR_ERR_UNSUPPORTED;
+    if (D0 > 14336) return PIR_ERR_UNSUPPORTED;
+    if (workspace_bytes < pir_rowsel_workspace_bytes(ctx, D0, B)) return PIR_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
 
     RowselArgs A;
     memset(&A, 0, sizeof(A));
     A.db = db;
-    A.query = query;
+    A.qT = reinterpret_cast<const uint32_t *>(workspace);
     A.out = out;
     A.status = ctx->d_status;
     A.N = ctx->N;
@@ -299,30 +388,36 @@ extern "C" int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_
         A.r32[l] = ctx->r32[l];
         A.mu[l] = ctx->mu[l];
     }
-    // Polynomials per pass: the padded count Mp must be MT * msplit with
-    // msplit | NWC, and the query slice D0 * Mp words must fit on chip.
-    uint32_t mp_cap = 32;
-    while (mp_cap > 2 && (uint64_t)D0 * mp_cap * 4 > IN0_MAX_BYTES) mp_cap >>= 1;
-    if ((uint64_t)D0 * mp_cap * 4 > IN0_MAX_BYTES) return PIR_ERR_UNSUPPORTED;
-    const uint32_t b_per_pass = mp_cap / 2;
+    const uint32_t cap = mp_capacity(D0);
+    if (!cap) return PIR_ERR_UNSUPPORTED;
+    const uint32_t b_per_pass = cap / 2;
     cudaStream_t st = (cudaStream_t)stream;
     for (uint32_t b0 = 0; b0 < B; b0 += b_per_pass) {
         const uint32_t nb = min(b_per_pass, B - b0);
         A.b0 = b0;
         A.Mv = 2 * nb;
+        A.Mp = padded_mp(A.Mv);
+        A.PS = (D0 * A.Mp + 3) / 4 * 4;
+        // the pass's query slices, point-major
+        const dim3 tgrid((unsigned)((A.P + 31) / 32), (A.PS + 31) / 32);
+        uint32_t *qT = reinterpret_cast<uint32_t *>(workspace);
+        transpose_query_kernel<<<tgrid, 256, 0, st>>>(query, qT, A.P, D0, A.Mp, A.Mv, b0, A.PS);
+        if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
+        // thread tile MT polynomials x 4 columns; warps split the padded
+        // polynomials (msplit) and the rows of a chunk (ksplit >= 2)
         int rc;
-        if (A.Mv <= 2) {
-            A.Mp = 2;
+        if (A.Mp == 2) {
             A.msplit = 1;
             A.ksplit = NWC;
             rc = launch_pass<2>(ctx, A, st);
-        } else {
-            uint32_t mp = 4;
-            while (mp < A.Mv) mp <<= 1;
-            A.Mp = mp;
-            A.msplit = mp / 4;
-            A.ksplit = NWC / A.msplit;
+        } else if (A.Mp == 4) {
+            A.msplit = 1;
+            A.ksplit = NWC;
             rc = launch_pass<4>(ctx, A, st);
+        } else {
+            A.msplit = A.Mp / 8;
+            A.ksplit = NWC / A.msplit;
+            rc = launch_pass<8>(ctx, A, st);
         }
         if (rc) return rc;
     }

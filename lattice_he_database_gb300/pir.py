@@ -62,8 +62,11 @@ def lib() -> ctypes.CDLL:
         L.pir_db_encode.restype = ctypes.c_int
         L.pir_db_encode.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
                                     _vp, _vp]
+        L.pir_rowsel_workspace_bytes.restype = ctypes.c_uint64
+        L.pir_rowsel_workspace_bytes.argtypes = [_vp, ctypes.c_uint32, ctypes.c_uint32]
         L.pir_rowsel.restype = ctypes.c_int
-        L.pir_rowsel.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, ctypes.c_uint32, _vp, _vp]
+        L.pir_rowsel.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, ctypes.c_uint32, _vp, _vp,
+                                 ctypes.c_uint64, _vp]
         L.pir_scalar_workspace_bytes.restype = ctypes.c_uint64
         L.pir_scalar_workspace_bytes.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
         L.pir_scalar_scan.restype = ctypes.c_int
@@ -191,10 +194,21 @@ def pir_db_encode(ctx: Ctx, raw: torch.Tensor, k0: int, kcnt: int, D0: int, D1: 
                                _stream(stream)), "pir_db_encode")
 
 
+def pir_rowsel_workspace_bytes(ctx: Ctx, D0: int, B: int) -> int:
+    return int(lib().pir_rowsel_workspace_bytes(ctx, D0, B))
+
+
 def pir_rowsel(ctx: Ctx, db: torch.Tensor, D0: int, D1: int, query: torch.Tensor, B: int, out: torch.Tensor,
-               stream=None):
+               workspace: torch.Tensor, stream=None):
+    ws = _dev_ptr(workspace, workspace.element_size(), "workspace")
     _check(lib().pir_rowsel(ctx, _dev_ptr(db, 4, "db"), D0, D1, _dev_ptr(query, 4, "query"), B,
-                            _dev_ptr(out, 4, "out"), _stream(stream)), "pir_rowsel")
+                            _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(),
+                            _stream(stream)), "pir_rowsel")
+
+
+def rowsel_workspace(ctx: Ctx, D0: int, B: int, device="cuda") -> torch.Tensor:
+    """A device workspace sized for pir_rowsel(D0, B)."""
+    return torch.empty(pir_rowsel_workspace_bytes(ctx, D0, B), dtype=torch.uint8, device=device)
 
 
 # ---------------------------------------------------------------- scalar scan
@@ -258,6 +272,7 @@ class RowselServer:
         self.q_ntt = empty_u32(self.q_words, dev)
         self.o_ntt = empty_u32(self.o_words, dev)
         self.o_coef = empty_u32(self.o_words, dev)
+        self.ws = rowsel_workspace(ctx, D0, B, dev)
         self.stream = stream or torch.cuda.current_stream(dev)
         self.launches_per_answer = 3
 
@@ -266,7 +281,7 @@ class RowselServer:
         q = self.q_coef if q_coef is None else q_coef
         c = self.ctx
         pir_ntt_fwd(c, q, self.q_ntt, self.B * self.D0 * 2, self.stream)
-        pir_rowsel(c, self.db, self.D0, self.D1, self.q_ntt, self.B, self.o_ntt, self.stream)
+        pir_rowsel(c, self.db, self.D0, self.D1, self.q_ntt, self.B, self.o_ntt, self.ws, self.stream)
         pir_ntt_inv(c, self.o_ntt, self.o_coef, self.B * self.D1 * 2, self.stream)
         return self.o_coef
 
