@@ -22,7 +22,7 @@
 // Kernel structure (one CTA per SM, persistent over 128-row DB tiles):
 //   warp 0      TMA producer: the 128 x 64-byte DB tile (tensor map) and the
 //               matching 256 x 64 fp16 digit tile (1-D bulk copy of a block
-//               pre-swizzled by the prep kernel) into a 3-stage ring;
+//               pre-swizzled by the prep kernel) into a 4-stage ring;
 //   warp 1      TMEM allocator and the single MMA-issuing thread:
 //               4 x tcgen05.mma (M=128, N=256, K=16) per stage into one of
 //               two 256-column fp32 accumulators (double buffered so that a
@@ -43,7 +43,7 @@
 
 namespace {
 
-constexpr int SC_NS = 3;                      // pipeline stages
+constexpr int SC_NS = 4;                      // pipeline stages (4 x 56 KiB)
 constexpr int SC_KB = 64;                     // DB bytes (K elements) per stage
 constexpr int SC_TM = 128;                    // DB rows per tile (MMA M)
 constexpr int SC_BQ = 64;                     // queries per pass (digit planes hold 4 x 64 rows)
