@@ -348,6 +348,11 @@ uint32_t padded_mp(uint32_t Mv) {
 
 }  // namespace
 
+// Tensor-core path for large batches (rowsel_tc.cu).
+bool rowsel_tc_eligible(uint32_t D0, uint32_t Mv);
+int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *qT, uint32_t PS,
+                   uint32_t b0, uint32_t Mv, uint32_t *out, cudaStream_t st);
+
 extern "C" uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t B) {
     if (!ctx || D0 == 0 || B == 0 || D0 > 14336) return 0;
     const uint32_t cap = mp_capacity(D0);
@@ -403,9 +408,14 @@ extern "C" int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_
         uint32_t *qT = reinterpret_cast<uint32_t *>(workspace);
         transpose_query_kernel<<<tgrid, 256, 0, st>>>(query, qT, A.P, D0, A.Mp, A.Mv, b0, A.PS);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
+        int rc;
+        if (rowsel_tc_eligible(D0, A.Mv)) {  // 17..32 polynomials: exact fp16 tensor-core GEMMs
+            rc = rowsel_tc_pass(ctx, db, D0, D1, qT, A.PS, b0, A.Mv, out, st);
+            if (rc) return rc;
+            continue;
+        }
         // thread tile MT polynomials x 4 columns; warps split the padded
         // polynomials (msplit) and the rows of a chunk (ksplit >= 2)
-        int rc;
         if (A.Mp == 2) {
             A.msplit = 1;
             A.ksplit = NWC;

@@ -1,0 +1,501 @@
+// rowsel_tc.cu — RowSel on the tensor cores for query batches (2B > 16 polynomials).
+//
+// GPIR section 2: RowSel is L*N point-wise GEMMs
+//     M_out[p,m,n] = sum_k M_in0[p,m,k] * M_in1[p,k,n]  mod q_l.
+// With a batch of queries every DB word meets 2B query words, and the
+// 32x32->64-bit multiply-adds of the CUDA-core scan become the bound.  This
+// path computes the same sums exactly on the fp16 tensor cores (tcgen05
+// kind::f16, fp32 accumulation in TMEM), using the byte-split idea of VIPIR
+// section 4.1 on both operands:
+//   * query residues a < 2^29 as balanced base-256 digits a_i in [-128, 128]
+//     (a = sum_i 256^i a_i exactly; a_3 <= 32),
+//   * DB residues b < 2^29 as their plain bytes b_j in [0, 255],
+// so a*b = sum_{i,j} 256^(i+j) a_i b_j.  Every digit product is an integer of
+// magnitude <= 128*255, and D0 <= 512 of them sum below 2^24: exact in fp32.
+//
+// MMA tile (one per 32 DB columns of a point): M = 128 rows (i, m) = 4 query
+// digit planes x 32 polynomials, N = 128 columns (j, n) = 4 DB byte planes x
+// 32 columns, K = D0.  The A operand (query digits of the point) sits in
+// TMEM for all tiles of the point; the accumulator (128 columns, double
+// buffered) then holds S_ij[m][n].  The epilogue forms
+//     out[m][n] = sum_i 2^(8i) (sum_j 2^(8j) S_ij[m][n])  mod q
+// with one 64-bit Barrett reduction per (i, m, n) and a cross-plane sum.
+//
+// Warp roles (448 threads, one CTA per SM, persistent over a range of points):
+//   warps 0-3   query digits of the next point -> TMEM (tcgen05.st), warp w
+//               writes digit plane w into TMEM lanes 32w..32w+31;
+//   warps 4-7   epilogue: tcgen05.ld of a finished accumulator, reduction,
+//               cross-plane sum through shared memory, output stores;
+//   warps 8-11  converters: 64 x 32 DB words (TMA-staged) -> 4 byte planes
+//               of fp16 in the 128B-swizzled K-major layout of the B operand;
+//   warp 12     TMEM allocation and the TMA producer of DB word tiles;
+//   warp 13     MMA issue (one thread).
+// All mbarrier waits are bounded; TMEM is always released.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <cstring>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int TC_NS = 8;                       // pipeline stages
+constexpr int TC_KS = 64;                      // DB rows (K) per stage
+constexpr int TC_NT = 32;                      // DB columns per MMA tile
+constexpr uint32_t TC_RAW_BYTES = TC_KS * TC_NT * 4;   // 8 KiB of DB words
+constexpr uint32_t TC_B_BYTES = 128 * 128;             // 128 rows x 64 fp16
+constexpr int TC_THREADS = 14 * 32;
+constexpr uint32_t TC_TMEM_COLS = 512;
+constexpr uint32_t TC_ACC_COL = 256;           // accumulators at columns 256 and 384
+constexpr uint32_t TC_MAX_D0 = 512;            // exactness bound of one fp32 accumulation
+
+struct TcArgs {
+    const uint32_t *qT;     // point-major query, [P][PS], 32 polynomials per k
+    uint32_t *out;
+    uint32_t *status;
+    uint32_t N, D0, D1, S, Wlast, PS, Kp, b0, Mv;
+    uint64_t P;
+    uint32_t q[PIR_MAX_RNS];
+    uint64_t mu[PIR_MAX_RNS];
+    uint64_t bias[PIR_MAX_RNS];       // multiple of q >= 2^50 (makes signed sums positive)
+    uint32_t c[PIR_MAX_RNS][4];       // 2^(8i) mod q
+    uint32_t cs[PIR_MAX_RNS][4];      // Shoup companions of c
+};
+
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t j) {
+    return (row >> 3) * 1024u + (row & 7u) * 128u + ((j ^ (row & 7u)) << 4);
+}
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// kind::f16, A = B = F16, D = F32, K-major, N = 128, M = 128
+constexpr uint32_t TC_IDESC = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a_tmem), "l"(bdesc), "r"(TC_IDESC), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Balanced base-256 digit `plane` of a < 2^32, as the fp16 bit pattern.
+__device__ __forceinline__ uint32_t digit_half(uint32_t a, uint32_t plane) {
+    int d = 0;
+    int64_t y = a;
+    for (uint32_t i = 0; i <= plane; ++i) {
+        const int lo = (int)(y & 0xFF);
+        d = (i < 3) ? ((lo ^ 0x80) - 0x80) : (int)y;  // the top digit keeps the rest (<= 33 for a < 2^29)
+        y = (y - d) >> 8;
+    }
+    return (uint32_t)__half_as_ushort(__int2half_rn(d));
+}
+
+// Number of 32-column tiles of slab s.
+__device__ __forceinline__ uint32_t tiles_of(const TcArgs &A, uint32_t s) {
+    const uint32_t w = (s == A.S - 1) ? A.Wlast : PIR_SLAB;
+    return (w + TC_NT - 1) / TC_NT;
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    rowsel_tc_kernel(const __grid_constant__ CUtensorMap full_map, const __grid_constant__ CUtensorMap last_map,
+                     const __grid_constant__ TcArgs A) {
+    extern __shared__ uint8_t smraw[];
+    const uint32_t base_s = smem_u32(smraw);
+    uint8_t *sm = smraw + (((base_s + 1023u) & ~1023u) - base_s);
+    uint8_t *stB = sm;                                   // [NS][16 KiB] fp16 digit tiles
+    uint8_t *stR = stB + TC_NS * TC_B_BYTES;             // [NS][8 KiB] DB words
+    uint32_t *red = reinterpret_cast<uint32_t *>(stR + TC_NS * TC_RAW_BYTES);  // [4][32][32]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(red + 4 * 32 * 32);
+    uint64_t *rfull = bars, *bfull = bars + TC_NS, *empty = bars + 2 * TC_NS;
+    uint64_t *accf = bars + 3 * TC_NS, *acce = accf + 2, *afull = acce + 2, *aempty = afull + 1, *done = aempty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t p_begin = (uint64_t)blockIdx.x * A.P / gridDim.x;
+    const uint64_t p_end = (uint64_t)(blockIdx.x + 1) * A.P / gridDim.x;
+    const uint32_t nks = A.Kp / TC_KS;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TC_NS; ++s) {
+            mbar_init(rfull + s, 1);
+            mbar_init(bfull + s, 4);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf + b, 1);
+            mbar_init(acce + b, 4);
+        }
+        mbar_init(afull, 4);
+        mbar_init(aempty, 1);
+        mbar_init(done, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 12) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TC_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 12 && lane == 0) {
+        // ------------------------------------------------ TMA producer: DB word tiles
+        const uint64_t pol = policy_evict_first();
+        uint32_t it = 0;
+        for (uint64_t p = p_begin; p < p_end; ++p)
+            for (uint32_t s = 0; s < A.S; ++s) {
+                const uint32_t nt = tiles_of(A, s);
+                for (uint32_t t = 0; t < nt; ++t)
+                    for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
+                        const uint32_t st = it % TC_NS, ph = (it / TC_NS) & 1;
+                        if (abort_flag || !mbar_wait(empty + st, ph ^ 1, A.status)) {
+                            abort_flag = 1;
+                            continue;
+                        }
+                        mbar_arrive_expect_tx(rfull + st, TC_RAW_BYTES);
+                        if (s + 1 < A.S)
+                            tma_load_4d(stR + st * TC_RAW_BYTES, &full_map, (int)(t * TC_NT), (int)(ks * TC_KS),
+                                        (int)s, (int)p, rfull + st, pol);
+                        else
+                            tma_load_4d(stR + st * TC_RAW_BYTES, &last_map, (int)(t * TC_NT), (int)(ks * TC_KS), 0,
+                                        (int)p, rfull + st, pol);
+                    }
+            }
+        for (uint32_t i = 0; i < TC_NS && i < it; ++i) {  // copies in flight land first
+            const uint32_t j = it - 1 - i;
+            mbar_wait(rfull + j % TC_NS, (j / TC_NS) & 1, A.status);
+        }
+    } else if (warp == 13 && lane == 0) {
+        // ------------------------------------------------ MMA issue
+        uint32_t it = 0, g = 0, pc = 0;
+        for (uint64_t p = p_begin; p < p_end; ++p) {
+            bool first = true;
+            for (uint32_t s = 0; s < A.S; ++s) {
+                const uint32_t nt = tiles_of(A, s);
+                for (uint32_t t = 0; t < nt; ++t, ++g) {
+                    const uint32_t buf = g & 1, use = (g >> 1) & 1;
+                    if (!abort_flag && !mbar_wait(acce + buf, use ^ 1, A.status)) abort_flag = 1;
+                    if (first) {
+                        if (!abort_flag && !mbar_wait(afull, pc & 1, A.status)) abort_flag = 1;
+                        first = false;
+                    }
+                    fence_after();
+                    const uint32_t d = tmem + TC_ACC_COL + buf * 128;
+                    for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
+                        const uint32_t st = it % TC_NS, ph = (it / TC_NS) & 1;
+                        if (!abort_flag && !mbar_wait(bfull + st, ph, A.status)) abort_flag = 1;
+                        if (abort_flag) continue;
+                        fence_after();
+                        const uint32_t b0 = smem_u32(stB + st * TC_B_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA; A: 8 TMEM columns per 16 K
+                            mma_ts(d, tmem + ks * 32 + kk * 8, sdesc(b0 + 32 * kk), (ks | kk) ? 1u : 0u);
+                        commit(empty + st);
+                    }
+                    if (!abort_flag) commit(accf + buf);
+                }
+            }
+            commit(aempty);  // A (query digits) reusable once this point's MMAs finish
+            ++pc;
+        }
+        commit(done);
+        mbar_wait(done, 0, A.status);
+    } else if (warp < 4) {
+        // ------------------------------------------------ query digits -> TMEM (plane = warp)
+        const uint32_t plane = warp, m = lane;
+        uint32_t pc = 0;
+        for (uint64_t p = p_begin; p < p_end; ++p, ++pc) {
+            if (!abort_flag && !mbar_wait(aempty, (pc & 1) ^ 1, A.status)) abort_flag = 1;
+            fence_after();
+            if (!abort_flag) {
+                const uint32_t *src = A.qT + p * A.PS;
+                for (uint32_t kc = 0; kc < A.Kp / 64; ++kc) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const uint32_t k0 = kc * 64 + 2 * e;
+                        const uint32_t a0 = (k0 < A.D0 && m < A.Mv) ? __ldg(src + (uint64_t)k0 * 32 + m) : 0u;
+                        const uint32_t a1 =
+                            (k0 + 1 < A.D0 && m < A.Mv) ? __ldg(src + (uint64_t)(k0 + 1) * 32 + m) : 0u;
+                        v[e] = digit_half(a0, plane) | (digit_half(a1, plane) << 16);
+                    }
+                    tmem_st32(tmem + ((plane * 32u) << 16) + kc * 32, v);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull);
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------ epilogue
+        const uint32_t plane = warp & 3, m = lane;
+        const uint32_t etid = threadIdx.x - 128;  // 0..127
+        uint32_t g = 0;
+        for (uint64_t p = p_begin; p < p_end; ++p) {
+            const uint32_t l = (uint32_t)(p / A.N);
+            const uint32_t q = A.q[l];
+            const uint64_t mu = A.mu[l], bias = A.bias[l];
+            const uint32_t ci = A.c[l][plane], cis = A.cs[l][plane];
+            for (uint32_t s = 0; s < A.S; ++s) {
+                const uint32_t nt = tiles_of(A, s);
+                const uint32_t Ws = (s == A.S - 1) ? A.Wlast : PIR_SLAB;
+                for (uint32_t t = 0; t < nt; ++t, ++g) {
+                    const uint32_t buf = g & 1, use = (g >> 1) & 1;
+                    if (!abort_flag && !mbar_wait(accf + buf, use, A.status)) abort_flag = 1;
+                    fence_after();
+                    int64_t W[32];
+#pragma unroll
+                    for (int n = 0; n < 32; ++n) W[n] = 0;
+                    if (!abort_flag) {
+                        const uint32_t taddr = tmem + ((plane * 32u) << 16) + TC_ACC_COL + buf * 128;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t v[32];
+                            tmem_ld32(taddr + j * 32, v);
+                            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                            for (int n = 0; n < 32; ++n)
+                                W[n] += (int64_t)__float2int_rn(__uint_as_float(v[n])) << (8 * j);
+                        }
+                    }
+                    fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acce + buf);  // accumulator drained
+                    named_barrier(2, 128);                    // previous tile's readers of red are done
+#pragma unroll
+                    for (int n = 0; n < 32; ++n) {
+                        const uint32_t r = barrett64((uint64_t)(W[n] + (int64_t)bias), q, mu);
+                        uint32_t u = shoup_mul(r, ci, cis, q);
+                        red[(plane * 32 + m) * 32 + n] = u >= q ? u - q : u;
+                    }
+                    named_barrier(2, 128);
+                    for (uint32_t idx = etid; idx < 32 * 32; idx += 128) {
+                        const uint32_t mm = idx >> 5, nn = idx & 31;
+                        const uint32_t col = t * TC_NT + nn;
+                        if (mm >= A.Mv || col >= Ws) continue;
+                        const uint32_t n_glob = s * PIR_SLAB + col;
+                        if (n_glob >= A.D1) continue;
+                        uint32_t x = red[mm * 32 + nn] + red[(32 + mm) * 32 + nn];
+                        x = x >= q ? x - q : x;
+                        uint32_t y = red[(64 + mm) * 32 + nn] + red[(96 + mm) * 32 + nn];
+                        y = y >= q ? y - q : y;
+                        x += y;
+                        x = x >= q ? x - q : x;
+                        const uint64_t b = A.b0 + (mm >> 1);
+                        A.out[((b * A.D1 + n_glob) * 2 + (mm & 1)) * A.P + p] = x;
+                    }
+                }
+            }
+        }
+    } else if (warp < 12) {
+        // ------------------------------------------------ converters: DB words -> 4 fp16 byte planes
+        const uint32_t ct = threadIdx.x - 256;  // 0..127
+        uint32_t it = 0;
+        for (uint64_t p = p_begin; p < p_end; ++p)
+            for (uint32_t s = 0; s < A.S; ++s) {
+                const uint32_t nt = tiles_of(A, s);
+                for (uint32_t t = 0; t < nt; ++t)
+                    for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
+                        const uint32_t st = it % TC_NS, ph = (it / TC_NS) & 1;
+                        if (!abort_flag && !mbar_wait(rfull + st, ph, A.status)) abort_flag = 1;
+                        if (!abort_flag) {
+                            const uint32_t *raw = reinterpret_cast<const uint32_t *>(stR + st * TC_RAW_BYTES);
+                            uint8_t *bt = stB + st * TC_B_BYTES;
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const uint32_t task = ct + 128 * h;   // column n, 8 rows kc*8 .. kc*8+7
+                                const uint32_t n = task & 31, kc = task >> 5;
+                                uint32_t w[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) w[e] = raw[(kc * 8 + e) * TC_NT + n];
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    uint32_t hv[4];
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        // bytes j of two words -> halves 0x64xx = 1024 + byte
+                                        const uint32_t x = __byte_perm(w[2 * e], w[2 * e + 1], j | ((4 + j) << 8));
+                                        const uint32_t hh = (x & 0x00FF00FFu) | 0x64006400u;
+                                        const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&hh),
+                                                                  __floats2half2_rn(1024.f, 1024.f));
+                                        hv[e] = *reinterpret_cast<const uint32_t *>(&r);
+                                    }
+                                    *reinterpret_cast<uint4 *>(bt + sw128(j * 32 + n, kc)) =
+                                        make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                                }
+                            }
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bfull + st);
+                    }
+            }
+    }
+
+    fence_before();
+    __syncthreads();
+    if (warp == 12) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS)
+                     : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &r) ==
+                cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+size_t tc_smem_bytes() { return 1024 + (size_t)TC_NS * (TC_B_BYTES + TC_RAW_BYTES) + 4 * 32 * 32 * 4 + 512; }
+
+uint64_t powmod_host(uint64_t b, uint64_t e, uint64_t m) {
+    uint64_t r = 1 % m;
+    b %= m;
+    for (; e; e >>= 1) {
+        if (e & 1) r = (uint64_t)((unsigned __int128)r * b % m);
+        b = (uint64_t)((unsigned __int128)b * b % m);
+    }
+    return r;
+}
+
+}  // namespace
+
+// Whether a RowSel pass of Mv polynomials over D0 rows runs on this path.
+bool rowsel_tc_eligible(uint32_t D0, uint32_t Mv) { return Mv > 16 && D0 <= TC_MAX_D0; }
+
+// One RowSel pass on the tensor cores.  qT holds the pass's query slices
+// (32 polynomials per k, PS words per point); db is the slab-encoded DB.
+int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *qT, uint32_t PS,
+                   uint32_t b0, uint32_t Mv, uint32_t *out, cudaStream_t st) {
+    auto encode = encode_fn();
+    if (!encode) return PIR_ERR_CUDA;
+    const uint64_t P = (uint64_t)ctx->L * ctx->N;
+    const uint32_t D1p = (D1 + 3) / 4 * 4;
+    const uint32_t S = (D1 + PIR_SLAB - 1) / PIR_SLAB;
+    const uint32_t Wlast = D1p - PIR_SLAB * (S - 1);
+
+    // Full slabs: 4-D view (column, row k, slab, point) of the first S-1 slabs of every point.
+    CUtensorMap full_map, last_map;
+    memset(&full_map, 0, sizeof(full_map));
+    memset(&last_map, 0, sizeof(last_map));
+    const cuuint32_t box[4] = {TC_NT, TC_KS, 1, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    void *dbp = const_cast<uint32_t *>(db);
+    if (S > 1) {
+        const cuuint64_t dim[4] = {PIR_SLAB, D0, S - 1, P};
+        const cuuint64_t str[3] = {(cuuint64_t)PIR_SLAB * 4, (cuuint64_t)D0 * PIR_SLAB * 4, (cuuint64_t)D0 * D1p * 4};
+        if (encode(&full_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, dbp, dim, str, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PIR_ERR_ARG;
+    }
+    {
+        // Last slab of every point: (column, row k, 1, point), base at slab S-1.
+        const cuuint64_t dim[4] = {Wlast, D0, 1, P};
+        const cuuint64_t str[3] = {(cuuint64_t)Wlast * 4, (cuuint64_t)D0 * Wlast * 4, (cuuint64_t)D0 * D1p * 4};
+        void *lastp = const_cast<uint32_t *>(db + (uint64_t)(S - 1) * D0 * PIR_SLAB);
+        if (encode(&last_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, lastp, dim, str, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PIR_ERR_ARG;
+    }
+    if (S == 1) full_map = last_map;  // never used
+
+    TcArgs a;
+    memset(&a, 0, sizeof(a));
+    a.qT = qT;
+    a.out = out;
+    a.status = ctx->d_status;
+    a.N = ctx->N;
+    a.D0 = D0;
+    a.D1 = D1;
+    a.S = S;
+    a.Wlast = Wlast;
+    a.PS = PS;
+    a.Kp = (D0 + TC_KS - 1) / TC_KS * TC_KS;
+    a.b0 = b0;
+    a.Mv = Mv;
+    a.P = P;
+    for (uint32_t l = 0; l < ctx->L; ++l) {
+        const uint64_t q = ctx->q[l];
+        a.q[l] = (uint32_t)q;
+        a.mu[l] = ctx->mu[l];
+        a.bias[l] = ((1ull << 50) + q - 1) / q * q;
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t c = (uint32_t)powmod_host(2, 8 * i, q);
+            a.c[l][i] = c;
+            a.cs[l][i] = (uint32_t)(((uint64_t)c << 32) / q);
+        }
+    }
+    const size_t smem = tc_smem_bytes();
+    static bool attr_set[64] = {};
+    if (ctx->device < 64 && !attr_set[ctx->device]) {
+        if (cudaFuncSetAttribute(rowsel_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return PIR_ERR_CUDA;
+        attr_set[ctx->device] = true;
+    }
+    const uint64_t grid = P < (uint64_t)ctx->num_sms ? P : (uint64_t)ctx->num_sms;
+    rowsel_tc_kernel<<<(unsigned)grid, TC_THREADS, smem, st>>>(full_map, last_map, a);
+    return launch_status(cudaGetLastError());
+}

@@ -43,6 +43,8 @@ def _small_case(pir, N, L, D0, D1, B, seed):
     (64, 2, 40, 200, 5),     # padded polynomial count (M = 10 -> 16)
     (16, 2, 9, 44, 16),      # M = 32
     (16, 2, 9, 44, 17),      # two passes (16 + 1)
+    (16, 2, 512, 300, 16),   # tensor-core path: D0 = 512, 3 slabs (128 + 128 + 44)
+    (64, 3, 100, 37, 12),    # tensor-core path, padded polynomials (24 of 32), ragged rows
 ])
 def test_encode_and_rowsel_small(pir, N, L, D0, D1, B):
     ctx, qs, psis, raw, db_t, query = _small_case(pir, N, L, D0, D1, B, seed=(N + D0 + D1 + B) % 251)
@@ -84,11 +86,12 @@ def test_rowsel_one_hot_returns_record(pir):
     assert pir.pir_status(ctx) == 0
 
 
-@pytest.mark.parametrize("B", [1, 2, 4, 8, 16])
-def test_rowsel_max_residues(pir, B):
+@pytest.mark.parametrize("B,D0", [(1, 1000), (2, 1000), (4, 1000), (8, 1000), (16, 1000), (16, 512)])
+def test_rowsel_max_residues(pir, B, D0):
     """All residues q-1 (largest products, longest lazy chains) for every split
-    of rows and polynomials across warps: out = D0 mod q."""
-    N, L, D0, D1 = 64, 3, 1000, 9
+    of rows and polynomials across warps, and on the tensor-core path
+    (B = 16, D0 = 512): out = D0 mod q."""
+    N, L, D1 = 64, 3, 9
     qs = oracle.primes(N, L)
     ctx = pir.pir_ctx_create(N, qs)
     P = L * N
@@ -105,6 +108,29 @@ def test_rowsel_max_residues(pir, B):
     got = to_host_u32(out).reshape(B, D1, 2, L, N)
     for l in range(L):
         assert (got[..., l, :] == D0 % qs[l]).all()
+    assert pir.pir_status(ctx) == 0
+
+
+def test_rowsel_tensor_path_digit_extremes(pir):
+    """Tensor-core path at its exactness limit: DB words 0x1EFFFFFF (three
+    bytes 255) against query words 0x1F7F7F80 (balanced digits -128, -128,
+    -128, 32) over D0 = 512 rows puts every digit-plane sum at
+    512 * 255 * 128, just below 2^24; out = D0 * a * b mod q."""
+    N, L, D0, D1, B = 64, 3, 512, 33, 16
+    qs = oracle.primes(N, L)
+    ctx = pir.pir_ctx_create(N, qs)
+    P = L * N
+    D1p = (D1 + 3) // 4 * 4
+    a, b = 0x1F7F7F80, 0x1EFFFFFF
+    assert a < min(qs) and b < min(qs)
+    db_t = to_dev(np.full(P * D0 * D1p, b, np.uint32))
+    query = np.full((B, D0, 2, L, N), a, np.uint32)
+    out = pir.empty_u32(B * D1 * 2 * P)
+    out.fill_(-1)
+    pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(query), B, out, pir.rowsel_workspace(ctx, D0, B))
+    got = to_host_u32(out).reshape(B, D1, 2, L, N)
+    for l in range(L):
+        assert (got[..., l, :] == (D0 * a * b) % qs[l]).all()
     assert pir.pir_status(ctx) == 0
 
 
