@@ -48,6 +48,130 @@ __global__ void __launch_bounds__(kNttThreads) ntt_kernel(const uint32_t *__rest
     }
 }
 
+// N = 4096: 256 threads x 16 elements, three rounds of four butterfly stages.
+// The first round reads its 16 elements straight from global memory
+// (coalesced: element t + 256 i for the forward, 16t .. 16t+15 for the
+// inverse) and the last round writes straight back, so a row crosses shared
+// memory only twice.  Early-round twiddles are the same for all threads of a
+// warp (broadcast loads); the butterflies are branch-free.
+constexpr int kN4 = 4096, kT4 = 256;
+
+__device__ __forceinline__ uint32_t umin32(uint32_t a, uint32_t b) { return a < b ? a : b; }
+
+// One forward round of 4 stages (s0..s0+3) on x[16] = elements g + tlow*i.
+__device__ __forceinline__ void fwd_round16(uint32_t (&x)[16], uint32_t s0, uint32_t high,
+                                            const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
+                                            uint32_t q) {
+    const uint32_t q2 = 2 * q;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int d = 16 >> (r + 1);
+        const uint32_t m = 1u << (s0 + r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (i & d) continue;
+            const uint32_t idx = m + ((high << r) | (uint32_t)(i >> (4 - r)));
+            const uint32_t w = __ldg(W + idx), wp = __ldg(Wp + idx);
+            const uint32_t a = umin32(x[i], x[i] - q2);          // [0, 2q)
+            const uint32_t t = shoup_mul(x[i + d], w, wp, q);    // [0, 2q)
+            x[i] = a + t;
+            x[i + d] = a - t + q2;
+        }
+    }
+}
+
+// One inverse round of 4 stages s_hi..s_hi-3 on x[16] = elements g + tlow*i.
+__device__ __forceinline__ void inv_round16(uint32_t (&x)[16], uint32_t s_hi, uint32_t high,
+                                            const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
+                                            uint32_t q) {
+    const uint32_t q2 = 2 * q;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int d = 1 << r;
+        const uint32_t m = 1u << (s_hi - r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (i & d) continue;
+            const uint32_t idx = m + ((high << (3 - r)) | (uint32_t)(i >> (r + 1)));
+            const uint32_t w = __ldg(W + idx), wp = __ldg(Wp + idx);
+            const uint32_t u = x[i] + x[i + d];
+            const uint32_t v = x[i] - x[i + d] + q2;
+            x[i] = umin32(u, u - q2);                            // [0, 2q)
+            x[i + d] = shoup_mul(v, w, wp, q);                   // [0, 2q)
+        }
+    }
+}
+
+template <bool FWD>
+__global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict__ in, uint32_t *out,
+                                                      const __grid_constant__ RnsParams P) {
+    __shared__ __align__(16) uint32_t sm[kN4];
+    const uint64_t row = blockIdx.x;
+    const uint32_t l = (uint32_t)(row % P.L);
+    const uint32_t q = P.q[l];
+    const uint32_t *W = P.tw + (size_t)l * 4 * kN4 + (FWD ? TW_FWD : TW_INV) * kN4;
+    const uint32_t *Wp = P.tw + (size_t)l * 4 * kN4 + (FWD ? TW_FWD_SHOUP : TW_INV_SHOUP) * kN4;
+    const uint32_t *src = in + row * kN4;
+    uint32_t *dst = out + row * kN4;
+    const uint32_t t = threadIdx.x;
+    uint32_t x[16];
+    if (FWD) {
+        // round 0: stages 0-3, distance 256, elements t + 256 i
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = src[t + 256 * i];
+        fwd_round16(x, 0, 0, W, Wp, q);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sm[t + 256 * i] = x[i];
+        __syncthreads();
+        // round 1: stages 4-7, distance 16, elements (t>>4)*256 + (t&15) + 16 i
+        const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = sm[g1 + 16 * i];
+        fwd_round16(x, 4, t >> 4, W, Wp, q);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sm[g1 + 16 * i] = x[i];
+        __syncthreads();
+        // round 2: stages 8-11, distance 1, elements 16t .. 16t+15
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(sm + 16 * t + i);
+            x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
+        }
+        fwd_round16(x, 8, t, W, Wp, q);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<uint4 *>(dst + 16 * t + i) =
+                make_uint4(fwd_final(x[i], q), fwd_final(x[i + 1], q), fwd_final(x[i + 2], q), fwd_final(x[i + 3], q));
+    } else {
+        // round 0: stages 11-8, distance 1, elements 16t .. 16t+15
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * t + i);
+            x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
+        }
+        inv_round16(x, 11, t, W, Wp, q);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<uint4 *>(sm + 16 * t + i) = make_uint4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+        __syncthreads();
+        // round 1: stages 7-4, distance 16
+        const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = sm[g1 + 16 * i];
+        inv_round16(x, 7, t >> 4, W, Wp, q);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sm[g1 + 16 * i] = x[i];
+        __syncthreads();
+        // round 2: stages 3-0, distance 256, elements t + 256 i; then N^-1
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = sm[t + 256 * i];
+        inv_round16(x, 3, 0, W, Wp, q);
+        const uint32_t ni = P.ninv[l], nis = P.ninv_shoup[l];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[t + 256 * i] = inv_final(x[i], ni, nis, q);
+    }
+}
+
 template <bool FWD>
 int ntt_launch(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream) {
     if (!ctx) return PIR_ERR_ARG;
@@ -60,6 +184,11 @@ int ntt_launch(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, vo
     if (grid > 0x7fffffffull) return PIR_ERR_ARG;
     const size_t smem = (size_t)rpc * ctx->N * sizeof(uint32_t);
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
+    if (ctx->N == (uint32_t)kN4) {
+        if (in != out && (uint64_t)((in < out ? out - in : in - out)) < rows * kN4) return PIR_ERR_ARG;  // partial overlap
+        ntt4096_kernel<FWD><<<(unsigned)rows, kT4, 0, (cudaStream_t)stream>>>(in, out, rns_params(ctx));
+        return launch_status(cudaGetLastError());
+    }
     ntt_kernel<FWD><<<(unsigned)grid, kNttThreads, smem, (cudaStream_t)stream>>>(in, out, rows, rpc,
                                                                                   rns_params(ctx));
     return launch_status(cudaGetLastError());
