@@ -146,12 +146,14 @@ int pir_db_encode(pir_ctx *ctx, const uint32_t *raw, uint32_t k0, uint32_t kcnt,
                   uint32_t D0, uint32_t D1, uint32_t *db, void *stream);
 
 /*
- * pir_rowsel_workspace_bytes — device workspace pir_rowsel needs for D0 DB
- * rows and B queries: one pass's query in point-major order,
- * L*N * roundup(D0*Mp, 4) words, Mp = the pass's polynomial count (2B for
- * one query, padded to a power of two, at most 32).  0 for invalid sizes.
+ * pir_rowsel_workspace_bytes — device workspace pir_rowsel needs for a
+ * D0 x D1 DB and B queries: the largest pass's query in point-major order
+ * (L*N * roundup(D0*Mp, 4) words, Mp = the pass's polynomial count padded to
+ * a power of two, at most 32) and its results in point-major order
+ * (L*N * 2*nb * roundup(D1, 4) words, nb = queries in the pass).
+ * 0 for invalid sizes.
  */
-uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t B);
+uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t D1, uint32_t B);
 
 /*
  * pir_rowsel — the RowSel scan (GPIR section 2):
@@ -162,10 +164,11 @@ uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t B)
  *   db    : device, encoded by pir_db_encode for the same ctx, D0, D1.
  *   query : device, [B][D0][2][L][N] uint32 residues (NTT form).
  *   out   : device, [B][D1][2][L][N] uint32 (NTT form, canonical residues).
- *   workspace : device, >= pir_rowsel_workspace_bytes(ctx, D0, B) bytes,
+ *   workspace : device, >= pir_rowsel_workspace_bytes(ctx, D0, D1, B) bytes,
  *               16-byte aligned; holds the query transposed to point-major
- *               order (GPIR's NTT-to-GEMM layout change); contents undefined
- *               after the call.
+ *               order and the results before they are transposed back
+ *               (GPIR's NTT-to-GEMM layout change, both directions);
+ *               contents undefined after the call.
  * The DB is read from HBM once per pass; a pass covers as many queries as
  * fit the on-chip query buffer (16 queries for D0 <= 896, fewer for larger
  * D0); larger batches take ceil(B / per-pass) passes.

@@ -52,6 +52,7 @@ struct RowselArgs {
     uint32_t N, L, D0, D1, D1p, S, Wlast;
     uint32_t B, b0, Mv, Mp, msplit, ksplit, nchunks;
     uint32_t PS, nb;         // query slice stride (words) and number of slice buffers (1 or 2)
+    uint32_t *outT;          // point-major results [P][Mv][D1p] of the pass
     uint64_t P, units;
     uint32_t q[PIR_MAX_RNS], r32[PIR_MAX_RNS];
     uint64_t mu[PIR_MAX_RNS];
@@ -89,6 +90,39 @@ __global__ void __launch_bounds__(256) transpose_query_kernel(const uint32_t *__
         const uint64_t p = p0 + j;
         const uint32_t r = r0 + tx;
         if (p < P && r < PS) qT[p * PS + r] = r < rows ? tile[tx][j] : 0u;
+    }
+}
+
+// Results of a pass from the point-major block outT[p][m][n] (row length
+// D1p) to out[b][n][c][p] (m = 2(b - b0) + c): a tile of 32 points x 32
+// (m, n) rows moves through shared memory, coalesced on both sides.
+__global__ void __launch_bounds__(256) transpose_out_kernel(const uint32_t *__restrict__ outT,
+                                                            uint32_t *__restrict__ out, uint64_t P, uint32_t D1,
+                                                            uint32_t D1p, uint32_t Mv, uint32_t b0) {
+    __shared__ uint32_t tile[32][33];
+    const uint64_t p0 = (uint64_t)blockIdx.x * 32;
+    const uint32_t r0 = blockIdx.y * 32;            // row r = m * D1 + n
+    const uint32_t rows = Mv * D1;
+    const uint32_t tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (uint32_t j = ty; j < 32; j += 8) {
+        const uint64_t p = p0 + j;
+        const uint32_t r = r0 + tx;
+        uint32_t v = 0;
+        if (p < P && r < rows) {
+            const uint32_t m = r / D1, n = r - m * D1;
+            v = outT[(p * Mv + m) * D1p + n];
+        }
+        tile[j][tx] = v;
+    }
+    __syncthreads();
+    for (uint32_t i = ty; i < 32; i += 8) {
+        const uint32_t r = r0 + i;
+        const uint64_t p = p0 + tx;
+        if (r < rows && p < P) {
+            const uint32_t m = r / D1, n = r - m * D1;
+            const uint64_t b = b0 + (m >> 1);
+            out[((b * D1 + n) * 2 + (m & 1)) * P + p] = tile[tx][i];
+        }
     }
 }
 
@@ -261,19 +295,18 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
 
         // ---- unit epilogue: one reduction per output, then the write
         const uint32_t nbase = s * PIR_SLAB;
+        // results go to the point-major block outT[p][m][n] (coalesced); a
+        // transpose kernel then lays them out as [b][n][c][p]
+        uint32_t *ot = A.outT + p * (uint64_t)A.Mv * A.D1p + nbase;
         if (A.ksplit == 1) {
             if (active) {
 #pragma unroll
                 for (int i = 0; i < MT; ++i) {
                     const uint32_t m = ms * MT + i;
                     if (m >= A.Mv) continue;
-                    const uint64_t b = A.b0 + (m >> 1);
-                    const uint32_t cc = m & 1;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t n = nbase + 4 * lane + j;
-                        if (n < A.D1) A.out[((b * A.D1 + n) * 2 + cc) * A.P + p] = barrett64(acc[i][j], q, mu);
-                    }
+                    *reinterpret_cast<uint4 *>(ot + (uint64_t)m * A.D1p + 4 * lane) =
+                        make_uint4(barrett64(acc[i][0], q, mu), barrett64(acc[i][1], q, mu),
+                                   barrett64(acc[i][2], q, mu), barrett64(acc[i][3], q, mu));
                 }
             }
         } else {
@@ -289,12 +322,9 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
             const uint32_t tot = A.Mv * Ws;
             for (uint32_t idx = ctid; idx < tot; idx += NWC * 32) {
                 const uint32_t m = idx / Ws, col = idx - m * Ws;
-                const uint32_t n = nbase + col;
-                if (n >= A.D1) continue;
                 uint32_t sum = 0;  // < ksplit * q < 2^32
                 for (uint32_t kk = 0; kk < A.ksplit; ++kk) sum += red[(kk * A.Mp + m) * PIR_SLAB + col];
-                const uint64_t b = A.b0 + (m >> 1);
-                A.out[((b * A.D1 + n) * 2 + (m & 1)) * A.P + p] = sum % q;
+                ot[(uint64_t)m * A.D1p + col] = sum % q;
             }
         }
     }
@@ -351,15 +381,36 @@ uint32_t padded_mp(uint32_t Mv) {
 // Tensor-core path for large batches (rowsel_tc.cu).
 bool rowsel_tc_eligible(uint32_t D0, uint32_t Mv);
 int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *qT, uint32_t PS,
-                   uint32_t b0, uint32_t Mv, uint32_t *out, cudaStream_t st);
+                   uint32_t Mv, uint32_t *outT, cudaStream_t st);
 
-extern "C" uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t B) {
-    if (!ctx || D0 == 0 || B == 0 || D0 > 14336) return 0;
+namespace {
+
+// Workspace: the pass's query slices (point-major) followed by the pass's
+// results (point-major, 256-byte aligned).
+struct WsLayout {
+    uint64_t qT_words, outT_offset_words, total_bytes;
+};
+
+WsLayout ws_layout(const pir_ctx *ctx, uint32_t D0, uint32_t D1, uint32_t B) {
+    WsLayout w{0, 0, 0};
     const uint32_t cap = mp_capacity(D0);
-    if (!cap) return 0;
-    const uint32_t mp = padded_mp(2 * (B < cap / 2 ? B : cap / 2));
+    if (!cap) return w;
+    const uint32_t nb = B < cap / 2 ? B : cap / 2;   // queries in the largest pass
+    const uint32_t mp = padded_mp(2 * nb);
+    const uint64_t P = (uint64_t)ctx->L * ctx->N;
     const uint64_t ps = ((uint64_t)D0 * mp + 3) / 4 * 4;
-    return (uint64_t)ctx->L * ctx->N * ps * 4;
+    const uint64_t D1p = ((uint64_t)D1 + 3) / 4 * 4;
+    w.qT_words = P * ps;
+    w.outT_offset_words = (w.qT_words + 63) / 64 * 64;
+    w.total_bytes = (w.outT_offset_words + P * 2 * nb * D1p) * 4;
+    return w;
+}
+
+}  // namespace
+
+extern "C" uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t D1, uint32_t B) {
+    if (!ctx || D0 == 0 || D1 == 0 || B == 0 || D0 > 14336) return 0;
+    return ws_layout(ctx, D0, D1, B).total_bytes;
 }
 
 extern "C" int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *query,
@@ -368,13 +419,15 @@ extern "C" int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_
     if (!aligned16(db) || !aligned16(query) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
     if (D0 == 0 || D1 == 0 || B == 0) return PIR_ERR_ARG;
     if (D0 > 14336) return PIR_ERR_UNSUPPORTED;
-    if (workspace_bytes < pir_rowsel_workspace_bytes(ctx, D0, B)) return PIR_ERR_ARG;
+    const WsLayout wl = ws_layout(ctx, D0, D1, B);
+    if (workspace_bytes < wl.total_bytes) return PIR_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
 
     RowselArgs A;
     memset(&A, 0, sizeof(A));
     A.db = db;
     A.qT = reinterpret_cast<const uint32_t *>(workspace);
+    A.outT = reinterpret_cast<uint32_t *>(workspace) + wl.outT_offset_words;
     A.out = out;
     A.status = ctx->d_status;
     A.N = ctx->N;
@@ -408,15 +461,12 @@ extern "C" int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_
         uint32_t *qT = reinterpret_cast<uint32_t *>(workspace);
         transpose_query_kernel<<<tgrid, 256, 0, st>>>(query, qT, A.P, D0, A.Mp, A.Mv, b0, A.PS);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
-        int rc;
+        int rc = PIR_OK;
         if (rowsel_tc_eligible(D0, A.Mv)) {  // 17..32 polynomials: exact fp16 tensor-core GEMMs
-            rc = rowsel_tc_pass(ctx, db, D0, D1, qT, A.PS, b0, A.Mv, out, st);
-            if (rc) return rc;
-            continue;
-        }
+            rc = rowsel_tc_pass(ctx, db, D0, D1, qT, A.PS, A.Mv, A.outT, st);
         // thread tile MT polynomials x 4 columns; warps split the padded
         // polynomials (msplit) and the rows of a chunk (ksplit >= 2)
-        if (A.Mp == 2) {
+        } else if (A.Mp == 2) {
             A.msplit = 1;
             A.ksplit = NWC;
             rc = launch_pass<2>(ctx, A, st);
@@ -430,6 +480,10 @@ extern "C" int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_
             rc = launch_pass<8>(ctx, A, st);
         }
         if (rc) return rc;
+        // the pass's results into the caller's [B][D1][2][L][N] layout
+        const dim3 ogrid((unsigned)((A.P + 31) / 32), (A.Mv * D1 + 31) / 32);
+        transpose_out_kernel<<<ogrid, 256, 0, st>>>(A.outT, out, A.P, D1, A.D1p, A.Mv, b0);
+        if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
     }
     return PIR_OK;
 }

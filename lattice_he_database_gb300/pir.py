@@ -63,7 +63,7 @@ def lib() -> ctypes.CDLL:
         L.pir_db_encode.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
                                     _vp, _vp]
         L.pir_rowsel_workspace_bytes.restype = ctypes.c_uint64
-        L.pir_rowsel_workspace_bytes.argtypes = [_vp, ctypes.c_uint32, ctypes.c_uint32]
+        L.pir_rowsel_workspace_bytes.argtypes = [_vp, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
         L.pir_rowsel.restype = ctypes.c_int
         L.pir_rowsel.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, ctypes.c_uint32, _vp, _vp,
                                  ctypes.c_uint64, _vp]
@@ -194,8 +194,8 @@ def pir_db_encode(ctx: Ctx, raw: torch.Tensor, k0: int, kcnt: int, D0: int, D1: 
                                _stream(stream)), "pir_db_encode")
 
 
-def pir_rowsel_workspace_bytes(ctx: Ctx, D0: int, B: int) -> int:
-    return int(lib().pir_rowsel_workspace_bytes(ctx, D0, B))
+def pir_rowsel_workspace_bytes(ctx: Ctx, D0: int, D1: int, B: int) -> int:
+    return int(lib().pir_rowsel_workspace_bytes(ctx, D0, D1, B))
 
 
 def pir_rowsel(ctx: Ctx, db: torch.Tensor, D0: int, D1: int, query: torch.Tensor, B: int, out: torch.Tensor,
@@ -206,9 +206,9 @@ def pir_rowsel(ctx: Ctx, db: torch.Tensor, D0: int, D1: int, query: torch.Tensor
                             _stream(stream)), "pir_rowsel")
 
 
-def rowsel_workspace(ctx: Ctx, D0: int, B: int, device="cuda") -> torch.Tensor:
-    """A device workspace sized for pir_rowsel(D0, B)."""
-    return torch.empty(pir_rowsel_workspace_bytes(ctx, D0, B), dtype=torch.uint8, device=device)
+def rowsel_workspace(ctx: Ctx, D0: int, D1: int, B: int, device="cuda") -> torch.Tensor:
+    """A device workspace sized for pir_rowsel(D0, D1, B)."""
+    return torch.empty(pir_rowsel_workspace_bytes(ctx, D0, D1, B), dtype=torch.uint8, device=device)
 
 
 # ---------------------------------------------------------------- scalar scan
@@ -272,7 +272,7 @@ class RowselServer:
         self.q_ntt = empty_u32(self.q_words, dev)
         self.o_ntt = empty_u32(self.o_words, dev)
         self.o_coef = empty_u32(self.o_words, dev)
-        self.ws = rowsel_workspace(ctx, D0, B, dev)
+        self.ws = rowsel_workspace(ctx, D0, D1, B, dev)
         self.stream = stream or torch.cuda.current_stream(dev)
         self.launches_per_answer = 3
 

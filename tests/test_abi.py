@@ -77,7 +77,7 @@ def test_error_strings_and_null_ctx(lib):
     assert "invalid" in pir.pir_strerror(pir.PIR_ERR_ARG)
     assert lib.pir_db_bytes(None, 4, 4) == 0
     assert lib.pir_rowsel(None, None, 1, 1, None, 1, None, None, 0, None) == pir.PIR_ERR_ARG
-    assert lib.pir_rowsel_workspace_bytes(None, 4, 1) == 0
+    assert lib.pir_rowsel_workspace_bytes(None, 4, 4, 1) == 0
     assert lib.pir_ntt_fwd(None, None, None, 1, None) == pir.PIR_ERR_ARG
     assert lib.pir_scalar_workspace_bytes(0, 64) == 0
 

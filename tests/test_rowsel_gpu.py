@@ -59,7 +59,7 @@ def test_encode_and_rowsel_small(pir, N, L, D0, D1, B):
         assert (gather_db_device(db_t, N, L, D0, D1, kp.reshape(-1), npd.reshape(-1)) == 0).all()
     out = pir.empty_u32(B * D1 * 2 * L * N)
     out.fill_(-1)
-    pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(query), B, out, pir.rowsel_workspace(ctx, D0, B))
+    pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(query), B, out, pir.rowsel_workspace(ctx, D0, D1, B))
     got = to_host_u32(out).reshape(B, D1, 2, L, N)
     assert np.array_equal(got, oracle.rowsel(enc, query, qs))
     assert pir.pir_status(ctx) == 0
@@ -77,7 +77,7 @@ def test_rowsel_one_hot_returns_record(pir):
         q = np.zeros((1, D0, 2, L, N), np.uint32)
         q[0, istar, 0] = 1       # the constant polynomial 1: all ones in NTT form
         out = pir.empty_u32(D1 * 2 * L * N)
-        pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(q), 1, out, pir.rowsel_workspace(ctx, D0, 1))
+        pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(q), 1, out, pir.rowsel_workspace(ctx, D0, D1, 1))
         pir.pir_ntt_inv(ctx, out, out, D1 * 2)
         got = to_host_u32(out).reshape(D1, 2, L, N)
         for l in range(L):
@@ -104,7 +104,7 @@ def test_rowsel_max_residues(pir, B, D0):
     query = np.broadcast_to(np.array(qs, np.uint32).reshape(1, 1, 1, L, 1) - 1, (B, D0, 2, L, N)).copy()
     out = pir.empty_u32(B * D1 * 2 * P)
     out.fill_(-1)
-    pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(query), B, out, pir.rowsel_workspace(ctx, D0, B))
+    pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(query), B, out, pir.rowsel_workspace(ctx, D0, D1, B))
     got = to_host_u32(out).reshape(B, D1, 2, L, N)
     for l in range(L):
         assert (got[..., l, :] == D0 % qs[l]).all()
@@ -127,7 +127,7 @@ def test_rowsel_tensor_path_digit_extremes(pir):
     query = np.full((B, D0, 2, L, N), a, np.uint32)
     out = pir.empty_u32(B * D1 * 2 * P)
     out.fill_(-1)
-    pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(query), B, out, pir.rowsel_workspace(ctx, D0, B))
+    pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(query), B, out, pir.rowsel_workspace(ctx, D0, D1, B))
     got = to_host_u32(out).reshape(B, D1, 2, L, N)
     for l in range(L):
         assert (got[..., l, :] == (D0 * a * b) % qs[l]).all()
@@ -140,7 +140,7 @@ def test_rowsel_rejects_bad_arguments(pir):
     db = pir.empty_u32(pir.pir_db_bytes(ctx, 4, 4) // 4)
     q = pir.empty_u32(4 * 2 * 2 * 64)
     out = pir.empty_u32(4 * 2 * 2 * 64)
-    ws = pir.rowsel_workspace(ctx, 4, 1)
+    ws = pir.rowsel_workspace(ctx, 4, 4, 1)
     for args in [(0, 4, 1), (4, 0, 1), (4, 4, 0)]:
         with pytest.raises(pir.PirError):
             pir.pir_rowsel(ctx, db, args[0], args[1], q, args[2], out, ws)
@@ -182,7 +182,7 @@ def _full_size(pir, name, sample_cols):
         out_coef = to_host_u32(res).reshape(B, D1, 2, L, N)
     else:
         q_ntt = query
-        pir.pir_rowsel(ctx, db_t, D0, D1, q_t, B, out, pir.rowsel_workspace(ctx, D0, B))
+        pir.pir_rowsel(ctx, db_t, D0, D1, q_t, B, out, pir.rowsel_workspace(ctx, D0, D1, B))
         out_ntt = to_host_u32(out).reshape(B, D1, 2, L, N)
         out_coef = None
     assert pir.pir_status(ctx) == 0
