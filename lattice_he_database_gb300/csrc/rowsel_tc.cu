@@ -23,12 +23,15 @@
 //
 // Warp roles (448 threads, one CTA per SM, persistent over a range of points):
 //   warps 0-3   query digits of the next point -> TMEM (tcgen05.st), warp w
-//               writes digit plane w into TMEM lanes 32w..32w+31;
+//               writes digit plane w into TMEM lanes 32w..32w+31, from the
+//               point's query slice that the producer bulk-copies into
+//               shared memory while the previous point is still in flight;
 //   warps 4-7   epilogue: tcgen05.ld of a finished accumulator, reduction,
 //               cross-plane sum through shared memory, output stores;
 //   warps 8-11  converters: 64 x 32 DB words (TMA-staged) -> 4 byte planes
 //               of fp16 in the 128B-swizzled K-major layout of the B operand;
-//   warp 12     TMEM allocation and the TMA producer of DB word tiles;
+//   warp 12     TMEM allocation and the TMA producer of query slices and DB
+//               word tiles;
 //   warp 13     MMA issue (one thread).
 // All mbarrier waits are bounded; TMEM is always released.
 #include <cuda.h>
@@ -41,7 +44,7 @@
 
 namespace {
 
-constexpr int TC_NS = 8;                       // pipeline stages
+constexpr int TC_NS = 6;                       // pipeline stages
 constexpr int TC_KS = 64;                      // DB rows (K) per stage
 constexpr int TC_NT = 32;                      // DB columns per MMA tile
 constexpr uint32_t TC_RAW_BYTES = TC_KS * TC_NT * 4;   // 8 KiB of DB words
@@ -50,12 +53,13 @@ constexpr int TC_THREADS = 14 * 32;
 constexpr uint32_t TC_TMEM_COLS = 512;
 constexpr uint32_t TC_ACC_COL = 256;           // accumulators at columns 256 and 384
 constexpr uint32_t TC_MAX_D0 = 512;            // exactness bound of one fp32 accumulation
+constexpr uint32_t TC_Q_BYTES = TC_MAX_D0 * 32 * 4;     // one point's query slice (64 KiB)
 
 struct TcArgs {
     const uint32_t *qT;     // point-major query, [P][PS], 32 polynomials per k
-    uint32_t *out;
+    uint32_t *outT;         // point-major results [P][Mv][D1p]
     uint32_t *status;
-    uint32_t N, D0, D1, S, Wlast, PS, Kp, b0, Mv;
+    uint32_t N, D0, D1, D1p, S, Wlast, PS, Kp, Mv;
     uint64_t P;
     uint32_t q[PIR_MAX_RNS];
     uint64_t mu[PIR_MAX_RNS];
@@ -124,16 +128,16 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-// Balanced base-256 digit `plane` of a < 2^32, as the fp16 bit pattern.
-__device__ __forceinline__ uint32_t digit_half(uint32_t a, uint32_t plane) {
-    int d = 0;
-    int64_t y = a;
-    for (uint32_t i = 0; i <= plane; ++i) {
-        const int lo = (int)(y & 0xFF);
-        d = (i < 3) ? ((lo ^ 0x80) - 0x80) : (int)y;  // the top digit keeps the rest (<= 33 for a < 2^29)
-        y = (y - d) >> 8;
-    }
-    return (uint32_t)__half_as_ushort(__int2half_rn(d));
+// Balanced base-256 digit `plane` of two residues a0, a1 < 2^29, packed as
+// two fp16 values (a0 in the low half).  a + 0x808080 has the bytes d_i + 128
+// (i < 3) and d_3 on top, because balanced digits never carry; 0x64xx is the
+// fp16 value 1024 + xx, so subtracting 1152 (1024 for the top digit) leaves d.
+__device__ __forceinline__ uint32_t digit_pair(uint32_t a0, uint32_t a1, uint32_t plane) {
+    const uint32_t x0 = a0 + 0x808080u, x1 = a1 + 0x808080u;
+    const uint32_t hh = (__byte_perm(x0, x1, plane | ((4 + plane) << 8)) & 0x00FF00FFu) | 0x64006400u;
+    const float off = plane < 3 ? 1152.f : 1024.f;
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&hh), __floats2half2_rn(off, off));
+    return *reinterpret_cast<const uint32_t *>(&r);
 }
 
 // Number of 32-column tiles of slab s.
@@ -150,11 +154,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint8_t *sm = smraw + (((base_s + 1023u) & ~1023u) - base_s);
     uint8_t *stB = sm;                                   // [NS][16 KiB] fp16 digit tiles
     uint8_t *stR = stB + TC_NS * TC_B_BYTES;             // [NS][8 KiB] DB words
-    uint32_t *red = reinterpret_cast<uint32_t *>(stR + TC_NS * TC_RAW_BYTES);  // [4][32][32]
+    uint32_t *qsm = reinterpret_cast<uint32_t *>(stR + TC_NS * TC_RAW_BYTES);   // [D0][32] query slice
+    uint32_t *red = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(qsm) + TC_Q_BYTES);  // [4][32][32]
     uint64_t *bars = reinterpret_cast<uint64_t *>(red + 4 * 32 * 32);
     uint64_t *rfull = bars, *bfull = bars + TC_NS, *empty = bars + 2 * TC_NS;
     uint64_t *accf = bars + 3 * TC_NS, *acce = accf + 2, *afull = acce + 2, *aempty = afull + 1, *done = aempty + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    uint64_t *qfull = done + 1, *qempty = qfull + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(qempty + 1);
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -175,6 +181,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         mbar_init(afull, 4);
         mbar_init(aempty, 1);
         mbar_init(done, 1);
+        mbar_init(qfull, 1);
+        mbar_init(qempty, 4);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -192,8 +200,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 12 && lane == 0) {
         // ------------------------------------------------ TMA producer: DB word tiles
         const uint64_t pol = policy_evict_first();
-        uint32_t it = 0;
-        for (uint64_t p = p_begin; p < p_end; ++p)
+        const uint32_t qbytes = A.PS * 4;
+        uint32_t it = 0, pc = 0;
+        for (uint64_t p = p_begin; p < p_end; ++p, ++pc) {
+            // the point's query slice (the query warps release the buffer once digitised)
+            if (abort_flag || !mbar_wait(qempty, (pc & 1) ^ 1, A.status)) {
+                abort_flag = 1;
+            } else {
+                mbar_arrive_expect_tx(qfull, qbytes);
+                bulk_g2s(qsm, A.qT + p * A.PS, qbytes, qfull, pol);
+            }
             for (uint32_t s = 0; s < A.S; ++s) {
                 const uint32_t nt = tiles_of(A, s);
                 for (uint32_t t = 0; t < nt; ++t)
@@ -212,10 +228,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                         (int)p, rfull + st, pol);
                     }
             }
+        }
         for (uint32_t i = 0; i < TC_NS && i < it; ++i) {  // copies in flight land first
             const uint32_t j = it - 1 - i;
             mbar_wait(rfull + j % TC_NS, (j / TC_NS) & 1, A.status);
         }
+        if (pc) mbar_wait(qfull, (pc - 1) & 1, A.status);
     } else if (warp == 13 && lane == 0) {
         // ------------------------------------------------ MMA issue
         uint32_t it = 0, g = 0, pc = 0;
@@ -256,19 +274,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t plane = warp, m = lane;
         uint32_t pc = 0;
         for (uint64_t p = p_begin; p < p_end; ++p, ++pc) {
+            if (!abort_flag && !mbar_wait(qfull, pc & 1, A.status)) abort_flag = 1;
             if (!abort_flag && !mbar_wait(aempty, (pc & 1) ^ 1, A.status)) abort_flag = 1;
             fence_after();
             if (!abort_flag) {
-                const uint32_t *src = A.qT + p * A.PS;
+                const bool live = m < A.Mv;
                 for (uint32_t kc = 0; kc < A.Kp / 64; ++kc) {
                     uint32_t v[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const uint32_t k0 = kc * 64 + 2 * e;
-                        const uint32_t a0 = (k0 < A.D0 && m < A.Mv) ? __ldg(src + (uint64_t)k0 * 32 + m) : 0u;
-                        const uint32_t a1 =
-                            (k0 + 1 < A.D0 && m < A.Mv) ? __ldg(src + (uint64_t)(k0 + 1) * 32 + m) : 0u;
-                        v[e] = digit_half(a0, plane) | (digit_half(a1, plane) << 16);
+                        const uint32_t a0 = (live && k0 < A.D0) ? qsm[k0 * 32 + m] : 0u;
+                        const uint32_t a1 = (live && k0 + 1 < A.D0) ? qsm[(k0 + 1) * 32 + m] : 0u;
+                        v[e] = digit_pair(a0, a1, plane);
                     }
                     tmem_st32(tmem + ((plane * 32u) << 16) + kc * 32, v);
                 }
@@ -276,7 +294,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull);
+            if (lane == 0) {
+                mbar_arrive(afull);
+                mbar_arrive(qempty);
+            }
         }
     } else if (warp < 8) {
         // ------------------------------------------------ epilogue
@@ -326,15 +347,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         const uint32_t col = t * TC_NT + nn;
                         if (mm >= A.Mv || col >= Ws) continue;
                         const uint32_t n_glob = s * PIR_SLAB + col;
-                        if (n_glob >= A.D1) continue;
                         uint32_t x = red[mm * 32 + nn] + red[(32 + mm) * 32 + nn];
                         x = x >= q ? x - q : x;
                         uint32_t y = red[(64 + mm) * 32 + nn] + red[(96 + mm) * 32 + nn];
                         y = y >= q ? y - q : y;
                         x += y;
                         x = x >= q ? x - q : x;
-                        const uint64_t b = A.b0 + (mm >> 1);
-                        A.out[((b * A.D1 + n_glob) * 2 + (mm & 1)) * A.P + p] = x;
+                        A.outT[(p * A.Mv + mm) * A.D1p + n_glob] = x;
                     }
                 }
             }
@@ -406,7 +425,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-size_t tc_smem_bytes() { return 1024 + (size_t)TC_NS * (TC_B_BYTES + TC_RAW_BYTES) + 4 * 32 * 32 * 4 + 512; }
+size_t tc_smem_bytes() { return 1024 + (size_t)TC_NS * (TC_B_BYTES + TC_RAW_BYTES) + TC_Q_BYTES + 4 * 32 * 32 * 4 + 512; }
 
 uint64_t powmod_host(uint64_t b, uint64_t e, uint64_t m) {
     uint64_t r = 1 % m;
@@ -426,7 +445,7 @@ bool rowsel_tc_eligible(uint32_t D0, uint32_t Mv) { return Mv > 16 && D0 <= TC_M
 // One RowSel pass on the tensor cores.  qT holds the pass's query slices
 // (32 polynomials per k, PS words per point); db is the slab-encoded DB.
 int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *qT, uint32_t PS,
-                   uint32_t b0, uint32_t Mv, uint32_t *out, cudaStream_t st) {
+                   uint32_t Mv, uint32_t *outT, cudaStream_t st) {
     auto encode = encode_fn();
     if (!encode) return PIR_ERR_CUDA;
     const uint64_t P = (uint64_t)ctx->L * ctx->N;
@@ -464,16 +483,16 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
     TcArgs a;
     memset(&a, 0, sizeof(a));
     a.qT = qT;
-    a.out = out;
+    a.outT = outT;
     a.status = ctx->d_status;
     a.N = ctx->N;
     a.D0 = D0;
     a.D1 = D1;
+    a.D1p = D1p;
     a.S = S;
     a.Wlast = Wlast;
     a.PS = PS;
     a.Kp = (D0 + TC_KS - 1) / TC_KS * TC_KS;
-    a.b0 = b0;
     a.Mv = Mv;
     a.P = P;
     for (uint32_t l = 0; l < ctx->L; ++l) {
