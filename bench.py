@@ -52,6 +52,9 @@ WORKLOADS = {
                        desc="Scalar-HE scan: DB 131072 x 131072 uint8 (16 GiB) x Q 131072 x 64 uint32, mod 2^32"),
     "scalar_2g_prof": dict(kind="scalar", R=16384, C=131072, B=64,
                            desc="Scalar-HE scan profiling case: DB 16384 x 131072 uint8 (2 GiB), B=64"),
+    # small case of the B=16 workload for profiler captures (3 GiB, tensor-core path)
+    "rowsel_3g_b16_prof": dict(N=4096, L=3, D0=512, D1=128, B=16, domain="ntt",
+                               desc="RowSel 3 GiB profiling case: N=4096, 3 primes, D0=512 x D1=128, B=16"),
     # small case of the 64 GiB pipeline for profiler captures (3 GiB, 2 column slabs)
     "rowsel_3g_prof": dict(N=4096, L=3, D0=256, D1=256, B=1, domain="coeff",
                            desc="RowSel 3 GiB profiling case: N=4096, 3 primes, D0=256 x D1=256, B=1, "
@@ -171,7 +174,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- oracle (CPU) leg
-ORACLE_POINTS = 1024   # evaluation points per oracle sample (of L*N = 12288)
+ORACLE_POINTS = 4096   # evaluation points per oracle sample (of L*N = 12288)
 
 
 def _oracle_rowsel_inputs(cfg, ncols):
@@ -283,6 +286,17 @@ def run_reference(args, cfg):
 
 
 # ---------------------------------------------------------------- GPU leg
+def launches_per_step(cfg) -> int:
+    """Kernels one RowSel step launches: per pass a query transpose, the scan
+    and a result transpose; plus the query NTT and result INTT in coefficient
+    form.  Queries per pass follow the on-chip query-slice budget (112 KiB)."""
+    cap = 32
+    while cap > 2 and cfg["D0"] * cap * 4 > 112 * 1024:
+        cap //= 2
+    passes = -(-cfg["B"] // (cap // 2))
+    return 3 * passes + (2 if cfg["domain"] == "coeff" else 0)
+
+
 def kernel_rooflines(coeff, q_bytes, o_bytes, ntt_fwd_ms, ntt_inv_ms, hbm_peak):
     """HBM fractions of the NTT kernels of the step (read + write of every residue)."""
     if not coeff:
@@ -516,7 +530,7 @@ def run_ours(args, cfg):
             "e2e": None if e2e_ms is None else {
                 "value": logical_db / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": q_bytes,
                 "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps * (3 if coeff else 1),
+            "gpu_launches": args.steps * launches_per_step(cfg),
             "cpu_baseline": cpu,
         }
         print(json.dumps(result), flush=True)
