@@ -55,12 +55,18 @@ WORKLOADS = {
     # small case of the B=16 workload for profiler captures (3 GiB, tensor-core path)
     "rowsel_3g_b16_prof": dict(N=4096, L=3, D0=512, D1=128, B=16, domain="ntt",
                                desc="RowSel 3 GiB profiling case: N=4096, 3 primes, D0=512 x D1=128, B=16"),
+    # ring-packing GEMM of expansion-based packing: the pages' 64 GiB configuration
+    # (hint H of Dr = 256 x n = 1280 polynomials, 15 GiB), one client
+    "exppack_15g": dict(kind="exppack", N=4096, L=3, n=1280, Dr=256, B=1,
+                        desc="ExpPack GEMM H*C + (0|G): N=4096, 3 primes, hint Dr=256 x n=1280 polys (15 GiB), "
+                             "B=1; step = lift+NTT(G, 256 polys) + the point-wise GEMM"),
     # small case of the 64 GiB pipeline for profiler captures (3 GiB, 2 column slabs)
     "rowsel_3g_prof": dict(N=4096, L=3, D0=256, D1=256, B=1, domain="coeff",
                            desc="RowSel 3 GiB profiling case: N=4096, 3 primes, D0=256 x D1=256, B=1, "
                                 "NTT + RowSel + INTT"),
 }
 METRIC = "DB GB/s scanned & queries/s (RowSel, 64 GiB DB), % of GB300 HBM roofline"
+EXPPACK_METRIC = "ring-packing GEMM H*C + (0|G): hint GB/s scanned"
 
 
 def parse():
@@ -259,6 +265,8 @@ def run_reference(args, cfg):
         return
     if cfg.get("kind") == "scalar":
         return run_reference_scalar(args, cfg)
+    if cfg.get("kind") == "exppack":
+        return run_reference_exppack(args, cfg)
     per_step = 120.0 / max(1, args.steps + args.warmup)
     ncols, threads = oracle_rowsel_calibrate(cfg, per_step)
     q0, db, qu = _oracle_rowsel_inputs(cfg, ncols)
@@ -285,16 +293,89 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+def _oracle_exppack_inputs(cfg, rows):
+    import oracle
+    import synth
+    n, B = cfg["n"], cfg["B"]
+    q0 = oracle.primes(cfg["N"], 1)[0]
+    H = synth.residues(11, (rows, n, 1, ORACLE_POINTS), [q0], tid=synth.T_EXTRA)
+    C = synth.residues(12, (B, n, 2, 1, ORACLE_POINTS), [q0], tid=synth.T_EXTRA)
+    G = synth.residues(13, (B, rows, 1, ORACLE_POINTS), [q0], tid=synth.T_EXTRA)
+    return q0, H, C, G
+
+
+def oracle_exppack_calibrate(cfg, seconds: float):
+    """Hint rows per oracle call so that one call takes about `seconds` on all host cores."""
+    import oracle
+    threads = oracle.default_threads()
+    q0, H, C, G = _oracle_exppack_inputs(cfg, threads)
+    t = time.perf_counter()
+    oracle.exppack(H, C, G, [q0], threads=threads)
+    t1 = time.perf_counter() - t
+    return min(cfg["Dr"], threads * max(1, int(seconds / max(t1, 1e-4)))), threads
+
+
+def oracle_exppack_sample(cfg, budget_s: float):
+    """Time the oracle ring-packing GEMM on a bounded sample: all n hint
+    columns and B clients, ORACLE_POINTS evaluation points of prime 0 and a
+    calibrated number of hint rows.  Returns (GB/s, threads, description, seconds)."""
+    import oracle
+    rows, threads = oracle_exppack_calibrate(cfg, budget_s)
+    q0, H, C, G = _oracle_exppack_inputs(cfg, rows)
+    t = time.perf_counter()
+    oracle.exppack(H, C, G, [q0], threads=threads)
+    dt = time.perf_counter() - t
+    desc = ("oracle ExpPack GEMM on %d of %d hint rows x %d of %d evaluation points, all n=%d, B=%d"
+            % (rows, cfg["Dr"], ORACLE_POINTS, cfg["L"] * cfg["N"], cfg["n"], cfg["B"]))
+    return rows * cfg["n"] * ORACLE_POINTS * 4 / dt / 1e9, threads, desc, dt
+
+
+def run_reference_exppack(args, cfg):
+    """Reference arm for the ring-packing GEMM: the oracle on a bounded sample
+    (all n hint columns and B clients, ORACLE_POINTS evaluation points of
+    prime 0, a calibrated number of hint rows)."""
+    import oracle
+    n, Dr, B, N = cfg["n"], cfg["Dr"], cfg["B"], cfg["N"]
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    rows, threads = oracle_exppack_calibrate(cfg, per_step)
+    q0, H, C, G = _oracle_exppack_inputs(cfg, rows)
+    for _ in range(args.warmup):
+        oracle.exppack(H, C, G, [q0], threads=threads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.exppack(H, C, G, [q0], threads=threads)
+    dt = (time.perf_counter() - t) / max(1, args.steps)
+    value = rows * n * ORACLE_POINTS * 4 / dt / 1e9
+    sample = ("oracle ExpPack GEMM per step: %d of %d hint rows x %d of %d evaluation points, all n=%d, B=%d"
+              % (rows, Dr, ORACLE_POINTS, cfg["L"] * N, n, B))
+    line = {
+        "impl": "reference", "metric": EXPPACK_METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic (seeded SplitMix64 residues)",
+        "config": {"workload": args.workload, "desc": cfg["desc"]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- GPU leg
-def launches_per_step(cfg) -> int:
-    """Kernels one RowSel step launches: per pass a query transpose, the scan
-    and a result transpose; plus the query NTT and result INTT in coefficient
-    form.  Queries per pass follow the on-chip query-slice budget (112 KiB)."""
+def rowsel_passes(D0, B) -> int:
+    """Query passes of one RowSel call: queries per pass follow the on-chip
+    query-slice budget (112 KiB of 4-byte residues for 2 polynomials each)."""
     cap = 32
-    while cap > 2 and cfg["D0"] * cap * 4 > 112 * 1024:
+    while cap > 2 and D0 * cap * 4 > 112 * 1024:
         cap //= 2
-    passes = -(-cfg["B"] // (cap // 2))
-    return 3 * passes + (2 if cfg["domain"] == "coeff" else 0)
+    return -(-B // (cap // 2))
+
+
+def launches_per_step(cfg) -> int:
+    """Kernels one step launches: per RowSel pass a query transpose, the scan
+    and a result transpose; plus the query NTT and result INTT in coefficient
+    form, or the lift + NTT of G for the ring-packing GEMM."""
+    if cfg.get("kind") == "exppack":
+        return 3 * rowsel_passes(cfg["n"], cfg["B"]) + 1
+    return 3 * rowsel_passes(cfg["D0"], cfg["B"]) + (2 if cfg["domain"] == "coeff" else 0)
 
 
 def kernel_rooflines(coeff, q_bytes, o_bytes, ntt_fwd_ms, ntt_inv_ms, hbm_peak):
@@ -370,6 +451,148 @@ def run_scalar(args, cfg):
         print(json.dumps(line), flush=True)
     ctx.close()
     return line
+
+
+def run_exppack(args, cfg):
+    """Ring-packing GEMM: one step = lift + NTT of the scan output G, then
+    H*C + (0|G) over the resident hint."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    import synth.device as sd
+    from lattice_he_database_gb300 import pir
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    N, L, n, Dr, B = cfg["N"], cfg["L"], cfg["n"], cfg["Dr"], cfg["B"]
+    qs = pir.pir_primes(N, L)
+    ctx = pir.pir_ctx_create(N, qs, local)
+    P = L * N
+    h_db = torch.empty(pir.pir_db_bytes(ctx, n, Dr) // 4, dtype=torch.int32, device="cuda")
+    rows = max(1, min(n, (1 << 30) // (Dr * N * 4)))
+    raw = torch.empty(rows * Dr * N, dtype=torch.int32, device="cuda")
+    for k0 in range(0, n, rows):
+        kc = min(rows, n - k0)
+        sd.fill_words(raw[: kc * Dr * N], 7, synth.T_HINT, idx0=k0 * Dr * N)
+        pir.pir_db_encode(ctx, raw[: kc * Dr * N], k0, kc, n, Dr, h_db)
+    torch.cuda.synchronize()
+    del raw
+    graw = torch.empty(B * Dr * N, dtype=torch.int32, device="cuda")
+    sd.fill_words(graw, 7, synth.T_SCAN_OUT)
+    C = torch.empty(B * n * 2 * P, dtype=torch.int32, device="cuda")
+    sd.fill_residues(C, 7, synth.T_SPECIAL, N, qs)
+    G = torch.empty(B * Dr * P, dtype=torch.int32, device="cuda")
+    out = torch.empty(B * Dr * 2 * P, dtype=torch.int32, device="cuda")
+    ws = pir.rowsel_workspace(ctx, n, Dr, B)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        pir.pir_lift_ntt(ctx, graw, G, B * Dr, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        pir.pir_exppack(ctx, h_db, n, Dr, C, G, B, out, ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(kev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_total = max_over_ranks(t0.elapsed_time(t1))
+    lift_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in kev]))
+    gemm_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in kev]))
+    if pir.pir_status(ctx):
+        raise RuntimeError("device status word set")
+
+    hint_bytes = P * n * Dr * 4
+    c_bytes, g_bytes, o_bytes, graw_bytes = B * n * 2 * P * 4, B * Dr * P * 4, B * Dr * 2 * P * 4, B * Dr * N * 4
+
+    # end to end: C and the scan words from pinned host memory, the packed ciphertexts back
+    c_host = torch.empty(C.numel(), dtype=torch.int32, pin_memory=True)
+    c_host.copy_(C.cpu())
+    g_host = torch.empty(graw.numel(), dtype=torch.int32, pin_memory=True)
+    g_host.copy_(graw.cpu())
+    o_host = torch.empty(out.numel(), dtype=torch.int32, pin_memory=True)
+    ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            C.copy_(c_host, non_blocking=True)
+            graw.copy_(g_host, non_blocking=True)
+            step()
+            o_host.copy_(out, non_blocking=True)
+
+    e2e_ms = None
+    if ke:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / ke
+
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    algo = hint_bytes + c_bytes + g_bytes + o_bytes
+    achieved = algo / (gemm_ms * 1e-3) / 1e9
+    lift_bytes = graw_bytes + g_bytes
+    result = None
+    if rank == 0:
+        line = {
+            "metric": EXPPACK_METRIC, "value": aggregate_throughput(hint_bytes, args.steps, ms_total, world) / 1e9,
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_total / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "u32",
+            "data": "synthetic: seeded SplitMix64 hint and scan words U[0,2^32), special-ct residues U[0,q_i)",
+            "config": {"workload": args.workload, "desc": cfg["desc"], "hint_bytes": hint_bytes, "B": B,
+                       "l2": "inputs larger than L2 (hint %.1f GiB), no flush" % (hint_bytes / GIB),
+                       "parallelism": "replicas x%d" % world},
+            "kernel_ms": {"lift_ntt": lift_ms, "exppack": gemm_ms},
+            "kernels": {"lift_ntt": {"bound": "hbm", "unit": "GB/s", "peak": hbm_peak,
+                                     "achieved": lift_bytes / (lift_ms * 1e-3) / 1e9,
+                                     "frac": lift_bytes / (lift_ms * 1e-3) / 1e9 / hbm_peak,
+                                     "algorithmic_bytes_per_launch": lift_bytes}},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": profile_traffic("rowsel_kernel_exppack_15g"),
+                         "kernel": "rowsel_kernel (pir_exppack)", "peak_source": "%s hbm_gbs (copy)" % peak_kind,
+                         "algorithmic_bytes_per_launch": algo},
+            "clocks": clk,
+            "e2e": None if e2e_ms is None else {
+                "value": hint_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": c_bytes + graw_bytes, "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * launches_per_step(cfg),
+            "cpu_baseline": None,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            gbs, threads, desc, secs = oracle_exppack_sample(cfg, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                    "sample": desc, "seconds": round(secs, 2)}
+        print(json.dumps(line), flush=True)
+        result = line
+    ctx.close()
+    return result
 
 
 def device_db(ctx, D0, D1, seed):
@@ -548,6 +771,8 @@ def main():
         run_reference(args, cfg)
     elif cfg.get("kind") == "scalar":
         run_scalar(args, cfg)
+    elif cfg.get("kind") == "exppack":
+        run_exppack(args, cfg)
     else:
         run_ours(args, cfg)
 

@@ -116,6 +116,20 @@ int pir_ntt_fwd(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, v
 int pir_ntt_inv(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream);
 
 /*
+ * pir_lift_ntt — lift plain 32-bit coefficients into R_q and transform them
+ * (VIPIR 3.5.2 and 3.6 step 3: the INT32 scan output, read as length-N
+ * coefficient vectors, becomes polynomials that are taken to NTT form, G).
+ *   raw : device, [cnt][N] uint32, any value; coefficient t of polynomial i
+ *         is raw[i*N + t], lifted to its residue mod q_l for every prime l.
+ *   out : device, [cnt][L][N], out[i][l] = NTT(raw[i] mod q_l) with the
+ *         output convention of pir_ntt_fwd.
+ *   raw and out must not overlap.
+ * Errors: PIR_ERR_ARG (NULL/unaligned pointer, overlap, size overflow),
+ * PIR_ERR_CUDA.  cnt = 0 is a no-op.
+ */
+int pir_lift_ntt(pir_ctx *ctx, const uint32_t *raw, uint32_t *out, uint64_t cnt, void *stream);
+
+/*
  * pir_db_bytes — bytes of the encoded RowSel DB for a D0 x D1 grid of records
  * (GPIR section 2: DB[i][j], i < D0, j < D1), i.e. L*N*D0*D1p*4 with
  * D1p = D1 rounded up to a multiple of 4.  Returns 0 for invalid sizes.
@@ -178,6 +192,32 @@ uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t D1
 int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1,
                const uint32_t *query, uint32_t B, uint32_t *out,
                void *workspace, uint64_t workspace_bytes, void *stream);
+
+/*
+ * pir_exppack — the INT32 modular GEMM of expansion-based ring packing
+ * (VIPIR 3.5.2): with H (Dr x n polynomials) and G (Dr x B polynomials), the
+ * NTT-domain forms of the B-batched SimplePIR hint and answers, and C
+ * (n x 2B polynomials) the expanded "special" ciphertexts of B clients,
+ *     out = H * C + (0 | G),
+ * i.e. for client b, output ciphertext r (one per hint row) and RNS point p:
+ *     out[b][r][c][p] = sum_{k<n} H[r][k][p] * C[b][k][c][p]
+ *                       + (c == 1 ? G[b][r][p] : 0)        mod q_{l(p)}.
+ * This is RowSel's point-wise GEMM with the hint as the DB: record (k, r) of a
+ * D0 = n by D1 = Dr DB is H[r][k].
+ *   h_db : device, H encoded by pir_db_encode(ctx, ..., D0 = n, D1 = Dr),
+ *          record (k, r) = polynomial H[r][k] (coefficients, lifted mod q_l).
+ *   C    : device, [B][n][2][L][N] residues (NTT form).
+ *   G    : device, [B][Dr][L][N] residues (NTT form), added to polynomial 1
+ *          (the "b" part) of every output ciphertext; must not be NULL.
+ *   out  : device, [B][Dr][2][L][N] (NTT form).
+ *   workspace : as for pir_rowsel, pir_rowsel_workspace_bytes(ctx, n, Dr, B).
+ * Reading: "(0 | G)" is taken as (0, G_b) per client ciphertext, G joining
+ * the polynomial that carries the message.
+ * Errors: as pir_rowsel; PIR_ERR_ARG for a NULL or unaligned G.
+ */
+int pir_exppack(pir_ctx *ctx, const uint32_t *h_db, uint32_t n, uint32_t Dr, const uint32_t *C,
+                const uint32_t *G, uint32_t B, uint32_t *out, void *workspace,
+                uint64_t workspace_bytes, void *stream);
 
 /*
  * pir_scalar_workspace_bytes — device workspace pir_scalar_scan needs for a

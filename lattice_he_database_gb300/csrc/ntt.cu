@@ -12,7 +12,9 @@ namespace {
 constexpr int kNttThreads = 512;
 constexpr uint32_t kMaxRowsPerCta = 4096 / 16;  // rows per CTA for the smallest ring (N = 16)
 
-template <bool FWD>
+// LIFT: the input is [cnt][N] plain 32-bit coefficients; row r = poly*L + l
+// reads polynomial poly and lifts each coefficient to its residue mod q_l.
+template <bool FWD, bool LIFT>
 __global__ void __launch_bounds__(kNttThreads) ntt_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                           uint64_t rows, uint32_t rpc,
                                                           const __grid_constant__ RnsParams P) {
@@ -22,9 +24,16 @@ __global__ void __launch_bounds__(kNttThreads) ntt_kernel(const uint32_t *__rest
     const uint64_t row0 = (uint64_t)blockIdx.x * rpc;
     const uint32_t nrows = (uint32_t)((rows - row0) < rpc ? (rows - row0) : rpc);
     const uint32_t nwords = nrows * N;  // multiple of 16
-    const uint4 *src = reinterpret_cast<const uint4 *>(in + row0 * N);
     uint4 *s4 = reinterpret_cast<uint4 *>(sm);
-    for (uint32_t i = threadIdx.x; i < nwords / 4; i += blockDim.x) s4[i] = src[i];
+    if (LIFT) {
+        for (uint32_t i = threadIdx.x; i < nwords; i += blockDim.x) {
+            const uint64_t row = row0 + (i >> logN);
+            sm[i] = in[(row / L) * N + (i & (N - 1))] % P.q[row % L];
+        }
+    } else {
+        const uint4 *src = reinterpret_cast<const uint4 *>(in + row0 * N);
+        for (uint32_t i = threadIdx.x; i < nwords / 4; i += blockDim.x) s4[i] = src[i];
+    }
     if (threadIdx.x < nrows) row_prime[threadIdx.x] = (uint8_t)((row0 + threadIdx.x) % L);
     __syncthreads();
 
@@ -102,23 +111,24 @@ __device__ __forceinline__ void inv_round16(uint32_t (&x)[16], uint32_t s_hi, ui
     }
 }
 
-template <bool FWD>
+template <bool FWD, bool LIFT>
 __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                       const __grid_constant__ RnsParams P) {
+    static_assert(FWD || !LIFT, "the lift feeds the forward transform only");
     __shared__ __align__(16) uint32_t sm[kN4];
     const uint64_t row = blockIdx.x;
     const uint32_t l = (uint32_t)(row % P.L);
     const uint32_t q = P.q[l];
     const uint32_t *W = P.tw + (size_t)l * 4 * kN4 + (FWD ? TW_FWD : TW_INV) * kN4;
     const uint32_t *Wp = P.tw + (size_t)l * 4 * kN4 + (FWD ? TW_FWD_SHOUP : TW_INV_SHOUP) * kN4;
-    const uint32_t *src = in + row * kN4;
+    const uint32_t *src = in + (LIFT ? row / P.L : row) * kN4;
     uint32_t *dst = out + row * kN4;
     const uint32_t t = threadIdx.x;
     uint32_t x[16];
     if (FWD) {
         // round 0: stages 0-3, distance 256, elements t + 256 i
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = src[t + 256 * i];
+        for (int i = 0; i < 16; ++i) x[i] = LIFT ? src[t + 256 * i] % q : src[t + 256 * i];
         fwd_round16(x, 0, 0, W, Wp, q);
 #pragma unroll
         for (int i = 0; i < 16; ++i) sm[t + 256 * i] = x[i];
@@ -172,25 +182,31 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
     }
 }
 
-template <bool FWD>
+template <bool FWD, bool LIFT = false>
 int ntt_launch(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream) {
     if (!ctx) return PIR_ERR_ARG;
     if (cnt == 0) return PIR_OK;
     if (!in || !out || !aligned16(in) || !aligned16(out)) return PIR_ERR_ARG;
     const uint64_t rows = cnt * ctx->L;
     if (rows / ctx->L != cnt || rows > (1ull << 40)) return PIR_ERR_ARG;
+    if (LIFT) {  // [cnt][N] in, [cnt][L][N] out: the two must not overlap at all
+        const uint64_t ib = cnt * ctx->N * 4, ob = rows * ctx->N * 4;
+        const uintptr_t a = (uintptr_t)in, b = (uintptr_t)out;
+        if (a < b + ob && b < a + ib) return PIR_ERR_ARG;
+    }
     const uint32_t rpc = ctx->N >= 4096 ? 1 : 4096 / ctx->N;
     const uint64_t grid = (rows + rpc - 1) / rpc;
     if (grid > 0x7fffffffull) return PIR_ERR_ARG;
     const size_t smem = (size_t)rpc * ctx->N * sizeof(uint32_t);
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
     if (ctx->N == (uint32_t)kN4) {
-        if (in != out && (uint64_t)((in < out ? out - in : in - out)) < rows * kN4) return PIR_ERR_ARG;  // partial overlap
-        ntt4096_kernel<FWD><<<(unsigned)rows, kT4, 0, (cudaStream_t)stream>>>(in, out, rns_params(ctx));
+        if (!LIFT && in != out && (uint64_t)((in < out ? out - in : in - out)) < rows * kN4)
+            return PIR_ERR_ARG;  // partial overlap
+        ntt4096_kernel<FWD, LIFT><<<(unsigned)rows, kT4, 0, (cudaStream_t)stream>>>(in, out, rns_params(ctx));
         return launch_status(cudaGetLastError());
     }
-    ntt_kernel<FWD><<<(unsigned)grid, kNttThreads, smem, (cudaStream_t)stream>>>(in, out, rows, rpc,
-                                                                                  rns_params(ctx));
+    ntt_kernel<FWD, LIFT><<<(unsigned)grid, kNttThreads, smem, (cudaStream_t)stream>>>(in, out, rows, rpc,
+                                                                                        rns_params(ctx));
     return launch_status(cudaGetLastError());
 }
 
@@ -202,4 +218,8 @@ extern "C" int pir_ntt_fwd(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint
 
 extern "C" int pir_ntt_inv(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream) {
     return ntt_launch<false>(ctx, in, out, cnt, stream);
+}
+
+extern "C" int pir_lift_ntt(pir_ctx *ctx, const uint32_t *raw, uint32_t *out, uint64_t cnt, void *stream) {
+    return ntt_launch<true, true>(ctx, raw, out, cnt, stream);
 }

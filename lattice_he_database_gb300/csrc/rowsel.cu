@@ -96,9 +96,16 @@ __global__ void __launch_bounds__(256) transpose_query_kernel(const uint32_t *__
 // Results of a pass from the point-major block outT[p][m][n] (row length
 // D1p) to out[b][n][c][p] (m = 2(b - b0) + c): a tile of 32 points x 32
 // (m, n) rows moves through shared memory, coalesced on both sides.
+struct AddendArgs {
+    const uint32_t *G;       // [B][D1][L][N] residues added to polynomial c = 1, or null
+    uint32_t N;
+    uint32_t q[PIR_MAX_RNS];
+};
+
 __global__ void __launch_bounds__(256) transpose_out_kernel(const uint32_t *__restrict__ outT,
                                                             uint32_t *__restrict__ out, uint64_t P, uint32_t D1,
-                                                            uint32_t D1p, uint32_t Mv, uint32_t b0) {
+                                                            uint32_t D1p, uint32_t Mv, uint32_t b0,
+                                                            const __grid_constant__ AddendArgs add) {
     __shared__ uint32_t tile[32][33];
     const uint64_t p0 = (uint64_t)blockIdx.x * 32;
     const uint32_t r0 = blockIdx.y * 32;            // row r = m * D1 + n
@@ -121,7 +128,13 @@ __global__ void __launch_bounds__(256) transpose_out_kernel(const uint32_t *__re
         if (r < rows && p < P) {
             const uint32_t m = r / D1, n = r - m * D1;
             const uint64_t b = b0 + (m >> 1);
-            out[((b * D1 + n) * 2 + (m & 1)) * P + p] = tile[tx][i];
+            uint32_t v = tile[tx][i];
+            if (add.G && (m & 1)) {  // (0 | G): the second polynomial of each ciphertext
+                const uint32_t q = add.q[p / add.N];
+                v += add.G[(b * D1 + n) * P + p];
+                v = v >= q ? v - q : v;
+            }
+            out[((b * D1 + n) * 2 + (m & 1)) * P + p] = v;
         }
     }
 }
@@ -413,9 +426,14 @@ extern "C" uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, 
     return ws_layout(ctx, D0, D1, B).total_bytes;
 }
 
-extern "C" int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *query,
-                          uint32_t B, uint32_t *out, void *workspace, uint64_t workspace_bytes, void *stream) {
+namespace {
+
+// RowSel passes over an encoded DB, with an optional addend G on the second
+// polynomial of every result ciphertext (the ExpPack GEMM H*C + (0 | G)).
+int rowsel_impl(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *query, uint32_t B,
+                const uint32_t *G, uint32_t *out, void *workspace, uint64_t workspace_bytes, void *stream) {
     if (!ctx || !db || !query || !out || !workspace) return PIR_ERR_ARG;
+    if (G && !aligned16(G)) return PIR_ERR_ARG;
     if (!aligned16(db) || !aligned16(query) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
     if (D0 == 0 || D1 == 0 || B == 0) return PIR_ERR_ARG;
     if (D0 > 14336) return PIR_ERR_UNSUPPORTED;
@@ -481,9 +499,28 @@ extern "C" int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_
         }
         if (rc) return rc;
         // the pass's results into the caller's [B][D1][2][L][N] layout
+        AddendArgs add;
+        memset(&add, 0, sizeof(add));
+        add.G = G;
+        add.N = ctx->N;
+        for (uint32_t l = 0; l < ctx->L; ++l) add.q[l] = ctx->q[l];
         const dim3 ogrid((unsigned)((A.P + 31) / 32), (A.Mv * D1 + 31) / 32);
-        transpose_out_kernel<<<ogrid, 256, 0, st>>>(A.outT, out, A.P, D1, A.D1p, A.Mv, b0);
+        transpose_out_kernel<<<ogrid, 256, 0, st>>>(A.outT, out, A.P, D1, A.D1p, A.Mv, b0, add);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
     }
     return PIR_OK;
+}
+
+}  // namespace
+
+extern "C" int pir_rowsel(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *query,
+                          uint32_t B, uint32_t *out, void *workspace, uint64_t workspace_bytes, void *stream) {
+    return rowsel_impl(ctx, db, D0, D1, query, B, nullptr, out, workspace, workspace_bytes, stream);
+}
+
+extern "C" int pir_exppack(pir_ctx *ctx, const uint32_t *h_db, uint32_t n, uint32_t Dr, const uint32_t *C,
+                           const uint32_t *G, uint32_t B, uint32_t *out, void *workspace, uint64_t workspace_bytes,
+                           void *stream) {
+    if (!G) return PIR_ERR_ARG;
+    return rowsel_impl(ctx, h_db, n, Dr, C, B, G, out, workspace, workspace_bytes, stream);
 }

@@ -53,7 +53,7 @@ def lib() -> ctypes.CDLL:
         L.pir_ctx_destroy.argtypes = [_vp]
         L.pir_ctx_psi.restype = ctypes.c_int
         L.pir_ctx_psi.argtypes = [_vp, _u32p]
-        for name in ("pir_ntt_fwd", "pir_ntt_inv"):
+        for name in ("pir_ntt_fwd", "pir_ntt_inv", "pir_lift_ntt"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = [_vp, _vp, _vp, ctypes.c_uint64, _vp]
@@ -68,6 +68,9 @@ def lib() -> ctypes.CDLL:
         L.pir_rowsel.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, ctypes.c_uint32, _vp, _vp,
                                  ctypes.c_uint64, _vp]
         L.pir_scalar_workspace_bytes.restype = ctypes.c_uint64
+        L.pir_exppack.restype = ctypes.c_int
+        L.pir_exppack.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, _vp, ctypes.c_uint32, _vp, _vp,
+                                  ctypes.c_uint64, _vp]
         L.pir_scalar_workspace_bytes.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
         L.pir_scalar_scan.restype = ctypes.c_int
         L.pir_scalar_scan.argtypes = [_vp, _vp, ctypes.c_uint64, ctypes.c_uint64, _vp, ctypes.c_uint32, _vp,
@@ -183,6 +186,12 @@ def pir_ntt_inv(ctx: Ctx, inp: torch.Tensor, out: torch.Tensor, cnt: int, stream
            "pir_ntt_inv")
 
 
+def pir_lift_ntt(ctx: Ctx, raw: torch.Tensor, out: torch.Tensor, cnt: int, stream=None):
+    """out[i][l] = NTT(raw[i] mod q_l): [cnt][N] plain words -> [cnt][L][N]."""
+    _check(lib().pir_lift_ntt(ctx, _dev_ptr(raw, 4, "raw"), _dev_ptr(out, 4, "out"), cnt, _stream(stream)),
+           "pir_lift_ntt")
+
+
 # ---------------------------------------------------------------- RowSel
 def pir_db_bytes(ctx: Ctx, D0: int, D1: int) -> int:
     return int(lib().pir_db_bytes(ctx, D0, D1))
@@ -209,6 +218,15 @@ def pir_rowsel(ctx: Ctx, db: torch.Tensor, D0: int, D1: int, query: torch.Tensor
 def rowsel_workspace(ctx: Ctx, D0: int, D1: int, B: int, device="cuda") -> torch.Tensor:
     """A device workspace sized for pir_rowsel(D0, D1, B)."""
     return torch.empty(pir_rowsel_workspace_bytes(ctx, D0, D1, B), dtype=torch.uint8, device=device)
+
+
+def pir_exppack(ctx: Ctx, h_db: torch.Tensor, n: int, Dr: int, C: torch.Tensor, G: torch.Tensor, B: int,
+                out: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """out = H*C + (0|G) point-wise mod q (ring-packing GEMM); h_db encoded with D0 = n, D1 = Dr."""
+    ws = _dev_ptr(workspace, workspace.element_size(), "workspace")
+    _check(lib().pir_exppack(ctx, _dev_ptr(h_db, 4, "h_db"), n, Dr, _dev_ptr(C, 4, "C"), _dev_ptr(G, 4, "G"), B,
+             _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(), _stream(stream)),
+           "pir_exppack")
 
 
 # ---------------------------------------------------------------- scalar scan

@@ -174,7 +174,7 @@ def ntt_polys(polys: np.ndarray, qs, psis, inverse: bool = False, threads: int |
 
 
 def encode_records(raw: np.ndarray, qs, psis, threads: int | None = None) -> np.ndarray:
-    """raw [..., N] coefficients in [0, 2^16) -> NTT form [..., L, N]."""
+    """raw [..., N] plain 32-bit coefficients, each lifted mod q_l -> NTT form [..., L, N]."""
     raw = np.ascontiguousarray(raw, dtype=np.uint32)
     N = raw.shape[-1]
     cnt = raw.size // N
@@ -202,6 +202,23 @@ def rowsel(db: np.ndarray, query: np.ndarray, qs, cols=None, threads: int | None
     out = np.empty((B, cols.size, 2, L, N), dtype=np.uint32)
     lib().orc_rowsel(N, L, _p32(q), D0, D1, B, _p32(db), _p32(query), cols.size, _p32(cols),
                      _p32(out), threads or default_threads())
+    return out
+
+
+def exppack(H: np.ndarray, C: np.ndarray, G: np.ndarray, qs, threads: int | None = None) -> np.ndarray:
+    """Ring-packing GEMM of expansion-based packing (VIPIR 3.5.2): out = H*C + (0|G).
+
+    H [Dr][n][L][N], C [B][n][2][L][N], G [B][Dr][L][N] (NTT form) ->
+    out [B][Dr][2][L][N] with out[b][r][c] = sum_k H[r][k] * C[b][k][c] point-wise,
+    plus G[b][r] on c = 1 (the polynomial carrying the message), mod q_l.
+    The product is the RowSel sum with the DB record (k, r) := H[r][k].
+    """
+    H = np.ascontiguousarray(H, dtype=np.uint32)
+    Dr, n, L, N = H.shape
+    db = np.ascontiguousarray(H.transpose(1, 0, 2, 3))           # record (k, r)
+    out = rowsel(db, C, qs, threads=threads)                       # [B][Dr][2][L][N]
+    q = np.asarray(qs, dtype=np.uint64).reshape(1, 1, -1, 1)
+    out[:, :, 1] = ((out[:, :, 1].astype(np.uint64) + np.asarray(G, dtype=np.uint64)) % q).astype(np.uint32)
     return out
 
 

@@ -33,6 +33,9 @@ T_QUERY = 2        # query ciphertexts [B][D0][2][L][N]
 T_SCALAR_DB = 3    # scalar-HE DB bytes [R][C]
 T_SCALAR_Q = 4     # scalar-HE query words [C][B]
 T_EXTRA = 5        # anything else a test needs
+T_HINT = 6         # ring-packing hint words, record order [n][Dr][N] (record (k, r) = H[r][k])
+T_SCAN_OUT = 7     # INT32 scan results read as polynomials [B][Dr][N]
+T_SPECIAL = 8      # expanded special ciphertexts [B][n][2][L][N] (NTT form)
 
 
 def splitmix64(x: np.ndarray) -> np.ndarray:
@@ -109,3 +112,20 @@ def raw_records(seed: int, D1: int, N: int, ks, ns) -> np.ndarray:
     t = np.arange(N, dtype=np.uint64).reshape(1, 1, -1)
     idx = (ks * np.uint64(D1) + ns) * np.uint64(N) + t
     return coeffs_at(seed, idx)
+
+
+def words_at(seed: int, idx: np.ndarray, tid: int) -> np.ndarray:
+    """The 32-bit words of tensor `tid` at the given flat indices (same values as `words`)."""
+    v = values(seed, tid, np.asarray(idx, dtype=np.uint64))
+    return (v >> np.uint64(32)).astype(np.uint32)
+
+
+def hint_records(seed: int, Dr: int, N: int, ks, rs) -> np.ndarray:
+    """Hint polynomials H[r][k] (plain words) for k in ks, r in rs: [len(ks)][len(rs)][N].
+
+    Record (k, r) of the n x Dr hint grid occupies flat indices ((k*Dr + r)*N + t).
+    """
+    ks = np.asarray(ks, dtype=np.uint64).reshape(-1, 1, 1)
+    rs = np.asarray(rs, dtype=np.uint64).reshape(1, -1, 1)
+    t = np.arange(N, dtype=np.uint64).reshape(1, 1, -1)
+    return words_at(seed, (ks * np.uint64(Dr) + rs) * np.uint64(N) + t, T_HINT)

@@ -293,6 +293,102 @@ def test_rowsel_linear_and_column_subset():
     assert np.array_equal(oracle.rowsel(db, query, qs, cols=cols), o1[:, cols.astype(int)])
 
 
+def test_encode_records_lifts_full_32bit_words():
+    """Plain 32-bit words (the scan output that becomes G, the hint that
+    becomes H) are lifted as integers: the transform of w equals the sum of
+    the transforms of its base-2^16 halves, w = lo + 2^16 hi, mod q."""
+    N, qs = 64, [7937, 7681]
+    psis = [oracle.min_psi(q, N) for q in qs]
+    w = synth.words(21, (3, N))
+    w[0, :4] = [0xFFFFFFFF, 0x80000000, 7937, 7681 * 7937]
+    lo, hi = w & 0xFFFF, w >> 16
+    e, elo, ehi = (oracle.encode_records(a, qs, psis) for a in (w, lo, hi))
+    for l, q in enumerate(qs):
+        want = (elo[:, l].astype(np.int64) + (1 << 16) % q * ehi[:, l].astype(np.int64)) % q
+        assert np.array_equal(e[:, l], want)
+        # and the constant term of the inverse is the word itself mod q
+        back = oracle.ntt_polys(e, qs, psis, inverse=True)
+        assert np.array_equal(back[:, l], (w.astype(np.int64) % q).astype(np.uint32))
+
+
+# ------------------------------------------------------------------ ExpPack GEMM
+def _tiny_exppack(seed, N=16, qs=(4513, 4481), Dr=3, n=4, B=2):
+    qs = list(qs)
+    L = len(qs)
+    H = synth.residues(seed, (Dr, n, L, N), qs)
+    C = synth.residues(seed + 1, (B, n, 2, L, N), qs)
+    G = synth.residues(seed + 2, (B, Dr, L, N), qs)
+    return qs, H, C, G
+
+
+def test_exppack_bruteforce_python_ints():
+    """out[b][r][c] = sum_k H[r][k] C[b][k][c] + [c == 1] G[b][r], point-wise mod q."""
+    qs, H, C, G = _tiny_exppack(31)
+    Dr, n, L, N = H.shape
+    B = C.shape[0]
+    out = oracle.exppack(H, C, G, qs)
+    assert out.shape == (B, Dr, 2, L, N)
+    for b in range(B):
+        for r in range(Dr):
+            for c in range(2):
+                for l in range(L):
+                    for j in range(N):
+                        s = sum(int(H[r, k, l, j]) * int(C[b, k, c, l, j]) for k in range(n))
+                        s += int(G[b, r, l, j]) if c == 1 else 0
+                        assert out[b, r, c, l, j] == s % qs[l]
+
+
+def test_exppack_zero_specials_returns_zero_and_g():
+    """C = 0 leaves the trivial ciphertexts (0, G_b) for every hint row."""
+    qs, H, C, G = _tiny_exppack(32)
+    out = oracle.exppack(H, np.zeros_like(C), G, qs)
+    assert (out[:, :, 0] == 0).all()
+    assert np.array_equal(out[:, :, 1], G)
+
+
+def test_exppack_packed_ciphertext_decrypts_to_g_minus_hs():
+    """The packing's purpose as a closed form.  With RLWE secret z and special
+    ciphertexts C_k = (a_k, -a_k z - s_k) (noise-free encryptions of -s_k,
+    ciphertext (c0, c1) decrypting as c1 + c0 z), the row-r output decrypts to
+    G_r - sum_k s_k H[r][k] in R_q: the LWE decryption b - <a, s> of the
+    scan result, for all N coefficients at once.  Products are checked in the
+    coefficient domain with the schoolbook negacyclic product."""
+    N, qs, Dr, n, B = 32, [7937, 7681], 3, 5, 2
+    L = len(qs)
+    psis = [oracle.min_psi(q, N) for q in qs]
+    rng = np.random.default_rng(33)
+    Hc = rng.integers(0, 1 << 32, (Dr, n, N), dtype=np.uint64).astype(np.uint32)   # hint words
+    Gc = rng.integers(0, 1 << 32, (B, Dr, N), dtype=np.uint64).astype(np.uint32)   # scan words
+    z = rng.integers(0, 3, N).astype(np.int64) - 1                               # ternary secret
+    s = rng.integers(0, 3, (B, n)).astype(np.int64) - 1                          # LWE secrets
+    a = rng.integers(0, 1 << 20, (B, n, N)).astype(np.int64)
+    C = np.zeros((B, n, 2, L, N), np.uint32)
+    for l, q in enumerate(qs):
+        zq = (z % q).astype(np.uint32)
+        for b in range(B):
+            for k in range(n):
+                ak = (a[b, k] % q).astype(np.uint32)
+                az = oracle.negacyclic_mul(ak, zq, q).astype(np.int64)
+                c1 = (-az) % q
+                c1[0] = (c1[0] - s[b, k]) % q
+                C[b, k, 0, l] = ak
+                C[b, k, 1, l] = c1.astype(np.uint32)
+    H = oracle.encode_records(Hc, qs, psis)                  # [Dr][n][L][N]
+    G = oracle.encode_records(Gc, qs, psis)                  # [B][Dr][L][N]
+    Cn = oracle.ntt_polys(C, qs, psis)
+    out = oracle.ntt_polys(oracle.exppack(H, Cn, G, qs), qs, psis, inverse=True)
+    for l, q in enumerate(qs):
+        zq = (z % q).astype(np.uint32)
+        for b in range(B):
+            for r in range(Dr):
+                dec = (out[b, r, 1, l].astype(np.int64)
+                       + oracle.negacyclic_mul(out[b, r, 0, l], zq, q)) % q
+                want = Gc[b, r].astype(np.int64)
+                for k in range(n):
+                    want = want - s[b, k] * Hc[r, k].astype(np.int64)
+                assert np.array_equal(dec, want % q)
+
+
 # ------------------------------------------------------------------ scalar scan
 def test_scalar_scan_against_numpy_matmul():
     R, C, B = 37, 300, 5
