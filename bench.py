@@ -50,6 +50,11 @@ WORKLOADS = {
     # scalar-HE scan: byte DB x 64 query words mod 2^32 (tcgen05 fp16 path)
     "scalar_16g": dict(kind="scalar", R=131072, C=131072, B=64,
                        desc="Scalar-HE scan: DB 131072 x 131072 uint8 (16 GiB) x Q 131072 x 64 uint32, mod 2^32"),
+    "scalar_16g_b1": dict(kind="scalar", R=131072, C=131072, B=1,
+                          desc="Scalar-HE scan, one query: DB 131072 x 131072 uint8 (16 GiB) x Q 131072 uint32, "
+                               "mod 2^32 (CUDA-core GEMV path)"),
+    "scalar_2g_b1_prof": dict(kind="scalar", R=16384, C=131072, B=1,
+                              desc="Scalar-HE scan profiling case, one query: DB 16384 x 131072 uint8 (2 GiB)"),
     "scalar_2g_prof": dict(kind="scalar", R=16384, C=131072, B=64,
                            desc="Scalar-HE scan profiling case: DB 16384 x 131072 uint8 (2 GiB), B=64"),
     # small case of the B=16 workload for profiler captures (3 GiB, tensor-core path)
@@ -431,20 +436,31 @@ def run_scalar(args, cfg):
         raise RuntimeError("device status word set")
     peaks, kind = measured_peaks()
     db_bytes = R * C
-    flops = 2.0 * R * C * 4 * 64        # fp16 multiply-adds on 4 digit planes x 64 query slots
-    tf = flops / (ms * 1e-3) / 1e12
+    if B <= 4:
+        # CUDA-core GEMV: bound by the HBM read of the DB (+ Q and the output)
+        algo = db_bytes + 4 * C * B + 4 * R * B
+        gbs = algo / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None, "kernel": "gemv_kernel",
+                "peak_source": "%s hbm_gbs (copy)" % kind, "algorithmic_bytes_per_launch": algo}
+        dtype = "u8 x u32 (4-way byte dot products, u32 wrap-around)"
+    else:
+        flops = 2.0 * R * C * 4 * 64        # fp16 multiply-adds on 4 digit planes x 64 query slots
+        tf = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": tf, "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
+                "frac": tf / float(peaks["bf16_tflops"]), "traffic": None, "kernel": "scalar_kernel",
+                "peak_source": "%s bf16_tflops (fp16 dense rate is the same)" % kind,
+                "hbm_frac": db_bytes / (ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"])}
+        dtype = "u8 x u32 (fp16 digits, fp32 accumulate)"
     line = {
         "metric": "scalar-HE scan: DB GB/s scanned", "value": db_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u8 x u32 (fp16 digits, fp32 accumulate)",
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic: seeded SplitMix64 bytes U[0,256), words U[0,2^32)",
         "config": {"workload": args.workload, "desc": cfg["desc"], "R": R, "C": C, "B": B,
                    "l2": "inputs larger than L2 (DB %.1f GiB), no flush" % (db_bytes / GIB)},
         "queries_per_s": B * 1e3 / ms,
-        "roofline": {"bound": "tensor", "achieved": tf, "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
-                     "frac": tf / float(peaks["bf16_tflops"]), "traffic": None, "kernel": "scalar_kernel",
-                     "peak_source": "%s bf16_tflops (fp16 dense rate is the same)" % kind,
-                     "hbm_frac": db_bytes / (ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"])},
+        "roofline": roof,
         "clocks": clk, "gpu_launches": 2 * args.steps, "e2e": None, "cpu_baseline": None,
     }
     if rank == 0:

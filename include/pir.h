@@ -228,15 +228,18 @@ uint64_t pir_scalar_workspace_bytes(uint64_t C, uint32_t B);
 /*
  * pir_scalar_scan — scalar-HE DB fold (VIPIR 2.5 and 4.1):
  *   out[r][b] = sum_{c<C} db[r][c] * Q[c][b]  mod 2^32
- * computed on the tensor cores with the 4-way byte split of Q
- * (Q = sum_i 2^(8i) Q_i, VIPIR 4.1).
+ * with the 4-way byte split of Q (Q = sum_i 2^(8i) Q_i, VIPIR 4.1).
+ * 5 <= B <= 64 runs on the tensor cores (exact fp16 digit products, 64
+ * queries per pass whatever B is); B <= 4 runs as a GEMV on the CUDA cores
+ * (4-way byte dot products, VIPIR's single-query case, bounded by the HBM
+ * read of the DB).  Results are identical either way.
  *   db  : device, [R][C] uint8 row-major (bytes are unsigned).
  *   Q   : device, [C][B] uint32.
- *   out : device, [R][B] uint32.
+ *   out : device, [R][B] uint32 (fully overwritten).
  *   workspace : device, >= pir_scalar_workspace_bytes(C, B) bytes, 128-byte
  *               aligned; scratch for the split query, contents undefined
  *               after the call.
- * Requirements: R % 128 == 0, C % 128 == 0, B == 64.
+ * Requirements: R >= 1, C % 64 == 0, 1 <= B <= 64, R and C <= 2^31.
  * Errors: PIR_ERR_ARG, PIR_ERR_UNSUPPORTED (shape outside the requirements),
  * PIR_ERR_CUDA.
  */

@@ -356,6 +356,186 @@ __global__ void __launch_bounds__(SC_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------- small batches on CUDA cores
+//
+// For a handful of queries the tensor path wastes its 64-query width: one
+// query costs as much as 64.  With B <= 4 the scan is a GEMV that the CUDA
+// cores finish under the HBM time of the DB, using the same byte split with
+// plain (unsigned) bytes of Q:
+//     sum_c db[r][c] Q[c][b] = sum_i 2^(8i) sum_c db[r][c] Q_i[c][b]  mod 2^32,
+// where each inner sum is a chain of 4-way byte dot products (dp4a).  An
+// inner sum may wrap past 2^32: only its value mod 2^(32-8i) reaches the
+// result, so the wrap is harmless.
+//
+// Query prep: for every 128 DB columns (a box) and query b, the 32 groups of
+// 4 columns each become 4 "plane words" (byte j of plane word i = byte i of
+// Q[4g + j][b]), 512 bytes per (box, query), stored box-major so that one
+// bulk copy stages all B queries of a box.  The prep also zeroes the output,
+// which the scan adds into.
+//
+// Scan: persistent CTAs, one per SM; the (256-row tile, 128-column box)
+// units are split into equal contiguous ranges in tile-major order.  Warp 8
+// (one thread) streams each unit's 256 x 128-byte DB box (TMA, 128-byte
+// swizzle) and its plane words into a 6-stage ring; warps 0-7 own one DB row
+// per thread and keep 4 x B running sums (the two column halves of a box in
+// separate sums for instruction-level parallelism).  When the range moves to
+// another row tile, or ends, each thread adds its combined sums into the
+// output with a 32-bit atomic add (mod 2^32, so the order is irrelevant).
+constexpr int GV_RT = 256;                     // DB rows per tile (one per consumer thread)
+constexpr int GV_KB = 128;                     // DB columns per box (the 128-byte swizzle span)
+constexpr int GV_NS = 6;                       // pipeline stages
+constexpr int GV_THREADS = GV_RT + 32;
+constexpr uint32_t GV_DB_BYTES = GV_RT * GV_KB;        // 32 KiB
+constexpr uint32_t GV_QBOX_BYTES = GV_KB * 4;          // plane words of one query for one box: 512 B
+constexpr uint32_t GV_MAX_B = 4;
+
+__global__ void __launch_bounds__(256) gemv_prep_kernel(const uint32_t *__restrict__ Q, uint64_t C, uint32_t B,
+                                                        uint32_t nkb, uint32_t *__restrict__ planes,
+                                                        uint32_t *__restrict__ out, uint64_t out_words) {
+    const uint64_t tid = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
+    const uint64_t nthr = (uint64_t)gridDim.x * blockDim.x;
+    const uint64_t groups = (uint64_t)nkb * B * (GV_KB / 4);   // (box, query, group of 4 columns)
+    for (uint64_t i = tid; i < groups; i += nthr) {
+        const uint32_t g = (uint32_t)(i % (GV_KB / 4));
+        const uint64_t kb_b = i / (GV_KB / 4);
+        const uint32_t b = (uint32_t)(kb_b % B);
+        const uint64_t c0 = (kb_b / B) * GV_KB + 4ull * g;
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = (c0 + j < C) ? Q[(c0 + j) * B + b] : 0u;
+        uint32_t pl[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            pl[p] = ((w[0] >> (8 * p)) & 0xFFu) | (((w[1] >> (8 * p)) & 0xFFu) << 8) |
+                    (((w[2] >> (8 * p)) & 0xFFu) << 16) | (((w[3] >> (8 * p)) & 0xFFu) << 24);
+        *reinterpret_cast<uint4 *>(planes + i * 4) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+    }
+    for (uint64_t i = tid; i < out_words; i += nthr) out[i] = 0u;
+}
+
+struct GemvArgs {
+    const uint8_t *planes;   // [nkb][B][32 groups][4 planes] words
+    uint32_t *out;           // [R][B], zeroed by the prep kernel
+    uint32_t *status;
+    uint64_t R;
+    uint64_t units;          // ntiles * nkb
+    uint32_t nkb;
+};
+
+template <int NB>
+__global__ void __launch_bounds__(GV_THREADS, 1)
+    gemv_kernel(const __grid_constant__ CUtensorMap dbmap, const __grid_constant__ GemvArgs A) {
+    constexpr uint32_t QB = NB * GV_QBOX_BYTES;
+    extern __shared__ uint8_t smraw[];
+    const uint32_t base_s = smem_u32(smraw);
+    uint8_t *sm = smraw + (((base_s + 1023u) & ~1023u) - base_s);   // 1 KiB alignment for the swizzle
+    uint8_t *stD = sm;                                                // [NS][256 rows x 128 B]
+    uint8_t *stQ = stD + GV_NS * GV_DB_BYTES;                         // [NS][NB x 512 B]
+    uint64_t *full = reinterpret_cast<uint64_t *>(stQ + GV_NS * QB);
+    uint64_t *empty = full + GV_NS;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < GV_NS; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, GV_RT / 32);
+        }
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const uint64_t u0 = A.units * blockIdx.x / gridDim.x, u1 = A.units * (blockIdx.x + 1) / gridDim.x;
+
+    if (warp == GV_RT / 32) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_db = policy_evict_first(), pol_q = policy_evict_last();
+            uint32_t it = 0;
+            for (uint64_t u = u0; u < u1; ++u, ++it) {
+                const uint32_t s = it % GV_NS, ph = (it / GV_NS) & 1;
+                if (abort_flag || !mbar_wait(empty + s, ph ^ 1, A.status)) {
+                    abort_flag = 1;
+                    continue;
+                }
+                const uint32_t kb = (uint32_t)(u % A.nkb);
+                const uint32_t t = (uint32_t)(u / A.nkb);
+                mbar_arrive_expect_tx(full + s, GV_DB_BYTES + QB);
+                tma_load_2d(stD + s * GV_DB_BYTES, &dbmap, (int)(kb * GV_KB), (int)(t * GV_RT), full + s, pol_db);
+                bulk_g2s(stQ + s * QB, A.planes + (uint64_t)kb * QB, QB, full + s, pol_q);
+            }
+            // copies in flight land in this CTA's shared memory: wait for the last ones
+            for (uint32_t i = 0; i < GV_NS && i < it; ++i) {
+                const uint32_t j = it - 1 - i;
+                mbar_wait(full + j % GV_NS, (j / GV_NS) & 1, A.status);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumers: one DB row per thread
+    const uint32_t r = threadIdx.x;
+    const uint32_t rsw = r & 7u;
+    uint32_t acc[NB][4][2];
+    auto clear = [&]() {
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) acc[b][p][0] = acc[b][p][1] = 0u;
+    };
+    auto flush = [&](uint64_t tile) {
+        const uint64_t row = tile * GV_RT + r;
+        if (row < A.R && !abort_flag) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                uint32_t v = 0;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) v += (acc[b][p][0] + acc[b][p][1]) << (8 * p);
+                atomicAdd(A.out + row * NB + b, v);
+            }
+        }
+    };
+    clear();
+    uint32_t it = 0;
+    uint64_t cur = u0 < u1 ? u0 / A.nkb : 0;
+    for (uint64_t u = u0; u < u1; ++u, ++it) {
+        const uint64_t tile = u / A.nkb;
+        if (tile != cur) {
+            flush(cur);
+            clear();
+            cur = tile;
+        }
+        const uint32_t s = it % GV_NS, ph = (it / GV_NS) & 1;
+        if (!abort_flag && !mbar_wait(full + s, ph, A.status)) abort_flag = 1;
+        if (!abort_flag) {
+            const uint8_t *rowp = stD + s * GV_DB_BYTES + (r >> 3) * 1024u + rsw * 128u;
+            const uint4 *q4 = reinterpret_cast<const uint4 *>(stQ + s * QB);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {   // 16-byte chunk j: columns 16j .. 16j+15
+                const uint4 d = *reinterpret_cast<const uint4 *>(rowp + ((j ^ rsw) << 4));
+                const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+#pragma unroll
+                    for (int gg = 0; gg < 4; ++gg) {   // group 4j + gg: its 4 plane words
+                        const uint4 q = q4[b * (GV_KB / 4) + 4 * j + gg];
+                        const int h = j >> 2;        // column half of the box: separate sums
+                        acc[b][0][h] = __dp4a(dw[gg], q.x, acc[b][0][h]);
+                        acc[b][1][h] = __dp4a(dw[gg], q.y, acc[b][1][h]);
+                        acc[b][2][h] = __dp4a(dw[gg], q.z, acc[b][2][h]);
+                        acc[b][3][h] = __dp4a(dw[gg], q.w, acc[b][3][h]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + s);
+    }
+    if (u0 < u1) flush(cur);
+}
+
+size_t gemv_smem_bytes(uint32_t B) { return 1024 + (size_t)GV_NS * (GV_DB_BYTES + B * GV_QBOX_BYTES) + 256; }
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_tiled() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -370,6 +550,57 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_tiled() {
 }
 
 size_t scalar_smem_bytes() { return 1024 + (size_t)SC_NS * SC_STAGE_BYTES + 256; }
+
+template <int NB>
+int gemv_launch(pir_ctx *ctx, const CUtensorMap &map, const GemvArgs &a, cudaStream_t st) {
+    static bool attr_set[64] = {};
+    const size_t smem = gemv_smem_bytes(NB);
+    if (ctx->device >= 0 && ctx->device < 64 && !attr_set[ctx->device]) {
+        if (cudaFuncSetAttribute(gemv_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return PIR_ERR_CUDA;
+        attr_set[ctx->device] = true;
+    }
+    const uint64_t grid = a.units < (uint64_t)ctx->num_sms ? a.units : (uint64_t)ctx->num_sms;
+    gemv_kernel<NB><<<(unsigned)grid, GV_THREADS, smem, st>>>(map, a);
+    return launch_status(cudaGetLastError());
+}
+
+// B <= 4 queries: plane-word prep (also zeroes out) + the CUDA-core scan.
+// The workspace holds nkb * B * 512 bytes, within pir_scalar_workspace_bytes.
+int scalar_gemv(pir_ctx *ctx, PFN_cuTensorMapEncodeTiled_v12000 encode, const uint8_t *db, uint64_t R,
+                uint64_t C, const uint32_t *Q, uint32_t B, uint32_t *out, void *workspace, cudaStream_t st) {
+    CUtensorMap map;
+    memset(&map, 0, sizeof(map));
+    const cuuint64_t gdim[2] = {C, R};
+    const cuuint64_t gstride[1] = {C};
+    const cuuint32_t box[2] = {GV_KB, GV_RT};
+    const cuuint32_t estride[2] = {1, 1};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(db), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PIR_ERR_ARG;
+    const uint32_t nkb = (uint32_t)((C + GV_KB - 1) / GV_KB);
+    const uint64_t ntiles = (R + GV_RT - 1) / GV_RT;
+    uint32_t *planes = reinterpret_cast<uint32_t *>(workspace);
+    const uint64_t work = (uint64_t)nkb * B * (GV_KB / 4);
+    const uint64_t prep_blocks = (work + 255) / 256 < 4096 ? (work + 255) / 256 : 4096;
+    gemv_prep_kernel<<<(unsigned)(prep_blocks ? prep_blocks : 1), 256, 0, st>>>(Q, C, B, nkb, planes, out, R * B);
+    if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
+    GemvArgs a;
+    a.planes = reinterpret_cast<const uint8_t *>(workspace);
+    a.out = out;
+    a.status = ctx->d_status;
+    a.R = R;
+    a.units = ntiles * nkb;
+    a.nkb = nkb;
+    switch (B) {
+        case 1: return gemv_launch<1>(ctx, map, a, st);
+        case 2: return gemv_launch<2>(ctx, map, a, st);
+        case 3: return gemv_launch<3>(ctx, map, a, st);
+        default: return gemv_launch<4>(ctx, map, a, st);
+    }
+}
 
 }  // namespace
 
@@ -390,6 +621,7 @@ extern "C" int pir_scalar_scan(pir_ctx *ctx, const uint8_t *db, uint64_t R, uint
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
     auto encode = get_encode_tiled();
     if (!encode) return PIR_ERR_CUDA;
+    if (B <= GV_MAX_B) return scalar_gemv(ctx, encode, db, R, C, Q, B, out, workspace, (cudaStream_t)stream);
 
     CUtensorMap map;
     memset(&map, 0, sizeof(map));

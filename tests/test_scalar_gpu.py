@@ -2,8 +2,10 @@
 
 Bit-exact against the oracle on small shapes (ragged row tiles, partial
 accumulator chunks, B < 64), on adversarial values that put every partial
-sum of the fp16/fp32 tensor-core path at its largest magnitude, and on
-sampled rows of the full 131072 x 131072 DB with B = 64.
+sum of the fp16/fp32 tensor-core path at its largest magnitude, on the
+CUDA-core GEMV used for B <= 4 (ragged tiles and boxes, row tiles split
+between CTAs, wrapping byte-plane sums), and on sampled rows of the full
+131072 x 131072 DB with B = 64 and B = 1.
 """
 import numpy as np
 import pytest
@@ -51,6 +53,48 @@ def test_scalar_scan_small(env, R, C, B):
     assert np.array_equal(_run(pir, ctx, db, Q), oracle.scalar_scan(db, Q))
 
 
+@pytest.mark.parametrize("R,C,B", [
+    (1, 64, 1),          # one row, half a box (columns zero-filled by TMA)
+    (256, 128, 1),       # exactly one unit
+    (300, 1088, 2),      # ragged row tile and column box
+    (1000, 8192, 3),     # many units: CTA ranges split row tiles (atomic partial sums)
+    (513, 4160, 4),      # B = 4, ragged both ways
+    (40000, 192, 1),     # more row tiles than CTAs, 2 boxes per tile
+])
+def test_scalar_gemv_small_batches(env, R, C, B):
+    """B <= 4: the CUDA-core GEMV path."""
+    pir, ctx = env
+    db = synth.db_bytes((R + C + B) % 251, (R, C))
+    Q = synth.words((R + C + 2 * B) % 251, (C, B))
+    assert np.array_equal(_run(pir, ctx, db, Q), oracle.scalar_scan(db, Q))
+
+
+@pytest.mark.parametrize("B", [1, 4])
+def test_scalar_gemv_wraparound(env, B):
+    """All-255 DB times all-ones words: every byte-plane sum wraps past 2^32
+    (C * 255 * 255 > 2^32 at C = 131072) and only its low bits may survive."""
+    pir, ctx = env
+    R, C = 300, 131072
+    db = np.full((R, C), 255, np.uint8)
+    Q = np.full((C, B), 0xFFFFFFFF, np.uint32)
+    got = _run(pir, ctx, db, Q)
+    assert (got == (255 * 0xFFFFFFFF * C) % (1 << 32)).all()
+
+
+def test_scalar_gemv_one_hot(env):
+    pir, ctx = env
+    R, C, B = 700, 4096, 4
+    db = synth.db_bytes(19, (R, C))
+    Q = np.zeros((C, B), np.uint32)
+    cols = [0, 127, 128, C - 1]
+    for b, c in enumerate(cols):
+        Q[c, b] = 0x01000001            # byte planes 0 and 3: db + (db << 24)
+    got = _run(pir, ctx, db, Q)
+    for b, c in enumerate(cols):
+        v = db[:, c].astype(np.uint64)
+        assert np.array_equal(got[:, b], ((v + (v << 24)) % (1 << 32)).astype(np.uint32))
+
+
 @pytest.mark.parametrize("qword", [0x7F7F7F80, 0x7F7F7F7F, 0xFFFFFFFF, 0x80808080])
 def test_scalar_scan_extreme_digits(env, qword):
     """DB all 255 with words whose balanced digits are all -128 (0x7F7F7F80) or
@@ -91,12 +135,14 @@ def test_scalar_scan_rejects_bad_shapes(env):
         pir.pir_scalar_scan(ctx, db, 128, 64 * 64, Q, 64, out, ws[: 1024])
 
 
-def test_scalar_scan_full_size_sampled_rows(env):
-    """131072 x 131072 byte DB (16 GiB), 64 queries: sampled rows vs the oracle."""
+@pytest.mark.parametrize("B", [SCALAR["B"], 1])
+def test_scalar_scan_full_size_sampled_rows(env, B):
+    """131072 x 131072 byte DB (16 GiB), 64 queries (tensor path) and one
+    query (CUDA-core GEMV): sampled rows vs the oracle."""
     import torch
     import synth.device as sd
     pir, ctx = env
-    R, C, B = SCALAR["R"], SCALAR["C"], SCALAR["B"]
+    R, C = SCALAR["R"], SCALAR["C"]
     seed = 7
     db_t = torch.empty(R * C, dtype=torch.uint8, device="cuda")
     sd.fill_bytes(db_t, seed, synth.T_SCALAR_DB)
