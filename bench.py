@@ -441,7 +441,8 @@ def run_scalar(args, cfg):
         algo = db_bytes + 4 * C * B + 4 * R * B
         gbs = algo / (ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
-                "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None, "kernel": "gemv_kernel",
+                "frac": gbs / float(peaks["hbm_gbs"]), "traffic": profile_traffic("gemv_kernel_" + args.workload),
+                "kernel": "gemv_kernel",
                 "peak_source": "%s hbm_gbs (copy)" % kind, "algorithmic_bytes_per_launch": algo}
         dtype = "u8 x u32 (4-way byte dot products, u32 wrap-around)"
     else:
