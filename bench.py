@@ -710,21 +710,40 @@ def run_ours(args, cfg):
     if status:
         raise RuntimeError("device status word set: %d" % status)
 
-    # ---- end to end through the public API: pinned host query in, result out
+    # ---- end to end through the public API: pinned host query in, result out.
+    # Coefficient-form workloads use the pipelined query server (copies of
+    # the neighbouring queries overlap each scan); NTT-form ones the plain
+    # sequence copy-in -> RowSel -> copy-out on one stream.
     q_host = torch.empty(srv.q_words, dtype=torch.int32, pin_memory=True)
     q_host.copy_(srv.q_coef.cpu())
-    o_host = torch.empty(srv.o_words, dtype=torch.int32, pin_memory=True)
+    o_host = [torch.empty(srv.o_words, dtype=torch.int32, pin_memory=True) for _ in range(2)]
     ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
-    result_buf = srv.o_coef if coeff else srv.o_ntt
+    e2e_ms, e2e_how = None, None
+    if ke and coeff:
+        server = pir.PirServer(ctx, db, D0, D1, B)
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            srv.q_coef.copy_(q_host, non_blocking=True)
-            step()
-            o_host.copy_(result_buf, non_blocking=True)
+        def serve(n, t0):
+            for i in range(t0, t0 + n):
+                if i >= 2:
+                    server.wait(i - 2)          # its result buffer is reused now
+                server.submit(q_host, o_host[i % 2])
+            server.wait(t0 + n - 1)
 
-    e2e_ms = None
-    if ke:
+        serve(3, 0)                              # warm-up
+        torch.cuda.synchronize()
+        server.mark(0)
+        serve(ke, 3)
+        server.mark(1)
+        e2e_ms = server.elapsed_ms() / ke
+        e2e_how = "pir_server: 2 queries in flight, copies on their own streams"
+        server.close()
+    elif ke:
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                srv.q_coef.copy_(q_host, non_blocking=True)
+                step()
+                o_host[0].copy_(srv.o_ntt, non_blocking=True)
+
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize()
@@ -736,6 +755,7 @@ def run_ours(args, cfg):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / ke
+        e2e_how = "copy-in, RowSel, copy-out on one stream"
 
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
@@ -769,7 +789,7 @@ def run_ours(args, cfg):
             "clocks": clk,
             "e2e": None if e2e_ms is None else {
                 "value": logical_db / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": q_bytes,
-                "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms, "how": e2e_how},
             "gpu_launches": args.steps * launches_per_step(cfg),
             "cpu_baseline": cpu,
         }

@@ -46,7 +46,7 @@ extern "C" {
 #define PIR_ERR_ARG (-1)          /* invalid argument (size, pointer, parameters) */
 #define PIR_ERR_CUDA (-2)         /* a CUDA runtime/driver call or launch failed */
 #define PIR_ERR_UNSUPPORTED (-3)  /* valid but outside what this build supports */
-#define PIR_ERR_ALLOC (-4)        /* pir_ctx_create could not allocate its tables */
+#define PIR_ERR_ALLOC (-4)        /* pir_ctx_create / pir_server_create could not allocate */
 
 /* Bits of the device status word (pir_status). */
 #define PIR_STATUS_TIMEOUT 1u     /* a bounded device wait ran out */
@@ -274,6 +274,53 @@ int pir_scalar_scan_noalloc(pir_ctx *ctx, const uint8_t *db, uint64_t R, uint64_
  * Synchronises the context's device.
  */
 int pir_status(pir_ctx *ctx, uint32_t *flags, int clear);
+
+/*
+ * pir_server — a query stream over a resident RowSel DB (GPIR section 2,
+ * the online phase NTT(query) -> RowSel -> INTT(result), once per query),
+ * with host-memory queries and results.  Copies run on their own streams
+ * and overlap the scan of the neighbouring queries: query i+1 is copied in
+ * and the result of query i-1 is copied out while query i is scanned.  The
+ * pages serve queries this way but do not specify the mechanism; this is
+ * the host runtime around the three calls.
+ *
+ * pir_server_create: device buffers for two queries in flight (2 x query,
+ *   2 x result, one NTT-domain query and result, the RowSel workspace:
+ *   about 3 x (query + result) bytes), three non-blocking streams, events.
+ *   db must stay valid and unchanged while the server exists; ctx must
+ *   outlive it.  Errors: PIR_ERR_ARG, PIR_ERR_CUDA, PIR_ERR_ALLOC.
+ * pir_server_destroy: waits for all submitted work, frees everything.
+ * pir_server_submit: enqueues one query; returns at once with its ticket
+ *   (0, 1, 2, ... in submission order).
+ *     host_query  : [B][D0][2][L][N] coefficient-form residues (as the
+ *                   input of pir_ntt_fwd); must stay unchanged until the
+ *                   query's result has arrived (pir_server_wait).
+ *     host_result : [B][D1][2][L][N] coefficient-form results; written by
+ *                   the time pir_server_wait(ticket) returns; must not be
+ *                   reused by a later submit before then.
+ *   Both should be page-locked (cudaHostAlloc / cudaHostRegister); pageable
+ *   memory works but its copies do not overlap.  The result slot of ticket
+ *   t is reused by ticket t + 2, so at most two results are in flight per
+ *   pair of host buffers the caller alternates.
+ * pir_server_wait: blocks until the result of `ticket` (and of every
+ *   earlier ticket) is in host memory; PIR_ERR_CUDA if a kernel reported a
+ *   device-side timeout (pir_status) or CUDA failed; PIR_ERR_ARG for a
+ *   ticket not yet submitted.
+ * pir_server_mark / pir_server_elapsed_ms: device-clock timing of a stretch
+ *   of the stream: mark(0) records a start event on the copy-in stream
+ *   (before the next submitted query's copy), mark(1) an end event on the
+ *   copy-out stream (after the last submitted result's copy); elapsed_ms
+ *   waits for the end event and returns the time between them.
+ */
+typedef struct pir_server pir_server;
+int pir_server_create(pir_server **srv, pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1,
+                      uint32_t B);
+void pir_server_destroy(pir_server *srv);
+int pir_server_submit(pir_server *srv, const uint32_t *host_query, uint32_t *host_result,
+                      uint64_t *ticket);
+int pir_server_wait(pir_server *srv, uint64_t ticket);
+int pir_server_mark(pir_server *srv, int which);
+int pir_server_elapsed_ms(pir_server *srv, float *ms);
 
 /* pir_strerror — static description of a return code. */
 const char *pir_strerror(int code);

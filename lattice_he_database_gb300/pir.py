@@ -71,6 +71,19 @@ def lib() -> ctypes.CDLL:
         L.pir_exppack.restype = ctypes.c_int
         L.pir_exppack.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, _vp, ctypes.c_uint32, _vp, _vp,
                                   ctypes.c_uint64, _vp]
+        L.pir_server_create.restype = ctypes.c_int
+        L.pir_server_create.argtypes = [ctypes.POINTER(_vp), _vp, _vp, ctypes.c_uint32, ctypes.c_uint32,
+                                        ctypes.c_uint32]
+        L.pir_server_destroy.restype = None
+        L.pir_server_destroy.argtypes = [_vp]
+        L.pir_server_submit.restype = ctypes.c_int
+        L.pir_server_submit.argtypes = [_vp, _vp, _vp, ctypes.POINTER(ctypes.c_uint64)]
+        L.pir_server_wait.restype = ctypes.c_int
+        L.pir_server_wait.argtypes = [_vp, ctypes.c_uint64]
+        L.pir_server_mark.restype = ctypes.c_int
+        L.pir_server_mark.argtypes = [_vp, ctypes.c_int]
+        L.pir_server_elapsed_ms.restype = ctypes.c_int
+        L.pir_server_elapsed_ms.argtypes = [_vp, ctypes.POINTER(ctypes.c_float)]
         L.pir_scalar_workspace_bytes.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
         L.pir_scalar_scan.restype = ctypes.c_int
         L.pir_scalar_scan.argtypes = [_vp, _vp, ctypes.c_uint64, ctypes.c_uint64, _vp, ctypes.c_uint32, _vp,
@@ -104,6 +117,16 @@ def _dev_ptr(t: torch.Tensor, itemsize: int, what: str) -> int:
         raise ValueError("%s must be contiguous" % what)
     if t.element_size() != itemsize:
         raise ValueError("%s must have %d-byte elements" % (what, itemsize))
+    return t.data_ptr()
+
+
+def _host_ptr(t: torch.Tensor, nbytes: int, what: str) -> int:
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError("%s must be a host tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError("%s holds %d bytes, needs %d" % (what, t.numel() * t.element_size(), nbytes))
     return t.data_ptr()
 
 
@@ -310,3 +333,50 @@ class RowselServer:
             self.answer_device()
             o_host.copy_(self.o_coef, non_blocking=True)
         return o_host
+
+
+class PirServer:
+    """Pipelined query stream over a resident RowSel DB (pir_server_*): host
+    queries in coefficient form go in, host results in coefficient form come
+    out; copies overlap the scans of neighbouring queries."""
+
+    def __init__(self, ctx: Ctx, db: torch.Tensor, D0: int, D1: int, B: int):
+        self.ctx, self.db, self.D0, self.D1, self.B = ctx, db, D0, D1, B
+        P = ctx.L * ctx.N
+        self.q_bytes = B * D0 * 2 * P * 4
+        self.o_bytes = B * D1 * 2 * P * 4
+        h = _vp()
+        _check(lib().pir_server_create(ctypes.byref(h), ctx, _dev_ptr(db, 4, "db"), D0, D1, B), "pir_server_create")
+        self.handle = h.value
+        self._keep = {}
+
+    def close(self):
+        if self.handle:
+            lib().pir_server_destroy(self.handle)
+            self.handle = None
+            self._keep.clear()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def submit(self, q_host: torch.Tensor, o_host: torch.Tensor) -> int:
+        t = ctypes.c_uint64()
+        _check(lib().pir_server_submit(self.handle, _host_ptr(q_host, self.q_bytes, "query"),
+                                       _host_ptr(o_host, self.o_bytes, "result"), ctypes.byref(t)),
+               "pir_server_submit")
+        self._keep[t.value % 2] = (q_host, o_host)   # host buffers stay referenced while in flight
+        return t.value
+
+    def wait(self, ticket: int):
+        _check(lib().pir_server_wait(self.handle, ticket), "pir_server_wait")
+
+    def mark(self, which: int):
+        _check(lib().pir_server_mark(self.handle, which), "pir_server_mark")
+
+    def elapsed_ms(self) -> float:
+        ms = ctypes.c_float()
+        _check(lib().pir_server_elapsed_ms(self.handle, ctypes.byref(ms)), "pir_server_elapsed_ms")
+        return float(ms.value)

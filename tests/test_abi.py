@@ -80,6 +80,11 @@ def test_error_strings_and_null_ctx(lib):
     assert lib.pir_rowsel_workspace_bytes(None, 4, 4, 1) == 0
     assert lib.pir_ntt_fwd(None, None, None, 1, None) == pir.PIR_ERR_ARG
     assert lib.pir_scalar_workspace_bytes(0, 64) == 0
+    h = ctypes.c_void_p()
+    assert lib.pir_server_create(ctypes.byref(h), None, None, 1, 1, 1) == pir.PIR_ERR_ARG and not h.value
+    assert lib.pir_server_submit(None, None, None, None) == pir.PIR_ERR_ARG
+    assert lib.pir_server_wait(None, 0) == pir.PIR_ERR_ARG
+    lib.pir_server_destroy(None)
 
 
 @pytest.mark.parametrize("N,L,D0,D1", [(16, 2, 3, 5), (16, 1, 2, 128), (16, 3, 4, 130), (4096, 3, 2, 1365)])
