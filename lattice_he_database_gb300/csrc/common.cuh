@@ -30,6 +30,7 @@ struct RnsParams {
     uint32_t r32[PIR_MAX_RNS];
     uint64_t mu[PIR_MAX_RNS];
     const uint32_t *tw;  // [L][4][N]: psi^brv(i), shoup, psi^-brv(i), shoup
+    uint32_t *status;    // the context's device status word (bounded waits report here)
 };
 
 RnsParams rns_params(const pir_ctx *ctx);
@@ -142,6 +143,10 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
+
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy / TMA) accesses of the same locations.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Barrier among `nthreads` threads (a multiple of 32) with hardware id `id`.
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {

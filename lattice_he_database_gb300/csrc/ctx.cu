@@ -109,6 +109,7 @@ RnsParams rns_params(const pir_ctx *ctx) {
         P.mu[l] = ctx->mu[l];
     }
     P.tw = ctx->d_tw;
+    P.status = ctx->d_status;
     return P;
 }
 

@@ -62,40 +62,55 @@ __device__ __forceinline__ uint32_t slab_width(const RowselArgs &A, uint32_t s) 
     return s == A.S - 1 ? A.Wlast : PIR_SLAB;
 }
 
+// Both transposes move 64 x 64-word tiles through shared memory (row pitch
+// 65 words) with 16-byte global accesses on both sides: 256 threads, each
+// loading four 16-byte pieces along one side and storing four along the
+// other.  P = L*N is a multiple of 16, PS and the outT row length Mv*D1p are
+// multiples of 4, so a 16-byte piece is either wholly inside or wholly out.
+constexpr int TT = 64;
+constexpr int TPITCH = TT + 1;
+
 // Transpose of the query into qT[p][k][m] (m = 2b + c relative to the pass's
-// first query b0; polynomials m >= Mv of the padded count are zero).  One
-// CTA moves a tile of 32 points x 32 (k, m) rows through shared memory so
-// that both the reads (along p) and the writes (along (k, m)) are coalesced.
+// first query b0; polynomials m >= Mv of the padded count are zero).  Column
+// r = k*Mp + m of qT is row ((b0 + m/2)*D0 + k)*2 + (m&1) of the query.
 __global__ void __launch_bounds__(256) transpose_query_kernel(const uint32_t *__restrict__ query,
                                                               uint32_t *__restrict__ qT, uint64_t P,
                                                               uint32_t D0, uint32_t Mp, uint32_t Mv,
                                                               uint32_t b0, uint32_t PS) {
-    __shared__ uint32_t tile[32][33];
-    const uint64_t p0 = (uint64_t)blockIdx.x * 32;
-    const uint32_t r0 = blockIdx.y * 32;
+    __shared__ uint32_t tile[TT][TPITCH];   // [r][p]
+    const uint64_t p0 = (uint64_t)blockIdx.x * TT;
+    const uint32_t r0 = blockIdx.y * TT;
     const uint32_t rows = D0 * Mp;
-    const uint32_t tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-    for (uint32_t i = ty; i < 32; i += 8) {
-        const uint32_t r = r0 + i;
-        const uint64_t p = p0 + tx;
-        uint32_t v = 0;
+    const uint32_t lo = threadIdx.x & 15, hi = threadIdx.x >> 4;   // 16 x 16
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t rr = hi + 16 * i, r = r0 + rr;
+        const uint64_t p = p0 + 4 * lo;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (r < rows && p < P) {
             const uint32_t k = r / Mp, m = r - k * Mp;
-            if (m < Mv) v = query[(((uint64_t)(b0 + (m >> 1)) * D0 + k) * 2 + (m & 1)) * P + p];
+            if (m < Mv)
+                v = *reinterpret_cast<const uint4 *>(query + (((uint64_t)(b0 + (m >> 1)) * D0 + k) * 2 + (m & 1)) * P + p);
         }
-        tile[i][tx] = v;
+        uint32_t *t = &tile[rr][4 * lo];
+        t[0] = v.x; t[1] = v.y; t[2] = v.z; t[3] = v.w;
     }
     __syncthreads();
-    for (uint32_t j = ty; j < 32; j += 8) {
-        const uint64_t p = p0 + j;
-        const uint32_t r = r0 + tx;
-        if (p < P && r < PS) qT[p * PS + r] = r < rows ? tile[tx][j] : 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t pp = hi + 16 * i;
+        const uint64_t p = p0 + pp;
+        const uint32_t r = r0 + 4 * lo;
+        if (p < P && r < PS)
+            *reinterpret_cast<uint4 *>(qT + p * PS + r) =
+                make_uint4(tile[4 * lo][pp], tile[4 * lo + 1][pp], tile[4 * lo + 2][pp], tile[4 * lo + 3][pp]);
     }
 }
 
-// Results of a pass from the point-major block outT[p][m][n] (row length
-// D1p) to out[b][n][c][p] (m = 2(b - b0) + c): a tile of 32 points x 32
-// (m, n) rows moves through shared memory, coalesced on both sides.
+// Results of a pass from the point-major block outT[p][w] (w = m*D1p + n,
+// row length W = Mv*D1p) to out[b][n][c][p] (m = 2(b - b0) + c); padding
+// columns n >= D1 are dropped.  With an addend G (ring packing), G[b][n]
+// joins polynomial c = 1 of every ciphertext.
 struct AddendArgs {
     const uint32_t *G;       // [B][D1][L][N] residues added to polynomial c = 1, or null
     uint32_t N;
@@ -106,36 +121,43 @@ __global__ void __launch_bounds__(256) transpose_out_kernel(const uint32_t *__re
                                                             uint32_t *__restrict__ out, uint64_t P, uint32_t D1,
                                                             uint32_t D1p, uint32_t Mv, uint32_t b0,
                                                             const __grid_constant__ AddendArgs add) {
-    __shared__ uint32_t tile[32][33];
-    const uint64_t p0 = (uint64_t)blockIdx.x * 32;
-    const uint32_t r0 = blockIdx.y * 32;            // row r = m * D1 + n
-    const uint32_t rows = Mv * D1;
-    const uint32_t tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    for (uint32_t j = ty; j < 32; j += 8) {
-        const uint64_t p = p0 + j;
-        const uint32_t r = r0 + tx;
-        uint32_t v = 0;
-        if (p < P && r < rows) {
-            const uint32_t m = r / D1, n = r - m * D1;
-            v = outT[(p * Mv + m) * D1p + n];
-        }
-        tile[j][tx] = v;
+    __shared__ uint32_t tile[TT][TPITCH];   // [w][p]
+    const uint64_t p0 = (uint64_t)blockIdx.x * TT;
+    const uint32_t w0 = blockIdx.y * TT;
+    const uint32_t W = Mv * D1p;
+    const uint32_t lo = threadIdx.x & 15, hi = threadIdx.x >> 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t pp = hi + 16 * i;
+        const uint64_t p = p0 + pp;
+        const uint32_t w = w0 + 4 * lo;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (p < P && w < W) v = *reinterpret_cast<const uint4 *>(outT + p * W + w);
+        tile[4 * lo][pp] = v.x;
+        tile[4 * lo + 1][pp] = v.y;
+        tile[4 * lo + 2][pp] = v.z;
+        tile[4 * lo + 3][pp] = v.w;
     }
     __syncthreads();
-    for (uint32_t i = ty; i < 32; i += 8) {
-        const uint32_t r = r0 + i;
-        const uint64_t p = p0 + tx;
-        if (r < rows && p < P) {
-            const uint32_t m = r / D1, n = r - m * D1;
-            const uint64_t b = b0 + (m >> 1);
-            uint32_t v = tile[tx][i];
-            if (add.G && (m & 1)) {  // (0 | G): the second polynomial of each ciphertext
-                const uint32_t q = add.q[p / add.N];
-                v += add.G[(b * D1 + n) * P + p];
-                v = v >= q ? v - q : v;
-            }
-            out[((b * D1 + n) * 2 + (m & 1)) * P + p] = v;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t ww = hi + 16 * i, w = w0 + ww;
+        const uint64_t p = p0 + 4 * lo;
+        if (w >= W || p >= P) continue;
+        const uint32_t m = w / D1p, n = w - m * D1p;
+        if (n >= D1) continue;
+        const uint64_t b = b0 + (m >> 1);
+        const uint32_t *t = &tile[ww][4 * lo];
+        uint4 v = make_uint4(t[0], t[1], t[2], t[3]);
+        if (add.G && (m & 1)) {  // (0 | G): the second polynomial of each ciphertext
+            const uint32_t q = add.q[p / add.N];   // 4 consecutive points share a prime (N >= 16)
+            const uint4 g = *reinterpret_cast<const uint4 *>(add.G + (b * D1 + n) * P + p);
+            v.x += g.x; v.x = v.x >= q ? v.x - q : v.x;
+            v.y += g.y; v.y = v.y >= q ? v.y - q : v.y;
+            v.z += g.z; v.z = v.z >= q ? v.z - q : v.z;
+            v.w += g.w; v.w = v.w >= q ? v.w - q : v.w;
         }
+        *reinterpret_cast<uint4 *>(out + ((b * D1 + n) * 2 + (m & 1)) * P + p) = v;
     }
 }
 
@@ -475,7 +497,7 @@ int rowsel_impl(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, cons
         A.Mp = padded_mp(A.Mv);
         A.PS = (D0 * A.Mp + 3) / 4 * 4;
         // the pass's query slices, point-major
-        const dim3 tgrid((unsigned)((A.P + 31) / 32), (A.PS + 31) / 32);
+        const dim3 tgrid((unsigned)((A.P + TT - 1) / TT), (A.PS + TT - 1) / TT);
         uint32_t *qT = reinterpret_cast<uint32_t *>(workspace);
         transpose_query_kernel<<<tgrid, 256, 0, st>>>(query, qT, A.P, D0, A.Mp, A.Mv, b0, A.PS);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
@@ -504,7 +526,7 @@ int rowsel_impl(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, cons
         add.G = G;
         add.N = ctx->N;
         for (uint32_t l = 0; l < ctx->L; ++l) add.q[l] = ctx->q[l];
-        const dim3 ogrid((unsigned)((A.P + 31) / 32), (A.Mv * D1 + 31) / 32);
+        const dim3 ogrid((unsigned)((A.P + TT - 1) / TT), (A.Mv * A.D1p + TT - 1) / TT);
         transpose_out_kernel<<<ogrid, 256, 0, st>>>(A.outT, out, A.P, D1, A.D1p, A.Mv, b0, add);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
     }
