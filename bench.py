@@ -185,77 +185,135 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- oracle (CPU) leg
-ORACLE_POINTS = 4096   # evaluation points per oracle sample (of L*N = 12288)
+# Every oracle sample has a bounded size (host memory is not sized for the
+# workloads) and is repeated until its time budget is spent.
+SAMPLE_WORDS = 1 << 26   # at most 64 Mi DB (or hint) words per oracle sample
 
 
-def _oracle_rowsel_inputs(cfg, ncols):
-    import oracle
-    import synth
-    N, D0, B = cfg["N"], cfg["D0"], cfg["B"]
-    q0 = oracle.primes(N, 1)[0]
-    db = synth.residues(11, (D0, ncols, 1, ORACLE_POINTS), [q0], tid=synth.T_EXTRA)
-    qu = synth.residues(12, (B, D0, 2, 1, ORACLE_POINTS), [q0], tid=synth.T_EXTRA)
-    return q0, db, qu
+def sample_points(words_per_point: int) -> int:
+    """Evaluation points (prime 0) of a sample: a multiple of 16 in [16, 4096]."""
+    pts = SAMPLE_WORDS // max(1, words_per_point)
+    return max(16, min(4096, pts // 16 * 16))
 
 
-def oracle_rowsel_calibrate(cfg, seconds: float):
-    """Columns per oracle call so that one call takes about `seconds` on all host cores."""
-    import oracle
-    threads = oracle.default_threads()
-    q0, db, qu = _oracle_rowsel_inputs(cfg, threads)
+def repeat_for(fn, seconds: float):
+    """Calls fn until `seconds` have passed (at least once): (calls, seconds taken)."""
+    calls, t = 0, time.perf_counter()
+    while True:
+        fn()
+        calls += 1
+        dt = time.perf_counter() - t
+        if dt >= seconds:
+            return calls, dt
+
+
+def calls_per_step(fn, seconds: float) -> int:
+    """How many calls of fn fill about `seconds` (one timed call after a warm one)."""
+    fn()
     t = time.perf_counter()
-    oracle.rowsel(db, qu, [q0], threads=threads)
-    t1 = time.perf_counter() - t
-    ncols = threads * max(1, int(seconds / max(t1, 1e-4)))
-    return min(ncols, cfg["D1"]), threads
+    fn()
+    return max(1, int(round(seconds / max(time.perf_counter() - t, 1e-4))))
 
 
-def oracle_rowsel_sample(cfg, budget_s: float):
-    """Time the oracle RowSel on a bounded sample: all D0 rows and B queries,
-    ORACLE_POINTS evaluation points (prime 0) and a calibrated number of DB
-    columns.  Returns (GB/s, threads, description, seconds)."""
-    import oracle
-    ncols, threads = oracle_rowsel_calibrate(cfg, budget_s)
-    q0, db, qu = _oracle_rowsel_inputs(cfg, ncols)
-    t = time.perf_counter()
-    oracle.rowsel(db, qu, [q0], threads=threads)
-    dt = time.perf_counter() - t
-    nbytes = cfg["D0"] * ncols * ORACLE_POINTS * 4
-    desc = ("oracle RowSel on %d of %d DB columns x %d of %d evaluation points, all %d rows, B=%d"
-            % (ncols, cfg["D1"], ORACLE_POINTS, cfg["L"] * cfg["N"], cfg["D0"], cfg["B"]))
-    return nbytes / dt / 1e9, threads, desc, dt
+class RowselSample:
+    """Oracle RowSel on a bounded sample of a workload: all D0 rows and B
+    queries, one column per host thread, as many evaluation points of prime 0
+    as the sample size allows."""
+
+    def __init__(self, cfg):
+        import oracle
+        import synth
+        N, D0, B = cfg["N"], cfg["D0"], cfg["B"]
+        self.threads = oracle.default_threads()
+        self.ncols = min(cfg["D1"], self.threads)
+        self.pts = sample_points(D0 * self.ncols)
+        self.q0 = oracle.primes(N, 1)[0]
+        self.db = synth.residues(11, (D0, self.ncols, 1, self.pts), [self.q0], tid=synth.T_EXTRA)
+        self.qu = synth.residues(12, (B, D0, 2, 1, self.pts), [self.q0], tid=synth.T_EXTRA)
+        self.nbytes = D0 * self.ncols * self.pts * 4
+        self.desc = ("oracle RowSel on %d of %d DB columns x %d of %d evaluation points, all %d rows, B=%d"
+                     % (self.ncols, cfg["D1"], self.pts, cfg["L"] * N, D0, B))
+
+    def __call__(self):
+        import oracle
+        oracle.rowsel(self.db, self.qu, [self.q0], threads=self.threads)
 
 
-def run_reference_scalar(args, cfg):
-    """Reference arm for the scalar scan: the oracle on a bounded row sample."""
-    import oracle
-    import synth
-    R, C, B = cfg["R"], cfg["C"], cfg["B"]
-    threads = oracle.default_threads()
-    Q = synth.words(7, (C, B))
-    rows = threads
-    db = synth.db_bytes(7, (rows, C))
-    t = time.perf_counter()
-    oracle.scalar_scan(db, Q, threads=threads)
-    t1 = time.perf_counter() - t
+class ExppackSample:
+    """Oracle ring-packing GEMM on a bounded sample: all n hint columns and B
+    clients, one hint row per host thread, evaluation points of prime 0."""
+
+    def __init__(self, cfg):
+        import oracle
+        import synth
+        n, B = cfg["n"], cfg["B"]
+        self.threads = oracle.default_threads()
+        self.rows = min(cfg["Dr"], self.threads)
+        self.pts = sample_points(n * self.rows)
+        self.q0 = oracle.primes(cfg["N"], 1)[0]
+        self.H = synth.residues(11, (self.rows, n, 1, self.pts), [self.q0], tid=synth.T_EXTRA)
+        self.C = synth.residues(12, (B, n, 2, 1, self.pts), [self.q0], tid=synth.T_EXTRA)
+        self.G = synth.residues(13, (B, self.rows, 1, self.pts), [self.q0], tid=synth.T_EXTRA)
+        self.nbytes = self.rows * n * self.pts * 4
+        self.desc = ("oracle ExpPack GEMM on %d of %d hint rows x %d of %d evaluation points, all n=%d, B=%d"
+                     % (self.rows, cfg["Dr"], self.pts, cfg["L"] * cfg["N"], n, B))
+
+    def __call__(self):
+        import oracle
+        oracle.exppack(self.H, self.C, self.G, [self.q0], threads=self.threads)
+
+
+class ScalarSample:
+    """Oracle scalar scan on a bounded sample: one DB row per host thread
+    (all C columns) against the full query matrix."""
+
+    def __init__(self, cfg):
+        import oracle
+        import synth
+        R, C, B = cfg["R"], cfg["C"], cfg["B"]
+        self.threads = oracle.default_threads()
+        self.rows = min(R, self.threads)
+        self.Q = synth.words(7, (C, B))
+        self.db = synth.db_bytes(7, (self.rows, C))
+        self.nbytes = self.rows * C
+        self.desc = "oracle scalar scan on %d of %d DB rows x %d columns, B=%d" % (self.rows, R, C, B)
+
+    def __call__(self):
+        import oracle
+        oracle.scalar_scan(self.db, self.Q, threads=self.threads)
+
+
+def oracle_baseline(sample, seconds: float):
+    """cpu_baseline object: the sample repeated for about `seconds`."""
+    sample()                                   # first touch of the inputs
+    calls, dt = repeat_for(sample, seconds)
+    return {"value": sample.nbytes * calls / dt / 1e9, "unit": "GB/s", "cores": sample.threads, "kind": "oracle",
+            "sample": "%s; %d calls in %.1f s" % (sample.desc, calls, dt), "seconds": round(dt, 2)}
+
+
+def run_reference_sample(args, sample, metric, dtype, data, desc):
+    """Reference arm: each step repeats the bounded oracle sample for about
+    120 s / (steps + warmup) on all host cores."""
     per_step = 120.0 / max(1, args.steps + args.warmup)
-    rows = max(threads, threads * int(per_step / max(t1, 1e-4)))
-    rows = min(rows, R)
-    db = synth.db_bytes(7, (rows, C))
+    reps = calls_per_step(sample, per_step)
+
+    def one_step():
+        for _ in range(reps):
+            sample()
+
     for _ in range(args.warmup):
-        oracle.scalar_scan(db, Q, threads=threads)
+        one_step()
     t = time.perf_counter()
     for _ in range(args.steps):
-        oracle.scalar_scan(db, Q, threads=threads)
+        one_step()
     dt = (time.perf_counter() - t) / max(1, args.steps)
-    value = rows * C / dt / 1e9
-    sample = "oracle scalar scan per step: %d of %d DB rows x %d columns, B=%d" % (rows, R, C, B)
+    value = sample.nbytes * reps / dt / 1e9
     line = {
-        "impl": "reference", "metric": "scalar-HE scan: DB GB/s scanned", "value": value, "unit": "GB/s",
-        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8 x u32",
-        "data": "synthetic", "config": {"workload": args.workload, "desc": cfg["desc"]},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "impl": "reference", "metric": metric, "value": value, "unit": "GB/s", "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype, "data": data, "config": {"workload": args.workload, "desc": desc},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": sample.threads, "kind": "oracle",
+                         "sample": "per step %d calls of: %s" % (reps, sample.desc)},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -263,105 +321,19 @@ def run_reference_scalar(args, cfg):
 
 def run_reference(args, cfg):
     """Reference arm: the oracle as it stands, timed on the host cores."""
-    import oracle
-    import synth
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    if cfg.get("kind") == "scalar":
-        return run_reference_scalar(args, cfg)
-    if cfg.get("kind") == "exppack":
-        return run_reference_exppack(args, cfg)
-    per_step = 120.0 / max(1, args.steps + args.warmup)
-    ncols, threads = oracle_rowsel_calibrate(cfg, per_step)
-    q0, db, qu = _oracle_rowsel_inputs(cfg, ncols)
-    for _ in range(args.warmup):
-        oracle.rowsel(db, qu, [q0], threads=threads)
-    t = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.rowsel(db, qu, [q0], threads=threads)
-    dt = (time.perf_counter() - t) / max(1, args.steps)
-    N, D0, B = cfg["N"], cfg["D0"], cfg["B"]
-    nbytes = D0 * ncols * ORACLE_POINTS * 4
-    value = nbytes / dt / 1e9
-    sample = ("oracle RowSel per step: %d of %d DB columns x %d of %d evaluation points, all %d rows, B=%d"
-              % (ncols, cfg["D1"], ORACLE_POINTS, cfg["L"] * N, D0, B))
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "u32", "data": "synthetic (seeded SplitMix64 residues)",
-        "config": {"workload": args.workload, "desc": cfg["desc"]},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "queries_per_s": None,
-    }
-    print(json.dumps(line), flush=True)
-
-
-def _oracle_exppack_inputs(cfg, rows):
-    import oracle
-    import synth
-    n, B = cfg["n"], cfg["B"]
-    q0 = oracle.primes(cfg["N"], 1)[0]
-    H = synth.residues(11, (rows, n, 1, ORACLE_POINTS), [q0], tid=synth.T_EXTRA)
-    C = synth.residues(12, (B, n, 2, 1, ORACLE_POINTS), [q0], tid=synth.T_EXTRA)
-    G = synth.residues(13, (B, rows, 1, ORACLE_POINTS), [q0], tid=synth.T_EXTRA)
-    return q0, H, C, G
-
-
-def oracle_exppack_calibrate(cfg, seconds: float):
-    """Hint rows per oracle call so that one call takes about `seconds` on all host cores."""
-    import oracle
-    threads = oracle.default_threads()
-    q0, H, C, G = _oracle_exppack_inputs(cfg, threads)
-    t = time.perf_counter()
-    oracle.exppack(H, C, G, [q0], threads=threads)
-    t1 = time.perf_counter() - t
-    return min(cfg["Dr"], threads * max(1, int(seconds / max(t1, 1e-4)))), threads
-
-
-def oracle_exppack_sample(cfg, budget_s: float):
-    """Time the oracle ring-packing GEMM on a bounded sample: all n hint
-    columns and B clients, ORACLE_POINTS evaluation points of prime 0 and a
-    calibrated number of hint rows.  Returns (GB/s, threads, description, seconds)."""
-    import oracle
-    rows, threads = oracle_exppack_calibrate(cfg, budget_s)
-    q0, H, C, G = _oracle_exppack_inputs(cfg, rows)
-    t = time.perf_counter()
-    oracle.exppack(H, C, G, [q0], threads=threads)
-    dt = time.perf_counter() - t
-    desc = ("oracle ExpPack GEMM on %d of %d hint rows x %d of %d evaluation points, all n=%d, B=%d"
-            % (rows, cfg["Dr"], ORACLE_POINTS, cfg["L"] * cfg["N"], cfg["n"], cfg["B"]))
-    return rows * cfg["n"] * ORACLE_POINTS * 4 / dt / 1e9, threads, desc, dt
-
-
-def run_reference_exppack(args, cfg):
-    """Reference arm for the ring-packing GEMM: the oracle on a bounded sample
-    (all n hint columns and B clients, ORACLE_POINTS evaluation points of
-    prime 0, a calibrated number of hint rows)."""
-    import oracle
-    n, Dr, B, N = cfg["n"], cfg["Dr"], cfg["B"], cfg["N"]
-    per_step = 120.0 / max(1, args.steps + args.warmup)
-    rows, threads = oracle_exppack_calibrate(cfg, per_step)
-    q0, H, C, G = _oracle_exppack_inputs(cfg, rows)
-    for _ in range(args.warmup):
-        oracle.exppack(H, C, G, [q0], threads=threads)
-    t = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.exppack(H, C, G, [q0], threads=threads)
-    dt = (time.perf_counter() - t) / max(1, args.steps)
-    value = rows * n * ORACLE_POINTS * 4 / dt / 1e9
-    sample = ("oracle ExpPack GEMM per step: %d of %d hint rows x %d of %d evaluation points, all n=%d, B=%d"
-              % (rows, Dr, ORACLE_POINTS, cfg["L"] * N, n, B))
-    line = {
-        "impl": "reference", "metric": EXPPACK_METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic (seeded SplitMix64 residues)",
-        "config": {"workload": args.workload, "desc": cfg["desc"]},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
+    kind = cfg.get("kind")
+    if kind == "scalar":
+        run_reference_sample(args, ScalarSample(cfg), "scalar-HE scan: DB GB/s scanned", "u8 x u32",
+                             "synthetic", cfg["desc"])
+    elif kind == "exppack":
+        run_reference_sample(args, ExppackSample(cfg), EXPPACK_METRIC, "u32",
+                             "synthetic (seeded SplitMix64 residues)", cfg["desc"])
+    else:
+        run_reference_sample(args, RowselSample(cfg), METRIC, "u32", "synthetic (seeded SplitMix64 residues)",
+                             cfg["desc"])
 
 
 # ---------------------------------------------------------------- GPU leg
@@ -465,6 +437,8 @@ def run_scalar(args, cfg):
         "clocks": clk, "gpu_launches": 2 * args.steps, "e2e": None, "cpu_baseline": None,
     }
     if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = oracle_baseline(ScalarSample(cfg), args.cpu_seconds)
         print(json.dumps(line), flush=True)
     ctx.close()
     return line
@@ -603,9 +577,7 @@ def run_exppack(args, cfg):
             "cpu_baseline": None,
         }
         if not args.no_cpu_baseline and world == 1:
-            gbs, threads, desc, secs = oracle_exppack_sample(cfg, args.cpu_seconds)
-            line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                                    "sample": desc, "seconds": round(secs, 2)}
+            line["cpu_baseline"] = oracle_baseline(ExppackSample(cfg), args.cpu_seconds)
         print(json.dumps(line), flush=True)
         result = line
     ctx.close()
@@ -766,9 +738,7 @@ def run_ours(args, cfg):
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            gbs, threads, desc, secs = oracle_rowsel_sample(cfg, args.cpu_seconds)
-            cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
-                   "seconds": round(secs, 2)}
+            cpu = oracle_baseline(RowselSample(cfg), args.cpu_seconds)
         value = aggregate_throughput(logical_db, args.steps, ms_total, world) / 1e9
         result = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

@@ -185,7 +185,10 @@ uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t D1
  *               contents undefined after the call.
  * The DB is read from HBM once per pass; a pass covers as many queries as
  * fit the on-chip query buffer (16 queries for D0 <= 896, fewer for larger
- * D0); larger batches take ceil(B / per-pass) passes.
+ * D0); larger batches take ceil(B / per-pass) passes.  A pass of 9 to 16
+ * queries with D0 <= 512 and every q_l >= 2^26 runs on the tensor cores
+ * (exact fp16 digit products); every other pass on the CUDA cores.  Both
+ * give the same canonical residues.
  * Errors: PIR_ERR_ARG (zero sizes, NULL/unaligned, workspace too small),
  * PIR_ERR_CUDA, PIR_ERR_UNSUPPORTED (D0 > 14336).
  */

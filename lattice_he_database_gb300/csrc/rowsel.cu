@@ -414,7 +414,7 @@ uint32_t padded_mp(uint32_t Mv) {
 }  // namespace
 
 // Tensor-core path for large batches (rowsel_tc.cu).
-bool rowsel_tc_eligible(uint32_t D0, uint32_t Mv);
+bool rowsel_tc_eligible(const pir_ctx *ctx, uint32_t D0, uint32_t Mv);
 int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *qT, uint32_t PS,
                    uint32_t Mv, uint32_t *outT, cudaStream_t st);
 
@@ -502,7 +502,7 @@ int rowsel_impl(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, cons
         transpose_query_kernel<<<tgrid, 256, 0, st>>>(query, qT, A.P, D0, A.Mp, A.Mv, b0, A.PS);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
         int rc = PIR_OK;
-        if (rowsel_tc_eligible(D0, A.Mv)) {  // 17..32 polynomials: exact fp16 tensor-core GEMMs
+        if (rowsel_tc_eligible(ctx, D0, A.Mv)) {  // 17..32 polynomials, q >= 2^26: exact fp16 tensor-core GEMMs
             rc = rowsel_tc_pass(ctx, db, D0, D1, qT, A.PS, A.Mv, A.outT, st);
         // thread tile MT polynomials x 4 columns; warps split the padded
         // polynomials (msplit) and the rows of a chunk (ksplit >= 2)

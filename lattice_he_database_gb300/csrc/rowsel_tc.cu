@@ -21,18 +21,26 @@
 //     out[m][n] = sum_i 2^(8i) (sum_j 2^(8j) S_ij[m][n])  mod q
 // with one 64-bit Barrett reduction per (i, m, n) and a cross-plane sum.
 //
-// Warp roles (448 threads, one CTA per SM, persistent over a range of points):
+// Warp roles (512 threads, one CTA per SM, persistent over a range of points).
+// A warp's scheduler is fixed by warp % 4, and the MMA-issuing thread loses
+// most of its issue rate to any ALU-busy warp on its scheduler, so scheduler 1
+// carries only light roles besides the plane-1 epilogue:
 //   warps 0-3   query digits of the next point -> TMEM (tcgen05.st), warp w
 //               writes digit plane w into TMEM lanes 32w..32w+31, from the
 //               point's query slice that the producer bulk-copies into
 //               shared memory while the previous point is still in flight;
 //   warps 4-7   epilogue: tcgen05.ld of a finished accumulator, reduction,
 //               cross-plane sum through shared memory, output stores;
-//   warps 8-11  converters: 64 x 32 DB words (TMA-staged) -> 4 byte planes
-//               of fp16 in the 128B-swizzled K-major layout of the B operand;
-//   warp 12     TMEM allocation and the TMA producer of query slices and DB
-//               word tiles;
+//   converters  three groups of three warps, {0, 2, 3}, {8, 10, 11} and
+//               {12, 14, 15}, each converting every third stage: 64 x 32 DB
+//               words (TMA-staged) -> 4 byte planes of fp16 in the
+//               128B-swizzled K-major layout of the B operand;
+//   warp 9      TMEM allocation and the TMA producer of query slices and DB
+//               word tiles (with L2 prefetches one slab ahead);
 //   warp 13     MMA issue (one thread).
+// DB word stages (TMA -> converters) and fp16 operand stages (converters ->
+// MMA) are separate rings, so a word stage is refilled as soon as it has
+// been read.
 // All mbarrier waits are bounded; TMEM is always released.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -44,26 +52,30 @@
 
 namespace {
 
-constexpr int TC_NS = 6;                       // pipeline stages
+constexpr int TC_NR = 10;                      // DB word stages (TMA -> converters)
+constexpr int TC_NB = 4;                       // fp16 operand stages (converters -> MMA)
 constexpr int TC_KS = 64;                      // DB rows (K) per stage
 constexpr int TC_NT = 32;                      // DB columns per MMA tile
 constexpr uint32_t TC_RAW_BYTES = TC_KS * TC_NT * 4;   // 8 KiB of DB words
 constexpr uint32_t TC_B_BYTES = 128 * 128;             // 128 rows x 64 fp16
-constexpr int TC_THREADS = 14 * 32;
+constexpr int TC_THREADS = 16 * 32;
 constexpr uint32_t TC_TMEM_COLS = 512;
 constexpr uint32_t TC_ACC_COL = 256;           // accumulators at columns 256 and 384
 constexpr uint32_t TC_MAX_D0 = 512;            // exactness bound of one fp32 accumulation
+constexpr uint32_t TC_MIN_Q = 1u << 26;        // smallest prime the epilogue's reduction supports
 constexpr uint32_t TC_Q_BYTES = TC_MAX_D0 * 32 * 4;     // one point's query slice (64 KiB)
+constexpr uint32_t TC_RED_PITCH = 33;          // words per row of the epilogue's plane sums (no bank conflicts)
+constexpr uint32_t TC_PREFETCH_PIECE = 64 * 1024;
 
 struct TcArgs {
+    const uint32_t *db;     // slab-encoded DB (L2 prefetches of whole slab blocks)
     const uint32_t *qT;     // point-major query, [P][PS], 32 polynomials per k
     uint32_t *outT;         // point-major results [P][Mv][D1p]
     uint32_t *status;
     uint32_t N, D0, D1, D1p, S, Wlast, PS, Kp, Mv;
     uint64_t P;
     uint32_t q[PIR_MAX_RNS];
-    uint64_t mu[PIR_MAX_RNS];
-    uint64_t bias[PIR_MAX_RNS];       // multiple of q >= 2^50 (makes signed sums positive)
+    float qinv[PIR_MAX_RNS];          // 1/q rounded to fp32 (quotient estimate of the epilogue)
     uint32_t c[PIR_MAX_RNS][4];       // 2^(8i) mod q
     uint32_t cs[PIR_MAX_RNS][4];      // Shoup companions of c
 };
@@ -79,11 +91,21 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
 // kind::f16, A = B = F16, D = F32, K-major, N = 128, M = 128
 constexpr uint32_t TC_IDESC = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t accumulate) {
+// The four K = 16 MMAs of one 64-row stage: A (query digits) from TMEM
+// columns a_tmem + 8*kk, B (DB byte planes) from the stage's swizzled tile,
+// whose descriptor start address advances 32 bytes (2 units) per kk.  The
+// first stage of a tile (ks == 0) starts the accumulator from zero.
+__device__ __forceinline__ void mma_stage(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t ks) {
     asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-        "r"(a_tmem), "l"(bdesc), "r"(TC_IDESC), "r"(accumulate)
+        "{\n.reg .pred p, t;\n"
+        "setp.ne.b32 p, %3, 0;\n"
+        "setp.eq.b32 t, %3, %3;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %4, t;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %4, t;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %4, t;\n}\n" ::"r"(d),
+        "r"(a_tmem), "l"(bdesc), "r"(ks), "r"(TC_IDESC), "r"(a_tmem + 8), "l"(bdesc + 2), "r"(a_tmem + 16),
+        "l"(bdesc + 4), "r"(a_tmem + 24), "l"(bdesc + 6)
         : "memory");
 }
 
@@ -146,6 +168,62 @@ __device__ __forceinline__ uint32_t tiles_of(const TcArgs &A, uint32_t s) {
     return (w + TC_NT - 1) / TC_NT;
 }
 
+// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned address,
+// in pieces of at most 64 KiB.
+__device__ __forceinline__ void l2_prefetch(const void *src, uint64_t bytes) {
+    const char *s = static_cast<const char *>(src);
+    for (uint64_t off = 0; off < bytes; off += TC_PREFETCH_PIECE) {
+        const uint32_t n = (uint32_t)(bytes - off < TC_PREFETCH_PIECE ? bytes - off : TC_PREFETCH_PIECE);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s + off), "r"(n) : "memory");
+    }
+}
+
+// The contiguous block of DB slab s of point p (D0 rows of the slab's width).
+__device__ __forceinline__ void prefetch_slab(const TcArgs &A, uint64_t p, uint32_t s) {
+    const uint32_t w = (s == A.S - 1) ? A.Wlast : PIR_SLAB;
+    l2_prefetch(A.db + p * A.D0 * A.D1p + (uint64_t)s * A.D0 * PIR_SLAB, (uint64_t)A.D0 * w * 4);
+}
+
+// A stage holds 64 DB rows x 32 columns of words (row-major).  Converting it
+// writes the 4 byte planes as fp16 in the 128B-swizzled K-major B layout
+// (row j*32 + n, K = DB row).  The work is cut into 8 chunks of 8 rows; lane
+// n of a converter warp handles column n of chunks kc = gw, gw + 3, gw + 6
+// (gw = the warp's position 0..2 in its group of three).
+__device__ __forceinline__ void load_chunks(const uint32_t *raw, uint32_t gw, uint32_t n, uint32_t (&w)[3][8]) {
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        const uint32_t kc = gw + 3 * c;
+        if (kc < 8) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[c][e] = raw[(kc * 8 + e) * TC_NT + n];
+        }
+    }
+}
+
+__device__ __forceinline__ void store_chunks(uint8_t *bt, uint32_t gw, uint32_t n, const uint32_t (&w)[3][8]) {
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        const uint32_t kc = gw + 3 * c;
+        if (kc < 8) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t hv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    // bytes j of two words -> halves 0x64xx = 1024 + byte
+                    const uint32_t x = __byte_perm(w[c][2 * e], w[c][2 * e + 1], j | ((4 + j) << 8));
+                    const uint32_t hh = (x & 0x00FF00FFu) | 0x64006400u;
+                    const __half2 r =
+                        __hsub2(*reinterpret_cast<const __half2 *>(&hh), __floats2half2_rn(1024.f, 1024.f));
+                    hv[e] = *reinterpret_cast<const uint32_t *>(&r);
+                }
+                *reinterpret_cast<uint4 *>(bt + sw128(j * 32 + n, kc)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            }
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(TC_THREADS, 1)
     rowsel_tc_kernel(const __grid_constant__ CUtensorMap full_map, const __grid_constant__ CUtensorMap last_map,
                      const __grid_constant__ TcArgs A) {
@@ -153,12 +231,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t base_s = smem_u32(smraw);
     uint8_t *sm = smraw + (((base_s + 1023u) & ~1023u) - base_s);
     uint8_t *stB = sm;                                   // [NS][16 KiB] fp16 digit tiles
-    uint8_t *stR = stB + TC_NS * TC_B_BYTES;             // [NS][8 KiB] DB words
-    uint32_t *qsm = reinterpret_cast<uint32_t *>(stR + TC_NS * TC_RAW_BYTES);   // [D0][32] query slice
-    uint32_t *red = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(qsm) + TC_Q_BYTES);  // [4][32][32]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(red + 4 * 32 * 32);
-    uint64_t *rfull = bars, *bfull = bars + TC_NS, *empty = bars + 2 * TC_NS;
-    uint64_t *accf = bars + 3 * TC_NS, *acce = accf + 2, *afull = acce + 2, *aempty = afull + 1, *done = aempty + 1;
+    uint8_t *stR = stB + TC_NB * TC_B_BYTES;             // [NR][8 KiB] DB words
+    uint32_t *qsm = reinterpret_cast<uint32_t *>(stR + TC_NR * TC_RAW_BYTES);   // [D0][32] query slice
+    uint32_t *red = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(qsm) + TC_Q_BYTES);  // [128][33]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(red + 128 * TC_RED_PITCH);
+    uint64_t *rfull = bars, *rempty = rfull + TC_NR, *bfull = rempty + TC_NR, *bempty = bfull + TC_NB;
+    uint64_t *accf = bempty + TC_NB, *acce = accf + 2, *afull = acce + 2, *aempty = afull + 1, *done = aempty + 1;
     uint64_t *qfull = done + 1, *qempty = qfull + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(qempty + 1);
     __shared__ volatile int abort_flag;
@@ -169,10 +247,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t nks = A.Kp / TC_KS;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < TC_NS; ++s) {
+        for (int s = 0; s < TC_NR; ++s) {
             mbar_init(rfull + s, 1);
-            mbar_init(bfull + s, 4);
-            mbar_init(empty + s, 1);
+            mbar_init(rempty + s, 3);
+        }
+        for (int s = 0; s < TC_NB; ++s) {
+            mbar_init(bfull + s, 3);
+            mbar_init(bempty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf + b, 1);
@@ -186,7 +267,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 12) {
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TC_TMEM_COLS)
                      : "memory");
@@ -197,11 +278,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 12 && lane == 0) {
-        // ------------------------------------------------ TMA producer: DB word tiles
+    if (warp == 9 && lane == 0) {
+        // ------------------------------------------------ TMA producer: query slices and DB word tiles
+        // Every slab block is prefetched into L2 one slab ahead of its tile
+        // loads (and every query slice one point ahead), so HBM sees whole
+        // contiguous blocks and the 8 KiB tile loads are served from L2.
         const uint64_t pol = policy_evict_first();
         const uint32_t qbytes = A.PS * 4;
         uint32_t it = 0, pc = 0;
+        if (p_begin < p_end) prefetch_slab(A, p_begin, 0);
         for (uint64_t p = p_begin; p < p_end; ++p, ++pc) {
             // the point's query slice (the query warps release the buffer once digitised)
             if (abort_flag || !mbar_wait(qempty, (pc & 1) ^ 1, A.status)) {
@@ -210,12 +295,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 mbar_arrive_expect_tx(qfull, qbytes);
                 bulk_g2s(qsm, A.qT + p * A.PS, qbytes, qfull, pol);
             }
+            if (p + 1 < p_end) l2_prefetch(A.qT + (p + 1) * A.PS, qbytes);
             for (uint32_t s = 0; s < A.S; ++s) {
+                if (s + 1 < A.S)
+                    prefetch_slab(A, p, s + 1);
+                else if (p + 1 < p_end)
+                    prefetch_slab(A, p + 1, 0);
                 const uint32_t nt = tiles_of(A, s);
                 for (uint32_t t = 0; t < nt; ++t)
                     for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
-                        const uint32_t st = it % TC_NS, ph = (it / TC_NS) & 1;
-                        if (abort_flag || !mbar_wait(empty + st, ph ^ 1, A.status)) {
+                        const uint32_t st = it % TC_NR, ph = (it / TC_NR) & 1;
+                        if (abort_flag || !mbar_wait(rempty + st, ph ^ 1, A.status)) {
                             abort_flag = 1;
                             continue;
                         }
@@ -229,77 +319,116 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
             }
         }
-        for (uint32_t i = 0; i < TC_NS && i < it; ++i) {  // copies in flight land first
+        for (uint32_t i = 0; i < TC_NR && i < it; ++i) {  // copies in flight land first
             const uint32_t j = it - 1 - i;
-            mbar_wait(rfull + j % TC_NS, (j / TC_NS) & 1, A.status);
+            mbar_wait(rfull + j % TC_NR, (j / TC_NR) & 1, A.status);
         }
         if (pc) mbar_wait(qfull, (pc - 1) & 1, A.status);
     } else if (warp == 13 && lane == 0) {
         // ------------------------------------------------ MMA issue
-        uint32_t it = 0, g = 0, pc = 0;
+        // One thread whose warp shares its scheduler with three busy warps:
+        // the per-stage path is kept short (a local abort flag, descriptors
+        // advanced by addition, the stage's four MMAs in one asm block).
+        bool ab = false;
+        uint32_t it = 0, g = 0, pc = 0, st = 0, ph = 0;
+        const uint64_t bdesc0 = sdesc(smem_u32(stB));
         for (uint64_t p = p_begin; p < p_end; ++p) {
+            ab = ab || abort_flag;
             bool first = true;
             for (uint32_t s = 0; s < A.S; ++s) {
                 const uint32_t nt = tiles_of(A, s);
                 for (uint32_t t = 0; t < nt; ++t, ++g) {
                     const uint32_t buf = g & 1, use = (g >> 1) & 1;
-                    if (!abort_flag && !mbar_wait(acce + buf, use ^ 1, A.status)) abort_flag = 1;
+                    if (!ab && !mbar_wait(acce + buf, use ^ 1, A.status)) ab = true;
                     if (first) {
-                        if (!abort_flag && !mbar_wait(afull, pc & 1, A.status)) abort_flag = 1;
+                        if (!ab && !mbar_wait(afull, pc & 1, A.status)) ab = true;
                         first = false;
                     }
-                    fence_after();
                     const uint32_t d = tmem + TC_ACC_COL + buf * 128;
                     for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
-                        const uint32_t st = it % TC_NS, ph = (it / TC_NS) & 1;
-                        if (!abort_flag && !mbar_wait(bfull + st, ph, A.status)) abort_flag = 1;
-                        if (abort_flag) continue;
-                        fence_after();
-                        const uint32_t b0 = smem_u32(stB + st * TC_B_BYTES);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA; A: 8 TMEM columns per 16 K
-                            mma_ts(d, tmem + ks * 32 + kk * 8, sdesc(b0 + 32 * kk), (ks | kk) ? 1u : 0u);
-                        commit(empty + st);
+                        if (!ab && !mbar_wait(bfull + st, ph, A.status)) ab = true;
+                        if (!ab) {
+                            fence_after();
+                            mma_stage(d, tmem + ks * 32, bdesc0 + st * (TC_B_BYTES >> 4), ks);
+                            commit(bempty + st);
+                        }
+                        if (++st == TC_NB) {
+                            st = 0;
+                            ph ^= 1;
+                        }
                     }
-                    if (!abort_flag) commit(accf + buf);
+                    if (!ab) commit(accf + buf);
                 }
             }
             commit(aempty);  // A (query digits) reusable once this point's MMAs finish
             ++pc;
         }
+        if (ab) abort_flag = 1;
         commit(done);
         mbar_wait(done, 0, A.status);
-    } else if (warp < 4) {
-        // ------------------------------------------------ query digits -> TMEM (plane = warp)
-        const uint32_t plane = warp, m = lane;
-        uint32_t pc = 0;
+    } else if (warp < 4 || (warp >= 8 && (warp & 3) != 1)) {
+        // ------------------------------------------------ query digits and converters
+        // Warps 0-3 write the query digits of each point into TMEM (plane =
+        // warp) before that point's stages.  Three groups of three converter
+        // warps -- {0, 2, 3}, {8, 10, 11}, {12, 14, 15} -- take every third
+        // stage each; none of them shares a scheduler with the MMA warp (13).
+        const bool digitizer = warp < 4, converter = warp != 1;
+        const uint32_t gi = warp < 4 ? 0u : (uint32_t)(warp >> 2) - 1u;          // group 0..2
+        const uint32_t gw = (warp & 3) == 0 ? 0u : (uint32_t)(warp & 3) - 1u;     // position 0..2
+        uint32_t it = 0, pc = 0, sel = 0;                                         // sel = it % 3
         for (uint64_t p = p_begin; p < p_end; ++p, ++pc) {
-            if (!abort_flag && !mbar_wait(qfull, pc & 1, A.status)) abort_flag = 1;
-            if (!abort_flag && !mbar_wait(aempty, (pc & 1) ^ 1, A.status)) abort_flag = 1;
-            fence_after();
-            if (!abort_flag) {
-                const bool live = m < A.Mv;
-                for (uint32_t kc = 0; kc < A.Kp / 64; ++kc) {
-                    uint32_t v[32];
+            if (digitizer) {
+                // query digits -> TMEM (plane = warp, polynomial m = lane)
+                const uint32_t plane = warp, m = lane;
+                if (!abort_flag && !mbar_wait(qfull, pc & 1, A.status)) abort_flag = 1;
+                if (!abort_flag && !mbar_wait(aempty, (pc & 1) ^ 1, A.status)) abort_flag = 1;
+                fence_after();
+                if (!abort_flag) {
+                    const bool live = m < A.Mv;
+                    for (uint32_t kc = 0; kc < A.Kp / 64; ++kc) {
+                        uint32_t v[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const uint32_t k0 = kc * 64 + 2 * e;
-                        const uint32_t a0 = (live && k0 < A.D0) ? qsm[k0 * 32 + m] : 0u;
-                        const uint32_t a1 = (live && k0 + 1 < A.D0) ? qsm[(k0 + 1) * 32 + m] : 0u;
-                        v[e] = digit_pair(a0, a1, plane);
+                        for (int e = 0; e < 32; ++e) {
+                            const uint32_t k0 = kc * 64 + 2 * e;
+                            const uint32_t a0 = (live && k0 < A.D0) ? qsm[k0 * 32 + m] : 0u;
+                            const uint32_t a1 = (live && k0 + 1 < A.D0) ? qsm[(k0 + 1) * 32 + m] : 0u;
+                            v[e] = digit_pair(a0, a1, plane);
+                        }
+                        tmem_st32(tmem + ((plane * 32u) << 16) + kc * 32, v);
                     }
-                    tmem_st32(tmem + ((plane * 32u) << 16) + kc * 32, v);
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(afull);
+                    mbar_arrive(qempty);
+                }
             }
-            fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(afull);
-                mbar_arrive(qempty);
+            if (!converter) continue;
+            for (uint32_t s = 0; s < A.S; ++s) {
+                const uint32_t nt = tiles_of(A, s);
+                for (uint32_t t = 0; t < nt; ++t)
+                    for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
+                        const bool my_stage = sel == gi;
+                        sel = sel == 2 ? 0u : sel + 1;
+                        if (!my_stage) continue;
+                        const uint32_t rs = it % TC_NR, rph = (it / TC_NR) & 1;
+                        const uint32_t bs = it % TC_NB, bph = (it / TC_NB) & 1;
+                        uint32_t w[3][8];
+                        if (!abort_flag && !mbar_wait(rfull + rs, rph, A.status)) abort_flag = 1;
+                        if (!abort_flag)
+                            load_chunks(reinterpret_cast<const uint32_t *>(stR + rs * TC_RAW_BYTES), gw, lane, w);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(rempty + rs);     // the words are in registers
+                        if (!abort_flag && !mbar_wait(bempty + bs, bph ^ 1, A.status)) abort_flag = 1;
+                        if (!abort_flag) store_chunks(stB + bs * TC_B_BYTES, gw, lane, w);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bfull + bs);
+                    }
             }
         }
-    } else if (warp < 8) {
+    } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------ epilogue
         const uint32_t plane = warp & 3, m = lane;
         const uint32_t etid = threadIdx.x - 128;  // 0..127
@@ -307,7 +436,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (uint64_t p = p_begin; p < p_end; ++p) {
             const uint32_t l = (uint32_t)(p / A.N);
             const uint32_t q = A.q[l];
-            const uint64_t mu = A.mu[l], bias = A.bias[l];
+            const float qinv = A.qinv[l];
             const uint32_t ci = A.c[l][plane], cis = A.cs[l][plane];
             for (uint32_t s = 0; s < A.S; ++s) {
                 const uint32_t nt = tiles_of(A, s);
@@ -316,9 +445,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint32_t buf = g & 1, use = (g >> 1) & 1;
                     if (!abort_flag && !mbar_wait(accf + buf, use, A.status)) abort_flag = 1;
                     fence_after();
-                    int64_t W[32];
+                    // W[n] = sum_j 2^(8j) S_j[n] = sum_k d_i(query) * DB word is reduced
+                    // mod q without 64-bit arithmetic.  Its low 32 bits come exactly
+                    // from wrapping 32-bit sums of the integer plane sums S_j; the
+                    // quotient k = round(W / q) comes from an fp32 estimate of W.
+                    // Every partial sum of the estimate is below 128 * D0 * (2^24 + q)
+                    // <= 2^46, so its three roundings add at most 3 * 2^22, and
+                    // |W| / q <= 128 * D0 = 2^16; with q >= 2^26 the estimate of W / q
+                    // is off by less than 0.2, W - k*q lies in (-0.7q, 1.7q) and one
+                    // conditional add or subtract of q ends the reduction.
+                    uint32_t lo[32];
+                    float wf[32];
 #pragma unroll
-                    for (int n = 0; n < 32; ++n) W[n] = 0;
+                    for (int n = 0; n < 32; ++n) {
+                        lo[n] = 0;
+                        wf[n] = 0.f;
+                    }
                     if (!abort_flag) {
                         const uint32_t taddr = tmem + ((plane * 32u) << 16) + TC_ACC_COL + buf * 128;
 #pragma unroll
@@ -326,9 +468,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             uint32_t v[32];
                             tmem_ld32(taddr + j * 32, v);
                             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                            const float scale = (float)(1u << (8 * j));
 #pragma unroll
-                            for (int n = 0; n < 32; ++n)
-                                W[n] += (int64_t)__float2int_rn(__uint_as_float(v[n])) << (8 * j);
+                            for (int n = 0; n < 32; ++n) {
+                                const float x = __uint_as_float(v[n]);
+                                lo[n] += (uint32_t)__float2int_rn(x) << (8 * j);
+                                wf[n] = fmaf(x, scale, wf[n]);
+                            }
                         }
                     }
                     fence_before();
@@ -337,9 +483,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     named_barrier(2, 128);                    // previous tile's readers of red are done
 #pragma unroll
                     for (int n = 0; n < 32; ++n) {
-                        const uint32_t r = barrett64((uint64_t)(W[n] + (int64_t)bias), q, mu);
+                        const int32_t k = __float2int_rn(wf[n] * qinv);
+                        int32_t rs = (int32_t)(lo[n] - (uint32_t)k * q);
+                        rs += rs < 0 ? (int32_t)q : 0;
+                        const uint32_t r = (uint32_t)rs >= q ? (uint32_t)rs - q : (uint32_t)rs;
                         uint32_t u = shoup_mul(r, ci, cis, q);
-                        red[(plane * 32 + m) * 32 + n] = u >= q ? u - q : u;
+                        red[(plane * 32 + m) * TC_RED_PITCH + n] = u >= q ? u - q : u;
                     }
                     named_barrier(2, 128);
                     for (uint32_t idx = etid; idx < 32 * 32; idx += 128) {
@@ -347,9 +496,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         const uint32_t col = t * TC_NT + nn;
                         if (mm >= A.Mv || col >= Ws) continue;
                         const uint32_t n_glob = s * PIR_SLAB + col;
-                        uint32_t x = red[mm * 32 + nn] + red[(32 + mm) * 32 + nn];
+                        uint32_t x = red[mm * TC_RED_PITCH + nn] + red[(32 + mm) * TC_RED_PITCH + nn];
                         x = x >= q ? x - q : x;
-                        uint32_t y = red[(64 + mm) * 32 + nn] + red[(96 + mm) * 32 + nn];
+                        uint32_t y = red[(64 + mm) * TC_RED_PITCH + nn] + red[(96 + mm) * TC_RED_PITCH + nn];
                         y = y >= q ? y - q : y;
                         x += y;
                         x = x >= q ? x - q : x;
@@ -358,54 +507,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
             }
         }
-    } else if (warp < 12) {
-        // ------------------------------------------------ converters: DB words -> 4 fp16 byte planes
-        const uint32_t ct = threadIdx.x - 256;  // 0..127
-        uint32_t it = 0;
-        for (uint64_t p = p_begin; p < p_end; ++p)
-            for (uint32_t s = 0; s < A.S; ++s) {
-                const uint32_t nt = tiles_of(A, s);
-                for (uint32_t t = 0; t < nt; ++t)
-                    for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
-                        const uint32_t st = it % TC_NS, ph = (it / TC_NS) & 1;
-                        if (!abort_flag && !mbar_wait(rfull + st, ph, A.status)) abort_flag = 1;
-                        if (!abort_flag) {
-                            const uint32_t *raw = reinterpret_cast<const uint32_t *>(stR + st * TC_RAW_BYTES);
-                            uint8_t *bt = stB + st * TC_B_BYTES;
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const uint32_t task = ct + 128 * h;   // column n, 8 rows kc*8 .. kc*8+7
-                                const uint32_t n = task & 31, kc = task >> 5;
-                                uint32_t w[8];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) w[e] = raw[(kc * 8 + e) * TC_NT + n];
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    uint32_t hv[4];
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        // bytes j of two words -> halves 0x64xx = 1024 + byte
-                                        const uint32_t x = __byte_perm(w[2 * e], w[2 * e + 1], j | ((4 + j) << 8));
-                                        const uint32_t hh = (x & 0x00FF00FFu) | 0x64006400u;
-                                        const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&hh),
-                                                                  __floats2half2_rn(1024.f, 1024.f));
-                                        hv[e] = *reinterpret_cast<const uint32_t *>(&r);
-                                    }
-                                    *reinterpret_cast<uint4 *>(bt + sw128(j * 32 + n, kc)) =
-                                        make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                                }
-                            }
-                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bfull + st);
-                    }
-            }
     }
 
     fence_before();
     __syncthreads();
-    if (warp == 12) {
+    if (warp == 9) {
         fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS)
                      : "memory");
@@ -425,7 +531,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-size_t tc_smem_bytes() { return 1024 + (size_t)TC_NS * (TC_B_BYTES + TC_RAW_BYTES) + TC_Q_BYTES + 4 * 32 * 32 * 4 + 512; }
+size_t tc_smem_bytes() {
+    return 1024 + (size_t)TC_NB * TC_B_BYTES + (size_t)TC_NR * TC_RAW_BYTES + TC_Q_BYTES + 128 * TC_RED_PITCH * 4 +
+           (2 * TC_NR + 2 * TC_NB + 11) * 8 + 16;
+}
 
 uint64_t powmod_host(uint64_t b, uint64_t e, uint64_t m) {
     uint64_t r = 1 % m;
@@ -440,7 +549,12 @@ uint64_t powmod_host(uint64_t b, uint64_t e, uint64_t m) {
 }  // namespace
 
 // Whether a RowSel pass of Mv polynomials over D0 rows runs on this path.
-bool rowsel_tc_eligible(uint32_t D0, uint32_t Mv) { return Mv > 16 && D0 <= TC_MAX_D0; }
+bool rowsel_tc_eligible(const pir_ctx *ctx, uint32_t D0, uint32_t Mv) {
+    if (Mv <= 16 || D0 > TC_MAX_D0) return false;
+    for (uint32_t l = 0; l < ctx->L; ++l)
+        if (ctx->q[l] < TC_MIN_Q) return false;   // the epilogue's quotient estimate needs q >= 2^26
+    return true;
+}
 
 // One RowSel pass on the tensor cores.  qT holds the pass's query slices
 // (32 polynomials per k, PS words per point); db is the slab-encoded DB.
@@ -482,6 +596,7 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
 
     TcArgs a;
     memset(&a, 0, sizeof(a));
+    a.db = db;
     a.qT = qT;
     a.outT = outT;
     a.status = ctx->d_status;
@@ -498,8 +613,7 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
     for (uint32_t l = 0; l < ctx->L; ++l) {
         const uint64_t q = ctx->q[l];
         a.q[l] = (uint32_t)q;
-        a.mu[l] = ctx->mu[l];
-        a.bias[l] = ((1ull << 50) + q - 1) / q * q;
+        a.qinv[l] = 1.0f / (float)q;
         for (int i = 0; i < 4; ++i) {
             const uint32_t c = (uint32_t)powmod_host(2, 8 * i, q);
             a.c[l][i] = c;

@@ -134,6 +134,57 @@ def test_rowsel_tensor_path_digit_extremes(pir):
     assert pir.pir_status(ctx) == 0
 
 
+def _primes_between(N, L, lo, hi):
+    qs = oracle.primes(N, L, bound=hi)
+    assert len(qs) == L and all(lo <= q < hi for q in qs), qs
+    return qs
+
+
+@pytest.mark.parametrize("lo,hi", [(1 << 26, (1 << 26) + (1 << 20)), (1 << 25, 1 << 26)])
+def test_rowsel_b16_prime_sizes(pir, lo, hi):
+    """A 16-query pass with the smallest primes the tensor-core epilogue
+    supports (just above 2^26) and with primes below 2^26 (which take the
+    CUDA-core kernel): random residues compared element by element, and the
+    largest partial sums of the epilogue's quotient estimate (DB words with
+    three low bytes 255, query words with balanced digits -128, -128, -128)."""
+    N, L, D0, D1, B = 64, 2, 512, 40, 16
+    qs = _primes_between(N, L, lo, hi)
+    ctx = pir.pir_ctx_create(N, qs)
+    P = L * N
+    D1p = (D1 + 3) // 4 * 4
+    psis = [oracle.min_psi(q, N) for q in qs]
+    raw = synth.coeffs(31, (D0, D1, N))
+    db_t = pir.empty_u32(pir.pir_db_bytes(ctx, D0, D1) // 4)
+    pir.pir_db_encode(ctx, to_dev(raw), 0, D0, D0, D1, db_t)
+    enc = oracle.encode_records(raw, qs, psis)
+    query = synth.residues(32, (B, D0, 2, L, N), qs)
+    out = pir.empty_u32(B * D1 * 2 * P)
+    out.fill_(-1)
+    pir.pir_rowsel(ctx, db_t, D0, D1, to_dev(query), B, out, pir.rowsel_workspace(ctx, D0, D1, B))
+    got = to_host_u32(out).reshape(B, D1, 2, L, N)
+    assert np.array_equal(got, oracle.rowsel(enc, query, qs))
+    # extremes, written directly in the (single-slab) DB layout [p][k][n]:
+    # every DB word b_l, every query word a_l (per prime)
+    db_words = np.empty((P, D0 * D1p), np.uint32)
+    qext = np.empty((B, D0, 2, L, N), np.uint32)
+    want = []
+    for l, q in enumerate(qs):
+        top = q >> 24
+        b = (top - 1) * (1 << 24) + 0xFFFFFF if (top - 1) * (1 << 24) + 0xFFFFFF < q else q - 1
+        a = top * (1 << 24) - 0x808080
+        assert 0 <= a < q and 0 <= b < q
+        db_words[l * N:(l + 1) * N] = b
+        qext[..., l, :] = a
+        want.append(D0 * a * b % q)
+    out.fill_(-1)
+    pir.pir_rowsel(ctx, to_dev(db_words.reshape(-1)), D0, D1, to_dev(qext), B, out,
+                   pir.rowsel_workspace(ctx, D0, D1, B))
+    got = to_host_u32(out).reshape(B, D1, 2, L, N)
+    for l in range(L):
+        assert (got[..., l, :] == want[l]).all()
+    assert pir.pir_status(ctx) == 0
+
+
 def test_rowsel_rejects_bad_arguments(pir):
     qs = oracle.primes(64, 2)
     ctx = pir.pir_ctx_create(64, qs)
