@@ -733,6 +733,16 @@ def run_ours(args, cfg):
     hbm_peak = float(peaks["hbm_gbs"])
     algo_bytes = logical_db + q_bytes + o_bytes       # the RowSel kernel's algorithmic bytes per launch
     achieved = algo_bytes / (rowsel_ms * 1e-3) / 1e9
+    # passes of 9..16 queries with D0 <= 512 run on the tensor cores (primes >= 2^26 here)
+    on_tensor = 8 < B <= 16 and D0 <= 512
+    kernel = "rowsel_tc_kernel" if on_tensor else "rowsel_kernel"
+    tensor = None
+    if on_tensor:
+        # 16 digit-plane products per multiply-add, fp16 inputs, 2 flops each
+        flops = 2.0 * 16 * (2 * B) * D0 * D1 * P
+        tf = flops / (rowsel_ms * 1e-3) / 1e12
+        tensor = {"achieved": tf, "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
+                  "frac": tf / float(peaks["bf16_tflops"]), "algorithmic_flops_per_launch": flops}
 
     result = None
     if rank == 0:
@@ -753,9 +763,9 @@ def run_ours(args, cfg):
             "kernel_ms": {"ntt_fwd": ntt_fwd_ms, "rowsel": rowsel_ms, "ntt_inv": ntt_inv_ms},
             "kernels": kernel_rooflines(coeff, q_bytes, o_bytes, ntt_fwd_ms, ntt_inv_ms, hbm_peak),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": profile_traffic("rowsel_kernel_rowsel_64g"),
-                         "kernel": "rowsel_kernel", "peak_source": "%s hbm_gbs (copy)" % peak_kind,
-                         "algorithmic_bytes_per_launch": algo_bytes},
+                         "frac": achieved / hbm_peak, "traffic": profile_traffic("%s_%s" % (kernel, args.workload)),
+                         "kernel": kernel, "peak_source": "%s hbm_gbs (copy)" % peak_kind,
+                         "algorithmic_bytes_per_launch": algo_bytes, "tensor": tensor},
             "clocks": clk,
             "e2e": None if e2e_ms is None else {
                 "value": logical_db / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": q_bytes,

@@ -19,7 +19,8 @@
 // TMEM for all tiles of the point; the accumulator (128 columns, double
 // buffered) then holds S_ij[m][n].  The epilogue forms
 //     out[m][n] = sum_i 2^(8i) (sum_j 2^(8j) S_ij[m][n])  mod q
-// with one 64-bit Barrett reduction per (i, m, n) and a cross-plane sum.
+// with one reduction per (i, m, n) (32-bit arithmetic and an fp32 quotient
+// estimate, valid for q >= 2^26) and a cross-plane sum.
 //
 // Warp roles (512 threads, one CTA per SM, persistent over a range of points).
 // A warp's scheduler is fixed by warp % 4, and the MMA-issuing thread loses
@@ -28,7 +29,8 @@
 //   warps 0-3   query digits of the next point -> TMEM (tcgen05.st), warp w
 //               writes digit plane w into TMEM lanes 32w..32w+31, from the
 //               point's query slice that the producer bulk-copies into
-//               shared memory while the previous point is still in flight;
+//               shared memory while the previous point is still in flight
+//               (warps 0, 2, 3 also convert; warp 1 only writes digits);
 //   warps 4-7   epilogue: tcgen05.ld of a finished accumulator, reduction,
 //               cross-plane sum through shared memory, output stores;
 //   converters  three groups of three warps, {0, 2, 3}, {8, 10, 11} and
@@ -36,11 +38,14 @@
 //               words (TMA-staged) -> 4 byte planes of fp16 in the
 //               128B-swizzled K-major layout of the B operand;
 //   warp 9      TMEM allocation and the TMA producer of query slices and DB
-//               word tiles (with L2 prefetches one slab ahead);
+//               word tiles;
 //   warp 13     MMA issue (one thread).
 // DB word stages (TMA -> converters) and fp16 operand stages (converters ->
 // MMA) are separate rings, so a word stage is refilled as soon as it has
-// been read.
+// been read.  The MMA thread keeps its loop short: any shared-memory access
+// of the issuing thread (a barrier wait included) stalls until the tensor
+// core has taken its previous MMAs, so bookkeeping between MMAs leaves the
+// tensor pipe idle.
 // All mbarrier waits are bounded; TMEM is always released.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -52,8 +57,8 @@
 
 namespace {
 
-constexpr int TC_NR = 10;                      // DB word stages (TMA -> converters)
-constexpr int TC_NB = 4;                       // fp16 operand stages (converters -> MMA)
+constexpr int TC_NR = 6;                      // DB word stages (TMA -> converters)
+constexpr int TC_NB = 6;                       // fp16 operand stages (converters -> MMA)
 constexpr int TC_KS = 64;                      // DB rows (K) per stage
 constexpr int TC_NT = 32;                      // DB columns per MMA tile
 constexpr uint32_t TC_RAW_BYTES = TC_KS * TC_NT * 4;   // 8 KiB of DB words
@@ -68,7 +73,6 @@ constexpr uint32_t TC_RED_PITCH = 33;          // words per row of the epilogue'
 constexpr uint32_t TC_PREFETCH_PIECE = 64 * 1024;
 
 struct TcArgs {
-    const uint32_t *db;     // slab-encoded DB (L2 prefetches of whole slab blocks)
     const uint32_t *qT;     // point-major query, [P][PS], 32 polynomials per k
     uint32_t *outT;         // point-major results [P][Mv][D1p]
     uint32_t *status;
@@ -178,12 +182,6 @@ __device__ __forceinline__ void l2_prefetch(const void *src, uint64_t bytes) {
     }
 }
 
-// The contiguous block of DB slab s of point p (D0 rows of the slab's width).
-__device__ __forceinline__ void prefetch_slab(const TcArgs &A, uint64_t p, uint32_t s) {
-    const uint32_t w = (s == A.S - 1) ? A.Wlast : PIR_SLAB;
-    l2_prefetch(A.db + p * A.D0 * A.D1p + (uint64_t)s * A.D0 * PIR_SLAB, (uint64_t)A.D0 * w * 4);
-}
-
 // A stage holds 64 DB rows x 32 columns of words (row-major).  Converting it
 // writes the 4 byte planes as fp16 in the 128B-swizzled K-major B layout
 // (row j*32 + n, K = DB row).  The work is cut into 8 chunks of 8 rows; lane
@@ -280,13 +278,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     if (warp == 9 && lane == 0) {
         // ------------------------------------------------ TMA producer: query slices and DB word tiles
-        // Every slab block is prefetched into L2 one slab ahead of its tile
-        // loads (and every query slice one point ahead), so HBM sees whole
-        // contiguous blocks and the 8 KiB tile loads are served from L2.
+        // The next point's query slice is prefetched into L2 a point ahead.
+        // (Prefetching whole DB slab blocks ahead was measured too: 152 SMs x
+        // two 256 KiB slabs crowd the L2 next to the streaming result writes,
+        // and 40% of the DB was read twice.)
         const uint64_t pol = policy_evict_first();
         const uint32_t qbytes = A.PS * 4;
         uint32_t it = 0, pc = 0;
-        if (p_begin < p_end) prefetch_slab(A, p_begin, 0);
+
         for (uint64_t p = p_begin; p < p_end; ++p, ++pc) {
             // the point's query slice (the query warps release the buffer once digitised)
             if (abort_flag || !mbar_wait(qempty, (pc & 1) ^ 1, A.status)) {
@@ -297,10 +296,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             if (p + 1 < p_end) l2_prefetch(A.qT + (p + 1) * A.PS, qbytes);
             for (uint32_t s = 0; s < A.S; ++s) {
-                if (s + 1 < A.S)
-                    prefetch_slab(A, p, s + 1);
-                else if (p + 1 < p_end)
-                    prefetch_slab(A, p + 1, 0);
+
                 const uint32_t nt = tiles_of(A, s);
                 for (uint32_t t = 0; t < nt; ++t)
                     for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
@@ -568,6 +564,9 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
     const uint32_t Wlast = D1p - PIR_SLAB * (S - 1);
 
     // Full slabs: 4-D view (column, row k, slab, point) of the first S-1 slabs of every point.
+    // L2 promotion stays at 128 B: a tile reads one 128-byte line of each
+    // 512-byte slab row, and 256-byte promotion fetched the neighbouring
+    // tile's line too, which was evicted before use (30% more DRAM reads).
     CUtensorMap full_map, last_map;
     memset(&full_map, 0, sizeof(full_map));
     memset(&last_map, 0, sizeof(last_map));
@@ -578,7 +577,7 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
         const cuuint64_t dim[4] = {PIR_SLAB, D0, S - 1, P};
         const cuuint64_t str[3] = {(cuuint64_t)PIR_SLAB * 4, (cuuint64_t)D0 * PIR_SLAB * 4, (cuuint64_t)D0 * D1p * 4};
         if (encode(&full_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, dbp, dim, str, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PIR_ERR_ARG;
     }
@@ -588,7 +587,7 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
         const cuuint64_t str[3] = {(cuuint64_t)Wlast * 4, (cuuint64_t)D0 * Wlast * 4, (cuuint64_t)D0 * D1p * 4};
         void *lastp = const_cast<uint32_t *>(db + (uint64_t)(S - 1) * D0 * PIR_SLAB);
         if (encode(&last_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, lastp, dim, str, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PIR_ERR_ARG;
     }
@@ -596,7 +595,6 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
 
     TcArgs a;
     memset(&a, 0, sizeof(a));
-    a.db = db;
     a.qT = qT;
     a.outT = outT;
     a.status = ctx->d_status;
