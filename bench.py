@@ -13,7 +13,8 @@ Prints ONE JSON line (rank 0):
   e2e       the same metric through the public API with the query coming
             from pinned host memory and the result going back to it;
   roofline  the RowSel kernel's algorithmic bytes / its average launch time
-            against the measured HBM copy bandwidth;
+            against the measured HBM copy bandwidth, also as fractions of an
+            in-run read-only stream over the DB and of the 8 TB/s spec;
   cpu_baseline  the oracle (plain C, all host cores) on a bounded sample.
 
 --impl reference runs the oracle itself as the reference arm (each step a
@@ -71,6 +72,7 @@ WORKLOADS = {
                                 "NTT + RowSel + INTT"),
 }
 METRIC = "DB GB/s scanned & queries/s (RowSel, 64 GiB DB), % of GB300 HBM roofline"
+SPEC_HBM_GBS = 8000.0   # nominal GB300 HBM3e bandwidth (context for the roofline fractions)
 EXPPACK_METRIC = "ring-packing GEMM H*C + (0|G): hint GB/s scanned"
 
 
@@ -682,6 +684,18 @@ def run_ours(args, cfg):
     if status:
         raise RuntimeError("device status word set: %d" % status)
 
+    # in-run read-only stream over the encoded DB (the ceiling of a pure read)
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sd.read_probe(db, sink, stream)
+    r0 = torch.cuda.Event(enable_timing=True)
+    r1 = torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for _ in range(3):
+        sd.read_probe(db, sink, stream)
+    r1.record(stream)
+    torch.cuda.synchronize()
+    read_probe_gbs = 3 * db.numel() * 4 / (r0.elapsed_time(r1) * 1e-3) / 1e9
+
     # ---- end to end through the public API: pinned host query in, result out.
     # Coefficient-form workloads use the pipelined query server (copies of
     # the neighbouring queries overlap each scan); NTT-form ones the plain
@@ -765,7 +779,9 @@ def run_ours(args, cfg):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": profile_traffic("%s_%s" % (kernel, args.workload)),
                          "kernel": kernel, "peak_source": "%s hbm_gbs (copy)" % peak_kind,
-                         "algorithmic_bytes_per_launch": algo_bytes, "tensor": tensor},
+                         "algorithmic_bytes_per_launch": algo_bytes, "tensor": tensor,
+                         "read_probe_gbs": read_probe_gbs, "frac_of_read_probe": achieved / read_probe_gbs,
+                         "spec_gbs": SPEC_HBM_GBS, "frac_of_spec": achieved / SPEC_HBM_GBS},
             "clocks": clk,
             "e2e": None if e2e_ms is None else {
                 "value": logical_db / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": q_bytes,

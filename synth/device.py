@@ -2,7 +2,8 @@
 
 Fills device buffers with the same values as the host generator in
 ``synth/__init__.py`` (same counter-based SplitMix64 definition), so that
-multi-GiB benchmark inputs never pass through the host.
+multi-GiB benchmark inputs never pass through the host.  Also wraps the
+benchmark's read-only HBM stream probe.
 """
 from __future__ import annotations
 
@@ -42,6 +43,8 @@ def lib():
         L.synth_fill_bytes.restype = ctypes.c_int
         L.synth_fill_bytes.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32,
                                        ctypes.c_uint32, ctypes.c_void_p]
+        L.synth_read_probe.restype = ctypes.c_int
+        L.synth_read_probe.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]
         _lib = L
     return _lib
 
@@ -69,4 +72,11 @@ def fill_residues(t, seed, tid, N, qs, idx0=0, stream=None):
 
 def fill_bytes(t, seed, tid, idx0=0, stream=None):
     rc = lib().synth_fill_bytes(t.data_ptr(), t.numel(), idx0, seed, tid, _stream(stream))
+    assert rc == 0, rc
+
+
+def read_probe(t, sink, stream=None):
+    """One read-only pass over the bytes of device tensor t (sink: 1 int32 on the device)."""
+    rc = lib().synth_read_probe(t.data_ptr(), t.numel() * t.element_size() // 16 * 16, sink.data_ptr(),
+                                _stream(stream))
     assert rc == 0, rc

@@ -4,7 +4,8 @@
 //     v = splitmix64((tid << 56) ^ (seed << 48) ^ idx)
 // with splitmix64 the SplitMix64 output function (Steele, Lea, Flood,
 // OOPSLA 2014) applied to x + 0x9E3779B97F4A7C15.  Holds no arithmetic of
-// the PIR method; it only fills buffers with test and benchmark inputs.
+// the PIR method; it only fills buffers with test and benchmark inputs, and
+// has one measurement helper for the benchmark: a read-only HBM stream.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -57,6 +58,25 @@ __global__ void fill_bytes(uint8_t *out, uint64_t count, uint64_t idx0, uint32_t
     }
 }
 
+// Read-only stream over n 16-byte words: each thread folds its loads into
+// one word, stored only on a match that random data almost never gives;
+// the store depends on every load, so none is dropped.
+__global__ void __launch_bounds__(512) read_probe(const uint4 *__restrict__ p, uint64_t n, uint32_t *sink) {
+    uint32_t acc = 0;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n; i += 4 * stride) {
+        const uint4 a = __ldcs(p + i), b = __ldcs(p + i + stride), c = __ldcs(p + i + 2 * stride),
+                    d = __ldcs(p + i + 3 * stride);
+        acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^ d.z ^ d.w;
+    }
+    for (; i < n; i += stride) {
+        const uint4 a = __ldcs(p + i);
+        acc ^= a.x ^ a.y ^ a.z ^ a.w;
+    }
+    if (acc == 0x9E3779B9u) sink[0] = acc;   // data-dependent: keeps every load
+}
+
 int grid_for(uint64_t count) {
     uint64_t g = (count + 255) / 256;
     if (g > 152ull * 64) g = 152ull * 64;
@@ -83,5 +103,16 @@ extern "C" int synth_fill_bytes(uint8_t *out, uint64_t count, uint64_t idx0, uin
     if (!out || count % 16 || (reinterpret_cast<uintptr_t>(out) & 15)) return -1;
     if (count == 0) return 0;
     fill_bytes<<<grid_for(count / 16), 256, 0, (cudaStream_t)stream>>>(out, count, idx0, seed, tid);
+    return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
+
+// Reads `bytes` (a multiple of 16, 16-byte aligned) of device memory once.
+extern "C" int synth_read_probe(const void *p, uint64_t bytes, uint32_t *sink, void *stream) {
+    if (!p || !sink || (bytes & 15) || (reinterpret_cast<uintptr_t>(p) & 15)) return -1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return -2;
+    read_probe<<<sms * 4, 512, 0, (cudaStream_t)stream>>>(static_cast<const uint4 *>(p), bytes / 16, sink);
     return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
