@@ -126,6 +126,20 @@ __device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t adesc, uint64_t
         : "memory");
 }
 
+// The four K = 16 MMAs of one stage; descriptors advance 32 bytes (2 units) per
+// MMA inside the 128-byte swizzle atom.  acc = 0 starts the accumulator.
+__device__ __forceinline__ void mma4(uint32_t d, uint64_t ad, uint64_t bd, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p, t;\nsetp.ne.b32 p, %3, 0;\nsetp.eq.b32 t, %3, %3;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %4, t;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %4, t;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %4, t;\n}\n" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(acc), "r"(SC_IDESC), "l"(ad + 2), "l"(bd + 2), "l"(ad + 4), "l"(bd + 4), "l"(ad + 6),
+        "l"(bd + 6)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
@@ -229,34 +243,36 @@ __global__ void __launch_bounds__(SC_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t it = 0, g = 0;
+            bool ab = false;
+            uint32_t g = 0, s = 0, ph = 0;
+            const uint64_t ad0 = sdesc_sw128(smem_u32(stA)), bd0 = sdesc_sw128(smem_u32(stB));
             for (uint32_t t = blockIdx.x; t < A.ntiles; t += gridDim.x) {
+                ab = ab || abort_flag;
                 for (uint32_t ch = 0; ch < nchunks; ++ch, ++g) {
                     const uint32_t buf = g & 1, use = (g >> 1) & 1;
-                    bool ok = !abort_flag && mbar_wait(acce + buf, use ^ 1, A.status);
-                    if (!ok) abort_flag = 1;
-                    tc_fence_after();
+                    if (!ab && !mbar_wait(acce + buf, use ^ 1, A.status)) ab = true;
                     const uint32_t d = tmem + buf * SC_N;
-                    const uint32_t kb_end = min(A.nkb, (ch + 1) * SC_CHUNK_STAGES);
-                    for (uint32_t kb = ch * SC_CHUNK_STAGES; kb < kb_end; ++kb, ++it) {
-                        const uint32_t s = it % SC_NS, ph = (it / SC_NS) & 1;
-                        if (!abort_flag && !mbar_wait(conv + s, ph, A.status)) abort_flag = 1;
-                        if (abort_flag) continue;
-                        tc_fence_after();
-                        const uint32_t a0 = smem_u32(stA + s * SC_A_BYTES), b0 = smem_u32(stB + s * SC_B_BYTES);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)   // K = 16 fp16 = 32 bytes per MMA
-                            mma_f16(d, sdesc_sw128(a0 + 32 * k), sdesc_sw128(b0 + 32 * k),
-                                    (kb > ch * SC_CHUNK_STAGES || k > 0) ? 1u : 0u);
-                        mma_commit(empty + s);        // stage reusable once these MMAs finish
+                    const uint32_t kb0 = ch * SC_CHUNK_STAGES, kb_end = min(A.nkb, kb0 + SC_CHUNK_STAGES);
+                    for (uint32_t kb = kb0; kb < kb_end; ++kb) {
+                        if (!ab && !mbar_wait(conv + s, ph, A.status)) ab = true;
+                        if (!ab) {
+                            tc_fence_after();
+                            mma4(d, ad0 + s * (SC_A_BYTES >> 4), bd0 + s * (SC_B_BYTES >> 4), kb > kb0);
+                            mma_commit(empty + s);        // stage reusable once these MMAs finish
+                        }
+                        if (++s == SC_NS) {
+                            s = 0;
+                            ph ^= 1;
+                        }
                     }
-                    if (!abort_flag) mma_commit(accf + buf);  // chunk complete -> epilogue
+                    if (!ab) mma_commit(accf + buf);  // chunk complete -> epilogue
                 }
             }
-            // all issued MMAs complete before TMEM is released
+            if (ab) abort_flag = 1;
             mma_commit(done);
             mbar_wait(done, 0, A.status);
         }
+
     } else if (warp < 6) {
         // ------------------------------------------------ converters: bytes -> fp16, swizzled
         const uint32_t ct = threadIdx.x - 64;  // 0..127
