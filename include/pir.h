@@ -45,7 +45,7 @@ extern "C" {
 #define PIR_OK 0
 #define PIR_ERR_ARG (-1)          /* invalid argument (size, pointer, parameters) */
 #define PIR_ERR_CUDA (-2)         /* a CUDA runtime/driver call or launch failed */
-#define PIR_ERR_UNSUPPORTED (-3)  /* valid but outside what this build supports */
+#define PIR_ERR_UNSUPPORTED (-3)  /* valid but outside what the library implements */
 #define PIR_ERR_ALLOC (-4)        /* pir_ctx_create / pir_server_create could not allocate */
 
 /* Bits of the device status word (pir_status). */
