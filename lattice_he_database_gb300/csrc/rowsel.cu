@@ -166,8 +166,8 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
     extern __shared__ __align__(128) uint32_t smw[];
     uint32_t *ring = smw;                                    // NST * STAGE_WORDS
     uint32_t *in0s = ring + NST * STAGE_WORDS;               // nb * PS   (k-major query slices)
-    uint32_t *red = in0s + (size_t)A.nb * A.PS;              // ksplit * Mp * 128
-    uint64_t *bars = reinterpret_cast<uint64_t *>(red + (A.ksplit > 1 ? A.ksplit * A.Mp * PIR_SLAB : 0));
+    uint32_t *red = in0s + (size_t)A.nb * A.PS;              // Mp * 128 sums of the ksplit partials
+    uint64_t *bars = reinterpret_cast<uint64_t *>(red + (A.ksplit > 1 ? A.Mp * PIR_SLAB : 0));
     uint64_t *full = bars, *empty = bars + NST, *qfull = bars + 2 * NST, *qempty = qfull + 2;
     __shared__ volatile int abort_flag;
 
@@ -188,6 +188,8 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
         abort_flag = 0;
         fence_mbar_init();
     }
+    if (A.ksplit > 1)   // the partial-sum rows start at zero; each unit's reader clears what it read
+        for (uint32_t i = threadIdx.x; i < A.Mp * PIR_SLAB; i += blockDim.x) red[i] = 0;
     __syncthreads();
 
     // ------------------------------------------------------------ producer
@@ -345,20 +347,22 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
                 }
             }
         } else {
-            named_barrier(1, NWC * 32);  // previous unit's readers of `red` are done
+            // the ksplit partial residues of an output are summed with shared-
+            // memory atomics (at most 8 residues < 2^29: the sum fits 32 bits)
+            named_barrier(1, NWC * 32);  // previous unit's readers have read and cleared `red`
             if (active) {
 #pragma unroll
                 for (int i = 0; i < MT; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        red[(ks * A.Mp + ms * MT + i) * PIR_SLAB + 4 * lane + j] = barrett64(acc[i][j], q, mu);
+                        atomicAdd(red + (ms * MT + i) * PIR_SLAB + 4 * lane + j, barrett64(acc[i][j], q, mu));
             }
             named_barrier(1, NWC * 32);
             const uint32_t tot = A.Mv * Ws;
             for (uint32_t idx = ctid; idx < tot; idx += NWC * 32) {
                 const uint32_t m = idx / Ws, col = idx - m * Ws;
-                uint32_t sum = 0;  // < ksplit * q < 2^32
-                for (uint32_t kk = 0; kk < A.ksplit; ++kk) sum += red[(kk * A.Mp + m) * PIR_SLAB + col];
+                const uint32_t sum = red[m * PIR_SLAB + col];
+                red[m * PIR_SLAB + col] = 0;
                 ot[(uint64_t)m * A.D1p + col] = sum % q;
             }
         }
@@ -367,7 +371,7 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
 
 size_t rowsel_smem(const RowselArgs &A, uint32_t nb) {
     return (size_t)NST * STAGE_WORDS * 4 + (size_t)nb * A.PS * 4 +
-           (A.ksplit > 1 ? (size_t)A.ksplit * A.Mp * PIR_SLAB * 4 : 0) + (2 * NST + 4) * sizeof(uint64_t);
+           (A.ksplit > 1 ? (size_t)A.Mp * PIR_SLAB * 4 : 0) + (2 * NST + 4) * sizeof(uint64_t);
 }
 
 template <int MT>
