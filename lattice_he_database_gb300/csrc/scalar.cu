@@ -28,7 +28,8 @@
 //               two 256-column fp32 accumulators (double buffered so that a
 //               drain overlaps the next chunk's MMAs);
 //   warps 2-5   converters: DB bytes -> fp16 in the 128B-swizzled K-major
-//               layout the MMA reads;
+//               layout the MMA reads; two groups of two warps take the even
+//               and the odd stages, so two stages convert at once;
 //   warps 6-9   epilogue: tcgen05.ld of a drained accumulator, integer
 //               conversion and the shifted accumulation; one row per thread;
 //               the 64 running sums per row are written at the end of a tile.
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < SC_NS; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(conv + s, 4);
+            mbar_init(conv + s, 2);
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -275,18 +276,23 @@ __global__ void __launch_bounds__(SC_THREADS, 1)
 
     } else if (warp < 6) {
         // ------------------------------------------------ converters: bytes -> fp16, swizzled
-        const uint32_t ct = threadIdx.x - 64;  // 0..127
+        // two groups of two warps on alternating stages: warps 2, 3 the even
+        // stages, warps 4, 5 the odd ones (with SC_NS = 4 a ring slot always
+        // belongs to the same group, so parity waits never skip a phase)
+        const uint32_t grp = (uint32_t)(warp - 2) >> 1;
+        const uint32_t ct = ((uint32_t)(warp - 2) & 1u) * 32u + lane;   // 0..63 within the group
         uint32_t it = 0;
         for (uint32_t t = blockIdx.x; t < A.ntiles; t += gridDim.x) {
             for (uint32_t kb = 0; kb < A.nkb; ++kb, ++it) {
+                if ((it & 1u) != grp) continue;
                 const uint32_t s = it % SC_NS, ph = (it / SC_NS) & 1;
                 if (!abort_flag && !mbar_wait(full + s, ph, A.status)) abort_flag = 1;
                 if (!abort_flag) {
                     const uint8_t *u = stU + s * SC_U8_BYTES;
                     uint8_t *a = stA + s * SC_A_BYTES;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t q = ct + 128 * i;          // 16-byte piece: row q/4, part q%4
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t q = ct + 64 * i;           // 16-byte piece: row q/4, part q%4
                         const uint32_t row = q >> 2, part = q & 3;
                         const uint4 w = *reinterpret_cast<const uint4 *>(u + row * SC_KB + part * 16);
                         const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
