@@ -119,14 +119,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 // kind::f16, A = B = F16, D = F32, K-major A and B, N = 256, M = 128
 constexpr uint32_t SC_IDESC = (1u << 4) | ((uint32_t)(SC_N >> 3) << 17) | ((uint32_t)(SC_TM >> 4) << 24);
 
-__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
-        "l"(adesc), "l"(bdesc), "r"(SC_IDESC), "r"(accumulate)
-        : "memory");
-}
-
 // The four K = 16 MMAs of one stage; descriptors advance 32 bytes (2 units) per
 // MMA inside the 128-byte swizzle atom.  acc = 0 starts the accumulator.
 __device__ __forceinline__ void mma4(uint32_t d, uint64_t ad, uint64_t bd, uint32_t acc) {
