@@ -448,8 +448,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     // Every partial sum of the estimate is below 128 * D0 * (2^24 + q)
                     // <= 2^46, so its three roundings add at most 3 * 2^22, and
                     // |W| / q <= 128 * D0 = 2^16; with q >= 2^26 the estimate of W / q
-                    // is off by less than 0.2, W - k*q lies in (-0.7q, 1.7q) and one
-                    // conditional add or subtract of q ends the reduction.
+                    // is off by less than 0.2 and W - k*q lies in (-0.7q, 1.7q).
                     uint32_t lo[32];
                     float wf[32];
 #pragma unroll
@@ -479,12 +478,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     named_barrier(2, 128);                    // previous tile's readers of red are done
 #pragma unroll
                     for (int n = 0; n < 32; ++n) {
+                        // W - k*q lies in (-0.7q, 1.7q); + q makes it a positive 32-bit value
+                        // congruent to W, which the Shoup product accepts as is: 2^(8i) * W
+                        // mod q lands in [0, 2q)
                         const int32_t k = __float2int_rn(wf[n] * qinv);
-                        int32_t rs = (int32_t)(lo[n] - (uint32_t)k * q);
-                        rs += rs < 0 ? (int32_t)q : 0;
-                        const uint32_t r = (uint32_t)rs >= q ? (uint32_t)rs - q : (uint32_t)rs;
-                        uint32_t u = shoup_mul(r, ci, cis, q);
-                        red[(plane * 32 + m) * TC_RED_PITCH + n] = u >= q ? u - q : u;
+                        const uint32_t r = lo[n] - (uint32_t)k * q + q;
+                        red[(plane * 32 + m) * TC_RED_PITCH + n] = shoup_mul(r, ci, cis, q);
                     }
                     named_barrier(2, 128);
                     for (uint32_t idx = etid; idx < 32 * 32; idx += 128) {
@@ -492,11 +491,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         const uint32_t col = t * TC_NT + nn;
                         if (mm >= A.Mv || col >= Ws) continue;
                         const uint32_t n_glob = s * PIR_SLAB + col;
-                        uint32_t x = red[mm * TC_RED_PITCH + nn] + red[(32 + mm) * TC_RED_PITCH + nn];
-                        x = x >= q ? x - q : x;
-                        uint32_t y = red[(64 + mm) * TC_RED_PITCH + nn] + red[(96 + mm) * TC_RED_PITCH + nn];
-                        y = y >= q ? y - q : y;
-                        x += y;
+                        // four plane terms, each in [0, 2q): the sum is below 8q < 2^32
+                        uint32_t x = red[mm * TC_RED_PITCH + nn] + red[(32 + mm) * TC_RED_PITCH + nn] +
+                                     red[(64 + mm) * TC_RED_PITCH + nn] + red[(96 + mm) * TC_RED_PITCH + nn];
+                        x = x >= 4 * q ? x - 4 * q : x;
+                        x = x >= 2 * q ? x - 2 * q : x;
                         x = x >= q ? x - q : x;
                         A.outT[(p * A.Mv + mm) * A.D1p + n_glob] = x;
                     }

@@ -8,12 +8,16 @@ bounding S_3), without 64-bit arithmetic:
     lo = sum_j S_j << 8j              (wrapping 32-bit)
     wf = fma(S_3, 2^24, fma(S_2, 2^16, fma(S_1, 2^8, S_0)))   (fp32)
     k  = round_to_int(wf * fp32(1/q))
-    r  = lo - k*q (signed 32-bit), + q if negative, - q if >= q
+    r  = lo - k*q + q                 (wrapping 32-bit; must be in [0, 2^32))
+    u  = Shoup product r * (2^(8i) mod q), in [0, 2q)
+and the four digit planes i of one output are summed (below 8q) and
+reduced by conditional subtractions of 4q, 2q and q.
 
-This test replays those fp32 operations bit-exactly on the CPU (an fma is
-one rounding of the exact float64 value, which holds all the digits here)
-and checks r == W mod q for the largest partial sums the kernel can see,
-for primes from 2^26 (the smallest the kernel accepts) to 2^29.
+This test replays those operations bit-exactly on the CPU (an fma is one
+rounding of the exact float64 value, which holds all the digits here) and
+checks every step's range and the final residue against the exact value,
+for the largest partial sums the kernel can see and primes from 2^26 (the
+smallest the kernel accepts) to 2^29.
 """
 import numpy as np
 import pytest
@@ -36,11 +40,32 @@ def epilogue_reduce(S, q):
         wf = _f32(S[..., j].astype(np.float64) * float(1 << (8 * j)) + wf.astype(np.float64))
     qinv = np.float32(1.0) / np.float32(q)
     k = np.rint((wf * qinv).astype(np.float32)).astype(np.int64)          # __float2int_rn
-    r = ((lo.astype(np.int64) - k * q) & 0xFFFFFFFF).astype(np.int64)
-    r = np.where(r >= 1 << 31, r - (1 << 32), r)                            # signed 32-bit
-    r = np.where(r < 0, r + q, r)
-    r = np.where(r >= q, r - q, r)
-    return r
+    signed = ((lo.astype(np.int64) - k * q) & 0xFFFFFFFF).astype(np.int64)
+    signed = np.where(signed >= 1 << 31, signed - (1 << 32), signed)        # W - k*q as signed 32-bit
+    return signed + q                                                        # the kernel's r (unsigned)
+
+
+def shoup(y, w, q):
+    """Shoup product of 32-bit y by w < q: y*w mod q in [0, 2q)."""
+    wp = (w << 32) // q
+    y = np.asarray(y, dtype=object)
+    return np.array([(int(v) * w - ((int(v) * wp) >> 32) * q) & 0xFFFFFFFF for v in y.ravel()],
+                    dtype=np.int64).reshape(y.shape)
+
+
+def epilogue_output(S4, q):
+    """Full epilogue for S4 of shape [..., 4 planes, 4 byte planes]: the output residue."""
+    x = np.zeros(S4.shape[:-2], dtype=np.int64)
+    for i in range(4):
+        r = epilogue_reduce(S4[..., i, :], q)
+        assert (r > 0).all() and (r < 1 << 31).all()
+        u = shoup(r, pow(2, 8 * i, q), q)
+        assert (u < 2 * q).all()
+        x = x + u
+    assert (x < 8 * q).all()
+    for c in (4, 2, 1):
+        x = np.where(x >= c * q, x - c * q, x)
+    return x
 
 
 def _bounds(q, D0):
@@ -68,10 +93,16 @@ def test_reduction_exact_on_extremes(q):
     S = np.concatenate([corners * b, (corners * b) // 3,
                         rng.integers(-b, b + 1, size=(200000, 4), dtype=np.int64)])
     W = (S * (np.int64(1) << (8 * np.arange(4, dtype=np.int64)))).sum(axis=1)
-    want = np.mod(W, q)
-    got = epilogue_reduce(S, q)
+    r = epilogue_reduce(S, q)
+    # r is congruent to W, positive and below 2q + 0.7q (a valid Shoup input)
+    assert (np.mod(r - W, q) == 0).all() and (r > 0).all() and (r < 3 * q).all()
+    # the whole output path on groups of four planes
+    S4 = S[: (S.shape[0] // 4) * 4][:4000].reshape(-1, 4, 4)
+    W4 = (S4 * (np.int64(1) << (8 * np.arange(4, dtype=np.int64)))).sum(axis=2)
+    want = np.array([sum(int(W4[g, i]) << (8 * i) for i in range(4)) % q for g in range(W4.shape[0])])
+    got = epilogue_output(S4, q)
     bad = np.nonzero(got != want)[0]
-    assert bad.size == 0, (q, S[bad[:5]], got[bad[:5]], want[bad[:5]])
+    assert bad.size == 0, (q, got[bad[:5]], want[bad[:5]])
 
 
 def test_reduction_needs_the_prime_bound():
@@ -84,4 +115,5 @@ def test_reduction_needs_the_prime_bound():
     b = np.array([128 * 255 * D0] * 3 + [0], dtype=np.int64)
     S = np.random.default_rng(5).integers(-b, b + 1, size=(20000, 4), dtype=np.int64)
     W = (S * (np.int64(1) << (8 * np.arange(4, dtype=np.int64)))).sum(axis=1)
-    assert (epilogue_reduce(S, q) != np.mod(W, q)).any()
+    r = epilogue_reduce(S, q)
+    assert ((np.mod(r - W, q) != 0) | (r <= 0) | (r >= 3 * q)).any()
