@@ -47,6 +47,8 @@ WORKLOADS = {
                       desc="RowSel 6 GiB: N=4096, 3 primes, D0=256 x D1=512, B=1, NTT-domain query"),
     "rowsel_24g_b16": dict(N=4096, L=3, D0=512, D1=1024, B=16, domain="ntt",
                            desc="RowSel 24 GiB: N=4096, 3 primes, D0=512 x D1=1024, B=16 queries, NTT-domain"),
+    "rowsel_64g_b16": dict(N=4096, L=3, D0=1024, D1=1365, B=16, domain="ntt",
+                           desc="RowSel 64 GiB: N=4096, 3 primes, D0=1024 x D1=1365, B=16 queries, NTT-domain"),
     # scalar-HE scan: byte DB x 64 query words mod 2^32 (tcgen05 fp16 path)
     "scalar_16g": dict(kind="scalar", R=131072, C=131072, B=64,
                        desc="Scalar-HE scan: DB 131072 x 131072 uint8 (16 GiB) x Q 131072 x 64 uint32, mod 2^32"),
@@ -339,12 +341,18 @@ def run_reference(args, cfg):
 
 # ---------------------------------------------------------------- GPU leg
 def rowsel_passes(D0, B) -> int:
-    """Query passes of one RowSel call: queries per pass follow the on-chip
-    query-slice budget (112 KiB of 4-byte residues for 2 polynomials each)."""
+    """Query passes of one RowSel call (primes >= 2^26): 16 queries on the
+    tensor cores while more than 8 remain, the rest on the CUDA cores as many
+    as their on-chip query slice holds (112 KiB of 4-byte residues, 2
+    polynomials per query)."""
     cap = 32
     while cap > 2 and D0 * cap * 4 > 112 * 1024:
         cap //= 2
-    return -(-B // (cap // 2))
+    passes, left = 0, B
+    while left:
+        left -= min(left, 16) if left > 8 else min(left, cap // 2)
+        passes += 1
+    return passes
 
 
 def launches_per_step(cfg) -> int:
@@ -746,8 +754,8 @@ def run_ours(args, cfg):
     hbm_peak = float(peaks["hbm_gbs"])
     algo_bytes = logical_db + q_bytes + o_bytes       # the RowSel kernel's algorithmic bytes per launch
     achieved = algo_bytes / (rowsel_ms * 1e-3) / 1e9
-    # passes of 9..16 queries with D0 <= 512 run on the tensor cores (primes >= 2^26 here)
-    on_tensor = 8 < B <= 16 and D0 <= 512
+    # passes of 9..16 queries run on the tensor cores (primes >= 2^26 here)
+    on_tensor = 8 < B <= 16
     kernel = "rowsel_tc_kernel" if on_tensor else "rowsel_kernel"
     tensor = None
     if on_tensor:

@@ -183,12 +183,13 @@ uint64_t pir_rowsel_workspace_bytes(const pir_ctx *ctx, uint32_t D0, uint32_t D1
  *               order and the results before they are transposed back
  *               (GPIR's NTT-to-GEMM layout change, both directions);
  *               contents undefined after the call.
- * The DB is read from HBM once per pass; a pass covers as many queries as
- * fit the on-chip query buffer (16 queries for D0 <= 896, fewer for larger
- * D0); larger batches take ceil(B / per-pass) passes.  A pass of 9 to 16
- * queries with D0 <= 512 and every q_l >= 2^26 runs on the tensor cores
- * (exact fp16 digit products); every other pass on the CUDA cores.  Both
- * give the same canonical residues.
+ * The DB is read from HBM once per pass.  When every q_l >= 2^26, passes of
+ * 16 queries run on the tensor cores (exact fp16 digit products, the rows
+ * taken in K segments of 512) while more than 8 queries remain, any D0; a
+ * last pass of 9 to 15 queries too.  Every other pass (8 queries or fewer,
+ * or primes below 2^26) runs on the CUDA cores and covers as many queries
+ * as fit its on-chip query buffer (16 for D0 <= 896, fewer for larger D0).
+ * Both give the same canonical residues.
  * Errors: PIR_ERR_ARG (zero sizes, NULL/unaligned, workspace too small),
  * PIR_ERR_CUDA, PIR_ERR_UNSUPPORTED (D0 > 14336).
  */

@@ -418,11 +418,20 @@ uint32_t padded_mp(uint32_t Mv) {
 }  // namespace
 
 // Tensor-core path for large batches (rowsel_tc.cu).
-bool rowsel_tc_eligible(const pir_ctx *ctx, uint32_t D0, uint32_t Mv);
+bool rowsel_tc_primes_ok(const pir_ctx *ctx);
 int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, const uint32_t *qT, uint32_t PS,
                    uint32_t Mv, uint32_t *outT, cudaStream_t st);
 
 namespace {
+
+// Queries in the next pass when `left` remain: 16 on the tensor cores while
+// more than 8 remain (passes of 17..32 polynomials, any D0), otherwise as
+// many as one on-chip query slice of the CUDA-core kernel holds (cap
+// polynomials).  The pass runs on the tensor cores iff it has more than 8.
+uint32_t pass_queries(bool tc, uint32_t cap, uint32_t left) {
+    if (tc && left > 8) return left < 16 ? left : 16;
+    return left < cap / 2 ? left : cap / 2;
+}
 
 // Workspace: the pass's query slices (point-major) followed by the pass's
 // results (point-major, 256-byte aligned).
@@ -434,7 +443,13 @@ WsLayout ws_layout(const pir_ctx *ctx, uint32_t D0, uint32_t D1, uint32_t B) {
     WsLayout w{0, 0, 0};
     const uint32_t cap = mp_capacity(D0);
     if (!cap) return w;
-    const uint32_t nb = B < cap / 2 ? B : cap / 2;   // queries in the largest pass
+    const bool tc = rowsel_tc_primes_ok(ctx);
+    uint32_t nb = 0;   // queries in the largest pass
+    for (uint32_t left = B; left;) {
+        const uint32_t n = pass_queries(tc, cap, left);
+        nb = n > nb ? n : nb;
+        left -= n;
+    }
     const uint32_t mp = padded_mp(2 * nb);
     const uint64_t P = (uint64_t)ctx->L * ctx->N;
     const uint64_t ps = ((uint64_t)D0 * mp + 3) / 4 * 4;
@@ -492,10 +507,10 @@ int rowsel_impl(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, cons
     }
     const uint32_t cap = mp_capacity(D0);
     if (!cap) return PIR_ERR_UNSUPPORTED;
-    const uint32_t b_per_pass = cap / 2;
+    const bool tc = rowsel_tc_primes_ok(ctx);
     cudaStream_t st = (cudaStream_t)stream;
-    for (uint32_t b0 = 0; b0 < B; b0 += b_per_pass) {
-        const uint32_t nb = min(b_per_pass, B - b0);
+    for (uint32_t b0 = 0, nb = 0; b0 < B; b0 += nb) {
+        nb = pass_queries(tc, cap, B - b0);
         A.b0 = b0;
         A.Mv = 2 * nb;
         A.Mp = padded_mp(A.Mv);
@@ -506,7 +521,7 @@ int rowsel_impl(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, cons
         transpose_query_kernel<<<tgrid, 256, 0, st>>>(query, qT, A.P, D0, A.Mp, A.Mv, b0, A.PS);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
         int rc = PIR_OK;
-        if (rowsel_tc_eligible(ctx, D0, A.Mv)) {  // 17..32 polynomials, q >= 2^26: exact fp16 tensor-core GEMMs
+        if (tc && nb > 8) {  // 17..32 polynomials, q >= 2^26: exact fp16 tensor-core GEMMs
             rc = rowsel_tc_pass(ctx, db, D0, D1, qT, A.PS, A.Mv, A.outT, st);
         // thread tile MT polynomials x 4 columns; warps split the padded
         // polynomials (msplit) and the rows of a chunk (ksplit >= 2)

@@ -11,25 +11,28 @@
 //     (a = sum_i 256^i a_i exactly; a_3 <= 32),
 //   * DB residues b < 2^29 as their plain bytes b_j in [0, 255],
 // so a*b = sum_{i,j} 256^(i+j) a_i b_j.  Every digit product is an integer of
-// magnitude <= 128*255, and D0 <= 512 of them sum below 2^24: exact in fp32.
+// magnitude <= 128*255, and 512 of them sum below 2^24: exact in fp32.  The
+// rows of a point are therefore taken in K segments of at most 512 rows.
 //
-// MMA tile (one per 32 DB columns of a point): M = 128 rows (i, m) = 4 query
-// digit planes x 32 polynomials, N = 128 columns (j, n) = 4 DB byte planes x
-// 32 columns, K = D0.  The A operand (query digits of the point) sits in
-// TMEM for all tiles of the point; the accumulator (128 columns, double
-// buffered) then holds S_ij[m][n].  The epilogue forms
+// MMA tile (one per 32 DB columns of a point and segment): M = 128 rows
+// (i, m) = 4 query digit planes x 32 polynomials, N = 128 columns (j, n) =
+// 4 DB byte planes x 32 columns, K = the segment's rows.  The A operand
+// (query digits of the segment) sits in TMEM for all tiles of the segment;
+// the accumulator (128 columns, double buffered) then holds S_ij[m][n].
+// The epilogue forms
 //     out[m][n] = sum_i 2^(8i) (sum_j 2^(8j) S_ij[m][n])  mod q
 // with one reduction per (i, m, n) (32-bit arithmetic and an fp32 quotient
-// estimate, valid for q >= 2^26) and a cross-plane sum.
+// estimate, valid for q >= 2^26) and a cross-plane sum; segments after the
+// first add their residue to the stored one.
 //
 // Warp roles (512 threads, one CTA per SM, persistent over a range of points).
 // A warp's scheduler is fixed by warp % 4, and the MMA-issuing thread loses
 // most of its issue rate to any ALU-busy warp on its scheduler, so scheduler 1
 // carries only light roles besides the plane-1 epilogue:
-//   warps 0-3   query digits of the next point -> TMEM (tcgen05.st), warp w
+//   warps 0-3   query digits of the next segment -> TMEM (tcgen05.st), warp w
 //               writes digit plane w into TMEM lanes 32w..32w+31, from the
-//               point's query slice that the producer bulk-copies into
-//               shared memory while the previous point is still in flight
+//               segment's query slice that the producer bulk-copies into
+//               shared memory while the previous segment is still in flight
 //               (warps 0, 2, 3 also convert; warp 1 only writes digits);
 //   warps 4-7   epilogue: tcgen05.ld of a finished accumulator, reduction,
 //               cross-plane sum through shared memory, output stores;
@@ -66,9 +69,9 @@ constexpr uint32_t TC_B_BYTES = 128 * 128;             // 128 rows x 64 fp16
 constexpr int TC_THREADS = 16 * 32;
 constexpr uint32_t TC_TMEM_COLS = 512;
 constexpr uint32_t TC_ACC_COL = 256;           // accumulators at columns 256 and 384
-constexpr uint32_t TC_MAX_D0 = 512;            // exactness bound of one fp32 accumulation
+constexpr uint32_t TC_SEG = 512;               // rows per K segment: the exactness bound of one fp32 accumulation
 constexpr uint32_t TC_MIN_Q = 1u << 26;        // smallest prime the epilogue's reduction supports
-constexpr uint32_t TC_Q_BYTES = TC_MAX_D0 * 32 * 4;     // one point's query slice (64 KiB)
+constexpr uint32_t TC_Q_BYTES = TC_SEG * 32 * 4;        // one segment's query slice (64 KiB)
 constexpr uint32_t TC_RED_PITCH = 33;          // words per row of the epilogue's plane sums (no bank conflicts)
 constexpr uint32_t TC_PREFETCH_PIECE = 64 * 1024;
 
@@ -76,7 +79,8 @@ struct TcArgs {
     const uint32_t *qT;     // point-major query, [P][PS], 32 polynomials per k
     uint32_t *outT;         // point-major results [P][Mv][D1p]
     uint32_t *status;
-    uint32_t N, D0, D1, D1p, S, Wlast, PS, Kp, Mv;
+    uint32_t N, D0, D1, D1p, S, Wlast, PS, Mv;
+    uint32_t H, Dlast;      // K segments of TC_SEG rows per point (the last has Dlast rows)
     uint64_t P;
     uint32_t q[PIR_MAX_RNS];
     float qinv[PIR_MAX_RNS];          // 1/q rounded to fp32 (quotient estimate of the epilogue)
@@ -166,6 +170,12 @@ __device__ __forceinline__ uint32_t digit_pair(uint32_t a0, uint32_t a1, uint32_
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
+// Rows of K segment h and its 64-row stage count.
+__device__ __forceinline__ uint32_t seg_rows(const TcArgs &A, uint32_t h) { return h + 1 < A.H ? TC_SEG : A.Dlast; }
+__device__ __forceinline__ uint32_t seg_stages(const TcArgs &A, uint32_t h) {
+    return (seg_rows(A, h) + TC_KS - 1) / TC_KS;
+}
+
 // Number of 32-column tiles of slab s.
 __device__ __forceinline__ uint32_t tiles_of(const TcArgs &A, uint32_t s) {
     const uint32_t w = (s == A.S - 1) ? A.Wlast : PIR_SLAB;
@@ -242,7 +252,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t p_begin = (uint64_t)blockIdx.x * A.P / gridDim.x;
     const uint64_t p_end = (uint64_t)(blockIdx.x + 1) * A.P / gridDim.x;
-    const uint32_t nks = A.Kp / TC_KS;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_NR; ++s) {
@@ -278,25 +287,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     if (warp == 9 && lane == 0) {
         // ------------------------------------------------ TMA producer: query slices and DB word tiles
-        // The next point's query slice is prefetched into L2 a point ahead.
+        // The next segment's query slice is prefetched into L2 a segment ahead.
         // (Prefetching whole DB slab blocks ahead was measured too: 152 SMs x
         // two 256 KiB slabs crowd the L2 next to the streaming result writes,
         // and 40% of the DB was read twice.)
         const uint64_t pol = policy_evict_first();
-        const uint32_t qbytes = A.PS * 4;
         uint32_t it = 0, pc = 0;
 
-        for (uint64_t p = p_begin; p < p_end; ++p, ++pc) {
-            // the point's query slice (the query warps release the buffer once digitised)
+        for (uint64_t p = p_begin; p < p_end; ++p)
+          for (uint32_t h = 0; h < A.H; ++h, ++pc) {
+            // the segment's query slice (the query warps release the buffer once digitised)
+            const uint32_t nks = seg_stages(A, h), qbytes = seg_rows(A, h) * 32 * 4;
+            const uint32_t *qsrc = A.qT + p * A.PS + (uint64_t)h * TC_SEG * 32;
             if (abort_flag || !mbar_wait(qempty, (pc & 1) ^ 1, A.status)) {
                 abort_flag = 1;
             } else {
                 mbar_arrive_expect_tx(qfull, qbytes);
-                bulk_g2s(qsm, A.qT + p * A.PS, qbytes, qfull, pol);
+                bulk_g2s(qsm, qsrc, qbytes, qfull, pol);
             }
-            if (p + 1 < p_end) l2_prefetch(A.qT + (p + 1) * A.PS, qbytes);
+            if (h + 1 < A.H)
+                l2_prefetch(qsrc + TC_SEG * 32, seg_rows(A, h + 1) * 32 * 4);
+            else if (p + 1 < p_end)
+                l2_prefetch(A.qT + (p + 1) * A.PS, seg_rows(A, 0) * 32 * 4);
             for (uint32_t s = 0; s < A.S; ++s) {
-
                 const uint32_t nt = tiles_of(A, s);
                 for (uint32_t t = 0; t < nt; ++t)
                     for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
@@ -306,15 +319,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             continue;
                         }
                         mbar_arrive_expect_tx(rfull + st, TC_RAW_BYTES);
+                        const int y = (int)(h * TC_SEG + ks * TC_KS);   // DB row; rows >= D0 read as zero
                         if (s + 1 < A.S)
-                            tma_load_4d(stR + st * TC_RAW_BYTES, &full_map, (int)(t * TC_NT), (int)(ks * TC_KS),
-                                        (int)s, (int)p, rfull + st, pol);
+                            tma_load_4d(stR + st * TC_RAW_BYTES, &full_map, (int)(t * TC_NT), y, (int)s, (int)p,
+                                        rfull + st, pol);
                         else
-                            tma_load_4d(stR + st * TC_RAW_BYTES, &last_map, (int)(t * TC_NT), (int)(ks * TC_KS), 0,
-                                        (int)p, rfull + st, pol);
+                            tma_load_4d(stR + st * TC_RAW_BYTES, &last_map, (int)(t * TC_NT), y, 0, (int)p,
+                                        rfull + st, pol);
                     }
             }
-        }
+          }
         for (uint32_t i = 0; i < TC_NR && i < it; ++i) {  // copies in flight land first
             const uint32_t j = it - 1 - i;
             mbar_wait(rfull + j % TC_NR, (j / TC_NR) & 1, A.status);
@@ -328,9 +342,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         bool ab = false;
         uint32_t it = 0, g = 0, pc = 0, st = 0, ph = 0;
         const uint64_t bdesc0 = sdesc(smem_u32(stB));
-        for (uint64_t p = p_begin; p < p_end; ++p) {
+        for (uint64_t p = p_begin; p < p_end; ++p)
+          for (uint32_t h = 0; h < A.H; ++h) {
             ab = ab || abort_flag;
             bool first = true;
+            const uint32_t nks = seg_stages(A, h);
             for (uint32_t s = 0; s < A.S; ++s) {
                 const uint32_t nt = tiles_of(A, s);
                 for (uint32_t t = 0; t < nt; ++t, ++g) {
@@ -356,38 +372,40 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (!ab) commit(accf + buf);
                 }
             }
-            commit(aempty);  // A (query digits) reusable once this point's MMAs finish
+            commit(aempty);  // A (query digits) reusable once this segment's MMAs finish
             ++pc;
-        }
+          }
         if (ab) abort_flag = 1;
         commit(done);
         mbar_wait(done, 0, A.status);
     } else if (warp < 4 || (warp >= 8 && (warp & 3) != 1)) {
         // ------------------------------------------------ query digits and converters
-        // Warps 0-3 write the query digits of each point into TMEM (plane =
-        // warp) before that point's stages.  Three groups of three converter
+        // Warps 0-3 write the query digits of each segment into TMEM (plane =
+        // warp) before that segment's stages.  Three groups of three converter
         // warps -- {0, 2, 3}, {8, 10, 11}, {12, 14, 15} -- take every third
         // stage each; none of them shares a scheduler with the MMA warp (13).
         const bool digitizer = warp < 4, converter = warp != 1;
         const uint32_t gi = warp < 4 ? 0u : (uint32_t)(warp >> 2) - 1u;          // group 0..2
         const uint32_t gw = (warp & 3) == 0 ? 0u : (uint32_t)(warp & 3) - 1u;     // position 0..2
         uint32_t it = 0, pc = 0, sel = 0;                                         // sel = it % 3
-        for (uint64_t p = p_begin; p < p_end; ++p, ++pc) {
+        for (uint64_t p = p_begin; p < p_end; ++p)
+          for (uint32_t h = 0; h < A.H; ++h, ++pc) {
+            const uint32_t nks = seg_stages(A, h);
             if (digitizer) {
-                // query digits -> TMEM (plane = warp, polynomial m = lane)
-                const uint32_t plane = warp, m = lane;
+                // query digits of the segment -> TMEM (plane = warp, polynomial m = lane)
+                const uint32_t plane = warp, m = lane, rows = seg_rows(A, h);
                 if (!abort_flag && !mbar_wait(qfull, pc & 1, A.status)) abort_flag = 1;
                 if (!abort_flag && !mbar_wait(aempty, (pc & 1) ^ 1, A.status)) abort_flag = 1;
                 fence_after();
                 if (!abort_flag) {
                     const bool live = m < A.Mv;
-                    for (uint32_t kc = 0; kc < A.Kp / 64; ++kc) {
+                    for (uint32_t kc = 0; kc < nks; ++kc) {
                         uint32_t v[32];
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
                             const uint32_t k0 = kc * 64 + 2 * e;
-                            const uint32_t a0 = (live && k0 < A.D0) ? qsm[k0 * 32 + m] : 0u;
-                            const uint32_t a1 = (live && k0 + 1 < A.D0) ? qsm[(k0 + 1) * 32 + m] : 0u;
+                            const uint32_t a0 = (live && k0 < rows) ? qsm[k0 * 32 + m] : 0u;
+                            const uint32_t a1 = (live && k0 + 1 < rows) ? qsm[(k0 + 1) * 32 + m] : 0u;
                             v[e] = digit_pair(a0, a1, plane);
                         }
                         tmem_st32(tmem + ((plane * 32u) << 16) + kc * 32, v);
@@ -423,13 +441,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         if (lane == 0) mbar_arrive(bfull + bs);
                     }
             }
-        }
+          }
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------ epilogue
         const uint32_t plane = warp & 3, m = lane;
         const uint32_t etid = threadIdx.x - 128;  // 0..127
         uint32_t g = 0;
-        for (uint64_t p = p_begin; p < p_end; ++p) {
+        for (uint64_t p = p_begin; p < p_end; ++p)
+          for (uint32_t h = 0; h < A.H; ++h) {
             const uint32_t l = (uint32_t)(p / A.N);
             const uint32_t q = A.q[l];
             const float qinv = A.qinv[l];
@@ -445,9 +464,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     // mod q without 64-bit arithmetic.  Its low 32 bits come exactly
                     // from wrapping 32-bit sums of the integer plane sums S_j; the
                     // quotient k = round(W / q) comes from an fp32 estimate of W.
-                    // Every partial sum of the estimate is below 128 * D0 * (2^24 + q)
-                    // <= 2^46, so its three roundings add at most 3 * 2^22, and
-                    // |W| / q <= 128 * D0 = 2^16; with q >= 2^26 the estimate of W / q
+                    // Every partial sum of the estimate is below 128 * 512 * (2^24 + q)
+                    // <= 2^46 (a segment has at most 512 rows), so its three roundings
+                    // add at most 3 * 2^22, and |W| / q <= 128 * 512 = 2^16; with
+                    // q >= 2^26 the estimate of W / q
                     // is off by less than 0.2 and W - k*q lies in (-0.7q, 1.7q).
                     uint32_t lo[32];
                     float wf[32];
@@ -497,11 +517,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         x = x >= 4 * q ? x - 4 * q : x;
                         x = x >= 2 * q ? x - 2 * q : x;
                         x = x >= q ? x - q : x;
-                        A.outT[(p * A.Mv + mm) * A.D1p + n_glob] = x;
+                        uint32_t *o = A.outT + (p * A.Mv + mm) * A.D1p + n_glob;
+                        if (h) {   // later segments add to the sum this thread stored for the earlier ones
+                            x += *o;
+                            x = x >= q ? x - q : x;
+                        }
+                        *o = x;
                     }
                 }
             }
-        }
+          }
     }
 
     fence_before();
@@ -543,9 +568,8 @@ uint64_t powmod_host(uint64_t b, uint64_t e, uint64_t m) {
 
 }  // namespace
 
-// Whether a RowSel pass of Mv polynomials over D0 rows runs on this path.
-bool rowsel_tc_eligible(const pir_ctx *ctx, uint32_t D0, uint32_t Mv) {
-    if (Mv <= 16 || D0 > TC_MAX_D0) return false;
+// Whether the context's primes allow this path (passes of 17..32 polynomials).
+bool rowsel_tc_primes_ok(const pir_ctx *ctx) {
     for (uint32_t l = 0; l < ctx->L; ++l)
         if (ctx->q[l] < TC_MIN_Q) return false;   // the epilogue's quotient estimate needs q >= 2^26
     return true;
@@ -604,7 +628,8 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
     a.S = S;
     a.Wlast = Wlast;
     a.PS = PS;
-    a.Kp = (D0 + TC_KS - 1) / TC_KS * TC_KS;
+    a.H = (D0 + TC_SEG - 1) / TC_SEG;
+    a.Dlast = D0 - TC_SEG * (a.H - 1);
     a.Mv = Mv;
     a.P = P;
     for (uint32_t l = 0; l < ctx->L; ++l) {

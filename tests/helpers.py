@@ -13,6 +13,7 @@ CONFIGS = {
     "rowsel_6g": dict(N=4096, L=3, D0=256, D1=512, B=1, query_domain="ntt"),
     "rowsel_24g_b16": dict(N=4096, L=3, D0=512, D1=1024, B=16, query_domain="ntt"),
     "rowsel_64g": dict(N=4096, L=3, D0=1024, D1=1365, B=1, query_domain="coeff"),
+    "rowsel_64g_b16": dict(N=4096, L=3, D0=1024, D1=1365, B=16, query_domain="ntt"),
 }
 SCALAR = dict(R=131072, C=131072, B=64)
 

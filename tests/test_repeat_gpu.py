@@ -29,6 +29,7 @@ def pir():
 
 @pytest.mark.parametrize("D0,D1,B,launches", [
     (512, 64, 16, 40),     # tensor cores: 8192 points, 2 tiles per slab
+    (1100, 40, 16, 20),    # tensor cores, three K segments per point
     (256, 72, 1, 60),      # CUDA cores, ksplit = 8 partial sums per output
 ])
 def test_rowsel_repeated(pir, D0, D1, B, launches):

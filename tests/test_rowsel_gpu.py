@@ -45,6 +45,10 @@ def _small_case(pir, N, L, D0, D1, B, seed):
     (16, 2, 9, 44, 17),      # two passes (16 + 1)
     (16, 2, 512, 300, 16),   # tensor-core path: D0 = 512, 3 slabs (128 + 128 + 44)
     (64, 3, 100, 37, 12),    # tensor-core path, padded polynomials (24 of 32), ragged rows
+    (16, 2, 1000, 44, 16),   # tensor-core path, two K segments (512 + 488)
+    (16, 2, 1536, 40, 12),   # tensor-core path, three full K segments
+    (16, 1, 600, 130, 17),   # two passes: tensor cores (512 + 88 rows, 2 slabs), then 1 query on CUDA cores
+    (16, 2, 513, 9, 9),      # tensor-core path, second segment of a single row
 ])
 def test_encode_and_rowsel_small(pir, N, L, D0, D1, B):
     ctx, qs, psis, raw, db_t, query = _small_case(pir, N, L, D0, D1, B, seed=(N + D0 + D1 + B) % 251)
@@ -111,12 +115,14 @@ def test_rowsel_max_residues(pir, B, D0):
     assert pir.pir_status(ctx) == 0
 
 
-def test_rowsel_tensor_path_digit_extremes(pir):
+@pytest.mark.parametrize("D0", [512, 1024, 1100])
+def test_rowsel_tensor_path_digit_extremes(pir, D0):
     """Tensor-core path at its exactness limit: DB words 0x1EFFFFFF (three
     bytes 255) against query words 0x1F7F7F80 (balanced digits -128, -128,
-    -128, 32) over D0 = 512 rows puts every digit-plane sum at
-    512 * 255 * 128, just below 2^24; out = D0 * a * b mod q."""
-    N, L, D0, D1, B = 64, 3, 512, 33, 16
+    -128, 32) over a 512-row K segment puts every digit-plane sum at
+    512 * 255 * 128, just below 2^24; out = D0 * a * b mod q, with the
+    segments' residues added for D0 > 512."""
+    N, L, D1, B = 64, 3, 33, 16
     qs = oracle.primes(N, L)
     ctx = pir.pir_ctx_create(N, qs)
     P = L * N
@@ -263,6 +269,11 @@ def test_full_rowsel_6g(pir):
 
 def test_full_rowsel_24g_b16(pir):
     _full_size(pir, "rowsel_24g_b16", sample_cols=[0, 513, 1023])
+
+
+def test_full_rowsel_64g_b16(pir):
+    """16 queries over the 64 GiB DB: tensor cores, two K segments per point."""
+    _full_size(pir, "rowsel_64g_b16", sample_cols=[0, 700, 1364])
 
 
 def test_full_rowsel_64g_with_ntt(pir):
