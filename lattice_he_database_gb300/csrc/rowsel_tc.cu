@@ -74,6 +74,8 @@ constexpr uint32_t TC_MIN_Q = 1u << 26;        // smallest prime the epilogue's 
 constexpr uint32_t TC_Q_BYTES = TC_SEG * 32 * 4;        // one segment's query slice (64 KiB)
 constexpr uint32_t TC_RED_PITCH = 33;          // words per row of the epilogue's plane sums (no bank conflicts)
 constexpr uint32_t TC_PREFETCH_PIECE = 64 * 1024;
+constexpr float TC_MAGIC = 12582912.0f;        // 1.5 * 2^23
+constexpr uint32_t TC_MAGIC_BITS = 0x4B400000u;
 
 struct TcArgs {
     const uint32_t *qT;     // point-major query, [P][PS], 32 polynomials per k
@@ -453,6 +455,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t q = A.q[l];
             const float qinv = A.qinv[l];
             const uint32_t ci = A.c[l][plane], cis = A.cs[l][plane];
+            // + q, + 0x4B400000 * q for the quotient's magic bits, - the magic offsets in lo
+            const uint32_t lo_off = plane == 3 ? TC_MAGIC_BITS + (TC_MAGIC_BITS << 8) : TC_MAGIC_BITS << 24;
+            const uint32_t rc = q + TC_MAGIC_BITS * q - lo_off;
             for (uint32_t s = 0; s < A.S; ++s) {
                 const uint32_t nt = tiles_of(A, s);
                 const uint32_t Ws = (s == A.S - 1) ? A.Wlast : PIR_SLAB;
@@ -467,8 +472,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     // Every partial sum of the estimate is below 128 * 512 * (2^24 + q)
                     // <= 2^46 (a segment has at most 512 rows), so its three roundings
                     // add at most 3 * 2^22, and |W| / q <= 128 * 512 = 2^16; with
-                    // q >= 2^26 the estimate of W / q
-                    // is off by less than 0.2 and W - k*q lies in (-0.7q, 1.7q).
+                    // q >= 2^26 the estimate of W / q is off by less than 0.2 and
+                    // W - k*q lies in (-0.7q, 1.7q).
+                    // Integer conversions: an fp32 integer x with |x| < 2^22 gives
+                    // x + 1.5 * 2^23 exactly, whose bits are 0x4B400000 + x (an FADD
+                    // instead of a conversion).  That holds for S_3 (top DB byte
+                    // <= 31: |S| <= 128 * 31 * 512), for every S of plane 3 (top
+                    // query digit <= 32: |S| <= 32 * 255 * 512 < 2^22) and for the
+                    // quotient k; the other sums reach 2^24 and are converted.  The
+                    // offsets the magic bits leave in lo and in k*q are folded into rc.
                     uint32_t lo[32];
                     float wf[32];
 #pragma unroll
@@ -484,11 +496,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             tmem_ld32(taddr + j * 32, v);
                             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                             const float scale = (float)(1u << (8 * j));
+                            if (j == 3 || plane == 3) {
 #pragma unroll
-                            for (int n = 0; n < 32; ++n) {
-                                const float x = __uint_as_float(v[n]);
-                                lo[n] += (uint32_t)__float2int_rn(x) << (8 * j);
-                                wf[n] = fmaf(x, scale, wf[n]);
+                                for (int n = 0; n < 32; ++n) {
+                                    const float x = __uint_as_float(v[n]);
+                                    lo[n] += __float_as_uint(x + TC_MAGIC) << (8 * j);
+                                    wf[n] = fmaf(x, scale, wf[n]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int n = 0; n < 32; ++n) {
+                                    const float x = __uint_as_float(v[n]);
+                                    lo[n] += (uint32_t)__float2int_rn(x) << (8 * j);
+                                    wf[n] = fmaf(x, scale, wf[n]);
+                                }
                             }
                         }
                     }
@@ -501,28 +522,40 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         // W - k*q lies in (-0.7q, 1.7q); + q makes it a positive 32-bit value
                         // congruent to W, which the Shoup product accepts as is: 2^(8i) * W
                         // mod q lands in [0, 2q)
-                        const int32_t k = __float2int_rn(wf[n] * qinv);
-                        const uint32_t r = lo[n] - (uint32_t)k * q + q;
+                        const uint32_t kb = __float_as_uint(fmaf(wf[n], qinv, TC_MAGIC));   // 0x4B400000 + k
+                        const uint32_t r = lo[n] - kb * q + rc;
                         red[(plane * 32 + m) * TC_RED_PITCH + n] = shoup_mul(r, ci, cis, q);
                     }
                     named_barrier(2, 128);
-                    for (uint32_t idx = etid; idx < 32 * 32; idx += 128) {
-                        const uint32_t mm = idx >> 5, nn = idx & 31;
+                    {
+                        // this thread's outputs: column nn, rows m0, m0 + 4, ..., m0 + 28
+                        const uint32_t nn = etid & 31, m0 = etid >> 5;
                         const uint32_t col = t * TC_NT + nn;
-                        if (mm >= A.Mv || col >= Ws) continue;
-                        const uint32_t n_glob = s * PIR_SLAB + col;
-                        // four plane terms, each in [0, 2q): the sum is below 8q < 2^32
-                        uint32_t x = red[mm * TC_RED_PITCH + nn] + red[(32 + mm) * TC_RED_PITCH + nn] +
-                                     red[(64 + mm) * TC_RED_PITCH + nn] + red[(96 + mm) * TC_RED_PITCH + nn];
-                        x = x >= 4 * q ? x - 4 * q : x;
-                        x = x >= 2 * q ? x - 2 * q : x;
-                        x = x >= q ? x - q : x;
-                        uint32_t *o = A.outT + (p * A.Mv + mm) * A.D1p + n_glob;
-                        if (h) {   // later segments add to the sum this thread stored for the earlier ones
-                            x += *o;
-                            x = x >= q ? x - q : x;
+                        if (col < Ws) {
+                            uint32_t v[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const uint32_t *rr = red + (m0 + 4 * i) * TC_RED_PITCH + nn;
+                                // four plane terms, each in [0, 2q): the sum is below 8q < 2^32
+                                v[i] = rr[0] + rr[32 * TC_RED_PITCH] + rr[64 * TC_RED_PITCH] + rr[96 * TC_RED_PITCH];
+                            }
+                            uint32_t *o = A.outT + (p * A.Mv + m0) * A.D1p + s * PIR_SLAB + col;
+                            const size_t ostep = (size_t)4 * A.D1p;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                if (m0 + 4 * i < A.Mv) {
+                                    uint32_t x = v[i];
+                                    x = min(x, x - 4 * q);   // x - cq wraps above x when x < cq
+                                    x = min(x, x - 2 * q);
+                                    x = min(x, x - q);
+                                    if (h) {   // later segments add to the sum this thread stored for the earlier ones
+                                        x += o[i * ostep];
+                                        x = min(x, x - q);
+                                    }
+                                    o[i * ostep] = x;
+                                }
+                            }
                         }
-                        *o = x;
                     }
                 }
             }

@@ -1,14 +1,20 @@
 """Host check of the tensor-core RowSel epilogue's modular reduction.
 
 The kernel reduces W = sum_j 2^(8j) S_j mod q, where the S_j are the exact
-integer sums of one query digit plane against the four DB byte planes
-(|S_j| <= 128 * 255 * D0 for j < 3, the top byte of a residue below q
-bounding S_3), without 64-bit arithmetic:
+integer sums of one query digit plane i against the four DB byte planes
+over a K segment of at most 512 rows (|S_j| <= 128 * 255 * 512 for i, j < 3;
+the top query digit (<= 32) bounds plane 3, the top byte of a residue
+below q bounds S_3), without 64-bit arithmetic:
 
-    lo = sum_j S_j << 8j              (wrapping 32-bit)
+    lo = sum_j t_j << 8j              (wrapping 32-bit), where t_j is
+         S_j converted to an integer, or, where |S_j| < 2^22 (j = 3, and
+         every j of plane 3), the fp32 bits of S_j + 1.5 * 2^23, which are
+         0x4B400000 + S_j
     wf = fma(S_3, 2^24, fma(S_2, 2^16, fma(S_1, 2^8, S_0)))   (fp32)
-    k  = round_to_int(wf * fp32(1/q))
-    r  = lo - k*q + q                 (wrapping 32-bit; must be in [0, 2^32))
+    kb = fp32 bits of fma(wf, fp32(1/q), 1.5 * 2^23) = 0x4B400000 + k,
+         k = wf / q rounded to an integer
+    r  = lo - kb*q + (q + 0x4B400000*q - the magic offsets in lo)
+         (wrapping 32-bit; equals W - k*q + q, which must lie in [0, 2^32))
     u  = Shoup product r * (2^(8i) mod q), in [0, 2q)
 and the four digit planes i of one output are summed (below 8q) and
 reduced by conditional subtractions of 4q, 2q and q.
@@ -29,20 +35,42 @@ def _f32(x):
     return np.asarray(x, dtype=np.float64).astype(np.float32)
 
 
-def epilogue_reduce(S, q):
-    """The kernel's reduction for an array S of shape [..., 4] (int64)."""
+MAGIC = 12582912.0          # 1.5 * 2^23
+MAGIC_BITS = 0x4B400000
+M32 = 0xFFFFFFFF
+
+
+def _magic_bits(x):
+    """fp32 bits of x + 1.5 * 2^23 for integers |x| < 2^22 (then 0x4B400000 + x)."""
+    x = np.asarray(x, dtype=np.int64)
+    assert (np.abs(x) < 1 << 22).all()
+    bits = _f32(x.astype(np.float64) + MAGIC).view(np.uint32).astype(np.int64)
+    assert (bits == MAGIC_BITS + x).all()
+    return bits
+
+
+def epilogue_reduce(S, q, plane=0, strict=True):
+    """The kernel's reduction of digit plane `plane` for S of shape [..., 4] (int64):
+    the 32-bit value r that goes into the Shoup product.  A quotient outside
+    the magic conversion's range fails the call (strict) or gives r = -1."""
     S = np.asarray(S, dtype=np.int64)
-    lo = np.zeros(S.shape[:-1], dtype=np.uint64)
+    lo = np.zeros(S.shape[:-1], dtype=np.int64)
     wf = np.zeros(S.shape[:-1], dtype=np.float32)
     for j in range(4):
-        lo = (lo + ((S[..., j].astype(np.uint64) & 0xFFFFFFFF) << np.uint64(8 * j))) & np.uint64(0xFFFFFFFF)
+        t = _magic_bits(S[..., j]) if (j == 3 or plane == 3) else S[..., j] & M32   # else __float2int_rn
+        lo = (lo + (t << (8 * j))) & M32
         # fmaf(x, 2^(8j), wf): exact product and sum in float64 (< 2^53), one rounding to fp32
         wf = _f32(S[..., j].astype(np.float64) * float(1 << (8 * j)) + wf.astype(np.float64))
     qinv = np.float32(1.0) / np.float32(q)
-    k = np.rint((wf * qinv).astype(np.float32)).astype(np.int64)          # __float2int_rn
-    signed = ((lo.astype(np.int64) - k * q) & 0xFFFFFFFF).astype(np.int64)
-    signed = np.where(signed >= 1 << 31, signed - (1 << 32), signed)        # W - k*q as signed 32-bit
-    return signed + q                                                        # the kernel's r (unsigned)
+    # fmaf(wf, qinv, 1.5 * 2^23): the product is exact in float64 and the result lies in
+    # [2^23, 2^24), where fp32 steps by 1, so its one rounding is that of wf*qinv to an integer
+    k = np.rint(wf.astype(np.float64) * np.float64(qinv)).astype(np.int64)
+    k_ok = np.abs(k) < 1 << 22
+    assert k_ok.all() or not strict
+    kb = MAGIC_BITS + k
+    off = (MAGIC_BITS + (MAGIC_BITS << 8)) & M32 if plane == 3 else (MAGIC_BITS << 24) & M32
+    rc = (q + MAGIC_BITS * q - off) & M32
+    return np.where(k_ok, (lo - kb * q + rc) & M32, -1)
 
 
 def shoup(y, w, q):
@@ -57,20 +85,30 @@ def epilogue_output(S4, q):
     """Full epilogue for S4 of shape [..., 4 planes, 4 byte planes]: the output residue."""
     x = np.zeros(S4.shape[:-2], dtype=np.int64)
     for i in range(4):
-        r = epilogue_reduce(S4[..., i, :], q)
+        r = epilogue_reduce(S4[..., i, :], q, plane=i)
         assert (r > 0).all() and (r < 1 << 31).all()
         u = shoup(r, pow(2, 8 * i, q), q)
         assert (u < 2 * q).all()
         x = x + u
     assert (x < 8 * q).all()
     for c in (4, 2, 1):
-        x = np.where(x >= c * q, x - c * q, x)
+        x = np.minimum(x, (x - c * q) & M32)     # x - cq wraps above x when x < cq
     return x
 
 
-def _bounds(q, D0):
+def _bounds(q, D0, plane):
+    """Largest |S_j| of digit plane `plane` over D0 rows: query digits |d| <= 128
+    (the top digit of a residue below q: <= (q - 1 + 0x808080) >> 24), DB bytes
+    <= 255 (the top byte: <= (q - 1) >> 24)."""
+    d = 128 if plane < 3 else (q - 1 + 0x808080) >> 24
     top = (q - 1) >> 24
-    return np.array([128 * 255 * D0, 128 * 255 * D0, 128 * 255 * D0, 128 * top * D0], dtype=np.int64)
+    return np.array([d * 255 * D0, d * 255 * D0, d * 255 * D0, d * top * D0], dtype=np.int64)
+
+
+def _sums(b, rng, n):
+    """Every sign pattern of the extreme partial sums, a third of them, then random values."""
+    corners = np.array([[s0, s1, s2, s3] for s0 in (-1, 1) for s1 in (-1, 1) for s2 in (-1, 1) for s3 in (-1, 1)])
+    return np.concatenate([corners * b, (corners * b) // 3, rng.integers(-b, b + 1, size=(n, 4), dtype=np.int64)])
 
 
 @pytest.mark.parametrize("q", [None, "min", "mid", "max"])
@@ -85,35 +123,44 @@ def test_reduction_exact_on_extremes(q):
     else:
         q = oracle.primes(N, 1)[0]                                   # largest below 2^29
     assert q >= 1 << 26
-    D0 = 512
-    b = _bounds(q, D0)
+    D0 = 512                                                         # rows of one K segment
     rng = np.random.default_rng(q & 0xFFFF)
-    # every sign pattern of the extreme partial sums, then random values inside the bounds
-    corners = np.array([[s0, s1, s2, s3] for s0 in (-1, 1) for s1 in (-1, 1) for s2 in (-1, 1) for s3 in (-1, 1)])
-    S = np.concatenate([corners * b, (corners * b) // 3,
-                        rng.integers(-b, b + 1, size=(200000, 4), dtype=np.int64)])
-    W = (S * (np.int64(1) << (8 * np.arange(4, dtype=np.int64)))).sum(axis=1)
-    r = epilogue_reduce(S, q)
-    # r is congruent to W, positive and below 2q + 0.7q (a valid Shoup input)
-    assert (np.mod(r - W, q) == 0).all() and (r > 0).all() and (r < 3 * q).all()
+    pw = np.int64(1) << (8 * np.arange(4, dtype=np.int64))
+    for plane in range(4):
+        S = _sums(_bounds(q, D0, plane), rng, 50000)
+        W = (S * pw).sum(axis=1)
+        r = epilogue_reduce(S, q, plane)
+        # r is congruent to W (so W - kq + q did not leave [0, 2^32)), positive and below 3q
+        assert (np.mod(r - W, q) == 0).all() and (r > 0).all() and (r < 3 * q).all(), plane
     # the whole output path on groups of four planes
-    S4 = S[: (S.shape[0] // 4) * 4][:4000].reshape(-1, 4, 4)
-    W4 = (S4 * (np.int64(1) << (8 * np.arange(4, dtype=np.int64)))).sum(axis=2)
+    S4 = np.stack([_sums(_bounds(q, D0, i), rng, 4000)[:4000] for i in range(4)], axis=1)   # [g][i][j]
+    W4 = (S4 * pw).sum(axis=2)
     want = np.array([sum(int(W4[g, i]) << (8 * i) for i in range(4)) % q for g in range(W4.shape[0])])
     got = epilogue_output(S4, q)
     bad = np.nonzero(got != want)[0]
     assert bad.size == 0, (q, got[bad[:5]], want[bad[:5]])
 
 
+def test_top_digit_plane_fits_the_magic_conversion():
+    """The fp32 magic-constant conversion is exact only below 2^22: the top query
+    digit plane (digits <= 32) against full DB bytes over 512 rows stays below it
+    for every prime below 2^29, the lower planes against the top DB byte too."""
+    q = oracle.primes(4096, 1)[0]
+    assert q < 1 << 29
+    assert _bounds(q, 512, 3).max() < 1 << 22
+    assert max(_bounds(q, 512, i)[3] for i in range(3)) < 1 << 22
+    assert _bounds(q, 512, 0)[0] >= 1 << 22          # the lower planes need the exact conversion
+
+
 def test_reduction_needs_the_prime_bound():
-    """Below the bound the quotient estimate can be off by more than one:
-    with q just below 2^16, some sums inside the same bounds are reduced
-    wrongly (a fraction of a percent), which is why passes with smaller
-    primes take the CUDA-core kernel."""
+    """Below the bound the quotient estimate fails: with q just below 2^16
+    some sums inside the same bounds have a quotient beyond the magic
+    conversion's range or one off by more than one, which is why passes with
+    smaller primes take the CUDA-core kernel."""
     q = oracle.primes(16, 1, bound=1 << 16)[0]
     D0 = 512
     b = np.array([128 * 255 * D0] * 3 + [0], dtype=np.int64)
     S = np.random.default_rng(5).integers(-b, b + 1, size=(20000, 4), dtype=np.int64)
     W = (S * (np.int64(1) << (8 * np.arange(4, dtype=np.int64)))).sum(axis=1)
-    r = epilogue_reduce(S, q)
-    assert ((np.mod(r - W, q) != 0) | (r <= 0) | (r >= 3 * q)).any()
+    r = epilogue_reduce(S, q, strict=False)
+    assert ((r < 0) | (np.mod(r - W, q) != 0) | (r <= 0) | (r >= 3 * q)).any()
