@@ -8,7 +8,9 @@ Every function restates a definition from the pages (see oracle.c):
   * VIPIR (CSDN translation), sections 2.2-2.5, 4.1-4.3: RNS primes, the
     negacyclic NTT, the INT8 x INT32 scan mod 2^32;
   * GPIR (arXiv 2604.04696), section 2: RowSel as point-wise GEMMs
-    M_out[p,m,n] = sum_k M_in0[p,m,k] * M_in1[p,k,n] mod q.
+    M_out[p,m,n] = sum_k M_in0[p,m,k] * M_in1[p,k,n] mod q;
+  * GPIR sections 2-3 and VIPIR 3.6 step 7: ColTor, the column tournament of
+    RGSW-RLWE external products with the gadget decomposition Dcp (l = 5).
 """
 from __future__ import annotations
 
@@ -75,6 +77,15 @@ def lib():
         L.orc_rowsel.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, ctypes.c_uint32,
                                  ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint32,
                                  _u32p, _u32p, ctypes.c_int]
+        L.orc_dcp.restype = None
+        L.orc_dcp.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, ctypes.c_uint32, ctypes.c_uint32,
+                              _u32p, _u32p]
+        L.orc_ext_product.restype = None
+        L.orc_ext_product.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint32,
+                                      ctypes.c_uint32, _u32p, _u32p, _u32p]
+        L.orc_coltor_stage.restype = None
+        L.orc_coltor_stage.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint32,
+                                       ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint64, _u32p, ctypes.c_int]
         L.orc_scalar_scan.restype = None
         L.orc_scalar_scan.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32, _u8p,
                                       _u32p, _u32p, ctypes.c_int]
@@ -233,3 +244,61 @@ def scalar_scan(db_rows: np.ndarray, Q: np.ndarray, threads: int | None = None) 
     out = np.empty((R, B), dtype=np.uint32)
     lib().orc_scalar_scan(R, C, B, _p8(db_rows), _p32(Q), _p32(out), threads or default_threads())
     return out
+
+
+# --------------------------------------------------------------- ColTor
+def dcp(x: np.ndarray, qs, ell: int, w: int) -> np.ndarray:
+    """Gadget decomposition of one RNS polynomial x [L][N] (coefficient form):
+    digits [ell][N] with CRT(x[:, t]) = sum_u d[u][t] * 2^(w u)."""
+    x = np.ascontiguousarray(x, dtype=np.uint32)
+    L, N = x.shape
+    q = np.asarray(qs, dtype=np.uint32)
+    d = np.empty((ell, N), dtype=np.uint32)
+    lib().orc_dcp(N, L, _p32(q), ell, w, _p32(x), _p32(d))
+    return d
+
+
+def ext_product(C: np.ndarray, ct: np.ndarray, qs, psis, ell: int, w: int) -> np.ndarray:
+    """RGSW C [2 ell][2][L][N] (NTT form) times RLWE ct [2][L][N] (coefficient
+    form) -> [2][L][N] NTT form."""
+    C = np.ascontiguousarray(C, dtype=np.uint32)
+    ct = np.ascontiguousarray(ct, dtype=np.uint32)
+    _, _, L, N = C.shape
+    assert C.shape == (2 * ell, 2, L, N) and ct.shape == (2, L, N)
+    q = np.asarray(qs, dtype=np.uint32)
+    ps = np.asarray(psis, dtype=np.uint32)
+    out = np.empty((2, L, N), dtype=np.uint32)
+    lib().orc_ext_product(N, L, _p32(q), _p32(ps), ell, w, _p32(C), _p32(ct), _p32(out))
+    return out
+
+
+def coltor_stage(C: np.ndarray, cts: np.ndarray, qs, psis, ell: int, w: int,
+                 threads: int | None = None) -> np.ndarray:
+    """One tournament stage: cts [n][2][L][N] (NTT form) -> [ceil(n/2)][2][L][N],
+    out_i = ct_2i + C (x) (ct_2i+1 - ct_2i), a missing partner being zero."""
+    C = np.ascontiguousarray(C, dtype=np.uint32)
+    cts = np.ascontiguousarray(cts, dtype=np.uint32)
+    n, _, L, N = cts.shape
+    assert C.shape == (2 * ell, 2, L, N)
+    q = np.asarray(qs, dtype=np.uint32)
+    ps = np.asarray(psis, dtype=np.uint32)
+    out = np.empty(((n + 1) // 2, 2, L, N), dtype=np.uint32)
+    lib().orc_coltor_stage(N, L, _p32(q), _p32(ps), ell, w, _p32(C), _p32(cts), n, _p32(out),
+                           threads or default_threads())
+    return out
+
+
+def coltor_stages(n: int) -> int:
+    """Stages of a tournament over n ciphertexts: ceil(log2 n)."""
+    s = 0
+    while (1 << s) < n:
+        s += 1
+    return s
+
+
+def coltor(Cs: np.ndarray, cts: np.ndarray, qs, psis, ell: int, w: int, threads: int | None = None) -> np.ndarray:
+    """The whole tournament: stage s uses Cs[s]; cts [n][2][L][N] -> [2][L][N]."""
+    cur = np.ascontiguousarray(cts, dtype=np.uint32)
+    for s in range(coltor_stages(cur.shape[0])):
+        cur = coltor_stage(Cs[s], cur, qs, psis, ell, w, threads)
+    return cur[0].copy()

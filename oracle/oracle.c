@@ -12,7 +12,8 @@
  *            (CSDN translation), sections 2.2-2.5 and 4.1-4.3.
  *   [GPIR]   "GPIR: Enabling Practical Private Information Retrieval with
  *            GPUs" (arXiv 2604.04696), the RowSel paragraphs of section 2
- *            (the M_out[p,m,n] formulation).
+ *            (the M_out[p,m,n] formulation) and the ColTor / Dcp
+ *            paragraphs of sections 2-3 (the external product, l = 5).
  *
  * Readings of points the pages leave open are stated at each function and
  * listed in the design notes.  Integer arithmetic only; no lazy reduction,
@@ -440,4 +441,164 @@ void orc_scalar_scan(uint64_t nrows, uint64_t C, uint32_t B, const uint8_t *db_r
         pthread_create(&th[t], NULL, scalar_worker, &jobs[t]);
     }
     for (int t = 0; t < nthreads; t++) pthread_join(th[t], NULL);
+}
+
+/* ------------------------------------------------------------------ */
+/* ColTor: gadget decomposition and the RGSW-RLWE external product      */
+/* [GPIR section 2 and the ColTor paragraphs of section 3 (Dcp, l = 5); */
+/*  VIPIR 3.6 step 7 and section 5 (q ~ 2^87 in 3 RNS primes)]          */
+/* ------------------------------------------------------------------ */
+
+/*
+ * The integer X in [0, Q), Q = q_0 * ... * q_{L-1}, with X = x_l (mod q_l),
+ * by Garner's mixed-radix recurrence:
+ *     v_l = (((x_l - v_0) q_0^-1 - v_1) q_1^-1 - ... - v_{l-1}) q_{l-1}^-1  mod q_l
+ *     X   = v_0 + q_0 (v_1 + q_1 (v_2 + ...)).
+ * Requires Q < 2^128 (L <= 4 primes below 2^32).
+ */
+static u128 crt_garner(uint32_t L, const uint32_t *q, const uint32_t *x)
+{
+    uint32_t v[4];
+    for (uint32_t l = 0; l < L; l++) {
+        uint64_t t = x[l] % q[l];
+        for (uint32_t k = 0; k < l; k++) {
+            t = (t + q[l] - v[k] % q[l]) % q[l];
+            t = (uint64_t)mulmod((uint32_t)t, orc_invmod(q[k] % q[l], q[l]), q[l]);
+        }
+        v[l] = (uint32_t)t;
+    }
+    u128 X = 0;
+    for (int l = (int)L - 1; l >= 0; l--) X = X * q[l] + v[l];
+    return X;
+}
+
+/*
+ * Gadget decomposition Dcp of one polynomial of R_Q in coefficient form,
+ * x[l][t] (L rows of N residues): every coefficient X (the CRT value above)
+ * is written in base 2^w with ell digits,
+ *     X = sum_{u < ell} d_u 2^(w u),   d_u = floor(X / 2^(w u)) mod 2^w,
+ * and d[u][t] = d_u.  Readings (the pages fix only ell = 5 at Q ~ 2^87):
+ * unsigned digits of the CRT value, base 2^w with w * ell >= bits of Q
+ * (w = 18 for ell = 5), digit 0 the least significant.
+ */
+void orc_dcp(uint32_t N, uint32_t L, const uint32_t *q, uint32_t ell, uint32_t w,
+             const uint32_t *x, uint32_t *d)
+{
+    uint32_t xs[4];
+    const u128 mask = (w >= 128) ? ~(u128)0 : (((u128)1 << w) - 1);
+    for (uint32_t t = 0; t < N; t++) {
+        for (uint32_t l = 0; l < L; l++) xs[l] = x[(uint64_t)l * N + t];
+        u128 X = crt_garner(L, q, xs);
+        for (uint32_t u = 0; u < ell; u++) {
+            uint32_t sh = w * u;
+            d[(uint64_t)u * N + t] = sh >= 128 ? 0u : (uint32_t)((X >> sh) & mask);
+        }
+    }
+}
+
+/*
+ * External product of an RGSW ciphertext C with an RLWE ciphertext ct:
+ *     out_c = sum_{u < ell} NTT(Dcp_u(ct_0)) (.) C[u]_c
+ *           + sum_{u < ell} NTT(Dcp_u(ct_1)) (.) C[ell + u]_c      (c = 0, 1)
+ * point-wise mod q_l, where (.) is the point-wise product of NTT vectors.
+ *   C   : [2 ell][2][L][N], NTT form (row u pairs with digit u of ct_0,
+ *         row ell + u with digit u of ct_1: the layout Z + m * (I_2 x g)
+ *         of an RGSW encryption of m with gadget g_u = 2^(w u)).
+ *   ct  : [2][L][N], coefficient form.
+ *   out : [2][L][N], NTT form.
+ * Each digit is a plain integer below 2^w; it is lifted to every prime
+ * (reduced mod q_l) and transformed with the iterative NTT above.
+ */
+void orc_ext_product(uint32_t N, uint32_t L, const uint32_t *q, const uint32_t *psi, uint32_t ell,
+                     uint32_t w, const uint32_t *C, const uint32_t *ct, uint32_t *out)
+{
+    uint64_t PN = (uint64_t)L * N;
+    uint32_t *d = (uint32_t *)malloc(sizeof(uint32_t) * ell * N);
+    uint32_t *dn = (uint32_t *)malloc(sizeof(uint32_t) * 2 * ell * PN);   /* [cin][u][l][t] */
+    for (uint32_t cin = 0; cin < 2; cin++) {
+        orc_dcp(N, L, q, ell, w, ct + cin * PN, d);
+        for (uint32_t u = 0; u < ell; u++)
+            for (uint32_t l = 0; l < L; l++) {
+                uint32_t *row = dn + ((uint64_t)(cin * ell + u) * L + l) * N;
+                for (uint32_t t = 0; t < N; t++) row[t] = d[(uint64_t)u * N + t] % q[l];
+                orc_ntt_iter(q[l], psi[l], N, row);
+            }
+    }
+    for (uint32_t c = 0; c < 2; c++)
+        for (uint32_t l = 0; l < L; l++)
+            for (uint32_t j = 0; j < N; j++) {
+                u128 acc = 0;
+                for (uint32_t v = 0; v < 2 * ell; v++)
+                    acc += (u128)dn[((uint64_t)v * L + l) * N + j] *
+                           C[(((uint64_t)v * 2 + c) * L + l) * N + j];
+                out[((uint64_t)c * L + l) * N + j] = (uint32_t)(acc % q[l]);
+            }
+    free(d);
+    free(dn);
+}
+
+/*
+ * One ColTor stage (the column tournament's selection by one bit):
+ *     out_i = ct_{2i} + C (x) (ct_{2i+1} - ct_{2i}),   i < ceil(nin / 2),
+ * with (x) the external product above, all ciphertexts in NTT form; the
+ * difference is brought to coefficient form by the inverse NTT before Dcp.
+ * C encrypting 0 keeps ct_{2i}, C encrypting 1 takes ct_{2i+1}.
+ * Reading: when nin is odd the last ciphertext meets the zero ciphertext
+ * (the tournament padded with zeros to an even count).
+ *   in  : [nin][2][L][N], out : [ceil(nin/2)][2][L][N].
+ */
+typedef struct {
+    uint32_t N, L, ell, w;
+    const uint32_t *q, *psi, *C, *in;
+    uint64_t nin, i0, i1;
+    uint32_t *out;
+} coltor_job;
+
+static void *coltor_worker(void *arg)
+{
+    coltor_job *j = (coltor_job *)arg;
+    uint64_t PN = (uint64_t)j->L * j->N, CT = 2 * PN;
+    uint32_t *diff = (uint32_t *)malloc(sizeof(uint32_t) * CT);
+    uint32_t *ext = (uint32_t *)malloc(sizeof(uint32_t) * CT);
+    for (uint64_t i = j->i0; i < j->i1; i++) {
+        const uint32_t *even = j->in + 2 * i * CT;
+        const uint32_t *odd = (2 * i + 1 < j->nin) ? j->in + (2 * i + 1) * CT : NULL;
+        for (uint32_t c = 0; c < 2; c++)
+            for (uint32_t l = 0; l < j->L; l++) {
+                uint32_t ql = j->q[l];
+                uint64_t base = ((uint64_t)c * j->L + l) * j->N;
+                for (uint32_t t = 0; t < j->N; t++) {
+                    uint64_t o = odd ? odd[base + t] % ql : 0;
+                    diff[base + t] = (uint32_t)((o + ql - even[base + t] % ql) % ql);
+                }
+                orc_intt_iter(ql, j->psi[l], j->N, diff + base);
+            }
+        orc_ext_product(j->N, j->L, j->q, j->psi, j->ell, j->w, j->C, diff, ext);
+        uint32_t *dst = j->out + i * CT;
+        for (uint32_t c = 0; c < 2; c++)
+            for (uint32_t l = 0; l < j->L; l++) {
+                uint64_t base = ((uint64_t)c * j->L + l) * j->N;
+                for (uint32_t t = 0; t < j->N; t++)
+                    dst[base + t] = (uint32_t)(((uint64_t)even[base + t] % j->q[l] + ext[base + t]) % j->q[l]);
+            }
+    }
+    free(diff);
+    free(ext);
+    return NULL;
+}
+
+void orc_coltor_stage(uint32_t N, uint32_t L, const uint32_t *q, const uint32_t *psi, uint32_t ell,
+                      uint32_t w, const uint32_t *C, const uint32_t *in, uint64_t nin, uint32_t *out,
+                      int nthreads)
+{
+    uint64_t nout = (nin + 1) / 2;
+    nthreads = clamp_threads(nthreads, nout);
+    pthread_t th[256];
+    coltor_job jobs[256];
+    for (int i = 0; i < nthreads; i++) {
+        jobs[i] = (coltor_job){N, L, ell, w, q, psi, C, in, nin, nout * i / nthreads,
+                               nout * (i + 1) / nthreads, out};
+        pthread_create(&th[i], NULL, coltor_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; i++) pthread_join(th[i], NULL);
 }
