@@ -49,6 +49,9 @@ WORKLOADS = {
                            desc="RowSel 24 GiB: N=4096, 3 primes, D0=512 x D1=1024, B=16 queries, NTT-domain"),
     "rowsel_64g_b16": dict(N=4096, L=3, D0=1024, D1=1365, B=16, domain="ntt",
                            desc="RowSel 64 GiB: N=4096, 3 primes, D0=1024 x D1=1365, B=16 queries, NTT-domain"),
+    "coltor_1365": dict(kind="coltor", N=4096, L=3, n=1365, ell=5, w=18,
+                        desc="ColTor over the 1365 RowSel output ciphertexts of one 64 GiB query: N=4096, "
+                             "3 primes, 11 stages of RGSW-RLWE external products, l=5 digits of 18 bits"),
     # scalar-HE scan: byte DB x 64 query words mod 2^32 (tcgen05 fp16 path)
     "scalar_16g": dict(kind="scalar", R=131072, C=131072, B=64,
                        desc="Scalar-HE scan: DB 131072 x 131072 uint8 (16 GiB) x Q 131072 x 64 uint32, mod 2^32"),
@@ -75,6 +78,7 @@ WORKLOADS = {
 METRIC = "DB GB/s scanned & queries/s (RowSel, 64 GiB DB), % of GB300 HBM roofline"
 SPEC_HBM_GBS = 8000.0   # nominal GB300 HBM3e bandwidth (context for the roofline fractions)
 EXPPACK_METRIC = "ring-packing GEMM H*C + (0|G): hint GB/s scanned"
+COLTOR_METRIC = "ColTor column tournaments per second (RGSW-RLWE external products)"
 
 
 def parse():
@@ -286,11 +290,44 @@ class ScalarSample:
         oracle.scalar_scan(self.db, self.Q, threads=self.threads)
 
 
+class ColtorSample:
+    """Oracle ColTor on a bounded sample: one tournament stage over two
+    ciphertexts per host thread (one external product each), counted as the
+    fraction of a whole tournament (n - 1 external products) it performs."""
+    unit = "queries/s"
+
+    def __init__(self, cfg):
+        import oracle
+        import synth
+        N, L, n, ell = cfg["N"], cfg["L"], cfg["n"], cfg["ell"]
+        self.ell, self.w = ell, cfg["w"]
+        self.threads = oracle.default_threads()
+        self.pairs = max(1, min((n + 1) // 2, self.threads))
+        self.qs = oracle.primes(N, L)
+        self.psis = [oracle.min_psi(q, N) for q in self.qs]
+        self.C = synth.residues(11, (2 * ell, 2, L, N), self.qs, tid=synth.T_EXTRA)
+        self.cts = synth.residues(12, (2 * self.pairs, 2, L, N), self.qs, tid=synth.T_EXTRA)
+        self.nbytes = self.pairs / max(1, n - 1)      # tournaments per call
+        self.desc = ("oracle ColTor stage over %d ciphertexts (%d external products of %d per tournament), "
+                     "N=%d, L=%d, l=%d" % (2 * self.pairs, self.pairs, n - 1, N, L, ell))
+
+    def __call__(self):
+        import oracle
+        oracle.coltor_stage(self.C, self.cts, self.qs, self.psis, self.ell, self.w, threads=self.threads)
+
+
+def _rate(sample, units_per_s: float):
+    """A sample's rate in its metric unit (GB/s unless the sample says otherwise)."""
+    unit = getattr(sample, "unit", "GB/s")
+    return (units_per_s / 1e9 if unit == "GB/s" else units_per_s), unit
+
+
 def oracle_baseline(sample, seconds: float):
     """cpu_baseline object: the sample repeated for about `seconds`."""
     sample()                                   # first touch of the inputs
     calls, dt = repeat_for(sample, seconds)
-    return {"value": sample.nbytes * calls / dt / 1e9, "unit": "GB/s", "cores": sample.threads, "kind": "oracle",
+    value, unit = _rate(sample, sample.nbytes * calls / dt)
+    return {"value": value, "unit": unit, "cores": sample.threads, "kind": "oracle",
             "sample": "%s; %d calls in %.1f s" % (sample.desc, calls, dt), "seconds": round(dt, 2)}
 
 
@@ -310,14 +347,14 @@ def run_reference_sample(args, sample, metric, dtype, data, desc):
     for _ in range(args.steps):
         one_step()
     dt = (time.perf_counter() - t) / max(1, args.steps)
-    value = sample.nbytes * reps / dt / 1e9
+    value, unit = _rate(sample, sample.nbytes * reps / dt)
     line = {
-        "impl": "reference", "metric": metric, "value": value, "unit": "GB/s", "n_gpus": 0, "steps": args.steps,
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": 0, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype, "data": data, "config": {"workload": args.workload, "desc": desc},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": sample.threads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": unit, "cores": sample.threads, "kind": "oracle",
                          "sample": "per step %d calls of: %s" % (reps, sample.desc)},
-        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -333,6 +370,9 @@ def run_reference(args, cfg):
                              "synthetic", cfg["desc"])
     elif kind == "exppack":
         run_reference_sample(args, ExppackSample(cfg), EXPPACK_METRIC, "u32",
+                             "synthetic (seeded SplitMix64 residues)", cfg["desc"])
+    elif kind == "coltor":
+        run_reference_sample(args, ColtorSample(cfg), COLTOR_METRIC, "u32",
                              "synthetic (seeded SplitMix64 residues)", cfg["desc"])
     else:
         run_reference_sample(args, RowselSample(cfg), METRIC, "u32", "synthetic (seeded SplitMix64 residues)",
@@ -355,12 +395,34 @@ def rowsel_passes(D0, B) -> int:
     return passes
 
 
+def coltor_stages(n) -> int:
+    """Stages of a tournament over n ciphertexts: ceil(log2 n)."""
+    s = 0
+    while (1 << s) < n:
+        s += 1
+    return s
+
+
+def coltor_algorithmic_bytes(n, L, N, ell) -> int:
+    """Bytes a tournament must move at the least: every stage reads its input
+    ciphertexts and its RGSW ciphertext and writes its outputs."""
+    ct = 2 * L * N * 4
+    total, cnt = 0, n
+    while cnt > 1:
+        nxt = (cnt + 1) // 2
+        total += cnt * ct + 2 * ell * ct + nxt * ct
+        cnt = nxt
+    return total
+
+
 def launches_per_step(cfg) -> int:
     """Kernels one step launches: per RowSel pass a query transpose, the scan
     and a result transpose; plus the query NTT and result INTT in coefficient
     form, or the lift + NTT of G for the ring-packing GEMM."""
     if cfg.get("kind") == "exppack":
         return 3 * rowsel_passes(cfg["n"], cfg["B"]) + 1
+    if cfg.get("kind") == "coltor":
+        return 5 * coltor_stages(cfg["n"])
     return 3 * rowsel_passes(cfg["D0"], cfg["B"]) + (2 if cfg["domain"] == "coeff" else 0)
 
 
@@ -613,6 +675,125 @@ def device_db(ctx, D0, D1, seed):
     return db
 
 
+def run_coltor(args, cfg):
+    """ColTor: one step = the whole tournament over n RowSel output
+    ciphertexts (NTT form), S = ceil(log2 n) stages of five launches."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    import synth.device as sd
+    from lattice_he_database_gb300 import pir
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    N, L, n, ell, w = cfg["N"], cfg["L"], cfg["n"], cfg["ell"], cfg["w"]
+    qs = pir.pir_primes(N, L)
+    ctx = pir.pir_ctx_create(N, qs, local)
+    P = L * N
+    S = coltor_stages(n)
+    cts = torch.empty(n * 2 * P, dtype=torch.int32, device="cuda")
+    sd.fill_residues(cts, 7, synth.T_EXTRA, N, qs)
+    Cs = torch.empty(max(S, 1) * 2 * ell * 2 * P, dtype=torch.int32, device="cuda")
+    sd.fill_residues(Cs, 8, synth.T_EXTRA, N, qs)
+    out = torch.empty(2 * P, dtype=torch.int32, device="cuda")
+    ws = pir.coltor_workspace(ctx, n, ell)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def step():
+        pir.pir_coltor(ctx, Cs, ell, w, cts, n, out, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_total = max_over_ranks(t0.elapsed_time(t1))
+    if pir.pir_status(ctx):
+        raise RuntimeError("device status word set")
+
+    ct_bytes = n * 2 * P * 4
+    o_bytes = 2 * P * 4
+    cts_host = torch.empty(cts.numel(), dtype=torch.int32, pin_memory=True)
+    cts_host.copy_(cts.cpu())
+    o_host = torch.empty(out.numel(), dtype=torch.int32, pin_memory=True)
+    ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            cts.copy_(cts_host, non_blocking=True)
+            step()
+            o_host.copy_(out, non_blocking=True)
+
+    e2e_ms = None
+    if ke:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / ke
+
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    ms_step = ms_total / args.steps
+    algo = coltor_algorithmic_bytes(n, L, N, ell)
+    achieved = algo / (ms_step * 1e-3) / 1e9
+    nntt = 0
+    cnt = n
+    while cnt > 1:
+        pairs = (cnt + 1) // 2
+        nntt += pairs * (2 * L + 2 * ell * L)
+        cnt = pairs
+    result = None
+    if rank == 0:
+        line = {
+            "metric": COLTOR_METRIC, "value": world * args.steps / (ms_total * 1e-3), "unit": "queries/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+            "data": "synthetic: seeded SplitMix64 residues U[0,q_i) for the ciphertexts and RGSW rows",
+            "config": {"workload": args.workload, "desc": cfg["desc"], "n": n, "stages": S, "ell": ell, "w": w,
+                       "l2": "the first stage's digit NTTs (%.0f MB) exceed L2; no flush"
+                             % (((n + 1) // 2) * 2 * ell * P * 4 / 1e6),
+                       "parallelism": "replicas x%d" % world},
+            "external_products_per_s": world * args.steps * (n - 1) / (ms_total * 1e-3),
+            "ntt_per_step": nntt, "ntt_per_s": nntt / (ms_step * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": profile_traffic("coltor_%s" % args.workload),
+                         "kernel": "the tournament's five kernels per stage (NTT kernels dominate)",
+                         "peak_source": "%s hbm_gbs (copy)" % peak_kind, "algorithmic_bytes_per_launch": algo},
+            "clocks": clk,
+            "e2e": None if e2e_ms is None else {
+                "value": 1e3 / e2e_ms, "unit": "queries/s", "h2d_bytes_per_step": ct_bytes,
+                "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * launches_per_step(cfg),
+            "cpu_baseline": None,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = oracle_baseline(ColtorSample(cfg), args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+        result = line
+    ctx.close()
+    return result
+
+
 def run_ours(args, cfg):
     import torch
     import torch.distributed as dist
@@ -813,6 +994,8 @@ def main():
         run_scalar(args, cfg)
     elif cfg.get("kind") == "exppack":
         run_exppack(args, cfg)
+    elif cfg.get("kind") == "coltor":
+        run_coltor(args, cfg)
     else:
         run_ours(args, cfg)
 

@@ -224,6 +224,49 @@ int pir_exppack(pir_ctx *ctx, const uint32_t *h_db, uint32_t n, uint32_t Dr, con
                 uint64_t workspace_bytes, void *stream);
 
 /*
+ * ColTor — the column tournament of the OnionPIR family (GPIR section 2;
+ * GPIR section 3 for Dcp and l = 5; VIPIR 3.6 step 7 for the RGSW-RLWE
+ * external products after the first folding, VIPIR 5 for q ~ 2^87).
+ *
+ * Gadget decomposition Dcp (reading: unsigned digits of each coefficient's
+ * CRT value X in [0, Q), Q = q_0 ... q_{L-1}, base 2^w, ell digits, digit 0
+ * the least significant):   X = sum_{u<ell} Dcp_u 2^(w u).
+ * External product of an RGSW ciphertext C with an RLWE ciphertext ct:
+ *     C (x) ct = sum_u NTT(Dcp_u(ct_0)) . C[u] + NTT(Dcp_u(ct_1)) . C[ell+u]
+ * ("." point-wise mod q_l), so a noise-free RGSW of m (C[u] = (m g_u, 0),
+ * C[ell+u] = (0, m g_u), g_u = 2^(w u)) gives m * ct exactly.
+ * One tournament stage over n ciphertexts:
+ *     out_i = ct_2i + C (x) (ct_2i+1 - ct_2i),   i < ceil(n/2),
+ * a missing partner (n odd) being the zero ciphertext; C encrypting 0 keeps
+ * ct_2i, C encrypting 1 takes ct_2i+1.
+ *
+ *   C    : device, [2 ell][2][L][N] NTT form (one stage's RGSW ciphertext);
+ *          for pir_coltor, [S][2 ell][2][L][N] with S = ceil(log2 n) stages,
+ *          stage s selecting by bit s of the column index.
+ *   in   : device, [n][2][L][N] NTT form, canonical residues (the RowSel
+ *          output of one query is such a list with n = D1).
+ *   out  : device; pir_coltor_stage: [ceil(n/2)][2][L][N], pir_coltor:
+ *          [2][L][N]; NTT form; must not overlap in.
+ *   ell, w : 1 <= ell <= 16, 1 <= w <= 32, ell * w >= the bit length of Q
+ *          (ell = 5, w = 18 for three primes below 2^29).
+ *   workspace : device, >= pir_coltor_workspace_bytes(ctx, n, ell) bytes,
+ *          16-byte aligned; contents undefined after the call.
+ * The library owns nothing the caller passes; calls are asynchronous on
+ * stream.  Errors: PIR_ERR_ARG (NULL/unaligned pointers, n = 0 or > 2^32,
+ * ell or w out of range, digits not covering Q, workspace too small,
+ * in/out overlap), PIR_ERR_CUDA.
+ */
+uint64_t pir_coltor_workspace_bytes(const pir_ctx *ctx, uint64_t n, uint32_t ell);
+
+int pir_coltor_stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w,
+                     const uint32_t *in, uint64_t n, uint32_t *out,
+                     void *workspace, uint64_t workspace_bytes, void *stream);
+
+int pir_coltor(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w,
+               const uint32_t *in, uint64_t n, uint32_t *out,
+               void *workspace, uint64_t workspace_bytes, void *stream);
+
+/*
  * pir_scalar_workspace_bytes — device workspace pir_scalar_scan needs for a
  * C x B query matrix (0 for invalid sizes).
  */

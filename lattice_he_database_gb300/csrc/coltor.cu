@@ -1,0 +1,314 @@
+// coltor.cu — ColTor: the column tournament of RGSW-RLWE external products.
+//
+// GPIR section 2 (the ColTor phase of the OnionPIR family) and section 3
+// (Dcp, l = 5 digits); VIPIR 3.6 step 7 (RGSW-RLWE external products for the
+// folding after the first dimension) and section 5 (q ~ 2^87 in three RNS
+// primes).  One stage maps n ciphertexts (NTT form) to ceil(n/2):
+//     out_i = ct_2i + C (x) (ct_2i+1 - ct_2i)          (a missing partner is 0)
+// with the external product of the RGSW ciphertext C = [2 ell][2] RLWE rows
+//     C (x) ct = sum_u NTT(Dcp_u(ct_0)) . C[u] + NTT(Dcp_u(ct_1)) . C[ell + u],
+// where Dcp_u is digit u of each coefficient's CRT value X in [0, Q) in base
+// 2^w (unsigned digits, least significant first) and "." is the point-wise
+// product mod q_l.
+//
+// Per stage, five launches; every intermediate goes through HBM (for n = 1365
+// ciphertexts the first stage's digit polynomials alone are 336 MB, far past
+// L2), and the 2L inverse plus 2 ell L forward NTTs per pair bound the stage:
+//   1. coltor_diff_kernel   d_i = ct_2i+1 - ct_2i, [R][2][L][N]
+//   2. inverse NTT of d, in place (the library's NTT kernel)
+//   3. coltor_dcp_kernel    CRT value of each coefficient -> ell digits, [R][2][ell][N]
+//   4. lift + forward NTT of the digits (the library's NTT kernel) -> [R][2][ell][L][N]
+//   5. coltor_mac_kernel    out_i = ct_2i + sum_v D_v . C[v], lazy 64-bit sums
+#include <cstring>
+
+#include "common.cuh"
+
+extern "C" int pir_ntt_inv(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream);
+extern "C" int pir_lift_ntt(pir_ctx *ctx, const uint32_t *raw, uint32_t *out, uint64_t cnt, void *stream);
+
+namespace {
+
+typedef unsigned __int128 u128;
+
+constexpr uint32_t CT_THREADS = 256;
+constexpr uint32_t CT_MAX_ELL = 16;
+
+struct DiffArgs {
+    const uint32_t *in;
+    uint32_t *diff;
+    uint64_t n, R;          // input ciphertexts, pairs
+    uint32_t N, L;
+    uint32_t q[PIR_MAX_RNS];
+};
+
+// d_i = ct_2i+1 - ct_2i mod q_l, four words per thread.
+__global__ void __launch_bounds__(CT_THREADS) coltor_diff_kernel(const DiffArgs A) {
+    const uint64_t ct_words = 2ull * A.L * A.N;          // one ciphertext
+    const uint64_t total4 = A.R * ct_words / 4;
+    for (uint64_t v = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; v < total4;
+         v += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t w0 = v * 4;
+        const uint64_t i = w0 / ct_words, r = w0 - i * ct_words;
+        const uint32_t q = A.q[(r / A.N) % A.L];
+        const uint4 e = *reinterpret_cast<const uint4 *>(A.in + 2 * i * ct_words + r);
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (2 * i + 1 < A.n) o = *reinterpret_cast<const uint4 *>(A.in + (2 * i + 1) * ct_words + r);
+        uint4 d;
+        d.x = o.x + q - e.x; d.x = d.x >= q ? d.x - q : d.x;
+        d.y = o.y + q - e.y; d.y = d.y >= q ? d.y - q : d.y;
+        d.z = o.z + q - e.z; d.z = d.z >= q ? d.z - q : d.z;
+        d.w = o.w + q - e.w; d.w = d.w >= q ? d.w - q : d.w;
+        *reinterpret_cast<uint4 *>(A.diff + w0) = d;
+    }
+}
+
+struct DcpArgs {
+    const uint32_t *x;      // [polys][L][N] coefficient form
+    uint32_t *d;            // [polys][ell][N]
+    uint64_t polys;
+    uint32_t N, L, ell, w;
+    uint32_t q[PIR_MAX_RNS];
+    uint32_t hinv[PIR_MAX_RNS];      // (Q/q_l)^-1 mod q_l
+    uint32_t hinv_shoup[PIR_MAX_RNS];
+    uint64_t M_lo[PIR_MAX_RNS], M_hi[PIR_MAX_RNS];   // Q/q_l
+    uint64_t Q_lo, Q_hi;
+};
+
+// Dcp: X = sum_l [x_l (Q/q_l)^-1]_{q_l} * (Q/q_l), which lies in [0, L*Q) and
+// is brought into [0, Q) by at most L - 1 subtractions of Q; digit u is bits
+// [w u, w u + w) of X.  One thread per coefficient.
+__global__ void __launch_bounds__(CT_THREADS) coltor_dcp_kernel(const DcpArgs A) {
+    const uint64_t total = A.polys * A.N;
+    const u128 Q = ((u128)A.Q_hi << 64) | A.Q_lo;
+    const u128 mask = A.w >= 32 ? (u128)0xffffffffu : (((u128)1 << A.w) - 1);
+    for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total;
+         e += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t pi = e / A.N, t = e - pi * A.N;
+        const uint32_t *xp = A.x + pi * A.L * A.N + t;
+        u128 X = 0;
+        for (uint32_t l = 0; l < A.L; ++l) {
+            const uint32_t q = A.q[l];
+            uint32_t y = shoup_mul(xp[(uint64_t)l * A.N], A.hinv[l], A.hinv_shoup[l], q);
+            y = y >= q ? y - q : y;
+            X += (u128)y * (((u128)A.M_hi[l] << 64) | A.M_lo[l]);
+        }
+        for (uint32_t l = 1; l < A.L; ++l) X = X >= Q ? X - Q : X;
+        uint32_t *dp = A.d + pi * A.ell * A.N + t;
+        for (uint32_t u = 0; u < A.ell; ++u) {
+            const uint32_t sh = A.w * u;
+            dp[(uint64_t)u * A.N] = sh >= 128 ? 0u : (uint32_t)((X >> sh) & mask);
+        }
+    }
+}
+
+struct MacArgs {
+    const uint32_t *in;     // [n][2][L][N] (the even ciphertexts are added)
+    const uint32_t *dn;     // [R][2 ell][L][N] NTT of the digits
+    const uint32_t *C;      // [2 ell][2][L][N]
+    uint32_t *out;          // [R][2][L][N]
+    uint64_t R;
+    uint32_t N, L, ell;
+    uint32_t q[PIR_MAX_RNS];
+    uint64_t mu[PIR_MAX_RNS];
+};
+
+// out_i[c] = ct_2i[c] + sum_v D_i[v] . C[v][c]: per point both output
+// polynomials from one read of the 2 ell digit values; the 2 ell <= 32
+// products of residues below 2^29 sum below 2^63 without reduction.
+__global__ void __launch_bounds__(CT_THREADS) coltor_mac_kernel(const MacArgs A) {
+    const uint64_t LN = (uint64_t)A.L * A.N;
+    const uint64_t total = A.R * LN;
+    const uint32_t V = 2 * A.ell;
+    for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total;
+         e += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t i = e / LN, pt = e - i * LN;      // pt = l * N + j
+        const uint32_t l = (uint32_t)(pt / A.N);
+        const uint32_t q = A.q[l];
+        const uint32_t *dp = A.dn + i * V * LN + pt;
+        const uint32_t *cp = A.C + pt;
+        uint64_t acc0 = 0, acc1 = 0;
+        for (uint32_t v = 0; v < V; ++v) {
+            const uint64_t dv = dp[(uint64_t)v * LN];
+            acc0 += dv * cp[(uint64_t)(2 * v) * LN];
+            acc1 += dv * cp[(uint64_t)(2 * v + 1) * LN];
+        }
+        const uint32_t *ev = A.in + 2 * i * 2 * LN + pt;
+        uint32_t *op = A.out + i * 2 * LN + pt;
+        uint32_t r0 = barrett64(acc0, q, A.mu[l]) + ev[0];
+        uint32_t r1 = barrett64(acc1, q, A.mu[l]) + ev[LN];
+        op[0] = r0 >= q ? r0 - q : r0;
+        op[LN] = r1 >= q ? r1 - q : r1;
+    }
+}
+
+uint64_t align64(uint64_t words) { return (words + 63) / 64 * 64; }
+
+// Workspace regions (words) for stages of at most R pairs.
+struct CtLayout {
+    uint64_t diff, dig, dn, ping, pong, total;   // offsets and total words
+};
+
+CtLayout ct_layout(const pir_ctx *ctx, uint64_t n, uint32_t ell) {
+    const uint64_t R = (n + 1) / 2, LN = (uint64_t)ctx->L * ctx->N;
+    CtLayout c;
+    c.diff = 0;
+    c.dig = c.diff + align64(R * 2 * LN);
+    c.dn = c.dig + align64(R * 2 * ell * (uint64_t)ctx->N);
+    c.ping = c.dn + align64(R * 2 * ell * LN);
+    c.pong = c.ping + align64(R * 2 * LN);
+    c.total = c.pong + align64(((R + 1) / 2) * 2 * LN);
+    return c;
+}
+
+uint32_t bits_of_Q(const pir_ctx *ctx) {
+    u128 Q = 1;
+    for (uint32_t l = 0; l < ctx->L; ++l) Q *= ctx->q[l];
+    uint32_t b = 0;
+    while (b < 128 && (Q >> b) != 0) ++b;
+    return b;
+}
+
+int check_params(const pir_ctx *ctx, uint32_t ell, uint32_t w, uint64_t n) {
+    if (!ctx || n == 0) return PIR_ERR_ARG;
+    if (ell == 0 || ell > CT_MAX_ELL || w == 0 || w > 32) return PIR_ERR_ARG;
+    if ((uint64_t)ell * w < bits_of_Q(ctx)) return PIR_ERR_ARG;   // digits must cover [0, Q)
+    if (n > (1ull << 32)) return PIR_ERR_ARG;
+    return PIR_OK;
+}
+
+uint64_t grid_for(const pir_ctx *ctx, uint64_t work) {
+    const uint64_t g = (work + CT_THREADS - 1) / CT_THREADS;
+    const uint64_t cap = (uint64_t)ctx->num_sms * 8;
+    return g < 1 ? 1 : (g < cap ? g : cap);
+}
+
+// One stage from `in` (n ciphertexts) to `out` (ceil(n/2)); ws holds the
+// diff, digit and digit-NTT regions of a layout for at least n ciphertexts.
+int stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint32_t *in, uint64_t n, uint32_t *out,
+          uint32_t *ws, const CtLayout &lay, cudaStream_t st) {
+    const uint64_t R = (n + 1) / 2, LN = (uint64_t)ctx->L * ctx->N;
+    uint32_t *diff = ws + lay.diff, *dig = ws + lay.dig, *dn = ws + lay.dn;
+
+    DiffArgs da;
+    memset(&da, 0, sizeof(da));
+    da.in = in;
+    da.diff = diff;
+    da.n = n;
+    da.R = R;
+    da.N = ctx->N;
+    da.L = ctx->L;
+    for (uint32_t l = 0; l < ctx->L; ++l) da.q[l] = ctx->q[l];
+    coltor_diff_kernel<<<(unsigned)grid_for(ctx, R * 2 * LN / 4), CT_THREADS, 0, st>>>(da);
+    if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
+
+    int rc = pir_ntt_inv(ctx, diff, diff, R * 2, st);
+    if (rc) return rc;
+
+    DcpArgs ca;
+    memset(&ca, 0, sizeof(ca));
+    ca.x = diff;
+    ca.d = dig;
+    ca.polys = R * 2;
+    ca.N = ctx->N;
+    ca.L = ctx->L;
+    ca.ell = ell;
+    ca.w = w;
+    u128 Q = 1;
+    for (uint32_t l = 0; l < ctx->L; ++l) Q *= ctx->q[l];
+    ca.Q_lo = (uint64_t)Q;
+    ca.Q_hi = (uint64_t)(Q >> 64);
+    for (uint32_t l = 0; l < ctx->L; ++l) {
+        const uint32_t q = ctx->q[l];
+        const u128 M = Q / q;
+        const uint64_t Mmod = (uint64_t)(M % q);
+        // (Q/q_l)^-1 mod q_l by Fermat (q_l prime)
+        uint64_t inv = 1, b = Mmod, e = q - 2;
+        for (; e; e >>= 1) {
+            if (e & 1) inv = inv * b % q;
+            b = b * b % q;
+        }
+        ca.q[l] = q;
+        ca.hinv[l] = (uint32_t)inv;
+        ca.hinv_shoup[l] = (uint32_t)((inv << 32) / q);
+        ca.M_lo[l] = (uint64_t)M;
+        ca.M_hi[l] = (uint64_t)(M >> 64);
+    }
+    coltor_dcp_kernel<<<(unsigned)grid_for(ctx, R * 2 * ctx->N), CT_THREADS, 0, st>>>(ca);
+    if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
+
+    rc = pir_lift_ntt(ctx, dig, dn, R * 2 * ell, st);
+    if (rc) return rc;
+
+    MacArgs ma;
+    memset(&ma, 0, sizeof(ma));
+    ma.in = in;
+    ma.dn = dn;
+    ma.C = C;
+    ma.out = out;
+    ma.R = R;
+    ma.N = ctx->N;
+    ma.L = ctx->L;
+    ma.ell = ell;
+    for (uint32_t l = 0; l < ctx->L; ++l) {
+        ma.q[l] = ctx->q[l];
+        ma.mu[l] = ctx->mu[l];
+    }
+    coltor_mac_kernel<<<(unsigned)grid_for(ctx, R * LN), CT_THREADS, 0, st>>>(ma);
+    return launch_status(cudaGetLastError());
+}
+
+bool overlaps(const void *a, uint64_t abytes, const void *b, uint64_t bbytes) {
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + bbytes && y < x + abytes;
+}
+
+}  // namespace
+
+extern "C" uint64_t pir_coltor_workspace_bytes(const pir_ctx *ctx, uint64_t n, uint32_t ell) {
+    if (!ctx || n == 0 || ell == 0 || ell > CT_MAX_ELL || n > (1ull << 32)) return 0;
+    return ct_layout(ctx, n, ell).total * 4;
+}
+
+extern "C" int pir_coltor_stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint32_t *in,
+                                uint64_t n, uint32_t *out, void *workspace, uint64_t workspace_bytes,
+                                void *stream) {
+    int rc = check_params(ctx, ell, w, n);
+    if (rc) return rc;
+    if (!C || !in || !out || !workspace) return PIR_ERR_ARG;
+    if (!aligned16(C) || !aligned16(in) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
+    const CtLayout lay = ct_layout(ctx, n, ell);
+    if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
+    const uint64_t ctb = 2ull * ctx->L * ctx->N * 4;
+    if (overlaps(in, n * ctb, out, ((n + 1) / 2) * ctb)) return PIR_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
+    return stage(ctx, C, ell, w, in, n, out, static_cast<uint32_t *>(workspace), lay, (cudaStream_t)stream);
+}
+
+extern "C" int pir_coltor(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint32_t *in, uint64_t n,
+                          uint32_t *out, void *workspace, uint64_t workspace_bytes, void *stream) {
+    int rc = check_params(ctx, ell, w, n);
+    if (rc) return rc;
+    if (!C || !in || !out || !workspace) return PIR_ERR_ARG;
+    if (!aligned16(C) || !aligned16(in) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
+    const CtLayout lay = ct_layout(ctx, n, ell);
+    if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
+    const uint64_t ctw = 2ull * ctx->L * ctx->N;
+    if (overlaps(in, n * ctw * 4, out, ctw * 4)) return PIR_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (n == 1) return cudaMemcpyAsync(out, in, ctw * 4, cudaMemcpyDeviceToDevice, st) == cudaSuccess ? PIR_OK
+                                                                                              : PIR_ERR_CUDA;
+    uint32_t *ws = static_cast<uint32_t *>(workspace);
+    const uint64_t row = 2ull * ell * ctw;          // words of one stage's RGSW ciphertext
+    const uint32_t *cur = in;
+    uint64_t cnt = n;
+    for (uint32_t s = 0; cnt > 1; ++s) {
+        const uint64_t next = (cnt + 1) / 2;
+        uint32_t *dst = next == 1 ? out : ws + ((s & 1) ? lay.pong : lay.ping);
+        rc = stage(ctx, C + s * row, ell, w, cur, cnt, dst, ws, lay, st);
+        if (rc) return rc;
+        cur = dst;
+        cnt = next;
+    }
+    return PIR_OK;
+}

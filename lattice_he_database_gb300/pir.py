@@ -88,6 +88,13 @@ def lib() -> ctypes.CDLL:
         L.pir_scalar_scan.restype = ctypes.c_int
         L.pir_scalar_scan.argtypes = [_vp, _vp, ctypes.c_uint64, ctypes.c_uint64, _vp, ctypes.c_uint32, _vp,
                                       _vp, ctypes.c_uint64, _vp]
+        L.pir_coltor_workspace_bytes.restype = ctypes.c_uint64
+        L.pir_coltor_workspace_bytes.argtypes = [_vp, ctypes.c_uint64, ctypes.c_uint32]
+        for name in ("pir_coltor_stage", "pir_coltor"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, ctypes.c_uint64, _vp, _vp,
+                          ctypes.c_uint64, _vp]
         L.pir_status.restype = ctypes.c_int
         L.pir_status.argtypes = [_vp, _u32p, ctypes.c_int]
         L.pir_strerror.restype = ctypes.c_char_p
@@ -250,6 +257,34 @@ def pir_exppack(ctx: Ctx, h_db: torch.Tensor, n: int, Dr: int, C: torch.Tensor, 
     _check(lib().pir_exppack(ctx, _dev_ptr(h_db, 4, "h_db"), n, Dr, _dev_ptr(C, 4, "C"), _dev_ptr(G, 4, "G"), B,
              _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(), _stream(stream)),
            "pir_exppack")
+
+
+# ---------------------------------------------------------------- ColTor
+def pir_coltor_workspace_bytes(ctx: Ctx, n: int, ell: int) -> int:
+    return int(lib().pir_coltor_workspace_bytes(ctx, n, ell))
+
+
+def coltor_workspace(ctx: Ctx, n: int, ell: int, device="cuda") -> torch.Tensor:
+    """A device workspace sized for pir_coltor / pir_coltor_stage over n ciphertexts."""
+    return torch.empty(pir_coltor_workspace_bytes(ctx, n, ell), dtype=torch.uint8, device=device)
+
+
+def pir_coltor_stage(ctx: Ctx, C: torch.Tensor, ell: int, w: int, cts: torch.Tensor, n: int, out: torch.Tensor,
+                     workspace: torch.Tensor, stream=None):
+    """out_i = ct_2i + C (x) (ct_2i+1 - ct_2i), i < ceil(n/2) (all NTT form)."""
+    ws = _dev_ptr(workspace, workspace.element_size(), "workspace")
+    _check(lib().pir_coltor_stage(ctx, _dev_ptr(C, 4, "C"), ell, w, _dev_ptr(cts, 4, "in"), n,
+                                  _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(),
+                                  _stream(stream)), "pir_coltor_stage")
+
+
+def pir_coltor(ctx: Ctx, C: torch.Tensor, ell: int, w: int, cts: torch.Tensor, n: int, out: torch.Tensor,
+               workspace: torch.Tensor, stream=None):
+    """The whole tournament over n ciphertexts; C holds ceil(log2 n) stages' RGSW ciphertexts."""
+    ws = _dev_ptr(workspace, workspace.element_size(), "workspace")
+    _check(lib().pir_coltor(ctx, _dev_ptr(C, 4, "C"), ell, w, _dev_ptr(cts, 4, "in"), n,
+                            _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(),
+                            _stream(stream)), "pir_coltor")
 
 
 # ---------------------------------------------------------------- scalar scan

@@ -47,3 +47,16 @@ def test_samples_run_on_small_shapes(monkeypatch):
     assert sc.nbytes == 2 * 256
     line = bench.oracle_baseline(sc, 0.05)
     assert line["kind"] == "oracle" and line["cores"] == 2 and line["value"] > 0
+    ct = bench.ColtorSample(dict(N=16, L=3, n=11, ell=5, w=18))
+    ct()
+    assert ct.pairs == 2 and abs(ct.nbytes - 2 / 10) < 1e-12
+    line = bench.oracle_baseline(ct, 0.05)
+    assert line["unit"] == "queries/s" and line["value"] > 0
+
+
+@pytest.mark.parametrize("threads", [8, 72, 288])
+def test_coltor_sample_bounded(monkeypatch, threads):
+    monkeypatch.setattr(oracle, "default_threads", lambda: threads)
+    cfg = bench.WORKLOADS["coltor_1365"]
+    pairs = max(1, min((cfg["n"] + 1) // 2, threads))
+    assert pairs <= 288 and 2 * pairs * 2 * cfg["L"] * cfg["N"] * 4 < 300 * 1024 * 1024

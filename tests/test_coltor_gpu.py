@@ -1,0 +1,117 @@
+"""GPU parity: ColTor (gadget decomposition, RGSW-RLWE external product,
+tournament stages) against the oracle, bit-exact.
+
+Random RGSW rows and ciphertexts (seeded residues) at several ring sizes and
+gadget shapes, odd ciphertext counts (the missing partner is zero), the whole
+tournament, the 1365-ciphertext list one 64 GiB RowSel query produces, and the
+noise-free selection of ct[j*] at that size.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.helpers import ensure_built, to_dev, to_host_u32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pir():
+    ensure_built()
+    from lattice_he_database_gb300 import pir as p
+    return p
+
+
+def _setup(pir, N, L):
+    qs = oracle.primes(N, L)
+    psis = [oracle.min_psi(q, N) for q in qs]
+    return pir.pir_ctx_create(N, qs), qs, psis
+
+
+def _trivial_rgsw(bit, qs, N, ell, w):
+    """Noise-free RGSW of a constant bit, NTT form: C[u] = (bit g_u, 0), C[ell+u] = (0, bit g_u)."""
+    L = len(qs)
+    C = np.zeros((2 * ell, 2, L, N), dtype=np.uint32)
+    for u in range(ell):
+        for l, q in enumerate(qs):
+            C[u, 0, l] = C[ell + u, 1, l] = bit * pow(2, w * u, q)
+    return C
+
+
+@pytest.mark.parametrize("N,L,ell,w,n", [
+    (4096, 3, 5, 18, 2),
+    (4096, 3, 5, 18, 7),      # odd: the last ciphertext meets zero
+    (4096, 3, 3, 29, 16),     # fewer, wider digits
+    (256, 2, 4, 15, 9),
+    (64, 1, 1, 29, 5),        # one prime, one digit: Dcp is the identity
+    (16, 2, 16, 4, 3),        # many narrow digits (the top ones zero)
+])
+def test_stage_matches_oracle(pir, N, L, ell, w, n):
+    ctx, qs, psis = _setup(pir, N, L)
+    C = synth.residues(100 + n, (2 * ell, 2, L, N), qs)
+    cts = synth.residues(200 + n, (n, 2, L, N), qs)
+    out = pir.empty_u32(((n + 1) // 2) * 2 * L * N)
+    out.fill_(-1)
+    pir.pir_coltor_stage(ctx, to_dev(C), ell, w, to_dev(cts), n, out, pir.coltor_workspace(ctx, n, ell))
+    got = to_host_u32(out).reshape((n + 1) // 2, 2, L, N)
+    assert np.array_equal(got, oracle.coltor_stage(C, cts, qs, psis, ell, w))
+    assert pir.pir_status(ctx) == 0
+
+
+@pytest.mark.parametrize("n", [1, 2, 37])
+def test_tournament_matches_oracle(pir, n):
+    N, L, ell, w = 4096, 3, 5, 18
+    ctx, qs, psis = _setup(pir, N, L)
+    S = oracle.coltor_stages(n)
+    Cs = synth.residues(30 + n, (max(S, 1), 2 * ell, 2, L, N), qs)
+    cts = synth.residues(80 + n, (n, 2, L, N), qs)
+    out = pir.empty_u32(2 * L * N)
+    pir.pir_coltor(ctx, to_dev(Cs), ell, w, to_dev(cts), n, out, pir.coltor_workspace(ctx, n, ell))
+    got = to_host_u32(out).reshape(2, L, N)
+    assert np.array_equal(got, oracle.coltor(Cs, cts, qs, psis, ell, w))
+    assert pir.pir_status(ctx) == 0
+
+
+def test_tournament_full_size(pir):
+    """The 1365 ciphertexts of one 64 GiB RowSel query (D1 = 1365): 11 stages,
+    random RGSW rows, compared with the oracle; then noise-free RGSW bits of
+    j* = 1000 select ct[1000] exactly."""
+    import torch
+    N, L, ell, w, n = 4096, 3, 5, 18, 1365
+    ctx, qs, psis = _setup(pir, N, L)
+    S = oracle.coltor_stages(n)
+    assert S == 11
+    Cs = synth.residues(51, (S, 2 * ell, 2, L, N), qs)
+    cts = synth.residues(52, (n, 2, L, N), qs)
+    cts_d = to_dev(cts)
+    ws = pir.coltor_workspace(ctx, n, ell)
+    out = pir.empty_u32(2 * L * N)
+    pir.pir_coltor(ctx, to_dev(Cs), ell, w, cts_d, n, out, ws)
+    assert np.array_equal(to_host_u32(out).reshape(2, L, N), oracle.coltor(Cs, cts, qs, psis, ell, w))
+    jstar = 1000
+    sel = np.stack([_trivial_rgsw((jstar >> s) & 1, qs, N, ell, w) for s in range(S)])
+    out2 = torch.empty_like(out)
+    pir.pir_coltor(ctx, to_dev(sel), ell, w, cts_d, n, out2, ws)
+    assert np.array_equal(to_host_u32(out2).reshape(2, L, N), cts[jstar])
+    assert pir.pir_status(ctx) == 0
+
+
+def test_coltor_rejects_bad_arguments(pir):
+    N, L = 64, 3
+    ctx, qs, _ = _setup(pir, N, L)
+    C = pir.empty_u32(2 * 5 * 2 * L * N)
+    cts = pir.empty_u32(4 * 2 * L * N)
+    out = pir.empty_u32(2 * 2 * L * N)
+    ws = pir.coltor_workspace(ctx, 4, 5)
+    with pytest.raises(pir.PirError):                 # 5 digits of 17 bits do not cover Q ~ 2^87
+        pir.pir_coltor_stage(ctx, C, 5, 17, cts, 4, out, ws)
+    with pytest.raises(pir.PirError):                 # ell = 0
+        pir.pir_coltor_stage(ctx, C, 0, 18, cts, 4, out, ws)
+    with pytest.raises(pir.PirError):                 # workspace too small
+        pir.pir_coltor_stage(ctx, C, 5, 18, cts, 4, out, ws[:64])
+    with pytest.raises(pir.PirError):                 # out overlaps in
+        pir.pir_coltor_stage(ctx, C, 5, 18, cts, 4, cts, ws)
+    with pytest.raises(pir.PirError):                 # n = 0
+        pir.pir_coltor(ctx, C, 5, 18, cts, 0, out, ws)
+    assert pir.pir_coltor_workspace_bytes(ctx, 0, 5) == 0
