@@ -11,17 +11,21 @@
 // 2^w (unsigned digits, least significant first) and "." is the point-wise
 // product mod q_l.
 //
-// Per stage, five launches; every intermediate goes through HBM (for n = 1365
-// ciphertexts the first stage's digit polynomials alone are 336 MB, far past
-// L2), and the 2L inverse plus 2 ell L forward NTTs per pair bound the stage:
-//   1. coltor_diff_kernel   d_i = ct_2i+1 - ct_2i, [R][2][L][N]
-//   2. inverse NTT of d, in place (the library's NTT kernel)
-//   3. coltor_dcp_kernel    CRT value of each coefficient -> ell digits, [R][2][ell][N]
-//   4. lift + forward NTT of the digits (the library's NTT kernel) -> [R][2][ell][L][N]
-//   5. coltor_mac_kernel    out_i = ct_2i + sum_v D_v . C[v], lazy 64-bit sums
+// Per stage, four launches (five for N != 4096); every intermediate goes
+// through HBM (for n = 1365 ciphertexts the first stage's digit NTTs alone
+// are 336 MB, far past L2), and the 2L inverse plus 2 ell L forward NTTs per
+// pair bound the stage:
+//   1. coltor_diff_intt4096_kernel  d_i = INTT(ct_2i+1 - ct_2i), [R][2][L][N]
+//      (other N: coltor_diff_kernel, then the library's inverse NTT in place)
+//   2. coltor_dcp_kernel    CRT value of each coefficient -> ell digits, [R][2][ell][N]
+//   3. lift + forward NTT of the digits (the library's NTT kernel) -> [R][2][ell][L][N]
+//   4. coltor_mac_kernel    out_i = ct_2i + sum_v D_v . C[v], lazy 64-bit sums
+// The difference, decomposition and MAC kernels move four words per thread
+// and memory access; all three are bound by HBM.
 #include <cstring>
 
 #include "common.cuh"
+#include "ntt_core.cuh"
 
 extern "C" int pir_ntt_inv(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream);
 extern "C" int pir_lift_ntt(pir_ctx *ctx, const uint32_t *raw, uint32_t *out, uint64_t cnt, void *stream);
@@ -32,6 +36,16 @@ typedef unsigned __int128 u128;
 
 constexpr uint32_t CT_THREADS = 256;
 constexpr uint32_t CT_MAX_ELL = 16;
+
+// a[l] for a small runtime l without indexing the parameter array (which
+// would copy it to local memory).
+template <typename T>
+__device__ __forceinline__ T pick(const T (&a)[PIR_MAX_RNS], uint32_t l) {
+    T r = a[0];
+#pragma unroll
+    for (uint32_t k = 1; k < PIR_MAX_RNS; ++k) r = l == k ? a[k] : r;
+    return r;
+}
 
 struct DiffArgs {
     const uint32_t *in;
@@ -49,7 +63,7 @@ __global__ void __launch_bounds__(CT_THREADS) coltor_diff_kernel(const DiffArgs 
          v += (uint64_t)gridDim.x * blockDim.x) {
         const uint64_t w0 = v * 4;
         const uint64_t i = w0 / ct_words, r = w0 - i * ct_words;
-        const uint32_t q = A.q[(r / A.N) % A.L];
+        const uint32_t q = pick(A.q, (uint32_t)((r / A.N) % A.L));
         const uint4 e = *reinterpret_cast<const uint4 *>(A.in + 2 * i * ct_words + r);
         uint4 o = make_uint4(0, 0, 0, 0);
         if (2 * i + 1 < A.n) o = *reinterpret_cast<const uint4 *>(A.in + (2 * i + 1) * ct_words + r);
@@ -60,6 +74,60 @@ __global__ void __launch_bounds__(CT_THREADS) coltor_diff_kernel(const DiffArgs 
         d.w = o.w + q - e.w; d.w = d.w >= q ? d.w - q : d.w;
         *reinterpret_cast<uint4 *>(A.diff + w0) = d;
     }
+}
+
+struct DiffInttArgs {
+    const uint32_t *in;
+    uint32_t *diff;
+    const uint32_t *tw;     // [L][4][N] twiddle tables
+    uint64_t n;
+    uint32_t L;
+    uint32_t q[PIR_MAX_RNS], ninv[PIR_MAX_RNS], ninv_shoup[PIR_MAX_RNS];
+};
+
+// N = 4096: one CTA per difference row (pair i, polynomial c, prime l); the
+// first inverse round loads ct_2i+1 - ct_2i + q (in (0, 2q), the inverse
+// butterflies' input range) instead of a stored difference.  Rounds as in
+// the library's 4096-point inverse kernel.
+__global__ void __launch_bounds__(kT4) coltor_diff_intt4096_kernel(const __grid_constant__ DiffInttArgs A) {
+    __shared__ __align__(16) uint32_t sm[kN4];
+    const uint64_t row = blockIdx.x;
+    const uint32_t twoL = 2 * A.L;
+    const uint64_t i = row / twoL;
+    const uint32_t rem = (uint32_t)(row % twoL), l = rem % A.L;
+    const uint32_t q = A.q[l];
+    const uint32_t *W = A.tw + (size_t)l * 4 * kN4 + TW_INV * kN4;
+    const uint32_t *Wp = A.tw + (size_t)l * 4 * kN4 + TW_INV_SHOUP * kN4;
+    const uint32_t *ev = A.in + (2 * i * twoL + rem) * kN4;
+    const uint32_t *od = A.in + ((2 * i + 1) * twoL + rem) * kN4;
+    const bool has_odd = 2 * i + 1 < A.n;
+    const uint32_t t = threadIdx.x;
+    uint32_t x[16];
+#pragma unroll
+    for (int k = 0; k < 16; k += 4) {
+        const uint4 e = *reinterpret_cast<const uint4 *>(ev + 16 * t + k);
+        const uint4 o = has_odd ? *reinterpret_cast<const uint4 *>(od + 16 * t + k) : make_uint4(0, 0, 0, 0);
+        x[k] = o.x + q - e.x; x[k + 1] = o.y + q - e.y; x[k + 2] = o.z + q - e.z; x[k + 3] = o.w + q - e.w;
+    }
+    inv_round16(x, 11, t, W, Wp, q);
+#pragma unroll
+    for (int k = 0; k < 16; k += 4)
+        *reinterpret_cast<uint4 *>(sm + 16 * t + k) = make_uint4(x[k], x[k + 1], x[k + 2], x[k + 3]);
+    __syncthreads();
+    const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x[k] = sm[g1 + 16 * k];
+    inv_round16(x, 7, t >> 4, W, Wp, q);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) sm[g1 + 16 * k] = x[k];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x[k] = sm[t + 256 * k];
+    inv_round16(x, 3, 0, W, Wp, q);
+    uint32_t *dst = A.diff + row * kN4;
+    const uint32_t ni = A.ninv[l], nis = A.ninv_shoup[l];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) dst[t + 256 * k] = inv_final(x[k], ni, nis, q);
 }
 
 struct DcpArgs {
@@ -76,27 +144,64 @@ struct DcpArgs {
 
 // Dcp: X = sum_l [x_l (Q/q_l)^-1]_{q_l} * (Q/q_l), which lies in [0, L*Q) and
 // is brought into [0, Q) by at most L - 1 subtractions of Q; digit u is bits
-// [w u, w u + w) of X.  One thread per coefficient.
+// [w u, w u + w) of X.  One thread per four consecutive coefficients.
+__device__ __forceinline__ u128 crt_value(const DcpArgs &A, const uint32_t (&r)[PIR_MAX_RNS], u128 Q) {
+    u128 X = 0;
+#pragma unroll
+    for (uint32_t l = 0; l < PIR_MAX_RNS; ++l) {
+        if (l < A.L) {
+            const uint32_t q = A.q[l];
+            uint32_t y = shoup_mul(r[l], A.hinv[l], A.hinv_shoup[l], q);
+            y = y >= q ? y - q : y;
+            X += (u128)y * A.M_lo[l] + ((u128)((uint64_t)y * A.M_hi[l]) << 64);
+        }
+    }
+#pragma unroll
+    for (uint32_t l = 1; l < PIR_MAX_RNS; ++l)
+        if (l < A.L) X = X >= Q ? X - Q : X;
+    return X;
+}
+
 __global__ void __launch_bounds__(CT_THREADS) coltor_dcp_kernel(const DcpArgs A) {
-    const uint64_t total = A.polys * A.N;
+    const uint64_t total4 = A.polys * A.N / 4;
     const u128 Q = ((u128)A.Q_hi << 64) | A.Q_lo;
     const u128 mask = A.w >= 32 ? (u128)0xffffffffu : (((u128)1 << A.w) - 1);
-    for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total;
+    for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total4;
          e += (uint64_t)gridDim.x * blockDim.x) {
-        const uint64_t pi = e / A.N, t = e - pi * A.N;
+        const uint64_t t0 = e * 4;
+        const uint64_t pi = t0 / A.N, t = t0 - pi * A.N;
         const uint32_t *xp = A.x + pi * A.L * A.N + t;
-        u128 X = 0;
-        for (uint32_t l = 0; l < A.L; ++l) {
-            const uint32_t q = A.q[l];
-            uint32_t y = shoup_mul(xp[(uint64_t)l * A.N], A.hinv[l], A.hinv_shoup[l], q);
-            y = y >= q ? y - q : y;
-            X += (u128)y * (((u128)A.M_hi[l] << 64) | A.M_lo[l]);
+        uint4 rv[PIR_MAX_RNS];
+#pragma unroll
+        for (uint32_t l = 0; l < PIR_MAX_RNS; ++l)
+            rv[l] = l < A.L ? *reinterpret_cast<const uint4 *>(xp + (uint64_t)l * A.N) : make_uint4(0, 0, 0, 0);
+        u128 X[4];
+        {
+            uint32_t r[PIR_MAX_RNS];
+#pragma unroll
+            for (uint32_t l = 0; l < PIR_MAX_RNS; ++l) r[l] = rv[l].x;
+            X[0] = crt_value(A, r, Q);
+#pragma unroll
+            for (uint32_t l = 0; l < PIR_MAX_RNS; ++l) r[l] = rv[l].y;
+            X[1] = crt_value(A, r, Q);
+#pragma unroll
+            for (uint32_t l = 0; l < PIR_MAX_RNS; ++l) r[l] = rv[l].z;
+            X[2] = crt_value(A, r, Q);
+#pragma unroll
+            for (uint32_t l = 0; l < PIR_MAX_RNS; ++l) r[l] = rv[l].w;
+            X[3] = crt_value(A, r, Q);
         }
-        for (uint32_t l = 1; l < A.L; ++l) X = X >= Q ? X - Q : X;
         uint32_t *dp = A.d + pi * A.ell * A.N + t;
         for (uint32_t u = 0; u < A.ell; ++u) {
-            const uint32_t sh = A.w * u;
-            dp[(uint64_t)u * A.N] = sh >= 128 ? 0u : (uint32_t)((X >> sh) & mask);
+            uint4 d;
+            d.x = (uint32_t)(X[0] & mask);
+            d.y = (uint32_t)(X[1] & mask);
+            d.z = (uint32_t)(X[2] & mask);
+            d.w = (uint32_t)(X[3] & mask);
+            *reinterpret_cast<uint4 *>(dp + (uint64_t)u * A.N) = d;
+            if (A.w >= 128) break;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) X[k] >>= A.w;
         }
     }
 }
@@ -112,32 +217,43 @@ struct MacArgs {
     uint64_t mu[PIR_MAX_RNS];
 };
 
-// out_i[c] = ct_2i[c] + sum_v D_i[v] . C[v][c]: per point both output
-// polynomials from one read of the 2 ell digit values; the 2 ell <= 32
+// out_i[c] = ct_2i[c] + sum_v D_i[v] . C[v][c]: both output polynomials from
+// one read of the 2 ell digit values, four points per thread; the 2 ell <= 32
 // products of residues below 2^29 sum below 2^63 without reduction.
+__device__ __forceinline__ uint32_t mac_final(uint64_t acc, uint32_t e, uint32_t q, uint64_t mu) {
+    const uint32_t r = barrett64(acc, q, mu) + e;
+    return r >= q ? r - q : r;
+}
+
 __global__ void __launch_bounds__(CT_THREADS) coltor_mac_kernel(const MacArgs A) {
     const uint64_t LN = (uint64_t)A.L * A.N;
-    const uint64_t total = A.R * LN;
+    const uint64_t total4 = A.R * LN / 4;
     const uint32_t V = 2 * A.ell;
-    for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total;
+    for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total4;
          e += (uint64_t)gridDim.x * blockDim.x) {
-        const uint64_t i = e / LN, pt = e - i * LN;      // pt = l * N + j
+        const uint64_t e0 = e * 4;
+        const uint64_t i = e0 / LN, pt = e0 - i * LN;    // pt = l * N + j
         const uint32_t l = (uint32_t)(pt / A.N);
-        const uint32_t q = A.q[l];
         const uint32_t *dp = A.dn + i * V * LN + pt;
         const uint32_t *cp = A.C + pt;
-        uint64_t acc0 = 0, acc1 = 0;
+        uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
+#pragma unroll 2
         for (uint32_t v = 0; v < V; ++v) {
-            const uint64_t dv = dp[(uint64_t)v * LN];
-            acc0 += dv * cp[(uint64_t)(2 * v) * LN];
-            acc1 += dv * cp[(uint64_t)(2 * v + 1) * LN];
+            const uint4 d = *reinterpret_cast<const uint4 *>(dp + (uint64_t)v * LN);
+            const uint4 c0 = __ldg(reinterpret_cast<const uint4 *>(cp + (uint64_t)(2 * v) * LN));
+            const uint4 c1 = __ldg(reinterpret_cast<const uint4 *>(cp + (uint64_t)(2 * v + 1) * LN));
+            a0 += (uint64_t)d.x * c0.x; a1 += (uint64_t)d.y * c0.y; a2 += (uint64_t)d.z * c0.z; a3 += (uint64_t)d.w * c0.w;
+            b0 += (uint64_t)d.x * c1.x; b1 += (uint64_t)d.y * c1.y; b2 += (uint64_t)d.z * c1.z; b3 += (uint64_t)d.w * c1.w;
         }
-        const uint32_t *ev = A.in + 2 * i * 2 * LN + pt;
+        const uint32_t q = pick(A.q, l);
+        const uint64_t mu = pick(A.mu, l);
+        const uint4 ev0 = *reinterpret_cast<const uint4 *>(A.in + 2 * i * 2 * LN + pt);
+        const uint4 ev1 = *reinterpret_cast<const uint4 *>(A.in + 2 * i * 2 * LN + LN + pt);
         uint32_t *op = A.out + i * 2 * LN + pt;
-        uint32_t r0 = barrett64(acc0, q, A.mu[l]) + ev[0];
-        uint32_t r1 = barrett64(acc1, q, A.mu[l]) + ev[LN];
-        op[0] = r0 >= q ? r0 - q : r0;
-        op[LN] = r1 >= q ? r1 - q : r1;
+        *reinterpret_cast<uint4 *>(op) = make_uint4(mac_final(a0, ev0.x, q, mu), mac_final(a1, ev0.y, q, mu),
+                                                    mac_final(a2, ev0.z, q, mu), mac_final(a3, ev0.w, q, mu));
+        *reinterpret_cast<uint4 *>(op + LN) = make_uint4(mac_final(b0, ev1.x, q, mu), mac_final(b1, ev1.y, q, mu),
+                                                         mac_final(b2, ev1.z, q, mu), mac_final(b3, ev1.w, q, mu));
     }
 }
 
@@ -178,7 +294,7 @@ int check_params(const pir_ctx *ctx, uint32_t ell, uint32_t w, uint64_t n) {
 
 uint64_t grid_for(const pir_ctx *ctx, uint64_t work) {
     const uint64_t g = (work + CT_THREADS - 1) / CT_THREADS;
-    const uint64_t cap = (uint64_t)ctx->num_sms * 8;
+    const uint64_t cap = (uint64_t)ctx->num_sms * 16;
     return g < 1 ? 1 : (g < cap ? g : cap);
 }
 
@@ -198,11 +314,29 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint3
     da.N = ctx->N;
     da.L = ctx->L;
     for (uint32_t l = 0; l < ctx->L; ++l) da.q[l] = ctx->q[l];
-    coltor_diff_kernel<<<(unsigned)grid_for(ctx, R * 2 * LN / 4), CT_THREADS, 0, st>>>(da);
-    if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
-
-    int rc = pir_ntt_inv(ctx, diff, diff, R * 2, st);
-    if (rc) return rc;
+    int rc = PIR_OK;
+    if (ctx->N == (uint32_t)kN4) {
+        DiffInttArgs ia;
+        memset(&ia, 0, sizeof(ia));
+        ia.in = in;
+        ia.diff = diff;
+        ia.tw = ctx->d_tw;
+        ia.n = n;
+        ia.L = ctx->L;
+        for (uint32_t l = 0; l < ctx->L; ++l) {
+            ia.q[l] = ctx->q[l];
+            ia.ninv[l] = ctx->ninv[l];
+            ia.ninv_shoup[l] = ctx->ninv_shoup[l];
+        }
+        if (R * 2 * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
+        coltor_diff_intt4096_kernel<<<(unsigned)(R * 2 * ctx->L), kT4, 0, st>>>(ia);
+        if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
+    } else {
+        coltor_diff_kernel<<<(unsigned)grid_for(ctx, R * 2 * LN / 4), CT_THREADS, 0, st>>>(da);
+        if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
+        rc = pir_ntt_inv(ctx, diff, diff, R * 2, st);
+        if (rc) return rc;
+    }
 
     DcpArgs ca;
     memset(&ca, 0, sizeof(ca));
@@ -233,7 +367,7 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint3
         ca.M_lo[l] = (uint64_t)M;
         ca.M_hi[l] = (uint64_t)(M >> 64);
     }
-    coltor_dcp_kernel<<<(unsigned)grid_for(ctx, R * 2 * ctx->N), CT_THREADS, 0, st>>>(ca);
+    coltor_dcp_kernel<<<(unsigned)grid_for(ctx, R * 2 * ctx->N / 4), CT_THREADS, 0, st>>>(ca);
     if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
 
     rc = pir_lift_ntt(ctx, dig, dn, R * 2 * ell, st);
@@ -253,7 +387,7 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint3
         ma.q[l] = ctx->q[l];
         ma.mu[l] = ctx->mu[l];
     }
-    coltor_mac_kernel<<<(unsigned)grid_for(ctx, R * LN), CT_THREADS, 0, st>>>(ma);
+    coltor_mac_kernel<<<(unsigned)grid_for(ctx, R * LN / 4), CT_THREADS, 0, st>>>(ma);
     return launch_status(cudaGetLastError());
 }
 

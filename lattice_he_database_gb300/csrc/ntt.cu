@@ -57,60 +57,6 @@ __global__ void __launch_bounds__(kNttThreads) ntt_kernel(const uint32_t *__rest
     }
 }
 
-// N = 4096: 256 threads x 16 elements, three rounds of four butterfly stages.
-// The first round reads its 16 elements straight from global memory
-// (coalesced: element t + 256 i for the forward, 16t .. 16t+15 for the
-// inverse) and the last round writes straight back, so a row crosses shared
-// memory only twice.  Early-round twiddles are the same for all threads of a
-// warp (broadcast loads); the butterflies are branch-free.
-constexpr int kN4 = 4096, kT4 = 256;
-
-__device__ __forceinline__ uint32_t umin32(uint32_t a, uint32_t b) { return a < b ? a : b; }
-
-// One forward round of 4 stages (s0..s0+3) on x[16] = elements g + tlow*i.
-__device__ __forceinline__ void fwd_round16(uint32_t (&x)[16], uint32_t s0, uint32_t high,
-                                            const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
-                                            uint32_t q) {
-    const uint32_t q2 = 2 * q;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int d = 16 >> (r + 1);
-        const uint32_t m = 1u << (s0 + r);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if (i & d) continue;
-            const uint32_t idx = m + ((high << r) | (uint32_t)(i >> (4 - r)));
-            const uint32_t w = __ldg(W + idx), wp = __ldg(Wp + idx);
-            const uint32_t a = umin32(x[i], x[i] - q2);          // [0, 2q)
-            const uint32_t t = shoup_mul(x[i + d], w, wp, q);    // [0, 2q)
-            x[i] = a + t;
-            x[i + d] = a - t + q2;
-        }
-    }
-}
-
-// One inverse round of 4 stages s_hi..s_hi-3 on x[16] = elements g + tlow*i.
-__device__ __forceinline__ void inv_round16(uint32_t (&x)[16], uint32_t s_hi, uint32_t high,
-                                            const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
-                                            uint32_t q) {
-    const uint32_t q2 = 2 * q;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int d = 1 << r;
-        const uint32_t m = 1u << (s_hi - r);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if (i & d) continue;
-            const uint32_t idx = m + ((high << (3 - r)) | (uint32_t)(i >> (r + 1)));
-            const uint32_t w = __ldg(W + idx), wp = __ldg(Wp + idx);
-            const uint32_t u = x[i] + x[i + d];
-            const uint32_t v = x[i] - x[i + d] + q2;
-            x[i] = umin32(u, u - q2);                            // [0, 2q)
-            x[i + d] = shoup_mul(v, w, wp, q);                   // [0, 2q)
-        }
-    }
-}
-
 template <bool FWD, bool LIFT>
 __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                       const __grid_constant__ RnsParams P) {

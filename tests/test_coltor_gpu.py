@@ -2,8 +2,9 @@
 tournament stages) against the oracle, bit-exact.
 
 Random RGSW rows and ciphertexts (seeded residues) at several ring sizes and
-gadget shapes, odd ciphertext counts (the missing partner is zero), the whole
-tournament, the 1365-ciphertext list one 64 GiB RowSel query produces, and the
+gadget shapes, odd ciphertext counts (the missing partner is zero), stages
+small enough for the operation-level kernels and large enough for the fused
+stage-level kernel (N = 4096), the whole tournament, the 1365-ciphertext list one 64 GiB RowSel query produces, and the
 noise-free selection of ct[j*] at that size.
 """
 import numpy as np
@@ -46,11 +47,17 @@ def _trivial_rgsw(bit, qs, N, ell, w):
     (256, 2, 4, 15, 9),
     (64, 1, 1, 29, 5),        # one prime, one digit: Dcp is the identity
     (16, 2, 16, 4, 3),        # many narrow digits (the top ones zero)
+    # enough pairs for one CTA per SM: the stage-level (fused) kernel
+    (4096, 3, 5, 18, 333),    # odd count
+    (4096, 3, 3, 29, 400),
+    (4096, 2, 4, 15, 400),
+    (4096, 1, 1, 29, 400),
+    (4096, 3, 16, 6, 320),    # sixteen digits
 ])
 def test_stage_matches_oracle(pir, N, L, ell, w, n):
     ctx, qs, psis = _setup(pir, N, L)
-    C = synth.residues(100 + n, (2 * ell, 2, L, N), qs)
-    cts = synth.residues(200 + n, (n, 2, L, N), qs)
+    C = synth.residues(100 + n % 97, (2 * ell, 2, L, N), qs)
+    cts = synth.residues(200 + n % 53, (n, 2, L, N), qs)
     out = pir.empty_u32(((n + 1) // 2) * 2 * L * N)
     out.fill_(-1)
     pir.pir_coltor_stage(ctx, to_dev(C), ell, w, to_dev(cts), n, out, pir.coltor_workspace(ctx, n, ell))
