@@ -10,7 +10,9 @@ Every function restates a definition from the pages (see oracle.c):
   * GPIR (arXiv 2604.04696), section 2: RowSel as point-wise GEMMs
     M_out[p,m,n] = sum_k M_in0[p,m,k] * M_in1[p,k,n] mod q;
   * GPIR sections 2-3 and VIPIR 3.6 step 7: ColTor, the column tournament of
-    RGSW-RLWE external products with the gadget decomposition Dcp (l = 5).
+    RGSW-RLWE external products with the gadget decomposition Dcp (l = 5);
+  * GPIR sections 2-3: ExpandQuery, the expansion tree of Subs operations
+    (automorphism and key switching of the a polynomial).
 """
 from __future__ import annotations
 
@@ -86,6 +88,15 @@ def lib():
         L.orc_coltor_stage.restype = None
         L.orc_coltor_stage.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint32,
                                        ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint64, _u32p, ctypes.c_int]
+        L.orc_automorph.restype = None
+        L.orc_automorph.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, ctypes.c_uint32, _u32p, _u32p]
+        L.orc_subs.restype = None
+        L.orc_subs.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint32, ctypes.c_uint32,
+                               ctypes.c_uint32, _u32p, _u32p, _u32p]
+        L.orc_expand_stage.restype = None
+        L.orc_expand_stage.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint32,
+                                       ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint64, _u32p,
+                                       ctypes.c_int]
         L.orc_scalar_scan.restype = None
         L.orc_scalar_scan.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32, _u8p,
                                       _u32p, _u32p, ctypes.c_int]
@@ -302,3 +313,51 @@ def coltor(Cs: np.ndarray, cts: np.ndarray, qs, psis, ell: int, w: int, threads:
     for s in range(coltor_stages(cur.shape[0])):
         cur = coltor_stage(Cs[s], cur, qs, psis, ell, w, threads)
     return cur[0].copy()
+
+
+# --------------------------------------------------------------- ExpandQuery
+def automorph(a: np.ndarray, k: int, qs) -> np.ndarray:
+    """sigma_k(a) = a(X^k) for a [L][N] in coefficient form (k odd)."""
+    a = np.ascontiguousarray(a, dtype=np.uint32)
+    L, N = a.shape
+    q = np.asarray(qs, dtype=np.uint32)
+    out = np.empty_like(a)
+    lib().orc_automorph(N, L, _p32(q), k, _p32(a), _p32(out))
+    return out
+
+
+def subs(evk: np.ndarray, ct: np.ndarray, k: int, qs, psis, ell: int, w: int) -> np.ndarray:
+    """Subs(ct, k) with evk [ell][2][L][N]; ct and result [2][L][N], NTT form."""
+    evk = np.ascontiguousarray(evk, dtype=np.uint32)
+    ct = np.ascontiguousarray(ct, dtype=np.uint32)
+    _, L, N = ct.shape
+    assert evk.shape == (ell, 2, L, N)
+    q = np.asarray(qs, dtype=np.uint32)
+    ps = np.asarray(psis, dtype=np.uint32)
+    out = np.empty_like(ct)
+    lib().orc_subs(N, L, _p32(q), _p32(ps), ell, w, k, _p32(evk), _p32(ct), _p32(out))
+    return out
+
+
+def expand_stage(evk: np.ndarray, cts: np.ndarray, j: int, qs, psis, ell: int, w: int,
+                 threads: int | None = None) -> np.ndarray:
+    """Stage j of the expansion: cts [M][2][L][N] -> [2M][2][L][N] (NTT form)."""
+    evk = np.ascontiguousarray(evk, dtype=np.uint32)
+    cts = np.ascontiguousarray(cts, dtype=np.uint32)
+    M, _, L, N = cts.shape
+    assert evk.shape == (ell, 2, L, N) and (1 << j) < N
+    q = np.asarray(qs, dtype=np.uint32)
+    ps = np.asarray(psis, dtype=np.uint32)
+    out = np.empty((2 * M, 2, L, N), dtype=np.uint32)
+    lib().orc_expand_stage(N, L, _p32(q), _p32(ps), ell, w, j, _p32(evk), _p32(cts), M, _p32(out),
+                           threads or default_threads())
+    return out
+
+
+def expand(evks: np.ndarray, ct: np.ndarray, stages: int, qs, psis, ell: int, w: int,
+           threads: int | None = None) -> np.ndarray:
+    """ExpandQuery: one ciphertext [2][L][N] -> 2^stages ciphertexts; stage j uses evks[j]."""
+    cur = np.ascontiguousarray(ct, dtype=np.uint32)[None]
+    for j in range(stages):
+        cur = expand_stage(evks[j], cur, j, qs, psis, ell, w, threads)
+    return cur

@@ -602,3 +602,136 @@ void orc_coltor_stage(uint32_t N, uint32_t L, const uint32_t *q, const uint32_t 
     }
     for (int i = 0; i < nthreads; i++) pthread_join(th[i], NULL);
 }
+
+/* ------------------------------------------------------------------ */
+/* ExpandQuery: Subs (automorphism + key switching) and the expansion   */
+/* tree [GPIR section 2 (ExpandQuery, Subs, evk, up to log N stages)    */
+/*  and section 3 (Subs touches only the a polynomial)]                 */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Automorphism sigma_k: a(X) -> a(X^k) in Z_q[X]/(X^N+1), k odd, in
+ * coefficient form: coefficient t moves to t*k mod 2N, with a minus sign
+ * when that lands in [N, 2N) (X^N = -1).  a, out: [L][N].
+ */
+void orc_automorph(uint32_t N, uint32_t L, const uint32_t *q, uint32_t k, const uint32_t *a, uint32_t *out)
+{
+    for (uint32_t l = 0; l < L; l++)
+        for (uint32_t t = 0; t < N; t++) {
+            uint64_t e = (uint64_t)t * k % (2ull * N);
+            uint32_t v = a[(uint64_t)l * N + t] % q[l];
+            if (e < N) out[(uint64_t)l * N + e] = v;
+            else       out[(uint64_t)l * N + (e - N)] = (q[l] - v) % q[l];
+        }
+}
+
+/*
+ * Subs(ct, k) for ct = (c0, c1) decrypting as c0 + c1 s, with the
+ * evaluation key evk[u] = an RLWE encryption of sigma_k(s) g_u under s:
+ *     Subs(ct, k) = (NTT(sigma_k(c0)), 0)
+ *                 + sum_{u<ell} NTT(Dcp_u(sigma_k(c1))) (.) evk[u]
+ * Readings: only the a polynomial c1 is decomposed (GPIR section 3); Dcp is
+ * the decomposition of orc_dcp; evk is [ell][2][L][N] in NTT form.
+ *   ct, out : [2][L][N], NTT form.
+ */
+void orc_subs(uint32_t N, uint32_t L, const uint32_t *q, const uint32_t *psi, uint32_t ell, uint32_t w,
+              uint32_t k, const uint32_t *evk, const uint32_t *ct, uint32_t *out)
+{
+    uint64_t PN = (uint64_t)L * N;
+    uint32_t *c = (uint32_t *)malloc(sizeof(uint32_t) * 2 * PN);
+    uint32_t *s = (uint32_t *)malloc(sizeof(uint32_t) * 2 * PN);
+    uint32_t *d = (uint32_t *)malloc(sizeof(uint32_t) * ell * N);
+    uint32_t *dn = (uint32_t *)malloc(sizeof(uint32_t) * ell * PN);
+    memcpy(c, ct, sizeof(uint32_t) * 2 * PN);
+    for (uint32_t p = 0; p < 2; p++)
+        for (uint32_t l = 0; l < L; l++) orc_intt_iter(q[l], psi[l], N, c + p * PN + (uint64_t)l * N);
+    orc_automorph(N, L, q, k, c, s);              /* sigma(c0) */
+    orc_automorph(N, L, q, k, c + PN, s + PN);    /* sigma(c1) */
+    orc_dcp(N, L, q, ell, w, s + PN, d);
+    for (uint32_t u = 0; u < ell; u++)
+        for (uint32_t l = 0; l < L; l++) {
+            uint32_t *row = dn + ((uint64_t)u * L + l) * N;
+            for (uint32_t t = 0; t < N; t++) row[t] = d[(uint64_t)u * N + t] % q[l];
+            orc_ntt_iter(q[l], psi[l], N, row);
+        }
+    for (uint32_t l = 0; l < L; l++) orc_ntt_iter(q[l], psi[l], N, s + (uint64_t)l * N);   /* NTT(sigma(c0)) */
+    for (uint32_t p = 0; p < 2; p++)
+        for (uint32_t l = 0; l < L; l++)
+            for (uint32_t j = 0; j < N; j++) {
+                u128 acc = p == 0 ? s[(uint64_t)l * N + j] : 0;
+                for (uint32_t u = 0; u < ell; u++)
+                    acc += (u128)dn[((uint64_t)u * L + l) * N + j] * evk[(((uint64_t)u * 2 + p) * L + l) * N + j];
+                out[p * PN + (uint64_t)l * N + j] = (uint32_t)(acc % q[l]);
+            }
+    free(c);
+    free(s);
+    free(d);
+    free(dn);
+}
+
+/*
+ * One expansion stage j (Galois element k = N / 2^j + 1) over M ciphertexts:
+ *     out[i]     = ct_i + Subs(ct_i, k)
+ *     out[i + M] = (ct_i - Subs(ct_i, k)) * X^(-2^j)
+ * all in NTT form; the product by the monomial is point-wise by its NTT.
+ * Reading: the expansion tree of the SealPIR/OnionPIR family in this output
+ * order, so that after S stages ciphertext r carries coefficient r of the
+ * query plaintext, times 2^S, as a constant polynomial.
+ *   evk : [ell][2][L][N] (the key of this stage), in : [M][2][L][N],
+ *   out : [2M][2][L][N].
+ */
+typedef struct {
+    uint32_t N, L, ell, w, j;
+    const uint32_t *q, *psi, *evk, *in;
+    uint64_t M, i0, i1;
+    uint32_t *out;
+} expand_job;
+
+static void *expand_worker(void *arg)
+{
+    expand_job *jb = (expand_job *)arg;
+    uint32_t N = jb->N, L = jb->L;
+    uint64_t PN = (uint64_t)L * N, CT = 2 * PN;
+    uint32_t k = N / (1u << jb->j) + 1;
+    uint32_t *sub = (uint32_t *)malloc(sizeof(uint32_t) * CT);
+    uint32_t *mono = (uint32_t *)malloc(sizeof(uint32_t) * PN);
+    /* NTT(X^(-2^j)) = NTT(-X^(N - 2^j)) */
+    for (uint32_t l = 0; l < L; l++) {
+        uint32_t *row = mono + (uint64_t)l * N;
+        memset(row, 0, sizeof(uint32_t) * N);
+        row[N - (1u << jb->j)] = jb->q[l] - 1;                     /* j < log2 N */
+        orc_ntt_iter(jb->q[l], jb->psi[l], N, row);
+    }
+    for (uint64_t i = jb->i0; i < jb->i1; i++) {
+        const uint32_t *ct = jb->in + i * CT;
+        orc_subs(N, L, jb->q, jb->psi, jb->ell, jb->w, k, jb->evk, ct, sub);
+        uint32_t *o1 = jb->out + i * CT, *o2 = jb->out + (i + jb->M) * CT;
+        for (uint32_t p = 0; p < 2; p++)
+            for (uint32_t l = 0; l < L; l++) {
+                uint32_t ql = jb->q[l];
+                for (uint32_t t = 0; t < N; t++) {
+                    uint64_t x = p * PN + (uint64_t)l * N + t;
+                    uint64_t a = ct[x] % ql, b = sub[x];
+                    o1[x] = (uint32_t)((a + b) % ql);
+                    o2[x] = (uint32_t)((((a + ql - b) % ql) * mono[(uint64_t)l * N + t]) % ql);
+                }
+            }
+    }
+    free(sub);
+    free(mono);
+    return NULL;
+}
+
+void orc_expand_stage(uint32_t N, uint32_t L, const uint32_t *q, const uint32_t *psi, uint32_t ell, uint32_t w,
+                      uint32_t j, const uint32_t *evk, const uint32_t *in, uint64_t M, uint32_t *out,
+                      int nthreads)
+{
+    nthreads = clamp_threads(nthreads, M);
+    pthread_t th[256];
+    expand_job jobs[256];
+    for (int i = 0; i < nthreads; i++) {
+        jobs[i] = (expand_job){N, L, ell, w, j, q, psi, evk, in, M, M * i / nthreads, M * (i + 1) / nthreads, out};
+        pthread_create(&th[i], NULL, expand_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; i++) pthread_join(th[i], NULL);
+}
