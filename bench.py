@@ -49,6 +49,9 @@ WORKLOADS = {
                            desc="RowSel 24 GiB: N=4096, 3 primes, D0=512 x D1=1024, B=16 queries, NTT-domain"),
     "rowsel_64g_b16": dict(N=4096, L=3, D0=1024, D1=1365, B=16, domain="ntt",
                            desc="RowSel 64 GiB: N=4096, 3 primes, D0=1024 x D1=1365, B=16 queries, NTT-domain"),
+    "expand_1024": dict(kind="expand", N=4096, L=3, stages=10, ell=5, w=18,
+                        desc="ExpandQuery of one query ciphertext into the 1024 RowSel inputs of the 64 GiB DB: "
+                             "N=4096, 3 primes, 10 stages of Subs, l=5 digits of 18 bits"),
     "coltor_1365": dict(kind="coltor", N=4096, L=3, n=1365, ell=5, w=18,
                         desc="ColTor over the 1365 RowSel output ciphertexts of one 64 GiB query: N=4096, "
                              "3 primes, 11 stages of RGSW-RLWE external products, l=5 digits of 18 bits"),
@@ -79,6 +82,7 @@ METRIC = "DB GB/s scanned & queries/s (RowSel, 64 GiB DB), % of GB300 HBM roofli
 SPEC_HBM_GBS = 8000.0   # nominal GB300 HBM3e bandwidth (context for the roofline fractions)
 EXPPACK_METRIC = "ring-packing GEMM H*C + (0|G): hint GB/s scanned"
 COLTOR_METRIC = "ColTor column tournaments per second (RGSW-RLWE external products)"
+EXPAND_METRIC = "ExpandQuery expansions per second (Subs: automorphism + key switching)"
 
 
 def parse():
@@ -316,6 +320,33 @@ class ColtorSample:
         oracle.coltor_stage(self.C, self.cts, self.qs, self.psis, self.ell, self.w, threads=self.threads)
 
 
+class ExpandSample:
+    """Oracle ExpandQuery on a bounded sample: one expansion stage over one
+    ciphertext per host thread (one Subs each), counted as the fraction of a
+    whole expansion (2^stages - 1 Subs operations) it performs."""
+    unit = "queries/s"
+
+    def __init__(self, cfg):
+        import oracle
+        import synth
+        N, L, S, ell = cfg["N"], cfg["L"], cfg["stages"], cfg["ell"]
+        self.ell, self.w, self.stage = ell, cfg["w"], S - 1
+        self.threads = oracle.default_threads()
+        self.M = max(1, min(1 << (S - 1), self.threads))
+        self.qs = oracle.primes(N, L)
+        self.psis = [oracle.min_psi(q, N) for q in self.qs]
+        self.evk = synth.residues(13, (ell, 2, L, N), self.qs, tid=synth.T_EXTRA)
+        self.cts = synth.residues(14, (self.M, 2, L, N), self.qs, tid=synth.T_EXTRA)
+        self.nbytes = self.M / ((1 << S) - 1)          # expansions per call
+        self.desc = ("oracle ExpandQuery stage over %d ciphertexts (%d Subs of %d per expansion), N=%d, L=%d, l=%d"
+                     % (self.M, self.M, (1 << S) - 1, N, L, ell))
+
+    def __call__(self):
+        import oracle
+        oracle.expand_stage(self.evk, self.cts, self.stage, self.qs, self.psis, self.ell, self.w,
+                            threads=self.threads)
+
+
 def _rate(sample, units_per_s: float):
     """A sample's rate in its metric unit (GB/s unless the sample says otherwise)."""
     unit = getattr(sample, "unit", "GB/s")
@@ -374,6 +405,9 @@ def run_reference(args, cfg):
     elif kind == "coltor":
         run_reference_sample(args, ColtorSample(cfg), COLTOR_METRIC, "u32",
                              "synthetic (seeded SplitMix64 residues)", cfg["desc"])
+    elif kind == "expand":
+        run_reference_sample(args, ExpandSample(cfg), EXPAND_METRIC, "u32",
+                             "synthetic (seeded SplitMix64 residues)", cfg["desc"])
     else:
         run_reference_sample(args, RowselSample(cfg), METRIC, "u32", "synthetic (seeded SplitMix64 residues)",
                              cfg["desc"])
@@ -422,7 +456,9 @@ def launches_per_step(cfg) -> int:
     if cfg.get("kind") == "exppack":
         return 3 * rowsel_passes(cfg["n"], cfg["B"]) + 1
     if cfg.get("kind") == "coltor":
-        return 5 * coltor_stages(cfg["n"])
+        return 4 * coltor_stages(cfg["n"])
+    if cfg.get("kind") == "expand":
+        return 4 * cfg["stages"]
     return 3 * rowsel_passes(cfg["D0"], cfg["B"]) + (2 if cfg["domain"] == "coeff" else 0)
 
 
@@ -794,6 +830,121 @@ def run_coltor(args, cfg):
     return result
 
 
+def run_expand(args, cfg):
+    """ExpandQuery: one step = the whole expansion of one query ciphertext
+    (NTT form) into 2^stages ciphertexts, four launches per stage."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    import synth.device as sd
+    from lattice_he_database_gb300 import pir
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    N, L, S, ell, w = cfg["N"], cfg["L"], cfg["stages"], cfg["ell"], cfg["w"]
+    qs = pir.pir_primes(N, L)
+    ctx = pir.pir_ctx_create(N, qs, local)
+    P = L * N
+    ct = torch.empty(2 * P, dtype=torch.int32, device="cuda")
+    sd.fill_residues(ct, 9, synth.T_EXTRA, N, qs)
+    evks = torch.empty(S * ell * 2 * P, dtype=torch.int32, device="cuda")
+    sd.fill_residues(evks, 10, synth.T_EXTRA, N, qs)
+    out = torch.empty((1 << S) * 2 * P, dtype=torch.int32, device="cuda")
+    ws = pir.expand_workspace(ctx, 1 << (S - 1), ell)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def step():
+        pir.pir_expand(ctx, evks, ell, w, S, ct, out, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_total = max_over_ranks(t0.elapsed_time(t1))
+    if pir.pir_status(ctx):
+        raise RuntimeError("device status word set")
+
+    ct_bytes = 2 * P * 4
+    o_bytes = (1 << S) * 2 * P * 4
+    ct_host = torch.empty(ct.numel(), dtype=torch.int32, pin_memory=True)
+    ct_host.copy_(ct.cpu())
+    o_host = torch.empty(out.numel(), dtype=torch.int32, pin_memory=True)
+    ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            ct.copy_(ct_host, non_blocking=True)
+            step()
+            o_host.copy_(out, non_blocking=True)
+
+    e2e_ms = None
+    if ke:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / ke
+
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    ms_step = ms_total / args.steps
+    # at the least every stage reads its inputs and key and writes its outputs
+    algo = sum(((1 << j) * 3 + ell) * 2 * P * 4 for j in range(S))
+    achieved = algo / (ms_step * 1e-3) / 1e9
+    nsubs = (1 << S) - 1
+    nntt = nsubs * (L + ell * L)
+    result = None
+    if rank == 0:
+        line = {
+            "metric": EXPAND_METRIC, "value": world * args.steps / (ms_total * 1e-3), "unit": "queries/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+            "data": "synthetic: seeded SplitMix64 residues U[0,q_i) for the query ciphertext and keys",
+            "config": {"workload": args.workload, "desc": cfg["desc"], "stages": S, "outputs": 1 << S,
+                       "ell": ell, "w": w,
+                       "l2": "outputs %.0f MB exceed L2; no flush" % (o_bytes / 1e6),
+                       "parallelism": "replicas x%d" % world},
+            "subs_per_s": world * args.steps * nsubs / (ms_total * 1e-3),
+            "ntt_per_step": nntt, "ntt_per_s": nntt / (ms_step * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": profile_traffic("expand_%s" % args.workload),
+                         "kernel": "the expansion's four kernels per stage (NTT kernels dominate)",
+                         "peak_source": "%s hbm_gbs (copy)" % peak_kind, "algorithmic_bytes_per_launch": algo},
+            "clocks": clk,
+            "e2e": None if e2e_ms is None else {
+                "value": 1e3 / e2e_ms, "unit": "queries/s", "h2d_bytes_per_step": ct_bytes,
+                "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * launches_per_step(cfg),
+            "cpu_baseline": None,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = oracle_baseline(ExpandSample(cfg), args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+        result = line
+    ctx.close()
+    return result
+
+
 def run_ours(args, cfg):
     import torch
     import torch.distributed as dist
@@ -996,6 +1147,8 @@ def main():
         run_exppack(args, cfg)
     elif cfg.get("kind") == "coltor":
         run_coltor(args, cfg)
+    elif cfg.get("kind") == "expand":
+        run_expand(args, cfg)
     else:
         run_ours(args, cfg)
 

@@ -267,6 +267,42 @@ int pir_coltor(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w,
                void *workspace, uint64_t workspace_bytes, void *stream);
 
 /*
+ * ExpandQuery — the expansion tree of Subs operations (GPIR section 2:
+ * every depth of the tree is a stage with its own evaluation key, up to
+ * log2 N stages; GPIR section 3: Subs operates on the a polynomial only).
+ * A ciphertext ct = (c0, c1) decrypts as c0 + c1 s.  With sigma_k(a)(X) =
+ * a(X^k) and the gadget decomposition Dcp of pir_coltor:
+ *     Subs(ct, k) = (sigma_k(c0), 0) + sum_u NTT(Dcp_u(sigma_k(c1))) . evk[u]
+ * where evk[u] is an RLWE encryption of sigma_k(s) g_u under s.  Stage j
+ * (k = N/2^j + 1) over M ciphertexts writes 2M:
+ *     out[i]     = ct_i + Subs(ct_i, k)
+ *     out[i + M] = (ct_i - Subs(ct_i, k)) * X^(-2^j)
+ * so after S stages (pir_expand) ciphertext r carries coefficient r of the
+ * query's plaintext times 2^S (reading: the SealPIR/OnionPIR tree in this
+ * order; the client pre-scales by 2^-S).
+ *   evk  : device, [ell][2][L][N] NTT form (one stage's key); for
+ *          pir_expand, [stages][ell][2][L][N], stage j's key at j.
+ *   in   : device, [M][2][L][N] NTT form; for pir_expand one ciphertext.
+ *   out  : device, NTT form; pir_expand_stage: [2M][2][L][N], pir_expand:
+ *          [2^stages][2][L][N]; must not overlap the input.
+ *   ell, w : as for pir_coltor; j < log2 N; 1 <= stages <= log2 N.
+ *   workspace : device, >= pir_expand_workspace_bytes(ctx, M, ell) bytes
+ *          (pir_expand: M = 2^(stages-1)), 16-byte aligned; contents
+ *          undefined after the call.
+ * Errors: PIR_ERR_ARG (NULL/unaligned pointers, sizes or gadget parameters
+ * out of range, workspace too small, overlap), PIR_ERR_CUDA.
+ */
+uint64_t pir_expand_workspace_bytes(const pir_ctx *ctx, uint64_t M, uint32_t ell);
+
+int pir_expand_stage(pir_ctx *ctx, const uint32_t *evk, uint32_t ell, uint32_t w, uint32_t j,
+                     const uint32_t *in, uint64_t M, uint32_t *out,
+                     void *workspace, uint64_t workspace_bytes, void *stream);
+
+int pir_expand(pir_ctx *ctx, const uint32_t *evks, uint32_t ell, uint32_t w, uint32_t stages,
+               const uint32_t *ct, uint32_t *out,
+               void *workspace, uint64_t workspace_bytes, void *stream);
+
+/*
  * pir_scalar_workspace_bytes — device workspace pir_scalar_scan needs for a
  * C x B query matrix (0 for invalid sizes).
  */

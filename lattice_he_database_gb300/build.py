@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpir.so")
-SOURCES = ["ctx.cu", "ntt.cu", "encode.cu", "rowsel.cu", "rowsel_tc.cu", "scalar.cu", "server.cu", "coltor.cu"]
+SOURCES = ["ctx.cu", "ntt.cu", "encode.cu", "rowsel.cu", "rowsel_tc.cu", "scalar.cu", "server.cu", "coltor.cu", "expand.cu"]
 HEADERS = ["common.cuh", "ntt_core.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

@@ -17,14 +17,16 @@
 // pair bound the stage:
 //   1. coltor_diff_intt4096_kernel  d_i = INTT(ct_2i+1 - ct_2i), [R][2][L][N]
 //      (other N: coltor_diff_kernel, then the library's inverse NTT in place)
-//   2. coltor_dcp_kernel    CRT value of each coefficient -> ell digits, [R][2][ell][N]
+//   2. gadget_dcp_kernel    CRT value of each coefficient -> ell digits, [R][2][ell][N]
 //   3. lift + forward NTT of the digits (the library's NTT kernel) -> [R][2][ell][L][N]
 //   4. coltor_mac_kernel    out_i = ct_2i + sum_v D_v . C[v], lazy 64-bit sums
 // The difference, decomposition and MAC kernels move four words per thread
-// and memory access; all three are bound by HBM.
+// and memory access; all three are bound by HBM.  The decomposition is
+// shared with ExpandQuery (gadget.cuh).
 #include <cstring>
 
 #include "common.cuh"
+#include "gadget.cuh"
 #include "ntt_core.cuh"
 
 extern "C" int pir_ntt_inv(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream);
@@ -32,20 +34,7 @@ extern "C" int pir_lift_ntt(pir_ctx *ctx, const uint32_t *raw, uint32_t *out, ui
 
 namespace {
 
-typedef unsigned __int128 u128;
-
 constexpr uint32_t CT_THREADS = 256;
-constexpr uint32_t CT_MAX_ELL = 16;
-
-// a[l] for a small runtime l without indexing the parameter array (which
-// would copy it to local memory).
-template <typename T>
-__device__ __forceinline__ T pick(const T (&a)[PIR_MAX_RNS], uint32_t l) {
-    T r = a[0];
-#pragma unroll
-    for (uint32_t k = 1; k < PIR_MAX_RNS; ++k) r = l == k ? a[k] : r;
-    return r;
-}
 
 struct DiffArgs {
     const uint32_t *in;
@@ -130,82 +119,6 @@ __global__ void __launch_bounds__(kT4) coltor_diff_intt4096_kernel(const __grid_
     for (int k = 0; k < 16; ++k) dst[t + 256 * k] = inv_final(x[k], ni, nis, q);
 }
 
-struct DcpArgs {
-    const uint32_t *x;      // [polys][L][N] coefficient form
-    uint32_t *d;            // [polys][ell][N]
-    uint64_t polys;
-    uint32_t N, L, ell, w;
-    uint32_t q[PIR_MAX_RNS];
-    uint32_t hinv[PIR_MAX_RNS];      // (Q/q_l)^-1 mod q_l
-    uint32_t hinv_shoup[PIR_MAX_RNS];
-    uint64_t M_lo[PIR_MAX_RNS], M_hi[PIR_MAX_RNS];   // Q/q_l
-    uint64_t Q_lo, Q_hi;
-};
-
-// Dcp: X = sum_l [x_l (Q/q_l)^-1]_{q_l} * (Q/q_l), which lies in [0, L*Q) and
-// is brought into [0, Q) by at most L - 1 subtractions of Q; digit u is bits
-// [w u, w u + w) of X.  One thread per four consecutive coefficients.
-__device__ __forceinline__ u128 crt_value(const DcpArgs &A, const uint32_t (&r)[PIR_MAX_RNS], u128 Q) {
-    u128 X = 0;
-#pragma unroll
-    for (uint32_t l = 0; l < PIR_MAX_RNS; ++l) {
-        if (l < A.L) {
-            const uint32_t q = A.q[l];
-            uint32_t y = shoup_mul(r[l], A.hinv[l], A.hinv_shoup[l], q);
-            y = y >= q ? y - q : y;
-            X += (u128)y * A.M_lo[l] + ((u128)((uint64_t)y * A.M_hi[l]) << 64);
-        }
-    }
-#pragma unroll
-    for (uint32_t l = 1; l < PIR_MAX_RNS; ++l)
-        if (l < A.L) X = X >= Q ? X - Q : X;
-    return X;
-}
-
-__global__ void __launch_bounds__(CT_THREADS) coltor_dcp_kernel(const DcpArgs A) {
-    const uint64_t total4 = A.polys * A.N / 4;
-    const u128 Q = ((u128)A.Q_hi << 64) | A.Q_lo;
-    const u128 mask = A.w >= 32 ? (u128)0xffffffffu : (((u128)1 << A.w) - 1);
-    for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total4;
-         e += (uint64_t)gridDim.x * blockDim.x) {
-        const uint64_t t0 = e * 4;
-        const uint64_t pi = t0 / A.N, t = t0 - pi * A.N;
-        const uint32_t *xp = A.x + pi * A.L * A.N + t;
-        uint4 rv[PIR_MAX_RNS];
-#pragma unroll
-        for (uint32_t l = 0; l < PIR_MAX_RNS; ++l)
-            rv[l] = l < A.L ? *reinterpret_cast<const uint4 *>(xp + (uint64_t)l * A.N) : make_uint4(0, 0, 0, 0);
-        u128 X[4];
-        {
-            uint32_t r[PIR_MAX_RNS];
-#pragma unroll
-            for (uint32_t l = 0; l < PIR_MAX_RNS; ++l) r[l] = rv[l].x;
-            X[0] = crt_value(A, r, Q);
-#pragma unroll
-            for (uint32_t l = 0; l < PIR_MAX_RNS; ++l) r[l] = rv[l].y;
-            X[1] = crt_value(A, r, Q);
-#pragma unroll
-            for (uint32_t l = 0; l < PIR_MAX_RNS; ++l) r[l] = rv[l].z;
-            X[2] = crt_value(A, r, Q);
-#pragma unroll
-            for (uint32_t l = 0; l < PIR_MAX_RNS; ++l) r[l] = rv[l].w;
-            X[3] = crt_value(A, r, Q);
-        }
-        uint32_t *dp = A.d + pi * A.ell * A.N + t;
-        for (uint32_t u = 0; u < A.ell; ++u) {
-            uint4 d;
-            d.x = (uint32_t)(X[0] & mask);
-            d.y = (uint32_t)(X[1] & mask);
-            d.z = (uint32_t)(X[2] & mask);
-            d.w = (uint32_t)(X[3] & mask);
-            *reinterpret_cast<uint4 *>(dp + (uint64_t)u * A.N) = d;
-            if (A.w >= 128) break;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) X[k] >>= A.w;
-        }
-    }
-}
-
 struct MacArgs {
     const uint32_t *in;     // [n][2][L][N] (the even ciphertexts are added)
     const uint32_t *dn;     // [R][2 ell][L][N] NTT of the digits
@@ -276,27 +189,12 @@ CtLayout ct_layout(const pir_ctx *ctx, uint64_t n, uint32_t ell) {
     return c;
 }
 
-uint32_t bits_of_Q(const pir_ctx *ctx) {
-    u128 Q = 1;
-    for (uint32_t l = 0; l < ctx->L; ++l) Q *= ctx->q[l];
-    uint32_t b = 0;
-    while (b < 128 && (Q >> b) != 0) ++b;
-    return b;
-}
-
 int check_params(const pir_ctx *ctx, uint32_t ell, uint32_t w, uint64_t n) {
-    if (!ctx || n == 0) return PIR_ERR_ARG;
-    if (ell == 0 || ell > CT_MAX_ELL || w == 0 || w > 32) return PIR_ERR_ARG;
-    if ((uint64_t)ell * w < bits_of_Q(ctx)) return PIR_ERR_ARG;   // digits must cover [0, Q)
-    if (n > (1ull << 32)) return PIR_ERR_ARG;
-    return PIR_OK;
+    if (!ctx || n == 0 || n > (1ull << 32)) return PIR_ERR_ARG;
+    return gadget_params_ok(ctx, ell, w) ? PIR_OK : PIR_ERR_ARG;   // digits must cover [0, Q)
 }
 
-uint64_t grid_for(const pir_ctx *ctx, uint64_t work) {
-    const uint64_t g = (work + CT_THREADS - 1) / CT_THREADS;
-    const uint64_t cap = (uint64_t)ctx->num_sms * 16;
-    return g < 1 ? 1 : (g < cap ? g : cap);
-}
+uint64_t grid_for(const pir_ctx *ctx, uint64_t work) { return gadget_grid(ctx, work); }
 
 // One stage from `in` (n ciphertexts) to `out` (ceil(n/2)); ws holds the
 // diff, digit and digit-NTT regions of a layout for at least n ciphertexts.
@@ -338,37 +236,8 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint3
         if (rc) return rc;
     }
 
-    DcpArgs ca;
-    memset(&ca, 0, sizeof(ca));
-    ca.x = diff;
-    ca.d = dig;
-    ca.polys = R * 2;
-    ca.N = ctx->N;
-    ca.L = ctx->L;
-    ca.ell = ell;
-    ca.w = w;
-    u128 Q = 1;
-    for (uint32_t l = 0; l < ctx->L; ++l) Q *= ctx->q[l];
-    ca.Q_lo = (uint64_t)Q;
-    ca.Q_hi = (uint64_t)(Q >> 64);
-    for (uint32_t l = 0; l < ctx->L; ++l) {
-        const uint32_t q = ctx->q[l];
-        const u128 M = Q / q;
-        const uint64_t Mmod = (uint64_t)(M % q);
-        // (Q/q_l)^-1 mod q_l by Fermat (q_l prime)
-        uint64_t inv = 1, b = Mmod, e = q - 2;
-        for (; e; e >>= 1) {
-            if (e & 1) inv = inv * b % q;
-            b = b * b % q;
-        }
-        ca.q[l] = q;
-        ca.hinv[l] = (uint32_t)inv;
-        ca.hinv_shoup[l] = (uint32_t)((inv << 32) / q);
-        ca.M_lo[l] = (uint64_t)M;
-        ca.M_hi[l] = (uint64_t)(M >> 64);
-    }
-    coltor_dcp_kernel<<<(unsigned)grid_for(ctx, R * 2 * ctx->N / 4), CT_THREADS, 0, st>>>(ca);
-    if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
+    rc = gadget_dcp_launch(ctx, gadget_dcp_args(ctx, diff, LN, dig, R * 2, ell, w, 1), st);
+    if (rc) return rc;
 
     rc = pir_lift_ntt(ctx, dig, dn, R * 2 * ell, st);
     if (rc) return rc;
@@ -399,7 +268,7 @@ bool overlaps(const void *a, uint64_t abytes, const void *b, uint64_t bbytes) {
 }  // namespace
 
 extern "C" uint64_t pir_coltor_workspace_bytes(const pir_ctx *ctx, uint64_t n, uint32_t ell) {
-    if (!ctx || n == 0 || ell == 0 || ell > CT_MAX_ELL || n > (1ull << 32)) return 0;
+    if (!ctx || n == 0 || ell == 0 || ell > GD_MAX_ELL || n > (1ull << 32)) return 0;
     return ct_layout(ctx, n, ell).total * 4;
 }
 

@@ -1,0 +1,300 @@
+// expand.cu — ExpandQuery: the expansion tree of Subs operations.
+//
+// GPIR section 2 (ExpandQuery: every depth of the expansion tree is a stage
+// with its own evaluation key evk, up to log N stages) and section 3 (Subs
+// operates on the a polynomial only).  Stage j, Galois element k = N/2^j + 1,
+// over M ciphertexts ct = (c0, c1) in NTT form (decrypting as c0 + c1 s):
+//     S_i      = Subs(ct_i, k) = (sigma_k(c0), 0)
+//                + sum_u NTT(Dcp_u(sigma_k(c1))) . evk_j[u]
+//     out[i]     = ct_i + S_i
+//     out[i + M] = (ct_i - S_i) . NTT(X^(-2^j))
+// so that after S stages ciphertext r carries coefficient r of the query's
+// plaintext (times 2^S).  sigma_k(a)(X) = a(X^k): in coefficient form a
+// move of coefficient t to t k mod 2N with a sign, in NTT form a permutation
+// of the evaluation slots (slot j holds the value at zeta_j =
+// psi^(2 brv(j) + 1), and sigma_k(a)(zeta_j) = a(zeta_j^k)).
+//
+// Per stage, four launches:
+//   1. expand_intt_a4096_kernel  inverse NTT of every c1 (N = 4096; other N:
+//      a strided copy and the library's inverse NTT)
+//   2. gadget_dcp_kernel         digits of sigma_k(c1) (the automorphism as a
+//      gather with signs)
+//   3. lift + forward NTT of the digits (the library's NTT kernel)
+//   4. expand_mac_kernel         the key switch, sigma_k(c0) by slot
+//      permutation, and both outputs with the monomial's NTT
+#include <cstring>
+
+#include "common.cuh"
+#include "gadget.cuh"
+#include "ntt_core.cuh"
+
+extern "C" int pir_ntt_inv(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream);
+extern "C" int pir_lift_ntt(pir_ctx *ctx, const uint32_t *raw, uint32_t *out, uint64_t cnt, void *stream);
+
+namespace {
+
+struct InttAArgs {
+    const uint32_t *in;     // [M][2][L][N]
+    uint32_t *coef;         // [M][L][N]
+    const uint32_t *tw;
+    uint32_t L;
+    uint32_t q[PIR_MAX_RNS], ninv[PIR_MAX_RNS], ninv_shoup[PIR_MAX_RNS];
+};
+
+// N = 4096: one CTA per (ciphertext i, prime l) row of c1; rounds as in the
+// library's 4096-point inverse kernel.
+__global__ void __launch_bounds__(kT4) expand_intt_a4096_kernel(const __grid_constant__ InttAArgs A) {
+    __shared__ __align__(16) uint32_t sm[kN4];
+    const uint64_t row = blockIdx.x;
+    const uint64_t i = row / A.L;
+    const uint32_t l = (uint32_t)(row % A.L);
+    const uint32_t q = A.q[l];
+    const uint32_t *W = A.tw + (size_t)l * 4 * kN4 + TW_INV * kN4;
+    const uint32_t *Wp = A.tw + (size_t)l * 4 * kN4 + TW_INV_SHOUP * kN4;
+    const uint32_t *src = A.in + ((2 * i + 1) * A.L + l) * kN4;
+    const uint32_t t = threadIdx.x;
+    uint32_t x[16];
+#pragma unroll
+    for (int k = 0; k < 16; k += 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * t + k);
+        x[k] = v.x; x[k + 1] = v.y; x[k + 2] = v.z; x[k + 3] = v.w;
+    }
+    inv_round16(x, 11, t, W, Wp, q);
+#pragma unroll
+    for (int k = 0; k < 16; k += 4)
+        *reinterpret_cast<uint4 *>(sm + 16 * t + k) = make_uint4(x[k], x[k + 1], x[k + 2], x[k + 3]);
+    __syncthreads();
+    const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x[k] = sm[g1 + 16 * k];
+    inv_round16(x, 7, t >> 4, W, Wp, q);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) sm[g1 + 16 * k] = x[k];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x[k] = sm[t + 256 * k];
+    inv_round16(x, 3, 0, W, Wp, q);
+    uint32_t *dst = A.coef + row * kN4;
+    const uint32_t ni = A.ninv[l], nis = A.ninv_shoup[l];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) dst[t + 256 * k] = inv_final(x[k], ni, nis, q);
+}
+
+struct ExpMacArgs {
+    const uint32_t *in;     // [M][2][L][N]
+    const uint32_t *dn;     // [M][ell][L][N] NTT of the digits of sigma_k(c1)
+    const uint32_t *evk;    // [ell][2][L][N]
+    uint32_t *out;          // [2M][2][L][N]
+    const uint32_t *tw;     // [L][4][N]
+    uint64_t M;
+    uint32_t N, logN, L, ell, k, j;
+    uint32_t q[PIR_MAX_RNS];
+    uint64_t mu[PIR_MAX_RNS];
+};
+
+__device__ __forceinline__ uint32_t brv(uint32_t x, uint32_t logN) { return __brev(x) >> (32 - logN); }
+
+__device__ __forceinline__ uint32_t addq(uint32_t a, uint32_t b, uint32_t q) {
+    const uint32_t r = a + b;
+    return r >= q ? r - q : r;
+}
+
+__device__ __forceinline__ uint32_t subq(uint32_t a, uint32_t b, uint32_t q) {
+    const uint32_t r = a + q - b;
+    return r >= q ? r - q : r;
+}
+
+// Four consecutive slots per thread.  The ell <= 16 key-switch products of
+// residues below 2^29 sum below 2^62 without reduction.
+__global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs A) {
+    const uint64_t LN = (uint64_t)A.L * A.N;
+    const uint64_t total4 = A.M * LN / 4;
+    const uint32_t twoN = 2 * A.N;
+    for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total4;
+         e += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t e0 = e * 4;
+        const uint64_t i = e0 / LN, pt = e0 - i * LN;    // pt = l * N + slot
+        const uint32_t l = (uint32_t)(pt / A.N), s0 = (uint32_t)(pt - (uint64_t)l * A.N);
+        const uint32_t q = pick(A.q, l);
+        const uint64_t mu = pick(A.mu, l);
+        const uint32_t *dp = A.dn + i * A.ell * LN + pt;
+        const uint32_t *kp = A.evk + pt;
+        uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
+        for (uint32_t u = 0; u < A.ell; ++u) {
+            const uint4 d = *reinterpret_cast<const uint4 *>(dp + (uint64_t)u * LN);
+            const uint4 k0 = __ldg(reinterpret_cast<const uint4 *>(kp + (uint64_t)(2 * u) * LN));
+            const uint4 k1 = __ldg(reinterpret_cast<const uint4 *>(kp + (uint64_t)(2 * u + 1) * LN));
+            a0 += (uint64_t)d.x * k0.x; a1 += (uint64_t)d.y * k0.y; a2 += (uint64_t)d.z * k0.z; a3 += (uint64_t)d.w * k0.w;
+            b0 += (uint64_t)d.x * k1.x; b1 += (uint64_t)d.y * k1.y; b2 += (uint64_t)d.z * k1.z; b3 += (uint64_t)d.w * k1.w;
+        }
+        const uint64_t ks0[4] = {a0, a1, a2, a3}, ks1[4] = {b0, b1, b2, b3};
+        const uint32_t *c0 = A.in + i * 2 * LN + (uint64_t)l * A.N;
+        const uint32_t *c1 = c0 + LN;
+        const uint32_t *Tinv = A.tw + (size_t)l * 4 * A.N + TW_INV * A.N;
+        const uint4 v0 = *reinterpret_cast<const uint4 *>(c0 + s0);
+        const uint4 v1 = *reinterpret_cast<const uint4 *>(c1 + s0);
+        const uint32_t x0[4] = {v0.x, v0.y, v0.z, v0.w}, x1[4] = {v1.x, v1.y, v1.z, v1.w};
+        uint32_t o0[4], o1[4], p0[4], p1[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t slot = s0 + c;
+            const uint32_t odd = 2 * brv(slot, A.logN) + 1;
+            // sigma_k(c0) at this slot: c0 at the slot of zeta^k
+            const uint32_t ek = (uint32_t)(((uint64_t)A.k * odd) & (twoN - 1));
+            const uint32_t src = brv((ek - 1) >> 1, A.logN);
+            const uint32_t S0 = addq(c0[src], barrett64(ks0[c], q, mu), q);
+            const uint32_t S1 = barrett64(ks1[c], q, mu);
+            // NTT(X^(-2^j)) at this slot: psi^(-E), E = 2^j (2 brv(slot) + 1) mod 2N
+            const uint32_t E = (odd << A.j) & (twoN - 1);
+            const uint32_t m = E < A.N ? Tinv[brv(E, A.logN)] : q - Tinv[brv(E - A.N, A.logN)];
+            o0[c] = addq(x0[c], S0, q);
+            o1[c] = addq(x1[c], S1, q);
+            p0[c] = barrett64((uint64_t)subq(x0[c], S0, q) * m, q, mu);
+            p1[c] = barrett64((uint64_t)subq(x1[c], S1, q) * m, q, mu);
+        }
+        uint32_t *out1 = A.out + i * 2 * LN + pt;
+        uint32_t *out2 = A.out + (i + A.M) * 2 * LN + pt;
+        *reinterpret_cast<uint4 *>(out1) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+        *reinterpret_cast<uint4 *>(out1 + LN) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        *reinterpret_cast<uint4 *>(out2) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+        *reinterpret_cast<uint4 *>(out2 + LN) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+    }
+}
+
+uint64_t align64(uint64_t words) { return (words + 63) / 64 * 64; }
+
+// Workspace (words) for stages of at most Mmax input ciphertexts: c1 in
+// coefficient form, the digits, their NTTs, and the two buffers the stage
+// outputs alternate between (stage j writes 2^(j+1) ciphertexts).
+struct ExLayout {
+    uint64_t coef, dig, dn, ping, pong, total;
+};
+
+ExLayout ex_layout(const pir_ctx *ctx, uint64_t Mmax, uint32_t ell) {
+    const uint64_t LN = (uint64_t)ctx->L * ctx->N;
+    ExLayout x;
+    x.coef = 0;
+    x.dig = x.coef + align64(Mmax * LN);
+    x.dn = x.dig + align64(Mmax * ell * (uint64_t)ctx->N);
+    x.ping = x.dn + align64(Mmax * ell * LN);
+    x.pong = x.ping + align64(Mmax * 2 * LN);
+    x.total = x.pong + align64(Mmax * 2 * LN);
+    return x;
+}
+
+// k^-1 mod 2N for odd k (Newton iteration on 2-adic inverses).
+uint32_t inv_mod_2n(uint32_t k, uint32_t twoN) {
+    uint32_t x = k;                 // correct to 3 bits for odd k
+    for (int it = 0; it < 5; ++it) x *= 2 - k * x;
+    return x & (twoN - 1);
+}
+
+int one_stage(pir_ctx *ctx, const uint32_t *evk, uint32_t ell, uint32_t w, uint32_t j, const uint32_t *in,
+              uint64_t M, uint32_t *out, uint32_t *ws, const ExLayout &lay, cudaStream_t st) {
+    const uint64_t LN = (uint64_t)ctx->L * ctx->N;
+    uint32_t *coef = ws + lay.coef, *dig = ws + lay.dig, *dn = ws + lay.dn;
+    const uint32_t k = (ctx->N >> j) + 1;
+    int rc = PIR_OK;
+
+    if (ctx->N == (uint32_t)kN4) {
+        InttAArgs ia;
+        memset(&ia, 0, sizeof(ia));
+        ia.in = in;
+        ia.coef = coef;
+        ia.tw = ctx->d_tw;
+        ia.L = ctx->L;
+        for (uint32_t l = 0; l < ctx->L; ++l) {
+            ia.q[l] = ctx->q[l];
+            ia.ninv[l] = ctx->ninv[l];
+            ia.ninv_shoup[l] = ctx->ninv_shoup[l];
+        }
+        if (M * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
+        expand_intt_a4096_kernel<<<(unsigned)(M * ctx->L), kT4, 0, st>>>(ia);
+        if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
+    } else {
+        if (cudaMemcpy2DAsync(coef, LN * 4, in + LN, 2 * LN * 4, LN * 4, M, cudaMemcpyDeviceToDevice, st) !=
+            cudaSuccess)
+            return PIR_ERR_CUDA;
+        rc = pir_ntt_inv(ctx, coef, coef, M, st);
+        if (rc) return rc;
+    }
+
+    rc = gadget_dcp_launch(ctx, gadget_dcp_args(ctx, coef, LN, dig, M, ell, w, inv_mod_2n(k, 2 * ctx->N)), st);
+    if (rc) return rc;
+    rc = pir_lift_ntt(ctx, dig, dn, M * ell, st);
+    if (rc) return rc;
+
+    ExpMacArgs ma;
+    memset(&ma, 0, sizeof(ma));
+    ma.in = in;
+    ma.dn = dn;
+    ma.evk = evk;
+    ma.out = out;
+    ma.tw = ctx->d_tw;
+    ma.M = M;
+    ma.N = ctx->N;
+    ma.logN = ctx->logN;
+    ma.L = ctx->L;
+    ma.ell = ell;
+    ma.k = k;
+    ma.j = j;
+    for (uint32_t l = 0; l < ctx->L; ++l) {
+        ma.q[l] = ctx->q[l];
+        ma.mu[l] = ctx->mu[l];
+    }
+    expand_mac_kernel<<<(unsigned)gadget_grid(ctx, M * LN / 4), GD_THREADS, 0, st>>>(ma);
+    return launch_status(cudaGetLastError());
+}
+
+bool overlaps(const void *a, uint64_t abytes, const void *b, uint64_t bbytes) {
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + bbytes && y < x + abytes;
+}
+
+}  // namespace
+
+extern "C" uint64_t pir_expand_workspace_bytes(const pir_ctx *ctx, uint64_t M, uint32_t ell) {
+    if (!ctx || M == 0 || M > (1ull << 31) || ell == 0 || ell > GD_MAX_ELL) return 0;
+    return ex_layout(ctx, M, ell).total * 4;
+}
+
+extern "C" int pir_expand_stage(pir_ctx *ctx, const uint32_t *evk, uint32_t ell, uint32_t w, uint32_t j,
+                                const uint32_t *in, uint64_t M, uint32_t *out, void *workspace,
+                                uint64_t workspace_bytes, void *stream) {
+    if (!ctx || !evk || !in || !out || !workspace || M == 0 || M > (1ull << 31)) return PIR_ERR_ARG;
+    if (!gadget_params_ok(ctx, ell, w) || j >= ctx->logN) return PIR_ERR_ARG;
+    if (!aligned16(evk) || !aligned16(in) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
+    const ExLayout lay = ex_layout(ctx, M, ell);
+    if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
+    const uint64_t ctb = 2ull * ctx->L * ctx->N * 4;
+    if (overlaps(in, M * ctb, out, 2 * M * ctb)) return PIR_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
+    return one_stage(ctx, evk, ell, w, j, in, M, out, static_cast<uint32_t *>(workspace), lay,
+                     (cudaStream_t)stream);
+}
+
+extern "C" int pir_expand(pir_ctx *ctx, const uint32_t *evks, uint32_t ell, uint32_t w, uint32_t stages,
+                          const uint32_t *ct, uint32_t *out, void *workspace, uint64_t workspace_bytes,
+                          void *stream) {
+    if (!ctx || !evks || !ct || !out || !workspace || stages == 0 || stages > ctx->logN) return PIR_ERR_ARG;
+    if (!gadget_params_ok(ctx, ell, w)) return PIR_ERR_ARG;
+    if (!aligned16(evks) || !aligned16(ct) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
+    const uint64_t Mmax = 1ull << (stages - 1);
+    const ExLayout lay = ex_layout(ctx, Mmax, ell);
+    if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
+    const uint64_t ctw = 2ull * ctx->L * ctx->N;
+    if (overlaps(ct, ctw * 4, out, (2 * Mmax) * ctw * 4)) return PIR_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint32_t *ws = static_cast<uint32_t *>(workspace);
+    const uint64_t key = (uint64_t)ell * ctw;       // words of one stage's evaluation key
+    const uint32_t *cur = ct;
+    for (uint32_t j = 0; j < stages; ++j) {
+        const uint64_t M = 1ull << j;
+        uint32_t *dst = j + 1 == stages ? out : ws + ((j & 1) ? lay.pong : lay.ping);
+        const int rc = one_stage(ctx, evks + j * key, ell, w, j, cur, M, dst, ws, lay, st);
+        if (rc) return rc;
+        cur = dst;
+    }
+    return PIR_OK;
+}

@@ -95,6 +95,14 @@ def lib() -> ctypes.CDLL:
             f.restype = ctypes.c_int
             f.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, ctypes.c_uint64, _vp, _vp,
                           ctypes.c_uint64, _vp]
+        L.pir_expand_workspace_bytes.restype = ctypes.c_uint64
+        L.pir_expand_workspace_bytes.argtypes = [_vp, ctypes.c_uint64, ctypes.c_uint32]
+        L.pir_expand_stage.restype = ctypes.c_int
+        L.pir_expand_stage.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, _vp,
+                                       ctypes.c_uint64, _vp, _vp, ctypes.c_uint64, _vp]
+        L.pir_expand.restype = ctypes.c_int
+        L.pir_expand.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, _vp, _vp, _vp,
+                                 ctypes.c_uint64, _vp]
         L.pir_status.restype = ctypes.c_int
         L.pir_status.argtypes = [_vp, _u32p, ctypes.c_int]
         L.pir_strerror.restype = ctypes.c_char_p
@@ -285,6 +293,34 @@ def pir_coltor(ctx: Ctx, C: torch.Tensor, ell: int, w: int, cts: torch.Tensor, n
     _check(lib().pir_coltor(ctx, _dev_ptr(C, 4, "C"), ell, w, _dev_ptr(cts, 4, "in"), n,
                             _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(),
                             _stream(stream)), "pir_coltor")
+
+
+# ---------------------------------------------------------------- ExpandQuery
+def pir_expand_workspace_bytes(ctx: Ctx, M: int, ell: int) -> int:
+    return int(lib().pir_expand_workspace_bytes(ctx, M, ell))
+
+
+def expand_workspace(ctx: Ctx, M: int, ell: int, device="cuda") -> torch.Tensor:
+    """A device workspace for expansion stages of up to M input ciphertexts."""
+    return torch.empty(pir_expand_workspace_bytes(ctx, M, ell), dtype=torch.uint8, device=device)
+
+
+def pir_expand_stage(ctx: Ctx, evk: torch.Tensor, ell: int, w: int, j: int, cts: torch.Tensor, M: int,
+                     out: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """Stage j of ExpandQuery: M ciphertexts -> 2M (NTT form)."""
+    ws = _dev_ptr(workspace, workspace.element_size(), "workspace")
+    _check(lib().pir_expand_stage(ctx, _dev_ptr(evk, 4, "evk"), ell, w, j, _dev_ptr(cts, 4, "in"), M,
+                                  _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(),
+                                  _stream(stream)), "pir_expand_stage")
+
+
+def pir_expand(ctx: Ctx, evks: torch.Tensor, ell: int, w: int, stages: int, ct: torch.Tensor, out: torch.Tensor,
+               workspace: torch.Tensor, stream=None):
+    """ExpandQuery: one ciphertext -> 2^stages ciphertexts (NTT form)."""
+    ws = _dev_ptr(workspace, workspace.element_size(), "workspace")
+    _check(lib().pir_expand(ctx, _dev_ptr(evks, 4, "evks"), ell, w, stages, _dev_ptr(ct, 4, "ct"),
+                            _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(),
+                            _stream(stream)), "pir_expand")
 
 
 # ---------------------------------------------------------------- scalar scan
