@@ -49,6 +49,9 @@ WORKLOADS = {
                            desc="RowSel 24 GiB: N=4096, 3 primes, D0=512 x D1=1024, B=16 queries, NTT-domain"),
     "rowsel_64g_b16": dict(N=4096, L=3, D0=1024, D1=1365, B=16, domain="ntt",
                            desc="RowSel 64 GiB: N=4096, 3 primes, D0=1024 x D1=1365, B=16 queries, NTT-domain"),
+    "onion_64g": dict(kind="onion", N=4096, L=3, D0=1024, D1=1365, ell=5, w=18,
+                      desc="OnionPIR server path per query over the 64 GiB DB: ExpandQuery 1 -> 1024 "
+                           "ciphertexts, RowSel D0=1024 x D1=1365, ColTor 1365 -> 1 (N=4096, 3 primes, l=5)"),
     "expand_1024": dict(kind="expand", N=4096, L=3, stages=10, ell=5, w=18,
                         desc="ExpandQuery of one query ciphertext into the 1024 RowSel inputs of the 64 GiB DB: "
                              "N=4096, 3 primes, 10 stages of Subs, l=5 digits of 18 bits"),
@@ -83,6 +86,7 @@ SPEC_HBM_GBS = 8000.0   # nominal GB300 HBM3e bandwidth (context for the rooflin
 EXPPACK_METRIC = "ring-packing GEMM H*C + (0|G): hint GB/s scanned"
 COLTOR_METRIC = "ColTor column tournaments per second (RGSW-RLWE external products)"
 EXPAND_METRIC = "ExpandQuery expansions per second (Subs: automorphism + key switching)"
+ONION_METRIC = "OnionPIR queries per second (ExpandQuery + RowSel + ColTor), 64 GiB DB"
 
 
 def parse():
@@ -408,6 +412,10 @@ def run_reference(args, cfg):
     elif kind == "expand":
         run_reference_sample(args, ExpandSample(cfg), EXPAND_METRIC, "u32",
                              "synthetic (seeded SplitMix64 residues)", cfg["desc"])
+    elif kind == "onion":
+        print(json.dumps({"impl": "reference", "unavailable": "the composed OnionPIR path has no single oracle "
+                          "sample; its three phases have reference lines of their own (expand_1024, rowsel_64g, "
+                          "coltor_1365)"}), flush=True)
     else:
         run_reference_sample(args, RowselSample(cfg), METRIC, "u32", "synthetic (seeded SplitMix64 residues)",
                              cfg["desc"])
@@ -459,6 +467,8 @@ def launches_per_step(cfg) -> int:
         return 4 * coltor_stages(cfg["n"])
     if cfg.get("kind") == "expand":
         return 4 * cfg["stages"]
+    if cfg.get("kind") == "onion":
+        return 4 * (cfg["D0"].bit_length() - 1) + 3 * rowsel_passes(cfg["D0"], 1) + 4 * coltor_stages(cfg["D1"])
     return 3 * rowsel_passes(cfg["D0"], cfg["B"]) + (2 if cfg["domain"] == "coeff" else 0)
 
 
@@ -713,7 +723,7 @@ def device_db(ctx, D0, D1, seed):
 
 def run_coltor(args, cfg):
     """ColTor: one step = the whole tournament over n RowSel output
-    ciphertexts (NTT form), S = ceil(log2 n) stages of five launches."""
+    ciphertexts (NTT form), S = ceil(log2 n) stages of four launches."""
     import torch
 
     import __graft_entry__
@@ -945,6 +955,134 @@ def run_expand(args, cfg):
     return result
 
 
+def run_onion(args, cfg):
+    """The OnionPIR server path per query: ExpandQuery of the query
+    ciphertext into D0 = 1024, RowSel over the resident 64 GiB DB, ColTor of
+    the D1 = 1365 results into one answer ciphertext (all NTT form)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    import synth.device as sd
+    from lattice_he_database_gb300 import pir
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    N, L, D0, D1, ell, w = cfg["N"], cfg["L"], cfg["D0"], cfg["D1"], cfg["ell"], cfg["w"]
+    S, T = D0.bit_length() - 1, coltor_stages(D1)
+    qs = pir.pir_primes(N, L)
+    ctx = pir.pir_ctx_create(N, qs, local)
+    P = L * N
+    db = device_db(ctx, D0, D1, seed=7)
+    query = torch.empty(2 * P, dtype=torch.int32, device="cuda")
+    sd.fill_residues(query, 11, synth.T_EXTRA, N, qs)
+    evks = torch.empty(S * ell * 2 * P, dtype=torch.int32, device="cuda")
+    sd.fill_residues(evks, 12, synth.T_EXTRA, N, qs)
+    rgsw = torch.empty(T * 2 * ell * 2 * P, dtype=torch.int32, device="cuda")
+    sd.fill_residues(rgsw, 13, synth.T_EXTRA, N, qs)
+    expanded = torch.empty(D0 * 2 * P, dtype=torch.int32, device="cuda")
+    cols = torch.empty(D1 * 2 * P, dtype=torch.int32, device="cuda")
+    answer = torch.empty(2 * P, dtype=torch.int32, device="cuda")
+    ws_e = pir.expand_workspace(ctx, D0 // 2, ell)
+    ws_r = pir.rowsel_workspace(ctx, D0, D1, 1)
+    ws_c = pir.coltor_workspace(ctx, D1, ell)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        pir.pir_expand(ctx, evks, ell, w, S, query, expanded, ws_e, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        pir.pir_rowsel(ctx, db, D0, D1, expanded, 1, cols, ws_r, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        pir.pir_coltor(ctx, rgsw, ell, w, cols, D1, answer, ws_c, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(kev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_total = max_over_ranks(t0.elapsed_time(t1))
+    phase = [float(np.mean([e[k].elapsed_time(e[k + 1]) for e in kev])) for k in range(3)]
+    if pir.pir_status(ctx):
+        raise RuntimeError("device status word set")
+
+    q_host = torch.empty(query.numel(), dtype=torch.int32, pin_memory=True)
+    q_host.copy_(query.cpu())
+    a_host = torch.empty(answer.numel(), dtype=torch.int32, pin_memory=True)
+    ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            query.copy_(q_host, non_blocking=True)
+            step()
+            a_host.copy_(answer, non_blocking=True)
+
+    e2e_ms = None
+    if ke:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / ke
+
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    logical_db = P * D0 * D1 * 4
+    ms_step = ms_total / args.steps
+    db_gbs = logical_db / (phase[1] * 1e-3) / 1e9
+    result = None
+    if rank == 0:
+        line = {
+            "metric": ONION_METRIC, "value": world * args.steps / (ms_total * 1e-3), "unit": "queries/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+            "data": "synthetic: seeded SplitMix64 DB coefficients U[0,2^16), query, key and RGSW residues U[0,q_i)",
+            "config": {"workload": args.workload, "desc": cfg["desc"], "logical_db_bytes": logical_db,
+                       "l2": "inputs larger than L2 (DB %.1f GiB), no flush" % (logical_db / GIB),
+                       "parallelism": "replicas x%d" % world},
+            "phase_ms": {"expand": phase[0], "rowsel": phase[1], "coltor": phase[2]},
+            "db_gbs_in_rowsel": db_gbs,
+            "roofline": {"bound": "hbm", "achieved": db_gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": db_gbs / hbm_peak, "traffic": None, "kernel": "rowsel_kernel (the DB scan)",
+                         "peak_source": "%s hbm_gbs (copy)" % peak_kind,
+                         "algorithmic_bytes_per_launch": logical_db},
+            "clocks": clk,
+            "e2e": None if e2e_ms is None else {
+                "value": 1e3 / e2e_ms, "unit": "queries/s", "h2d_bytes_per_step": 2 * P * 4,
+                "d2h_bytes_per_step": 2 * P * 4, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * launches_per_step(cfg),
+            "cpu_baseline": None,
+        }
+        print(json.dumps(line), flush=True)
+        result = line
+    ctx.close()
+    return result
+
+
 def run_ours(args, cfg):
     import torch
     import torch.distributed as dist
@@ -1149,6 +1287,8 @@ def main():
         run_coltor(args, cfg)
     elif cfg.get("kind") == "expand":
         run_expand(args, cfg)
+    elif cfg.get("kind") == "onion":
+        run_onion(args, cfg)
     else:
         run_ours(args, cfg)
 

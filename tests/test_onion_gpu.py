@@ -1,0 +1,74 @@
+"""The OnionPIR server path end to end on the GPU: ExpandQuery -> RowSel ->
+ColTor (GPIR section 2: the three phases), under a ternary secret with
+noise-free encryptions and keys, so every step is exact mod q.
+
+The client's query encrypts X^(i*); the expansion gives D0 ciphertexts of
+which only i* decrypts to a nonzero constant (2^S); RowSel's point-wise GEMM
+with the encoded DB gives, for every column n, a ciphertext of
+2^S DB[i*][n]; ColTor with RGSW encryptions of the bits of j* keeps column
+j*.  The decryption of the final ciphertext must equal 2^S DB[i*][j*].
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.helpers import ensure_built, to_dev, to_host_u32
+from tests.test_expand_oracle import Keys, _mul, _rand, _signed, _sub
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pir():
+    ensure_built()
+    from lattice_he_database_gb300 import pir as p
+    return p
+
+
+def _rgsw(K, bit):
+    """RGSW(bit) = Z + bit * (I_2 x g): rows of Z encrypt 0 under s (noise-free), NTT form."""
+    L, N, ell = len(K.qs), K.N, K.ell
+    C = np.zeros((2 * ell, 2, L, N), dtype=np.uint32)
+    for r in range(2 * ell):
+        a = _rand(K.rng, K.qs, N)
+        C[r, 0] = _sub(np.zeros_like(a), _mul(a, K.sN, K.qs), K.qs)
+        C[r, 1] = a
+    for u in range(ell):
+        for l, q in enumerate(K.qs):
+            g = bit * pow(2, K.w * u, q) % q
+            C[u, 0, l] = (C[u, 0, l].astype(np.uint64) + g) % q
+            C[ell + u, 1, l] = (C[ell + u, 1, l].astype(np.uint64) + g) % q
+    return C
+
+
+@pytest.mark.parametrize("D0,D1,istar,jstar", [(16, 11, 5, 7), (64, 40, 63, 0), (1024, 24, 700, 17)])
+def test_query_returns_the_selected_record(pir, D0, D1, istar, jstar):
+    N, L, ell, w = 4096, 3, 5, 18
+    K = Keys(N, L, ell, w, seed=D0 + D1)
+    ctx = pir.pir_ctx_create(N, K.qs)
+    S = D0.bit_length() - 1
+    assert 1 << S == D0
+    # the DB: D0 x D1 records of 16-bit coefficients, encoded on the GPU
+    raw = synth.coeffs(D0 % 251, (D0, D1, N))
+    db = pir.empty_u32(pir.pir_db_bytes(ctx, D0, D1) // 4)
+    pir.pir_db_encode(ctx, to_dev(raw), 0, D0, D0, D1, db)
+    # client: Enc(X^i*), evaluation keys, RGSW bits of j*
+    mono = np.zeros(N, dtype=np.int64)
+    mono[istar] = 1
+    query = K.encrypt(_signed(mono, K.qs))
+    evks = np.stack([K.evk(N // (1 << j) + 1) for j in range(S)])
+    T = oracle.coltor_stages(D1)
+    rgsw = np.stack([_rgsw(K, (jstar >> s) & 1) for s in range(T)])
+    # server: ExpandQuery -> RowSel -> ColTor, all on the GPU
+    expanded = pir.empty_u32(D0 * 2 * L * N)
+    pir.pir_expand(ctx, to_dev(evks), ell, w, S, to_dev(query), expanded, pir.expand_workspace(ctx, D0 // 2, ell))
+    cols = pir.empty_u32(D1 * 2 * L * N)
+    pir.pir_rowsel(ctx, db, D0, D1, expanded, 1, cols, pir.rowsel_workspace(ctx, D0, D1, 1))
+    answer = pir.empty_u32(2 * L * N)
+    pir.pir_coltor(ctx, to_dev(rgsw), ell, w, cols, D1, answer, pir.coltor_workspace(ctx, D1, ell))
+    assert pir.pir_status(ctx) == 0
+    # client: decrypt
+    got = K.decrypt(to_host_u32(answer).reshape(2, L, N))
+    want = _signed(raw[istar, jstar].astype(np.int64) << S, K.qs)
+    assert np.array_equal(got, want)
