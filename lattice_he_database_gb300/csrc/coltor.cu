@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(CT_THREADS) coltor_mac_kernel(const MacArgs A)
         const uint32_t *dp = A.dn + i * V * LN + pt;
         const uint32_t *cp = A.C + pt;
         uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
-#pragma unroll 2
+#pragma unroll 4
         for (uint32_t v = 0; v < V; ++v) {
             const uint4 d = *reinterpret_cast<const uint4 *>(dp + (uint64_t)v * LN);
             const uint4 c0 = __ldg(reinterpret_cast<const uint4 *>(cp + (uint64_t)(2 * v) * LN));

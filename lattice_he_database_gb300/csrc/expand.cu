@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
         const uint32_t *dp = A.dn + i * A.ell * LN + pt;
         const uint32_t *kp = A.evk + pt;
         uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
+#pragma unroll 4
         for (uint32_t u = 0; u < A.ell; ++u) {
             const uint4 d = *reinterpret_cast<const uint4 *>(dp + (uint64_t)u * LN);
             const uint4 k0 = __ldg(reinterpret_cast<const uint4 *>(kp + (uint64_t)(2 * u) * LN));

@@ -97,19 +97,25 @@ __global__ void __launch_bounds__(GD_THREADS) gadget_dcp_kernel(const DcpArgs A)
                 }
             }
         }
-        u128 X[4];
+        // digits from a two-word window: after each digit the 128-bit value
+        // moves right by w (1 <= w <= 32, so both shifts stay below 64)
+        uint64_t lo[4], hi[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) X[c] = crt_value(A, r[c], Q);
+        for (int c = 0; c < 4; ++c) {
+            const u128 X = crt_value(A, r[c], Q);
+            lo[c] = (uint64_t)X;
+            hi[c] = (uint64_t)(X >> 64);
+        }
+        const uint32_t m32 = (uint32_t)mask, w = A.w, wr = 64 - A.w;
         uint32_t *dp = A.d + pi * A.ell * A.N + p;
         for (uint32_t u = 0; u < A.ell; ++u) {
-            uint4 d;
-            d.x = (uint32_t)(X[0] & mask);
-            d.y = (uint32_t)(X[1] & mask);
-            d.z = (uint32_t)(X[2] & mask);
-            d.w = (uint32_t)(X[3] & mask);
-            *reinterpret_cast<uint4 *>(dp + (uint64_t)u * A.N) = d;
+            *reinterpret_cast<uint4 *>(dp + (uint64_t)u * A.N) =
+                make_uint4((uint32_t)lo[0] & m32, (uint32_t)lo[1] & m32, (uint32_t)lo[2] & m32, (uint32_t)lo[3] & m32);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) X[k] >>= A.w;
+            for (int c = 0; c < 4; ++c) {
+                lo[c] = (lo[c] >> w) | (hi[c] << wr);
+                hi[c] >>= w;
+            }
         }
     }
 }
@@ -166,7 +172,7 @@ DcpArgs gadget_dcp_args(const pir_ctx *ctx, const uint32_t *x, uint64_t x_stride
 
 uint64_t gadget_grid(const pir_ctx *ctx, uint64_t work) {
     const uint64_t g = (work + GD_THREADS - 1) / GD_THREADS;
-    const uint64_t cap = (uint64_t)ctx->num_sms * 16;
+    const uint64_t cap = (uint64_t)ctx->num_sms * 64;
     return g < 1 ? 1 : (g < cap ? g : cap);
 }
 
