@@ -721,6 +721,32 @@ def device_db(ctx, D0, D1, seed):
     return db
 
 
+def graph_of(step, stream):
+    """A CUDA graph of one step (the library's launches on `stream`), for
+    fixed-shape pipelines whose small stages are bound by launch latency."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    return g
+
+
+def timed_ms(fn, steps, stream):
+    """Mean ms of `steps` calls of fn on `stream` (CUDA events)."""
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def run_coltor(args, cfg):
     """ColTor: one step = the whole tournament over n RowSel output
     ciphertexts (NTT form), S = ceil(log2 n) stages of four launches."""
@@ -754,6 +780,12 @@ def run_coltor(args, cfg):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    eager_ms = timed_ms(step, args.steps, stream)      # one launch sequence per call, for comparison
+    graph = graph_of(step, stream)
+
+    def run():
+        with torch.cuda.stream(stream):      # replay on the stream the events are recorded on
+            graph.replay()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -762,7 +794,7 @@ def run_coltor(args, cfg):
     torch.cuda.synchronize()
     t0.record(stream)
     for _ in range(args.steps):
-        step()
+        run()
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -780,7 +812,7 @@ def run_coltor(args, cfg):
     def e2e_step():
         with torch.cuda.stream(stream):
             cts.copy_(cts_host, non_blocking=True)
-            step()
+            run()
             o_host.copy_(out, non_blocking=True)
 
     e2e_ms = None
@@ -820,6 +852,9 @@ def run_coltor(args, cfg):
                              % (((n + 1) // 2) * 2 * ell * P * 4 / 1e6),
                        "parallelism": "replicas x%d" % world},
             "external_products_per_s": world * args.steps * (n - 1) / (ms_total * 1e-3),
+            "launch": "one CUDA graph per tournament (the call's %d launches captured once, replayed)"
+                      % launches_per_step(cfg),
+            "eager_ms_per_step": eager_ms,
             "ntt_per_step": nntt, "ntt_per_s": nntt / (ms_step * 1e-3),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": profile_traffic("coltor_%s" % args.workload),
@@ -872,6 +907,12 @@ def run_expand(args, cfg):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    eager_ms = timed_ms(step, args.steps, stream)      # one launch sequence per call, for comparison
+    graph = graph_of(step, stream)
+
+    def run():
+        with torch.cuda.stream(stream):      # replay on the stream the events are recorded on
+            graph.replay()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -880,7 +921,7 @@ def run_expand(args, cfg):
     torch.cuda.synchronize()
     t0.record(stream)
     for _ in range(args.steps):
-        step()
+        run()
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -898,7 +939,7 @@ def run_expand(args, cfg):
     def e2e_step():
         with torch.cuda.stream(stream):
             ct.copy_(ct_host, non_blocking=True)
-            step()
+            run()
             o_host.copy_(out, non_blocking=True)
 
     e2e_ms = None
@@ -935,6 +976,9 @@ def run_expand(args, cfg):
                        "l2": "outputs %.0f MB exceed L2; no flush" % (o_bytes / 1e6),
                        "parallelism": "replicas x%d" % world},
             "subs_per_s": world * args.steps * nsubs / (ms_total * 1e-3),
+            "launch": "one CUDA graph per expansion (the call's %d launches captured once, replayed)"
+                      % launches_per_step(cfg),
+            "eager_ms_per_step": eager_ms,
             "ntt_per_step": nntt, "ntt_per_s": nntt / (ms_step * 1e-3),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": profile_traffic("expand_%s" % args.workload),
@@ -990,18 +1034,31 @@ def run_onion(args, cfg):
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def expand():
         pir.pir_expand(ctx, evks, ell, w, S, query, expanded, ws_e, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        pir.pir_rowsel(ctx, db, D0, D1, expanded, 1, cols, ws_r, stream)
-        if ev is not None:
-            ev[2].record(stream)
+
+    def coltor():
         pir.pir_coltor(ctx, rgsw, ell, w, cols, D1, answer, ws_c, stream)
-        if ev is not None:
-            ev[3].record(stream)
+
+    for _ in range(2):                        # first calls (kernel attributes, caches) outside the graphs
+        expand()
+        pir.pir_rowsel(ctx, db, D0, D1, expanded, 1, cols, ws_r, stream)
+        coltor()
+    g_expand, g_coltor = graph_of(expand, stream), graph_of(coltor, stream)
+
+    def step(ev=None):
+        with torch.cuda.stream(stream):
+            if ev is not None:
+                ev[0].record(stream)
+            g_expand.replay()                 # the small expansion stages are bound by launch latency
+            if ev is not None:
+                ev[1].record(stream)
+            pir.pir_rowsel(ctx, db, D0, D1, expanded, 1, cols, ws_r, stream)
+            if ev is not None:
+                ev[2].record(stream)
+            g_coltor.replay()
+            if ev is not None:
+                ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -1065,6 +1122,7 @@ def run_onion(args, cfg):
                        "l2": "inputs larger than L2 (DB %.1f GiB), no flush" % (logical_db / GIB),
                        "parallelism": "replicas x%d" % world},
             "phase_ms": {"expand": phase[0], "rowsel": phase[1], "coltor": phase[2]},
+            "launch": "ExpandQuery and ColTor each replayed as one CUDA graph; RowSel launched directly",
             "db_gbs_in_rowsel": db_gbs,
             "roofline": {"bound": "hbm", "achieved": db_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": db_gbs / hbm_peak, "traffic": None, "kernel": "rowsel_kernel (the DB scan)",

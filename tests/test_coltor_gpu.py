@@ -122,3 +122,44 @@ def test_coltor_rejects_bad_arguments(pir):
     with pytest.raises(pir.PirError):                 # n = 0
         pir.pir_coltor(ctx, C, 5, 18, cts, 0, out, ws)
     assert pir.pir_coltor_workspace_bytes(ctx, 0, 5) == 0
+
+
+def test_graph_replay_matches_eager(pir):
+    """A pir_coltor / pir_expand call captured into a CUDA graph and replayed
+    gives the eager call's results (the bench replays such graphs)."""
+    import torch
+    N, L, ell, w = 4096, 3, 5, 18
+    ctx, qs, _ = _setup(pir, N, L)
+    stream = torch.cuda.Stream()
+    n = 300
+    S = oracle.coltor_stages(n)
+    Cs = to_dev(synth.residues(61, (S, 2 * ell, 2, L, N), qs))
+    cts = to_dev(synth.residues(62, (n, 2, L, N), qs))
+    ws = pir.coltor_workspace(ctx, n, ell)
+    eager, replay = pir.empty_u32(2 * L * N), pir.empty_u32(2 * L * N)
+    pir.pir_coltor(ctx, Cs, ell, w, cts, n, eager, ws, stream)
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        pir.pir_coltor(ctx, Cs, ell, w, cts, n, replay, ws, stream)
+    replay.fill_(-1)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(replay, eager)
+    Sx = 7
+    evks = to_dev(synth.residues(63, (Sx, ell, 2, L, N), qs))
+    ct = to_dev(synth.residues(64, (2, L, N), qs))
+    wsx = pir.expand_workspace(ctx, 1 << (Sx - 1), ell)
+    e_out, r_out = pir.empty_u32((1 << Sx) * 2 * L * N), pir.empty_u32((1 << Sx) * 2 * L * N)
+    pir.pir_expand(ctx, evks, ell, w, Sx, ct, e_out, wsx, stream)
+    g2 = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g2, stream=stream):
+        pir.pir_expand(ctx, evks, ell, w, Sx, ct, r_out, wsx, stream)
+    r_out.fill_(-1)
+    with torch.cuda.stream(stream):
+        g2.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(r_out, e_out)
+    assert pir.pir_status(ctx) == 0
