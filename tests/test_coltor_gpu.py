@@ -53,6 +53,8 @@ def _trivial_rgsw(bit, qs, N, ell, w):
     (4096, 2, 4, 15, 400),
     (4096, 1, 1, 29, 400),
     (4096, 3, 16, 6, 320),    # sixteen digits
+    (4096, 4, 6, 20, 5),      # four primes: Q ~ 2^116, Q/q_l above 2^64
+    (256, 4, 4, 29, 9),
 ])
 def test_stage_matches_oracle(pir, N, L, ell, w, n):
     ctx, qs, psis = _setup(pir, N, L)

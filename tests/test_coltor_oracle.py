@@ -61,7 +61,7 @@ def _random_cts(rng, n, qs, N):
     return cts
 
 
-@pytest.mark.parametrize("L,ell,w", [(3, 5, 18), (2, 4, 15), (1, 1, 29), (3, 3, 29)])
+@pytest.mark.parametrize("L,ell,w", [(3, 5, 18), (2, 4, 15), (1, 1, 29), (3, 3, 29), (4, 6, 20), (4, 4, 29)])
 def test_dcp_rebuilds_every_residue(L, ell, w):
     N = 4096
     qs, _ = _setup(N, L)
@@ -85,7 +85,7 @@ def test_dcp_rebuilds_every_residue(L, ell, w):
     assert top == Q - 1
 
 
-@pytest.mark.parametrize("N,L,ell,w", [(64, 3, 5, 18), (4096, 3, 5, 18), (256, 2, 4, 15)])
+@pytest.mark.parametrize("N,L,ell,w", [(64, 3, 5, 18), (4096, 3, 5, 18), (256, 2, 4, 15), (64, 4, 6, 20)])
 def test_ext_product_with_rgsw_of_one_is_identity(N, L, ell, w):
     qs, psis = _setup(N, L)
     rng = np.random.default_rng(N + L)

@@ -39,6 +39,7 @@ def _setup(pir, N, L):
     (256, 2, 4, 15, 2, 5),
     (64, 3, 5, 18, 5, 4),
     (16, 1, 1, 29, 1, 3),
+    (4096, 4, 6, 20, 2, 3),     # four primes: Q ~ 2^116
 ])
 def test_stage_matches_oracle(pir, N, L, ell, w, j, M):
     ctx, qs, psis = _setup(pir, N, L)

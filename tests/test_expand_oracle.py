@@ -133,7 +133,7 @@ def test_automorphism_permutes_ntt_slots(k):
 
 
 @pytest.mark.parametrize("N,L,ell,w,k", [(64, 3, 5, 18, 65), (64, 3, 5, 18, 33), (64, 3, 5, 18, 3),
-                                         (256, 2, 4, 15, 129), (4096, 3, 5, 18, 4097)])
+                                         (256, 2, 4, 15, 129), (4096, 3, 5, 18, 4097), (64, 4, 6, 20, 17)])
 def test_subs_decrypts_to_the_automorphism(N, L, ell, w, k):
     K = Keys(N, L, ell, w, seed=N + k)
     m = _signed(K.rng.integers(-1000, 1000, size=N), K.qs)
