@@ -128,6 +128,72 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
     }
 }
 
+// Forward (and lift + forward) for N = 4096 on two rows of the same prime
+// per CTA, rows 2pp*L + l and (2pp+1)*L + l: every twiddle load serves both
+// rows and each thread carries two independent butterfly chains.  Rounds as
+// in ntt4096_kernel.
+template <bool LIFT>
+__global__ void __launch_bounds__(kT4) ntt4096x2_fwd_kernel(const uint32_t *__restrict__ in, uint32_t *out,
+                                                            uint64_t cnt, const __grid_constant__ RnsParams P) {
+    __shared__ __align__(16) uint32_t sa[kN4];
+    __shared__ __align__(16) uint32_t sb[kN4];
+    const uint64_t pp = blockIdx.x / P.L;
+    const uint32_t l = blockIdx.x % P.L;
+    const uint64_t p0 = 2 * pp, p1 = p0 + 1;
+    const bool two = p1 < cnt;
+    const uint32_t q = P.q[l];
+    const uint32_t *W = P.tw + (size_t)l * 4 * kN4 + TW_FWD * kN4;
+    const uint32_t *Wp = P.tw + (size_t)l * 4 * kN4 + TW_FWD_SHOUP * kN4;
+    const uint32_t *src0 = in + (LIFT ? p0 : p0 * P.L + l) * kN4;
+    const uint32_t *src1 = in + (LIFT ? p1 : p1 * P.L + l) * kN4;
+    uint32_t *dst0 = out + (p0 * P.L + l) * kN4, *dst1 = out + (p1 * P.L + l) * kN4;
+    const uint32_t t = threadIdx.x;
+    uint32_t x[16], y[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t a = src0[t + 256 * i];
+        const uint32_t b = two ? src1[t + 256 * i] : 0u;
+        x[i] = LIFT ? a % q : a;
+        y[i] = LIFT ? b % q : b;
+    }
+    fwd_round16x2(x, y, 0, 0, W, Wp, q);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        sa[t + 256 * i] = x[i];
+        sb[t + 256 * i] = y[i];
+    }
+    __syncthreads();
+    const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        x[i] = sa[g1 + 16 * i];
+        y[i] = sb[g1 + 16 * i];
+    }
+    fwd_round16x2(x, y, 4, t >> 4, W, Wp, q);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        sa[g1 + 16 * i] = x[i];
+        sb[g1 + 16 * i] = y[i];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(sa + 16 * t + i);
+        const uint4 v = *reinterpret_cast<const uint4 *>(sb + 16 * t + i);
+        x[i] = u.x; x[i + 1] = u.y; x[i + 2] = u.z; x[i + 3] = u.w;
+        y[i] = v.x; y[i + 1] = v.y; y[i + 2] = v.z; y[i + 3] = v.w;
+    }
+    fwd_round16x2(x, y, 8, t, W, Wp, q);
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+        *reinterpret_cast<uint4 *>(dst0 + 16 * t + i) =
+            make_uint4(fwd_final(x[i], q), fwd_final(x[i + 1], q), fwd_final(x[i + 2], q), fwd_final(x[i + 3], q));
+        if (two)
+            *reinterpret_cast<uint4 *>(dst1 + 16 * t + i) = make_uint4(fwd_final(y[i], q), fwd_final(y[i + 1], q),
+                                                                        fwd_final(y[i + 2], q), fwd_final(y[i + 3], q));
+    }
+}
+
 template <bool FWD, bool LIFT = false>
 int ntt_launch(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream) {
     if (!ctx) return PIR_ERR_ARG;
@@ -148,7 +214,13 @@ int ntt_launch(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, vo
     if (ctx->N == (uint32_t)kN4) {
         if (!LIFT && in != out && (uint64_t)((in < out ? out - in : in - out)) < rows * kN4)
             return PIR_ERR_ARG;  // partial overlap
-        ntt4096_kernel<FWD, LIFT><<<(unsigned)rows, kT4, 0, (cudaStream_t)stream>>>(in, out, rns_params(ctx));
+        if (FWD && cnt > 1) {   // two rows of one prime per CTA
+            const uint64_t g2 = (cnt + 1) / 2 * ctx->L;
+            if (g2 > 0x7fffffffull) return PIR_ERR_ARG;
+            ntt4096x2_fwd_kernel<LIFT><<<(unsigned)g2, kT4, 0, (cudaStream_t)stream>>>(in, out, cnt, rns_params(ctx));
+        } else {
+            ntt4096_kernel<FWD, LIFT><<<(unsigned)rows, kT4, 0, (cudaStream_t)stream>>>(in, out, rns_params(ctx));
+        }
         return launch_status(cudaGetLastError());
     }
     ntt_kernel<FWD, LIFT><<<(unsigned)grid, kNttThreads, smem, (cudaStream_t)stream>>>(in, out, rows, rpc,

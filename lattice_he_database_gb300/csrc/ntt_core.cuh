@@ -179,6 +179,33 @@ __device__ __forceinline__ void fwd_round16(uint32_t (&x)[16], uint32_t s0, uint
     }
 }
 
+// fwd_round16 on two rows of the same prime at once: each twiddle is loaded
+// once for both, and the two rows' butterflies are independent work.
+__device__ __forceinline__ void fwd_round16x2(uint32_t (&x)[16], uint32_t (&y)[16], uint32_t s0, uint32_t high,
+                                              const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
+                                              uint32_t q) {
+    const uint32_t q2 = 2 * q;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int d = 16 >> (r + 1);
+        const uint32_t m = 1u << (s0 + r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (i & d) continue;
+            const uint32_t idx = m + ((high << r) | (uint32_t)(i >> (4 - r)));
+            const uint32_t w = __ldg(W + idx), wp = __ldg(Wp + idx);
+            const uint32_t a = umin32(x[i], x[i] - q2);
+            const uint32_t t = shoup_mul(x[i + d], w, wp, q);
+            x[i] = a + t;
+            x[i + d] = a - t + q2;
+            const uint32_t b = umin32(y[i], y[i] - q2);
+            const uint32_t u = shoup_mul(y[i + d], w, wp, q);
+            y[i] = b + u;
+            y[i + d] = b - u + q2;
+        }
+    }
+}
+
 // One inverse round of 4 stages s_hi..s_hi-3 on x[16] = elements g + tlow*i.
 __device__ __forceinline__ void inv_round16(uint32_t (&x)[16], uint32_t s_hi, uint32_t high,
                                             const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
