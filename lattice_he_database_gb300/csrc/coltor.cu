@@ -74,49 +74,35 @@ struct DiffInttArgs {
     uint32_t q[PIR_MAX_RNS], ninv[PIR_MAX_RNS], ninv_shoup[PIR_MAX_RNS];
 };
 
-// N = 4096: one CTA per difference row (pair i, polynomial c, prime l); the
-// first inverse round loads ct_2i+1 - ct_2i + q (in (0, 2q), the inverse
-// butterflies' input range) instead of a stored difference.  Rounds as in
-// the library's 4096-point inverse kernel.
+// N = 4096: one CTA per (pair i, prime l) transforms both difference rows
+// (polynomials c = 0, 1) with shared twiddles; the first inverse round loads
+// ct_2i+1 - ct_2i + q (in (0, 2q), the inverse butterflies' input range)
+// instead of a stored difference.  Rounds as in the library's inverse.
 __global__ void __launch_bounds__(kT4) coltor_diff_intt4096_kernel(const __grid_constant__ DiffInttArgs A) {
-    __shared__ __align__(16) uint32_t sm[kN4];
-    const uint64_t row = blockIdx.x;
-    const uint32_t twoL = 2 * A.L;
-    const uint64_t i = row / twoL;
-    const uint32_t rem = (uint32_t)(row % twoL), l = rem % A.L;
+    __shared__ __align__(16) uint32_t sa[kN4];
+    __shared__ __align__(16) uint32_t sb[kN4];
+    const uint64_t i = blockIdx.x / A.L;
+    const uint32_t l = blockIdx.x % A.L;
+    const uint64_t LN = (uint64_t)A.L * kN4;
     const uint32_t q = A.q[l];
     const uint32_t *W = A.tw + (size_t)l * 4 * kN4 + TW_INV * kN4;
     const uint32_t *Wp = A.tw + (size_t)l * 4 * kN4 + TW_INV_SHOUP * kN4;
-    const uint32_t *ev = A.in + (2 * i * twoL + rem) * kN4;
-    const uint32_t *od = A.in + ((2 * i + 1) * twoL + rem) * kN4;
+    const uint32_t *ev = A.in + 2 * i * 2 * LN + (uint64_t)l * kN4;          // polynomial 0 of ct_2i
+    const uint32_t *od = A.in + (2 * i + 1) * 2 * LN + (uint64_t)l * kN4;    // polynomial 0 of ct_2i+1
     const bool has_odd = 2 * i + 1 < A.n;
     const uint32_t t = threadIdx.x;
-    uint32_t x[16];
+    uint32_t x[16], y[16];
 #pragma unroll
     for (int k = 0; k < 16; k += 4) {
-        const uint4 e = *reinterpret_cast<const uint4 *>(ev + 16 * t + k);
-        const uint4 o = has_odd ? *reinterpret_cast<const uint4 *>(od + 16 * t + k) : make_uint4(0, 0, 0, 0);
-        x[k] = o.x + q - e.x; x[k + 1] = o.y + q - e.y; x[k + 2] = o.z + q - e.z; x[k + 3] = o.w + q - e.w;
+        const uint4 e0 = *reinterpret_cast<const uint4 *>(ev + 16 * t + k);
+        const uint4 e1 = *reinterpret_cast<const uint4 *>(ev + LN + 16 * t + k);
+        const uint4 o0 = has_odd ? *reinterpret_cast<const uint4 *>(od + 16 * t + k) : make_uint4(0, 0, 0, 0);
+        const uint4 o1 = has_odd ? *reinterpret_cast<const uint4 *>(od + LN + 16 * t + k) : make_uint4(0, 0, 0, 0);
+        x[k] = o0.x + q - e0.x; x[k + 1] = o0.y + q - e0.y; x[k + 2] = o0.z + q - e0.z; x[k + 3] = o0.w + q - e0.w;
+        y[k] = o1.x + q - e1.x; y[k + 1] = o1.y + q - e1.y; y[k + 2] = o1.z + q - e1.z; y[k + 3] = o1.w + q - e1.w;
     }
-    inv_round16(x, 11, t, W, Wp, q);
-#pragma unroll
-    for (int k = 0; k < 16; k += 4)
-        *reinterpret_cast<uint4 *>(sm + 16 * t + k) = make_uint4(x[k], x[k + 1], x[k + 2], x[k + 3]);
-    __syncthreads();
-    const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) x[k] = sm[g1 + 16 * k];
-    inv_round16(x, 7, t >> 4, W, Wp, q);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) sm[g1 + 16 * k] = x[k];
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 16; ++k) x[k] = sm[t + 256 * k];
-    inv_round16(x, 3, 0, W, Wp, q);
-    uint32_t *dst = A.diff + row * kN4;
-    const uint32_t ni = A.ninv[l], nis = A.ninv_shoup[l];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) dst[t + 256 * k] = inv_final(x[k], ni, nis, q);
+    uint32_t *dst = A.diff + i * 2 * LN + (uint64_t)l * kN4;
+    inv4096x2_rounds(x, y, sa, sb, W, Wp, q, A.ninv[l], A.ninv_shoup[l], dst, dst + LN, true);
 }
 
 struct MacArgs {
@@ -226,8 +212,8 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint3
             ia.ninv[l] = ctx->ninv[l];
             ia.ninv_shoup[l] = ctx->ninv_shoup[l];
         }
-        if (R * 2 * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
-        coltor_diff_intt4096_kernel<<<(unsigned)(R * 2 * ctx->L), kT4, 0, st>>>(ia);
+        if (R * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
+        coltor_diff_intt4096_kernel<<<(unsigned)(R * ctx->L), kT4, 0, st>>>(ia);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
     } else {
         coltor_diff_kernel<<<(unsigned)grid_for(ctx, R * 2 * LN / 4), CT_THREADS, 0, st>>>(da);

@@ -37,47 +37,35 @@ struct InttAArgs {
     const uint32_t *in;     // [M][2][L][N]
     uint32_t *coef;         // [M][L][N]
     const uint32_t *tw;
+    uint64_t M;
     uint32_t L;
     uint32_t q[PIR_MAX_RNS], ninv[PIR_MAX_RNS], ninv_shoup[PIR_MAX_RNS];
 };
 
-// N = 4096: one CTA per (ciphertext i, prime l) row of c1; rounds as in the
-// library's 4096-point inverse kernel.
+// N = 4096: one CTA per (ciphertexts 2i' and 2i'+1, prime l) transforms
+// both c1 rows with shared twiddles; rounds as in the library's inverse.
 __global__ void __launch_bounds__(kT4) expand_intt_a4096_kernel(const __grid_constant__ InttAArgs A) {
-    __shared__ __align__(16) uint32_t sm[kN4];
-    const uint64_t row = blockIdx.x;
-    const uint64_t i = row / A.L;
-    const uint32_t l = (uint32_t)(row % A.L);
+    __shared__ __align__(16) uint32_t sa[kN4];
+    __shared__ __align__(16) uint32_t sb[kN4];
+    const uint64_t i0 = 2 * (blockIdx.x / A.L), i1 = i0 + 1;
+    const uint32_t l = blockIdx.x % A.L;
+    const bool two = i1 < A.M;
     const uint32_t q = A.q[l];
     const uint32_t *W = A.tw + (size_t)l * 4 * kN4 + TW_INV * kN4;
     const uint32_t *Wp = A.tw + (size_t)l * 4 * kN4 + TW_INV_SHOUP * kN4;
-    const uint32_t *src = A.in + ((2 * i + 1) * A.L + l) * kN4;
+    const uint32_t *s0 = A.in + ((2 * i0 + 1) * A.L + l) * kN4;
+    const uint32_t *s1 = A.in + ((2 * i1 + 1) * A.L + l) * kN4;
     const uint32_t t = threadIdx.x;
-    uint32_t x[16];
+    uint32_t x[16], y[16];
 #pragma unroll
     for (int k = 0; k < 16; k += 4) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * t + k);
-        x[k] = v.x; x[k + 1] = v.y; x[k + 2] = v.z; x[k + 3] = v.w;
+        const uint4 u = *reinterpret_cast<const uint4 *>(s0 + 16 * t + k);
+        const uint4 v = two ? *reinterpret_cast<const uint4 *>(s1 + 16 * t + k) : make_uint4(0, 0, 0, 0);
+        x[k] = u.x; x[k + 1] = u.y; x[k + 2] = u.z; x[k + 3] = u.w;
+        y[k] = v.x; y[k + 1] = v.y; y[k + 2] = v.z; y[k + 3] = v.w;
     }
-    inv_round16(x, 11, t, W, Wp, q);
-#pragma unroll
-    for (int k = 0; k < 16; k += 4)
-        *reinterpret_cast<uint4 *>(sm + 16 * t + k) = make_uint4(x[k], x[k + 1], x[k + 2], x[k + 3]);
-    __syncthreads();
-    const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) x[k] = sm[g1 + 16 * k];
-    inv_round16(x, 7, t >> 4, W, Wp, q);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) sm[g1 + 16 * k] = x[k];
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 16; ++k) x[k] = sm[t + 256 * k];
-    inv_round16(x, 3, 0, W, Wp, q);
-    uint32_t *dst = A.coef + row * kN4;
-    const uint32_t ni = A.ninv[l], nis = A.ninv_shoup[l];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) dst[t + 256 * k] = inv_final(x[k], ni, nis, q);
+    inv4096x2_rounds(x, y, sa, sb, W, Wp, q, A.ninv[l], A.ninv_shoup[l], A.coef + (i0 * A.L + l) * kN4,
+                     A.coef + (i1 * A.L + l) * kN4, two);
 }
 
 struct ExpMacArgs {
@@ -209,8 +197,9 @@ int one_stage(pir_ctx *ctx, const uint32_t *evk, uint32_t ell, uint32_t w, uint3
             ia.ninv[l] = ctx->ninv[l];
             ia.ninv_shoup[l] = ctx->ninv_shoup[l];
         }
-        if (M * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
-        expand_intt_a4096_kernel<<<(unsigned)(M * ctx->L), kT4, 0, st>>>(ia);
+        if ((M + 1) / 2 * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
+        ia.M = M;
+        expand_intt_a4096_kernel<<<(unsigned)((M + 1) / 2 * ctx->L), kT4, 0, st>>>(ia);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
     } else {
         if (cudaMemcpy2DAsync(coef, LN * 4, in + LN, 2 * LN * 4, LN * 4, M, cudaMemcpyDeviceToDevice, st) !=

@@ -194,6 +194,30 @@ __global__ void __launch_bounds__(kT4) ntt4096x2_fwd_kernel(const uint32_t *__re
     }
 }
 
+// Inverse for N = 4096 on two rows of one prime per CTA (as the forward).
+__global__ void __launch_bounds__(kT4) ntt4096x2_inv_kernel(const uint32_t *__restrict__ in, uint32_t *out,
+                                                            uint64_t cnt, const __grid_constant__ RnsParams P) {
+    __shared__ __align__(16) uint32_t sa[kN4];
+    __shared__ __align__(16) uint32_t sb[kN4];
+    const uint64_t pp = blockIdx.x / P.L;
+    const uint32_t l = blockIdx.x % P.L;
+    const uint64_t r0 = (2 * pp) * P.L + l, r1 = (2 * pp + 1) * P.L + l;
+    const bool two = 2 * pp + 1 < cnt;
+    const uint32_t q = P.q[l];
+    const uint32_t *W = P.tw + (size_t)l * 4 * kN4 + TW_INV * kN4;
+    const uint32_t *Wp = P.tw + (size_t)l * 4 * kN4 + TW_INV_SHOUP * kN4;
+    const uint32_t t = threadIdx.x;
+    uint32_t x[16], y[16];
+#pragma unroll
+    for (int k = 0; k < 16; k += 4) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(in + r0 * kN4 + 16 * t + k);
+        const uint4 v = two ? *reinterpret_cast<const uint4 *>(in + r1 * kN4 + 16 * t + k) : make_uint4(0, 0, 0, 0);
+        x[k] = u.x; x[k + 1] = u.y; x[k + 2] = u.z; x[k + 3] = u.w;
+        y[k] = v.x; y[k + 1] = v.y; y[k + 2] = v.z; y[k + 3] = v.w;
+    }
+    inv4096x2_rounds(x, y, sa, sb, W, Wp, q, P.ninv[l], P.ninv_shoup[l], out + r0 * kN4, out + r1 * kN4, two);
+}
+
 template <bool FWD, bool LIFT = false>
 int ntt_launch(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream) {
     if (!ctx) return PIR_ERR_ARG;
@@ -214,10 +238,14 @@ int ntt_launch(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, vo
     if (ctx->N == (uint32_t)kN4) {
         if (!LIFT && in != out && (uint64_t)((in < out ? out - in : in - out)) < rows * kN4)
             return PIR_ERR_ARG;  // partial overlap
-        if (FWD && cnt > 1) {   // two rows of one prime per CTA
+        if (cnt > 1) {          // two rows of one prime per CTA
             const uint64_t g2 = (cnt + 1) / 2 * ctx->L;
             if (g2 > 0x7fffffffull) return PIR_ERR_ARG;
-            ntt4096x2_fwd_kernel<LIFT><<<(unsigned)g2, kT4, 0, (cudaStream_t)stream>>>(in, out, cnt, rns_params(ctx));
+            if (FWD)
+                ntt4096x2_fwd_kernel<LIFT><<<(unsigned)g2, kT4, 0, (cudaStream_t)stream>>>(in, out, cnt,
+                                                                                         rns_params(ctx));
+            else
+                ntt4096x2_inv_kernel<<<(unsigned)g2, kT4, 0, (cudaStream_t)stream>>>(in, out, cnt, rns_params(ctx));
         } else {
             ntt4096_kernel<FWD, LIFT><<<(unsigned)rows, kT4, 0, (cudaStream_t)stream>>>(in, out, rns_params(ctx));
         }

@@ -227,3 +227,71 @@ __device__ __forceinline__ void inv_round16(uint32_t (&x)[16], uint32_t s_hi, ui
         }
     }
 }
+
+// inv_round16 on two rows of the same prime (shared twiddle loads).
+__device__ __forceinline__ void inv_round16x2(uint32_t (&x)[16], uint32_t (&y)[16], uint32_t s_hi, uint32_t high,
+                                              const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
+                                              uint32_t q) {
+    const uint32_t q2 = 2 * q;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int d = 1 << r;
+        const uint32_t m = 1u << (s_hi - r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (i & d) continue;
+            const uint32_t idx = m + ((high << (3 - r)) | (uint32_t)(i >> (r + 1)));
+            const uint32_t w = __ldg(W + idx), wp = __ldg(Wp + idx);
+            const uint32_t u = x[i] + x[i + d];
+            const uint32_t v = x[i] - x[i + d] + q2;
+            x[i] = umin32(u, u - q2);
+            x[i + d] = shoup_mul(v, w, wp, q);
+            const uint32_t a = y[i] + y[i + d];
+            const uint32_t b = y[i] - y[i + d] + q2;
+            y[i] = umin32(a, a - q2);
+            y[i + d] = shoup_mul(b, w, wp, q);
+        }
+    }
+}
+
+// The three inverse rounds of a 4096-point transform on two rows of one
+// prime whose first-round inputs (16 consecutive values per thread, in
+// [0, 2q)) are already in x and y; the results (natural order, times N^-1,
+// canonical) go to dst0 and dst1 (dst1 skipped when !two).
+__device__ __forceinline__ void inv4096x2_rounds(uint32_t (&x)[16], uint32_t (&y)[16], uint32_t *sa, uint32_t *sb,
+                                                 const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
+                                                 uint32_t q, uint32_t ni, uint32_t nis, uint32_t *dst0, uint32_t *dst1,
+                                                 bool two) {
+    const uint32_t t = threadIdx.x;
+    inv_round16x2(x, y, 11, t, W, Wp, q);
+#pragma unroll
+    for (int k = 0; k < 16; k += 4) {
+        *reinterpret_cast<uint4 *>(sa + 16 * t + k) = make_uint4(x[k], x[k + 1], x[k + 2], x[k + 3]);
+        *reinterpret_cast<uint4 *>(sb + 16 * t + k) = make_uint4(y[k], y[k + 1], y[k + 2], y[k + 3]);
+    }
+    __syncthreads();
+    const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        x[k] = sa[g1 + 16 * k];
+        y[k] = sb[g1 + 16 * k];
+    }
+    inv_round16x2(x, y, 7, t >> 4, W, Wp, q);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        sa[g1 + 16 * k] = x[k];
+        sb[g1 + 16 * k] = y[k];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        x[k] = sa[t + 256 * k];
+        y[k] = sb[t + 256 * k];
+    }
+    inv_round16x2(x, y, 3, 0, W, Wp, q);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        dst0[t + 256 * k] = inv_final(x[k], ni, nis, q);
+        if (two) dst1[t + 256 * k] = inv_final(y[k], ni, nis, q);
+    }
+}
