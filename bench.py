@@ -520,9 +520,29 @@ def run_scalar(args, cfg):
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1) / args.steps
+    ms_total = max_over_ranks(t0.elapsed_time(t1))
+    ms = ms_total / args.steps
     if pir.pir_status(ctx):
         raise RuntimeError("device status word set")
+
+    # end to end: the query matrix from pinned host memory, the results back
+    q_host = torch.empty(Q.numel(), dtype=torch.int32, pin_memory=True)
+    q_host.copy_(Q.cpu())
+    o_host = torch.empty(out.numel(), dtype=torch.int32, pin_memory=True)
+    ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            Q.copy_(q_host, non_blocking=True)
+            pir.pir_scalar_scan(ctx, db, R, C, Q, B, out, ws, stream)
+            o_host.copy_(out, non_blocking=True)
+
+    e2e_ms = None
+    if ke:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms = timed_ms(e2e_step, ke, stream)
     peaks, kind = measured_peaks()
     db_bytes = R * C
     if B <= 4:
@@ -543,15 +563,19 @@ def run_scalar(args, cfg):
                 "hbm_frac": db_bytes / (ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"])}
         dtype = "u8 x u32 (fp16 digits, fp32 accumulate)"
     line = {
-        "metric": "scalar-HE scan: DB GB/s scanned", "value": db_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
+        "metric": "scalar-HE scan: DB GB/s scanned",
+        "value": aggregate_throughput(db_bytes, args.steps, ms_total, world) / 1e9, "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic: seeded SplitMix64 bytes U[0,256), words U[0,2^32)",
         "config": {"workload": args.workload, "desc": cfg["desc"], "R": R, "C": C, "B": B,
                    "l2": "inputs larger than L2 (DB %.1f GiB), no flush" % (db_bytes / GIB)},
-        "queries_per_s": B * 1e3 / ms,
+        "queries_per_s": world * B * 1e3 / ms,
         "roofline": roof,
-        "clocks": clk, "gpu_launches": 2 * args.steps, "e2e": None, "cpu_baseline": None,
+        "clocks": clk, "gpu_launches": 2 * args.steps, "cpu_baseline": None,
+        "e2e": None if e2e_ms is None else {
+            "value": db_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 4 * C * B,
+            "d2h_bytes_per_step": 4 * R * B, "ms_per_step": e2e_ms},
     }
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
