@@ -27,10 +27,10 @@
 //               4 x tcgen05.mma (M=128, N=256, K=16) per stage into one of
 //               two 256-column fp32 accumulators (double buffered so that a
 //               drain overlaps the next chunk's MMAs);
-//   warps 2-5   converters: DB bytes -> fp16 in the 128B-swizzled K-major
-//               layout the MMA reads; two groups of two warps take the even
+//   warps 2-9   converters: DB bytes -> fp16 in the 128B-swizzled K-major
+//               layout the MMA reads; two groups of four warps take the even
 //               and the odd stages, so two stages convert at once;
-//   warps 6-9   epilogue: tcgen05.ld of a drained accumulator, integer
+//   warps 10-13 epilogue: tcgen05.ld of a drained accumulator, integer
 //               conversion and the shifted accumulation; one row per thread;
 //               the 64 running sums per row are written at the end of a tile.
 // All mbarrier waits are bounded (PIR_STATUS_TIMEOUT); TMEM is always freed.
@@ -54,7 +54,7 @@ constexpr uint32_t SC_A_BYTES = SC_TM * 128;  // fp16 A tile: 128 rows x 64 halv
 constexpr uint32_t SC_B_BYTES = SC_N * 128;   // fp16 B tile: 256 rows x 64 halves
 constexpr uint32_t SC_U8_BYTES = SC_TM * SC_KB;
 constexpr uint32_t SC_STAGE_BYTES = SC_A_BYTES + SC_B_BYTES + SC_U8_BYTES;
-constexpr int SC_THREADS = 320;
+constexpr int SC_THREADS = 448;
 constexpr uint32_t SC_TMEM_COLS = 512;
 
 // Byte offset of (row, 16-byte chunk j) in a K-major tile with the 128-byte
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < SC_NS; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(conv + s, 2);
+            mbar_init(conv + s, 4);
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -266,13 +266,13 @@ __global__ void __launch_bounds__(SC_THREADS, 1)
             mbar_wait(done, 0, A.status);
         }
 
-    } else if (warp < 6) {
+    } else if (warp < 10) {
         // ------------------------------------------------ converters: bytes -> fp16, swizzled
-        // two groups of two warps on alternating stages: warps 2, 3 the even
-        // stages, warps 4, 5 the odd ones (with SC_NS = 4 a ring slot always
+        // two groups of four warps on alternating stages: warps 2-5 the even
+        // stages, warps 6-9 the odd ones (with SC_NS = 4 a ring slot always
         // belongs to the same group, so parity waits never skip a phase)
-        const uint32_t grp = (uint32_t)(warp - 2) >> 1;
-        const uint32_t ct = ((uint32_t)(warp - 2) & 1u) * 32u + lane;   // 0..63 within the group
+        const uint32_t grp = (uint32_t)(warp - 2) >> 2;
+        const uint32_t ct = ((uint32_t)(warp - 2) & 3u) * 32u + lane;   // 0..127 within the group
         uint32_t it = 0;
         for (uint32_t t = blockIdx.x; t < A.ntiles; t += gridDim.x) {
             for (uint32_t kb = 0; kb < A.nkb; ++kb, ++it) {
@@ -283,8 +283,8 @@ __global__ void __launch_bounds__(SC_THREADS, 1)
                     const uint8_t *u = stU + s * SC_U8_BYTES;
                     uint8_t *a = stA + s * SC_A_BYTES;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint32_t q = ct + 64 * i;           // 16-byte piece: row q/4, part q%4
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t q = ct + 128 * i;          // 16-byte piece: row q/4, part q%4
                         const uint32_t row = q >> 2, part = q & 3;
                         const uint4 w = *reinterpret_cast<const uint4 *>(u + row * SC_KB + part * 16);
                         const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
