@@ -528,21 +528,15 @@ def run_scalar(args, cfg):
     # end to end: the query matrix from pinned host memory, the results back
     q_host = torch.empty(Q.numel(), dtype=torch.int32, pin_memory=True)
     q_host.copy_(Q.cpu())
-    o_host = torch.empty(out.numel(), dtype=torch.int32, pin_memory=True)
+    o_host = [torch.empty(out.numel(), dtype=torch.int32, pin_memory=True) for _ in range(2)]
     ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            Q.copy_(q_host, non_blocking=True)
-            pir.pir_scalar_scan(ctx, db, R, C, Q, B, out, ws, stream)
-            o_host.copy_(out, non_blocking=True)
-
     e2e_ms = None
     if ke:
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        e2e_ms = timed_ms(e2e_step, ke, stream)
+        # two scans in flight: query matrix i+1 in and results i-1 out during scan i
+        Q2, out2 = [Q, torch.empty_like(Q)], [out, torch.empty_like(out)]
+        e2e_ms = pipelined_ms(lambda k: Q2[k].copy_(q_host, non_blocking=True),
+                              lambda k: pir.pir_scalar_scan(ctx, db, R, C, Q2[k], B, out2[k], ws, stream),
+                              lambda k: o_host[k].copy_(out2[k], non_blocking=True), stream, ke)
     peaks, kind = measured_peaks()
     db_bytes = R * C
     if B <= 4:
@@ -575,7 +569,8 @@ def run_scalar(args, cfg):
         "clocks": clk, "gpu_launches": 2 * args.steps, "cpu_baseline": None,
         "e2e": None if e2e_ms is None else {
             "value": db_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 4 * C * B,
-            "d2h_bytes_per_step": 4 * R * B, "ms_per_step": e2e_ms},
+            "d2h_bytes_per_step": 4 * R * B, "ms_per_step": e2e_ms,
+            "how": "2 steps in flight: copy-in, compute and copy-out on three streams"},
     }
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
@@ -661,29 +656,23 @@ def run_exppack(args, cfg):
     c_host.copy_(C.cpu())
     g_host = torch.empty(graw.numel(), dtype=torch.int32, pin_memory=True)
     g_host.copy_(graw.cpu())
-    o_host = torch.empty(out.numel(), dtype=torch.int32, pin_memory=True)
+    o_host = [torch.empty(out.numel(), dtype=torch.int32, pin_memory=True) for _ in range(2)]
     ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            C.copy_(c_host, non_blocking=True)
-            graw.copy_(g_host, non_blocking=True)
-            step()
-            o_host.copy_(out, non_blocking=True)
-
     e2e_ms = None
     if ke:
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(ke):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / ke
+        # two steps in flight: C and the scan words of step i+1 in, the packed
+        # ciphertexts of step i-1 out, while step i computes
+        C2, g2, out2 = [C, torch.empty_like(C)], [graw, torch.empty_like(graw)], [out, torch.empty_like(out)]
+
+        def copy_in(k):
+            C2[k].copy_(c_host, non_blocking=True)
+            g2[k].copy_(g_host, non_blocking=True)
+
+        def compute(k):
+            pir.pir_lift_ntt(ctx, g2[k], G, B * Dr, stream)
+            pir.pir_exppack(ctx, h_db, n, Dr, C2[k], G, B, out2[k], ws, stream)
+
+        e2e_ms = pipelined_ms(copy_in, compute, lambda k: o_host[k].copy_(out2[k], non_blocking=True), stream, ke)
 
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
@@ -713,7 +702,8 @@ def run_exppack(args, cfg):
             "clocks": clk,
             "e2e": None if e2e_ms is None else {
                 "value": hint_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": c_bytes + graw_bytes, "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": c_bytes + graw_bytes, "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms,
+                "how": "2 steps in flight: copy-in, compute and copy-out on three streams"},
             "gpu_launches": args.steps * launches_per_step(cfg),
             "cpu_baseline": None,
         }
@@ -760,6 +750,48 @@ def ntt_rate(ctx, stream, polys=6830):
     run()
     ms = timed_ms(run, 10, stream)
     return polys * L / (ms * 1e-3)
+
+
+def pipelined_ms(copy_in, compute, copy_out, stream, steps, warm=3):
+    """Mean ms per step of a stream of steps with two in flight: step i's
+    inputs are copied in on their own stream and step i-2's results copied
+    out on another while `stream` computes step i-1; slot k = i % 2 holds one
+    step's device buffers.  copy_in(k) and copy_out(k) enqueue on the current
+    stream, compute(k) runs with `stream` current.  The timed region runs
+    from the first copy-in to the last copy-out."""
+    import torch
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    q_free, in_done, comp_done, out_free = ([torch.cuda.Event(), torch.cuda.Event()] for _ in range(4))
+
+    def serve(n, t0):
+        for i in range(t0, t0 + n):
+            k = i % 2
+            with torch.cuda.stream(h2d):
+                if i >= 2:
+                    h2d.wait_event(q_free[k])
+                copy_in(k)
+                in_done[k].record(h2d)
+            stream.wait_event(in_done[k])
+            if i >= 2:
+                stream.wait_event(out_free[k])
+            with torch.cuda.stream(stream):
+                compute(k)
+            q_free[k].record(stream)
+            comp_done[k].record(stream)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(comp_done[k])
+                copy_out(k)
+                out_free[k].record(d2h)
+
+    serve(warm, 0)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(h2d)
+    serve(steps, warm)
+    e1.record(d2h)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
 
 
 def graph_of(step, stream):
@@ -847,28 +879,16 @@ def run_coltor(args, cfg):
     o_bytes = 2 * P * 4
     cts_host = torch.empty(cts.numel(), dtype=torch.int32, pin_memory=True)
     cts_host.copy_(cts.cpu())
-    o_host = torch.empty(out.numel(), dtype=torch.int32, pin_memory=True)
+    o_host = [torch.empty(out.numel(), dtype=torch.int32, pin_memory=True) for _ in range(2)]
     ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            cts.copy_(cts_host, non_blocking=True)
-            run()
-            o_host.copy_(out, non_blocking=True)
-
     e2e_ms = None
     if ke:
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(ke):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / ke
+        # two tournaments in flight, each slot with its own buffers and graph
+        cts2, out2 = [cts, torch.empty_like(cts)], [out, torch.empty_like(out)]
+        graphs = [graph, graph_of(lambda: pir.pir_coltor(ctx, Cs, ell, w, cts2[1], n, out2[1], ws, stream), stream)]
+        e2e_ms = pipelined_ms(lambda k: cts2[k].copy_(cts_host, non_blocking=True),
+                              lambda k: graphs[k].replay(),
+                              lambda k: o_host[k].copy_(out2[k], non_blocking=True), stream, ke)
 
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
@@ -908,7 +928,8 @@ def run_coltor(args, cfg):
             "clocks": clk,
             "e2e": None if e2e_ms is None else {
                 "value": 1e3 / e2e_ms, "unit": "queries/s", "h2d_bytes_per_step": ct_bytes,
-                "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms,
+                "how": "2 steps in flight: copy-in, compute and copy-out on three streams"},
             "gpu_launches": args.steps * launches_per_step(cfg),
             "cpu_baseline": None,
         }
@@ -978,28 +999,16 @@ def run_expand(args, cfg):
     o_bytes = (1 << S) * 2 * P * 4
     ct_host = torch.empty(ct.numel(), dtype=torch.int32, pin_memory=True)
     ct_host.copy_(ct.cpu())
-    o_host = torch.empty(out.numel(), dtype=torch.int32, pin_memory=True)
+    o_host = [torch.empty(out.numel(), dtype=torch.int32, pin_memory=True) for _ in range(2)]
     ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            ct.copy_(ct_host, non_blocking=True)
-            run()
-            o_host.copy_(out, non_blocking=True)
-
     e2e_ms = None
     if ke:
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(ke):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / ke
+        # two expansions in flight, each slot with its own buffers and graph
+        ct2, out2 = [ct, torch.empty_like(ct)], [out, torch.empty_like(out)]
+        graphs = [graph, graph_of(lambda: pir.pir_expand(ctx, evks, ell, w, S, ct2[1], out2[1], ws, stream), stream)]
+        e2e_ms = pipelined_ms(lambda k: ct2[k].copy_(ct_host, non_blocking=True),
+                              lambda k: graphs[k].replay(),
+                              lambda k: o_host[k].copy_(out2[k], non_blocking=True), stream, ke)
 
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
@@ -1036,7 +1045,8 @@ def run_expand(args, cfg):
             "clocks": clk,
             "e2e": None if e2e_ms is None else {
                 "value": 1e3 / e2e_ms, "unit": "queries/s", "h2d_bytes_per_step": ct_bytes,
-                "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": o_bytes, "ms_per_step": e2e_ms,
+                "how": "2 steps in flight: copy-in, compute and copy-out on three streams"},
             "gpu_launches": args.steps * launches_per_step(cfg),
             "cpu_baseline": None,
         }
@@ -1312,38 +1322,9 @@ def run_ours(args, cfg):
         # streams, the copy engines) while RowSel scans query i
         q_dev = [srv.q_coef, torch.empty_like(srv.q_coef)]
         o_dev = [srv.o_ntt, torch.empty_like(srv.o_ntt)]
-        h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
-        ev = lambda: torch.cuda.Event()
-        q_free, in_done, comp_done, out_free = ([ev(), ev()] for _ in range(4))
-
-        def serve(n, t0):
-            for i in range(t0, t0 + n):
-                k = i % 2
-                with torch.cuda.stream(h2d):
-                    if i >= 2:
-                        h2d.wait_event(q_free[k])
-                    q_dev[k].copy_(q_host, non_blocking=True)
-                    in_done[k].record(h2d)
-                stream.wait_event(in_done[k])
-                if i >= 2:
-                    stream.wait_event(out_free[k])
-                pir.pir_rowsel(ctx, db, D0, D1, q_dev[k], B, o_dev[k], srv.ws, stream)
-                q_free[k].record(stream)
-                comp_done[k].record(stream)
-                with torch.cuda.stream(d2h):
-                    d2h.wait_event(comp_done[k])
-                    o_host[k].copy_(o_dev[k], non_blocking=True)
-                    out_free[k].record(d2h)
-
-        serve(3, 0)                              # warm-up
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(h2d)
-        serve(ke, 3)
-        e1.record(d2h)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / ke
+        e2e_ms = pipelined_ms(lambda k: q_dev[k].copy_(q_host, non_blocking=True),
+                              lambda k: pir.pir_rowsel(ctx, db, D0, D1, q_dev[k], B, o_dev[k], srv.ws, stream),
+                              lambda k: o_host[k].copy_(o_dev[k], non_blocking=True), stream, ke)
         e2e_how = "2 queries in flight: copy-in, RowSel and copy-out on three streams"
 
     peaks, peak_kind = measured_peaks()
