@@ -52,6 +52,10 @@ WORKLOADS = {
     "onion_64g": dict(kind="onion", N=4096, L=3, D0=1024, D1=1365, ell=5, w=18,
                       desc="OnionPIR server path per query over the 64 GiB DB: ExpandQuery 1 -> 1024 "
                            "ciphertexts, RowSel D0=1024 x D1=1365, ColTor 1365 -> 1 (N=4096, 3 primes, l=5)"),
+    "onion_64g_b16": dict(kind="onion", N=4096, L=3, D0=1024, D1=1365, ell=5, w=18, B=16,
+                          desc="OnionPIR server path for 16 clients per pass over the 64 GiB DB: 16 x ExpandQuery "
+                               "1 -> 1024 ciphertexts, one RowSel pass D0=1024 x D1=1365 x 16 queries (tensor "
+                               "cores), 16 x ColTor 1365 -> 1 (N=4096, 3 primes, l=5)"),
     "expand_1024": dict(kind="expand", N=4096, L=3, stages=10, ell=5, w=18,
                         desc="ExpandQuery of one query ciphertext into the 1024 RowSel inputs of the 64 GiB DB: "
                              "N=4096, 3 primes, 10 stages of Subs, l=5 digits of 18 bits"),
@@ -468,7 +472,9 @@ def launches_per_step(cfg) -> int:
     if cfg.get("kind") == "expand":
         return 4 * cfg["stages"]
     if cfg.get("kind") == "onion":
-        return 4 * (cfg["D0"].bit_length() - 1) + 3 * rowsel_passes(cfg["D0"], 1) + 4 * coltor_stages(cfg["D1"])
+        B = cfg.get("B", 1)
+        return (B * 4 * (cfg["D0"].bit_length() - 1) + 3 * rowsel_passes(cfg["D0"], B)
+                + B * 4 * coltor_stages(cfg["D1"]))
     return 3 * rowsel_passes(cfg["D0"], cfg["B"]) + (2 if cfg["domain"] == "coeff" else 0)
 
 
@@ -1059,9 +1065,10 @@ def run_expand(args, cfg):
 
 
 def run_onion(args, cfg):
-    """The OnionPIR server path per query: ExpandQuery of the query
-    ciphertext into D0 = 1024, RowSel over the resident 64 GiB DB, ColTor of
-    the D1 = 1365 results into one answer ciphertext (all NTT form)."""
+    """The OnionPIR server path for B queries (B clients, each with its own
+    keys): B ExpandQuery calls of a query ciphertext into D0 = 1024, one
+    RowSel pass of the B queries over the resident 64 GiB DB, B ColTor calls
+    of the D1 = 1365 results into one answer ciphertext each (all NTT form)."""
     import torch
 
     import __graft_entry__
@@ -1073,49 +1080,64 @@ def run_onion(args, cfg):
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     N, L, D0, D1, ell, w = cfg["N"], cfg["L"], cfg["D0"], cfg["D1"], cfg["ell"], cfg["w"]
+    B = cfg.get("B", 1)
     S, T = D0.bit_length() - 1, coltor_stages(D1)
     qs = pir.pir_primes(N, L)
     ctx = pir.pir_ctx_create(N, qs, local)
     P = L * N
+    qw, ew, rw = 2 * P, S * ell * 2 * P, T * 2 * ell * 2 * P      # words per client
     db = device_db(ctx, D0, D1, seed=7)
-    query = torch.empty(2 * P, dtype=torch.int32, device="cuda")
-    sd.fill_residues(query, 11, synth.T_EXTRA, N, qs)
-    evks = torch.empty(S * ell * 2 * P, dtype=torch.int32, device="cuda")
+    # per client: the query ciphertext and the RGSW rows of its column bits
+    # (sent with every query), and its evaluation keys (resident, sent once);
+    # two slots of per-query buffers so that two steps can be in flight
+    query = [torch.empty(B * qw, dtype=torch.int32, device="cuda") for _ in range(2)]
+    sd.fill_residues(query[0], 11, synth.T_EXTRA, N, qs)
+    rgsw = [torch.empty(B * rw, dtype=torch.int32, device="cuda") for _ in range(2)]
+    sd.fill_residues(rgsw[0], 13, synth.T_EXTRA, N, qs)
+    query[1].copy_(query[0])
+    rgsw[1].copy_(rgsw[0])
+    evks = torch.empty(B * ew, dtype=torch.int32, device="cuda")
     sd.fill_residues(evks, 12, synth.T_EXTRA, N, qs)
-    rgsw = torch.empty(T * 2 * ell * 2 * P, dtype=torch.int32, device="cuda")
-    sd.fill_residues(rgsw, 13, synth.T_EXTRA, N, qs)
-    expanded = torch.empty(D0 * 2 * P, dtype=torch.int32, device="cuda")
-    cols = torch.empty(D1 * 2 * P, dtype=torch.int32, device="cuda")
-    answer = torch.empty(2 * P, dtype=torch.int32, device="cuda")
+    expanded = torch.empty(B * D0 * qw, dtype=torch.int32, device="cuda")
+    cols = torch.empty(B * D1 * qw, dtype=torch.int32, device="cuda")
+    answer = [torch.empty(B * qw, dtype=torch.int32, device="cuda") for _ in range(2)]
     ws_e = pir.expand_workspace(ctx, D0 // 2, ell)
-    ws_r = pir.rowsel_workspace(ctx, D0, D1, 1)
+    ws_r = pir.rowsel_workspace(ctx, D0, D1, B)
     ws_c = pir.coltor_workspace(ctx, D1, ell)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
-    def expand():
-        pir.pir_expand(ctx, evks, ell, w, S, query, expanded, ws_e, stream)
+    def expand(k):
+        for b in range(B):
+            pir.pir_expand(ctx, evks[b * ew:(b + 1) * ew], ell, w, S, query[k][b * qw:(b + 1) * qw],
+                           expanded[b * D0 * qw:(b + 1) * D0 * qw], ws_e, stream)
 
-    def coltor():
-        pir.pir_coltor(ctx, rgsw, ell, w, cols, D1, answer, ws_c, stream)
+    def rowsel():
+        pir.pir_rowsel(ctx, db, D0, D1, expanded, B, cols, ws_r, stream)
+
+    def coltor(k):
+        for b in range(B):
+            pir.pir_coltor(ctx, rgsw[k][b * rw:(b + 1) * rw], ell, w, cols[b * D1 * qw:(b + 1) * D1 * qw], D1,
+                           answer[k][b * qw:(b + 1) * qw], ws_c, stream)
 
     for _ in range(2):                        # first calls (kernel attributes, caches) outside the graphs
-        expand()
-        pir.pir_rowsel(ctx, db, D0, D1, expanded, 1, cols, ws_r, stream)
-        coltor()
-    g_expand, g_coltor = graph_of(expand, stream), graph_of(coltor, stream)
+        expand(0)
+        rowsel()
+        coltor(0)
+    g_expand = [graph_of(lambda: expand(0), stream), graph_of(lambda: expand(1), stream)]
+    g_coltor = [graph_of(lambda: coltor(0), stream), graph_of(lambda: coltor(1), stream)]
 
-    def step(ev=None):
+    def step(ev=None, k=0):
         with torch.cuda.stream(stream):
             if ev is not None:
                 ev[0].record(stream)
-            g_expand.replay()                 # the small expansion stages are bound by launch latency
+            g_expand[k].replay()              # the small expansion stages are bound by launch latency
             if ev is not None:
                 ev[1].record(stream)
-            pir.pir_rowsel(ctx, db, D0, D1, expanded, 1, cols, ws_r, stream)
+            rowsel()
             if ev is not None:
                 ev[2].record(stream)
-            g_coltor.replay()
+            g_coltor[k].replay()
             if ev is not None:
                 ev[3].record(stream)
 
@@ -1140,57 +1162,55 @@ def run_onion(args, cfg):
     if pir.pir_status(ctx):
         raise RuntimeError("device status word set")
 
-    q_host = torch.empty(query.numel(), dtype=torch.int32, pin_memory=True)
-    q_host.copy_(query.cpu())
-    a_host = torch.empty(answer.numel(), dtype=torch.int32, pin_memory=True)
+    # end to end: every step's query ciphertexts and RGSW rows in from pinned
+    # host memory, the answers out; two steps in flight
+    q_host = torch.empty(query[0].numel(), dtype=torch.int32, pin_memory=True)
+    q_host.copy_(query[0].cpu())
+    r_host = torch.empty(rgsw[0].numel(), dtype=torch.int32, pin_memory=True)
+    r_host.copy_(rgsw[0].cpu())
+    a_host = [torch.empty(answer[0].numel(), dtype=torch.int32, pin_memory=True) for _ in range(2)]
     ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            query.copy_(q_host, non_blocking=True)
-            step()
-            a_host.copy_(answer, non_blocking=True)
-
     e2e_ms = None
     if ke:
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(ke):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / ke
+        def copy_in(k):
+            query[k].copy_(q_host, non_blocking=True)
+            rgsw[k].copy_(r_host, non_blocking=True)
+
+        e2e_ms = pipelined_ms(copy_in, lambda k: step(None, k),
+                              lambda k: a_host[k].copy_(answer[k], non_blocking=True), stream, ke)
 
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     logical_db = P * D0 * D1 * 4
     ms_step = ms_total / args.steps
     db_gbs = logical_db / (phase[1] * 1e-3) / 1e9
+    on_tensor = 8 < B <= 16
     result = None
     if rank == 0:
         line = {
-            "metric": ONION_METRIC, "value": world * args.steps / (ms_total * 1e-3), "unit": "queries/s",
+            "metric": ONION_METRIC, "value": world * B * args.steps / (ms_total * 1e-3), "unit": "queries/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
             "data": "synthetic: seeded SplitMix64 DB coefficients U[0,2^16), query, key and RGSW residues U[0,q_i)",
-            "config": {"workload": args.workload, "desc": cfg["desc"], "logical_db_bytes": logical_db,
+            "config": {"workload": args.workload, "desc": cfg["desc"], "logical_db_bytes": logical_db, "B": B,
                        "l2": "inputs larger than L2 (DB %.1f GiB), no flush" % (logical_db / GIB),
                        "parallelism": "replicas x%d" % world},
             "phase_ms": {"expand": phase[0], "rowsel": phase[1], "coltor": phase[2]},
-            "launch": "ExpandQuery and ColTor each replayed as one CUDA graph; RowSel launched directly",
+            "launch": "the B ExpandQuery and the B ColTor calls each replayed as one CUDA graph; "
+                      "RowSel launched directly",
             "db_gbs_in_rowsel": db_gbs,
             "roofline": {"bound": "hbm", "achieved": db_gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": db_gbs / hbm_peak, "traffic": None, "kernel": "rowsel_kernel (the DB scan)",
+                         "frac": db_gbs / hbm_peak, "traffic": None,
+                         "kernel": "rowsel_tc_kernel (the DB scan, %d queries per pass)" % B if on_tensor
+                                   else "rowsel_kernel (the DB scan)",
                          "peak_source": "%s hbm_gbs (copy)" % peak_kind,
                          "algorithmic_bytes_per_launch": logical_db},
             "clocks": clk,
             "e2e": None if e2e_ms is None else {
-                "value": 1e3 / e2e_ms, "unit": "queries/s", "h2d_bytes_per_step": 2 * P * 4,
-                "d2h_bytes_per_step": 2 * P * 4, "ms_per_step": e2e_ms},
+                "value": B * 1e3 / e2e_ms, "unit": "queries/s", "h2d_bytes_per_step": B * (qw + rw) * 4,
+                "d2h_bytes_per_step": B * qw * 4, "ms_per_step": e2e_ms,
+                "how": "query ciphertexts and RGSW rows in, answers out; evaluation keys resident; "
+                       "2 steps in flight on three streams"},
             "gpu_launches": args.steps * launches_per_step(cfg),
             "cpu_baseline": None,
         }
