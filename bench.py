@@ -53,9 +53,10 @@ WORKLOADS = {
                       desc="OnionPIR server path per query over the 64 GiB DB: ExpandQuery 1 -> 1024 "
                            "ciphertexts, RowSel D0=1024 x D1=1365, ColTor 1365 -> 1 (N=4096, 3 primes, l=5)"),
     "onion_64g_b16": dict(kind="onion", N=4096, L=3, D0=1024, D1=1365, ell=5, w=18, B=16,
-                          desc="OnionPIR server path for 16 clients per pass over the 64 GiB DB: 16 x ExpandQuery "
-                               "1 -> 1024 ciphertexts, one RowSel pass D0=1024 x D1=1365 x 16 queries (tensor "
-                               "cores), 16 x ColTor 1365 -> 1 (N=4096, 3 primes, l=5)"),
+                          desc="OnionPIR server path for 16 clients per pass over the 64 GiB DB: 16 ExpandQuery "
+                               "1 -> 1024 ciphertexts (one batched call), one RowSel pass D0=1024 x D1=1365 x 16 "
+                               "queries (tensor cores), 16 ColTor 1365 -> 1 (one batched call); N=4096, 3 primes, "
+                               "l=5"),
     "expand_1024": dict(kind="expand", N=4096, L=3, stages=10, ell=5, w=18,
                         desc="ExpandQuery of one query ciphertext into the 1024 RowSel inputs of the 64 GiB DB: "
                              "N=4096, 3 primes, 10 stages of Subs, l=5 digits of 18 bits"),
@@ -472,9 +473,9 @@ def launches_per_step(cfg) -> int:
     if cfg.get("kind") == "expand":
         return 4 * cfg["stages"]
     if cfg.get("kind") == "onion":
-        B = cfg.get("B", 1)
-        return (B * 4 * (cfg["D0"].bit_length() - 1) + 3 * rowsel_passes(cfg["D0"], B)
-                + B * 4 * coltor_stages(cfg["D1"]))
+        # one batched expansion and one batched tournament for all B clients
+        return (4 * (cfg["D0"].bit_length() - 1) + 3 * rowsel_passes(cfg["D0"], cfg.get("B", 1))
+                + 4 * coltor_stages(cfg["D1"]))
     return 3 * rowsel_passes(cfg["D0"], cfg["B"]) + (2 if cfg["domain"] == "coeff" else 0)
 
 
@@ -1066,9 +1067,10 @@ def run_expand(args, cfg):
 
 def run_onion(args, cfg):
     """The OnionPIR server path for B queries (B clients, each with its own
-    keys): B ExpandQuery calls of a query ciphertext into D0 = 1024, one
-    RowSel pass of the B queries over the resident 64 GiB DB, B ColTor calls
-    of the D1 = 1365 results into one answer ciphertext each (all NTT form)."""
+    keys): the B expansions of a query ciphertext into D0 = 1024 (one batched
+    call), one RowSel pass of the B queries over the resident 64 GiB DB, the
+    B tournaments of the D1 = 1365 results into one answer ciphertext each
+    (one batched call); all NTT form."""
     import torch
 
     import __graft_entry__
@@ -1101,24 +1103,20 @@ def run_onion(args, cfg):
     expanded = torch.empty(B * D0 * qw, dtype=torch.int32, device="cuda")
     cols = torch.empty(B * D1 * qw, dtype=torch.int32, device="cuda")
     answer = [torch.empty(B * qw, dtype=torch.int32, device="cuda") for _ in range(2)]
-    ws_e = pir.expand_workspace(ctx, D0 // 2, ell)
+    ws_e = pir.expand_workspace(ctx, B * D0 // 2, ell)
     ws_r = pir.rowsel_workspace(ctx, D0, D1, B)
-    ws_c = pir.coltor_workspace(ctx, D1, ell)
+    ws_c = pir.coltor_batch_workspace(ctx, D1, B, ell)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
     def expand(k):
-        for b in range(B):
-            pir.pir_expand(ctx, evks[b * ew:(b + 1) * ew], ell, w, S, query[k][b * qw:(b + 1) * qw],
-                           expanded[b * D0 * qw:(b + 1) * D0 * qw], ws_e, stream)
+        pir.pir_expand_batch(ctx, evks, ell, w, S, query[k], B, expanded, ws_e, stream)
 
     def rowsel():
         pir.pir_rowsel(ctx, db, D0, D1, expanded, B, cols, ws_r, stream)
 
     def coltor(k):
-        for b in range(B):
-            pir.pir_coltor(ctx, rgsw[k][b * rw:(b + 1) * rw], ell, w, cols[b * D1 * qw:(b + 1) * D1 * qw], D1,
-                           answer[k][b * qw:(b + 1) * qw], ws_c, stream)
+        pir.pir_coltor_batch(ctx, rgsw[k], ell, w, cols, D1, B, answer[k], ws_c, stream)
 
     for _ in range(2):                        # first calls (kernel attributes, caches) outside the graphs
         expand(0)
@@ -1196,7 +1194,7 @@ def run_onion(args, cfg):
                        "l2": "inputs larger than L2 (DB %.1f GiB), no flush" % (logical_db / GIB),
                        "parallelism": "replicas x%d" % world},
             "phase_ms": {"expand": phase[0], "rowsel": phase[1], "coltor": phase[2]},
-            "launch": "the B ExpandQuery and the B ColTor calls each replayed as one CUDA graph; "
+            "launch": "the batched ExpandQuery and ColTor calls each replayed as one CUDA graph; "
                       "RowSel launched directly",
             "db_gbs_in_rowsel": db_gbs,
             "roofline": {"bound": "hbm", "achieved": db_gbs, "peak": hbm_peak, "unit": "GB/s",

@@ -267,6 +267,28 @@ int pir_coltor(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w,
                void *workspace, uint64_t workspace_bytes, void *stream);
 
 /*
+ * pir_coltor_batch — G independent tournaments of n ciphertexts each (G
+ * clients served by one RowSel pass, each with its own RGSW ciphertexts),
+ * run stage by stage as one tournament of G * ceil(n/2) pairs, so the small
+ * late stages of G tournaments share their launches.  Tournament b is
+ * exactly pir_coltor on its own inputs.
+ *   C    : device, [G][S][2 ell][2][L][N], S = ceil(log2 n): client b's
+ *          stages at b * S * 2 ell * 2 L N words.
+ *   in   : device, [G][n][2][L][N] (the RowSel output of G queries,
+ *          [B][D1][2][L][N], with G = B and n = D1).
+ *   out  : device, [G][2][L][N]; must not overlap in.
+ *   workspace : device, >= pir_coltor_batch_workspace_bytes(ctx, n, G,
+ *          ell) bytes (0 when G * ceil(n/2) >= 2^31), 16-byte aligned.
+ * Errors: as pir_coltor; PIR_ERR_ARG for G = 0 or G * ceil(n/2) >= 2^31.
+ * pir_coltor(...) is pir_coltor_batch with G = 1.
+ */
+uint64_t pir_coltor_batch_workspace_bytes(const pir_ctx *ctx, uint64_t n, uint64_t G, uint32_t ell);
+
+int pir_coltor_batch(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w,
+                     const uint32_t *in, uint64_t n, uint64_t G, uint32_t *out,
+                     void *workspace, uint64_t workspace_bytes, void *stream);
+
+/*
  * ExpandQuery — the expansion tree of Subs operations (GPIR section 2:
  * every depth of the tree is a stage with its own evaluation key, up to
  * log2 N stages; GPIR section 3: Subs operates on the a polynomial only).
@@ -301,6 +323,26 @@ int pir_expand_stage(pir_ctx *ctx, const uint32_t *evk, uint32_t ell, uint32_t w
 int pir_expand(pir_ctx *ctx, const uint32_t *evks, uint32_t ell, uint32_t w, uint32_t stages,
                const uint32_t *ct, uint32_t *out,
                void *workspace, uint64_t workspace_bytes, void *stream);
+
+/*
+ * pir_expand_batch — G independent expansions (G clients, each with its own
+ * query ciphertext and evaluation keys) run stage by stage as one expansion
+ * of G * 2^j ciphertexts at stage j, so the small early stages of G
+ * expansions share their launches.  Expansion b is exactly pir_expand on its
+ * own inputs.
+ *   evks : device, [G][stages][ell][2][L][N]: client b's keys at
+ *          b * stages * ell * 2 L N words.
+ *   ct   : device, [G][2][L][N], one query ciphertext per client.
+ *   out  : device, [G][2^stages][2][L][N] (the RowSel query layout
+ *          [B][D0][2][L][N] with B = G, D0 = 2^stages); must not overlap ct.
+ *   workspace : device, >= pir_expand_workspace_bytes(ctx, G * 2^(stages-1),
+ *          ell) bytes, 16-byte aligned.
+ * Errors: as pir_expand; PIR_ERR_ARG for G = 0 or G * 2^(stages-1) >= 2^31.
+ * pir_expand(...) is pir_expand_batch with G = 1.
+ */
+int pir_expand_batch(pir_ctx *ctx, const uint32_t *evks, uint32_t ell, uint32_t w, uint32_t stages,
+                     const uint32_t *ct, uint64_t G, uint32_t *out,
+                     void *workspace, uint64_t workspace_bytes, void *stream);
 
 /*
  * pir_scalar_workspace_bytes — device workspace pir_scalar_scan needs for a

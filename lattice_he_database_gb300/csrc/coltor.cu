@@ -23,6 +23,12 @@
 // The difference, decomposition and MAC kernels move four words per thread
 // and memory access; all three are bound by HBM.  The decomposition is
 // shared with ExpandQuery (gadget.cuh).
+//
+// Batches: G tournaments of n ciphertexts each (one per client, each with
+// its own RGSW ciphertexts) run as one tournament of G*ceil(n/2) pairs per
+// stage; global pair g belongs to tournament b = g / Rp (Rp = ceil(n/2)
+// pairs per tournament), and the stage output [G][Rp] is the next stage's
+// input [G][n' = Rp].
 #include <cstring>
 
 #include "common.cuh"
@@ -39,10 +45,18 @@ constexpr uint32_t CT_THREADS = 256;
 struct DiffArgs {
     const uint32_t *in;
     uint32_t *diff;
-    uint64_t n, R;          // input ciphertexts, pairs
+    uint64_t n, R, Rp;      // input ciphertexts per tournament, pairs in all, pairs per tournament
     uint32_t N, L;
     uint32_t q[PIR_MAX_RNS];
 };
+
+// Index of the even ciphertext of global pair g (tournament g / Rp).
+__device__ __forceinline__ uint64_t even_ct(uint64_t g, uint64_t Rp, uint64_t n, bool &has_odd) {
+    const uint32_t b = (uint32_t)g / (uint32_t)Rp;          // g < 2^31 (checked on the host)
+    const uint64_t i = g - (uint64_t)b * Rp;
+    has_odd = 2 * i + 1 < n;
+    return (uint64_t)b * n + 2 * i;
+}
 
 // d_i = ct_2i+1 - ct_2i mod q_l, four words per thread.
 __global__ void __launch_bounds__(CT_THREADS) coltor_diff_kernel(const DiffArgs A) {
@@ -53,9 +67,11 @@ __global__ void __launch_bounds__(CT_THREADS) coltor_diff_kernel(const DiffArgs 
         const uint64_t w0 = v * 4;
         const uint64_t i = w0 / ct_words, r = w0 - i * ct_words;
         const uint32_t q = pick(A.q, (uint32_t)((r / A.N) % A.L));
-        const uint4 e = *reinterpret_cast<const uint4 *>(A.in + 2 * i * ct_words + r);
+        bool has_odd;
+        const uint64_t ce = even_ct(i, A.Rp, A.n, has_odd);
+        const uint4 e = *reinterpret_cast<const uint4 *>(A.in + ce * ct_words + r);
         uint4 o = make_uint4(0, 0, 0, 0);
-        if (2 * i + 1 < A.n) o = *reinterpret_cast<const uint4 *>(A.in + (2 * i + 1) * ct_words + r);
+        if (has_odd) o = *reinterpret_cast<const uint4 *>(A.in + (ce + 1) * ct_words + r);
         uint4 d;
         d.x = o.x + q - e.x; d.x = d.x >= q ? d.x - q : d.x;
         d.y = o.y + q - e.y; d.y = d.y >= q ? d.y - q : d.y;
@@ -69,7 +85,7 @@ struct DiffInttArgs {
     const uint32_t *in;
     uint32_t *diff;
     const uint32_t *tw;     // [L][4][N] twiddle tables
-    uint64_t n;
+    uint64_t n, Rp;         // ciphertexts and pairs per tournament
     uint32_t L;
     uint32_t q[PIR_MAX_RNS], ninv[PIR_MAX_RNS], ninv_shoup[PIR_MAX_RNS];
 };
@@ -87,9 +103,10 @@ __global__ void __launch_bounds__(kT4) coltor_diff_intt4096_kernel(const __grid_
     const uint32_t q = A.q[l];
     const uint32_t *W = A.tw + (size_t)l * 4 * kN4 + TW_INV * kN4;
     const uint32_t *Wp = A.tw + (size_t)l * 4 * kN4 + TW_INV_SHOUP * kN4;
-    const uint32_t *ev = A.in + 2 * i * 2 * LN + (uint64_t)l * kN4;          // polynomial 0 of ct_2i
-    const uint32_t *od = A.in + (2 * i + 1) * 2 * LN + (uint64_t)l * kN4;    // polynomial 0 of ct_2i+1
-    const bool has_odd = 2 * i + 1 < A.n;
+    bool has_odd;
+    const uint64_t ce = even_ct(i, A.Rp, A.n, has_odd);
+    const uint32_t *ev = A.in + ce * 2 * LN + (uint64_t)l * kN4;             // polynomial 0 of ct_2i
+    const uint32_t *od = A.in + (ce + 1) * 2 * LN + (uint64_t)l * kN4;       // polynomial 0 of ct_2i+1
     const uint32_t t = threadIdx.x;
     uint32_t x[16], y[16];
 #pragma unroll
@@ -106,11 +123,11 @@ __global__ void __launch_bounds__(kT4) coltor_diff_intt4096_kernel(const __grid_
 }
 
 struct MacArgs {
-    const uint32_t *in;     // [n][2][L][N] (the even ciphertexts are added)
+    const uint32_t *in;     // [G][n][2][L][N] (the even ciphertexts are added)
     const uint32_t *dn;     // [R][2 ell][L][N] NTT of the digits
-    const uint32_t *C;      // [2 ell][2][L][N]
+    const uint32_t *C;      // tournament b's stage RGSW [2 ell][2][L][N] at C + b * c_stride
     uint32_t *out;          // [R][2][L][N]
-    uint64_t R;
+    uint64_t R, Rp, n, c_stride;
     uint32_t N, L, ell;
     uint32_t q[PIR_MAX_RNS];
     uint64_t mu[PIR_MAX_RNS];
@@ -133,8 +150,10 @@ __global__ void __launch_bounds__(CT_THREADS) coltor_mac_kernel(const MacArgs A)
         const uint64_t e0 = e * 4;
         const uint64_t i = e0 / LN, pt = e0 - i * LN;    // pt = l * N + j
         const uint32_t l = (uint32_t)(pt / A.N);
+        bool has_odd;
+        const uint64_t ce = even_ct(i, A.Rp, A.n, has_odd);
         const uint32_t *dp = A.dn + i * V * LN + pt;
-        const uint32_t *cp = A.C + pt;
+        const uint32_t *cp = A.C + (uint64_t)((uint32_t)i / (uint32_t)A.Rp) * A.c_stride + pt;
         uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
 #pragma unroll 4
         for (uint32_t v = 0; v < V; ++v) {
@@ -146,8 +165,8 @@ __global__ void __launch_bounds__(CT_THREADS) coltor_mac_kernel(const MacArgs A)
         }
         const uint32_t q = pick(A.q, l);
         const uint64_t mu = pick(A.mu, l);
-        const uint4 ev0 = *reinterpret_cast<const uint4 *>(A.in + 2 * i * 2 * LN + pt);
-        const uint4 ev1 = *reinterpret_cast<const uint4 *>(A.in + 2 * i * 2 * LN + LN + pt);
+        const uint4 ev0 = *reinterpret_cast<const uint4 *>(A.in + ce * 2 * LN + pt);
+        const uint4 ev1 = *reinterpret_cast<const uint4 *>(A.in + ce * 2 * LN + LN + pt);
         uint32_t *op = A.out + i * 2 * LN + pt;
         *reinterpret_cast<uint4 *>(op) = make_uint4(mac_final(a0, ev0.x, q, mu), mac_final(a1, ev0.y, q, mu),
                                                     mac_final(a2, ev0.z, q, mu), mac_final(a3, ev0.w, q, mu));
@@ -158,35 +177,47 @@ __global__ void __launch_bounds__(CT_THREADS) coltor_mac_kernel(const MacArgs A)
 
 uint64_t align64(uint64_t words) { return (words + 63) / 64 * 64; }
 
-// Workspace regions (words) for stages of at most R pairs.
+// Workspace regions (words) for the stages of G tournaments of n
+// ciphertexts (G * ceil(n/2) pairs in the first stage).
 struct CtLayout {
     uint64_t diff, dig, dn, ping, pong, total;   // offsets and total words
 };
 
-CtLayout ct_layout(const pir_ctx *ctx, uint64_t n, uint32_t ell) {
-    const uint64_t R = (n + 1) / 2, LN = (uint64_t)ctx->L * ctx->N;
+CtLayout ct_layout(const pir_ctx *ctx, uint64_t n, uint32_t ell, uint64_t G = 1) {
+    const uint64_t Rp = (n + 1) / 2, R = G * Rp, LN = (uint64_t)ctx->L * ctx->N;
     CtLayout c;
     c.diff = 0;
     c.dig = c.diff + align64(R * 2 * LN);
     c.dn = c.dig + align64(R * 2 * ell * (uint64_t)ctx->N);
     c.ping = c.dn + align64(R * 2 * ell * LN);
     c.pong = c.ping + align64(R * 2 * LN);
-    c.total = c.pong + align64(((R + 1) / 2) * 2 * LN);
+    c.total = c.pong + align64(G * ((Rp + 1) / 2) * 2 * LN);
     return c;
 }
 
-int check_params(const pir_ctx *ctx, uint32_t ell, uint32_t w, uint64_t n) {
-    if (!ctx || n == 0 || n > (1ull << 32)) return PIR_ERR_ARG;
+// Pair indices stay below 2^31 (32-bit tournament division in the kernels).
+int check_params(const pir_ctx *ctx, uint32_t ell, uint32_t w, uint64_t n, uint64_t G = 1) {
+    if (!ctx || n == 0 || G == 0 || n > (1ull << 32) || G > (1ull << 31) || G * ((n + 1) / 2) >= (1ull << 31))
+        return PIR_ERR_ARG;
     return gadget_params_ok(ctx, ell, w) ? PIR_OK : PIR_ERR_ARG;   // digits must cover [0, Q)
+}
+
+// Stages of a tournament of n ciphertexts: ceil(log2 n).
+uint32_t stages_of(uint64_t n) {
+    uint32_t s = 0;
+    while ((1ull << s) < n) ++s;
+    return s;
 }
 
 uint64_t grid_for(const pir_ctx *ctx, uint64_t work) { return gadget_grid(ctx, work); }
 
-// One stage from `in` (n ciphertexts) to `out` (ceil(n/2)); ws holds the
-// diff, digit and digit-NTT regions of a layout for at least n ciphertexts.
-int stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint32_t *in, uint64_t n, uint32_t *out,
-          uint32_t *ws, const CtLayout &lay, cudaStream_t st) {
-    const uint64_t R = (n + 1) / 2, LN = (uint64_t)ctx->L * ctx->N;
+// One stage of G tournaments from `in` ([G][n] ciphertexts) to `out`
+// ([G][ceil(n/2)]); tournament b's RGSW ciphertext is at C + b * c_stride.
+// ws holds the diff, digit and digit-NTT regions of a layout for at least
+// G tournaments of n ciphertexts.
+int stage(pir_ctx *ctx, const uint32_t *C, uint64_t c_stride, uint32_t ell, uint32_t w, const uint32_t *in,
+          uint64_t n, uint64_t G, uint32_t *out, uint32_t *ws, const CtLayout &lay, cudaStream_t st) {
+    const uint64_t Rp = (n + 1) / 2, R = G * Rp, LN = (uint64_t)ctx->L * ctx->N;
     uint32_t *diff = ws + lay.diff, *dig = ws + lay.dig, *dn = ws + lay.dn;
 
     DiffArgs da;
@@ -195,6 +226,7 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint3
     da.diff = diff;
     da.n = n;
     da.R = R;
+    da.Rp = Rp;
     da.N = ctx->N;
     da.L = ctx->L;
     for (uint32_t l = 0; l < ctx->L; ++l) da.q[l] = ctx->q[l];
@@ -206,6 +238,7 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint3
         ia.diff = diff;
         ia.tw = ctx->d_tw;
         ia.n = n;
+        ia.Rp = Rp;
         ia.L = ctx->L;
         for (uint32_t l = 0; l < ctx->L; ++l) {
             ia.q[l] = ctx->q[l];
@@ -235,6 +268,9 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint3
     ma.C = C;
     ma.out = out;
     ma.R = R;
+    ma.Rp = Rp;
+    ma.n = n;
+    ma.c_stride = c_stride;
     ma.N = ctx->N;
     ma.L = ctx->L;
     ma.ell = ell;
@@ -253,9 +289,15 @@ bool overlaps(const void *a, uint64_t abytes, const void *b, uint64_t bbytes) {
 
 }  // namespace
 
+extern "C" uint64_t pir_coltor_batch_workspace_bytes(const pir_ctx *ctx, uint64_t n, uint64_t G, uint32_t ell) {
+    if (!ctx || n == 0 || G == 0 || ell == 0 || ell > GD_MAX_ELL || n > (1ull << 32) || G > (1ull << 31) ||
+        G * ((n + 1) / 2) >= (1ull << 31))
+        return 0;
+    return ct_layout(ctx, n, ell, G).total * 4;
+}
+
 extern "C" uint64_t pir_coltor_workspace_bytes(const pir_ctx *ctx, uint64_t n, uint32_t ell) {
-    if (!ctx || n == 0 || ell == 0 || ell > GD_MAX_ELL || n > (1ull << 32)) return 0;
-    return ct_layout(ctx, n, ell).total * 4;
+    return pir_coltor_batch_workspace_bytes(ctx, n, 1, ell);
 }
 
 extern "C" int pir_coltor_stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint32_t *in,
@@ -270,34 +312,42 @@ extern "C" int pir_coltor_stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, u
     const uint64_t ctb = 2ull * ctx->L * ctx->N * 4;
     if (overlaps(in, n * ctb, out, ((n + 1) / 2) * ctb)) return PIR_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
-    return stage(ctx, C, ell, w, in, n, out, static_cast<uint32_t *>(workspace), lay, (cudaStream_t)stream);
+    return stage(ctx, C, 0, ell, w, in, n, 1, out, static_cast<uint32_t *>(workspace), lay, (cudaStream_t)stream);
 }
 
-extern "C" int pir_coltor(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint32_t *in, uint64_t n,
-                          uint32_t *out, void *workspace, uint64_t workspace_bytes, void *stream) {
-    int rc = check_params(ctx, ell, w, n);
+extern "C" int pir_coltor_batch(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint32_t *in,
+                                uint64_t n, uint64_t G, uint32_t *out, void *workspace, uint64_t workspace_bytes,
+                                void *stream) {
+    int rc = check_params(ctx, ell, w, n, G);
     if (rc) return rc;
     if (!C || !in || !out || !workspace) return PIR_ERR_ARG;
     if (!aligned16(C) || !aligned16(in) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
-    const CtLayout lay = ct_layout(ctx, n, ell);
+    const CtLayout lay = ct_layout(ctx, n, ell, G);
     if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
     const uint64_t ctw = 2ull * ctx->L * ctx->N;
-    if (overlaps(in, n * ctw * 4, out, ctw * 4)) return PIR_ERR_ARG;
+    if (overlaps(in, G * n * ctw * 4, out, G * ctw * 4)) return PIR_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
-    if (n == 1) return cudaMemcpyAsync(out, in, ctw * 4, cudaMemcpyDeviceToDevice, st) == cudaSuccess ? PIR_OK
-                                                                                              : PIR_ERR_CUDA;
+    if (n == 1)
+        return cudaMemcpyAsync(out, in, G * ctw * 4, cudaMemcpyDeviceToDevice, st) == cudaSuccess ? PIR_OK
+                                                                                                : PIR_ERR_CUDA;
     uint32_t *ws = static_cast<uint32_t *>(workspace);
     const uint64_t row = 2ull * ell * ctw;          // words of one stage's RGSW ciphertext
+    const uint64_t c_stride = stages_of(n) * row;   // words of one tournament's RGSW ciphertexts
     const uint32_t *cur = in;
     uint64_t cnt = n;
     for (uint32_t s = 0; cnt > 1; ++s) {
         const uint64_t next = (cnt + 1) / 2;
         uint32_t *dst = next == 1 ? out : ws + ((s & 1) ? lay.pong : lay.ping);
-        rc = stage(ctx, C + s * row, ell, w, cur, cnt, dst, ws, lay, st);
+        rc = stage(ctx, C + s * row, c_stride, ell, w, cur, cnt, G, dst, ws, lay, st);
         if (rc) return rc;
         cur = dst;
         cnt = next;
     }
     return PIR_OK;
+}
+
+extern "C" int pir_coltor(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w, const uint32_t *in, uint64_t n,
+                          uint32_t *out, void *workspace, uint64_t workspace_bytes, void *stream) {
+    return pir_coltor_batch(ctx, C, ell, w, in, n, 1, out, workspace, workspace_bytes, stream);
 }

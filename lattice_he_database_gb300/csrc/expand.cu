@@ -22,6 +22,12 @@
 //   3. lift + forward NTT of the digits (the library's NTT kernel)
 //   4. expand_mac_kernel         the key switch, sigma_k(c0) by slot
 //      permutation, and both outputs with the monomial's NTT
+//
+// Batches: G expansions (one per client, each with its own keys) run as one
+// expansion of G*M ciphertexts per stage; global ciphertext g belongs to
+// client b = g / M, and client b's outputs i and i + M go to b*2M + i and
+// b*2M + i + M, so after the last stage client b's 2^S ciphertexts are
+// contiguous (the layout RowSel takes for a batch of queries).
 #include <cstring>
 
 #include "common.cuh"
@@ -69,12 +75,12 @@ __global__ void __launch_bounds__(kT4) expand_intt_a4096_kernel(const __grid_con
 }
 
 struct ExpMacArgs {
-    const uint32_t *in;     // [M][2][L][N]
-    const uint32_t *dn;     // [M][ell][L][N] NTT of the digits of sigma_k(c1)
-    const uint32_t *evk;    // [ell][2][L][N]
-    uint32_t *out;          // [2M][2][L][N]
+    const uint32_t *in;     // [G][M][2][L][N]
+    const uint32_t *dn;     // [G][M][ell][L][N] NTT of the digits of sigma_k(c1)
+    const uint32_t *evk;    // client b's stage key [ell][2][L][N] at evk + b * evk_stride
+    uint32_t *out;          // [G][2M][2][L][N]
     const uint32_t *tw;     // [L][4][N]
-    uint64_t M;
+    uint64_t M, GM, evk_stride;
     uint32_t N, logN, L, ell, k, j;
     uint32_t q[PIR_MAX_RNS];
     uint64_t mu[PIR_MAX_RNS];
@@ -96,7 +102,7 @@ __device__ __forceinline__ uint32_t subq(uint32_t a, uint32_t b, uint32_t q) {
 // residues below 2^29 sum below 2^62 without reduction.
 __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs A) {
     const uint64_t LN = (uint64_t)A.L * A.N;
-    const uint64_t total4 = A.M * LN / 4;
+    const uint64_t total4 = A.GM * LN / 4;
     const uint32_t twoN = 2 * A.N;
     for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total4;
          e += (uint64_t)gridDim.x * blockDim.x) {
@@ -105,8 +111,10 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
         const uint32_t l = (uint32_t)(pt / A.N), s0 = (uint32_t)(pt - (uint64_t)l * A.N);
         const uint32_t q = pick(A.q, l);
         const uint64_t mu = pick(A.mu, l);
+        const uint32_t b = (uint32_t)i / (uint32_t)A.M;         // G * M < 2^31 (checked on the host)
+        const uint64_t ib = i - (uint64_t)b * A.M;
         const uint32_t *dp = A.dn + i * A.ell * LN + pt;
-        const uint32_t *kp = A.evk + pt;
+        const uint32_t *kp = A.evk + b * A.evk_stride + pt;
         uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
 #pragma unroll 4
         for (uint32_t u = 0; u < A.ell; ++u) {
@@ -141,8 +149,8 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
             p0[c] = barrett64((uint64_t)subq(x0[c], S0, q) * m, q, mu);
             p1[c] = barrett64((uint64_t)subq(x1[c], S1, q) * m, q, mu);
         }
-        uint32_t *out1 = A.out + i * 2 * LN + pt;
-        uint32_t *out2 = A.out + (i + A.M) * 2 * LN + pt;
+        uint32_t *out1 = A.out + ((uint64_t)b * 2 * A.M + ib) * 2 * LN + pt;
+        uint32_t *out2 = out1 + A.M * 2 * LN;
         *reinterpret_cast<uint4 *>(out1) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
         *reinterpret_cast<uint4 *>(out1 + LN) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
         *reinterpret_cast<uint4 *>(out2) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
@@ -178,9 +186,12 @@ uint32_t inv_mod_2n(uint32_t k, uint32_t twoN) {
     return x & (twoN - 1);
 }
 
-int one_stage(pir_ctx *ctx, const uint32_t *evk, uint32_t ell, uint32_t w, uint32_t j, const uint32_t *in,
-              uint64_t M, uint32_t *out, uint32_t *ws, const ExLayout &lay, cudaStream_t st) {
-    const uint64_t LN = (uint64_t)ctx->L * ctx->N;
+// Stage j of G expansions: in [G][M], out [G][2M]; client b's key at
+// evk + b * evk_stride.
+int one_stage(pir_ctx *ctx, const uint32_t *evk, uint64_t evk_stride, uint32_t ell, uint32_t w, uint32_t j,
+              const uint32_t *in, uint64_t M, uint64_t G, uint32_t *out, uint32_t *ws, const ExLayout &lay,
+              cudaStream_t st) {
+    const uint64_t LN = (uint64_t)ctx->L * ctx->N, GM = G * M;
     uint32_t *coef = ws + lay.coef, *dig = ws + lay.dig, *dn = ws + lay.dn;
     const uint32_t k = (ctx->N >> j) + 1;
     int rc = PIR_OK;
@@ -197,21 +208,21 @@ int one_stage(pir_ctx *ctx, const uint32_t *evk, uint32_t ell, uint32_t w, uint3
             ia.ninv[l] = ctx->ninv[l];
             ia.ninv_shoup[l] = ctx->ninv_shoup[l];
         }
-        if ((M + 1) / 2 * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
-        ia.M = M;
-        expand_intt_a4096_kernel<<<(unsigned)((M + 1) / 2 * ctx->L), kT4, 0, st>>>(ia);
+        if ((GM + 1) / 2 * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
+        ia.M = GM;
+        expand_intt_a4096_kernel<<<(unsigned)((GM + 1) / 2 * ctx->L), kT4, 0, st>>>(ia);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
     } else {
-        if (cudaMemcpy2DAsync(coef, LN * 4, in + LN, 2 * LN * 4, LN * 4, M, cudaMemcpyDeviceToDevice, st) !=
+        if (cudaMemcpy2DAsync(coef, LN * 4, in + LN, 2 * LN * 4, LN * 4, GM, cudaMemcpyDeviceToDevice, st) !=
             cudaSuccess)
             return PIR_ERR_CUDA;
-        rc = pir_ntt_inv(ctx, coef, coef, M, st);
+        rc = pir_ntt_inv(ctx, coef, coef, GM, st);
         if (rc) return rc;
     }
 
-    rc = gadget_dcp_launch(ctx, gadget_dcp_args(ctx, coef, LN, dig, M, ell, w, inv_mod_2n(k, 2 * ctx->N)), st);
+    rc = gadget_dcp_launch(ctx, gadget_dcp_args(ctx, coef, LN, dig, GM, ell, w, inv_mod_2n(k, 2 * ctx->N)), st);
     if (rc) return rc;
-    rc = pir_lift_ntt(ctx, dig, dn, M * ell, st);
+    rc = pir_lift_ntt(ctx, dig, dn, GM * ell, st);
     if (rc) return rc;
 
     ExpMacArgs ma;
@@ -222,6 +233,8 @@ int one_stage(pir_ctx *ctx, const uint32_t *evk, uint32_t ell, uint32_t w, uint3
     ma.out = out;
     ma.tw = ctx->d_tw;
     ma.M = M;
+    ma.GM = GM;
+    ma.evk_stride = evk_stride;
     ma.N = ctx->N;
     ma.logN = ctx->logN;
     ma.L = ctx->L;
@@ -232,7 +245,7 @@ int one_stage(pir_ctx *ctx, const uint32_t *evk, uint32_t ell, uint32_t w, uint3
         ma.q[l] = ctx->q[l];
         ma.mu[l] = ctx->mu[l];
     }
-    expand_mac_kernel<<<(unsigned)gadget_grid(ctx, M * LN / 4), GD_THREADS, 0, st>>>(ma);
+    expand_mac_kernel<<<(unsigned)gadget_grid(ctx, GM * LN / 4), GD_THREADS, 0, st>>>(ma);
     return launch_status(cudaGetLastError());
 }
 
@@ -259,32 +272,40 @@ extern "C" int pir_expand_stage(pir_ctx *ctx, const uint32_t *evk, uint32_t ell,
     const uint64_t ctb = 2ull * ctx->L * ctx->N * 4;
     if (overlaps(in, M * ctb, out, 2 * M * ctb)) return PIR_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
-    return one_stage(ctx, evk, ell, w, j, in, M, out, static_cast<uint32_t *>(workspace), lay,
+    return one_stage(ctx, evk, 0, ell, w, j, in, M, 1, out, static_cast<uint32_t *>(workspace), lay,
                      (cudaStream_t)stream);
+}
+
+extern "C" int pir_expand_batch(pir_ctx *ctx, const uint32_t *evks, uint32_t ell, uint32_t w, uint32_t stages,
+                                const uint32_t *ct, uint64_t G, uint32_t *out, void *workspace,
+                                uint64_t workspace_bytes, void *stream) {
+    if (!ctx || !evks || !ct || !out || !workspace || stages == 0 || stages > ctx->logN) return PIR_ERR_ARG;
+    if (G == 0 || G >= (1ull << 31) >> (stages - 1)) return PIR_ERR_ARG;     // G * 2^(stages-1) < 2^31
+    if (!gadget_params_ok(ctx, ell, w)) return PIR_ERR_ARG;
+    if (!aligned16(evks) || !aligned16(ct) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
+    const uint64_t Mmax = 1ull << (stages - 1);
+    const ExLayout lay = ex_layout(ctx, G * Mmax, ell);
+    if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
+    const uint64_t ctw = 2ull * ctx->L * ctx->N;
+    if (overlaps(ct, G * ctw * 4, out, G * (2 * Mmax) * ctw * 4)) return PIR_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint32_t *ws = static_cast<uint32_t *>(workspace);
+    const uint64_t key = (uint64_t)ell * ctw;       // words of one stage's evaluation key
+    const uint64_t stride = stages * key;           // words of one client's keys
+    const uint32_t *cur = ct;
+    for (uint32_t j = 0; j < stages; ++j) {
+        const uint64_t M = 1ull << j;
+        uint32_t *dst = j + 1 == stages ? out : ws + ((j & 1) ? lay.pong : lay.ping);
+        const int rc = one_stage(ctx, evks + j * key, stride, ell, w, j, cur, M, G, dst, ws, lay, st);
+        if (rc) return rc;
+        cur = dst;
+    }
+    return PIR_OK;
 }
 
 extern "C" int pir_expand(pir_ctx *ctx, const uint32_t *evks, uint32_t ell, uint32_t w, uint32_t stages,
                           const uint32_t *ct, uint32_t *out, void *workspace, uint64_t workspace_bytes,
                           void *stream) {
-    if (!ctx || !evks || !ct || !out || !workspace || stages == 0 || stages > ctx->logN) return PIR_ERR_ARG;
-    if (!gadget_params_ok(ctx, ell, w)) return PIR_ERR_ARG;
-    if (!aligned16(evks) || !aligned16(ct) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
-    const uint64_t Mmax = 1ull << (stages - 1);
-    const ExLayout lay = ex_layout(ctx, Mmax, ell);
-    if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
-    const uint64_t ctw = 2ull * ctx->L * ctx->N;
-    if (overlaps(ct, ctw * 4, out, (2 * Mmax) * ctw * 4)) return PIR_ERR_ARG;
-    if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
-    cudaStream_t st = (cudaStream_t)stream;
-    uint32_t *ws = static_cast<uint32_t *>(workspace);
-    const uint64_t key = (uint64_t)ell * ctw;       // words of one stage's evaluation key
-    const uint32_t *cur = ct;
-    for (uint32_t j = 0; j < stages; ++j) {
-        const uint64_t M = 1ull << j;
-        uint32_t *dst = j + 1 == stages ? out : ws + ((j & 1) ? lay.pong : lay.ping);
-        const int rc = one_stage(ctx, evks + j * key, ell, w, j, cur, M, dst, ws, lay, st);
-        if (rc) return rc;
-        cur = dst;
-    }
-    return PIR_OK;
+    return pir_expand_batch(ctx, evks, ell, w, stages, ct, 1, out, workspace, workspace_bytes, stream);
 }

@@ -103,6 +103,14 @@ def lib() -> ctypes.CDLL:
         L.pir_expand.restype = ctypes.c_int
         L.pir_expand.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, _vp, _vp, _vp,
                                  ctypes.c_uint64, _vp]
+        L.pir_coltor_batch_workspace_bytes.restype = ctypes.c_uint64
+        L.pir_coltor_batch_workspace_bytes.argtypes = [_vp, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
+        L.pir_coltor_batch.restype = ctypes.c_int
+        L.pir_coltor_batch.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, ctypes.c_uint64,
+                                       ctypes.c_uint64, _vp, _vp, ctypes.c_uint64, _vp]
+        L.pir_expand_batch.restype = ctypes.c_int
+        L.pir_expand_batch.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, _vp,
+                                       ctypes.c_uint64, _vp, _vp, ctypes.c_uint64, _vp]
         L.pir_status.restype = ctypes.c_int
         L.pir_status.argtypes = [_vp, _u32p, ctypes.c_int]
         L.pir_strerror.restype = ctypes.c_char_p
@@ -295,6 +303,25 @@ def pir_coltor(ctx: Ctx, C: torch.Tensor, ell: int, w: int, cts: torch.Tensor, n
                             _stream(stream)), "pir_coltor")
 
 
+def pir_coltor_batch_workspace_bytes(ctx: Ctx, n: int, G: int, ell: int) -> int:
+    return int(lib().pir_coltor_batch_workspace_bytes(ctx, n, G, ell))
+
+
+def coltor_batch_workspace(ctx: Ctx, n: int, G: int, ell: int, device="cuda") -> torch.Tensor:
+    """A device workspace sized for pir_coltor_batch: G tournaments of n ciphertexts."""
+    return torch.empty(pir_coltor_batch_workspace_bytes(ctx, n, G, ell), dtype=torch.uint8, device=device)
+
+
+def pir_coltor_batch(ctx: Ctx, C: torch.Tensor, ell: int, w: int, cts: torch.Tensor, n: int, G: int,
+                     out: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """G tournaments of n ciphertexts each ([G][n] in, [G] out); C holds each
+    client's ceil(log2 n) stages' RGSW ciphertexts, client after client."""
+    ws = _dev_ptr(workspace, workspace.element_size(), "workspace")
+    _check(lib().pir_coltor_batch(ctx, _dev_ptr(C, 4, "C"), ell, w, _dev_ptr(cts, 4, "in"), n, G,
+                                  _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(),
+                                  _stream(stream)), "pir_coltor_batch")
+
+
 # ---------------------------------------------------------------- ExpandQuery
 def pir_expand_workspace_bytes(ctx: Ctx, M: int, ell: int) -> int:
     return int(lib().pir_expand_workspace_bytes(ctx, M, ell))
@@ -321,6 +348,17 @@ def pir_expand(ctx: Ctx, evks: torch.Tensor, ell: int, w: int, stages: int, ct: 
     _check(lib().pir_expand(ctx, _dev_ptr(evks, 4, "evks"), ell, w, stages, _dev_ptr(ct, 4, "ct"),
                             _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(),
                             _stream(stream)), "pir_expand")
+
+
+def pir_expand_batch(ctx: Ctx, evks: torch.Tensor, ell: int, w: int, stages: int, ct: torch.Tensor, G: int,
+                     out: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """G expansions ([G] query ciphertexts in, [G][2^stages] out); evks holds
+    each client's stages' keys, client after client.  The workspace is
+    expand_workspace(ctx, G * 2^(stages-1), ell)."""
+    ws = _dev_ptr(workspace, workspace.element_size(), "workspace")
+    _check(lib().pir_expand_batch(ctx, _dev_ptr(evks, 4, "evks"), ell, w, stages, _dev_ptr(ct, 4, "ct"), G,
+                                  _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(),
+                                  _stream(stream)), "pir_expand_batch")
 
 
 # ---------------------------------------------------------------- scalar scan

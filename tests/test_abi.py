@@ -86,6 +86,9 @@ def test_error_strings_and_null_ctx(lib):
     assert lib.pir_expand_workspace_bytes(None, 4, 5) == 0
     assert lib.pir_expand_stage(None, None, 5, 18, 0, None, 1, None, None, 0, None) == pir.PIR_ERR_ARG
     assert lib.pir_expand(None, None, 5, 18, 3, None, None, None, 0, None) == pir.PIR_ERR_ARG
+    assert lib.pir_coltor_batch_workspace_bytes(None, 4, 2, 5) == 0
+    assert lib.pir_coltor_batch(None, None, 5, 18, None, 4, 2, None, None, 0, None) == pir.PIR_ERR_ARG
+    assert lib.pir_expand_batch(None, None, 5, 18, 3, None, 2, None, None, 0, None) == pir.PIR_ERR_ARG
     h = ctypes.c_void_p()
     assert lib.pir_server_create(ctypes.byref(h), None, None, 1, 1, 1) == pir.PIR_ERR_ARG and not h.value
     assert lib.pir_server_submit(None, None, None, None) == pir.PIR_ERR_ARG

@@ -165,3 +165,68 @@ def test_graph_replay_matches_eager(pir):
     torch.cuda.synchronize()
     assert torch.equal(r_out, e_out)
     assert pir.pir_status(ctx) == 0
+
+
+@pytest.mark.parametrize("N,L,ell,w,n,G", [
+    (4096, 3, 5, 18, 11, 3),     # odd n: every tournament's last pair meets zero
+    (4096, 3, 5, 18, 2, 4),
+    (256, 2, 4, 15, 9, 3),       # the operation-level path (N != 4096)
+    (4096, 3, 5, 18, 1, 2),      # no stage: a copy per client
+])
+def test_batch_matches_oracle_per_client(pir, N, L, ell, w, n, G):
+    """G tournaments in one call, each with its own RGSW ciphertexts, equal
+    the oracle's tournament of each client on its own inputs."""
+    ctx, qs, psis = _setup(pir, N, L)
+    S = oracle.coltor_stages(n)
+    Cs = synth.residues(40 + n + G, (G, max(S, 1), 2 * ell, 2, L, N), qs)
+    cts = synth.residues(90 + n + G, (G, n, 2, L, N), qs)
+    out = pir.empty_u32(G * 2 * L * N)
+    out.fill_(-1)
+    C_dev = to_dev(np.ascontiguousarray(Cs[:, :S])) if S else to_dev(Cs)
+    pir.pir_coltor_batch(ctx, C_dev, ell, w, to_dev(cts), n, G, out,
+                         pir.coltor_batch_workspace(ctx, n, G, ell))
+    got = to_host_u32(out).reshape(G, 2, L, N)
+    for b in range(G):
+        assert np.array_equal(got[b], oracle.coltor(Cs[b, :max(S, 1)], cts[b], qs, psis, ell, w)), b
+    assert pir.pir_status(ctx) == 0
+
+
+def test_batch_of_16_full_size(pir):
+    """16 tournaments over 1365 ciphertexts (a 16-query RowSel output of the
+    64 GiB DB): every client equals its own single-tournament call, and the
+    last client equals the oracle."""
+    N, L, ell, w, n, G = 4096, 3, 5, 18, 1365, 16
+    ctx, qs, psis = _setup(pir, N, L)
+    S = oracle.coltor_stages(n)
+    P = L * N
+    Cs = synth.residues(61, (G, S, 2 * ell, 2, L, N), qs)
+    cts = synth.residues(62, (G, n, 2, L, N), qs)
+    C_dev, cts_dev = to_dev(Cs).reshape(-1), to_dev(cts).reshape(-1)      # flat, sliced per client
+    out = pir.empty_u32(G * 2 * P)
+    pir.pir_coltor_batch(ctx, C_dev, ell, w, cts_dev, n, G, out, pir.coltor_batch_workspace(ctx, n, G, ell))
+    got = to_host_u32(out).reshape(G, 2, L, N)
+    ws = pir.coltor_workspace(ctx, n, ell)
+    one = pir.empty_u32(2 * P)
+    for b in range(G):
+        pir.pir_coltor(ctx, C_dev[b * S * 2 * ell * 2 * P:(b + 1) * S * 2 * ell * 2 * P], ell, w,
+                       cts_dev[b * n * 2 * P:(b + 1) * n * 2 * P], n, one, ws)
+        assert np.array_equal(got[b], to_host_u32(one).reshape(2, L, N)), b
+    assert np.array_equal(got[G - 1], oracle.coltor(Cs[G - 1], cts[G - 1], qs, psis, ell, w))
+    assert pir.pir_status(ctx) == 0
+
+
+def test_batch_rejects_bad_arguments(pir):
+    N, L = 64, 3
+    ctx, qs, _ = _setup(pir, N, L)
+    C = pir.empty_u32(2 * 10 * 2 * L * N)
+    cts = pir.empty_u32(2 * 4 * 2 * L * N)
+    out = pir.empty_u32(2 * 2 * L * N)
+    ws = pir.coltor_batch_workspace(ctx, 4, 2, 5)
+    with pytest.raises(pir.PirError):                 # G = 0
+        pir.pir_coltor_batch(ctx, C, 5, 18, cts, 4, 0, out, ws)
+    with pytest.raises(pir.PirError):                 # workspace for one tournament only
+        pir.pir_coltor_batch(ctx, C, 5, 18, cts, 4, 2, out, pir.coltor_workspace(ctx, 4, 5))
+    with pytest.raises(pir.PirError):                 # out overlaps in
+        pir.pir_coltor_batch(ctx, C, 5, 18, cts, 4, 2, cts[8 * L * N:], ws)
+    assert pir.pir_coltor_batch_workspace_bytes(ctx, 4, 0, 5) == 0
+    assert pir.pir_coltor_batch_workspace_bytes(ctx, 4, 1, 5) == pir.pir_coltor_workspace_bytes(ctx, 4, 5)

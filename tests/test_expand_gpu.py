@@ -118,3 +118,56 @@ def test_expand_rejects_bad_arguments(pir):
     with pytest.raises(pir.PirError):                 # out overlaps in
         pir.pir_expand_stage(ctx, evk, 5, 18, 0, cts, 2, cts, ws)
     assert pir.pir_expand_workspace_bytes(ctx, 0, 5) == 0
+
+
+@pytest.mark.parametrize("N,L,S,G", [(4096, 3, 3, 3), (4096, 3, 1, 4), (256, 2, 4, 3)])
+def test_batch_matches_oracle_per_client(pir, N, L, S, G):
+    """G expansions in one call, each with its own query and keys, equal the
+    oracle's expansion of each client; client b's outputs are contiguous."""
+    ell, w = (5, 18) if L == 3 else (4, 15)
+    ctx, qs, psis = _setup(pir, N, L)
+    evks = synth.residues(130 + S + G, (G, S, ell, 2, L, N), qs)
+    cts = synth.residues(140 + S + G, (G, 2, L, N), qs)
+    out = pir.empty_u32(G * (1 << S) * 2 * L * N)
+    out.fill_(-1)
+    pir.pir_expand_batch(ctx, to_dev(evks), ell, w, S, to_dev(cts), G, out,
+                         pir.expand_workspace(ctx, G << (S - 1), ell))
+    got = to_host_u32(out).reshape(G, 1 << S, 2, L, N)
+    for b in range(G):
+        assert np.array_equal(got[b], oracle.expand(evks[b], cts[b], S, qs, psis, ell, w)), b
+    assert pir.pir_status(ctx) == 0
+
+
+def test_batch_of_16_full_size(pir):
+    """16 expansions into 1024 ciphertexts each (the RowSel input of 16
+    queries over the 64 GiB DB): every client equals its own single call, the
+    last client equals the oracle."""
+    N, L, ell, w, S, G = 4096, 3, 5, 18, 10, 16
+    ctx, qs, psis = _setup(pir, N, L)
+    P = L * N
+    evks = synth.residues(150, (G, S, ell, 2, L, N), qs)
+    cts = synth.residues(151, (G, 2, L, N), qs)
+    e_dev, c_dev = to_dev(evks).reshape(-1), to_dev(cts).reshape(-1)      # flat, sliced per client
+    out = pir.empty_u32(G * (1 << S) * 2 * P)
+    pir.pir_expand_batch(ctx, e_dev, ell, w, S, c_dev, G, out, pir.expand_workspace(ctx, G << (S - 1), ell))
+    ws = pir.expand_workspace(ctx, 1 << (S - 1), ell)
+    one = pir.empty_u32((1 << S) * 2 * P)
+    for b in range(G):
+        pir.pir_expand(ctx, e_dev[b * S * ell * 2 * P:(b + 1) * S * ell * 2 * P], ell, w, S,
+                       c_dev[b * 2 * P:(b + 1) * 2 * P], one, ws)
+        assert bool((out[b * (1 << S) * 2 * P:(b + 1) * (1 << S) * 2 * P] == one).all()), b
+    got = to_host_u32(out[(G - 1) * (1 << S) * 2 * P:]).reshape(1 << S, 2, L, N)
+    assert np.array_equal(got, oracle.expand(evks[G - 1], cts[G - 1], S, qs, psis, ell, w))
+    assert pir.pir_status(ctx) == 0
+
+
+def test_batch_rejects_bad_arguments(pir):
+    N, L = 64, 3
+    ctx, qs, _ = _setup(pir, N, L)
+    evks = pir.empty_u32(2 * 3 * 5 * 2 * L * N)
+    cts = pir.empty_u32(2 * 2 * L * N)
+    out = pir.empty_u32(2 * 8 * 2 * L * N)
+    with pytest.raises(pir.PirError):                 # G = 0
+        pir.pir_expand_batch(ctx, evks, 5, 18, 3, cts, 0, out, pir.expand_workspace(ctx, 8, 5))
+    with pytest.raises(pir.PirError):                 # workspace for one expansion only
+        pir.pir_expand_batch(ctx, evks, 5, 18, 3, cts, 2, out, pir.expand_workspace(ctx, 4, 5))

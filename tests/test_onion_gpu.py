@@ -76,9 +76,9 @@ def test_query_returns_the_selected_record(pir, D0, D1, istar, jstar):
 
 def test_batch_of_clients_on_the_tensor_path(pir):
     """Ten clients, each with its own secret, keys, record and column, served
-    together: ten expansions, one RowSel pass of B = 10 queries (the tensor
-    cores: primes >= 2^26, 8 < B <= 16) and ten tournaments.  Every answer
-    decrypts under its own client's secret to 2^S DB[i*_b][j*_b]."""
+    together: one batched expansion, one RowSel pass of B = 10 queries (the
+    tensor cores: primes >= 2^26, 8 < B <= 16) and one batched tournament.
+    Every answer decrypts under its own client's secret to 2^S DB[i*_b][j*_b]."""
     N, L, ell, w, D0, D1, B = 4096, 3, 5, 18, 16, 11, 10
     S, T = 4, oracle.coltor_stages(D1)
     qs = oracle.primes(N, L)
@@ -87,25 +87,25 @@ def test_batch_of_clients_on_the_tensor_path(pir):
     db = pir.empty_u32(pir.pir_db_bytes(ctx, D0, D1) // 4)
     pir.pir_db_encode(ctx, to_dev(raw), 0, D0, D0, D1, db)
     P = L * N
-    expanded = pir.empty_u32(B * D0 * 2 * P)
-    ws_e = pir.expand_workspace(ctx, D0 // 2, ell)
-    clients = []
+    clients, queries, evks, rgsws = [], [], [], []
     for b in range(B):
         K = Keys(N, L, ell, w, seed=500 + b)
         istar, jstar = (5 * b + 3) % D0, (7 * b + 2) % D1
         mono = np.zeros(N, dtype=np.int64)
         mono[istar] = 1
-        evks = np.stack([K.evk(N // (1 << j) + 1) for j in range(S)])
-        rgsw = np.stack([_rgsw(K, (jstar >> s) & 1) for s in range(T)])
-        pir.pir_expand(ctx, to_dev(evks), ell, w, S, to_dev(K.encrypt(_signed(mono, K.qs))),
-                       expanded[b * D0 * 2 * P:(b + 1) * D0 * 2 * P], ws_e)
-        clients.append((K, istar, jstar, rgsw))
+        queries.append(K.encrypt(_signed(mono, K.qs)))
+        evks.append(np.stack([K.evk(N // (1 << j) + 1) for j in range(S)]))
+        rgsws.append(np.stack([_rgsw(K, (jstar >> s) & 1) for s in range(T)]))
+        clients.append((K, istar, jstar))
+    expanded = pir.empty_u32(B * D0 * 2 * P)
+    pir.pir_expand_batch(ctx, to_dev(np.stack(evks)), ell, w, S, to_dev(np.stack(queries)), B, expanded,
+                         pir.expand_workspace(ctx, B * D0 // 2, ell))
     cols = pir.empty_u32(B * D1 * 2 * P)
     pir.pir_rowsel(ctx, db, D0, D1, expanded, B, cols, pir.rowsel_workspace(ctx, D0, D1, B))
-    ws_c = pir.coltor_workspace(ctx, D1, ell)
-    for b, (K, istar, jstar, rgsw) in enumerate(clients):
-        answer = pir.empty_u32(2 * P)
-        pir.pir_coltor(ctx, to_dev(rgsw), ell, w, cols[b * D1 * 2 * P:(b + 1) * D1 * 2 * P], D1, answer, ws_c)
-        got = K.decrypt(to_host_u32(answer).reshape(2, L, N))
-        assert np.array_equal(got, _signed(raw[istar, jstar].astype(np.int64) << S, K.qs)), b
+    answers = pir.empty_u32(B * 2 * P)
+    pir.pir_coltor_batch(ctx, to_dev(np.stack(rgsws)), ell, w, cols, D1, B, answers,
+                         pir.coltor_batch_workspace(ctx, D1, B, ell))
     assert pir.pir_status(ctx) == 0
+    got = to_host_u32(answers).reshape(B, 2, L, N)
+    for b, (K, istar, jstar) in enumerate(clients):
+        assert np.array_equal(K.decrypt(got[b]), _signed(raw[istar, jstar].astype(np.int64) << S, K.qs)), b
