@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
     const uint32_t *src = in + (LIFT ? row / P.L : row) * kN4;
     uint32_t *dst = out + row * kN4;
     const uint32_t t = threadIdx.x;
+    const Swz4096 z(t);       // shared-memory placement of the row
     uint32_t x[16];
     if (FWD) {
         // round 0: stages 0-3, distance 256, elements t + 256 i
@@ -77,22 +78,18 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
         for (int i = 0; i < 16; ++i) x[i] = LIFT ? src[t + 256 * i] % q : src[t + 256 * i];
         fwd_round16(x, 0, 0, W, Wp, q);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sm[t + 256 * i] = x[i];
+        for (int i = 0; i < 16; ++i) sm[z.col(i)] = x[i];
         __syncthreads();
         // round 1: stages 4-7, distance 16, elements (t>>4)*256 + (t&15) + 16 i
-        const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = sm[g1 + 16 * i];
+        for (int i = 0; i < 16; ++i) x[i] = sm[z.mid(i)];
         fwd_round16(x, 4, t >> 4, W, Wp, q);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sm[g1 + 16 * i] = x[i];
+        for (int i = 0; i < 16; ++i) sm[z.mid(i)] = x[i];
         __syncthreads();
         // round 2: stages 8-11, distance 1, elements 16t .. 16t+15
 #pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(sm + 16 * t + i);
-            x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
-        }
+        for (int i = 0; i < 16; ++i) x[i] = sm[z.row(i)];
         fwd_round16(x, 8, t, W, Wp, q);
 #pragma unroll
         for (int i = 0; i < 16; i += 4)
@@ -107,20 +104,18 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
         }
         inv_round16(x, 11, t, W, Wp, q);
 #pragma unroll
-        for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<uint4 *>(sm + 16 * t + i) = make_uint4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+        for (int i = 0; i < 16; ++i) sm[z.row(i)] = x[i];
         __syncthreads();
         // round 1: stages 7-4, distance 16
-        const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = sm[g1 + 16 * i];
+        for (int i = 0; i < 16; ++i) x[i] = sm[z.mid(i)];
         inv_round16(x, 7, t >> 4, W, Wp, q);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sm[g1 + 16 * i] = x[i];
+        for (int i = 0; i < 16; ++i) sm[z.mid(i)] = x[i];
         __syncthreads();
         // round 2: stages 3-0, distance 256, elements t + 256 i; then N^-1
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = sm[t + 256 * i];
+        for (int i = 0; i < 16; ++i) x[i] = sm[z.col(i)];
         inv_round16(x, 3, 0, W, Wp, q);
         const uint32_t ni = P.ninv[l], nis = P.ninv_shoup[l];
 #pragma unroll
@@ -131,7 +126,7 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
 // Forward (and lift + forward) for N = 4096 on two rows of the same prime
 // per CTA, rows 2pp*L + l and (2pp+1)*L + l: every twiddle load serves both
 // rows and each thread carries two independent butterfly chains.  Rounds as
-// in ntt4096_kernel.
+// in ntt4096_kernel; rows placed in shared memory by Swz4096.
 template <bool LIFT>
 __global__ void __launch_bounds__(kT4) ntt4096x2_fwd_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                             uint64_t cnt, const __grid_constant__ RnsParams P) {
@@ -156,32 +151,30 @@ __global__ void __launch_bounds__(kT4) ntt4096x2_fwd_kernel(const uint32_t *__re
         x[i] = LIFT ? a % q : a;
         y[i] = LIFT ? b % q : b;
     }
+    const Swz4096 z(t);
     fwd_round16x2(x, y, 0, 0, W, Wp, q);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        sa[t + 256 * i] = x[i];
-        sb[t + 256 * i] = y[i];
+        sa[z.col(i)] = x[i];
+        sb[z.col(i)] = y[i];
     }
     __syncthreads();
-    const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        x[i] = sa[g1 + 16 * i];
-        y[i] = sb[g1 + 16 * i];
+        x[i] = sa[z.mid(i)];
+        y[i] = sb[z.mid(i)];
     }
     fwd_round16x2(x, y, 4, t >> 4, W, Wp, q);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        sa[g1 + 16 * i] = x[i];
-        sb[g1 + 16 * i] = y[i];
+        sa[z.mid(i)] = x[i];
+        sb[z.mid(i)] = y[i];
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 16; i += 4) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(sa + 16 * t + i);
-        const uint4 v = *reinterpret_cast<const uint4 *>(sb + 16 * t + i);
-        x[i] = u.x; x[i + 1] = u.y; x[i + 2] = u.z; x[i + 3] = u.w;
-        y[i] = v.x; y[i + 1] = v.y; y[i + 2] = v.z; y[i + 3] = v.w;
+    for (int i = 0; i < 16; ++i) {
+        x[i] = sa[z.row(i)];
+        y[i] = sb[z.row(i)];
     }
     fwd_round16x2(x, y, 8, t, W, Wp, q);
 #pragma unroll

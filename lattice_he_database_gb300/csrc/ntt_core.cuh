@@ -151,9 +151,33 @@ __device__ __forceinline__ uint32_t inv_final(uint32_t x, uint32_t ninv, uint32_
 // The first round reads its 16 elements straight from global memory
 // (coalesced: element t + 256 i for the forward, 16t .. 16t+15 for the
 // inverse) and the last round writes straight back, so a row crosses shared
-// memory only twice.  Early-round twiddles are the same for all threads of a
+// memory only twice; in shared memory it is placed by Swz4096 (below).  Early-round twiddles are the same for all threads of a
 // warp (broadcast loads); the butterflies are branch-free.
 constexpr int kN4 = 4096, kT4 = 256;
+
+// Placement of a 4096-point row in shared memory.  With a = 256 hi + 16 mid
+// + lo (4-bit digits), element a sits at
+//     256 hi + 16 (mid ^ (hi & 1)) + (lo ^ mid),
+// a bijection under which each access pattern of the three radix-16 rounds,
+// over the 32 threads t of a warp, hits 32 distinct banks:
+//     t + 256 i                    at e_(i & 1) + 256 i     (col)
+//     256 (t>>4) + (t&15) + 16 i   at b1 ^ 17 i             (mid)
+//     16 t + i                     at b2 ^ i                (row)
+// (in natural placement the second pattern is a 2-way and the vectorised
+// third a 4-way bank conflict).
+struct Swz4096 {
+    uint32_t e0, e1, b1, b2;
+    __device__ __forceinline__ explicit Swz4096(uint32_t t) {
+        const uint32_t hi = t >> 4, lo = t & 15;
+        e0 = (hi << 4) | (lo ^ hi);
+        e1 = ((hi ^ 1) << 4) | (lo ^ hi);
+        b1 = (hi << 8) | ((hi & 1) << 4) | lo;
+        b2 = (hi << 8) | ((lo ^ (hi & 1)) << 4) | lo;
+    }
+    __device__ __forceinline__ uint32_t col(int i) const { return ((i & 1) ? e1 : e0) + 256u * (uint32_t)i; }
+    __device__ __forceinline__ uint32_t mid(int i) const { return b1 ^ (17u * (uint32_t)i); }
+    __device__ __forceinline__ uint32_t row(int i) const { return b2 ^ (uint32_t)i; }
+};
 
 __device__ __forceinline__ uint32_t umin32(uint32_t a, uint32_t b) { return a < b ? a : b; }
 
@@ -263,30 +287,30 @@ __device__ __forceinline__ void inv4096x2_rounds(uint32_t (&x)[16], uint32_t (&y
                                                  uint32_t q, uint32_t ni, uint32_t nis, uint32_t *dst0, uint32_t *dst1,
                                                  bool two) {
     const uint32_t t = threadIdx.x;
+    const Swz4096 z(t);
     inv_round16x2(x, y, 11, t, W, Wp, q);
 #pragma unroll
-    for (int k = 0; k < 16; k += 4) {
-        *reinterpret_cast<uint4 *>(sa + 16 * t + k) = make_uint4(x[k], x[k + 1], x[k + 2], x[k + 3]);
-        *reinterpret_cast<uint4 *>(sb + 16 * t + k) = make_uint4(y[k], y[k + 1], y[k + 2], y[k + 3]);
+    for (int k = 0; k < 16; ++k) {
+        sa[z.row(k)] = x[k];
+        sb[z.row(k)] = y[k];
     }
     __syncthreads();
-    const uint32_t g1 = ((t >> 4) << 8) | (t & 15);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        x[k] = sa[g1 + 16 * k];
-        y[k] = sb[g1 + 16 * k];
+        x[k] = sa[z.mid(k)];
+        y[k] = sb[z.mid(k)];
     }
     inv_round16x2(x, y, 7, t >> 4, W, Wp, q);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        sa[g1 + 16 * k] = x[k];
-        sb[g1 + 16 * k] = y[k];
+        sa[z.mid(k)] = x[k];
+        sb[z.mid(k)] = y[k];
     }
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        x[k] = sa[t + 256 * k];
-        y[k] = sb[t + 256 * k];
+        x[k] = sa[z.col(k)];
+        y[k] = sb[z.col(k)];
     }
     inv_round16x2(x, y, 3, 0, W, Wp, q);
 #pragma unroll
