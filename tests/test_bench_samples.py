@@ -60,3 +60,29 @@ def test_coltor_sample_bounded(monkeypatch, threads):
     cfg = bench.WORKLOADS["coltor_1365"]
     pairs = max(1, min((cfg["n"] + 1) // 2, threads))
     assert pairs <= 288 and 2 * pairs * 2 * cfg["L"] * cfg["N"] * 4 < 300 * 1024 * 1024
+
+
+def test_launch_counts_of_the_workloads():
+    """The bench's gpu_launches claim per step, counted by hand from the
+    library's call structure: a RowSel pass is three launches (query
+    transpose, scan, result transpose), a coefficient-form query adds its NTT
+    and the result INTT, an expansion or tournament stage is four launches
+    (INTT, decomposition, lift + NTT, MAC), ring packing adds the lift + NTT
+    of G.  Batched expansions and tournaments launch per stage, not per
+    client."""
+    import bench
+    W = bench.WORKLOADS
+    assert bench.launches_per_step(W["rowsel_64g"]) == 3 + 2
+    assert bench.launches_per_step(W["rowsel_24g_b16"]) == 3            # one pass of 16 on the tensor cores
+    assert bench.launches_per_step(W["expand_1024"]) == 4 * 10
+    assert bench.launches_per_step(W["coltor_1365"]) == 4 * 11
+    assert bench.launches_per_step(W["onion_64g"]) == 4 * 10 + 3 + 4 * 11
+    assert bench.launches_per_step(W["onion_64g_b16"]) == 4 * 10 + 3 + 4 * 11
+    assert bench.launches_per_step(W["exppack_15g"]) == 3 + 1
+    # pass planning: 16 per pass on the tensor cores while more than 8 remain,
+    # then the CUDA cores (16 queries fit the on-chip slice for D0 <= 896)
+    assert bench.rowsel_passes(1024, 16) == 1
+    assert bench.rowsel_passes(1024, 17) == 2
+    assert bench.rowsel_passes(600, 40) == 3          # 16 + 16 + 8
+    assert bench.rowsel_passes(512, 8) == 1           # CUDA cores, 8 of 16
+    assert bench.rowsel_passes(4096, 8) == 4          # D0 = 4096: 4 polynomials (2 queries) per CUDA-core pass
