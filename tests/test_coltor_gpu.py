@@ -3,9 +3,10 @@ tournament stages) against the oracle, bit-exact.
 
 Random RGSW rows and ciphertexts (seeded residues) at several ring sizes and
 gadget shapes, odd ciphertext counts (the missing partner is zero), stages
-small enough for the operation-level kernels and large enough for the fused
-stage-level kernel (N = 4096), the whole tournament, the 1365-ciphertext list one 64 GiB RowSel query produces, and the
-noise-free selection of ct[j*] at that size.
+of a few pairs and of several hundred (grids past one CTA per SM), the whole
+tournament, the 1365-ciphertext list one 64 GiB RowSel query produces, the
+noise-free selection of ct[j*] at that size, and batches of tournaments
+(one per client) in one call.
 """
 import numpy as np
 import pytest
@@ -47,7 +48,7 @@ def _trivial_rgsw(bit, qs, N, ell, w):
     (256, 2, 4, 15, 9),
     (64, 1, 1, 29, 5),        # one prime, one digit: Dcp is the identity
     (16, 2, 16, 4, 3),        # many narrow digits (the top ones zero)
-    # enough pairs for one CTA per SM: the stage-level (fused) kernel
+    # several hundred pairs: grids past one CTA per SM
     (4096, 3, 5, 18, 333),    # odd count
     (4096, 3, 3, 29, 400),
     (4096, 2, 4, 15, 400),
