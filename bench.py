@@ -356,17 +356,70 @@ class ExpandSample:
                             threads=self.threads)
 
 
+class OnionSample:
+    """Oracle OnionPIR path, composed from bounded samples of its three
+    phases (ExpandQuery, RowSel over all D0 rows for the B queries, ColTor):
+    a call runs one call of each phase's sample and times it; a query costs
+    the sum over the phases of (time per call) / (queries per call), where a
+    call covers the fraction of a query's expansion, DB scan or tournament
+    its sample performs."""
+    unit = "queries/s"
+
+    def __init__(self, cfg):
+        N, L, D0, D1, ell, w = cfg["N"], cfg["L"], cfg["D0"], cfg["D1"], cfg["ell"], cfg["w"]
+        B = cfg.get("B", 1)
+        S = D0.bit_length() - 1
+        self.phases = [
+            ExpandSample(dict(N=N, L=L, stages=S, ell=ell, w=w)),
+            RowselSample(dict(N=N, L=L, D0=D0, D1=D1, B=B)),
+            ColtorSample(dict(N=N, L=L, n=D1, ell=ell, w=w)),
+        ]
+        r = self.phases[1]
+        # queries per call: expansions or tournaments per call, or the scanned
+        # fraction of the DB times the B queries the scan serves
+        self.per_call = [self.phases[0].nbytes, r.nbytes / (D0 * D1 * L * N * 4) * B, self.phases[2].nbytes]
+        self.threads = r.threads
+        self.nbytes = 0.0
+        self.reset()
+        self.desc = "oracle OnionPIR path per query, composed of: " + "; ".join(x.desc for x in self.phases)
+
+    def reset(self):
+        self.spent = [0.0, 0.0, 0.0]
+        self.calls = 0
+
+    def __call__(self):
+        for i, ph in enumerate(self.phases):
+            t = time.perf_counter()
+            ph()
+            self.spent[i] += time.perf_counter() - t
+        self.calls += 1
+
+    def queries_per_s(self) -> float:
+        per_query = sum(t / max(1, self.calls) / q for t, q in zip(self.spent, self.per_call))
+        return 1.0 / per_query
+
+
 def _rate(sample, units_per_s: float):
     """A sample's rate in its metric unit (GB/s unless the sample says otherwise)."""
     unit = getattr(sample, "unit", "GB/s")
     return (units_per_s / 1e9 if unit == "GB/s" else units_per_s), unit
 
 
+def _sample_rate(sample, calls: int, dt: float):
+    """Rate of `calls` calls of a sample taking dt seconds in its metric unit;
+    a composed sample reports its own."""
+    if hasattr(sample, "queries_per_s"):
+        return sample.queries_per_s(), sample.unit
+    return _rate(sample, sample.nbytes * calls / dt)
+
+
 def oracle_baseline(sample, seconds: float):
     """cpu_baseline object: the sample repeated for about `seconds`."""
     sample()                                   # first touch of the inputs
+    if hasattr(sample, "reset"):
+        sample.reset()
     calls, dt = repeat_for(sample, seconds)
-    value, unit = _rate(sample, sample.nbytes * calls / dt)
+    value, unit = _sample_rate(sample, calls, dt)
     return {"value": value, "unit": unit, "cores": sample.threads, "kind": "oracle",
             "sample": "%s; %d calls in %.1f s" % (sample.desc, calls, dt), "seconds": round(dt, 2)}
 
@@ -383,11 +436,13 @@ def run_reference_sample(args, sample, metric, dtype, data, desc):
 
     for _ in range(args.warmup):
         one_step()
+    if hasattr(sample, "reset"):
+        sample.reset()
     t = time.perf_counter()
     for _ in range(args.steps):
         one_step()
     dt = (time.perf_counter() - t) / max(1, args.steps)
-    value, unit = _rate(sample, sample.nbytes * reps / dt)
+    value, unit = _sample_rate(sample, reps * args.steps, dt * args.steps)
     line = {
         "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": 0, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -418,9 +473,8 @@ def run_reference(args, cfg):
         run_reference_sample(args, ExpandSample(cfg), EXPAND_METRIC, "u32",
                              "synthetic (seeded SplitMix64 residues)", cfg["desc"])
     elif kind == "onion":
-        print(json.dumps({"impl": "reference", "unavailable": "the composed OnionPIR path has no single oracle "
-                          "sample; its three phases have reference lines of their own (expand_1024, rowsel_64g, "
-                          "coltor_1365)"}), flush=True)
+        run_reference_sample(args, OnionSample(cfg), ONION_METRIC, "u32", "synthetic (seeded SplitMix64 residues)",
+                             cfg["desc"])
     else:
         run_reference_sample(args, RowselSample(cfg), METRIC, "u32", "synthetic (seeded SplitMix64 residues)",
                              cfg["desc"])
@@ -1212,6 +1266,8 @@ def run_onion(args, cfg):
             "gpu_launches": args.steps * launches_per_step(cfg),
             "cpu_baseline": None,
         }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = oracle_baseline(OnionSample(cfg), args.cpu_seconds)
         print(json.dumps(line), flush=True)
         result = line
     ctx.close()

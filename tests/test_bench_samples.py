@@ -86,3 +86,24 @@ def test_launch_counts_of_the_workloads():
     assert bench.rowsel_passes(600, 40) == 3          # 16 + 16 + 8
     assert bench.rowsel_passes(512, 8) == 1           # CUDA cores, 8 of 16
     assert bench.rowsel_passes(4096, 8) == 4          # D0 = 4096: 4 polynomials (2 queries) per CUDA-core pass
+
+
+def test_onion_sample_composes_the_phases(monkeypatch):
+    """The composed OnionPIR sample: each phase covers the fraction of a
+    query its sample performs (expansions and tournaments per call, the
+    scanned fraction of the DB times B), and a query costs the sum of each
+    phase's time per call over its queries per call."""
+    monkeypatch.setattr(oracle, "default_threads", lambda: 2)
+    N, L, D0, D1, B = 64, 3, 16, 11, 2
+    on = bench.OnionSample(dict(N=N, L=L, D0=D0, D1=D1, ell=5, w=18, B=B))
+    e, r, c = on.phases
+    assert abs(on.per_call[0] - 2 / 15) < 1e-12                # 2 of the 15 Subs of a 16-way expansion
+    assert abs(on.per_call[1] - r.nbytes / (D0 * D1 * L * N * 4) * B) < 1e-12
+    assert abs(on.per_call[2] - 2 / 10) < 1e-12                # 2 of the 10 external products
+    on()
+    on()
+    assert on.calls == 2 and all(t > 0 for t in on.spent)
+    want = 1.0 / sum(t / 2 / q for t, q in zip(on.spent, on.per_call))
+    assert abs(on.queries_per_s() - want) < 1e-9 * want
+    line = bench.oracle_baseline(on, 0.05)
+    assert line["unit"] == "queries/s" and line["value"] > 0 and line["cores"] == 2
