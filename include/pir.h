@@ -252,7 +252,7 @@ int pir_exppack(pir_ctx *ctx, const uint32_t *h_db, uint32_t n, uint32_t Dr, con
  *   workspace : device, >= pir_coltor_workspace_bytes(ctx, n, ell) bytes,
  *          16-byte aligned; contents undefined after the call.
  * The library owns nothing the caller passes; calls are asynchronous on
- * stream.  Errors: PIR_ERR_ARG (NULL/unaligned pointers, n = 0 or > 2^32,
+ * stream.  Errors: PIR_ERR_ARG (NULL/unaligned pointers, n = 0 or ceil(n/2) >= 2^31,
  * ell or w out of range, digits not covering Q, workspace too small,
  * in/out overlap), PIR_ERR_CUDA.
  */
