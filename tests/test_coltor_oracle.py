@@ -11,7 +11,8 @@ product, tournament stage) against facts that do not come from the oracle:
   odd ones (a missing partner counts as zero); the whole tournament with the
   bits of j* returns ct[j*];
 * on tiny rings the product equals a brute-force evaluation: big-integer
-  CRT digits, the O(N^2) NTT definition and the point-wise sums;
+  CRT digits, the O(N^2) NTT definition and the point-wise sums (two and
+  four primes);
 * the product is linear in C.
 
 GPIR sections 2-3 (ColTor, Dcp, l = 5) and VIPIR 3.6 step 7 / section 5
@@ -153,8 +154,9 @@ def test_tournament_returns_the_selected_ciphertext(n, jstar):
     assert np.array_equal(oracle.coltor(Cs, cts, qs, psis, ell, w), cts[jstar])
 
 
-def test_ext_product_brute_force_tiny():
-    N, L, ell, w = 16, 2, 4, 15
+@pytest.mark.parametrize("L,ell,w", [(2, 4, 15), (4, 6, 20)])   # four primes: Q ~ 2^116, Q/q_l above 2^64
+def test_ext_product_brute_force_tiny(L, ell, w):
+    N = 16
     qs, psis = _setup(N, L)
     Q = _Q(qs)
     assert Q.bit_length() <= ell * w

@@ -13,6 +13,10 @@ against facts that do not come from the oracle:
 * after S expansion stages, ciphertext r decrypts to
   2^S * sum_{t = r mod 2^S} m_t X^(t - r): each output carries its own
   coefficient of the query plaintext (the tree's defining property).
+* with random keys and ciphertexts on a 16-point ring, Subs and whole
+  expansion stages equal the definitions evaluated with Python integers
+  (O(N^2) NTT and inverse, the automorphism written out, big-integer CRT
+  digits), up to four primes (Q/q_l above 2^64).
 
 GPIR sections 2-3 (ExpandQuery, Subs, evk; Subs decomposes only the a
 polynomial) are the passages the oracle follows.
@@ -158,3 +162,77 @@ def test_expansion_separates_the_coefficients(N, S, support):
         for t in range(r, N, 1 << S):
             want[t - r] = coeffs[t] << S
         assert np.array_equal(K.decrypt(out[r]), _signed(want, K.qs)), r
+
+
+def _subs_brute(evk, ct, k, qs, psis, ell, w):
+    """Subs(ct, k) on a tiny ring from the definitions: the O(N^2) inverse and
+    forward NTT, the automorphism as t -> t k mod 2N with X^N = -1 written
+    out, big-integer CRT digits, point-wise sums."""
+    L, N = ct.shape[1], ct.shape[2]
+    Q = 1
+    for q in qs:
+        Q *= q
+    basis = [(Q // q) * pow(Q // q, -1, q) for q in qs]
+
+    def coef(poly):            # [L][N] NTT form -> [L][N] Python ints, coefficient form
+        return [[int(v) for v in oracle.intt_direct(poly[l], q, psis[l])] for l, q in enumerate(qs)]
+
+    def sigma(c):              # coefficient form, per prime
+        out = [[0] * N for _ in qs]
+        for l, q in enumerate(qs):
+            for t in range(N):
+                e = t * k % (2 * N)
+                if e < N:
+                    out[l][e] = (out[l][e] + c[l][t]) % q
+                else:
+                    out[l][e - N] = (out[l][e - N] - c[l][t]) % q
+        return out
+
+    def ntt(c):                # [L][N] ints -> [L][N] uint32, NTT form
+        return np.stack([oracle.ntt_direct(np.array(c[l], dtype=np.uint32), q, psis[l]) for l, q in enumerate(qs)])
+
+    s0, s1 = sigma(coef(ct[0])), sigma(coef(ct[1]))
+    X = [sum(s1[l][t] * basis[l] for l in range(L)) % Q for t in range(N)]
+    acc = np.zeros((2, L, N), dtype=object)
+    for u in range(ell):
+        d = [(x >> (w * u)) & ((1 << w) - 1) for x in X]
+        dn = ntt([[v % q for v in d] for q in qs]).astype(object)
+        for c in range(2):
+            acc[c] += dn * evk[u, c].astype(object)
+    acc[0] += ntt(s0).astype(object)
+    for l, q in enumerate(qs):
+        acc[:, l] %= q
+    return acc.astype(np.uint32)
+
+
+@pytest.mark.parametrize("L,ell,w,k", [(2, 4, 15, 17), (2, 4, 15, 5), (3, 5, 18, 9), (4, 6, 20, 31)])
+def test_subs_brute_force_tiny(L, ell, w, k):
+    """Random (not noise-free) keys and ciphertexts: the oracle's Subs equals
+    the definitions evaluated with Python integers."""
+    N = 16
+    qs, psis = _setup(N, L)
+    rng = np.random.default_rng(L * 100 + k)
+    evk = _rand(rng, qs, N, (ell, 2))
+    ct = _rand(rng, qs, N, (2,))
+    assert np.array_equal(oracle.subs(evk, ct, k, qs, psis, ell, w), _subs_brute(evk, ct, k, qs, psis, ell, w))
+
+
+@pytest.mark.parametrize("j,M", [(0, 1), (1, 3), (3, 2)])
+def test_expand_stage_brute_force_tiny(j, M):
+    """Stage j over M random ciphertexts: out[i] = ct_i + Subs(ct_i, N/2^j + 1)
+    and out[i + M] = (ct_i - Subs) . NTT(X^(-2^j)), with X^(-2^j) written out
+    as -X^(N - 2^j) and transformed by the O(N^2) definition."""
+    N, L, ell, w = 16, 2, 4, 15
+    qs, psis = _setup(N, L)
+    rng = np.random.default_rng(10 * j + M)
+    evk = _rand(rng, qs, N, (ell, 2))
+    cts = _rand(rng, qs, N, (M, 2))
+    k = N // (1 << j) + 1
+    mono = np.stack([oracle.ntt_direct(np.array([0] * (N - (1 << j)) + [q - 1] + [0] * ((1 << j) - 1),
+                                                dtype=np.uint32), q, psis[l]) for l, q in enumerate(qs)])
+    got = oracle.expand_stage(evk, cts, j, qs, psis, ell, w)
+    for i in range(M):
+        S = _subs_brute(evk, cts[i], k, qs, psis, ell, w)
+        assert np.array_equal(got[i], _add(cts[i], S, qs)), i
+        diff = _sub(cts[i], S, qs)
+        assert np.array_equal(got[i + M], np.stack([_mul(diff[c], mono, qs) for c in range(2)])), i
