@@ -141,17 +141,23 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def profile_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary of `kernel`, if any."""
-    path = os.path.join(ROOT, "profiles", "%s.md" % kernel)
+def profile_traffic(kernel: str) -> dict:
+    """DRAM bytes per launch from the committed ncu summary of `kernel`, with
+    where they come from: {"traffic": bytes or None, "traffic_source": {...}}.
+    The summary's `traffic_case:` line names the case the counters were taken
+    on (and how they were scaled to a full launch, if they were)."""
+    rel = os.path.join("profiles", "%s.md" % kernel)
+    value, case = None, None
     try:
-        for line in open(path):
+        for line in open(os.path.join(ROOT, rel)):
             if line.startswith("traffic_bytes_per_launch:"):
                 v = line.split(":", 1)[1].strip()
-                return None if v in ("", "null") else float(v)
+                value = None if v in ("", "null") else float(v)
+            elif line.startswith("traffic_case:"):
+                case = line.split(":", 1)[1].strip()
     except OSError:
-        pass
-    return None
+        return {"traffic": None, "traffic_source": None}
+    return {"traffic": value, "traffic_source": {"profile": rel, "case": case}}
 
 
 # ---------------------------------------------------------------- clocks
@@ -605,7 +611,7 @@ def run_scalar(args, cfg):
         algo = db_bytes + 4 * C * B + 4 * R * B
         gbs = algo / (ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
-                "frac": gbs / float(peaks["hbm_gbs"]), "traffic": profile_traffic("gemv_kernel_" + args.workload),
+                "frac": gbs / float(peaks["hbm_gbs"]), **profile_traffic("gemv_kernel_" + args.workload),
                 "kernel": "gemv_kernel",
                 "peak_source": "%s hbm_gbs (copy)" % kind, "algorithmic_bytes_per_launch": algo}
         dtype = "u8 x u32 (4-way byte dot products, u32 wrap-around)"
@@ -613,7 +619,8 @@ def run_scalar(args, cfg):
         flops = 2.0 * R * C * 4 * 64        # fp16 multiply-adds on 4 digit planes x 64 query slots
         tf = flops / (ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": tf, "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
-                "frac": tf / float(peaks["bf16_tflops"]), "traffic": None, "kernel": "scalar_kernel",
+                "frac": tf / float(peaks["bf16_tflops"]), **profile_traffic("scalar_kernel_" + args.workload),
+                "kernel": "scalar_kernel",
                 "peak_source": "%s bf16_tflops (fp16 dense rate is the same)" % kind,
                 "hbm_frac": db_bytes / (ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"])}
         dtype = "u8 x u32 (fp16 digits, fp32 accumulate)"
@@ -757,7 +764,7 @@ def run_exppack(args, cfg):
                                      "frac": lift_bytes / (lift_ms * 1e-3) / 1e9 / hbm_peak,
                                      "algorithmic_bytes_per_launch": lift_bytes}},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": profile_traffic("rowsel_kernel_exppack_15g"),
+                         "frac": achieved / hbm_peak, **profile_traffic("rowsel_kernel_exppack_15g"),
                          "kernel": "rowsel_kernel (pir_exppack)", "peak_source": "%s hbm_gbs (copy)" % peak_kind,
                          "algorithmic_bytes_per_launch": algo},
             "clocks": clk,
@@ -983,7 +990,7 @@ def run_coltor(args, cfg):
                     "frac": nntt / (ms_step * 1e-3) / ntt_alone,
                     "note": "the step's transforms against the 4096-point lift + NTT kernel timed alone in this run"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": profile_traffic("coltor_%s" % args.workload),
+                         "frac": achieved / hbm_peak, **profile_traffic("coltor_%s" % args.workload),
                          "kernel": "the tournament's five kernels per stage (NTT kernels dominate)",
                          "peak_source": "%s hbm_gbs (copy)" % peak_kind, "algorithmic_bytes_per_launch": algo},
             "clocks": clk,
@@ -1100,7 +1107,7 @@ def run_expand(args, cfg):
                     "frac": nntt / (ms_step * 1e-3) / ntt_alone,
                     "note": "the step's transforms against the 4096-point lift + NTT kernel timed alone in this run"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": profile_traffic("expand_%s" % args.workload),
+                         "frac": achieved / hbm_peak, **profile_traffic("expand_%s" % args.workload),
                          "kernel": "the expansion's four kernels per stage (NTT kernels dominate)",
                          "peak_source": "%s hbm_gbs (copy)" % peak_kind, "algorithmic_bytes_per_launch": algo},
             "clocks": clk,
@@ -1252,7 +1259,7 @@ def run_onion(args, cfg):
                       "RowSel launched directly",
             "db_gbs_in_rowsel": db_gbs,
             "roofline": {"bound": "hbm", "achieved": db_gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": db_gbs / hbm_peak, "traffic": None,
+                         "frac": db_gbs / hbm_peak, "traffic": None, "traffic_source": None,
                          "kernel": "rowsel_tc_kernel (the DB scan, %d queries per pass)" % B if on_tensor
                                    else "rowsel_kernel (the DB scan)",
                          "peak_source": "%s hbm_gbs (copy)" % peak_kind,
@@ -1435,7 +1442,7 @@ def run_ours(args, cfg):
             "kernel_ms": {"ntt_fwd": ntt_fwd_ms, "rowsel": rowsel_ms, "ntt_inv": ntt_inv_ms},
             "kernels": kernel_rooflines(coeff, q_bytes, o_bytes, ntt_fwd_ms, ntt_inv_ms, hbm_peak),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": profile_traffic("%s_%s" % (kernel, args.workload)),
+                         "frac": achieved / hbm_peak, **profile_traffic("%s_%s" % (kernel, args.workload)),
                          "kernel": kernel, "peak_source": "%s hbm_gbs (copy)" % peak_kind,
                          "algorithmic_bytes_per_launch": algo_bytes, "tensor": tensor,
                          "read_probe_gbs": read_probe_gbs, "frac_of_read_probe": achieved / read_probe_gbs,

@@ -311,6 +311,9 @@ extern "C" int pir_coltor_stage(pir_ctx *ctx, const uint32_t *C, uint32_t ell, u
     if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
     const uint64_t ctb = 2ull * ctx->L * ctx->N * 4;
     if (overlaps(in, n * ctb, out, ((n + 1) / 2) * ctb)) return PIR_ERR_ARG;
+    // the stage writes its digits into the workspace while it reads in and writes out
+    if (overlaps(workspace, lay.total * 4, in, n * ctb) || overlaps(workspace, lay.total * 4, out, ((n + 1) / 2) * ctb))
+        return PIR_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
     return stage(ctx, C, 0, ell, w, in, n, 1, out, static_cast<uint32_t *>(workspace), lay, (cudaStream_t)stream);
 }
@@ -326,6 +329,9 @@ extern "C" int pir_coltor_batch(pir_ctx *ctx, const uint32_t *C, uint32_t ell, u
     if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
     const uint64_t ctw = 2ull * ctx->L * ctx->N;
     if (overlaps(in, G * n * ctw * 4, out, G * ctw * 4)) return PIR_ERR_ARG;
+    // the stages ping-pong through the workspace while the first reads in and the last writes out
+    if (overlaps(workspace, lay.total * 4, in, G * n * ctw * 4) || overlaps(workspace, lay.total * 4, out, G * ctw * 4))
+        return PIR_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
     if (n == 1)

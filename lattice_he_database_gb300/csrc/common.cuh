@@ -19,6 +19,8 @@ struct pir_ctx {
     uint64_t mu[PIR_MAX_RNS];          // floor(2^64 / q)
     uint32_t *d_tw;                    // device twiddles [L][4][N]
     uint32_t *d_status;                // device status word
+    uint64_t wait_limit_ns;            // limit of the kernels' ordinary waits (pir_ctx_set_wait_limit)
+    uint32_t test_hook;                // PIR_HOOK_* (pir_ctx_set_test_hook); PIR_HOOK_NONE in normal use
 };
 
 // Parameters of the RNS ring passed by value to kernels.
@@ -107,11 +109,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 // Wall-clock limit of one device-side wait.  A correct launch never waits
 // more than milliseconds; the limit only turns a lost arrival into an error.
+// Kernels that take a context's limit (pir_ctx_set_wait_limit) use it for
+// their ordinary waits; the waits that drain a kernel's own copies in flight
+// before it exits always keep this full limit.
 #define PIR_WAIT_LIMIT_NS 2000000000ull
 
 // Bounded wait for the phase with parity `parity` of an mbarrier.  Returns
-// false (and sets PIR_STATUS_TIMEOUT in *status) if the limit runs out.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status) {
+// false (and sets PIR_STATUS_TIMEOUT in *status) if `limit_ns` runs out.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                          uint64_t limit_ns = PIR_WAIT_LIMIT_NS) {
     uint32_t a = smem_u32(bar);
     for (int i = 0; i < 128; ++i)
         if (mbar_try_wait(a, parity)) return true;
@@ -119,7 +125,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     while (true) {
         for (int i = 0; i < 256; ++i)
             if (mbar_try_wait(a, parity)) return true;
-        if (global_timer_ns() - t0 > PIR_WAIT_LIMIT_NS) {
+        if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(status, PIR_STATUS_TIMEOUT);
             return false;
         }

@@ -125,6 +125,8 @@ extern "C" int pir_ctx_create(pir_ctx **out, uint32_t N, uint32_t L, const uint3
     pir_ctx *c = (pir_ctx *)calloc(1, sizeof(pir_ctx));
     if (!c) return PIR_ERR_ALLOC;
     c->device = device;
+    c->wait_limit_ns = PIR_WAIT_LIMIT_NS;
+    c->test_hook = PIR_HOOK_NONE;
     cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device);
     c->N = N;
     c->L = L;
@@ -193,6 +195,18 @@ extern "C" int pir_status(pir_ctx *ctx, uint32_t *flags, int clear) {
     if (cudaDeviceSynchronize() != cudaSuccess) return PIR_ERR_CUDA;
     if (cudaMemcpy(flags, ctx->d_status, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return PIR_ERR_CUDA;
     if (clear && cudaMemset(ctx->d_status, 0, sizeof(uint32_t)) != cudaSuccess) return PIR_ERR_CUDA;
+    return PIR_OK;
+}
+
+extern "C" int pir_ctx_set_wait_limit(pir_ctx *ctx, uint64_t ns) {
+    if (!ctx || ns > PIR_WAIT_LIMIT_NS) return PIR_ERR_ARG;
+    ctx->wait_limit_ns = ns ? ns : PIR_WAIT_LIMIT_NS;
+    return PIR_OK;
+}
+
+extern "C" int pir_ctx_set_test_hook(pir_ctx *ctx, uint32_t hook) {
+    if (!ctx || hook > PIR_HOOK_WITHHOLD_LAST_COPY) return PIR_ERR_ARG;
+    ctx->test_hook = hook;
     return PIR_OK;
 }
 

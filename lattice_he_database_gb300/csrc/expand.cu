@@ -271,6 +271,9 @@ extern "C" int pir_expand_stage(pir_ctx *ctx, const uint32_t *evk, uint32_t ell,
     if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
     const uint64_t ctb = 2ull * ctx->L * ctx->N * 4;
     if (overlaps(in, M * ctb, out, 2 * M * ctb)) return PIR_ERR_ARG;
+    // the stage keeps its digits and coefficient-form rows in the workspace while it reads in and writes out
+    if (overlaps(workspace, lay.total * 4, in, M * ctb) || overlaps(workspace, lay.total * 4, out, 2 * M * ctb))
+        return PIR_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
     return one_stage(ctx, evk, 0, ell, w, j, in, M, 1, out, static_cast<uint32_t *>(workspace), lay,
                      (cudaStream_t)stream);
@@ -288,6 +291,9 @@ extern "C" int pir_expand_batch(pir_ctx *ctx, const uint32_t *evks, uint32_t ell
     if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
     const uint64_t ctw = 2ull * ctx->L * ctx->N;
     if (overlaps(ct, G * ctw * 4, out, G * (2 * Mmax) * ctw * 4)) return PIR_ERR_ARG;
+    // the stages ping-pong through the workspace while the first reads ct and the last writes out
+    if (overlaps(workspace, lay.total * 4, ct, G * ctw * 4) || overlaps(workspace, lay.total * 4, out, G * (2 * Mmax) * ctw * 4))
+        return PIR_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
     uint32_t *ws = static_cast<uint32_t *>(workspace);

@@ -56,6 +56,8 @@ struct RowselArgs {
     uint64_t P, units;
     uint32_t q[PIR_MAX_RNS], r32[PIR_MAX_RNS];
     uint64_t mu[PIR_MAX_RNS];
+    uint64_t wait_ns;        // limit of the ordinary waits (drains keep PIR_WAIT_LIMIT_NS)
+    uint32_t hook;           // PIR_HOOK_* of the context
 };
 
 __device__ __forceinline__ uint32_t slab_width(const RowselArgs &A, uint32_t s) {
@@ -198,12 +200,13 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
             const uint64_t pol = policy_evict_first();
             uint32_t stage = 0, phase = 0, pc = 0;
             uint64_t issued = 0, cur_p = ~0ull;
+            bool withheld = false;
             for (uint64_t u = u0; u < u1 && !abort_flag; ++u) {
                 const uint64_t p = u / A.S;
                 const uint32_t s = (uint32_t)(u - p * A.S);
                 if (p != cur_p) {  // the point's query slice goes first (consumers need it first)
                     const uint32_t slot = pc % A.nb, use = (pc / A.nb) & 1;
-                    if (!mbar_wait(qempty + slot, use ^ 1, A.status)) {
+                    if (!mbar_wait(qempty + slot, use ^ 1, A.status, A.wait_ns)) {
                         abort_flag = 1;
                         break;
                     }
@@ -217,19 +220,33 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
                 for (uint32_t c = 0; c < A.nchunks; ++c) {
                     const uint32_t rows = min((uint32_t)KC, A.D0 - c * KC);
                     const uint32_t bytes = rows * Ws * 4;
-                    if (!mbar_wait(empty + stage, phase ^ 1, A.status)) {
+                    if (!mbar_wait(empty + stage, phase ^ 1, A.status, A.wait_ns)) {
                         abort_flag = 1;
                         break;
                     }
-                    mbar_arrive_expect_tx(full + stage, bytes);
-                    bulk_g2s(ring + stage * STAGE_WORDS, src + (uint64_t)c * KC * Ws, bytes, full + stage, pol);
-                    ++issued;
+                    if (A.hook == PIR_HOOK_WITHHOLD_LAST_COPY && blockIdx.x == 0 && u + 1 == u1 &&
+                        c + 1 == A.nchunks) {
+                        // failure-path test: the CTA's last chunk is never copied, so its
+                        // consumers' wait runs out; nothing reuses this stage afterwards
+                        withheld = true;
+                    } else {
+                        mbar_arrive_expect_tx(full + stage, bytes);
+                        bulk_g2s(ring + stage * STAGE_WORDS, src + (uint64_t)c * KC * Ws, bytes, full + stage, pol);
+                        ++issued;
+                    }
                     if (++stage == NST) { stage = 0; phase ^= 1; }
                 }
             }
             // The copies still in flight target this CTA's shared memory:
-            // wait (bounded) for the last ring copies and query slices to land.
-            const uint32_t pend = issued < (uint64_t)NST ? (uint32_t)issued : (uint32_t)NST;
+            // wait (bounded, full limit) for the last ring copies and query
+            // slices to land.  A withheld copy was the CTA's last chunk: step
+            // back over its stage, and only NST - 1 stages before it can hold
+            // copies still in flight.
+            if (withheld) {
+                if (stage == 0) { stage = NST - 1; phase ^= 1; } else { --stage; }
+            }
+            const uint32_t cap = withheld ? NST - 1 : NST;
+            const uint32_t pend = issued < (uint64_t)cap ? (uint32_t)issued : cap;
             for (uint32_t i = 0; i < pend; ++i) {
                 if (stage == 0) { stage = NST - 1; phase ^= 1; } else { --stage; }
                 mbar_wait(full + stage, phase, A.status);
@@ -263,7 +280,7 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
                 if (lane == 0) mbar_arrive(qempty + qslot);
             }
             qslot = pc % A.nb;
-            if (!abort_flag && !mbar_wait(qfull + qslot, (pc / A.nb) & 1, A.status)) abort_flag = 1;
+            if (!abort_flag && !mbar_wait(qfull + qslot, (pc / A.nb) & 1, A.status, A.wait_ns)) abort_flag = 1;
             ++pc;
             cur_p = p;
         }
@@ -280,7 +297,7 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
         for (uint32_t c = 0; c < A.nchunks; ++c) {
             const uint32_t rows = min((uint32_t)KC, A.D0 - c * KC);
             bool ok = !abort_flag;
-            if (ok && !mbar_wait(full + stage, phase, A.status)) {
+            if (ok && !mbar_wait(full + stage, phase, A.status, A.wait_ns)) {
                 abort_flag = 1;
                 ok = false;
             }
@@ -489,6 +506,8 @@ int rowsel_impl(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, cons
     A.outT = reinterpret_cast<uint32_t *>(workspace) + wl.outT_offset_words;
     A.out = out;
     A.status = ctx->d_status;
+    A.wait_ns = ctx->wait_limit_ns;
+    A.hook = ctx->test_hook;
     A.N = ctx->N;
     A.L = ctx->L;
     A.D0 = D0;

@@ -113,6 +113,10 @@ def lib() -> ctypes.CDLL:
                                        ctypes.c_uint64, _vp, _vp, ctypes.c_uint64, _vp]
         L.pir_status.restype = ctypes.c_int
         L.pir_status.argtypes = [_vp, _u32p, ctypes.c_int]
+        L.pir_ctx_set_wait_limit.restype = ctypes.c_int
+        L.pir_ctx_set_wait_limit.argtypes = [_vp, ctypes.c_uint64]
+        L.pir_ctx_set_test_hook.restype = ctypes.c_int
+        L.pir_ctx_set_test_hook.argtypes = [_vp, ctypes.c_uint32]
         L.pir_strerror.restype = ctypes.c_char_p
         L.pir_strerror.argtypes = [ctypes.c_int]
         _lib = L
@@ -219,6 +223,20 @@ def pir_status(ctx: Ctx, clear: bool = True) -> int:
     flags = ctypes.c_uint32(0)
     _check(lib().pir_status(ctx, ctypes.byref(flags), int(clear)), "pir_status")
     return int(flags.value)
+
+
+PIR_HOOK_NONE = 0
+PIR_HOOK_WITHHOLD_LAST_COPY = 1
+
+
+def pir_ctx_set_wait_limit(ctx: Ctx, ns: int):
+    """Limit of the kernels' ordinary device waits (0 = the default 2 s)."""
+    _check(lib().pir_ctx_set_wait_limit(ctx, ns), "pir_ctx_set_wait_limit")
+
+
+def pir_ctx_set_test_hook(ctx: Ctx, hook: int):
+    """Failure-path test hook (PIR_HOOK_*); PIR_HOOK_NONE in normal use."""
+    _check(lib().pir_ctx_set_test_hook(ctx, hook), "pir_ctx_set_test_hook")
 
 
 # ---------------------------------------------------------------- NTT

@@ -108,6 +108,7 @@ def test_tournament_full_size(pir):
 
 
 def test_coltor_rejects_bad_arguments(pir):
+    import torch
     N, L = 64, 3
     ctx, qs, _ = _setup(pir, N, L)
     C = pir.empty_u32(2 * 5 * 2 * L * N)
@@ -122,6 +123,12 @@ def test_coltor_rejects_bad_arguments(pir):
         pir.pir_coltor_stage(ctx, C, 5, 18, cts, 4, out, ws[:64])
     with pytest.raises(pir.PirError):                 # out overlaps in
         pir.pir_coltor_stage(ctx, C, 5, 18, cts, 4, cts, ws)
+    with pytest.raises(pir.PirError):                 # out inside the workspace
+        pir.pir_coltor_stage(ctx, C, 5, 18, cts, 4, ws[: out.numel() * 4].view(torch.int32), ws)
+    with pytest.raises(pir.PirError):                 # in inside the workspace
+        pir.pir_coltor_stage(ctx, C, 5, 18, ws[: cts.numel() * 4].view(torch.int32), 4, out, ws)
+    with pytest.raises(pir.PirError):                 # out inside the workspace (whole tournament)
+        pir.pir_coltor(ctx, C, 5, 18, cts, 4, ws[-(out.numel() // 2) * 4:].view(torch.int32), ws)
     with pytest.raises(pir.PirError):                 # n = 0
         pir.pir_coltor(ctx, C, 5, 18, cts, 0, out, ws)
     assert pir.pir_coltor_workspace_bytes(ctx, 0, 5) == 0
@@ -217,6 +224,7 @@ def test_batch_of_16_full_size(pir):
 
 
 def test_batch_rejects_bad_arguments(pir):
+    import torch
     N, L = 64, 3
     ctx, qs, _ = _setup(pir, N, L)
     C = pir.empty_u32(2 * 10 * 2 * L * N)
@@ -229,5 +237,7 @@ def test_batch_rejects_bad_arguments(pir):
         pir.pir_coltor_batch(ctx, C, 5, 18, cts, 4, 2, out, pir.coltor_workspace(ctx, 4, 5))
     with pytest.raises(pir.PirError):                 # out overlaps in
         pir.pir_coltor_batch(ctx, C, 5, 18, cts, 4, 2, cts[8 * L * N:], ws)
+    with pytest.raises(pir.PirError):                 # out inside the workspace
+        pir.pir_coltor_batch(ctx, C, 5, 18, cts, 4, 2, ws[: out.numel() * 4].view(torch.int32), ws)
     assert pir.pir_coltor_batch_workspace_bytes(ctx, 4, 0, 5) == 0
     assert pir.pir_coltor_batch_workspace_bytes(ctx, 4, 1, 5) == pir.pir_coltor_workspace_bytes(ctx, 4, 5)

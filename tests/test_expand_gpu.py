@@ -101,6 +101,7 @@ def test_expansion_decrypts_to_coefficients(pir, N, S):
 
 
 def test_expand_rejects_bad_arguments(pir):
+    import torch
     N, L = 64, 3
     ctx, qs, _ = _setup(pir, N, L)
     evk = pir.empty_u32(7 * 5 * 2 * L * N)
@@ -117,6 +118,14 @@ def test_expand_rejects_bad_arguments(pir):
         pir.pir_expand(ctx, evk, 5, 18, 4, cts, out, ws[:64])
     with pytest.raises(pir.PirError):                 # out overlaps in
         pir.pir_expand_stage(ctx, evk, 5, 18, 0, cts, 2, cts, ws)
+    with pytest.raises(pir.PirError):                 # out inside the workspace
+        pir.pir_expand_stage(ctx, evk, 5, 18, 0, cts, 2, ws[: 4 * 2 * L * N * 4].view(torch.int32), ws)
+    with pytest.raises(pir.PirError):                 # in inside the workspace
+        pir.pir_expand_stage(ctx, evk, 5, 18, 0, ws[: cts.numel() * 4].view(torch.int32), 2, out, ws)
+    with pytest.raises(pir.PirError):                 # out inside the workspace (whole expansion)
+        pir.pir_expand(ctx, evk, 5, 18, 2, cts, ws[-4 * 2 * L * N * 4:].view(torch.int32), ws)
+    with pytest.raises(pir.PirError):                 # out inside the workspace (batch of two clients)
+        pir.pir_expand_batch(ctx, evk, 5, 18, 1, cts, 2, ws[: 4 * 2 * L * N * 4].view(torch.int32), ws)
     assert pir.pir_expand_workspace_bytes(ctx, 0, 5) == 0
 
 
