@@ -250,8 +250,9 @@ int pir_exppack(pir_ctx *ctx, const uint32_t *h_db, uint32_t n, uint32_t Dr, con
  *   ell, w : 1 <= ell <= 16, 1 <= w <= 32, ell * w >= the bit length of Q
  *          (ell = 5, w = 18 for three primes below 2^29).
  *   workspace : device, >= pir_coltor_workspace_bytes(ctx, n, ell) bytes,
- *          16-byte aligned; must overlap neither in nor out; contents
- *          undefined after the call.
+ *          16-byte aligned; the part the call uses (its first
+ *          pir_coltor_workspace_bytes bytes) must overlap neither in nor out;
+ *          contents undefined after the call.
  * The library owns nothing the caller passes; calls are asynchronous on
  * stream.  Errors: PIR_ERR_ARG (NULL/unaligned pointers, n = 0 or ceil(n/2) >= 2^31,
  * ell or w out of range, digits not covering Q, workspace too small,
@@ -310,8 +311,10 @@ int pir_coltor_batch(pir_ctx *ctx, const uint32_t *C, uint32_t ell, uint32_t w,
  *          [2^stages][2][L][N]; must not overlap the input.
  *   ell, w : as for pir_coltor; j < log2 N; 1 <= stages <= log2 N.
  *   workspace : device, >= pir_expand_workspace_bytes(ctx, M, ell) bytes
- *          (pir_expand: M = 2^(stages-1)), 16-byte aligned; must overlap
- *          neither the input nor out; contents undefined after the call.
+ *          (pir_expand: M = 2^(stages-1)), 16-byte aligned; the part the
+ *          call uses (its first pir_expand_workspace_bytes bytes) must
+ *          overlap neither the input nor out; contents undefined after the
+ *          call.
  * Errors: PIR_ERR_ARG (NULL/unaligned pointers, sizes or gadget parameters
  * out of range, workspace too small, input/output overlap, workspace
  * overlapping the input or out), PIR_ERR_CUDA.
@@ -414,8 +417,8 @@ int pir_status(pir_ctx *ctx, uint32_t *flags, int clear);
  *   kernel never exits with copies into its shared memory outstanding.
  *   Errors: PIR_ERR_ARG (NULL ctx, ns > 2e9).
  * pir_ctx_set_test_hook — PIR_HOOK_WITHHOLD_LAST_COPY makes the first CTA
- *   of the CUDA-core RowSel scan never issue the bulk copy of its last DB
- *   chunk: its consumers' wait for that chunk runs out, the kernel sets
+ *   of either RowSel scan (CUDA cores or tensor cores) never issue the copy
+ *   of its last DB chunk or tile: the wait for it runs out, the kernel sets
  *   PIR_STATUS_TIMEOUT, stops computing, drains its other copies and
  *   returns; the results of that launch are unspecified.  PIR_HOOK_NONE
  *   (the default) turns it off.  Host state only: no launch is made.

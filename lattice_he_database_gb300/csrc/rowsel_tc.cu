@@ -88,6 +88,8 @@ struct TcArgs {
     float qinv[PIR_MAX_RNS];          // 1/q rounded to fp32 (quotient estimate of the epilogue)
     uint32_t c[PIR_MAX_RNS][4];       // 2^(8i) mod q
     uint32_t cs[PIR_MAX_RNS][4];      // Shoup companions of c
+    uint64_t wait_ns;                 // limit of the ordinary waits (drains keep PIR_WAIT_LIMIT_NS)
+    uint32_t hook;                    // PIR_HOOK_* of the context
 };
 
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t j) {
@@ -295,13 +297,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // and 40% of the DB was read twice.)
         const uint64_t pol = policy_evict_first();
         uint32_t it = 0, pc = 0;
+        bool withheld = false;
 
         for (uint64_t p = p_begin; p < p_end; ++p)
           for (uint32_t h = 0; h < A.H; ++h, ++pc) {
             // the segment's query slice (the query warps release the buffer once digitised)
             const uint32_t nks = seg_stages(A, h), qbytes = seg_rows(A, h) * 32 * 4;
             const uint32_t *qsrc = A.qT + p * A.PS + (uint64_t)h * TC_SEG * 32;
-            if (abort_flag || !mbar_wait(qempty, (pc & 1) ^ 1, A.status)) {
+            if (abort_flag || !mbar_wait(qempty, (pc & 1) ^ 1, A.status, A.wait_ns)) {
                 abort_flag = 1;
             } else {
                 mbar_arrive_expect_tx(qfull, qbytes);
@@ -316,8 +319,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (uint32_t t = 0; t < nt; ++t)
                     for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
                         const uint32_t st = it % TC_NR, ph = (it / TC_NR) & 1;
-                        if (abort_flag || !mbar_wait(rempty + st, ph ^ 1, A.status)) {
+                        if (abort_flag || !mbar_wait(rempty + st, ph ^ 1, A.status, A.wait_ns)) {
                             abort_flag = 1;
+                            continue;
+                        }
+                        if (A.hook == PIR_HOOK_WITHHOLD_LAST_COPY && blockIdx.x == 0 && p + 1 == p_end &&
+                            h + 1 == A.H && s + 1 == A.S && t + 1 == nt && ks + 1 == nks) {
+                            // failure-path test: the CTA's last DB tile is never copied, so
+                            // its converters' wait runs out; nothing reuses this stage
+                            withheld = true;
                             continue;
                         }
                         mbar_arrive_expect_tx(rfull + st, TC_RAW_BYTES);
@@ -331,7 +341,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
             }
           }
-        for (uint32_t i = 0; i < TC_NR && i < it; ++i) {  // copies in flight land first
+        // copies in flight land first (full limit); a withheld copy was the last stage
+        for (uint32_t i = withheld ? 1u : 0u; i < TC_NR && i < it; ++i) {
             const uint32_t j = it - 1 - i;
             mbar_wait(rfull + j % TC_NR, (j / TC_NR) & 1, A.status);
         }
@@ -353,14 +364,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t nt = tiles_of(A, s);
                 for (uint32_t t = 0; t < nt; ++t, ++g) {
                     const uint32_t buf = g & 1, use = (g >> 1) & 1;
-                    if (!ab && !mbar_wait(acce + buf, use ^ 1, A.status)) ab = true;
+                    if (!ab && !mbar_wait(acce + buf, use ^ 1, A.status, A.wait_ns)) ab = true;
                     if (first) {
-                        if (!ab && !mbar_wait(afull, pc & 1, A.status)) ab = true;
+                        if (!ab && !mbar_wait(afull, pc & 1, A.status, A.wait_ns)) ab = true;
                         first = false;
                     }
                     const uint32_t d = tmem + TC_ACC_COL + buf * 128;
                     for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
-                        if (!ab && !mbar_wait(bfull + st, ph, A.status)) ab = true;
+                        if (!ab && !mbar_wait(bfull + st, ph, A.status, A.wait_ns)) ab = true;
                         if (!ab) {
                             fence_after();
                             mma_stage(d, tmem + ks * 32, bdesc0 + st * (TC_B_BYTES >> 4), ks);
@@ -396,8 +407,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (digitizer) {
                 // query digits of the segment -> TMEM (plane = warp, polynomial m = lane)
                 const uint32_t plane = warp, m = lane, rows = seg_rows(A, h);
-                if (!abort_flag && !mbar_wait(qfull, pc & 1, A.status)) abort_flag = 1;
-                if (!abort_flag && !mbar_wait(aempty, (pc & 1) ^ 1, A.status)) abort_flag = 1;
+                if (!abort_flag && !mbar_wait(qfull, pc & 1, A.status, A.wait_ns)) abort_flag = 1;
+                if (!abort_flag && !mbar_wait(aempty, (pc & 1) ^ 1, A.status, A.wait_ns)) abort_flag = 1;
                 fence_after();
                 if (!abort_flag) {
                     const bool live = m < A.Mv;
@@ -432,12 +443,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         const uint32_t rs = it % TC_NR, rph = (it / TC_NR) & 1;
                         const uint32_t bs = it % TC_NB, bph = (it / TC_NB) & 1;
                         uint32_t w[3][8];
-                        if (!abort_flag && !mbar_wait(rfull + rs, rph, A.status)) abort_flag = 1;
+                        if (!abort_flag && !mbar_wait(rfull + rs, rph, A.status, A.wait_ns)) abort_flag = 1;
                         if (!abort_flag)
                             load_chunks(reinterpret_cast<const uint32_t *>(stR + rs * TC_RAW_BYTES), gw, lane, w);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(rempty + rs);     // the words are in registers
-                        if (!abort_flag && !mbar_wait(bempty + bs, bph ^ 1, A.status)) abort_flag = 1;
+                        if (!abort_flag && !mbar_wait(bempty + bs, bph ^ 1, A.status, A.wait_ns)) abort_flag = 1;
                         if (!abort_flag) store_chunks(stB + bs * TC_B_BYTES, gw, lane, w);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bfull + bs);
@@ -463,7 +474,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t Ws = (s == A.S - 1) ? A.Wlast : PIR_SLAB;
                 for (uint32_t t = 0; t < nt; ++t, ++g) {
                     const uint32_t buf = g & 1, use = (g >> 1) & 1;
-                    if (!abort_flag && !mbar_wait(accf + buf, use, A.status)) abort_flag = 1;
+                    if (!abort_flag && !mbar_wait(accf + buf, use, A.status, A.wait_ns)) abort_flag = 1;
                     fence_after();
                     // W[n] = sum_j 2^(8j) S_j[n] = sum_k d_i(query) * DB word is reduced
                     // mod q without 64-bit arithmetic.  Its low 32 bits come exactly
@@ -654,6 +665,8 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
     a.qT = qT;
     a.outT = outT;
     a.status = ctx->d_status;
+    a.wait_ns = ctx->wait_limit_ns;
+    a.hook = ctx->test_hook;
     a.N = ctx->N;
     a.D0 = D0;
     a.D1 = D1;

@@ -128,7 +128,7 @@ def test_coltor_rejects_bad_arguments(pir):
     with pytest.raises(pir.PirError):                 # in inside the workspace
         pir.pir_coltor_stage(ctx, C, 5, 18, ws[: cts.numel() * 4].view(torch.int32), 4, out, ws)
     with pytest.raises(pir.PirError):                 # out inside the workspace (whole tournament)
-        pir.pir_coltor(ctx, C, 5, 18, cts, 4, ws[-(out.numel() // 2) * 4:].view(torch.int32), ws)
+        pir.pir_coltor(ctx, C, 5, 18, cts, 4, ws[: (out.numel() // 2) * 4].view(torch.int32), ws)
     with pytest.raises(pir.PirError):                 # n = 0
         pir.pir_coltor(ctx, C, 5, 18, cts, 0, out, ws)
     assert pir.pir_coltor_workspace_bytes(ctx, 0, 5) == 0

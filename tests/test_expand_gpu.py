@@ -123,7 +123,7 @@ def test_expand_rejects_bad_arguments(pir):
     with pytest.raises(pir.PirError):                 # in inside the workspace
         pir.pir_expand_stage(ctx, evk, 5, 18, 0, ws[: cts.numel() * 4].view(torch.int32), 2, out, ws)
     with pytest.raises(pir.PirError):                 # out inside the workspace (whole expansion)
-        pir.pir_expand(ctx, evk, 5, 18, 2, cts, ws[-4 * 2 * L * N * 4:].view(torch.int32), ws)
+        pir.pir_expand(ctx, evk, 5, 18, 2, cts, ws[: 4 * 2 * L * N * 4].view(torch.int32), ws)
     with pytest.raises(pir.PirError):                 # out inside the workspace (batch of two clients)
         pir.pir_expand_batch(ctx, evk, 5, 18, 1, cts, 2, ws[: 4 * 2 * L * N * 4].view(torch.int32), ws)
     assert pir.pir_expand_workspace_bytes(ctx, 0, 5) == 0

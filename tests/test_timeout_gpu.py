@@ -1,11 +1,12 @@
 """The bounded-wait recovery path, exercised without faulting the GPU.
 
-Every device wait of the RowSel scan gives up after a limit, sets
+Every device wait of the RowSel scans gives up after a limit, sets
 PIR_STATUS_TIMEOUT in the context's status word, stops computing, drains its
 own bulk copies in flight and returns, so the context stays usable.  Here a
-test hook makes the first CTA of the CUDA-core scan never issue the copy of
-its last DB chunk (a wait that nothing will ever satisfy), with the
-context's wait limit shortened to 1 ms.  The launch must return promptly
+test hook makes the first CTA of the scan never issue the copy of its last
+DB chunk (a wait that nothing will ever satisfy), with the context's wait
+limit shortened to 1 ms: on the CUDA cores (1 and 3 queries) and on the
+tensor cores (9 queries, two K segments per point).  The launch must return promptly
 with the status bit set; the next launch on the same context, with the hook
 off and the default limit, must be bit-exact against the oracle with a clean
 status word.
@@ -29,7 +30,7 @@ def pir():
     return p
 
 
-@pytest.mark.parametrize("D0,D1,B", [(16, 16, 1), (300, 40, 3)])
+@pytest.mark.parametrize("D0,D1,B", [(16, 16, 1), (300, 40, 3), (520, 8, 9)])
 def test_withheld_copy_times_out_and_context_recovers(pir, D0, D1, B):
     import torch
     N, L = 4096, 2
