@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(CT_THREADS) coltor_diff_kernel(const DiffArgs 
 struct DiffInttArgs {
     const uint32_t *in;
     uint32_t *diff;
-    const uint32_t *tw;     // [L][4][N] twiddle tables
+    const uint32_t *tw;     // [L][2][N] twiddle pairs (tw_pairs)
     uint64_t n, Rp;         // ciphertexts and pairs per tournament
     uint32_t L;
     uint32_t q[PIR_MAX_RNS], ninv[PIR_MAX_RNS], ninv_shoup[PIR_MAX_RNS];
@@ -101,8 +101,7 @@ __global__ void __launch_bounds__(kT4) coltor_diff_intt4096_kernel(const __grid_
     const uint32_t l = blockIdx.x % A.L;
     const uint64_t LN = (uint64_t)A.L * kN4;
     const uint32_t q = A.q[l];
-    const uint32_t *W = A.tw + (size_t)l * 4 * kN4 + TW_INV * kN4;
-    const uint32_t *Wp = A.tw + (size_t)l * 4 * kN4 + TW_INV_SHOUP * kN4;
+    const uint2 *T = tw_pairs(A.tw, l, kN4, TW_INV);
     bool has_odd;
     const uint64_t ce = even_ct(i, A.Rp, A.n, has_odd);
     const uint32_t *ev = A.in + ce * 2 * LN + (uint64_t)l * kN4;             // polynomial 0 of ct_2i
@@ -119,7 +118,7 @@ __global__ void __launch_bounds__(kT4) coltor_diff_intt4096_kernel(const __grid_
         y[k] = o1.x + q - e1.x; y[k + 1] = o1.y + q - e1.y; y[k + 2] = o1.z + q - e1.z; y[k + 3] = o1.w + q - e1.w;
     }
     uint32_t *dst = A.diff + i * 2 * LN + (uint64_t)l * kN4;
-    inv4096x2_rounds(x, y, sa, sb, W, Wp, q, A.ninv[l], A.ninv_shoup[l], dst, dst + LN, true);
+    inv4096x2_rounds(x, y, sa, sb, T, q, A.ninv[l], A.ninv_shoup[l], dst, dst + LN, true);
 }
 
 struct MacArgs {

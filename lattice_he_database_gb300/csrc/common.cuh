@@ -31,14 +31,18 @@ struct RnsParams {
     uint32_t ninv_shoup[PIR_MAX_RNS];
     uint32_t r32[PIR_MAX_RNS];
     uint64_t mu[PIR_MAX_RNS];
-    const uint32_t *tw;  // [L][4][N]: psi^brv(i), shoup, psi^-brv(i), shoup
+    const uint32_t *tw;  // [L][2][N] pairs {w, floor(w 2^32 / q)}: w = psi^brv(i), then psi^-brv(i)
     uint32_t *status;    // the context's device status word (bounded waits report here)
 };
 
 RnsParams rns_params(const pir_ctx *ctx);
 
-// Twiddle sub-table offsets (in units of N words) within one prime's block.
-enum { TW_FWD = 0, TW_FWD_SHOUP = 1, TW_INV = 2, TW_INV_SHOUP = 3 };
+// Twiddle pairs {w, Shoup companion} of prime l in direction TW_FWD
+// (psi^brv(i)) or TW_INV (psi^-brv(i)): one 8-byte load per butterfly.
+enum { TW_FWD = 0, TW_INV = 1 };
+__host__ __device__ __forceinline__ const uint2 *tw_pairs(const uint32_t *tw, uint32_t l, uint32_t N, int dir) {
+    return reinterpret_cast<const uint2 *>(tw) + ((size_t)l * 2 + (size_t)dir) * N;
+}
 
 static inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -50,6 +54,12 @@ int launch_status(cudaError_t e);  // maps a CUDA error to PIR_OK / PIR_ERR_CUDA
 __device__ __forceinline__ uint32_t shoup_mul(uint32_t y, uint32_t w, uint32_t wp, uint32_t q) {
     uint32_t qh = __umulhi(y, wp);
     return y * w - qh * q;
+}
+
+// x mod q up to one subtraction for a 32-bit x: with m = floor(2^32 / q)
+// (= mu >> 32), x - floor(x m / 2^32) q lies in [0, 2q) (Barrett).
+__device__ __forceinline__ uint32_t barrett32_lazy(uint32_t x, uint32_t q, uint32_t m) {
+    return x - __umulhi(x, m) * q;
 }
 
 // Barrett reduction of a 64-bit value: x mod q with mu = floor(2^64 / q).

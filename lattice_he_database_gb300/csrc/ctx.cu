@@ -132,7 +132,7 @@ extern "C" int pir_ctx_create(pir_ctx **out, uint32_t N, uint32_t L, const uint3
     c->L = L;
     while ((1u << c->logN) < N) ++c->logN;
 
-    std::vector<uint32_t> tw((size_t)L * 4 * N);
+    std::vector<uint32_t> tw((size_t)L * 4 * N);   // [L][2][N] pairs {w, shoup(w)}
     for (uint32_t l = 0; l < L; ++l) {
         uint32_t ql = q[l];
         c->q[l] = ql;
@@ -143,15 +143,16 @@ extern "C" int pir_ctx_create(pir_ctx **out, uint32_t N, uint32_t L, const uint3
         c->r32[l] = (uint32_t)((1ull << 32) % ql);
         c->mu[l] = (uint64_t)(((unsigned __int128)1 << 64) / ql);
         uint64_t psi_inv = powmod64(c->psi[l], ql - 2, ql);
-        uint32_t *T = tw.data() + (size_t)l * 4 * N;
+        uint32_t *F = tw.data() + ((size_t)l * 2 + TW_FWD) * 2 * N;
+        uint32_t *I = tw.data() + ((size_t)l * 2 + TW_INV) * 2 * N;
         for (uint32_t i = 0; i < N; ++i) {
             uint32_t e = bit_reverse(i, c->logN);
             uint32_t wf = (uint32_t)powmod64(c->psi[l], e, ql);
             uint32_t wi = (uint32_t)powmod64(psi_inv, e, ql);
-            T[TW_FWD * N + i] = wf;
-            T[TW_FWD_SHOUP * N + i] = shoup_of(wf, ql);
-            T[TW_INV * N + i] = wi;
-            T[TW_INV_SHOUP * N + i] = shoup_of(wi, ql);
+            F[2 * i] = wf;
+            F[2 * i + 1] = shoup_of(wf, ql);
+            I[2 * i] = wi;
+            I[2 * i + 1] = shoup_of(wi, ql);
         }
     }
     if (cudaMalloc(&c->d_tw, tw.size() * sizeof(uint32_t)) != cudaSuccess) { free(c); return PIR_ERR_ALLOC; }

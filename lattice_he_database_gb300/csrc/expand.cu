@@ -57,8 +57,7 @@ __global__ void __launch_bounds__(kT4) expand_intt_a4096_kernel(const __grid_con
     const uint32_t l = blockIdx.x % A.L;
     const bool two = i1 < A.M;
     const uint32_t q = A.q[l];
-    const uint32_t *W = A.tw + (size_t)l * 4 * kN4 + TW_INV * kN4;
-    const uint32_t *Wp = A.tw + (size_t)l * 4 * kN4 + TW_INV_SHOUP * kN4;
+    const uint2 *T = tw_pairs(A.tw, l, kN4, TW_INV);
     const uint32_t *s0 = A.in + ((2 * i0 + 1) * A.L + l) * kN4;
     const uint32_t *s1 = A.in + ((2 * i1 + 1) * A.L + l) * kN4;
     const uint32_t t = threadIdx.x;
@@ -70,7 +69,7 @@ __global__ void __launch_bounds__(kT4) expand_intt_a4096_kernel(const __grid_con
         x[k] = u.x; x[k + 1] = u.y; x[k + 2] = u.z; x[k + 3] = u.w;
         y[k] = v.x; y[k + 1] = v.y; y[k + 2] = v.z; y[k + 3] = v.w;
     }
-    inv4096x2_rounds(x, y, sa, sb, W, Wp, q, A.ninv[l], A.ninv_shoup[l], A.coef + (i0 * A.L + l) * kN4,
+    inv4096x2_rounds(x, y, sa, sb, T, q, A.ninv[l], A.ninv_shoup[l], A.coef + (i0 * A.L + l) * kN4,
                      A.coef + (i1 * A.L + l) * kN4, two);
 }
 
@@ -127,7 +126,7 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
         const uint64_t ks0[4] = {a0, a1, a2, a3}, ks1[4] = {b0, b1, b2, b3};
         const uint32_t *c0 = A.in + i * 2 * LN + (uint64_t)l * A.N;
         const uint32_t *c1 = c0 + LN;
-        const uint32_t *Tinv = A.tw + (size_t)l * 4 * A.N + TW_INV * A.N;
+        const uint2 *Tinv = tw_pairs(A.tw, l, A.N, TW_INV);   // .x: psi^-brv(i)
         const uint4 v0 = *reinterpret_cast<const uint4 *>(c0 + s0);
         const uint4 v1 = *reinterpret_cast<const uint4 *>(c1 + s0);
         const uint32_t x0[4] = {v0.x, v0.y, v0.z, v0.w}, x1[4] = {v1.x, v1.y, v1.z, v1.w};
@@ -143,7 +142,7 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
             const uint32_t S1 = barrett64(ks1[c], q, mu);
             // NTT(X^(-2^j)) at this slot: psi^(-E), E = 2^j (2 brv(slot) + 1) mod 2N
             const uint32_t E = (odd << A.j) & (twoN - 1);
-            const uint32_t m = E < A.N ? Tinv[brv(E, A.logN)] : q - Tinv[brv(E - A.N, A.logN)];
+            const uint32_t m = E < A.N ? Tinv[brv(E, A.logN)].x : q - Tinv[brv(E - A.N, A.logN)].x;
             o0[c] = addq(x0[c], S0, q);
             o1[c] = addq(x1[c], S1, q);
             p0[c] = barrett64((uint64_t)subq(x0[c], S0, q) * m, q, mu);

@@ -9,6 +9,14 @@
 
 namespace {
 
+// Loads that bypass L1: a row is read once, and L1 is better spent on the
+// twiddle pairs that every CTA of a prime reads.
+__device__ __forceinline__ uint32_t ld_na(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.global.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 constexpr int kNttThreads = 512;
 constexpr uint32_t kMaxRowsPerCta = 4096 / 16;  // rows per CTA for the smallest ring (N = 16)
 
@@ -28,7 +36,9 @@ __global__ void __launch_bounds__(kNttThreads) ntt_kernel(const uint32_t *__rest
     if (LIFT) {
         for (uint32_t i = threadIdx.x; i < nwords; i += blockDim.x) {
             const uint64_t row = row0 + (i >> logN);
-            sm[i] = in[(row / L) * N + (i & (N - 1))] % P.q[row % L];
+            const uint32_t l = (uint32_t)(row % L), q = P.q[l];
+            const uint32_t r = barrett32_lazy(in[(row / L) * N + (i & (N - 1))], q, (uint32_t)(P.mu[l] >> 32));
+            sm[i] = r >= q ? r - q : r;
         }
     } else {
         const uint4 *src = reinterpret_cast<const uint4 *>(in + row0 * N);
@@ -65,8 +75,8 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
     const uint64_t row = blockIdx.x;
     const uint32_t l = (uint32_t)(row % P.L);
     const uint32_t q = P.q[l];
-    const uint32_t *W = P.tw + (size_t)l * 4 * kN4 + (FWD ? TW_FWD : TW_INV) * kN4;
-    const uint32_t *Wp = P.tw + (size_t)l * 4 * kN4 + (FWD ? TW_FWD_SHOUP : TW_INV_SHOUP) * kN4;
+    const uint2 *T = tw_pairs(P.tw, l, kN4, FWD ? TW_FWD : TW_INV);
+    const uint32_t mb = (uint32_t)(P.mu[l] >> 32);   // floor(2^32 / q) for the lift
     const uint32_t *src = in + (LIFT ? row / P.L : row) * kN4;
     uint32_t *dst = out + row * kN4;
     const uint32_t t = threadIdx.x;
@@ -75,26 +85,26 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
     if (FWD) {
         // round 0: stages 0-3, distance 256, elements t + 256 i
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = LIFT ? src[t + 256 * i] % q : src[t + 256 * i];
-        fwd_round16(x, 0, 0, W, Wp, q);
+        for (int i = 0; i < 16; ++i) x[i] = LIFT ? barrett32_lazy(src[t + 256 * i], q, mb) : src[t + 256 * i];
+        fwd_round16(x, 0, 0, T, q);
 #pragma unroll
         for (int i = 0; i < 16; ++i) sm[z.col(i)] = x[i];
         __syncthreads();
         // round 1: stages 4-7, distance 16, elements (t>>4)*256 + (t&15) + 16 i
 #pragma unroll
         for (int i = 0; i < 16; ++i) x[i] = sm[z.mid(i)];
-        fwd_round16(x, 4, t >> 4, W, Wp, q);
+        fwd_round16(x, 4, t >> 4, T, q);
 #pragma unroll
         for (int i = 0; i < 16; ++i) sm[z.mid(i)] = x[i];
         __syncthreads();
         // round 2: stages 8-11, distance 1, elements 16t .. 16t+15
 #pragma unroll
         for (int i = 0; i < 16; ++i) x[i] = sm[z.row(i)];
-        fwd_round16(x, 8, t, W, Wp, q);
+        fwd_round16(x, 8, t, T, q);
 #pragma unroll
         for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<uint4 *>(dst + 16 * t + i) =
-                make_uint4(fwd_final(x[i], q), fwd_final(x[i + 1], q), fwd_final(x[i + 2], q), fwd_final(x[i + 3], q));
+            *reinterpret_cast<uint4 *>(dst + 16 * t + i) = make_uint4(fwd_final6(x[i], q), fwd_final6(x[i + 1], q),
+                                                                      fwd_final6(x[i + 2], q), fwd_final6(x[i + 3], q));
     } else {
         // round 0: stages 11-8, distance 1, elements 16t .. 16t+15
 #pragma unroll
@@ -102,21 +112,21 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
             const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * t + i);
             x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
         }
-        inv_round16(x, 11, t, W, Wp, q);
+        inv_round16(x, 11, t, T, q);
 #pragma unroll
         for (int i = 0; i < 16; ++i) sm[z.row(i)] = x[i];
         __syncthreads();
         // round 1: stages 7-4, distance 16
 #pragma unroll
         for (int i = 0; i < 16; ++i) x[i] = sm[z.mid(i)];
-        inv_round16(x, 7, t >> 4, W, Wp, q);
+        inv_round16(x, 7, t >> 4, T, q);
 #pragma unroll
         for (int i = 0; i < 16; ++i) sm[z.mid(i)] = x[i];
         __syncthreads();
         // round 2: stages 3-0, distance 256, elements t + 256 i; then N^-1
 #pragma unroll
         for (int i = 0; i < 16; ++i) x[i] = sm[z.col(i)];
-        inv_round16(x, 3, 0, W, Wp, q);
+        inv_round16(x, 3, 0, T, q);
         const uint32_t ni = P.ninv[l], nis = P.ninv_shoup[l];
 #pragma unroll
         for (int i = 0; i < 16; ++i) dst[t + 256 * i] = inv_final(x[i], ni, nis, q);
@@ -126,19 +136,27 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
 // Forward (and lift + forward) for N = 4096 on two rows of the same prime
 // per CTA, rows 2pp*L + l and (2pp+1)*L + l: every twiddle load serves both
 // rows and each thread carries two independent butterfly chains.  Rounds as
-// in ntt4096_kernel; rows placed in shared memory by Swz4096.
+// in ntt4096_kernel; rows placed in shared memory by Swz4096.  (An exchange
+// of the last round's inputs by warp shuffles -- a 16 x 16 transpose inside
+// each half-warp by xor butterflies, 32 shuffles and 64 selects per row --
+// measured slower than the swizzled shared-memory exchange.)
 template <bool LIFT>
-__global__ void __launch_bounds__(kT4) ntt4096x2_fwd_kernel(const uint32_t *__restrict__ in, uint32_t *out,
+__global__ void __launch_bounds__(kT4, 4) ntt4096x2_fwd_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                             uint64_t cnt, const __grid_constant__ RnsParams P) {
     __shared__ __align__(16) uint32_t sa[kN4];
     __shared__ __align__(16) uint32_t sb[kN4];
-    const uint64_t pp = blockIdx.x / P.L;
-    const uint32_t l = blockIdx.x % P.L;
+    // Prime-major CTA order: the CTAs resident on an SM at a time transform
+    // rows of one prime, so one prime's 32 KiB of twiddle pairs stays in L1
+    // (pair-major order kept all L tables live and missed L1 on a third of
+    // the twiddle loads; the lift's raw rows are then re-read from L2 per prime).
+    const uint64_t npairs = (cnt + 1) / 2;
+    const uint64_t pp = blockIdx.x % npairs;
+    const uint32_t l = (uint32_t)(blockIdx.x / npairs);
     const uint64_t p0 = 2 * pp, p1 = p0 + 1;
     const bool two = p1 < cnt;
     const uint32_t q = P.q[l];
-    const uint32_t *W = P.tw + (size_t)l * 4 * kN4 + TW_FWD * kN4;
-    const uint32_t *Wp = P.tw + (size_t)l * 4 * kN4 + TW_FWD_SHOUP * kN4;
+    const uint2 *T = tw_pairs(P.tw, l, kN4, TW_FWD);
+    const uint32_t mb = (uint32_t)(P.mu[l] >> 32);   // floor(2^32 / q) for the lift
     const uint32_t *src0 = in + (LIFT ? p0 : p0 * P.L + l) * kN4;
     const uint32_t *src1 = in + (LIFT ? p1 : p1 * P.L + l) * kN4;
     uint32_t *dst0 = out + (p0 * P.L + l) * kN4, *dst1 = out + (p1 * P.L + l) * kN4;
@@ -146,13 +164,13 @@ __global__ void __launch_bounds__(kT4) ntt4096x2_fwd_kernel(const uint32_t *__re
     uint32_t x[16], y[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const uint32_t a = src0[t + 256 * i];
-        const uint32_t b = two ? src1[t + 256 * i] : 0u;
-        x[i] = LIFT ? a % q : a;
-        y[i] = LIFT ? b % q : b;
+        const uint32_t a = ld_na(src0 + t + 256 * i);
+        const uint32_t b = two ? ld_na(src1 + t + 256 * i) : 0u;
+        x[i] = LIFT ? barrett32_lazy(a, q, mb) : a;   // [0, 2q): the rounds' input range
+        y[i] = LIFT ? barrett32_lazy(b, q, mb) : b;
     }
     const Swz4096 z(t);
-    fwd_round16x2(x, y, 0, 0, W, Wp, q);
+    fwd_round16x2(x, y, 0, 0, T, q);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         sa[z.col(i)] = x[i];
@@ -164,7 +182,7 @@ __global__ void __launch_bounds__(kT4) ntt4096x2_fwd_kernel(const uint32_t *__re
         x[i] = sa[z.mid(i)];
         y[i] = sb[z.mid(i)];
     }
-    fwd_round16x2(x, y, 4, t >> 4, W, Wp, q);
+    fwd_round16x2(x, y, 4, t >> 4, T, q);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         sa[z.mid(i)] = x[i];
@@ -176,19 +194,19 @@ __global__ void __launch_bounds__(kT4) ntt4096x2_fwd_kernel(const uint32_t *__re
         x[i] = sa[z.row(i)];
         y[i] = sb[z.row(i)];
     }
-    fwd_round16x2(x, y, 8, t, W, Wp, q);
+    fwd_round16x2(x, y, 8, t, T, q);
 #pragma unroll
     for (int i = 0; i < 16; i += 4) {
-        *reinterpret_cast<uint4 *>(dst0 + 16 * t + i) =
-            make_uint4(fwd_final(x[i], q), fwd_final(x[i + 1], q), fwd_final(x[i + 2], q), fwd_final(x[i + 3], q));
+        *reinterpret_cast<uint4 *>(dst0 + 16 * t + i) = make_uint4(fwd_final6(x[i], q), fwd_final6(x[i + 1], q),
+                                                                   fwd_final6(x[i + 2], q), fwd_final6(x[i + 3], q));
         if (two)
-            *reinterpret_cast<uint4 *>(dst1 + 16 * t + i) = make_uint4(fwd_final(y[i], q), fwd_final(y[i + 1], q),
-                                                                        fwd_final(y[i + 2], q), fwd_final(y[i + 3], q));
+            *reinterpret_cast<uint4 *>(dst1 + 16 * t + i) = make_uint4(fwd_final6(y[i], q), fwd_final6(y[i + 1], q),
+                                                                       fwd_final6(y[i + 2], q), fwd_final6(y[i + 3], q));
     }
 }
 
 // Inverse for N = 4096 on two rows of one prime per CTA (as the forward).
-__global__ void __launch_bounds__(kT4) ntt4096x2_inv_kernel(const uint32_t *__restrict__ in, uint32_t *out,
+__global__ void __launch_bounds__(kT4, 4) ntt4096x2_inv_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                             uint64_t cnt, const __grid_constant__ RnsParams P) {
     __shared__ __align__(16) uint32_t sa[kN4];
     __shared__ __align__(16) uint32_t sb[kN4];
@@ -197,8 +215,7 @@ __global__ void __launch_bounds__(kT4) ntt4096x2_inv_kernel(const uint32_t *__re
     const uint64_t r0 = (2 * pp) * P.L + l, r1 = (2 * pp + 1) * P.L + l;
     const bool two = 2 * pp + 1 < cnt;
     const uint32_t q = P.q[l];
-    const uint32_t *W = P.tw + (size_t)l * 4 * kN4 + TW_INV * kN4;
-    const uint32_t *Wp = P.tw + (size_t)l * 4 * kN4 + TW_INV_SHOUP * kN4;
+    const uint2 *T = tw_pairs(P.tw, l, kN4, TW_INV);
     const uint32_t t = threadIdx.x;
     uint32_t x[16], y[16];
 #pragma unroll
@@ -208,7 +225,7 @@ __global__ void __launch_bounds__(kT4) ntt4096x2_inv_kernel(const uint32_t *__re
         x[k] = u.x; x[k + 1] = u.y; x[k + 2] = u.z; x[k + 3] = u.w;
         y[k] = v.x; y[k + 1] = v.y; y[k + 2] = v.z; y[k + 3] = v.w;
     }
-    inv4096x2_rounds(x, y, sa, sb, W, Wp, q, P.ninv[l], P.ninv_shoup[l], out + r0 * kN4, out + r1 * kN4, two);
+    inv4096x2_rounds(x, y, sa, sb, T, q, P.ninv[l], P.ninv_shoup[l], out + r0 * kN4, out + r1 * kN4, two);
 }
 
 template <bool FWD, bool LIFT = false>

@@ -9,7 +9,9 @@
 // order).  Inverse: Gentleman-Sande with psi^-brv(m+i), natural-order output,
 // then the factor N^-1.  Butterflies use Shoup products with Harvey's lazy
 // ranges: forward values live in [0, 4q), inverse values in [0, 2q); q < 2^29
-// keeps 4q below 2^32.
+// keeps 4q below 2^32.  The 4096-point forward rounds go further (see
+// fwd_round16).  Twiddles are read as {w, Shoup companion} pairs, one 8-byte
+// load per butterfly.
 //
 // Stages are processed three at a time in registers: a thread loads 8
 // elements spaced by the smallest butterfly distance of the round, runs the
@@ -44,8 +46,7 @@ __device__ __forceinline__ void gs_bfly(uint32_t &x, uint32_t &y, uint32_t w, ui
 // round's R bits (so e = (high << (log2 tlow + R)) | (i << log2 tlow) | low).
 template <int R>
 __device__ __forceinline__ void fwd_round_group(uint32_t *row, uint32_t g, uint32_t tlow, uint32_t s0,
-                                                uint32_t high, const uint32_t *__restrict__ W,
-                                                const uint32_t *__restrict__ Wp, uint32_t q) {
+                                                uint32_t high, const uint2 *__restrict__ T, uint32_t q) {
     constexpr int G = 1 << R;
     uint32_t x[G];
 #pragma unroll
@@ -59,8 +60,8 @@ __device__ __forceinline__ void fwd_round_group(uint32_t *row, uint32_t g, uint3
         for (int i = 0; i < G; ++i) {
             if (i & d) continue;
             uint32_t blk = (high << r) | (uint32_t)(i >> (R - r));
-            uint32_t w = __ldg(W + m + blk), wp = __ldg(Wp + m + blk);
-            ct_bfly(x[i], x[i + d], w, wp, q, q2);
+            const uint2 w = __ldg(T + m + blk);
+            ct_bfly(x[i], x[i + d], w.x, w.y, q, q2);
         }
     }
 #pragma unroll
@@ -72,8 +73,7 @@ __device__ __forceinline__ void fwd_round_group(uint32_t *row, uint32_t g, uint3
 // first (smallest) stage.
 template <int R>
 __device__ __forceinline__ void inv_round_group(uint32_t *row, uint32_t g, uint32_t tlow, uint32_t s_hi,
-                                                uint32_t high, const uint32_t *__restrict__ W,
-                                                const uint32_t *__restrict__ Wp, uint32_t q) {
+                                                uint32_t high, const uint2 *__restrict__ T, uint32_t q) {
     constexpr int G = 1 << R;
     uint32_t x[G];
 #pragma unroll
@@ -87,8 +87,8 @@ __device__ __forceinline__ void inv_round_group(uint32_t *row, uint32_t g, uint3
         for (int i = 0; i < G; ++i) {
             if (i & d) continue;
             uint32_t blk = (high << (R - 1 - r)) | (uint32_t)(i >> (r + 1));
-            uint32_t w = __ldg(W + m + blk), wp = __ldg(Wp + m + blk);
-            gs_bfly(x[i], x[i + d], w, wp, q, q2);
+            const uint2 w = __ldg(T + m + blk);
+            gs_bfly(x[i], x[i + d], w.x, w.y, q, q2);
         }
     }
 #pragma unroll
@@ -114,20 +114,19 @@ __device__ void ntt_rows_smem(uint32_t *sm, uint32_t nrows, const RnsParams &P, 
             const uint32_t r = v >> lg, vv = v & ((1u << lg) - 1);
             const uint32_t l = prime_of(r);
             const uint32_t q = P.q[l];
-            const uint32_t *W = P.tw + (size_t)l * 4 * N + (FWD ? TW_FWD : TW_INV) * N;
-            const uint32_t *Wp = P.tw + (size_t)l * 4 * N + (FWD ? TW_FWD_SHOUP : TW_INV_SHOUP) * N;
+            const uint2 *T = tw_pairs(P.tw, l, N, FWD ? TW_FWD : TW_INV);
             const uint32_t low = vv & (tlow - 1), high = vv >> log_tlow;
             const uint32_t g = (high << (log_tlow + R)) | low;
             uint32_t *row = sm + (size_t)r * N;
             if (FWD) {
-                if (R == 3) fwd_round_group<3>(row, g, tlow, done, high, W, Wp, q);
-                else if (R == 2) fwd_round_group<2>(row, g, tlow, done, high, W, Wp, q);
-                else fwd_round_group<1>(row, g, tlow, done, high, W, Wp, q);
+                if (R == 3) fwd_round_group<3>(row, g, tlow, done, high, T, q);
+                else if (R == 2) fwd_round_group<2>(row, g, tlow, done, high, T, q);
+                else fwd_round_group<1>(row, g, tlow, done, high, T, q);
             } else {
                 const uint32_t s_hi = logN - 1 - done;
-                if (R == 3) inv_round_group<3>(row, g, tlow, s_hi, high, W, Wp, q);
-                else if (R == 2) inv_round_group<2>(row, g, tlow, s_hi, high, W, Wp, q);
-                else inv_round_group<1>(row, g, tlow, s_hi, high, W, Wp, q);
+                if (R == 3) inv_round_group<3>(row, g, tlow, s_hi, high, T, q);
+                else if (R == 2) inv_round_group<2>(row, g, tlow, s_hi, high, T, q);
+                else inv_round_group<1>(row, g, tlow, s_hi, high, T, q);
             }
         }
         __syncthreads();
@@ -181,11 +180,28 @@ struct Swz4096 {
 
 __device__ __forceinline__ uint32_t umin32(uint32_t a, uint32_t b) { return a < b ? a : b; }
 
-// One forward round of 4 stages (s0..s0+3) on x[16] = elements g + tlow*i.
+// The 4096-point forward rounds reduce the upper butterfly input only at
+// stages 3, 5, 7, 9 and 11.  A CT butterfly without reduction maps x in
+// [0, B) and any 32-bit y to x + t and x - t + 2q in [0, B + 2q) (t, the
+// Shoup product, lies in [0, 2q)), and the lower input is never reduced (a
+// Shoup product accepts any 32-bit value).  From inputs below 2q the bound
+// after stage s is 4q, 6q, 8q for s = 0, 1, 2; at a reducing stage x < 8q
+// drops below 4q by one conditional subtraction of 4q, so the bound
+// alternates 6q, 8q.  8q < 2^32 for q < 2^29, and outputs leave below 6q
+// (fwd_final6).
+__host__ __device__ constexpr bool fwd_reduces(uint32_t s) { return s >= 3 && (s & 1); }
+
+__device__ __forceinline__ void ct_bfly_lazy(uint32_t &x, uint32_t &y, uint2 w, uint32_t q, bool reduce) {
+    const uint32_t a = reduce ? umin32(x, x - 4 * q) : x;
+    const uint32_t t = shoup_mul(y, w.x, w.y, q);
+    x = a + t;
+    y = a - t + 2 * q;
+}
+
+// One forward round of 4 stages (s0..s0+3, s0 a compile-time constant at
+// every call) on x[16] = elements g + tlow*i.
 __device__ __forceinline__ void fwd_round16(uint32_t (&x)[16], uint32_t s0, uint32_t high,
-                                            const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
-                                            uint32_t q) {
-    const uint32_t q2 = 2 * q;
+                                            const uint2 *__restrict__ T, uint32_t q) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int d = 16 >> (r + 1);
@@ -193,22 +209,16 @@ __device__ __forceinline__ void fwd_round16(uint32_t (&x)[16], uint32_t s0, uint
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             if (i & d) continue;
-            const uint32_t idx = m + ((high << r) | (uint32_t)(i >> (4 - r)));
-            const uint32_t w = __ldg(W + idx), wp = __ldg(Wp + idx);
-            const uint32_t a = umin32(x[i], x[i] - q2);          // [0, 2q)
-            const uint32_t t = shoup_mul(x[i + d], w, wp, q);    // [0, 2q)
-            x[i] = a + t;
-            x[i + d] = a - t + q2;
+            const uint2 w = __ldg(T + m + ((high << r) | (uint32_t)(i >> (4 - r))));
+            ct_bfly_lazy(x[i], x[i + d], w, q, fwd_reduces(s0 + r));
         }
     }
 }
 
-// fwd_round16 on two rows of the same prime at once: each twiddle is loaded
-// once for both, and the two rows' butterflies are independent work.
+// fwd_round16 on two rows of the same prime at once: each twiddle pair is
+// loaded once for both, and the two rows' butterflies are independent work.
 __device__ __forceinline__ void fwd_round16x2(uint32_t (&x)[16], uint32_t (&y)[16], uint32_t s0, uint32_t high,
-                                              const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
-                                              uint32_t q) {
-    const uint32_t q2 = 2 * q;
+                                              const uint2 *__restrict__ T, uint32_t q) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int d = 16 >> (r + 1);
@@ -216,24 +226,23 @@ __device__ __forceinline__ void fwd_round16x2(uint32_t (&x)[16], uint32_t (&y)[1
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             if (i & d) continue;
-            const uint32_t idx = m + ((high << r) | (uint32_t)(i >> (4 - r)));
-            const uint32_t w = __ldg(W + idx), wp = __ldg(Wp + idx);
-            const uint32_t a = umin32(x[i], x[i] - q2);
-            const uint32_t t = shoup_mul(x[i + d], w, wp, q);
-            x[i] = a + t;
-            x[i + d] = a - t + q2;
-            const uint32_t b = umin32(y[i], y[i] - q2);
-            const uint32_t u = shoup_mul(y[i + d], w, wp, q);
-            y[i] = b + u;
-            y[i + d] = b - u + q2;
+            const uint2 w = __ldg(T + m + ((high << r) | (uint32_t)(i >> (4 - r))));
+            ct_bfly_lazy(x[i], x[i + d], w, q, fwd_reduces(s0 + r));
+            ct_bfly_lazy(y[i], y[i + d], w, q, fwd_reduces(s0 + r));
         }
     }
+}
+
+// Final reduction of the 4096-point forward outputs: [0, 6q) -> [0, q).
+__device__ __forceinline__ uint32_t fwd_final6(uint32_t x, uint32_t q) {
+    x = umin32(x, x - 4 * q);
+    x = umin32(x, x - 2 * q);
+    return umin32(x, x - q);
 }
 
 // One inverse round of 4 stages s_hi..s_hi-3 on x[16] = elements g + tlow*i.
 __device__ __forceinline__ void inv_round16(uint32_t (&x)[16], uint32_t s_hi, uint32_t high,
-                                            const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
-                                            uint32_t q) {
+                                            const uint2 *__restrict__ T, uint32_t q) {
     const uint32_t q2 = 2 * q;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -242,20 +251,18 @@ __device__ __forceinline__ void inv_round16(uint32_t (&x)[16], uint32_t s_hi, ui
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             if (i & d) continue;
-            const uint32_t idx = m + ((high << (3 - r)) | (uint32_t)(i >> (r + 1)));
-            const uint32_t w = __ldg(W + idx), wp = __ldg(Wp + idx);
+            const uint2 w = __ldg(T + m + ((high << (3 - r)) | (uint32_t)(i >> (r + 1))));
             const uint32_t u = x[i] + x[i + d];
             const uint32_t v = x[i] - x[i + d] + q2;
             x[i] = umin32(u, u - q2);                            // [0, 2q)
-            x[i + d] = shoup_mul(v, w, wp, q);                   // [0, 2q)
+            x[i + d] = shoup_mul(v, w.x, w.y, q);                // [0, 2q)
         }
     }
 }
 
 // inv_round16 on two rows of the same prime (shared twiddle loads).
 __device__ __forceinline__ void inv_round16x2(uint32_t (&x)[16], uint32_t (&y)[16], uint32_t s_hi, uint32_t high,
-                                              const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
-                                              uint32_t q) {
+                                              const uint2 *__restrict__ T, uint32_t q) {
     const uint32_t q2 = 2 * q;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -264,16 +271,15 @@ __device__ __forceinline__ void inv_round16x2(uint32_t (&x)[16], uint32_t (&y)[1
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             if (i & d) continue;
-            const uint32_t idx = m + ((high << (3 - r)) | (uint32_t)(i >> (r + 1)));
-            const uint32_t w = __ldg(W + idx), wp = __ldg(Wp + idx);
+            const uint2 w = __ldg(T + m + ((high << (3 - r)) | (uint32_t)(i >> (r + 1))));
             const uint32_t u = x[i] + x[i + d];
             const uint32_t v = x[i] - x[i + d] + q2;
             x[i] = umin32(u, u - q2);
-            x[i + d] = shoup_mul(v, w, wp, q);
+            x[i + d] = shoup_mul(v, w.x, w.y, q);
             const uint32_t a = y[i] + y[i + d];
             const uint32_t b = y[i] - y[i + d] + q2;
             y[i] = umin32(a, a - q2);
-            y[i + d] = shoup_mul(b, w, wp, q);
+            y[i + d] = shoup_mul(b, w.x, w.y, q);
         }
     }
 }
@@ -283,12 +289,11 @@ __device__ __forceinline__ void inv_round16x2(uint32_t (&x)[16], uint32_t (&y)[1
 // [0, 2q)) are already in x and y; the results (natural order, times N^-1,
 // canonical) go to dst0 and dst1 (dst1 skipped when !two).
 __device__ __forceinline__ void inv4096x2_rounds(uint32_t (&x)[16], uint32_t (&y)[16], uint32_t *sa, uint32_t *sb,
-                                                 const uint32_t *__restrict__ W, const uint32_t *__restrict__ Wp,
-                                                 uint32_t q, uint32_t ni, uint32_t nis, uint32_t *dst0, uint32_t *dst1,
-                                                 bool two) {
+                                                 const uint2 *__restrict__ T, uint32_t q, uint32_t ni, uint32_t nis,
+                                                 uint32_t *dst0, uint32_t *dst1, bool two) {
     const uint32_t t = threadIdx.x;
     const Swz4096 z(t);
-    inv_round16x2(x, y, 11, t, W, Wp, q);
+    inv_round16x2(x, y, 11, t, T, q);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
         sa[z.row(k)] = x[k];
@@ -300,7 +305,7 @@ __device__ __forceinline__ void inv4096x2_rounds(uint32_t (&x)[16], uint32_t (&y
         x[k] = sa[z.mid(k)];
         y[k] = sb[z.mid(k)];
     }
-    inv_round16x2(x, y, 7, t >> 4, W, Wp, q);
+    inv_round16x2(x, y, 7, t >> 4, T, q);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
         sa[z.mid(k)] = x[k];
@@ -312,7 +317,7 @@ __device__ __forceinline__ void inv4096x2_rounds(uint32_t (&x)[16], uint32_t (&y
         x[k] = sa[z.col(k)];
         y[k] = sb[z.col(k)];
     }
-    inv_round16x2(x, y, 3, 0, W, Wp, q);
+    inv_round16x2(x, y, 3, 0, T, q);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
         dst0[t + 256 * k] = inv_final(x[k], ni, nis, q);

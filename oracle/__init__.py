@@ -12,7 +12,10 @@ Every function restates a definition from the pages (see oracle.c):
   * GPIR sections 2-3 and VIPIR 3.6 step 7: ColTor, the column tournament of
     RGSW-RLWE external products with the gadget decomposition Dcp (l = 5);
   * GPIR sections 2-3: ExpandQuery, the expansion tree of Subs operations
-    (automorphism and key switching of the a polynomial).
+    (automorphism and key switching of the a polynomial);
+  * GPIR section 2 (the expanded query also yields the RGSW ciphertexts of
+    the column bits): the conversion of the expanded gadget ciphertexts
+    RLWE'(m) into RGSW(m) with a key-switching key of s^2 (a reading).
 """
 from __future__ import annotations
 
@@ -93,6 +96,9 @@ def lib():
         L.orc_subs.restype = None
         L.orc_subs.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint32, ctypes.c_uint32,
                                ctypes.c_uint32, _u32p, _u32p, _u32p]
+        L.orc_rgsw_convert.restype = None
+        L.orc_rgsw_convert.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint32,
+                                       ctypes.c_uint32, _u32p, _u32p, _u32p]
         L.orc_expand_stage.restype = None
         L.orc_expand_stage.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint32,
                                        ctypes.c_uint32, ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint64, _u32p,
@@ -361,3 +367,19 @@ def expand(evks: np.ndarray, ct: np.ndarray, stages: int, qs, psis, ell: int, w:
     for j in range(stages):
         cur = expand_stage(evks[j], cur, j, qs, psis, ell, w, threads)
     return cur
+
+
+def rgsw_convert(ksk: np.ndarray, cts: np.ndarray, qs, psis, ell: int, w: int) -> np.ndarray:
+    """RGSW(m) [2 ell][2][L][N] from RLWE'(m) = cts [ell][2][L][N] (ciphertexts of
+    m g_u) and the key-switching key ksk [ell][2][L][N] (ciphertexts of s^2 g_v),
+    all NTT form: rows u are cts[u], rows ell + u = (0, c0_u) + sum_v
+    NTT(Dcp_v(c1_u)) . ksk[v]."""
+    ksk = np.ascontiguousarray(ksk, dtype=np.uint32)
+    cts = np.ascontiguousarray(cts, dtype=np.uint32)
+    _, _, L, N = cts.shape
+    assert cts.shape == (ell, 2, L, N) and ksk.shape == (ell, 2, L, N)
+    q = np.asarray(qs, dtype=np.uint32)
+    ps = np.asarray(psis, dtype=np.uint32)
+    out = np.empty((2 * ell, 2, L, N), dtype=np.uint32)
+    lib().orc_rgsw_convert(N, L, _p32(q), _p32(ps), ell, w, _p32(ksk), _p32(cts), _p32(out))
+    return out

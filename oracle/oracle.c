@@ -735,3 +735,58 @@ void orc_expand_stage(uint32_t N, uint32_t L, const uint32_t *q, const uint32_t 
     }
     for (int i = 0; i < nthreads; i++) pthread_join(th[i], NULL);
 }
+
+/* ------------------------------------------------------------------ */
+/* RGSW ciphertexts from the expanded query                             */
+/* [GPIR section 2: the expanded query ciphertext carries both indices,  */
+/*  the expansion yields the D0 RowSel ciphertexts "and RGSW"            */
+/*  ciphertexts; the conversion itself is not defined on the pages]      */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Reading: the client places m g_u (g_u = 2^(w u), the gadget of orc_dcp)
+ * in ell query coefficients, so the expansion yields RLWE'(m) = the ell
+ * ciphertexts ct_u = (c0_u, c1_u) of m g_u.  An RGSW ciphertext of m in the
+ * row layout of orc_ext_product needs rows u encrypting m g_u (ct_u itself)
+ * and rows ell + u encrypting m s g_u.  With a key-switching key
+ * ksk[v] = RLWE(s^2 g_v) the latter is
+ *     C[ell + u] = (0, c0_u) + sum_{v<ell} NTT(Dcp_v(c1_u)) (.) ksk[v]
+ * which decrypts to c0_u s + c1_u s^2 = s (c0_u + c1_u s) = m s g_u + s e_u.
+ *   ksk : [ell][2][L][N], NTT form.
+ *   in  : [ell][2][L][N], NTT form (ct_u for u < ell).
+ *   out : [2 ell][2][L][N], NTT form (out[u] = ct_u, out[ell + u] above).
+ * c1_u is brought to coefficient form by the inverse NTT before Dcp.
+ */
+void orc_rgsw_convert(uint32_t N, uint32_t L, const uint32_t *q, const uint32_t *psi, uint32_t ell,
+                      uint32_t w, const uint32_t *ksk, const uint32_t *in, uint32_t *out)
+{
+    uint64_t PN = (uint64_t)L * N, CT = 2 * PN;
+    uint32_t *c1 = (uint32_t *)malloc(sizeof(uint32_t) * PN);
+    uint32_t *d = (uint32_t *)malloc(sizeof(uint32_t) * ell * N);
+    uint32_t *dn = (uint32_t *)malloc(sizeof(uint32_t) * ell * PN);
+    for (uint32_t u = 0; u < ell; u++) {
+        const uint32_t *ct = in + u * CT;
+        memcpy(out + u * CT, ct, sizeof(uint32_t) * CT);
+        memcpy(c1, ct + PN, sizeof(uint32_t) * PN);
+        for (uint32_t l = 0; l < L; l++) orc_intt_iter(q[l], psi[l], N, c1 + (uint64_t)l * N);
+        orc_dcp(N, L, q, ell, w, c1, d);
+        for (uint32_t v = 0; v < ell; v++)
+            for (uint32_t l = 0; l < L; l++) {
+                uint32_t *row = dn + ((uint64_t)v * L + l) * N;
+                for (uint32_t t = 0; t < N; t++) row[t] = d[(uint64_t)v * N + t] % q[l];
+                orc_ntt_iter(q[l], psi[l], N, row);
+            }
+        uint32_t *dst = out + (ell + u) * CT;
+        for (uint32_t p = 0; p < 2; p++)
+            for (uint32_t l = 0; l < L; l++)
+                for (uint32_t j = 0; j < N; j++) {
+                    u128 acc = p == 1 ? ct[(uint64_t)l * N + j] : 0;     /* (0, c0) */
+                    for (uint32_t v = 0; v < ell; v++)
+                        acc += (u128)dn[((uint64_t)v * L + l) * N + j] * ksk[(((uint64_t)v * 2 + p) * L + l) * N + j];
+                    dst[p * PN + (uint64_t)l * N + j] = (uint32_t)(acc % q[l]);
+                }
+    }
+    free(c1);
+    free(d);
+    free(dn);
+}
