@@ -356,6 +356,40 @@ int pir_expand_batch(pir_ctx *ctx, const uint32_t *evks, uint32_t ell, uint32_t 
 uint64_t pir_scalar_workspace_bytes(uint64_t C, uint32_t B);
 
 /*
+ * pir_rgsw_convert — the RGSW ciphertexts of the column tournament from the
+ * expanded query (GPIR section 2: the query ciphertext carries both the row
+ * and the column index, and the expansion yields the D0 RowSel ciphertexts
+ * and RGSW ciphertexts; the pages do not define the conversion, this is a
+ * reading).  The client places m g_u (g_u = 2^(w u), the gadget of
+ * pir_coltor, pre-scaled by 2^-S for an S-stage expansion) in ell query
+ * coefficients, so the expansion yields RLWE'(m) = the ell ciphertexts
+ * ct_u = (c0_u, c1_u) of m g_u.  The RGSW ciphertext of m in pir_coltor's
+ * row layout is
+ *     C[u] = ct_u,    C[ell + u] = (0, c0_u) + sum_v NTT(Dcp_v(c1_u)) . ksk[v]
+ * where ksk[v] is an RLWE encryption of s^2 g_v under the client's secret s
+ * (a key-switching key); row ell + u decrypts to s (c0_u + c1_u s) = m s g_u.
+ *   ksk  : device, [G][ell][2][L][N] NTT form, client b's key at
+ *          b * ell * 2 L N words.
+ *   in   : device, [G][n][ell][2][L][N] NTT form: client b's n gadget lists
+ *          (e.g. its ceil(log2 D1) column bits), canonical residues.
+ *   out  : device, [G][n][2 ell][2][L][N] NTT form: the RGSW ciphertexts, as
+ *          pir_coltor_batch takes them ([G][S][2 ell][2][L][N] with S = n).
+ *   ell, w : as for pir_coltor.
+ *   workspace : device, >= pir_rgsw_convert_workspace_bytes(ctx, n, G, ell)
+ *          bytes (0 when n G ell >= 2^31), 16-byte aligned; the part the
+ *          call uses overlaps neither in nor out; contents undefined after.
+ * The library owns nothing the caller passes; asynchronous on stream.
+ * Errors: PIR_ERR_ARG (NULL/unaligned pointers, n = 0, G = 0, n G ell >=
+ * 2^31, ell or w out of range, digits not covering Q, workspace too small,
+ * overlaps), PIR_ERR_CUDA.
+ */
+uint64_t pir_rgsw_convert_workspace_bytes(const pir_ctx *ctx, uint64_t n, uint64_t G, uint32_t ell);
+
+int pir_rgsw_convert(pir_ctx *ctx, const uint32_t *ksk, uint32_t ell, uint32_t w,
+                     const uint32_t *in, uint64_t n, uint64_t G, uint32_t *out,
+                     void *workspace, uint64_t workspace_bytes, void *stream);
+
+/*
  * pir_scalar_scan — scalar-HE DB fold (VIPIR 2.5 and 4.1):
  *   out[r][b] = sum_{c<C} db[r][c] * Q[c][b]  mod 2^32
  * with the 4-way byte split of Q (Q = sum_i 2^(8i) Q_i, VIPIR 4.1).

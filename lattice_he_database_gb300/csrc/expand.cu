@@ -23,6 +23,14 @@
 //   4. expand_mac_kernel         the key switch, sigma_k(c0) by slot
 //      permutation, and both outputs with the monomial's NTT
 //
+// RGSW ciphertexts from the expansion (pir_rgsw_convert; a reading, the pages
+// say only that the expanded query also yields the RGSW ciphertexts of the
+// column tournament): the expansion outputs ct_u = RLWE(m g_u), u < ell, are
+// the rows u of RGSW(m); rows ell + u = (0, c0_u) + sum_v NTT(Dcp_v(c1_u)) .
+// ksk[v] with ksk[v] = RLWE(s^2 g_v), which decrypt to s (c0_u + c1_u s) =
+// m s g_u.  The same four launches as a stage, without the automorphism:
+// inverse NTT of c1, Dcp, lift + NTT of the digits, rgsw_mac_kernel.
+//
 // Batches: G expansions (one per client, each with its own keys) run as one
 // expansion of G*M ciphertexts per stage; global ciphertext g belongs to
 // client b = g / M, and client b's outputs i and i + M go to b*2M + i and
@@ -157,6 +165,56 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
     }
 }
 
+struct RgswMacArgs {
+    const uint32_t *in;     // [M][2][L][N] gadget ciphertexts, M = G * n * ell
+    const uint32_t *dn;     // [M][ell][L][N] NTT of the digits of c1
+    const uint32_t *ksk;    // client b's key [ell][2][L][N] at ksk + b * ksk_stride
+    uint32_t *out;          // [G * n][2 ell][2][L][N]
+    uint64_t M, per_client, ksk_stride;   // per_client = n * ell input ciphertexts
+    uint32_t N, L, ell;
+    uint32_t q[PIR_MAX_RNS];
+    uint64_t mu[PIR_MAX_RNS];
+};
+
+// Four consecutive slots per thread: input ciphertext i = (RGSW r, row u)
+// goes to row u of RGSW r unchanged and, key-switched, to row ell + u.
+__global__ void __launch_bounds__(GD_THREADS) rgsw_mac_kernel(const RgswMacArgs A) {
+    const uint64_t LN = (uint64_t)A.L * A.N;
+    const uint64_t total4 = A.M * LN / 4;
+    for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total4;
+         e += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t e0 = e * 4;
+        const uint64_t i = e0 / LN, pt = e0 - i * LN;    // pt = l * N + slot
+        const uint32_t l = (uint32_t)(pt / A.N);
+        const uint32_t q = pick(A.q, l);
+        const uint64_t mu = pick(A.mu, l);
+        const uint32_t b = (uint32_t)i / (uint32_t)A.per_client;   // M < 2^31 (checked on the host)
+        const uint32_t *dp = A.dn + i * A.ell * LN + pt;
+        const uint32_t *kp = A.ksk + b * A.ksk_stride + pt;
+        uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
+#pragma unroll 4
+        for (uint32_t u = 0; u < A.ell; ++u) {
+            const uint4 d = *reinterpret_cast<const uint4 *>(dp + (uint64_t)u * LN);
+            const uint4 k0 = __ldg(reinterpret_cast<const uint4 *>(kp + (uint64_t)(2 * u) * LN));
+            const uint4 k1 = __ldg(reinterpret_cast<const uint4 *>(kp + (uint64_t)(2 * u + 1) * LN));
+            a0 += (uint64_t)d.x * k0.x; a1 += (uint64_t)d.y * k0.y; a2 += (uint64_t)d.z * k0.z; a3 += (uint64_t)d.w * k0.w;
+            b0 += (uint64_t)d.x * k1.x; b1 += (uint64_t)d.y * k1.y; b2 += (uint64_t)d.z * k1.z; b3 += (uint64_t)d.w * k1.w;
+        }
+        const uint4 v0 = *reinterpret_cast<const uint4 *>(A.in + i * 2 * LN + pt);
+        const uint4 v1 = *reinterpret_cast<const uint4 *>(A.in + i * 2 * LN + LN + pt);
+        const uint64_t r = i / A.ell, u = i - r * A.ell;
+        uint32_t *row_u = A.out + (r * 2 * A.ell + u) * 2 * LN + pt;
+        uint32_t *row_s = A.out + (r * 2 * A.ell + A.ell + u) * 2 * LN + pt;
+        *reinterpret_cast<uint4 *>(row_u) = v0;
+        *reinterpret_cast<uint4 *>(row_u + LN) = v1;
+        *reinterpret_cast<uint4 *>(row_s) =
+            make_uint4(barrett64(a0, q, mu), barrett64(a1, q, mu), barrett64(a2, q, mu), barrett64(a3, q, mu));
+        *reinterpret_cast<uint4 *>(row_s + LN) =
+            make_uint4(addq(v0.x, barrett64(b0, q, mu), q), addq(v0.y, barrett64(b1, q, mu), q),
+                       addq(v0.z, barrett64(b2, q, mu), q), addq(v0.w, barrett64(b3, q, mu), q));
+    }
+}
+
 uint64_t align64(uint64_t words) { return (words + 63) / 64 * 64; }
 
 // Workspace (words) for stages of at most Mmax input ciphertexts: c1 in
@@ -185,16 +243,10 @@ uint32_t inv_mod_2n(uint32_t k, uint32_t twoN) {
     return x & (twoN - 1);
 }
 
-// Stage j of G expansions: in [G][M], out [G][2M]; client b's key at
-// evk + b * evk_stride.
-int one_stage(pir_ctx *ctx, const uint32_t *evk, uint64_t evk_stride, uint32_t ell, uint32_t w, uint32_t j,
-              const uint32_t *in, uint64_t M, uint64_t G, uint32_t *out, uint32_t *ws, const ExLayout &lay,
-              cudaStream_t st) {
-    const uint64_t LN = (uint64_t)ctx->L * ctx->N, GM = G * M;
-    uint32_t *coef = ws + lay.coef, *dig = ws + lay.dig, *dn = ws + lay.dn;
-    const uint32_t k = (ctx->N >> j) + 1;
-    int rc = PIR_OK;
-
+// The a polynomial c1 of each of the GM ciphertexts in `in` ([GM][2][L][N],
+// NTT form) in coefficient form, coef [GM][L][N].
+int c1_to_coef(pir_ctx *ctx, const uint32_t *in, uint64_t GM, uint32_t *coef, cudaStream_t st) {
+    const uint64_t LN = (uint64_t)ctx->L * ctx->N;
     if (ctx->N == (uint32_t)kN4) {
         InttAArgs ia;
         memset(&ia, 0, sizeof(ia));
@@ -210,14 +262,26 @@ int one_stage(pir_ctx *ctx, const uint32_t *evk, uint64_t evk_stride, uint32_t e
         if ((GM + 1) / 2 * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
         ia.M = GM;
         expand_intt_a4096_kernel<<<(unsigned)((GM + 1) / 2 * ctx->L), kT4, 0, st>>>(ia);
-        if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
-    } else {
-        if (cudaMemcpy2DAsync(coef, LN * 4, in + LN, 2 * LN * 4, LN * 4, GM, cudaMemcpyDeviceToDevice, st) !=
-            cudaSuccess)
-            return PIR_ERR_CUDA;
-        rc = pir_ntt_inv(ctx, coef, coef, GM, st);
-        if (rc) return rc;
+        return cudaGetLastError() == cudaSuccess ? PIR_OK : PIR_ERR_CUDA;
     }
+    if (cudaMemcpy2DAsync(coef, LN * 4, in + LN, 2 * LN * 4, LN * 4, GM, cudaMemcpyDeviceToDevice, st) !=
+        cudaSuccess)
+        return PIR_ERR_CUDA;
+    return pir_ntt_inv(ctx, coef, coef, GM, st);
+}
+
+// Stage j of G expansions: in [G][M], out [G][2M]; client b's key at
+// evk + b * evk_stride.
+int one_stage(pir_ctx *ctx, const uint32_t *evk, uint64_t evk_stride, uint32_t ell, uint32_t w, uint32_t j,
+              const uint32_t *in, uint64_t M, uint64_t G, uint32_t *out, uint32_t *ws, const ExLayout &lay,
+              cudaStream_t st) {
+    const uint64_t LN = (uint64_t)ctx->L * ctx->N, GM = G * M;
+    uint32_t *coef = ws + lay.coef, *dig = ws + lay.dig, *dn = ws + lay.dn;
+    const uint32_t k = (ctx->N >> j) + 1;
+    int rc = PIR_OK;
+
+    rc = c1_to_coef(ctx, in, GM, coef, st);
+    if (rc) return rc;
 
     rc = gadget_dcp_launch(ctx, gadget_dcp_args(ctx, coef, LN, dig, GM, ell, w, inv_mod_2n(k, 2 * ctx->N)), st);
     if (rc) return rc;
@@ -313,4 +377,74 @@ extern "C" int pir_expand(pir_ctx *ctx, const uint32_t *evks, uint32_t ell, uint
                           const uint32_t *ct, uint32_t *out, void *workspace, uint64_t workspace_bytes,
                           void *stream) {
     return pir_expand_batch(ctx, evks, ell, w, stages, ct, 1, out, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------- RGSW conversion
+namespace {
+
+// Workspace (words) of pir_rgsw_convert over M gadget ciphertexts.
+struct RgLayout {
+    uint64_t coef, dig, dn, total;
+};
+
+RgLayout rg_layout(const pir_ctx *ctx, uint64_t M, uint32_t ell) {
+    const uint64_t LN = (uint64_t)ctx->L * ctx->N;
+    RgLayout r;
+    r.coef = 0;
+    r.dig = align64(M * LN);
+    r.dn = r.dig + align64(M * ell * (uint64_t)ctx->N);
+    r.total = r.dn + align64(M * ell * LN);
+    return r;
+}
+
+}  // namespace
+
+extern "C" uint64_t pir_rgsw_convert_workspace_bytes(const pir_ctx *ctx, uint64_t n, uint64_t G, uint32_t ell) {
+    if (!ctx || n == 0 || G == 0 || ell == 0 || ell > GD_MAX_ELL || n > (1ull << 31) || G > (1ull << 31) ||
+        n * G * ell >= (1ull << 31))
+        return 0;
+    return rg_layout(ctx, n * G * ell, ell).total * 4;
+}
+
+extern "C" int pir_rgsw_convert(pir_ctx *ctx, const uint32_t *ksk, uint32_t ell, uint32_t w, const uint32_t *in,
+                                uint64_t n, uint64_t G, uint32_t *out, void *workspace, uint64_t workspace_bytes,
+                                void *stream) {
+    if (!ctx || !ksk || !in || !out || !workspace || n == 0 || G == 0) return PIR_ERR_ARG;
+    if (!gadget_params_ok(ctx, ell, w) || n > (1ull << 31) || G > (1ull << 31) || n * G * ell >= (1ull << 31))
+        return PIR_ERR_ARG;
+    if (!aligned16(ksk) || !aligned16(in) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
+    const uint64_t M = n * G * ell, LN = (uint64_t)ctx->L * ctx->N;
+    const RgLayout lay = rg_layout(ctx, M, ell);
+    if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
+    const uint64_t in_b = M * 2 * LN * 4, out_b = 2 * M * 2 * LN * 4, ws_b = lay.total * 4;
+    if (overlaps(in, in_b, out, out_b) || overlaps(workspace, ws_b, in, in_b) || overlaps(workspace, ws_b, out, out_b))
+        return PIR_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint32_t *ws = static_cast<uint32_t *>(workspace);
+    uint32_t *coef = ws + lay.coef, *dig = ws + lay.dig, *dn = ws + lay.dn;
+    int rc = c1_to_coef(ctx, in, M, coef, st);
+    if (rc) return rc;
+    rc = gadget_dcp_launch(ctx, gadget_dcp_args(ctx, coef, LN, dig, M, ell, w, 1), st);
+    if (rc) return rc;
+    rc = pir_lift_ntt(ctx, dig, dn, M * ell, st);
+    if (rc) return rc;
+    RgswMacArgs ma;
+    memset(&ma, 0, sizeof(ma));
+    ma.in = in;
+    ma.dn = dn;
+    ma.ksk = ksk;
+    ma.out = out;
+    ma.M = M;
+    ma.per_client = n * ell;
+    ma.ksk_stride = (uint64_t)ell * 2 * LN;
+    ma.N = ctx->N;
+    ma.L = ctx->L;
+    ma.ell = ell;
+    for (uint32_t l = 0; l < ctx->L; ++l) {
+        ma.q[l] = ctx->q[l];
+        ma.mu[l] = ctx->mu[l];
+    }
+    rgsw_mac_kernel<<<(unsigned)gadget_grid(ctx, M * LN / 4), GD_THREADS, 0, st>>>(ma);
+    return launch_status(cudaGetLastError());
 }

@@ -111,6 +111,11 @@ def lib() -> ctypes.CDLL:
         L.pir_expand_batch.restype = ctypes.c_int
         L.pir_expand_batch.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, _vp,
                                        ctypes.c_uint64, _vp, _vp, ctypes.c_uint64, _vp]
+        L.pir_rgsw_convert_workspace_bytes.restype = ctypes.c_uint64
+        L.pir_rgsw_convert_workspace_bytes.argtypes = [_vp, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
+        L.pir_rgsw_convert.restype = ctypes.c_int
+        L.pir_rgsw_convert.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, ctypes.c_uint64,
+                                       ctypes.c_uint64, _vp, _vp, ctypes.c_uint64, _vp]
         L.pir_status.restype = ctypes.c_int
         L.pir_status.argtypes = [_vp, _u32p, ctypes.c_int]
         L.pir_ctx_set_wait_limit.restype = ctypes.c_int
@@ -507,3 +512,24 @@ class PirServer:
         ms = ctypes.c_float()
         _check(lib().pir_server_elapsed_ms(self.handle, ctypes.byref(ms)), "pir_server_elapsed_ms")
         return float(ms.value)
+
+
+# ---------------------------------------------------------------- RGSW from the expanded query
+def pir_rgsw_convert_workspace_bytes(ctx: Ctx, n: int, G: int, ell: int) -> int:
+    return int(lib().pir_rgsw_convert_workspace_bytes(ctx, n, G, ell))
+
+
+def rgsw_convert_workspace(ctx: Ctx, n: int, G: int, ell: int, device="cuda") -> torch.Tensor:
+    """A device workspace for pir_rgsw_convert of G clients x n RGSW ciphertexts."""
+    return torch.empty(pir_rgsw_convert_workspace_bytes(ctx, n, G, ell), dtype=torch.uint8, device=device)
+
+
+def pir_rgsw_convert(ctx: Ctx, ksk: torch.Tensor, ell: int, w: int, cts: torch.Tensor, n: int, G: int,
+                     out: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """RGSW ciphertexts [G][n][2 ell][2][L][N] from the expanded gadget
+    ciphertexts [G][n][ell][2][L][N] and each client's key-switching key of
+    s^2 ([G][ell][2][L][N]), all NTT form."""
+    ws = _dev_ptr(workspace, workspace.element_size(), "workspace")
+    _check(lib().pir_rgsw_convert(ctx, _dev_ptr(ksk, 4, "ksk"), ell, w, _dev_ptr(cts, 4, "in"), n, G,
+                                  _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(),
+                                  _stream(stream)), "pir_rgsw_convert")

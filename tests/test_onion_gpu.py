@@ -7,6 +7,13 @@ which only i* decrypts to a nonzero constant (2^S); RowSel's point-wise GEMM
 with the encoded DB gives, for every column n, a ciphertext of
 2^S DB[i*][n]; ColTor with RGSW encryptions of the bits of j* keeps column
 j*.  The decryption of the final ciphertext must equal 2^S DB[i*][j*].
+
+In the one-ciphertext form (GPIR section 2: the query carries both indices)
+the same query also carries, in coefficients D0 .. D0 + T ell - 1, the
+gadget values b_s g_u of the bits b_s of j* pre-scaled by 2^-S; the
+expansion turns them into the gadget ciphertexts of each bit and
+pir_rgsw_convert, with a key-switching key of s^2, into the RGSW
+ciphertexts ColTor takes.
 """
 import numpy as np
 import pytest
@@ -14,7 +21,7 @@ import pytest
 import oracle
 import synth
 from tests.helpers import ensure_built, to_dev, to_host_u32
-from tests.test_expand_oracle import Keys, _mul, _rand, _signed, _sub
+from tests.test_expand_oracle import Keys, _mul, _qcol, _rand, _signed, _sub
 
 pytestmark = pytest.mark.gpu
 
@@ -105,6 +112,101 @@ def test_batch_of_clients_on_the_tensor_path(pir):
     answers = pir.empty_u32(B * 2 * P)
     pir.pir_coltor_batch(ctx, to_dev(np.stack(rgsws)), ell, w, cols, D1, B, answers,
                          pir.coltor_batch_workspace(ctx, D1, B, ell))
+    assert pir.pir_status(ctx) == 0
+    got = to_host_u32(answers).reshape(B, 2, L, N)
+    for b, (K, istar, jstar) in enumerate(clients):
+        assert np.array_equal(K.decrypt(got[b]), _signed(raw[istar, jstar].astype(np.int64) << S, K.qs)), b
+
+
+def _ksk(K):
+    """Key-switching key: noise-free encryptions of s^2 g_v, v < ell."""
+    N = K.N
+    full = np.convolve(K.s.astype(np.int64), K.s.astype(np.int64))
+    s2 = full[:N].copy()
+    s2[: len(full) - N] -= full[N:]
+    rows = []
+    for v in range(K.ell):
+        g = np.array([pow(2, K.w * v, q) for q in K.qs], dtype=np.uint64).reshape(-1, 1)
+        rows.append(K.encrypt(((_signed(s2, K.qs).astype(np.uint64) * g) % _qcol(K.qs)).astype(np.uint32)))
+    return np.stack(rows)
+
+
+def _one_ciphertext_query(K, D0, T, istar, jstar, S):
+    """[L][N] plaintext residues: X^(i*) in the first D0 coefficients, and
+    2^-S b_s g_u at D0 + s ell + u for the bits b_s of j*."""
+    m = np.zeros((len(K.qs), K.N), dtype=np.uint32)
+    m[:, istar] = 1
+    for s in range(T):
+        if (jstar >> s) & 1:
+            for u in range(K.ell):
+                for l, q in enumerate(K.qs):
+                    m[l, D0 + s * K.ell + u] = pow(2, K.w * u, q) * pow(pow(2, S, q), -1, q) % q
+    return m
+
+
+@pytest.mark.parametrize("D0,D1,istar,jstar", [(16, 11, 9, 6), (64, 40, 1, 39)])
+def test_one_query_ciphertext_with_converted_rgsw(pir, D0, D1, istar, jstar):
+    N, L, ell, w = 4096, 3, 5, 18
+    K = Keys(N, L, ell, w, seed=3 * D0 + D1)
+    ctx = pir.pir_ctx_create(N, K.qs)
+    T = oracle.coltor_stages(D1)
+    S = (D0 + T * ell - 1).bit_length()          # expansion outputs cover the row and the column part
+    raw = synth.coeffs(D0 + 1, (D0, D1, N))
+    db = pir.empty_u32(pir.pir_db_bytes(ctx, D0, D1) // 4)
+    pir.pir_db_encode(ctx, to_dev(raw), 0, D0, D0, D1, db)
+    query = K.encrypt(_one_ciphertext_query(K, D0, T, istar, jstar, S))
+    evks = np.stack([K.evk(N // (1 << j) + 1) for j in range(S)])
+    expanded = pir.empty_u32((1 << S) * 2 * L * N)
+    pir.pir_expand(ctx, to_dev(evks), ell, w, S, to_dev(query), expanded, pir.expand_workspace(ctx, 1 << (S - 1), ell))
+    P2 = 2 * L * N
+    rgsw = pir.empty_u32(T * 2 * ell * P2)
+    pir.pir_rgsw_convert(ctx, to_dev(_ksk(K)), ell, w, expanded[D0 * P2:(D0 + T * ell) * P2], T, 1, rgsw,
+                         pir.rgsw_convert_workspace(ctx, T, 1, ell))
+    cols = pir.empty_u32(D1 * P2)
+    pir.pir_rowsel(ctx, db, D0, D1, expanded[: D0 * P2], 1, cols, pir.rowsel_workspace(ctx, D0, D1, 1))
+    answer = pir.empty_u32(P2)
+    pir.pir_coltor(ctx, rgsw, ell, w, cols, D1, answer, pir.coltor_workspace(ctx, D1, ell))
+    assert pir.pir_status(ctx) == 0
+    got = K.decrypt(to_host_u32(answer).reshape(2, L, N))
+    assert np.array_equal(got, _signed(raw[istar, jstar].astype(np.int64) << S, K.qs))
+
+
+def test_batch_of_one_ciphertext_queries_on_the_tensor_path(pir):
+    """Nine clients, each sending one query ciphertext (row and column
+    index), their own expansion keys and key-switching key: one batched
+    expansion, one batched conversion to RGSW, one RowSel pass of B = 9
+    queries on the tensor cores, one batched tournament."""
+    N, L, ell, w, D0, D1, B = 4096, 3, 5, 18, 16, 11, 9
+    T = oracle.coltor_stages(D1)
+    S = (D0 + T * ell - 1).bit_length()
+    qs = oracle.primes(N, L)
+    ctx = pir.pir_ctx_create(N, qs)
+    raw = synth.coeffs(91, (D0, D1, N))
+    db = pir.empty_u32(pir.pir_db_bytes(ctx, D0, D1) // 4)
+    pir.pir_db_encode(ctx, to_dev(raw), 0, D0, D0, D1, db)
+    P2 = 2 * L * N
+    clients, queries, evks, ksks = [], [], [], []
+    for b in range(B):
+        K = Keys(N, L, ell, w, seed=900 + b)
+        istar, jstar = (3 * b + 1) % D0, (5 * b + 4) % D1
+        queries.append(K.encrypt(_one_ciphertext_query(K, D0, T, istar, jstar, S)))
+        evks.append(np.stack([K.evk(N // (1 << j) + 1) for j in range(S)]))
+        ksks.append(_ksk(K))
+        clients.append((K, istar, jstar))
+    M = 1 << S
+    expanded = pir.empty_u32(B * M * P2)
+    pir.pir_expand_batch(ctx, to_dev(np.stack(evks)), ell, w, S, to_dev(np.stack(queries)), B, expanded,
+                         pir.expand_workspace(ctx, B * M // 2, ell))
+    ex = expanded.view(B, M * P2)
+    rows = ex[:, : D0 * P2].contiguous()                       # [B][D0] RowSel queries
+    gadget = ex[:, D0 * P2:(D0 + T * ell) * P2].contiguous()   # [B][T][ell] gadget ciphertexts
+    rgsw = pir.empty_u32(B * T * 2 * ell * P2)
+    pir.pir_rgsw_convert(ctx, to_dev(np.stack(ksks)), ell, w, gadget, T, B, rgsw,
+                         pir.rgsw_convert_workspace(ctx, T, B, ell))
+    cols = pir.empty_u32(B * D1 * P2)
+    pir.pir_rowsel(ctx, db, D0, D1, rows, B, cols, pir.rowsel_workspace(ctx, D0, D1, B))
+    answers = pir.empty_u32(B * P2)
+    pir.pir_coltor_batch(ctx, rgsw, ell, w, cols, D1, B, answers, pir.coltor_batch_workspace(ctx, D1, B, ell))
     assert pir.pir_status(ctx) == 0
     got = to_host_u32(answers).reshape(B, 2, L, N)
     for b, (K, istar, jstar) in enumerate(clients):
