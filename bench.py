@@ -50,13 +50,16 @@ WORKLOADS = {
     "rowsel_64g_b16": dict(N=4096, L=3, D0=1024, D1=1365, B=16, domain="ntt",
                            desc="RowSel 64 GiB: N=4096, 3 primes, D0=1024 x D1=1365, B=16 queries, NTT-domain"),
     "onion_64g": dict(kind="onion", N=4096, L=3, D0=1024, D1=1365, ell=5, w=18,
-                      desc="OnionPIR server path per query over the 64 GiB DB: ExpandQuery 1 -> 1024 "
-                           "ciphertexts, RowSel D0=1024 x D1=1365, ColTor 1365 -> 1 (N=4096, 3 primes, l=5)"),
+                      desc="OnionPIR server path per query over the 64 GiB DB: ExpandQuery of the row "
+                           "ciphertext 1 -> 1024 and of the column ciphertext 1 -> 64 (55 gadget ciphertexts "
+                           "of the 11 column bits), their conversion to 11 RGSW ciphertexts, RowSel "
+                           "D0=1024 x D1=1365, ColTor 1365 -> 1 (N=4096, 3 primes, l=5)"),
     "onion_64g_b16": dict(kind="onion", N=4096, L=3, D0=1024, D1=1365, ell=5, w=18, B=16,
                           desc="OnionPIR server path for 16 clients per pass over the 64 GiB DB: 16 ExpandQuery "
-                               "1 -> 1024 ciphertexts (one batched call), one RowSel pass D0=1024 x D1=1365 x 16 "
-                               "queries (tensor cores), 16 ColTor 1365 -> 1 (one batched call); N=4096, 3 primes, "
-                               "l=5"),
+                               "of the row ciphertexts 1 -> 1024 and of the column ciphertexts 1 -> 64 (batched "
+                               "calls), 16 x 11 RGSW conversions (one batched call), one RowSel pass D0=1024 x "
+                               "D1=1365 x 16 queries (tensor cores), 16 ColTor 1365 -> 1 (one batched call); "
+                               "N=4096, 3 primes, l=5"),
     "expand_1024": dict(kind="expand", N=4096, L=3, stages=10, ell=5, w=18,
                         desc="ExpandQuery of one query ciphertext into the 1024 RowSel inputs of the 64 GiB DB: "
                              "N=4096, 3 primes, 10 stages of Subs, l=5 digits of 18 bits"),
@@ -362,35 +365,65 @@ class ExpandSample:
                             threads=self.threads)
 
 
+class RgswSample:
+    """Oracle conversion of one client's expanded gadget ciphertexts into one
+    RGSW ciphertext (ell key switches), counted as the fraction of a query's
+    T = ceil(log2 D1) conversions it performs."""
+    unit = "queries/s"
+
+    def __init__(self, cfg):
+        import oracle
+        import synth
+        N, L, ell, T = cfg["N"], cfg["L"], cfg["ell"], cfg["T"]
+        self.ell, self.w = ell, cfg["w"]
+        self.threads = 1
+        self.qs = oracle.primes(N, L)
+        self.psis = [oracle.min_psi(q, N) for q in self.qs]
+        self.ksk = synth.residues(15, (ell, 2, L, N), self.qs, tid=synth.T_EXTRA)
+        self.cts = synth.residues(16, (ell, 2, L, N), self.qs, tid=synth.T_EXTRA)
+        self.nbytes = 1.0 / T                          # queries per call
+        self.desc = "oracle RGSW conversion of one column bit (%d key switches; %d bits per query), N=%d, L=%d" % (
+            ell, T, N, L)
+
+    def __call__(self):
+        import oracle
+        oracle.rgsw_convert(self.ksk, self.cts, self.qs, self.psis, self.ell, self.w)
+
+
 class OnionSample:
-    """Oracle OnionPIR path, composed from bounded samples of its three
-    phases (ExpandQuery, RowSel over all D0 rows for the B queries, ColTor):
-    a call runs one call of each phase's sample and times it; a query costs
-    the sum over the phases of (time per call) / (queries per call), where a
-    call covers the fraction of a query's expansion, DB scan or tournament
-    its sample performs."""
+    """Oracle OnionPIR path, composed from bounded samples of its phases
+    (ExpandQuery of the row and of the column ciphertext, the RGSW
+    conversion of the column bits, RowSel over all D0 rows for the B
+    queries, ColTor): a call runs one call of each phase's sample and times
+    it; a query costs the sum over the phases of (time per call) / (queries
+    per call), where a call covers the fraction of a query's expansion,
+    conversion, DB scan or tournament its sample performs."""
     unit = "queries/s"
 
     def __init__(self, cfg):
         N, L, D0, D1, ell, w = cfg["N"], cfg["L"], cfg["D0"], cfg["D1"], cfg["ell"], cfg["w"]
         B = cfg.get("B", 1)
         S = D0.bit_length() - 1
+        T = coltor_stages(D1)
         self.phases = [
             ExpandSample(dict(N=N, L=L, stages=S, ell=ell, w=w)),
+            ExpandSample(dict(N=N, L=L, stages=column_stages(T, ell), ell=ell, w=w)),
+            RgswSample(dict(N=N, L=L, ell=ell, w=w, T=T)),
             RowselSample(dict(N=N, L=L, D0=D0, D1=D1, B=B)),
             ColtorSample(dict(N=N, L=L, n=D1, ell=ell, w=w)),
         ]
-        r = self.phases[1]
-        # queries per call: expansions or tournaments per call, or the scanned
-        # fraction of the DB times the B queries the scan serves
-        self.per_call = [self.phases[0].nbytes, r.nbytes / (D0 * D1 * L * N * 4) * B, self.phases[2].nbytes]
+        r = self.phases[3]
+        # queries per call: expansions, conversions or tournaments per call,
+        # or the scanned fraction of the DB times the B queries the scan serves
+        self.per_call = [self.phases[0].nbytes, self.phases[1].nbytes, self.phases[2].nbytes,
+                         r.nbytes / (D0 * D1 * L * N * 4) * B, self.phases[4].nbytes]
         self.threads = r.threads
         self.nbytes = 0.0
         self.reset()
         self.desc = "oracle OnionPIR path per query, composed of: " + "; ".join(x.desc for x in self.phases)
 
     def reset(self):
-        self.spent = [0.0, 0.0, 0.0]
+        self.spent = [0.0] * len(self.phases)
         self.calls = 0
 
     def __call__(self):
@@ -510,6 +543,12 @@ def coltor_stages(n) -> int:
     return s
 
 
+def column_stages(T, ell) -> int:
+    """Expansion stages of the column ciphertext: its T * ell gadget values
+    (ell per column bit) are coefficients 0 .. T ell - 1."""
+    return coltor_stages(T * ell)
+
+
 def coltor_algorithmic_bytes(n, L, N, ell) -> int:
     """Bytes a tournament must move at the least: every stage reads its input
     ciphertexts and its RGSW ciphertext and writes its outputs."""
@@ -533,9 +572,11 @@ def launches_per_step(cfg) -> int:
     if cfg.get("kind") == "expand":
         return 4 * cfg["stages"]
     if cfg.get("kind") == "onion":
-        # one batched expansion and one batched tournament for all B clients
-        return (4 * (cfg["D0"].bit_length() - 1) + 3 * rowsel_passes(cfg["D0"], cfg.get("B", 1))
-                + 4 * coltor_stages(cfg["D1"]))
+        # for all B clients: the batched row and column expansions, the batched
+        # RGSW conversion, the RowSel passes and the batched tournament
+        T = coltor_stages(cfg["D1"])
+        return (4 * (cfg["D0"].bit_length() - 1) + 4 * column_stages(T, cfg["ell"]) + 4
+                + 3 * rowsel_passes(cfg["D0"], cfg.get("B", 1)) + 4 * T)
     return 3 * rowsel_passes(cfg["D0"], cfg["B"]) + (2 if cfg["domain"] == "coeff" else 0)
 
 
@@ -1128,10 +1169,13 @@ def run_expand(args, cfg):
 
 def run_onion(args, cfg):
     """The OnionPIR server path for B queries (B clients, each with its own
-    keys): the B expansions of a query ciphertext into D0 = 1024 (one batched
-    call), one RowSel pass of the B queries over the resident 64 GiB DB, the
-    B tournaments of the D1 = 1365 results into one answer ciphertext each
-    (one batched call); all NTT form."""
+    keys): the B expansions of the row query ciphertext into D0 = 1024 and of
+    the column query ciphertext into 64 (its first T ell = 55 outputs are the
+    gadget ciphertexts of the T = 11 column bits), the conversion of those
+    into T RGSW ciphertexts per client, one RowSel pass of the B queries over
+    the resident 64 GiB DB, and the B tournaments of the D1 = 1365 results
+    into one answer ciphertext each; every phase one (batched) call, all NTT
+    form."""
     import torch
 
     import __graft_entry__
@@ -1145,26 +1189,37 @@ def run_onion(args, cfg):
     N, L, D0, D1, ell, w = cfg["N"], cfg["L"], cfg["D0"], cfg["D1"], cfg["ell"], cfg["w"]
     B = cfg.get("B", 1)
     S, T = D0.bit_length() - 1, coltor_stages(D1)
+    Sc = column_stages(T, ell)
+    Mc = 1 << Sc
     qs = pir.pir_primes(N, L)
     ctx = pir.pir_ctx_create(N, qs, local)
     P = L * N
-    qw, ew, rw = 2 * P, S * ell * 2 * P, T * 2 * ell * 2 * P      # words per client
+    qw = 2 * P                                           # words of a ciphertext
     db = device_db(ctx, D0, D1, seed=7)
-    # per client: the query ciphertext and the RGSW rows of its column bits
-    # (sent with every query), and its evaluation keys (resident, sent once);
-    # two slots of per-query buffers so that two steps can be in flight
+    # per client and query: a row and a column query ciphertext; resident per
+    # client (sent once): the expansion keys of S stages (the column
+    # expansion takes the first Sc of them, stored again so that a batched
+    # call finds client b's at b * Sc keys) and the key-switching key of s^2.
+    # Two slots of per-query buffers so that two steps can be in flight.
     query = [torch.empty(B * qw, dtype=torch.int32, device="cuda") for _ in range(2)]
+    colq = [torch.empty(B * qw, dtype=torch.int32, device="cuda") for _ in range(2)]
     sd.fill_residues(query[0], 11, synth.T_EXTRA, N, qs)
-    rgsw = [torch.empty(B * rw, dtype=torch.int32, device="cuda") for _ in range(2)]
-    sd.fill_residues(rgsw[0], 13, synth.T_EXTRA, N, qs)
+    sd.fill_residues(colq[0], 14, synth.T_EXTRA, N, qs)
     query[1].copy_(query[0])
-    rgsw[1].copy_(rgsw[0])
-    evks = torch.empty(B * ew, dtype=torch.int32, device="cuda")
+    colq[1].copy_(colq[0])
+    evks = torch.empty(B * S * ell * qw, dtype=torch.int32, device="cuda")
     sd.fill_residues(evks, 12, synth.T_EXTRA, N, qs)
+    evks_c = evks.view(B, S * ell * qw)[:, : Sc * ell * qw].contiguous().view(-1)
+    ksk = torch.empty(B * ell * qw, dtype=torch.int32, device="cuda")
+    sd.fill_residues(ksk, 13, synth.T_EXTRA, N, qs)
     expanded = torch.empty(B * D0 * qw, dtype=torch.int32, device="cuda")
+    col_exp = torch.empty(B * Mc * qw, dtype=torch.int32, device="cuda")
+    rgsw = torch.empty(B * T * 2 * ell * qw, dtype=torch.int32, device="cuda")
     cols = torch.empty(B * D1 * qw, dtype=torch.int32, device="cuda")
     answer = [torch.empty(B * qw, dtype=torch.int32, device="cuda") for _ in range(2)]
     ws_e = pir.expand_workspace(ctx, B * D0 // 2, ell)
+    ws_ec = pir.expand_workspace(ctx, B * Mc // 2, ell)
+    ws_g = pir.rgsw_convert_workspace(ctx, T, B, ell)
     ws_r = pir.rowsel_workspace(ctx, D0, D1, B)
     ws_c = pir.coltor_batch_workspace(ctx, D1, B, ell)
     stream = torch.cuda.Stream()
@@ -1173,17 +1228,23 @@ def run_onion(args, cfg):
     def expand(k):
         pir.pir_expand_batch(ctx, evks, ell, w, S, query[k], B, expanded, ws_e, stream)
 
+    def column(k):
+        pir.pir_expand_batch(ctx, evks_c, ell, w, Sc, colq[k], B, col_exp, ws_ec, stream)
+        pir.pir_rgsw_convert(ctx, ksk, ell, w, col_exp, T, B, rgsw, ws_g, stream, in_stride=Mc)
+
     def rowsel():
         pir.pir_rowsel(ctx, db, D0, D1, expanded, B, cols, ws_r, stream)
 
     def coltor(k):
-        pir.pir_coltor_batch(ctx, rgsw[k], ell, w, cols, D1, B, answer[k], ws_c, stream)
+        pir.pir_coltor_batch(ctx, rgsw, ell, w, cols, D1, B, answer[k], ws_c, stream)
 
     for _ in range(2):                        # first calls (kernel attributes, caches) outside the graphs
         expand(0)
+        column(0)
         rowsel()
         coltor(0)
     g_expand = [graph_of(lambda: expand(0), stream), graph_of(lambda: expand(1), stream)]
+    g_column = [graph_of(lambda: column(0), stream), graph_of(lambda: column(1), stream)]
     g_coltor = [graph_of(lambda: coltor(0), stream), graph_of(lambda: coltor(1), stream)]
 
     def step(ev=None, k=0):
@@ -1193,12 +1254,15 @@ def run_onion(args, cfg):
             g_expand[k].replay()              # the small expansion stages are bound by launch latency
             if ev is not None:
                 ev[1].record(stream)
-            rowsel()
+            g_column[k].replay()
             if ev is not None:
                 ev[2].record(stream)
-            g_coltor[k].replay()
+            rowsel()
             if ev is not None:
                 ev[3].record(stream)
+            g_coltor[k].replay()
+            if ev is not None:
+                ev[4].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -1206,7 +1270,7 @@ def run_onion(args, cfg):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -1217,23 +1281,23 @@ def run_onion(args, cfg):
     torch.cuda.synchronize()
     clk = clocks.stop()
     ms_total = max_over_ranks(t0.elapsed_time(t1))
-    phase = [float(np.mean([e[k].elapsed_time(e[k + 1]) for e in kev])) for k in range(3)]
+    phase = [float(np.mean([e[k].elapsed_time(e[k + 1]) for e in kev])) for k in range(4)]
     if pir.pir_status(ctx):
         raise RuntimeError("device status word set")
 
-    # end to end: every step's query ciphertexts and RGSW rows in from pinned
-    # host memory, the answers out; two steps in flight
+    # end to end: every step's row and column query ciphertexts in from
+    # pinned host memory, the answers out; two steps in flight
     q_host = torch.empty(query[0].numel(), dtype=torch.int32, pin_memory=True)
     q_host.copy_(query[0].cpu())
-    r_host = torch.empty(rgsw[0].numel(), dtype=torch.int32, pin_memory=True)
-    r_host.copy_(rgsw[0].cpu())
+    c_host = torch.empty(colq[0].numel(), dtype=torch.int32, pin_memory=True)
+    c_host.copy_(colq[0].cpu())
     a_host = [torch.empty(answer[0].numel(), dtype=torch.int32, pin_memory=True) for _ in range(2)]
     ke = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
     e2e_ms = None
     if ke:
         def copy_in(k):
             query[k].copy_(q_host, non_blocking=True)
-            rgsw[k].copy_(r_host, non_blocking=True)
+            colq[k].copy_(c_host, non_blocking=True)
 
         e2e_ms = pipelined_ms(copy_in, lambda k: step(None, k),
                               lambda k: a_host[k].copy_(answer[k], non_blocking=True), stream, ke)
@@ -1242,7 +1306,7 @@ def run_onion(args, cfg):
     hbm_peak = float(peaks["hbm_gbs"])
     logical_db = P * D0 * D1 * 4
     ms_step = ms_total / args.steps
-    db_gbs = logical_db / (phase[1] * 1e-3) / 1e9
+    db_gbs = logical_db / (phase[2] * 1e-3) / 1e9
     on_tensor = 8 < B <= 16
     result = None
     if rank == 0:
@@ -1250,13 +1314,14 @@ def run_onion(args, cfg):
             "metric": ONION_METRIC, "value": world * B * args.steps / (ms_total * 1e-3), "unit": "queries/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
-            "data": "synthetic: seeded SplitMix64 DB coefficients U[0,2^16), query, key and RGSW residues U[0,q_i)",
+            "data": "synthetic: seeded SplitMix64 DB coefficients U[0,2^16), query and key residues U[0,q_i)",
             "config": {"workload": args.workload, "desc": cfg["desc"], "logical_db_bytes": logical_db, "B": B,
                        "l2": "inputs larger than L2 (DB %.1f GiB), no flush" % (logical_db / GIB),
                        "parallelism": "replicas x%d" % world},
-            "phase_ms": {"expand": phase[0], "rowsel": phase[1], "coltor": phase[2]},
-            "launch": "the batched ExpandQuery and ColTor calls each replayed as one CUDA graph; "
-                      "RowSel launched directly",
+            "phase_ms": {"expand": phase[0], "column_expand_and_rgsw": phase[1], "rowsel": phase[2],
+                         "coltor": phase[3]},
+            "launch": "the batched row expansion, column expansion + RGSW conversion and ColTor calls each "
+                      "replayed as one CUDA graph; RowSel launched directly",
             "db_gbs_in_rowsel": db_gbs,
             "roofline": {"bound": "hbm", "achieved": db_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": db_gbs / hbm_peak, "traffic": None, "traffic_source": None,
@@ -1266,10 +1331,10 @@ def run_onion(args, cfg):
                          "algorithmic_bytes_per_launch": logical_db},
             "clocks": clk,
             "e2e": None if e2e_ms is None else {
-                "value": B * 1e3 / e2e_ms, "unit": "queries/s", "h2d_bytes_per_step": B * (qw + rw) * 4,
+                "value": B * 1e3 / e2e_ms, "unit": "queries/s", "h2d_bytes_per_step": B * 2 * qw * 4,
                 "d2h_bytes_per_step": B * qw * 4, "ms_per_step": e2e_ms,
-                "how": "query ciphertexts and RGSW rows in, answers out; evaluation keys resident; "
-                       "2 steps in flight on three streams"},
+                "how": "row and column query ciphertexts in, answers out; expansion and key-switching keys "
+                       "resident; 2 steps in flight on three streams"},
             "gpu_launches": args.steps * launches_per_step(cfg),
             "cpu_baseline": None,
         }

@@ -370,8 +370,10 @@ uint64_t pir_scalar_workspace_bytes(uint64_t C, uint32_t B);
  * (a key-switching key); row ell + u decrypts to s (c0_u + c1_u s) = m s g_u.
  *   ksk  : device, [G][ell][2][L][N] NTT form, client b's key at
  *          b * ell * 2 L N words.
- *   in   : device, [G][n][ell][2][L][N] NTT form: client b's n gadget lists
- *          (e.g. its ceil(log2 D1) column bits), canonical residues.
+ *   in   : device, NTT form, canonical residues: client b's n gadget lists
+ *          ([n][ell][2][L][N], e.g. its ceil(log2 D1) column bits) at
+ *          b * in_stride ciphertexts; in_stride >= n ell, 0 meaning n ell
+ *          (contiguous); a client's expansion output can be passed as is.
  *   out  : device, [G][n][2 ell][2][L][N] NTT form: the RGSW ciphertexts, as
  *          pir_coltor_batch takes them ([G][S][2 ell][2][L][N] with S = n).
  *   ell, w : as for pir_coltor.
@@ -380,13 +382,14 @@ uint64_t pir_scalar_workspace_bytes(uint64_t C, uint32_t B);
  *          call uses overlaps neither in nor out; contents undefined after.
  * The library owns nothing the caller passes; asynchronous on stream.
  * Errors: PIR_ERR_ARG (NULL/unaligned pointers, n = 0, G = 0, n G ell >=
- * 2^31, ell or w out of range, digits not covering Q, workspace too small,
- * overlaps), PIR_ERR_CUDA.
+ * 2^31, in_stride below n ell or the strided input reaching 2^31
+ * ciphertexts, ell or w out of range, digits not covering Q, workspace too
+ * small, overlaps), PIR_ERR_CUDA.
  */
 uint64_t pir_rgsw_convert_workspace_bytes(const pir_ctx *ctx, uint64_t n, uint64_t G, uint32_t ell);
 
 int pir_rgsw_convert(pir_ctx *ctx, const uint32_t *ksk, uint32_t ell, uint32_t w,
-                     const uint32_t *in, uint64_t n, uint64_t G, uint32_t *out,
+                     const uint32_t *in, uint64_t in_stride, uint64_t n, uint64_t G, uint32_t *out,
                      void *workspace, uint64_t workspace_bytes, void *stream);
 
 /*

@@ -48,10 +48,10 @@ extern "C" int pir_lift_ntt(pir_ctx *ctx, const uint32_t *raw, uint32_t *out, ui
 namespace {
 
 struct InttAArgs {
-    const uint32_t *in;     // [M][2][L][N]
+    const uint32_t *in;     // ciphertext i at in + ((i / per) * stride + i % per) * 2 L N words
     uint32_t *coef;         // [M][L][N]
     const uint32_t *tw;
-    uint64_t M;
+    uint64_t M, per, stride;   // per = stride = M for a contiguous [M][2][L][N] input
     uint32_t L;
     uint32_t q[PIR_MAX_RNS], ninv[PIR_MAX_RNS], ninv_shoup[PIR_MAX_RNS];
 };
@@ -66,8 +66,9 @@ __global__ void __launch_bounds__(kT4) expand_intt_a4096_kernel(const __grid_con
     const bool two = i1 < A.M;
     const uint32_t q = A.q[l];
     const uint2 *T = tw_pairs(A.tw, l, kN4, TW_INV);
-    const uint32_t *s0 = A.in + ((2 * i0 + 1) * A.L + l) * kN4;
-    const uint32_t *s1 = A.in + ((2 * i1 + 1) * A.L + l) * kN4;
+    const uint64_t j0 = (i0 / A.per) * A.stride + i0 % A.per, j1 = (i1 / A.per) * A.stride + i1 % A.per;
+    const uint32_t *s0 = A.in + ((2 * j0 + 1) * A.L + l) * kN4;
+    const uint32_t *s1 = A.in + ((2 * j1 + 1) * A.L + l) * kN4;
     const uint32_t t = threadIdx.x;
     uint32_t x[16], y[16];
 #pragma unroll
@@ -166,11 +167,11 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
 }
 
 struct RgswMacArgs {
-    const uint32_t *in;     // [M][2][L][N] gadget ciphertexts, M = G * n * ell
+    const uint32_t *in;     // gadget ciphertexts: client b's n * ell at in + b * in_stride * 2 L N words
     const uint32_t *dn;     // [M][ell][L][N] NTT of the digits of c1
     const uint32_t *ksk;    // client b's key [ell][2][L][N] at ksk + b * ksk_stride
     uint32_t *out;          // [G * n][2 ell][2][L][N]
-    uint64_t M, per_client, ksk_stride;   // per_client = n * ell input ciphertexts
+    uint64_t M, per_client, in_stride, ksk_stride;   // per_client = n * ell input ciphertexts
     uint32_t N, L, ell;
     uint32_t q[PIR_MAX_RNS];
     uint64_t mu[PIR_MAX_RNS];
@@ -200,8 +201,9 @@ __global__ void __launch_bounds__(GD_THREADS) rgsw_mac_kernel(const RgswMacArgs 
             a0 += (uint64_t)d.x * k0.x; a1 += (uint64_t)d.y * k0.y; a2 += (uint64_t)d.z * k0.z; a3 += (uint64_t)d.w * k0.w;
             b0 += (uint64_t)d.x * k1.x; b1 += (uint64_t)d.y * k1.y; b2 += (uint64_t)d.z * k1.z; b3 += (uint64_t)d.w * k1.w;
         }
-        const uint4 v0 = *reinterpret_cast<const uint4 *>(A.in + i * 2 * LN + pt);
-        const uint4 v1 = *reinterpret_cast<const uint4 *>(A.in + i * 2 * LN + LN + pt);
+        const uint64_t src = (uint64_t)b * A.in_stride + (i - (uint64_t)b * A.per_client);
+        const uint4 v0 = *reinterpret_cast<const uint4 *>(A.in + src * 2 * LN + pt);
+        const uint4 v1 = *reinterpret_cast<const uint4 *>(A.in + src * 2 * LN + LN + pt);
         const uint64_t r = i / A.ell, u = i - r * A.ell;
         uint32_t *row_u = A.out + (r * 2 * A.ell + u) * 2 * LN + pt;
         uint32_t *row_s = A.out + (r * 2 * A.ell + A.ell + u) * 2 * LN + pt;
@@ -243,10 +245,13 @@ uint32_t inv_mod_2n(uint32_t k, uint32_t twoN) {
     return x & (twoN - 1);
 }
 
-// The a polynomial c1 of each of the GM ciphertexts in `in` ([GM][2][L][N],
-// NTT form) in coefficient form, coef [GM][L][N].
-int c1_to_coef(pir_ctx *ctx, const uint32_t *in, uint64_t GM, uint32_t *coef, cudaStream_t st) {
+// The a polynomial c1 of each of the GM ciphertexts in `in` (NTT form) in
+// coefficient form, coef [GM][L][N]; ciphertext i is at in + ((i / per) *
+// stride + i % per) * 2 L N words (per = stride = GM: contiguous).
+int c1_to_coef(pir_ctx *ctx, const uint32_t *in, uint64_t GM, uint32_t *coef, cudaStream_t st,
+               uint64_t per = 0, uint64_t stride = 0) {
     const uint64_t LN = (uint64_t)ctx->L * ctx->N;
+    if (per == 0) per = stride = GM;
     if (ctx->N == (uint32_t)kN4) {
         InttAArgs ia;
         memset(&ia, 0, sizeof(ia));
@@ -261,12 +266,15 @@ int c1_to_coef(pir_ctx *ctx, const uint32_t *in, uint64_t GM, uint32_t *coef, cu
         }
         if ((GM + 1) / 2 * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
         ia.M = GM;
+        ia.per = per;
+        ia.stride = stride;
         expand_intt_a4096_kernel<<<(unsigned)((GM + 1) / 2 * ctx->L), kT4, 0, st>>>(ia);
         return cudaGetLastError() == cudaSuccess ? PIR_OK : PIR_ERR_CUDA;
     }
-    if (cudaMemcpy2DAsync(coef, LN * 4, in + LN, 2 * LN * 4, LN * 4, GM, cudaMemcpyDeviceToDevice, st) !=
-        cudaSuccess)
-        return PIR_ERR_CUDA;
+    for (uint64_t b = 0; b < GM / per; ++b)   // one strided copy of the c1 rows per block of `per`
+        if (cudaMemcpy2DAsync(coef + b * per * LN, LN * 4, in + (b * stride * 2 + 1) * LN, 2 * LN * 4, LN * 4, per,
+                              cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return PIR_ERR_CUDA;
     return pir_ntt_inv(ctx, coef, coef, GM, st);
 }
 
@@ -407,23 +415,27 @@ extern "C" uint64_t pir_rgsw_convert_workspace_bytes(const pir_ctx *ctx, uint64_
 }
 
 extern "C" int pir_rgsw_convert(pir_ctx *ctx, const uint32_t *ksk, uint32_t ell, uint32_t w, const uint32_t *in,
-                                uint64_t n, uint64_t G, uint32_t *out, void *workspace, uint64_t workspace_bytes,
-                                void *stream) {
+                                uint64_t in_stride, uint64_t n, uint64_t G, uint32_t *out, void *workspace,
+                                uint64_t workspace_bytes, void *stream) {
     if (!ctx || !ksk || !in || !out || !workspace || n == 0 || G == 0) return PIR_ERR_ARG;
     if (!gadget_params_ok(ctx, ell, w) || n > (1ull << 31) || G > (1ull << 31) || n * G * ell >= (1ull << 31))
+        return PIR_ERR_ARG;
+    if (in_stride == 0) in_stride = n * ell;
+    if (in_stride < n * ell || in_stride > (1ull << 31) || (G - 1) * in_stride + n * ell >= (1ull << 31))
         return PIR_ERR_ARG;
     if (!aligned16(ksk) || !aligned16(in) || !aligned16(out) || !aligned16(workspace)) return PIR_ERR_ARG;
     const uint64_t M = n * G * ell, LN = (uint64_t)ctx->L * ctx->N;
     const RgLayout lay = rg_layout(ctx, M, ell);
     if (workspace_bytes < lay.total * 4) return PIR_ERR_ARG;
-    const uint64_t in_b = M * 2 * LN * 4, out_b = 2 * M * 2 * LN * 4, ws_b = lay.total * 4;
+    const uint64_t in_b = ((G - 1) * in_stride + n * ell) * 2 * LN * 4, out_b = 2 * M * 2 * LN * 4,
+                   ws_b = lay.total * 4;
     if (overlaps(in, in_b, out, out_b) || overlaps(workspace, ws_b, in, in_b) || overlaps(workspace, ws_b, out, out_b))
         return PIR_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PIR_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
     uint32_t *ws = static_cast<uint32_t *>(workspace);
     uint32_t *coef = ws + lay.coef, *dig = ws + lay.dig, *dn = ws + lay.dn;
-    int rc = c1_to_coef(ctx, in, M, coef, st);
+    int rc = c1_to_coef(ctx, in, M, coef, st, n * ell, in_stride);
     if (rc) return rc;
     rc = gadget_dcp_launch(ctx, gadget_dcp_args(ctx, coef, LN, dig, M, ell, w, 1), st);
     if (rc) return rc;
@@ -437,6 +449,7 @@ extern "C" int pir_rgsw_convert(pir_ctx *ctx, const uint32_t *ksk, uint32_t ell,
     ma.out = out;
     ma.M = M;
     ma.per_client = n * ell;
+    ma.in_stride = in_stride;
     ma.ksk_stride = (uint64_t)ell * 2 * LN;
     ma.N = ctx->N;
     ma.L = ctx->L;

@@ -115,7 +115,7 @@ def lib() -> ctypes.CDLL:
         L.pir_rgsw_convert_workspace_bytes.argtypes = [_vp, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
         L.pir_rgsw_convert.restype = ctypes.c_int
         L.pir_rgsw_convert.argtypes = [_vp, _vp, ctypes.c_uint32, ctypes.c_uint32, _vp, ctypes.c_uint64,
-                                       ctypes.c_uint64, _vp, _vp, ctypes.c_uint64, _vp]
+                                       ctypes.c_uint64, ctypes.c_uint64, _vp, _vp, ctypes.c_uint64, _vp]
         L.pir_status.restype = ctypes.c_int
         L.pir_status.argtypes = [_vp, _u32p, ctypes.c_int]
         L.pir_ctx_set_wait_limit.restype = ctypes.c_int
@@ -525,11 +525,12 @@ def rgsw_convert_workspace(ctx: Ctx, n: int, G: int, ell: int, device="cuda") ->
 
 
 def pir_rgsw_convert(ctx: Ctx, ksk: torch.Tensor, ell: int, w: int, cts: torch.Tensor, n: int, G: int,
-                     out: torch.Tensor, workspace: torch.Tensor, stream=None):
+                     out: torch.Tensor, workspace: torch.Tensor, stream=None, in_stride: int = 0):
     """RGSW ciphertexts [G][n][2 ell][2][L][N] from the expanded gadget
-    ciphertexts [G][n][ell][2][L][N] and each client's key-switching key of
-    s^2 ([G][ell][2][L][N]), all NTT form."""
+    ciphertexts (client b's n ell of them at b * in_stride ciphertexts,
+    in_stride = 0: contiguous) and each client's key-switching key of s^2
+    ([G][ell][2][L][N]), all NTT form."""
     ws = _dev_ptr(workspace, workspace.element_size(), "workspace")
-    _check(lib().pir_rgsw_convert(ctx, _dev_ptr(ksk, 4, "ksk"), ell, w, _dev_ptr(cts, 4, "in"), n, G,
+    _check(lib().pir_rgsw_convert(ctx, _dev_ptr(ksk, 4, "ksk"), ell, w, _dev_ptr(cts, 4, "in"), in_stride, n, G,
                                   _dev_ptr(out, 4, "out"), ws, workspace.numel() * workspace.element_size(),
                                   _stream(stream)), "pir_rgsw_convert")

@@ -67,17 +67,21 @@ def test_launch_counts_of_the_workloads():
     library's call structure: a RowSel pass is three launches (query
     transpose, scan, result transpose), a coefficient-form query adds its NTT
     and the result INTT, an expansion or tournament stage is four launches
+    (INTT, decomposition, lift + NTT, MAC), the RGSW conversion is four more
     (INTT, decomposition, lift + NTT, MAC), ring packing adds the lift + NTT
-    of G.  Batched expansions and tournaments launch per stage, not per
-    client."""
+    of G.  Batched expansions, conversions and tournaments launch per stage,
+    not per client.  OnionPIR: the row expansion (10 stages), the column
+    expansion (6 stages: 11 bits x 5 gadget values = 55 <= 64 outputs), the
+    conversion, the RowSel pass and the tournament (11 stages)."""
     import bench
     W = bench.WORKLOADS
     assert bench.launches_per_step(W["rowsel_64g"]) == 3 + 2
     assert bench.launches_per_step(W["rowsel_24g_b16"]) == 3            # one pass of 16 on the tensor cores
     assert bench.launches_per_step(W["expand_1024"]) == 4 * 10
     assert bench.launches_per_step(W["coltor_1365"]) == 4 * 11
-    assert bench.launches_per_step(W["onion_64g"]) == 4 * 10 + 3 + 4 * 11
-    assert bench.launches_per_step(W["onion_64g_b16"]) == 4 * 10 + 3 + 4 * 11
+    assert bench.column_stages(11, 5) == 6
+    assert bench.launches_per_step(W["onion_64g"]) == 4 * 10 + 4 * 6 + 4 + 3 + 4 * 11
+    assert bench.launches_per_step(W["onion_64g_b16"]) == 4 * 10 + 4 * 6 + 4 + 3 + 4 * 11
     assert bench.launches_per_step(W["exppack_15g"]) == 3 + 1
     # pass planning: 16 per pass on the tensor cores while more than 8 remain,
     # then the CUDA cores (16 queries fit the on-chip slice for D0 <= 896)
@@ -90,16 +94,18 @@ def test_launch_counts_of_the_workloads():
 
 def test_onion_sample_composes_the_phases(monkeypatch):
     """The composed OnionPIR sample: each phase covers the fraction of a
-    query its sample performs (expansions and tournaments per call, the
-    scanned fraction of the DB times B), and a query costs the sum of each
-    phase's time per call over its queries per call."""
+    query its sample performs (expansions, conversions and tournaments per
+    call, the scanned fraction of the DB times B), and a query costs the sum
+    of each phase's time per call over its queries per call."""
     monkeypatch.setattr(oracle, "default_threads", lambda: 2)
     N, L, D0, D1, B = 64, 3, 16, 11, 2
     on = bench.OnionSample(dict(N=N, L=L, D0=D0, D1=D1, ell=5, w=18, B=B))
-    e, r, c = on.phases
+    e, ec, g, r, c = on.phases
     assert abs(on.per_call[0] - 2 / 15) < 1e-12                # 2 of the 15 Subs of a 16-way expansion
-    assert abs(on.per_call[1] - r.nbytes / (D0 * D1 * L * N * 4) * B) < 1e-12
-    assert abs(on.per_call[2] - 2 / 10) < 1e-12                # 2 of the 10 external products
+    assert abs(on.per_call[1] - 2 / 31) < 1e-12                # column: 4 bits x 5 values -> 32 outputs, 31 Subs
+    assert abs(on.per_call[2] - 1 / 4) < 1e-12                 # one of the 4 bits' conversions
+    assert abs(on.per_call[3] - r.nbytes / (D0 * D1 * L * N * 4) * B) < 1e-12
+    assert abs(on.per_call[4] - 2 / 10) < 1e-12                # 2 of the 10 external products
     on()
     on()
     assert on.calls == 2 and all(t > 0 for t in on.spent)

@@ -199,10 +199,10 @@ def test_batch_of_one_ciphertext_queries_on_the_tensor_path(pir):
                          pir.expand_workspace(ctx, B * M // 2, ell))
     ex = expanded.view(B, M * P2)
     rows = ex[:, : D0 * P2].contiguous()                       # [B][D0] RowSel queries
-    gadget = ex[:, D0 * P2:(D0 + T * ell) * P2].contiguous()   # [B][T][ell] gadget ciphertexts
     rgsw = pir.empty_u32(B * T * 2 * ell * P2)
-    pir.pir_rgsw_convert(ctx, to_dev(np.stack(ksks)), ell, w, gadget, T, B, rgsw,
-                         pir.rgsw_convert_workspace(ctx, T, B, ell))
+    # client b's T ell gadget ciphertexts sit at b M + D0 in the expansion output
+    pir.pir_rgsw_convert(ctx, to_dev(np.stack(ksks)), ell, w, expanded[D0 * P2:], T, B, rgsw,
+                         pir.rgsw_convert_workspace(ctx, T, B, ell), in_stride=M)
     cols = pir.empty_u32(B * D1 * P2)
     pir.pir_rowsel(ctx, db, D0, D1, rows, B, cols, pir.rowsel_workspace(ctx, D0, D1, B))
     answers = pir.empty_u32(B * P2)
