@@ -84,6 +84,22 @@ WORKLOADS = {
     "exppack_15g": dict(kind="exppack", N=4096, L=3, n=1280, Dr=256, B=1,
                         desc="ExpPack GEMM H*C + (0|G): N=4096, 3 primes, hint Dr=256 x n=1280 polys (15 GiB), "
                              "B=1; step = lift+NTT(G, 256 polys) + the point-wise GEMM"),
+    # the full-size workloads' per-point shapes on fewer evaluation points (a
+    # smaller ring), for profiler captures of a few GB: traffic per point is
+    # the same, so a full launch's traffic is the small launch's times the
+    # ratio of points (12288 / 384 = 32, 12288 / 1536 = 8)
+    "rowsel_64g_shape_2g_prof": dict(N=128, L=3, D0=1024, D1=1365, B=1, domain="ntt",
+                                     desc="RowSel profiling case with the 64 GiB workload's point shape: N=128, "
+                                          "3 primes (384 points), D0=1024 x D1=1365, B=1 (2.1 GB DB)"),
+    "rowsel_64g_shape_2g_b16_prof": dict(N=128, L=3, D0=1024, D1=1365, B=16, domain="ntt",
+                                         desc="RowSel profiling case with the 64 GiB workload's point shape: "
+                                              "N=128, 3 primes (384 points), D0=1024 x D1=1365, B=16 (2.1 GB DB)"),
+    "rowsel_24g_shape_3g_b16_prof": dict(N=512, L=3, D0=512, D1=1024, B=16, domain="ntt",
+                                         desc="RowSel profiling case with the 24 GiB workload's point shape: "
+                                              "N=512, 3 primes (1536 points), D0=512 x D1=1024, B=16 (3.2 GB DB)"),
+    "exppack_15g_shape_2g_prof": dict(kind="exppack", N=512, L=3, n=1280, Dr=256, B=1,
+                                      desc="ExpPack profiling case with the 15 GiB hint's point shape: N=512, "
+                                           "3 primes (1536 points), hint Dr=256 x n=1280 (2.0 GB), B=1"),
     # small case of the 64 GiB pipeline for profiler captures (3 GiB, 2 column slabs)
     "rowsel_3g_prof": dict(N=4096, L=3, D0=256, D1=256, B=1, domain="coeff",
                            desc="RowSel 3 GiB profiling case: N=4096, 3 primes, D0=256 x D1=256, B=1, "

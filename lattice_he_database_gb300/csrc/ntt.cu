@@ -149,9 +149,9 @@ __global__ void __launch_bounds__(kT4, 4) ntt4096x2_fwd_kernel(const uint32_t *_
     // rows of one prime, so one prime's 32 KiB of twiddle pairs stays in L1
     // (pair-major order kept all L tables live and missed L1 on a third of
     // the twiddle loads; the lift's raw rows are then re-read from L2 per prime).
-    const uint64_t npairs = (cnt + 1) / 2;
+    const uint32_t npairs = (uint32_t)((cnt + 1) / 2);   // the grid (npairs * L CTAs) is below 2^31
     const uint64_t pp = blockIdx.x % npairs;
-    const uint32_t l = (uint32_t)(blockIdx.x / npairs);
+    const uint32_t l = blockIdx.x / npairs;
     const uint64_t p0 = 2 * pp, p1 = p0 + 1;
     const bool two = p1 < cnt;
     const uint32_t q = P.q[l];
