@@ -124,6 +124,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiler runs)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="default workload only: skip the short timings of the other north-star configurations")
     return ap.parse_args()
 
 
@@ -608,7 +610,7 @@ def kernel_rooflines(coeff, q_bytes, o_bytes, ntt_fwd_ms, ntt_inv_ms, hbm_peak):
     return out
 
 
-def run_scalar(args, cfg):
+def run_scalar(args, cfg, emit=True):
     """Scalar-HE scan: one step = digit split of Q + the tensor-core scan."""
     import torch
 
@@ -700,7 +702,8 @@ def run_scalar(args, cfg):
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = oracle_baseline(ScalarSample(cfg), args.cpu_seconds)
-        print(json.dumps(line), flush=True)
+        if emit:
+            print(json.dumps(line), flush=True)
     ctx.close()
     return line
 
@@ -1362,7 +1365,7 @@ def run_onion(args, cfg):
     return result
 
 
-def run_ours(args, cfg):
+def run_ours(args, cfg, emit=True):
     import torch
     import torch.distributed as dist
 
@@ -1535,7 +1538,8 @@ def run_ours(args, cfg):
             "gpu_launches": args.steps * launches_per_step(cfg),
             "cpu_baseline": cpu,
         }
-        print(json.dumps(result), flush=True)
+        if emit:
+            print(json.dumps(result), flush=True)
     ctx.close()
     if world > 1:
         dist.barrier()
@@ -1543,9 +1547,51 @@ def run_ours(args, cfg):
     return result
 
 
+# The other configurations of the benchmark spec, timed briefly after the
+# headline one in the default run (one GPU), so that their numbers come from
+# the same run: the tiny RowSel, the 6 GiB single query, the 24 GiB 16-query
+# batch on the tensor cores and the 16 GiB x 64 scalar scan.
+NORTH_STAR_CONFIGS = ["tiny", "rowsel_6g", "rowsel_24g_b16", "scalar_16g"]
+WORKLOADS["tiny"] = dict(N=4096, L=2, D0=16, D1=16, B=1, domain="ntt",
+                         desc="Tiny RowSel: N=4096, 2 primes, D0=16 x D1=16, B=1, NTT-domain query (L2-resident)")
+
+
+def north_star_configs(args):
+    """Short timings (20 steps, CUDA events) of NORTH_STAR_CONFIGS."""
+    out = {}
+    for name in NORTH_STAR_CONFIGS:
+        sub = argparse.Namespace(**vars(args))
+        sub.workload, sub.steps, sub.warmup = name, 20, 3
+        sub.no_cpu_baseline, sub.no_e2e = True, True
+        cfg = WORKLOADS[name]
+        line = (run_scalar if cfg.get("kind") == "scalar" else run_ours)(sub, cfg, emit=False)
+        if line is None:
+            continue
+        r = line["roofline"]
+        entry = {"desc": cfg["desc"], "value": line["value"], "unit": line["unit"], "ms_per_step": line["ms_per_step"],
+                 "steps": 20, "kernel": r.get("kernel"), "bound": r["bound"], "roofline_frac": r["frac"],
+                 "roofline_unit": r["unit"], "achieved": r["achieved"], "peak": r["peak"],
+                 "clocks": line.get("clocks")}
+        if r.get("hbm_frac") is not None:
+            entry["hbm_frac"] = r["hbm_frac"]
+        if r.get("tensor"):
+            entry["tensor_frac"] = r["tensor"]["frac"]
+        if "queries_per_s" in line:
+            entry["queries_per_s"] = line["queries_per_s"]
+        out[name] = entry
+    return out
+
+
 def main():
     args = parse()
     cfg = WORKLOADS[args.workload]
+    if (args.impl == "ours" and args.workload == "rowsel_64g" and not args.no_configs
+            and int(os.environ.get("WORLD_SIZE", "1")) == 1):
+        line = run_ours(args, cfg, emit=False)
+        if line is not None:
+            line["north_star_configs"] = north_star_configs(args)
+            print(json.dumps(line), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args, cfg)
     elif cfg.get("kind") == "scalar":
