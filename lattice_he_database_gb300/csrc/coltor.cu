@@ -257,7 +257,7 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint64_t c_stride, uint32_t ell, uint
     rc = gadget_dcp_launch(ctx, gadget_dcp_args(ctx, diff, LN, dig, R * 2, ell, w, 1), st);
     if (rc) return rc;
 
-    rc = pir_lift_ntt(ctx, dig, dn, R * 2 * ell, st);
+    rc = lift_ntt_digits(ctx, dig, dn, R * 2 * ell, w, st);
     if (rc) return rc;
 
     MacArgs ma;

@@ -48,6 +48,9 @@ static inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t
 
 int launch_status(cudaError_t e);  // maps a CUDA error to PIR_OK / PIR_ERR_CUDA
 
+// Lift + forward NTT of cnt rows of gadget digits below 2^w (ntt.cu).
+int lift_ntt_digits(pir_ctx *ctx, const uint32_t *raw, uint32_t *out, uint64_t cnt, uint32_t w, void *stream);
+
 // ---------------------------------------------------------------- modular helpers
 // Shoup product: w * y mod q in [0, 2q) for y < 2^32, w < q < 2^31,
 // wp = floor(w * 2^32 / q).

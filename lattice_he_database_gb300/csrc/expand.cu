@@ -293,7 +293,7 @@ int one_stage(pir_ctx *ctx, const uint32_t *evk, uint64_t evk_stride, uint32_t e
 
     rc = gadget_dcp_launch(ctx, gadget_dcp_args(ctx, coef, LN, dig, GM, ell, w, inv_mod_2n(k, 2 * ctx->N)), st);
     if (rc) return rc;
-    rc = pir_lift_ntt(ctx, dig, dn, GM * ell, st);
+    rc = lift_ntt_digits(ctx, dig, dn, GM * ell, w, st);
     if (rc) return rc;
 
     ExpMacArgs ma;
@@ -439,7 +439,7 @@ extern "C" int pir_rgsw_convert(pir_ctx *ctx, const uint32_t *ksk, uint32_t ell,
     if (rc) return rc;
     rc = gadget_dcp_launch(ctx, gadget_dcp_args(ctx, coef, LN, dig, M, ell, w, 1), st);
     if (rc) return rc;
-    rc = pir_lift_ntt(ctx, dig, dn, M * ell, st);
+    rc = lift_ntt_digits(ctx, dig, dn, M * ell, w, st);
     if (rc) return rc;
     RgswMacArgs ma;
     memset(&ma, 0, sizeof(ma));

@@ -140,7 +140,9 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
 // of the last round's inputs by warp shuffles -- a 16 x 16 transpose inside
 // each half-warp by xor butterflies, 32 shuffles and 64 selects per row --
 // measured slower than the swizzled shared-memory exchange.)
-template <bool LIFT>
+// SMALL (with LIFT): the caller guarantees every input word is below every
+// q_l (gadget digits), so the lift is the identity.
+template <bool LIFT, bool SMALL = false>
 __global__ void __launch_bounds__(kT4, 4) ntt4096x2_fwd_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                             uint64_t cnt, const __grid_constant__ RnsParams P) {
     __shared__ __align__(16) uint32_t sa[kN4];
@@ -166,8 +168,8 @@ __global__ void __launch_bounds__(kT4, 4) ntt4096x2_fwd_kernel(const uint32_t *_
     for (int i = 0; i < 16; ++i) {
         const uint32_t a = ld_na(src0 + t + 256 * i);
         const uint32_t b = two ? ld_na(src1 + t + 256 * i) : 0u;
-        x[i] = LIFT ? barrett32_lazy(a, q, mb) : a;   // [0, 2q): the rounds' input range
-        y[i] = LIFT ? barrett32_lazy(b, q, mb) : b;
+        x[i] = (LIFT && !SMALL) ? barrett32_lazy(a, q, mb) : a;   // [0, 2q): the rounds' input range
+        y[i] = (LIFT && !SMALL) ? barrett32_lazy(b, q, mb) : b;
     }
     const Swz4096 z(t);
     fwd_round16x2(x, y, 0, 0, T, q);
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kT4, 4) ntt4096x2_inv_kernel(const uint32_t *_
     inv4096x2_rounds(x, y, sa, sb, T, q, P.ninv[l], P.ninv_shoup[l], out + r0 * kN4, out + r1 * kN4, two);
 }
 
-template <bool FWD, bool LIFT = false>
+template <bool FWD, bool LIFT = false, bool SMALL = false>
 int ntt_launch(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, void *stream) {
     if (!ctx) return PIR_ERR_ARG;
     if (cnt == 0) return PIR_OK;
@@ -252,7 +254,7 @@ int ntt_launch(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, vo
             const uint64_t g2 = (cnt + 1) / 2 * ctx->L;
             if (g2 > 0x7fffffffull) return PIR_ERR_ARG;
             if (FWD)
-                ntt4096x2_fwd_kernel<LIFT><<<(unsigned)g2, kT4, 0, (cudaStream_t)stream>>>(in, out, cnt,
+                ntt4096x2_fwd_kernel<LIFT, SMALL><<<(unsigned)g2, kT4, 0, (cudaStream_t)stream>>>(in, out, cnt,
                                                                                          rns_params(ctx));
             else
                 ntt4096x2_inv_kernel<<<(unsigned)g2, kT4, 0, (cudaStream_t)stream>>>(in, out, cnt, rns_params(ctx));
@@ -277,5 +279,16 @@ extern "C" int pir_ntt_inv(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint
 }
 
 extern "C" int pir_lift_ntt(pir_ctx *ctx, const uint32_t *raw, uint32_t *out, uint64_t cnt, void *stream) {
+    return ntt_launch<true, true>(ctx, raw, out, cnt, stream);
+}
+
+// The lift + forward NTT of gadget digits (ColTor, ExpandQuery, the RGSW
+// conversion): when every digit is below every prime (2^w <= min q_l) the
+// lift is the identity and is skipped; otherwise as pir_lift_ntt.
+int lift_ntt_digits(pir_ctx *ctx, const uint32_t *raw, uint32_t *out, uint64_t cnt, uint32_t w, void *stream) {
+    if (!ctx) return PIR_ERR_ARG;
+    uint32_t qmin = ctx->q[0];
+    for (uint32_t l = 1; l < ctx->L; ++l) qmin = ctx->q[l] < qmin ? ctx->q[l] : qmin;
+    if (w < 32 && (1ull << w) <= qmin) return ntt_launch<true, true, true>(ctx, raw, out, cnt, stream);
     return ntt_launch<true, true>(ctx, raw, out, cnt, stream);
 }
