@@ -9,47 +9,52 @@
 // section 4.1 on both operands:
 //   * query residues a < 2^29 as balanced base-256 digits a_i in [-128, 128]
 //     (a = sum_i 256^i a_i exactly; a_3 <= 32),
-//   * DB residues b < 2^29 as their plain bytes b_j in [0, 255],
+//   * DB residues b < 2^29 as their plain bytes b_j in [0, 255], each taken
+//     as the fp16 subnormal b_j * 2^-24 (the halfword 0x00bb: a zero
+//     extension, two byte permutes per DB word),
 // so a*b = sum_{i,j} 256^(i+j) a_i b_j.  Every digit product is an integer of
-// magnitude <= 128*255, and 512 of them sum below 2^24: exact in fp32.  The
-// rows of a point are therefore taken in K segments of at most 512 rows.
+// magnitude <= 128*255 (times 2^-24), and 512 of them sum below 2^24 (times
+// 2^-24): exact in fp32.  The rows of a point are therefore taken in K
+// segments of at most 512 rows.
 //
-// MMA tile (one per 32 DB columns of a point and segment): M = 128 rows
-// (i, m) = 4 query digit planes x 32 polynomials, N = 128 columns (j, n) =
-// 4 DB byte planes x 32 columns, K = the segment's rows.  The A operand
-// (query digits of the segment) sits in TMEM for all tiles of the segment;
-// the accumulator (128 columns, double buffered) then holds S_ij[m][n].
+// MMA (M = 128, N = 256, K = 16): M rows = 32 polynomials x 4 query digit
+// planes (row 4m + i), N columns = 64 DB columns x 4 byte planes, K = DB
+// rows.  The A operand (query digits of the segment, 256 TMEM columns) sits in
+// TMEM for all tiles of the segment; the B operand is MN-major (a DB row's
+// bytes are contiguous along N, so a word's four bytes land side by side);
+// one accumulator (the other 256 TMEM columns) holds S_ij[m][n] * 2^-24 for
+// one 64-column tile.  Each MMA carries 128 tensor cycles of work, twice the
+// N = 128 shape: the issuing loop's fixed cost per barrier wait is then
+// mostly hidden behind the tensor pipe.
+//
 // The epilogue forms
 //     out[m][n] = sum_i 2^(8i) (sum_j 2^(8j) S_ij[m][n])  mod q
 // with one reduction per (i, m, n) (32-bit arithmetic and an fp32 quotient
-// estimate, valid for q >= 2^26) and a cross-plane sum; segments after the
-// first add their residue to the stored one.
+// estimate, valid for q >= 2^26) and a cross-plane sum over the four lanes
+// 4m .. 4m+3 by warp shuffles; segments after the first add their residue to
+// the stored one.
 //
-// Warp roles (512 threads, one CTA per SM, persistent over a range of points).
-// A warp's scheduler is fixed by warp % 4, and the MMA-issuing thread loses
-// most of its issue rate to any ALU-busy warp on its scheduler, so scheduler 1
-// carries only light roles besides the plane-1 epilogue:
-//   warps 0-3   query digits of the next segment -> TMEM (tcgen05.st), warp w
-//               writes digit plane w into TMEM lanes 32w..32w+31, from the
-//               segment's query slice that the producer bulk-copies into
-//               shared memory while the previous segment is still in flight
-//               (warps 0, 2, 3 also convert; warp 1 only writes digits);
-//   warps 4-7   epilogue: tcgen05.ld of a finished accumulator, reduction,
-//               cross-plane sum through shared memory, output stores;
-//   converters  three groups of three warps, {0, 2, 3}, {8, 10, 11} and
-//               {12, 14, 15}, each converting every third stage: 64 x 32 DB
-//               words (TMA-staged) -> 4 byte planes of fp16 in the
-//               128B-swizzled K-major layout of the B operand;
-//   warp 9      TMEM allocation and the TMA producer of query slices and DB
-//               word tiles;
-//   warp 13     MMA issue (one thread).
+// Warp roles (22 warps, one CTA per SM, persistent over a range of points).
+// A warp's scheduler is warp % 4 and a warp reaches only the TMEM lane
+// quarter warp % 4:
+//   warp 0        TMEM allocation; lane 0 is the TMA producer of query
+//                 slices and DB word tiles;
+//   warps 1-16    epilogue, four per lane quarter, each draining 64 of the
+//                 256 accumulator columns right after the tile's MMAs (so
+//                 the single accumulator is free again within a TMEM load),
+//                 then reducing them; they also write the query digits of
+//                 each segment into TMEM (lane quarter x a quarter of the rows);
+//   warp 17       MMA issue: the warp runs the loop (control flow and
+//                 operands warp-uniform), one elected lane issues;
+//   warps 18-21   converters: 64 x 64 DB words (TMA-staged) -> their bytes
+//                 as fp16 subnormals in the 128B-swizzled MN-major layout of
+//                 the B operand, a quarter of every stage each.
+// Registers: the 16 epilogue warps hold a drained tile (64 values a thread),
+// which caps the CTA at 22 warps; two converter warps measured 9.9 ms on the
+// 24 GiB x 16 case, four 7.3 ms, six the same, eight slower (spills).
 // DB word stages (TMA -> converters) and fp16 operand stages (converters ->
 // MMA) are separate rings, so a word stage is refilled as soon as it has
-// been read.  The MMA thread keeps its loop short: any shared-memory access
-// of the issuing thread (a barrier wait included) stalls until the tensor
-// core has taken its previous MMAs, so bookkeeping between MMAs leaves the
-// tensor pipe idle.
-// All mbarrier waits are bounded; TMEM is always released.
+// been read.  All mbarrier waits are bounded; TMEM is always released.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -60,22 +65,29 @@
 
 namespace {
 
-constexpr int TC_NR = 6;                      // DB word stages (TMA -> converters)
-constexpr int TC_NB = 6;                       // fp16 operand stages (converters -> MMA)
+constexpr int TC_NR = 4;                       // DB word stages (TMA -> converters)
+constexpr int TC_NB = 3;                       // fp16 operand stages (converters -> MMA)
 constexpr int TC_KS = 64;                      // DB rows (K) per stage
-constexpr int TC_NT = 32;                      // DB columns per MMA tile
-constexpr uint32_t TC_RAW_BYTES = TC_KS * TC_NT * 4;   // 8 KiB of DB words
-constexpr uint32_t TC_B_BYTES = 128 * 128;             // 128 rows x 64 fp16
-constexpr int TC_THREADS = 16 * 32;
+constexpr int TC_NT = 64;                      // DB columns per tile (N = 256)
+constexpr uint32_t TC_RAW_BYTES = TC_KS * TC_NT * 4;   // 16 KiB of DB words
+constexpr uint32_t TC_B_GROUP = 4096;                  // 8 rows x 256 halves
+constexpr uint32_t TC_B_BYTES = (TC_KS / 8) * TC_B_GROUP;   // 32 KiB
+constexpr int TC_EPI_WARPS = 16;
+constexpr int TC_CONV_WARPS = 4;
+constexpr int TC_W_MMA = 17;
+constexpr int TC_W_CONV = 18;
+constexpr int TC_THREADS = 22 * 32;
 constexpr uint32_t TC_TMEM_COLS = 512;
-constexpr uint32_t TC_ACC_COL = 256;           // accumulators at columns 256 and 384
+constexpr uint32_t TC_ACC_COL = 256;           // the accumulator: columns 256..511
 constexpr uint32_t TC_SEG = 512;               // rows per K segment: the exactness bound of one fp32 accumulation
 constexpr uint32_t TC_MIN_Q = 1u << 26;        // smallest prime the epilogue's reduction supports
 constexpr uint32_t TC_Q_BYTES = TC_SEG * 32 * 4;        // one segment's query slice (64 KiB)
-constexpr uint32_t TC_RED_PITCH = 33;          // words per row of the epilogue's plane sums (no bank conflicts)
 constexpr uint32_t TC_PREFETCH_PIECE = 64 * 1024;
 constexpr float TC_MAGIC = 12582912.0f;        // 1.5 * 2^23
 constexpr uint32_t TC_MAGIC_BITS = 0x4B400000u;
+constexpr float TC_SMAGIC = 0.75f;             // 1.5 * 2^-1: x + 0.75 has ulp 2^-24 for |x| <= 1/4
+constexpr uint32_t TC_SMAGIC_BITS = 0x3F400000u;
+constexpr float TC_UNSCALE = 16777216.0f;      // 2^24: accumulators hold S * 2^-24
 
 struct TcArgs {
     const uint32_t *qT;     // point-major query, [P][PS], 32 polynomials per k
@@ -92,22 +104,25 @@ struct TcArgs {
     uint32_t hook;                    // PIR_HOOK_* of the context
 };
 
-__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t j) {
-    return (row >> 3) * 1024u + (row & 7u) * 128u + ((j ^ (row & 7u)) << 4);
+// B operand of a stage (64 DB rows = K, 256 columns = N), MN-major with the
+// 128-byte swizzle: atoms of 8 K rows x 64 N halves (1 KiB), the four N
+// atoms of a group of 8 rows side by side (leading byte offset 1 KiB), groups
+// of 8 rows 4 KiB apart (stride byte offset); inside an atom, 16-byte chunk c
+// of row r sits at chunk position c ^ r.  One K = 16 MMA reads 8 KiB.
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(1024 >> 4) << 16) | ((uint64_t)(TC_B_GROUP >> 4) << 32) |
+           (1ull << 46) | (2ull << 61);
 }
 
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// kind::f16, A = B = F16, D = F32, K-major, N = 128, M = 128
-constexpr uint32_t TC_IDESC = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+// kind::f16, A = B = F16, D = F32, A K-major (TMEM), B MN-major, N = 256, M = 128
+constexpr uint32_t TC_IDESC = (1u << 4) | (1u << 16) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
 
 // The four K = 16 MMAs of one 64-row stage: A (query digits) from TMEM
-// columns a_tmem + 8*kk, B (DB byte planes) from the stage's swizzled tile,
-// whose descriptor start address advances 32 bytes (2 units) per kk.  The
-// first stage of a tile (ks == 0) starts the accumulator from zero.
+// columns a_tmem + 8*kk, B (DB bytes) from the stage's swizzled tile, whose
+// descriptor start address advances two row groups (8 KiB = 512 units) per
+// kk.  The first stage of a tile (ks == 0) starts the accumulator from zero.
 __device__ __forceinline__ void mma_stage(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t ks) {
+    constexpr uint64_t kstep = (2 * TC_B_GROUP) >> 4;
     asm volatile(
         "{\n.reg .pred p, t;\n"
         "setp.ne.b32 p, %3, 0;\n"
@@ -116,9 +131,20 @@ __device__ __forceinline__ void mma_stage(uint32_t d, uint32_t a_tmem, uint64_t 
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %4, t;\n"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %4, t;\n"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %4, t;\n}\n" ::"r"(d),
-        "r"(a_tmem), "l"(bdesc), "r"(ks), "r"(TC_IDESC), "r"(a_tmem + 8), "l"(bdesc + 2), "r"(a_tmem + 16),
-        "l"(bdesc + 4), "r"(a_tmem + 24), "l"(bdesc + 6)
+        "r"(a_tmem), "l"(bdesc), "r"(ks), "r"(TC_IDESC), "r"(a_tmem + 8), "l"(bdesc + kstep), "r"(a_tmem + 16),
+        "l"(bdesc + 2 * kstep), "r"(a_tmem + 24), "l"(bdesc + 3 * kstep)
         : "memory");
+}
+
+// One lane of a fully active warp (the same one every time): true there.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n.reg .pred P;\n"
+        "elect.sync _|P, 0xffffffff;\n"
+        "selp.u32 %0, 1, 0, P;\n}\n"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 __device__ __forceinline__ void commit(uint64_t *bar) {
@@ -162,6 +188,35 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Bounded wait that lets the thread sleep in the hardware until the phase
+// completes (suspend-time hint) instead of spinning: for warps that wait most
+// of the time, so their issue slots go to the warps sharing their scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(1000000u)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t *status, uint64_t limit_ns) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait_sleep(a, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_sleep(a, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(status, PIR_STATUS_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // Balanced base-256 digit `plane` of two residues a0, a1 < 2^29, packed as
 // two fp16 values (a0 in the low half).  a + 0x808080 has the bytes d_i + 128
 // (i < 3) and d_3 on top, because balanced digits never carry; 0x64xx is the
@@ -180,7 +235,7 @@ __device__ __forceinline__ uint32_t seg_stages(const TcArgs &A, uint32_t h) {
     return (seg_rows(A, h) + TC_KS - 1) / TC_KS;
 }
 
-// Number of 32-column tiles of slab s.
+// Number of 64-column tiles of slab s.
 __device__ __forceinline__ uint32_t tiles_of(const TcArgs &A, uint32_t s) {
     const uint32_t w = (s == A.S - 1) ? A.Wlast : PIR_SLAB;
     return (w + TC_NT - 1) / TC_NT;
@@ -196,42 +251,39 @@ __device__ __forceinline__ void l2_prefetch(const void *src, uint64_t bytes) {
     }
 }
 
-// A stage holds 64 DB rows x 32 columns of words (row-major).  Converting it
-// writes the 4 byte planes as fp16 in the 128B-swizzled K-major B layout
-// (row j*32 + n, K = DB row).  The work is cut into 8 chunks of 8 rows; lane
-// n of a converter warp handles column n of chunks kc = gw, gw + 3, gw + 6
-// (gw = the warp's position 0..2 in its group of three).
-__device__ __forceinline__ void load_chunks(const uint32_t *raw, uint32_t gw, uint32_t n, uint32_t (&w)[3][8]) {
+// A stage holds 64 DB rows x 64 columns of words (row-major, 256 bytes a
+// row).  Converting it writes every byte as an fp16 subnormal (the halfword
+// 0x00bb = bb * 2^-24) into the MN-major B tile; byte j of column
+// n = 32 hr + 4 q4 + e (hr = 0, 1; q4 = 0..7; e = 0..3) goes to
+//     N = 128 hr + 64 (e / 2) + 8 q4 + 4 (e % 2) + j,
+// i.e. N atom 2 hr + e / 2, chunk q4.  A lane's task is one row and four
+// columns (one 16-byte load): columns 4 q4 + 0, 1 fill chunk q4 of atom 2 hr,
+// columns 4 q4 + 2, 3 chunk q4 of atom 2 hr + 1, so the eight lanes of a
+// quarter-warp (one half row) load 128 contiguous bytes and store to eight
+// distinct chunk positions.  Converter warp cw takes rows 8c + 2cw + (0, 1),
+// c = 0..7: a quarter of every stage.
+constexpr int TC_CTASKS = 8;
+
+__device__ __forceinline__ void load_tasks(const uint32_t *raw, uint32_t cw, uint32_t lane, uint4 (&w)[TC_CTASKS]) {
+    const uint32_t *base = raw + (2 * cw + (lane >> 4)) * TC_NT + 4 * (lane & 15);
 #pragma unroll
-    for (int c = 0; c < 3; ++c) {
-        const uint32_t kc = gw + 3 * c;
-        if (kc < 8) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[c][e] = raw[(kc * 8 + e) * TC_NT + n];
-        }
-    }
+    for (int c = 0; c < TC_CTASKS; ++c) w[c] = *reinterpret_cast<const uint4 *>(base + 8 * c * TC_NT);
 }
 
-__device__ __forceinline__ void store_chunks(uint8_t *bt, uint32_t gw, uint32_t n, const uint32_t (&w)[3][8]) {
+// bytes 0, 1 (sel 0x4140) or 2, 3 (sel 0x4342) of x, each zero-extended to a halfword
+__device__ __forceinline__ uint32_t zx_pair(uint32_t x, uint32_t sel) { return __byte_perm(x, 0u, sel); }
+
+__device__ __forceinline__ void store_tasks(uint8_t *bt, uint32_t cw, uint32_t lane, const uint4 (&w)[TC_CTASKS]) {
+    const uint32_t q16 = lane & 15, hr = q16 >> 3, q4 = q16 & 7;
+    const uint32_t re = 2 * cw + (lane >> 4);   // row in its group of 8
+    uint8_t *pe = bt + hr * 2048 + re * 128 + ((q4 ^ re) << 4);
 #pragma unroll
-    for (int c = 0; c < 3; ++c) {
-        const uint32_t kc = gw + 3 * c;
-        if (kc < 8) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t hv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    // bytes j of two words -> halves 0x64xx = 1024 + byte
-                    const uint32_t x = __byte_perm(w[c][2 * e], w[c][2 * e + 1], j | ((4 + j) << 8));
-                    const uint32_t hh = (x & 0x00FF00FFu) | 0x64006400u;
-                    const __half2 r =
-                        __hsub2(*reinterpret_cast<const __half2 *>(&hh), __floats2half2_rn(1024.f, 1024.f));
-                    hv[e] = *reinterpret_cast<const uint32_t *>(&r);
-                }
-                *reinterpret_cast<uint4 *>(bt + sw128(j * 32 + n, kc)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            }
-        }
+    for (int c = 0; c < TC_CTASKS; ++c) {
+        uint8_t *d = pe + c * TC_B_GROUP;
+        *reinterpret_cast<uint4 *>(d) = make_uint4(zx_pair(w[c].x, 0x4140), zx_pair(w[c].x, 0x4342),
+                                                   zx_pair(w[c].y, 0x4140), zx_pair(w[c].y, 0x4342));
+        *reinterpret_cast<uint4 *>(d + 1024) = make_uint4(zx_pair(w[c].z, 0x4140), zx_pair(w[c].z, 0x4342),
+                                                          zx_pair(w[c].w, 0x4140), zx_pair(w[c].w, 0x4342));
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -242,15 +294,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     extern __shared__ uint8_t smraw[];
     const uint32_t base_s = smem_u32(smraw);
     uint8_t *sm = smraw + (((base_s + 1023u) & ~1023u) - base_s);
-    uint8_t *stB = sm;                                   // [NS][16 KiB] fp16 digit tiles
-    uint8_t *stR = stB + TC_NB * TC_B_BYTES;             // [NR][8 KiB] DB words
-    uint32_t *qsm = reinterpret_cast<uint32_t *>(stR + TC_NR * TC_RAW_BYTES);   // [D0][32] query slice
-    uint32_t *red = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(qsm) + TC_Q_BYTES);  // [128][33]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(red + 128 * TC_RED_PITCH);
+    uint8_t *stB = sm;                                   // [NB][32 KiB] fp16 operand tiles
+    uint8_t *stR = stB + TC_NB * TC_B_BYTES;             // [NR][16 KiB] DB words
+    uint32_t *qsm = reinterpret_cast<uint32_t *>(stR + TC_NR * TC_RAW_BYTES);   // [512][32] query slice
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(qsm) + TC_Q_BYTES);
     uint64_t *rfull = bars, *rempty = rfull + TC_NR, *bfull = rempty + TC_NR, *bempty = bfull + TC_NB;
-    uint64_t *accf = bempty + TC_NB, *acce = accf + 2, *afull = acce + 2, *aempty = afull + 1, *done = aempty + 1;
-    uint64_t *qfull = done + 1, *qempty = qfull + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(qempty + 1);
+    uint64_t *accf = bempty + TC_NB, *acce = accf + 1, *afull = acce + 1, *qfull = afull + 1, *qempty = qfull + 1;
+    uint64_t *done = qempty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -260,25 +311,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_NR; ++s) {
             mbar_init(rfull + s, 1);
-            mbar_init(rempty + s, 3);
+            mbar_init(rempty + s, TC_CONV_WARPS);
         }
         for (int s = 0; s < TC_NB; ++s) {
-            mbar_init(bfull + s, 3);
+            mbar_init(bfull + s, TC_CONV_WARPS);
             mbar_init(bempty + s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(accf + b, 1);
-            mbar_init(acce + b, 4);
-        }
-        mbar_init(afull, 4);
-        mbar_init(aempty, 1);
-        mbar_init(done, 1);
+        mbar_init(accf, 1);
+        mbar_init(acce, TC_EPI_WARPS);
+        mbar_init(afull, TC_EPI_WARPS);
         mbar_init(qfull, 1);
-        mbar_init(qempty, 4);
+        mbar_init(qempty, TC_EPI_WARPS);
+        mbar_init(done, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TC_TMEM_COLS)
                      : "memory");
@@ -289,19 +337,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 9 && lane == 0) {
+    if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer: query slices and DB word tiles
         // The next segment's query slice is prefetched into L2 a segment ahead.
-        // (Prefetching whole DB slab blocks ahead was measured too: 152 SMs x
-        // two 256 KiB slabs crowd the L2 next to the streaming result writes,
-        // and 40% of the DB was read twice.)
         const uint64_t pol = policy_evict_first();
         uint32_t it = 0, pc = 0;
         bool withheld = false;
 
         for (uint64_t p = p_begin; p < p_end; ++p)
           for (uint32_t h = 0; h < A.H; ++h, ++pc) {
-            // the segment's query slice (the query warps release the buffer once digitised)
+            // the segment's query slice (the digit writers release the buffer once digitised)
             const uint32_t nks = seg_stages(A, h), qbytes = seg_rows(A, h) * 32 * 4;
             const uint32_t *qsrc = A.qT + p * A.PS + (uint64_t)h * TC_SEG * 32;
             if (abort_flag || !mbar_wait(qempty, (pc & 1) ^ 1, A.status, A.wait_ns)) {
@@ -319,7 +364,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (uint32_t t = 0; t < nt; ++t)
                     for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
                         const uint32_t st = it % TC_NR, ph = (it / TC_NR) & 1;
-                        if (abort_flag || !mbar_wait(rempty + st, ph ^ 1, A.status, A.wait_ns)) {
+                        if (abort_flag || !mbar_wait_sleep(rempty + st, ph ^ 1, A.status, A.wait_ns)) {
                             abort_flag = 1;
                             continue;
                         }
@@ -347,224 +392,216 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_wait(rfull + j % TC_NR, (j / TC_NR) & 1, A.status);
         }
         if (pc) mbar_wait(qfull, (pc - 1) & 1, A.status);
-    } else if (warp == 13 && lane == 0) {
+    } else if (warp == TC_W_MMA) {
         // ------------------------------------------------ MMA issue
-        // One thread whose warp shares its scheduler with three busy warps:
-        // the per-stage path is kept short (a local abort flag, descriptors
-        // advanced by addition, the stage's four MMAs in one asm block).
+        // The whole warp runs the loop (its control flow and operands stay
+        // warp-uniform); one elected lane issues the MMAs and commits.
         bool ab = false;
-        uint32_t it = 0, g = 0, pc = 0, st = 0, ph = 0;
-        const uint64_t bdesc0 = sdesc(smem_u32(stB));
+        uint32_t g = 0, pc = 0, st = 0, ph = 0;
+        const uint64_t bdesc0 = sdesc_mn(smem_u32(stB));
+        const uint32_t d = tmem + TC_ACC_COL;
         for (uint64_t p = p_begin; p < p_end; ++p)
-          for (uint32_t h = 0; h < A.H; ++h) {
-            ab = ab || abort_flag;
+          for (uint32_t h = 0; h < A.H; ++h, ++pc) {
+            ab = __any_sync(0xffffffffu, ab || abort_flag);
             bool first = true;
             const uint32_t nks = seg_stages(A, h);
             for (uint32_t s = 0; s < A.S; ++s) {
                 const uint32_t nt = tiles_of(A, s);
                 for (uint32_t t = 0; t < nt; ++t, ++g) {
-                    const uint32_t buf = g & 1, use = (g >> 1) & 1;
-                    if (!ab && !mbar_wait(acce + buf, use ^ 1, A.status, A.wait_ns)) ab = true;
+                    // the previous tile's accumulator has been drained; the segment's digits are in TMEM
+                    bool bad = !ab && !mbar_wait(acce, (g & 1) ^ 1, A.status, A.wait_ns);
                     if (first) {
-                        if (!ab && !mbar_wait(afull, pc & 1, A.status, A.wait_ns)) ab = true;
+                        bad = bad || (!ab && !mbar_wait(afull, pc & 1, A.status, A.wait_ns));
                         first = false;
                     }
-                    const uint32_t d = tmem + TC_ACC_COL + buf * 128;
-                    for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
-                        if (!ab && !mbar_wait(bfull + st, ph, A.status, A.wait_ns)) ab = true;
+                    ab = __any_sync(0xffffffffu, ab || bad);
+                    for (uint32_t ks = 0; ks < nks; ++ks) {
+                        ab = __any_sync(0xffffffffu, ab || !mbar_wait(bfull + st, ph, A.status, A.wait_ns));
                         if (!ab) {
                             fence_after();
-                            mma_stage(d, tmem + ks * 32, bdesc0 + st * (TC_B_BYTES >> 4), ks);
-                            commit(bempty + st);
+                            if (elect_one()) {
+                                mma_stage(d, tmem + ks * 32, bdesc0 + st * (TC_B_BYTES >> 4), ks);
+                                commit(bempty + st);
+                            }
+                            __syncwarp();
                         }
                         if (++st == TC_NB) {
                             st = 0;
                             ph ^= 1;
                         }
                     }
-                    if (!ab) commit(accf + buf);
+                    if (!ab && elect_one()) commit(accf);
+                    __syncwarp();
                 }
             }
-            commit(aempty);  // A (query digits) reusable once this segment's MMAs finish
-            ++pc;
           }
-        if (ab) abort_flag = 1;
-        commit(done);
+        if (lane == 0 && ab) abort_flag = 1;
+        if (elect_one()) commit(done);
+        __syncwarp();
         mbar_wait(done, 0, A.status);
-    } else if (warp < 4 || (warp >= 8 && (warp & 3) != 1)) {
-        // ------------------------------------------------ query digits and converters
-        // Warps 0-3 write the query digits of each segment into TMEM (plane =
-        // warp) before that segment's stages.  Three groups of three converter
-        // warps -- {0, 2, 3}, {8, 10, 11}, {12, 14, 15} -- take every third
-        // stage each; none of them shares a scheduler with the MMA warp (13).
-        const bool digitizer = warp < 4, converter = warp != 1;
-        const uint32_t gi = warp < 4 ? 0u : (uint32_t)(warp >> 2) - 1u;          // group 0..2
-        const uint32_t gw = (warp & 3) == 0 ? 0u : (uint32_t)(warp & 3) - 1u;     // position 0..2
-        uint32_t it = 0, pc = 0, sel = 0;                                         // sel = it % 3
+    } else if (warp >= TC_W_CONV) {
+        // ------------------------------------------------ converters
+        const uint32_t cw = (uint32_t)(warp - TC_W_CONV);
+        uint32_t it = 0;
         for (uint64_t p = p_begin; p < p_end; ++p)
-          for (uint32_t h = 0; h < A.H; ++h, ++pc) {
+          for (uint32_t h = 0; h < A.H; ++h) {
             const uint32_t nks = seg_stages(A, h);
-            if (digitizer) {
-                // query digits of the segment -> TMEM (plane = warp, polynomial m = lane)
-                const uint32_t plane = warp, m = lane, rows = seg_rows(A, h);
-                if (!abort_flag && !mbar_wait(qfull, pc & 1, A.status, A.wait_ns)) abort_flag = 1;
-                if (!abort_flag && !mbar_wait(aempty, (pc & 1) ^ 1, A.status, A.wait_ns)) abort_flag = 1;
-                fence_after();
-                if (!abort_flag) {
-                    const bool live = m < A.Mv;
-                    for (uint32_t kc = 0; kc < nks; ++kc) {
-                        uint32_t v[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const uint32_t k0 = kc * 64 + 2 * e;
-                            const uint32_t a0 = (live && k0 < rows) ? qsm[k0 * 32 + m] : 0u;
-                            const uint32_t a1 = (live && k0 + 1 < rows) ? qsm[(k0 + 1) * 32 + m] : 0u;
-                            v[e] = digit_pair(a0, a1, plane);
-                        }
-                        tmem_st32(tmem + ((plane * 32u) << 16) + kc * 32, v);
-                    }
-                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                }
-                fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(afull);
-                    mbar_arrive(qempty);
-                }
-            }
-            if (!converter) continue;
             for (uint32_t s = 0; s < A.S; ++s) {
                 const uint32_t nt = tiles_of(A, s);
                 for (uint32_t t = 0; t < nt; ++t)
                     for (uint32_t ks = 0; ks < nks; ++ks, ++it) {
-                        const bool my_stage = sel == gi;
-                        sel = sel == 2 ? 0u : sel + 1;
-                        if (!my_stage) continue;
                         const uint32_t rs = it % TC_NR, rph = (it / TC_NR) & 1;
                         const uint32_t bs = it % TC_NB, bph = (it / TC_NB) & 1;
-                        uint32_t w[3][8];
+                        uint4 w[TC_CTASKS];
                         if (!abort_flag && !mbar_wait(rfull + rs, rph, A.status, A.wait_ns)) abort_flag = 1;
                         if (!abort_flag)
-                            load_chunks(reinterpret_cast<const uint32_t *>(stR + rs * TC_RAW_BYTES), gw, lane, w);
+                            load_tasks(reinterpret_cast<const uint32_t *>(stR + rs * TC_RAW_BYTES), cw, lane, w);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(rempty + rs);     // the words are in registers
                         if (!abort_flag && !mbar_wait(bempty + bs, bph ^ 1, A.status, A.wait_ns)) abort_flag = 1;
-                        if (!abort_flag) store_chunks(stB + bs * TC_B_BYTES, gw, lane, w);
+                        if (!abort_flag) store_tasks(stB + bs * TC_B_BYTES, cw, lane, w);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bfull + bs);
                     }
             }
           }
-    } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------ epilogue
-        const uint32_t plane = warp & 3, m = lane;
-        const uint32_t etid = threadIdx.x - 128;  // 0..127
-        uint32_t g = 0;
+    } else if (warp >= 1 && warp <= TC_EPI_WARPS) {
+        // ------------------------------------------------ epilogue and query digits (warps 1-16)
+        // Lane quarter qq = warp % 4 (TMEM lanes 32 qq .. 32 qq + 31 = polynomials
+        // 8 qq .. 8 qq + 7, lane = 4 (m - 8 qq) + i), accumulator columns
+        // 64 cq .. 64 cq + 63 (cq = (warp - 1) / 4): DB columns
+        // n = 32 hr + 4 q4 + 2 (cq % 2) + e1 with hr = cq / 2, q4 = 0..7, e1 = 0, 1.
+        const uint32_t qq = (uint32_t)warp & 3u, cq = (uint32_t)(warp - 1) >> 2;
+        const uint32_t i = (uint32_t)lane & 3u, m = 8 * qq + ((uint32_t)lane >> 2);
+        const uint32_t b0 = i & 1u, b1 = i >> 1;
+        const bool live = m < A.Mv;
+        uint32_t g = 0, pc = 0;
         for (uint64_t p = p_begin; p < p_end; ++p)
-          for (uint32_t h = 0; h < A.H; ++h) {
+          for (uint32_t h = 0; h < A.H; ++h, ++pc) {
             const uint32_t l = (uint32_t)(p / A.N);
             const uint32_t q = A.q[l];
             const float qinv = A.qinv[l];
-            const uint32_t ci = A.c[l][plane], cis = A.cs[l][plane];
-            // + q, + 0x4B400000 * q for the quotient's magic bits, - the magic offsets in lo
-            const uint32_t lo_off = plane == 3 ? TC_MAGIC_BITS + (TC_MAGIC_BITS << 8) : TC_MAGIC_BITS << 24;
-            const uint32_t rc = q + TC_MAGIC_BITS * q - lo_off;
+            const uint32_t ci = A.c[l][i], cis = A.cs[l][i];
+            // + q, + 0x4B400000 * q for the quotient's magic bits, - the magic offset of S_3 in lo
+            const uint32_t rc = q + TC_MAGIC_BITS * q - (TC_SMAGIC_BITS << 24);
+            const uint32_t nks = seg_stages(A, h), rows = seg_rows(A, h);
+            // query digits of the segment -> TMEM.  The A operand is free: every
+            // MMA of the previous segment completed before its last accumulator
+            // was handed to this warp.
+            // (every TMEM access below is taken or skipped by the whole warp)
+            bool ok = __all_sync(0xffffffffu, !abort_flag && mbar_wait_sleep(qfull, pc & 1, A.status, A.wait_ns));
+            if (!ok) abort_flag = 1;
+            fence_after();
+            if (ok) {
+                for (uint32_t kc = cq; kc < nks; kc += 4) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const uint32_t k0 = kc * 64 + 2 * e;
+                        const uint32_t a0 = (live && k0 < rows) ? qsm[k0 * 32 + m] : 0u;
+                        const uint32_t a1 = (live && k0 + 1 < rows) ? qsm[(k0 + 1) * 32 + m] : 0u;
+                        v[e] = digit_pair(a0, a1, i);
+                    }
+                    tmem_st32(tmem + ((qq * 32u) << 16) + kc * 32, v);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(afull);
+                mbar_arrive(qempty);
+            }
             for (uint32_t s = 0; s < A.S; ++s) {
                 const uint32_t nt = tiles_of(A, s);
                 const uint32_t Ws = (s == A.S - 1) ? A.Wlast : PIR_SLAB;
                 for (uint32_t t = 0; t < nt; ++t, ++g) {
-                    const uint32_t buf = g & 1, use = (g >> 1) & 1;
-                    if (!abort_flag && !mbar_wait(accf + buf, use, A.status, A.wait_ns)) abort_flag = 1;
+                    ok = __all_sync(0xffffffffu, !abort_flag && mbar_wait_sleep(accf, g & 1, A.status, A.wait_ns));
+                    if (!ok) abort_flag = 1;
                     fence_after();
-                    // W[n] = sum_j 2^(8j) S_j[n] = sum_k d_i(query) * DB word is reduced
-                    // mod q without 64-bit arithmetic.  Its low 32 bits come exactly
-                    // from wrapping 32-bit sums of the integer plane sums S_j; the
-                    // quotient k = round(W / q) comes from an fp32 estimate of W.
-                    // Every partial sum of the estimate is below 128 * 512 * (2^24 + q)
-                    // <= 2^46 (a segment has at most 512 rows), so its three roundings
-                    // add at most 3 * 2^22, and |W| / q <= 128 * 512 = 2^16; with
-                    // q >= 2^26 the estimate of W / q is off by less than 0.2 and
-                    // W - k*q lies in (-0.7q, 1.7q).
-                    // Integer conversions: an fp32 integer x with |x| < 2^22 gives
-                    // x + 1.5 * 2^23 exactly, whose bits are 0x4B400000 + x (an FADD
-                    // instead of a conversion).  That holds for S_3 (top DB byte
-                    // <= 31: |S| <= 128 * 31 * 512), for every S of plane 3 (top
-                    // query digit <= 32: |S| <= 32 * 255 * 512 < 2^22) and for the
-                    // quotient k; the other sums reach 2^24 and are converted.  The
-                    // offsets the magic bits leave in lo and in k*q are folded into rc.
-                    uint32_t lo[32];
-                    float wf[32];
+                    uint32_t v0[32], v1[32];
+                    if (ok) {
+                        const uint32_t taddr = tmem + ((qq * 32u) << 16) + TC_ACC_COL + 64 * cq;
+                        tmem_ld32(taddr, v0);
+                        tmem_ld32(taddr + 32, v1);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    } else {
 #pragma unroll
-                    for (int n = 0; n < 32; ++n) {
-                        lo[n] = 0;
-                        wf[n] = 0.f;
-                    }
-                    if (!abort_flag) {
-                        const uint32_t taddr = tmem + ((plane * 32u) << 16) + TC_ACC_COL + buf * 128;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint32_t v[32];
-                            tmem_ld32(taddr + j * 32, v);
-                            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                            const float scale = (float)(1u << (8 * j));
-                            if (j == 3 || plane == 3) {
-#pragma unroll
-                                for (int n = 0; n < 32; ++n) {
-                                    const float x = __uint_as_float(v[n]);
-                                    lo[n] += __float_as_uint(x + TC_MAGIC) << (8 * j);
-                                    wf[n] = fmaf(x, scale, wf[n]);
-                                }
-                            } else {
-#pragma unroll
-                                for (int n = 0; n < 32; ++n) {
-                                    const float x = __uint_as_float(v[n]);
-                                    lo[n] += (uint32_t)__float2int_rn(x) << (8 * j);
-                                    wf[n] = fmaf(x, scale, wf[n]);
-                                }
-                            }
-                        }
+                        for (int x = 0; x < 32; ++x) v0[x] = v1[x] = 0u;
                     }
                     fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(acce + buf);  // accumulator drained
-                    named_barrier(2, 128);                    // previous tile's readers of red are done
+                    if (lane == 0) mbar_arrive(acce);  // accumulator drained: the next tile's MMAs may start
+                    // W = sum_j 2^(8j) S_j = sum_k d_i(query) * DB word is reduced mod q
+                    // without 64-bit arithmetic.  Its low 32 bits come exactly from
+                    // wrapping 32-bit sums of the integer plane sums S_j; the quotient
+                    // k = round(W / q) comes from an fp32 estimate of W.  Every partial
+                    // sum of the estimate is below 128 * 512 * (2^24 + q) <= 2^46 (a
+                    // segment has at most 512 rows), so its three roundings add at most
+                    // 3 * 2^22, and |W| / q <= 128 * 512 = 2^16; with q >= 2^26 the
+                    // estimate of W / q is off by less than 0.2 and W - k*q lies in
+                    // (-0.7q, 1.7q).  The accumulators hold x = S * 2^-24: S_3 (top DB
+                    // byte <= 31: |S| <= 128 * 31 * 512 < 2^22) comes from the bits of
+                    // x + 0.75 (exact, ulp 2^-24: 0x3F400000 + S), the other sums
+                    // (up to 2^24) from converting x * 2^24 (exact).
+                    uint32_t y[16];
 #pragma unroll
-                    for (int n = 0; n < 32; ++n) {
+                    for (int u = 0; u < 16; ++u) {
+                        // local column u = 8 t' + 2 q4' + e1: load t', q4 = 4 t' + q4'
+                        const int tp = u >> 3, q4p = (u >> 1) & 3, e1 = u & 1;
+                        uint32_t lo = 0;
+                        float wf = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int idx = 8 * q4p + 4 * e1 + j;
+                            const float x = __uint_as_float(tp ? v1[idx] : v0[idx]);
+                            const uint32_t si = j == 3 ? __float_as_uint(x + TC_SMAGIC)
+                                                       : (uint32_t)__float2int_rn(x * TC_UNSCALE);
+                            lo += si << (8 * j);
+                            wf = fmaf(x, TC_UNSCALE * (float)(1u << (8 * j)), wf);
+                        }
                         // W - k*q lies in (-0.7q, 1.7q); + q makes it a positive 32-bit value
                         // congruent to W, which the Shoup product accepts as is: 2^(8i) * W
                         // mod q lands in [0, 2q)
-                        const uint32_t kb = __float_as_uint(fmaf(wf[n], qinv, TC_MAGIC));   // 0x4B400000 + k
-                        const uint32_t r = lo[n] - kb * q + rc;
-                        red[(plane * 32 + m) * TC_RED_PITCH + n] = shoup_mul(r, ci, cis, q);
+                        const uint32_t kb = __float_as_uint(fmaf(wf, qinv, TC_MAGIC));   // 0x4B400000 + k
+                        const uint32_t r = lo - kb * q + rc;
+                        y[u] = shoup_mul(r, ci, cis, q);
                     }
-                    named_barrier(2, 128);
-                    {
-                        // this thread's outputs: column nn, rows m0, m0 + 4, ..., m0 + 28
-                        const uint32_t nn = etid & 31, m0 = etid >> 5;
-                        const uint32_t col = t * TC_NT + nn;
-                        if (col < Ws) {
-                            uint32_t v[8];
+                    // Sum over the four planes (lanes 4m' .. 4m'+3) as a reduce-scatter:
+                    // after the xor-1 step a lane keeps the columns u with u % 2 == i % 2,
+                    // after the xor-2 step those with u % 4 == i (four terms in [0, 2q):
+                    // below 8q < 2^32).
+                    uint32_t z[8];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const uint32_t *rr = red + (m0 + 4 * i) * TC_RED_PITCH + nn;
-                                // four plane terms, each in [0, 2q): the sum is below 8q < 2^32
-                                v[i] = rr[0] + rr[32 * TC_RED_PITCH] + rr[64 * TC_RED_PITCH] + rr[96 * TC_RED_PITCH];
-                            }
-                            uint32_t *o = A.outT + (p * A.Mv + m0) * A.D1p + s * PIR_SLAB + col;
-                            const size_t ostep = (size_t)4 * A.D1p;
+                    for (int a = 0; a < 8; ++a) {
+                        const uint32_t keep = b0 ? y[2 * a + 1] : y[2 * a];
+                        const uint32_t send = b0 ? y[2 * a] : y[2 * a + 1];
+                        z[a] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                    }
+                    uint32_t wsum[4];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                if (m0 + 4 * i < A.Mv) {
-                                    uint32_t x = v[i];
-                                    x = min(x, x - 4 * q);   // x - cq wraps above x when x < cq
-                                    x = min(x, x - 2 * q);
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t keep = b1 ? z[2 * c + 1] : z[2 * c];
+                        const uint32_t send = b1 ? z[2 * c] : z[2 * c + 1];
+                        wsum[c] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+                    }
+                    if (live && ok) {
+                        uint32_t *orow = A.outT + (p * A.Mv + m) * A.D1p + s * PIR_SLAB + t * TC_NT;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            // column u = 4c + i: t' = c / 2, q4 = 4 t' + 2 (c % 2) + b1, e1 = b0
+                            const uint32_t q4 = 4 * (c >> 1) + 2 * (c & 1) + b1;
+                            const uint32_t n = 32 * (cq >> 1) + 4 * q4 + 2 * (cq & 1) + b0;
+                            if (t * TC_NT + n < Ws) {
+                                uint32_t x = wsum[c];
+                                x = min(x, x - 4 * q);   // x - cq wraps above x when x < cq
+                                x = min(x, x - 2 * q);
+                                x = min(x, x - q);
+                                if (h) {   // later segments add to the sum this thread stored for the earlier ones
+                                    x += orow[n];
                                     x = min(x, x - q);
-                                    if (h) {   // later segments add to the sum this thread stored for the earlier ones
-                                        x += o[i * ostep];
-                                        x = min(x, x - q);
-                                    }
-                                    o[i * ostep] = x;
                                 }
+                                orow[n] = x;
                             }
                         }
                     }
@@ -575,7 +612,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 0) {
         fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS)
                      : "memory");
@@ -596,8 +633,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 size_t tc_smem_bytes() {
-    return 1024 + (size_t)TC_NB * TC_B_BYTES + (size_t)TC_NR * TC_RAW_BYTES + TC_Q_BYTES + 128 * TC_RED_PITCH * 4 +
-           (2 * TC_NR + 2 * TC_NB + 11) * 8 + 16;
+    return 1024 + (size_t)TC_NB * TC_B_BYTES + (size_t)TC_NR * TC_RAW_BYTES + TC_Q_BYTES +
+           (2 * TC_NR + 2 * TC_NB + 6) * 8 + 16;
 }
 
 uint64_t powmod_host(uint64_t b, uint64_t e, uint64_t m) {
@@ -631,9 +668,7 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
     const uint32_t Wlast = D1p - PIR_SLAB * (S - 1);
 
     // Full slabs: 4-D view (column, row k, slab, point) of the first S-1 slabs of every point.
-    // L2 promotion stays at 128 B: a tile reads one 128-byte line of each
-    // 512-byte slab row, and 256-byte promotion fetched the neighbouring
-    // tile's line too, which was evicted before use (30% more DRAM reads).
+    // A tile reads one 256-byte half of each 512-byte slab row (L2 promotion 256 B).
     CUtensorMap full_map, last_map;
     memset(&full_map, 0, sizeof(full_map));
     memset(&last_map, 0, sizeof(last_map));
@@ -644,7 +679,7 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
         const cuuint64_t dim[4] = {PIR_SLAB, D0, S - 1, P};
         const cuuint64_t str[3] = {(cuuint64_t)PIR_SLAB * 4, (cuuint64_t)D0 * PIR_SLAB * 4, (cuuint64_t)D0 * D1p * 4};
         if (encode(&full_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, dbp, dim, str, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PIR_ERR_ARG;
     }
@@ -654,7 +689,7 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
         const cuuint64_t str[3] = {(cuuint64_t)Wlast * 4, (cuuint64_t)D0 * Wlast * 4, (cuuint64_t)D0 * D1p * 4};
         void *lastp = const_cast<uint32_t *>(db + (uint64_t)(S - 1) * D0 * PIR_SLAB);
         if (encode(&last_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, lastp, dim, str, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PIR_ERR_ARG;
     }

@@ -4,16 +4,17 @@ The kernel reduces W = sum_j 2^(8j) S_j mod q, where the S_j are the exact
 integer sums of one query digit plane i against the four DB byte planes
 over a K segment of at most 512 rows (|S_j| <= 128 * 255 * 512 for i, j < 3;
 the top query digit (<= 32) bounds plane 3, the top byte of a residue
-below q bounds S_3), without 64-bit arithmetic:
+below q bounds S_3), without 64-bit arithmetic.  The DB bytes enter the
+tensor cores as fp16 subnormals b * 2^-24, so the accumulators hold
+x_j = S_j * 2^-24 (exact in fp32):
 
     lo = sum_j t_j << 8j              (wrapping 32-bit), where t_j is
-         S_j converted to an integer, or, where |S_j| < 2^22 (j = 3, and
-         every j of plane 3), the fp32 bits of S_j + 1.5 * 2^23, which are
-         0x4B400000 + S_j
-    wf = fma(S_3, 2^24, fma(S_2, 2^16, fma(S_1, 2^8, S_0)))   (fp32)
+         x_j * 2^24 converted to an integer, or, for j = 3 (|S_3| < 2^22),
+         the fp32 bits of x_3 + 0.75, which are 0x3F400000 + S_3
+    wf = fma(x_3, 2^48, fma(x_2, 2^40, fma(x_1, 2^32, x_0 * 2^24)))   (fp32)
     kb = fp32 bits of fma(wf, fp32(1/q), 1.5 * 2^23) = 0x4B400000 + k,
          k = wf / q rounded to an integer
-    r  = lo - kb*q + (q + 0x4B400000*q - the magic offsets in lo)
+    r  = lo - kb*q + (q + 0x4B400000*q - the magic offset in lo)
          (wrapping 32-bit; equals W - k*q + q, which must lie in [0, 2^32))
     u  = Shoup product r * (2^(8i) mod q), in [0, 2q)
 and the four digit planes i of one output are summed (below 8q) and
@@ -37,15 +38,27 @@ def _f32(x):
 
 MAGIC = 12582912.0          # 1.5 * 2^23
 MAGIC_BITS = 0x4B400000
+SMAGIC = 0.75               # 1.5 * 2^-1
+SMAGIC_BITS = 0x3F400000
 M32 = 0xFFFFFFFF
 
 
-def _magic_bits(x):
-    """fp32 bits of x + 1.5 * 2^23 for integers |x| < 2^22 (then 0x4B400000 + x)."""
-    x = np.asarray(x, dtype=np.int64)
-    assert (np.abs(x) < 1 << 22).all()
-    bits = _f32(x.astype(np.float64) + MAGIC).view(np.uint32).astype(np.int64)
-    assert (bits == MAGIC_BITS + x).all()
+def _scaled(S):
+    """The accumulator value S * 2^-24 as fp32 (exact for |S| < 2^24)."""
+    S = np.asarray(S, dtype=np.int64)
+    assert (np.abs(S) < 1 << 24).all()
+    x = _f32(S.astype(np.float64) / float(1 << 24))
+    assert (x.astype(np.float64) * float(1 << 24) == S).all()
+    return x
+
+
+def _smagic_bits(S):
+    """fp32 bits of S * 2^-24 + 0.75 for integers |S| <= 2^22 (then 0x3F400000 + S)."""
+    S = np.asarray(S, dtype=np.int64)
+    assert (np.abs(S) <= 1 << 22).all()
+    x = _scaled(S)
+    bits = _f32(x.astype(np.float64) + SMAGIC).view(np.uint32).astype(np.int64)
+    assert (bits == SMAGIC_BITS + S).all()
     return bits
 
 
@@ -57,10 +70,14 @@ def epilogue_reduce(S, q, plane=0, strict=True):
     lo = np.zeros(S.shape[:-1], dtype=np.int64)
     wf = np.zeros(S.shape[:-1], dtype=np.float32)
     for j in range(4):
-        t = _magic_bits(S[..., j]) if (j == 3 or plane == 3) else S[..., j] & M32   # else __float2int_rn
+        x = _scaled(S[..., j])
+        if j == 3:
+            t = _smagic_bits(S[..., j])
+        else:   # __float2int_rn(x * 2^24): the product is exact, so the conversion returns S
+            t = np.rint(x.astype(np.float64) * float(1 << 24)).astype(np.int64) & M32
         lo = (lo + (t << (8 * j))) & M32
-        # fmaf(x, 2^(8j), wf): exact product and sum in float64 (< 2^53), one rounding to fp32
-        wf = _f32(S[..., j].astype(np.float64) * float(1 << (8 * j)) + wf.astype(np.float64))
+        # fmaf(x, 2^(8j+24), wf): exact product and sum in float64 (< 2^53), one rounding to fp32
+        wf = _f32(x.astype(np.float64) * float(1 << (8 * j + 24)) + wf.astype(np.float64))
     qinv = np.float32(1.0) / np.float32(q)
     # fmaf(wf, qinv, 1.5 * 2^23): the product is exact in float64 and the result lies in
     # [2^23, 2^24), where fp32 steps by 1, so its one rounding is that of wf*qinv to an integer
@@ -68,7 +85,7 @@ def epilogue_reduce(S, q, plane=0, strict=True):
     k_ok = np.abs(k) < 1 << 22
     assert k_ok.all() or not strict
     kb = MAGIC_BITS + k
-    off = (MAGIC_BITS + (MAGIC_BITS << 8)) & M32 if plane == 3 else (MAGIC_BITS << 24) & M32
+    off = (SMAGIC_BITS << 24) & M32
     rc = (q + MAGIC_BITS * q - off) & M32
     return np.where(k_ok, (lo - kb * q + rc) & M32, -1)
 
@@ -141,15 +158,17 @@ def test_reduction_exact_on_extremes(q):
     assert bad.size == 0, (q, got[bad[:5]], want[bad[:5]])
 
 
-def test_top_digit_plane_fits_the_magic_conversion():
-    """The fp32 magic-constant conversion is exact only below 2^22: the top query
-    digit plane (digits <= 32) against full DB bytes over 512 rows stays below it
-    for every prime below 2^29, the lower planes against the top DB byte too."""
+def test_top_byte_sums_fit_the_magic_conversion():
+    """The fp32 magic-constant conversion (x + 0.75 with ulp 2^-24) is exact only
+    for |S| <= 2^22: every query digit plane against the top DB byte (<= 31 for
+    residues below 2^29) over 512 rows stays below it; the other byte planes reach
+    2^24 and take the exact conversion, and every sum stays below 2^24 (exact
+    accumulators and exact scaling)."""
     q = oracle.primes(4096, 1)[0]
     assert q < 1 << 29
-    assert _bounds(q, 512, 3).max() < 1 << 22
-    assert max(_bounds(q, 512, i)[3] for i in range(3)) < 1 << 22
-    assert _bounds(q, 512, 0)[0] >= 1 << 22          # the lower planes need the exact conversion
+    assert max(_bounds(q, 512, i)[3] for i in range(4)) < 1 << 22
+    assert _bounds(q, 512, 0)[0] >= 1 << 22          # the lower byte planes need the exact conversion
+    assert max(_bounds(q, 512, i).max() for i in range(4)) < 1 << 24
 
 
 def test_reduction_needs_the_prime_bound():
