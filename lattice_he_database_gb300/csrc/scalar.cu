@@ -23,7 +23,9 @@
 //   warp 0      TMA producer: the 128 x 64-byte DB tile (tensor map) and the
 //               matching 256 x 64 fp16 digit tile (1-D bulk copy of a block
 //               pre-swizzled by the prep kernel) into a 4-stage ring;
-//   warp 1      TMEM allocator and the single MMA-issuing thread:
+//   warp 1      TMEM allocator and MMA issue (the warp runs the loop, so
+//               its control flow and operands stay warp-uniform; one elected
+//               lane issues):
 //               4 x tcgen05.mma (M=128, N=256, K=16) per stage into one of
 //               two 256-column fp32 accumulators (double buffered so that a
 //               drain overlaps the next chunk's MMAs);
@@ -56,6 +58,17 @@ constexpr uint32_t SC_U8_BYTES = SC_TM * SC_KB;
 constexpr uint32_t SC_STAGE_BYTES = SC_A_BYTES + SC_B_BYTES + SC_U8_BYTES;
 constexpr int SC_THREADS = 448;
 constexpr uint32_t SC_TMEM_COLS = 512;
+
+// One lane of a fully active warp (the same one every time): true there.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n.reg .pred P;\n"
+        "elect.sync _|P, 0xffffffff;\n"
+        "selp.u32 %0, 1, 0, P;\n}\n"
+        : "=r"(pred));
+    return pred != 0;
+}
 
 // Byte offset of (row, 16-byte chunk j) in a K-major tile with the 128-byte
 // swizzle: rows of 128 B, 8-row groups of 1 KiB, chunk index XOR (row % 8).
@@ -235,36 +248,41 @@ __global__ void __launch_bounds__(SC_THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            bool ab = false;
-            uint32_t g = 0, s = 0, ph = 0;
-            const uint64_t ad0 = sdesc_sw128(smem_u32(stA)), bd0 = sdesc_sw128(smem_u32(stB));
-            for (uint32_t t = blockIdx.x; t < A.ntiles; t += gridDim.x) {
-                ab = ab || abort_flag;
-                for (uint32_t ch = 0; ch < nchunks; ++ch, ++g) {
-                    const uint32_t buf = g & 1, use = (g >> 1) & 1;
-                    if (!ab && !mbar_wait(acce + buf, use ^ 1, A.status)) ab = true;
-                    const uint32_t d = tmem + buf * SC_N;
-                    const uint32_t kb0 = ch * SC_CHUNK_STAGES, kb_end = min(A.nkb, kb0 + SC_CHUNK_STAGES);
-                    for (uint32_t kb = kb0; kb < kb_end; ++kb) {
-                        if (!ab && !mbar_wait(conv + s, ph, A.status)) ab = true;
-                        if (!ab) {
-                            tc_fence_after();
+        // The whole warp runs the loop (control flow and operands warp-uniform);
+        // one elected lane issues the MMAs and commits.
+        bool ab = false;
+        uint32_t g = 0, s = 0, ph = 0;
+        const uint64_t ad0 = sdesc_sw128(smem_u32(stA)), bd0 = sdesc_sw128(smem_u32(stB));
+        for (uint32_t t = blockIdx.x; t < A.ntiles; t += gridDim.x) {
+            ab = __any_sync(0xffffffffu, ab || abort_flag);
+            for (uint32_t ch = 0; ch < nchunks; ++ch, ++g) {
+                const uint32_t buf = g & 1, use = (g >> 1) & 1;
+                ab = __any_sync(0xffffffffu, ab || !mbar_wait(acce + buf, use ^ 1, A.status));
+                const uint32_t d = tmem + buf * SC_N;
+                const uint32_t kb0 = ch * SC_CHUNK_STAGES, kb_end = min(A.nkb, kb0 + SC_CHUNK_STAGES);
+                for (uint32_t kb = kb0; kb < kb_end; ++kb) {
+                    ab = __any_sync(0xffffffffu, ab || !mbar_wait(conv + s, ph, A.status));
+                    if (!ab) {
+                        tc_fence_after();
+                        if (elect_one()) {
                             mma4(d, ad0 + s * (SC_A_BYTES >> 4), bd0 + s * (SC_B_BYTES >> 4), kb > kb0);
                             mma_commit(empty + s);        // stage reusable once these MMAs finish
                         }
-                        if (++s == SC_NS) {
-                            s = 0;
-                            ph ^= 1;
-                        }
+                        __syncwarp();
                     }
-                    if (!ab) mma_commit(accf + buf);  // chunk complete -> epilogue
+                    if (++s == SC_NS) {
+                        s = 0;
+                        ph ^= 1;
+                    }
                 }
+                if (!ab && elect_one()) mma_commit(accf + buf);  // chunk complete -> epilogue
+                __syncwarp();
             }
-            if (ab) abort_flag = 1;
-            mma_commit(done);
-            mbar_wait(done, 0, A.status);
         }
+        if (lane == 0 && ab) abort_flag = 1;
+        if (elect_one()) mma_commit(done);
+        __syncwarp();
+        mbar_wait(done, 0, A.status);
 
     } else if (warp < 10) {
         // ------------------------------------------------ converters: bytes -> fp16, swizzled
