@@ -60,6 +60,7 @@ __device__ __forceinline__ uint64_t even_ct(uint64_t g, uint64_t Rp, uint64_t n,
 
 // d_i = ct_2i+1 - ct_2i mod q_l, four words per thread.
 __global__ void __launch_bounds__(CT_THREADS) coltor_diff_kernel(const DiffArgs A) {
+    pdl_wait();
     const uint64_t ct_words = 2ull * A.L * A.N;          // one ciphertext
     const uint64_t total4 = A.R * ct_words / 4;
     for (uint64_t v = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; v < total4;
@@ -95,6 +96,7 @@ struct DiffInttArgs {
 // ct_2i+1 - ct_2i + q (in (0, 2q), the inverse butterflies' input range)
 // instead of a stored difference.  Rounds as in the library's inverse.
 __global__ void __launch_bounds__(kT4) coltor_diff_intt4096_kernel(const __grid_constant__ DiffInttArgs A) {
+    pdl_wait();
     __shared__ __align__(16) uint32_t sa[kN4];
     __shared__ __align__(16) uint32_t sb[kN4];
     const uint64_t i = blockIdx.x / A.L;
@@ -141,6 +143,7 @@ __device__ __forceinline__ uint32_t mac_final(uint64_t acc, uint32_t e, uint32_t
 }
 
 __global__ void __launch_bounds__(CT_THREADS) coltor_mac_kernel(const MacArgs A) {
+    pdl_wait();
     const uint64_t LN = (uint64_t)A.L * A.N;
     const uint64_t total4 = A.R * LN / 4;
     const uint32_t V = 2 * A.ell;
@@ -245,10 +248,10 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint64_t c_stride, uint32_t ell, uint
             ia.ninv_shoup[l] = ctx->ninv_shoup[l];
         }
         if (R * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
-        coltor_diff_intt4096_kernel<<<(unsigned)(R * ctx->L), kT4, 0, st>>>(ia);
+        pdl_launch(coltor_diff_intt4096_kernel, dim3((unsigned)(R * ctx->L)), dim3(kT4), 0, st, ia);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
     } else {
-        coltor_diff_kernel<<<(unsigned)grid_for(ctx, R * 2 * LN / 4), CT_THREADS, 0, st>>>(da);
+        pdl_launch(coltor_diff_kernel, dim3((unsigned)grid_for(ctx, R * 2 * LN / 4)), dim3(CT_THREADS), 0, st, da);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
         rc = pir_ntt_inv(ctx, diff, diff, R * 2, st);
         if (rc) return rc;
@@ -277,7 +280,7 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint64_t c_stride, uint32_t ell, uint
         ma.q[l] = ctx->q[l];
         ma.mu[l] = ctx->mu[l];
     }
-    coltor_mac_kernel<<<(unsigned)grid_for(ctx, R * LN / 4), CT_THREADS, 0, st>>>(ma);
+    pdl_launch(coltor_mac_kernel, dim3((unsigned)grid_for(ctx, R * LN / 4)), dim3(CT_THREADS), 0, st, ma);
     return launch_status(cudaGetLastError());
 }
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "pir.h"
@@ -50,6 +51,34 @@ int launch_status(cudaError_t e);  // maps a CUDA error to PIR_OK / PIR_ERR_CUDA
 
 // Lift + forward NTT of cnt rows of gadget digits below 2^w (ntt.cu).
 int lift_ntt_digits(pir_ctx *ctx, const uint32_t *raw, uint32_t *out, uint64_t cnt, uint32_t w, void *stream);
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel started by pdl_launch may be launched before the previous kernel
+// of its stream has finished flushing its memory: the next grid's launch
+// overlaps the previous grid's completion, which shortens chains of
+// dependent kernels (ColTor and ExpandQuery run ~40 a call).  Such kernels
+// call pdl_wait() before touching global memory; it returns once the
+// previous kernel has completed and its memory operations are visible (and
+// at once for an ordinary launch).  The kernels do not trigger their
+// dependents early (griddepcontrol.launch_dependents at entry let waiting
+// CTAs take SM slots from the previous kernel's last waves: slower in CUDA
+// graphs), so the trigger is the implicit one at completion.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t pdl_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- modular helpers
 // Shoup product: w * y mod q in [0, 2q) for y < 2^32, w < q < 2^31,

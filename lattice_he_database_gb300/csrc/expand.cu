@@ -59,6 +59,7 @@ struct InttAArgs {
 // N = 4096: one CTA per (ciphertexts 2i' and 2i'+1, prime l) transforms
 // both c1 rows with shared twiddles; rounds as in the library's inverse.
 __global__ void __launch_bounds__(kT4) expand_intt_a4096_kernel(const __grid_constant__ InttAArgs A) {
+    pdl_wait();
     __shared__ __align__(16) uint32_t sa[kN4];
     __shared__ __align__(16) uint32_t sb[kN4];
     const uint64_t i0 = 2 * (blockIdx.x / A.L), i1 = i0 + 1;
@@ -109,6 +110,7 @@ __device__ __forceinline__ uint32_t subq(uint32_t a, uint32_t b, uint32_t q) {
 // Four consecutive slots per thread.  The ell <= 16 key-switch products of
 // residues below 2^29 sum below 2^62 without reduction.
 __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs A) {
+    pdl_wait();
     const uint64_t LN = (uint64_t)A.L * A.N;
     const uint64_t total4 = A.GM * LN / 4;
     const uint32_t twoN = 2 * A.N;
@@ -180,6 +182,7 @@ struct RgswMacArgs {
 // Four consecutive slots per thread: input ciphertext i = (RGSW r, row u)
 // goes to row u of RGSW r unchanged and, key-switched, to row ell + u.
 __global__ void __launch_bounds__(GD_THREADS) rgsw_mac_kernel(const RgswMacArgs A) {
+    pdl_wait();
     const uint64_t LN = (uint64_t)A.L * A.N;
     const uint64_t total4 = A.M * LN / 4;
     for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total4;
@@ -268,7 +271,7 @@ int c1_to_coef(pir_ctx *ctx, const uint32_t *in, uint64_t GM, uint32_t *coef, cu
         ia.M = GM;
         ia.per = per;
         ia.stride = stride;
-        expand_intt_a4096_kernel<<<(unsigned)((GM + 1) / 2 * ctx->L), kT4, 0, st>>>(ia);
+        pdl_launch(expand_intt_a4096_kernel, dim3((unsigned)((GM + 1) / 2 * ctx->L)), dim3(kT4), 0, st, ia);
         return cudaGetLastError() == cudaSuccess ? PIR_OK : PIR_ERR_CUDA;
     }
     for (uint64_t b = 0; b < GM / per; ++b)   // one strided copy of the c1 rows per block of `per`
@@ -316,7 +319,7 @@ int one_stage(pir_ctx *ctx, const uint32_t *evk, uint64_t evk_stride, uint32_t e
         ma.q[l] = ctx->q[l];
         ma.mu[l] = ctx->mu[l];
     }
-    expand_mac_kernel<<<(unsigned)gadget_grid(ctx, GM * LN / 4), GD_THREADS, 0, st>>>(ma);
+    pdl_launch(expand_mac_kernel, dim3((unsigned)gadget_grid(ctx, GM * LN / 4)), dim3(GD_THREADS), 0, st, ma);
     return launch_status(cudaGetLastError());
 }
 
@@ -458,6 +461,6 @@ extern "C" int pir_rgsw_convert(pir_ctx *ctx, const uint32_t *ksk, uint32_t ell,
         ma.q[l] = ctx->q[l];
         ma.mu[l] = ctx->mu[l];
     }
-    rgsw_mac_kernel<<<(unsigned)gadget_grid(ctx, M * LN / 4), GD_THREADS, 0, st>>>(ma);
+    pdl_launch(rgsw_mac_kernel, dim3((unsigned)gadget_grid(ctx, M * LN / 4)), dim3(GD_THREADS), 0, st, ma);
     return launch_status(cudaGetLastError());
 }

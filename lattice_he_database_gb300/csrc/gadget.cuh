@@ -62,6 +62,7 @@ __device__ __forceinline__ u128 crt_value(const DcpArgs &A, const uint32_t (&r)[
 
 // One thread per four consecutive output coefficients.
 __global__ void __launch_bounds__(GD_THREADS) gadget_dcp_kernel(const DcpArgs A) {
+    pdl_wait();
     const uint64_t total4 = A.polys * A.N / 4;
     const u128 Q = ((u128)A.Q_hi << 64) | A.Q_lo;
     const u128 mask = A.w >= 32 ? (u128)0xffffffffu : (((u128)1 << A.w) - 1);
@@ -177,7 +178,7 @@ uint64_t gadget_grid(const pir_ctx *ctx, uint64_t work) {
 }
 
 int gadget_dcp_launch(const pir_ctx *ctx, const DcpArgs &A, cudaStream_t st) {
-    gadget_dcp_kernel<<<(unsigned)gadget_grid(ctx, A.polys * A.N / 4), GD_THREADS, 0, st>>>(A);
+    pdl_launch(gadget_dcp_kernel, dim3((unsigned)gadget_grid(ctx, A.polys * A.N / 4)), dim3(GD_THREADS), 0, st, A);
     return cudaGetLastError() == cudaSuccess ? PIR_OK : PIR_ERR_CUDA;
 }
 

@@ -26,6 +26,7 @@ template <bool FWD, bool LIFT>
 __global__ void __launch_bounds__(kNttThreads) ntt_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                           uint64_t rows, uint32_t rpc,
                                                           const __grid_constant__ RnsParams P) {
+    pdl_wait();
     extern __shared__ __align__(16) uint32_t sm[];
     __shared__ uint8_t row_prime[kMaxRowsPerCta];
     const uint32_t N = P.N, L = P.L, logN = P.logN;
@@ -70,6 +71,7 @@ __global__ void __launch_bounds__(kNttThreads) ntt_kernel(const uint32_t *__rest
 template <bool FWD, bool LIFT>
 __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                       const __grid_constant__ RnsParams P) {
+    pdl_wait();
     static_assert(FWD || !LIFT, "the lift feeds the forward transform only");
     __shared__ __align__(16) uint32_t sm[kN4];
     const uint64_t row = blockIdx.x;
@@ -145,6 +147,7 @@ __global__ void __launch_bounds__(kT4) ntt4096_kernel(const uint32_t *__restrict
 template <bool LIFT, bool SMALL = false>
 __global__ void __launch_bounds__(kT4, 4) ntt4096x2_fwd_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                             uint64_t cnt, const __grid_constant__ RnsParams P) {
+    pdl_wait();
     __shared__ __align__(16) uint32_t sa[kN4];
     __shared__ __align__(16) uint32_t sb[kN4];
     // Prime-major CTA order: the CTAs resident on an SM at a time transform
@@ -210,6 +213,7 @@ __global__ void __launch_bounds__(kT4, 4) ntt4096x2_fwd_kernel(const uint32_t *_
 // Inverse for N = 4096 on two rows of one prime per CTA (as the forward).
 __global__ void __launch_bounds__(kT4, 4) ntt4096x2_inv_kernel(const uint32_t *__restrict__ in, uint32_t *out,
                                                             uint64_t cnt, const __grid_constant__ RnsParams P) {
+    pdl_wait();
     __shared__ __align__(16) uint32_t sa[kN4];
     __shared__ __align__(16) uint32_t sb[kN4];
     const uint64_t pp = blockIdx.x / P.L;
@@ -254,17 +258,19 @@ int ntt_launch(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, vo
             const uint64_t g2 = (cnt + 1) / 2 * ctx->L;
             if (g2 > 0x7fffffffull) return PIR_ERR_ARG;
             if (FWD)
-                ntt4096x2_fwd_kernel<LIFT, SMALL><<<(unsigned)g2, kT4, 0, (cudaStream_t)stream>>>(in, out, cnt,
-                                                                                         rns_params(ctx));
+                pdl_launch(ntt4096x2_fwd_kernel<LIFT, SMALL>, dim3((unsigned)g2), dim3(kT4), 0, (cudaStream_t)stream, in,
+                           out, cnt, rns_params(ctx));
             else
-                ntt4096x2_inv_kernel<<<(unsigned)g2, kT4, 0, (cudaStream_t)stream>>>(in, out, cnt, rns_params(ctx));
+                pdl_launch(ntt4096x2_inv_kernel, dim3((unsigned)g2), dim3(kT4), 0, (cudaStream_t)stream, in, out, cnt,
+                           rns_params(ctx));
         } else {
-            ntt4096_kernel<FWD, LIFT><<<(unsigned)rows, kT4, 0, (cudaStream_t)stream>>>(in, out, rns_params(ctx));
+            pdl_launch(ntt4096_kernel<FWD, LIFT>, dim3((unsigned)rows), dim3(kT4), 0, (cudaStream_t)stream, in, out,
+                       rns_params(ctx));
         }
         return launch_status(cudaGetLastError());
     }
-    ntt_kernel<FWD, LIFT><<<(unsigned)grid, kNttThreads, smem, (cudaStream_t)stream>>>(in, out, rows, rpc,
-                                                                                        rns_params(ctx));
+    pdl_launch(ntt_kernel<FWD, LIFT>, dim3((unsigned)grid), dim3(kNttThreads), smem, (cudaStream_t)stream, in, out,
+               rows, rpc, rns_params(ctx));
     return launch_status(cudaGetLastError());
 }
 
