@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(256) transpose_query_kernel(const uint32_t *__
                                                               uint32_t D0, uint32_t Mp, uint32_t Mv,
                                                               uint32_t b0, uint32_t PS) {
     __shared__ uint32_t tile[TT][TPITCH];   // [r][p]
+    pdl_wait();
     const uint64_t p0 = (uint64_t)blockIdx.x * TT;
     const uint32_t r0 = blockIdx.y * TT;
     const uint32_t rows = D0 * Mp;
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(256) transpose_out_kernel(const uint32_t *__re
                                                             uint32_t D1p, uint32_t Mv, uint32_t b0,
                                                             const __grid_constant__ AddendArgs add) {
     __shared__ uint32_t tile[TT][TPITCH];   // [w][p]
+    pdl_wait();
     const uint64_t p0 = (uint64_t)blockIdx.x * TT;
     const uint32_t w0 = blockIdx.y * TT;
     const uint32_t W = Mv * D1p;
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(NTHREADS) rowsel_kernel(const __grid_constant_
     if (A.ksplit > 1)   // the partial-sum rows start at zero; each unit's reader clears what it read
         for (uint32_t i = threadIdx.x; i < A.Mp * PIR_SLAB; i += blockDim.x) red[i] = 0;
     __syncthreads();
+    pdl_wait();   // the set-up above touches no global memory
 
     // ------------------------------------------------------------ producer
     if (warp == NWC) {
@@ -413,7 +416,7 @@ int launch_pass(pir_ctx *ctx, RowselArgs &A, cudaStream_t st) {
         return PIR_ERR_CUDA;
     const uint64_t cap = (uint64_t)ctx->num_sms * per_sm;
     const uint64_t grid = A.units < cap ? A.units : cap;
-    rowsel_kernel<MT><<<(unsigned)grid, NTHREADS, smem, st>>>(A);
+    pdl_launch(rowsel_kernel<MT>, dim3((unsigned)grid), dim3(NTHREADS), smem, st, A);
     return launch_status(cudaGetLastError());
 }
 
@@ -537,7 +540,7 @@ int rowsel_impl(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, cons
         // the pass's query slices, point-major
         const dim3 tgrid((unsigned)((A.P + TT - 1) / TT), (A.PS + TT - 1) / TT);
         uint32_t *qT = reinterpret_cast<uint32_t *>(workspace);
-        transpose_query_kernel<<<tgrid, 256, 0, st>>>(query, qT, A.P, D0, A.Mp, A.Mv, b0, A.PS);
+        pdl_launch(transpose_query_kernel, tgrid, dim3(256), 0, st, query, qT, A.P, D0, A.Mp, A.Mv, b0, A.PS);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
         int rc = PIR_OK;
         if (tc && nb > 8) {  // 17..32 polynomials, q >= 2^26: exact fp16 tensor-core GEMMs
@@ -565,7 +568,8 @@ int rowsel_impl(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, cons
         add.N = ctx->N;
         for (uint32_t l = 0; l < ctx->L; ++l) add.q[l] = ctx->q[l];
         const dim3 ogrid((unsigned)((A.P + TT - 1) / TT), (A.Mv * A.D1p + TT - 1) / TT);
-        transpose_out_kernel<<<ogrid, 256, 0, st>>>(A.outT, out, A.P, D1, A.D1p, A.Mv, b0, add);
+        pdl_launch(transpose_out_kernel, ogrid, dim3(256), 0, st, (const uint32_t *)A.outT, out, A.P, D1, A.D1p, A.Mv, b0,
+                   add);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
     }
     return PIR_OK;

@@ -336,6 +336,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();   // the set-up above touches no global memory
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer: query slices and DB word tiles
@@ -732,6 +733,6 @@ int rowsel_tc_pass(pir_ctx *ctx, const uint32_t *db, uint32_t D0, uint32_t D1, c
         attr_set[ctx->device] = true;
     }
     const uint64_t grid = P < (uint64_t)ctx->num_sms ? P : (uint64_t)ctx->num_sms;
-    rowsel_tc_kernel<<<(unsigned)grid, TC_THREADS, smem, st>>>(full_map, last_map, a);
+    pdl_launch(rowsel_tc_kernel, dim3((unsigned)grid), dim3(TC_THREADS), smem, st, full_map, last_map, a);
     return launch_status(cudaGetLastError());
 }

@@ -82,6 +82,7 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
 __global__ void __launch_bounds__(256) digits_kernel(const uint32_t *__restrict__ Q, uint32_t C, uint32_t B,
                                                      uint8_t *__restrict__ ws) {
     __shared__ uint32_t tile[64][SC_BQ + 1];
+    pdl_wait();
     const uint32_t kb = blockIdx.x;
     for (uint32_t i = threadIdx.x; i < 64 * SC_BQ; i += blockDim.x) {
         const uint32_t k = i / SC_BQ, b = i % SC_BQ;
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();   // the set-up above touches no global memory
     const uint32_t nchunks = (A.nkb + SC_CHUNK_STAGES - 1) / SC_CHUNK_STAGES;
 
     if (warp == 0) {
@@ -423,6 +425,7 @@ constexpr uint32_t GV_MAX_B = 4;
 __global__ void __launch_bounds__(256) gemv_prep_kernel(const uint32_t *__restrict__ Q, uint64_t C, uint32_t B,
                                                         uint32_t nkb, uint32_t *__restrict__ planes,
                                                         uint32_t *__restrict__ out, uint64_t out_words) {
+    pdl_wait();
     const uint64_t tid = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
     const uint64_t nthr = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t groups = (uint64_t)nkb * B * (GV_KB / 4);   // (box, query, group of 4 columns)
@@ -476,6 +479,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();   // the set-up above touches no global memory
     const uint64_t u0 = A.units * blockIdx.x / gridDim.x, u1 = A.units * (blockIdx.x + 1) / gridDim.x;
 
     if (warp == GV_RT / 32) {
@@ -593,7 +597,7 @@ int gemv_launch(pir_ctx *ctx, const CUtensorMap &map, const GemvArgs &a, cudaStr
         attr_set[ctx->device] = true;
     }
     const uint64_t grid = a.units < (uint64_t)ctx->num_sms ? a.units : (uint64_t)ctx->num_sms;
-    gemv_kernel<NB><<<(unsigned)grid, GV_THREADS, smem, st>>>(map, a);
+    pdl_launch(gemv_kernel<NB>, dim3((unsigned)grid), dim3(GV_THREADS), smem, st, map, a);
     return launch_status(cudaGetLastError());
 }
 
@@ -616,7 +620,8 @@ int scalar_gemv(pir_ctx *ctx, PFN_cuTensorMapEncodeTiled_v12000 encode, const ui
     uint32_t *planes = reinterpret_cast<uint32_t *>(workspace);
     const uint64_t work = (uint64_t)nkb * B * (GV_KB / 4);
     const uint64_t prep_blocks = (work + 255) / 256 < 4096 ? (work + 255) / 256 : 4096;
-    gemv_prep_kernel<<<(unsigned)(prep_blocks ? prep_blocks : 1), 256, 0, st>>>(Q, C, B, nkb, planes, out, R * B);
+    pdl_launch(gemv_prep_kernel, dim3((unsigned)(prep_blocks ? prep_blocks : 1)), dim3(256), 0, st, Q, C, B, nkb, planes,
+               out, R * B);
     if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
     GemvArgs a;
     a.planes = reinterpret_cast<const uint8_t *>(workspace);
@@ -667,7 +672,7 @@ extern "C" int pir_scalar_scan(pir_ctx *ctx, const uint8_t *db, uint64_t R, uint
 
     cudaStream_t st = (cudaStream_t)stream;
     const uint32_t nkb = (uint32_t)(C / SC_KB);
-    digits_kernel<<<nkb, 256, 0, st>>>(Q, (uint32_t)C, B, reinterpret_cast<uint8_t *>(workspace));
+    pdl_launch(digits_kernel, dim3(nkb), dim3(256), 0, st, Q, (uint32_t)C, B, reinterpret_cast<uint8_t *>(workspace));
     if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
 
     const size_t smem = scalar_smem_bytes();
@@ -688,7 +693,7 @@ extern "C" int pir_scalar_scan(pir_ctx *ctx, const uint8_t *db, uint64_t R, uint
     a.ntiles = (uint32_t)((R + SC_TM - 1) / SC_TM);
     a.nkb = nkb;
     const uint32_t grid = a.ntiles < (uint32_t)ctx->num_sms ? a.ntiles : (uint32_t)ctx->num_sms;
-    scalar_kernel<<<grid, SC_THREADS, smem, st>>>(map, a);
+    pdl_launch(scalar_kernel, grid, dim3(SC_THREADS), smem, st, map, a);
     return launch_status(cudaGetLastError());
 }
 
