@@ -49,6 +49,8 @@ def _small_case(pir, N, L, D0, D1, B, seed):
     (16, 2, 1536, 40, 12),   # tensor-core path, three full K segments
     (16, 1, 600, 130, 17),   # two passes: tensor cores (512 + 88 rows, 2 slabs), then 1 query on CUDA cores
     (16, 2, 513, 9, 9),      # tensor-core path, second segment of a single row
+    (16, 2, 130, 200, 16),   # tensor-core path, last slab of 72 columns: a full and a ragged 64-column tile
+    (16, 2, 64, 100, 10),    # tensor-core path, one 100-column slab (64 + 36), 20 of 32 polynomials
 ])
 def test_encode_and_rowsel_small(pir, N, L, D0, D1, B):
     ctx, qs, psis, raw, db_t, query = _small_case(pir, N, L, D0, D1, B, seed=(N + D0 + D1 + B) % 251)
