@@ -1,7 +1,7 @@
 """GPU parity: the scalar-HE scan (byte DB x 32-bit query words mod 2^32).
 
 Bit-exact against the oracle on small shapes (ragged row tiles, partial
-accumulator chunks, B < 64), on adversarial values that put every partial
+accumulator chunks, B < 64, more row tiles than SMs), on adversarial values that put every partial
 sum of the fp16/fp32 tensor-core path at its largest magnitude, on the
 CUDA-core GEMV used for B <= 4 (ragged tiles and boxes, row tiles split
 between CTAs, wrapping byte-plane sums), and on sampled rows of the full
@@ -45,6 +45,8 @@ def _run(pir, ctx, db, Q):
     (300, 640, 64),      # ragged last tile (rows zero-filled by TMA)
     (128, 1024, 5),      # B < 64
     (257, 192, 1),       # B = 1, ragged
+    (64, 8192, 64),      # one ragged row tile over 16 accumulator chunks
+    (20000, 1088, 33),   # more row tiles than SMs (a second, partial wave), B < 64
 ])
 def test_scalar_scan_small(env, R, C, B):
     pir, ctx = env
