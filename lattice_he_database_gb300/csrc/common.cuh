@@ -19,6 +19,7 @@ struct pir_ctx {
     uint32_t r32[PIR_MAX_RNS];         // 2^32 mod q
     uint64_t mu[PIR_MAX_RNS];          // floor(2^64 / q)
     uint32_t *d_tw;                    // device twiddles [L][4][N]
+    uint32_t *d_xpow;                  // device [logN][L][N]: NTT(X^(-2^j)) mod q_l, slot order (ExpandQuery)
     uint32_t *d_status;                // device status word
     uint64_t wait_limit_ns;            // limit of the kernels' ordinary waits (pir_ctx_set_wait_limit)
     uint32_t test_hook;                // PIR_HOOK_* (pir_ctx_set_test_hook); PIR_HOOK_NONE in normal use

@@ -133,6 +133,10 @@ extern "C" int pir_ctx_create(pir_ctx **out, uint32_t N, uint32_t L, const uint3
     while ((1u << c->logN) < N) ++c->logN;
 
     std::vector<uint32_t> tw((size_t)L * 4 * N);   // [L][2][N] pairs {w, shoup(w)}
+    // NTT(X^(-2^j)) for every expansion stage j < logN: slot s holds the value
+    // at psi^(2 brv(s) + 1), i.e. psi^(-E) with E = 2^j (2 brv(s) + 1) mod 2N.
+    std::vector<uint32_t> xpow((size_t)c->logN * L * N);
+    std::vector<uint32_t> pinv((size_t)2 * N);
     for (uint32_t l = 0; l < L; ++l) {
         uint32_t ql = q[l];
         c->q[l] = ql;
@@ -154,16 +158,31 @@ extern "C" int pir_ctx_create(pir_ctx **out, uint32_t N, uint32_t L, const uint3
             I[2 * i] = wi;
             I[2 * i + 1] = shoup_of(wi, ql);
         }
+        pinv[0] = 1;
+        for (uint32_t e = 1; e < 2 * N; ++e) pinv[e] = (uint32_t)((uint64_t)pinv[e - 1] * psi_inv % ql);
+        for (uint32_t j = 0; j < c->logN; ++j)
+            for (uint32_t s = 0; s < N; ++s) {
+                const uint32_t E = (uint32_t)(((uint64_t)(2 * bit_reverse(s, c->logN) + 1) << j) & (2 * N - 1));
+                xpow[((size_t)j * L + l) * N + s] = pinv[E];
+            }
     }
     if (cudaMalloc(&c->d_tw, tw.size() * sizeof(uint32_t)) != cudaSuccess) { free(c); return PIR_ERR_ALLOC; }
-    if (cudaMalloc(&c->d_status, 256) != cudaSuccess) {
+    if (cudaMalloc(&c->d_xpow, xpow.size() * sizeof(uint32_t)) != cudaSuccess) {
         cudaFree(c->d_tw);
         free(c);
         return PIR_ERR_ALLOC;
     }
+    if (cudaMalloc(&c->d_status, 256) != cudaSuccess) {
+        cudaFree(c->d_tw);
+        cudaFree(c->d_xpow);
+        free(c);
+        return PIR_ERR_ALLOC;
+    }
     if (cudaMemcpy(c->d_tw, tw.data(), tw.size() * sizeof(uint32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(c->d_xpow, xpow.data(), xpow.size() * sizeof(uint32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemset(c->d_status, 0, 256) != cudaSuccess) {
         cudaFree(c->d_tw);
+        cudaFree(c->d_xpow);
         cudaFree(c->d_status);
         free(c);
         return PIR_ERR_CUDA;
@@ -179,6 +198,7 @@ extern "C" void pir_ctx_destroy(pir_ctx *ctx) {
     cudaSetDevice(ctx->device);
     cudaDeviceSynchronize();
     cudaFree(ctx->d_tw);
+    cudaFree(ctx->d_xpow);
     cudaFree(ctx->d_status);
     cudaSetDevice(prev);
     free(ctx);

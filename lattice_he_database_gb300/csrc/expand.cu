@@ -88,9 +88,9 @@ struct ExpMacArgs {
     const uint32_t *dn;     // [G][M][ell][L][N] NTT of the digits of sigma_k(c1)
     const uint32_t *evk;    // client b's stage key [ell][2][L][N] at evk + b * evk_stride
     uint32_t *out;          // [G][2M][2][L][N]
-    const uint32_t *tw;     // [L][4][N]
+    const uint32_t *xpow;   // the stage's NTT(X^(-2^j)), [L][N]
     uint64_t M, GM, evk_stride;
-    uint32_t N, logN, L, ell, k, j;
+    uint32_t N, logN, L, ell, k;
     uint32_t q[PIR_MAX_RNS];
     uint64_t mu[PIR_MAX_RNS];
 };
@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
         const uint64_t ks0[4] = {a0, a1, a2, a3}, ks1[4] = {b0, b1, b2, b3};
         const uint32_t *c0 = A.in + i * 2 * LN + (uint64_t)l * A.N;
         const uint32_t *c1 = c0 + LN;
-        const uint2 *Tinv = tw_pairs(A.tw, l, A.N, TW_INV);   // .x: psi^-brv(i)
+        const uint4 xm = __ldg(reinterpret_cast<const uint4 *>(A.xpow + pt));   // NTT(X^(-2^j)) at the 4 slots
+        const uint32_t xmv[4] = {xm.x, xm.y, xm.z, xm.w};
         const uint4 v0 = *reinterpret_cast<const uint4 *>(c0 + s0);
         const uint4 v1 = *reinterpret_cast<const uint4 *>(c1 + s0);
         const uint32_t x0[4] = {v0.x, v0.y, v0.z, v0.w}, x1[4] = {v1.x, v1.y, v1.z, v1.w};
@@ -151,9 +152,7 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
             const uint32_t src = brv((ek - 1) >> 1, A.logN);
             const uint32_t S0 = addq(c0[src], barrett64(ks0[c], q, mu), q);
             const uint32_t S1 = barrett64(ks1[c], q, mu);
-            // NTT(X^(-2^j)) at this slot: psi^(-E), E = 2^j (2 brv(slot) + 1) mod 2N
-            const uint32_t E = (odd << A.j) & (twoN - 1);
-            const uint32_t m = E < A.N ? Tinv[brv(E, A.logN)].x : q - Tinv[brv(E - A.N, A.logN)].x;
+            const uint32_t m = xmv[c];
             o0[c] = addq(x0[c], S0, q);
             o1[c] = addq(x1[c], S1, q);
             p0[c] = barrett64((uint64_t)subq(x0[c], S0, q) * m, q, mu);
@@ -305,7 +304,7 @@ int one_stage(pir_ctx *ctx, const uint32_t *evk, uint64_t evk_stride, uint32_t e
     ma.dn = dn;
     ma.evk = evk;
     ma.out = out;
-    ma.tw = ctx->d_tw;
+    ma.xpow = ctx->d_xpow + (size_t)j * ctx->L * ctx->N;
     ma.M = M;
     ma.GM = GM;
     ma.evk_stride = evk_stride;
@@ -314,7 +313,6 @@ int one_stage(pir_ctx *ctx, const uint32_t *evk, uint64_t evk_stride, uint32_t e
     ma.L = ctx->L;
     ma.ell = ell;
     ma.k = k;
-    ma.j = j;
     for (uint32_t l = 0; l < ctx->L; ++l) {
         ma.q[l] = ctx->q[l];
         ma.mu[l] = ctx->mu[l];
