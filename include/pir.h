@@ -20,7 +20,8 @@
  *  - All buffers are owned and allocated by the caller; pointers marked
  *    "device" must be device memory of the context's GPU, 16-byte aligned.
  *    The library allocates device memory only in pir_ctx_create (its
- *    twiddle tables and a status word) and frees it in pir_ctx_destroy.
+ *    twiddle tables, the expansion stages' monomial factors and a status
+ *    word) and frees it in pir_ctx_destroy.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and returns before it completes.  Inputs must stay valid and
  *    unmodified until the stream reaches the work.
@@ -80,7 +81,9 @@ int pir_primes(uint32_t N, uint32_t L, uint32_t *q);
  * pir_ctx_create — build a context for ring degree N and RNS primes q[0..L)
  * on CUDA device `device`: validates the parameters (as pir_params_check),
  * selects for each q_i the smallest primitive 2N-th root of unity psi_i, and
- * uploads its twiddle tables.  *out receives the context (NULL on error).
+ * uploads its twiddle tables and, for ExpandQuery, NTT(X^(-2^j)) for every
+ * stage j < log2 N (log2 N * L * N words).  *out receives the context (NULL
+ * on error).
  * Errors: PIR_ERR_ARG, PIR_ERR_CUDA, PIR_ERR_ALLOC.
  */
 int pir_ctx_create(pir_ctx **out, uint32_t N, uint32_t L, const uint32_t *q, int device);
