@@ -147,6 +147,9 @@ __global__ void __launch_bounds__(CT_THREADS) coltor_mac_kernel(const MacArgs A)
     const uint64_t LN = (uint64_t)A.L * A.N;
     const uint64_t total4 = A.R * LN / 4;
     const uint32_t V = 2 * A.ell;
+    // the digit transforms are read exactly once: let them leave L2 first, so
+    // that the RGSW rows and the next stage's inputs stay (2% per tournament)
+    const uint64_t pol_first = policy_evict_first();
     for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total4;
          e += (uint64_t)gridDim.x * blockDim.x) {
         const uint64_t e0 = e * 4;
@@ -159,7 +162,7 @@ __global__ void __launch_bounds__(CT_THREADS) coltor_mac_kernel(const MacArgs A)
         uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
 #pragma unroll 4
         for (uint32_t v = 0; v < V; ++v) {
-            const uint4 d = *reinterpret_cast<const uint4 *>(dp + (uint64_t)v * LN);
+            const uint4 d = ld_policy(dp + (uint64_t)v * LN, pol_first);
             const uint4 c0 = __ldg(reinterpret_cast<const uint4 *>(cp + (uint64_t)(2 * v) * LN));
             const uint4 c1 = __ldg(reinterpret_cast<const uint4 *>(cp + (uint64_t)(2 * v + 1) * LN));
             a0 += (uint64_t)d.x * c0.x; a1 += (uint64_t)d.y * c0.y; a2 += (uint64_t)d.z * c0.z; a3 += (uint64_t)d.w * c0.w;

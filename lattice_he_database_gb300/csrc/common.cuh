@@ -182,6 +182,16 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// 16-byte global load with an L2 eviction-priority policy (createpolicy);
+// for data the kernel only reads.
+__device__ __forceinline__ uint4 ld_policy(const void *p, uint64_t policy) {
+    uint4 v;
+    asm("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p), "l"(policy));
+    return v;
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,

@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
     const uint64_t LN = (uint64_t)A.L * A.N;
     const uint64_t total4 = A.GM * LN / 4;
     const uint32_t twoN = 2 * A.N;
+    const uint64_t pol_first = policy_evict_first();   // the digit transforms are read once
     for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total4;
          e += (uint64_t)gridDim.x * blockDim.x) {
         const uint64_t e0 = e * 4;
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
         uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
 #pragma unroll 4
         for (uint32_t u = 0; u < A.ell; ++u) {
-            const uint4 d = *reinterpret_cast<const uint4 *>(dp + (uint64_t)u * LN);
+            const uint4 d = ld_policy(dp + (uint64_t)u * LN, pol_first);
             const uint4 k0 = __ldg(reinterpret_cast<const uint4 *>(kp + (uint64_t)(2 * u) * LN));
             const uint4 k1 = __ldg(reinterpret_cast<const uint4 *>(kp + (uint64_t)(2 * u + 1) * LN));
             a0 += (uint64_t)d.x * k0.x; a1 += (uint64_t)d.y * k0.y; a2 += (uint64_t)d.z * k0.z; a3 += (uint64_t)d.w * k0.w;
