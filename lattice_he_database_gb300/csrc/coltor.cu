@@ -170,8 +170,8 @@ __global__ void __launch_bounds__(CT_THREADS) coltor_mac_kernel(const MacArgs A)
         }
         const uint32_t q = pick(A.q, l);
         const uint64_t mu = pick(A.mu, l);
-        const uint4 ev0 = *reinterpret_cast<const uint4 *>(A.in + ce * 2 * LN + pt);
-        const uint4 ev1 = *reinterpret_cast<const uint4 *>(A.in + ce * 2 * LN + LN + pt);
+        const uint4 ev0 = ld_policy(A.in + ce * 2 * LN + pt, pol_first);
+        const uint4 ev1 = ld_policy(A.in + ce * 2 * LN + LN + pt, pol_first);
         uint32_t *op = A.out + i * 2 * LN + pt;
         *reinterpret_cast<uint4 *>(op) = make_uint4(mac_final(a0, ev0.x, q, mu), mac_final(a1, ev0.y, q, mu),
                                                     mac_final(a2, ev0.z, q, mu), mac_final(a3, ev0.w, q, mu));

@@ -73,10 +73,10 @@ __global__ void __launch_bounds__(GD_THREADS) gadget_dcp_kernel(const DcpArgs A)
         const uint32_t *xp = A.x + pi * A.x_stride;
         uint32_t r[4][PIR_MAX_RNS];
         if (A.kinv == 1) {
+            const uint64_t pol = policy_evict_first();   // the coefficient rows are read once
 #pragma unroll
             for (uint32_t l = 0; l < PIR_MAX_RNS; ++l) {
-                const uint4 v = l < A.L ? *reinterpret_cast<const uint4 *>(xp + (uint64_t)l * A.N + p)
-                                        : make_uint4(0, 0, 0, 0);
+                const uint4 v = l < A.L ? ld_policy(xp + (uint64_t)l * A.N + p, pol) : make_uint4(0, 0, 0, 0);
                 r[0][l] = v.x; r[1][l] = v.y; r[2][l] = v.z; r[3][l] = v.w;
             }
         } else {
