@@ -109,6 +109,8 @@ __device__ __forceinline__ uint32_t subq(uint32_t a, uint32_t b, uint32_t q) {
 
 // Four consecutive slots per thread.  The ell <= 16 key-switch products of
 // residues below 2^29 sum below 2^62 without reduction.
+// EC = ell when known at compile time (ell = 5: the digit loop unrolled), else 0.
+template <uint32_t EC>
 __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs A) {
     pdl_wait();
     const uint64_t LN = (uint64_t)A.L * A.N;
@@ -127,8 +129,9 @@ __global__ void __launch_bounds__(GD_THREADS) expand_mac_kernel(const ExpMacArgs
         const uint32_t *dp = A.dn + i * A.ell * LN + pt;
         const uint32_t *kp = A.evk + b * A.evk_stride + pt;
         uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0, b0 = 0, b1 = 0, b2 = 0, b3 = 0;
-#pragma unroll 4
-        for (uint32_t u = 0; u < A.ell; ++u) {
+        const uint32_t ell = EC ? EC : A.ell;
+#pragma unroll (EC ? 5 : 4)
+        for (uint32_t u = 0; u < ell; ++u) {
             const uint4 d = ld_policy(dp + (uint64_t)u * LN, pol_first);
             const uint4 k0 = __ldg(reinterpret_cast<const uint4 *>(kp + (uint64_t)(2 * u) * LN));
             const uint4 k1 = __ldg(reinterpret_cast<const uint4 *>(kp + (uint64_t)(2 * u + 1) * LN));
@@ -318,7 +321,10 @@ int one_stage(pir_ctx *ctx, const uint32_t *evk, uint64_t evk_stride, uint32_t e
         ma.q[l] = ctx->q[l];
         ma.mu[l] = ctx->mu[l];
     }
-    pdl_launch(expand_mac_kernel, dim3((unsigned)gadget_grid(ctx, GM * LN / 4)), dim3(GD_THREADS), 0, st, ma);
+    if (ell == 5)
+        pdl_launch(expand_mac_kernel<5>, dim3((unsigned)gadget_grid(ctx, GM * LN / 4)), dim3(GD_THREADS), 0, st, ma);
+    else
+        pdl_launch(expand_mac_kernel<0>, dim3((unsigned)gadget_grid(ctx, GM * LN / 4)), dim3(GD_THREADS), 0, st, ma);
     return launch_status(cudaGetLastError());
 }
 
