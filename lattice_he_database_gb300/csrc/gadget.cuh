@@ -60,7 +60,9 @@ __device__ __forceinline__ u128 crt_value(const DcpArgs &A, const uint32_t (&r)[
     return X;
 }
 
-// One thread per four consecutive output coefficients.
+// One thread per four consecutive output coefficients; EC = ell when known
+// at compile time (the digit loop unrolled), else 0.
+template <uint32_t EC>
 __global__ void __launch_bounds__(GD_THREADS) gadget_dcp_kernel(const DcpArgs A) {
     pdl_wait();
     const uint64_t total4 = A.polys * A.N / 4;
@@ -108,8 +110,10 @@ __global__ void __launch_bounds__(GD_THREADS) gadget_dcp_kernel(const DcpArgs A)
             hi[c] = (uint64_t)(X >> 64);
         }
         const uint32_t m32 = (uint32_t)mask, w = A.w, wr = 64 - A.w;
-        uint32_t *dp = A.d + pi * A.ell * A.N + p;
-        for (uint32_t u = 0; u < A.ell; ++u) {
+        const uint32_t ell = EC ? EC : A.ell;
+        uint32_t *dp = A.d + pi * ell * A.N + p;
+#pragma unroll (EC ? EC : 1)
+        for (uint32_t u = 0; u < ell; ++u) {
             *reinterpret_cast<uint4 *>(dp + (uint64_t)u * A.N) =
                 make_uint4((uint32_t)lo[0] & m32, (uint32_t)lo[1] & m32, (uint32_t)lo[2] & m32, (uint32_t)lo[3] & m32);
 #pragma unroll
@@ -178,7 +182,10 @@ uint64_t gadget_grid(const pir_ctx *ctx, uint64_t work) {
 }
 
 int gadget_dcp_launch(const pir_ctx *ctx, const DcpArgs &A, cudaStream_t st) {
-    pdl_launch(gadget_dcp_kernel, dim3((unsigned)gadget_grid(ctx, A.polys * A.N / 4)), dim3(GD_THREADS), 0, st, A);
+    if (A.ell == 5)
+        pdl_launch(gadget_dcp_kernel<5>, dim3((unsigned)gadget_grid(ctx, A.polys * A.N / 4)), dim3(GD_THREADS), 0, st, A);
+    else
+        pdl_launch(gadget_dcp_kernel<0>, dim3((unsigned)gadget_grid(ctx, A.polys * A.N / 4)), dim3(GD_THREADS), 0, st, A);
     return cudaGetLastError() == cudaSuccess ? PIR_OK : PIR_ERR_CUDA;
 }
 
