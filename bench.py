@@ -125,7 +125,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiler runs)")
     ap.add_argument("--no-configs", action="store_true",
-                    help="default workload only: skip the short timings of the other north-star configurations")
+                    help="default workload only: skip the short timings of the other benchmark configurations")
     return ap.parse_args()
 
 
@@ -1547,19 +1547,19 @@ def run_ours(args, cfg, emit=True):
     return result
 
 
-# The other configurations of the benchmark spec, timed briefly after the
-# headline one in the default run (one GPU), so that their numbers come from
-# the same run: the tiny RowSel, the 6 GiB single query, the 24 GiB 16-query
-# batch on the tensor cores and the 16 GiB x 64 scalar scan.
-NORTH_STAR_CONFIGS = ["tiny", "rowsel_6g", "rowsel_24g_b16", "scalar_16g"]
+# The other benchmark configurations, timed briefly after the headline one in
+# the default run (one GPU), so that their numbers come from the same run:
+# the tiny RowSel, the 6 GiB single query, the 24 GiB 16-query batch on the
+# tensor cores and the 16 GiB x 64 scalar scan.
+OTHER_CONFIGS = ["tiny", "rowsel_6g", "rowsel_24g_b16", "scalar_16g"]
 WORKLOADS["tiny"] = dict(N=4096, L=2, D0=16, D1=16, B=1, domain="ntt",
                          desc="Tiny RowSel: N=4096, 2 primes, D0=16 x D1=16, B=1, NTT-domain query (L2-resident)")
 
 
-def north_star_configs(args):
-    """Short timings (20 steps, CUDA events) of NORTH_STAR_CONFIGS."""
+def other_configs(args):
+    """Short timings (20 steps, CUDA events) of OTHER_CONFIGS."""
     out = {}
-    for name in NORTH_STAR_CONFIGS:
+    for name in OTHER_CONFIGS:
         sub = argparse.Namespace(**vars(args))
         sub.workload, sub.steps, sub.warmup = name, 20, 3
         sub.no_cpu_baseline, sub.no_e2e = True, True
@@ -1589,7 +1589,7 @@ def main():
             and int(os.environ.get("WORLD_SIZE", "1")) == 1):
         line = run_ours(args, cfg, emit=False)
         if line is not None:
-            line["north_star_configs"] = north_star_configs(args)
+            line["other_configs"] = other_configs(args)
             print(json.dumps(line), flush=True)
         return
     if args.impl == "reference":
