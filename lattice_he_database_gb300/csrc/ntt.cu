@@ -254,7 +254,10 @@ int ntt_launch(pir_ctx *ctx, const uint32_t *in, uint32_t *out, uint64_t cnt, vo
     if (ctx->N == (uint32_t)kN4) {
         if (!LIFT && in != out && (uint64_t)((in < out ? out - in : in - out)) < rows * kN4)
             return PIR_ERR_ARG;  // partial overlap
-        if (cnt > 1) {          // two rows of one prime per CTA
+        // two rows of one prime per CTA, unless that leaves SMs idle: a small
+        // launch (the first stages of an expansion, the last of a tournament)
+        // is latency-bound, and one row per CTA halves each CTA's chain
+        if (cnt > 1 && (cnt + 1) / 2 * ctx->L >= (uint64_t)ctx->num_sms) {
             const uint64_t g2 = (cnt + 1) / 2 * ctx->L;
             if (g2 > 0x7fffffffull) return PIR_ERR_ARG;
             if (FWD)
