@@ -123,6 +123,32 @@ __global__ void __launch_bounds__(kT4) coltor_diff_intt4096_kernel(const __grid_
     inv4096x2_rounds(x, y, sa, sb, T, q, A.ninv[l], A.ninv_shoup[l], dst, dst + LN, true);
 }
 
+// The same, one difference row (pair i, polynomial c, prime l) per CTA: for
+// small stages, where a CTA per (pair, prime) would leave SMs idle and each
+// CTA's chain of rounds sets the stage's latency.
+__global__ void __launch_bounds__(kT4) coltor_diff_intt4096_row_kernel(const __grid_constant__ DiffInttArgs A) {
+    pdl_wait();
+    __shared__ __align__(16) uint32_t sm[kN4];
+    const uint64_t i = blockIdx.x / (2 * A.L);
+    const uint32_t c = (blockIdx.x / A.L) & 1u, l = blockIdx.x % A.L;
+    const uint64_t LN = (uint64_t)A.L * kN4;
+    const uint32_t q = A.q[l];
+    const uint2 *T = tw_pairs(A.tw, l, kN4, TW_INV);
+    bool has_odd;
+    const uint64_t ce = even_ct(i, A.Rp, A.n, has_odd);
+    const uint32_t *ev = A.in + ce * 2 * LN + c * LN + (uint64_t)l * kN4;
+    const uint32_t *od = A.in + (ce + 1) * 2 * LN + c * LN + (uint64_t)l * kN4;
+    const uint32_t t = threadIdx.x;
+    uint32_t x[16];
+#pragma unroll
+    for (int k = 0; k < 16; k += 4) {
+        const uint4 e = *reinterpret_cast<const uint4 *>(ev + 16 * t + k);
+        const uint4 o = has_odd ? *reinterpret_cast<const uint4 *>(od + 16 * t + k) : make_uint4(0, 0, 0, 0);
+        x[k] = o.x + q - e.x; x[k + 1] = o.y + q - e.y; x[k + 2] = o.z + q - e.z; x[k + 3] = o.w + q - e.w;
+    }
+    inv4096_rounds(x, sm, T, q, A.ninv[l], A.ninv_shoup[l], A.diff + i * 2 * LN + c * LN + (uint64_t)l * kN4);
+}
+
 struct MacArgs {
     const uint32_t *in;     // [G][n][2][L][N] (the even ciphertexts are added)
     const uint32_t *dn;     // [R][2 ell][L][N] NTT of the digits
@@ -253,8 +279,11 @@ int stage(pir_ctx *ctx, const uint32_t *C, uint64_t c_stride, uint32_t ell, uint
             ia.ninv[l] = ctx->ninv[l];
             ia.ninv_shoup[l] = ctx->ninv_shoup[l];
         }
-        if (R * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
-        pdl_launch(coltor_diff_intt4096_kernel, dim3((unsigned)(R * ctx->L)), dim3(kT4), 0, st, ia);
+        if (R * 2 * ctx->L > 0x7fffffffull) return PIR_ERR_ARG;
+        if (R * ctx->L >= (uint64_t)ctx->num_sms)
+            pdl_launch(coltor_diff_intt4096_kernel, dim3((unsigned)(R * ctx->L)), dim3(kT4), 0, st, ia);
+        else   // a small stage: one row per CTA
+            pdl_launch(coltor_diff_intt4096_row_kernel, dim3((unsigned)(R * 2 * ctx->L)), dim3(kT4), 0, st, ia);
         if (cudaGetLastError() != cudaSuccess) return PIR_ERR_CUDA;
     } else {
         pdl_launch(coltor_diff_kernel, dim3((unsigned)grid_for(ctx, R * 2 * LN / 4)), dim3(CT_THREADS), 0, st, da);

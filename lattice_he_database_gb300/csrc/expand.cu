@@ -83,6 +83,27 @@ __global__ void __launch_bounds__(kT4) expand_intt_a4096_kernel(const __grid_con
                      A.coef + (i1 * A.L + l) * kN4, two);
 }
 
+// The same, one ciphertext's c1 row (ciphertext i, prime l) per CTA: for
+// small stages, where each CTA's chain of rounds sets the stage's latency.
+__global__ void __launch_bounds__(kT4) expand_intt_a4096_row_kernel(const __grid_constant__ InttAArgs A) {
+    pdl_wait();
+    __shared__ __align__(16) uint32_t sm[kN4];
+    const uint64_t i = blockIdx.x / A.L;
+    const uint32_t l = blockIdx.x % A.L;
+    const uint32_t q = A.q[l];
+    const uint2 *T = tw_pairs(A.tw, l, kN4, TW_INV);
+    const uint64_t j = (i / A.per) * A.stride + i % A.per;
+    const uint32_t *src = A.in + ((2 * j + 1) * A.L + l) * kN4;
+    const uint32_t t = threadIdx.x;
+    uint32_t x[16];
+#pragma unroll
+    for (int k = 0; k < 16; k += 4) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(src + 16 * t + k);
+        x[k] = u.x; x[k + 1] = u.y; x[k + 2] = u.z; x[k + 3] = u.w;
+    }
+    inv4096_rounds(x, sm, T, q, A.ninv[l], A.ninv_shoup[l], A.coef + (i * A.L + l) * kN4);
+}
+
 struct ExpMacArgs {
     const uint32_t *in;     // [G][M][2][L][N]
     const uint32_t *dn;     // [G][M][ell][L][N] NTT of the digits of sigma_k(c1)
@@ -274,7 +295,10 @@ int c1_to_coef(pir_ctx *ctx, const uint32_t *in, uint64_t GM, uint32_t *coef, cu
         ia.M = GM;
         ia.per = per;
         ia.stride = stride;
-        pdl_launch(expand_intt_a4096_kernel, dim3((unsigned)((GM + 1) / 2 * ctx->L)), dim3(kT4), 0, st, ia);
+        if ((GM + 1) / 2 * ctx->L >= (uint64_t)ctx->num_sms)
+            pdl_launch(expand_intt_a4096_kernel, dim3((unsigned)((GM + 1) / 2 * ctx->L)), dim3(kT4), 0, st, ia);
+        else   // a small stage: one row per CTA
+            pdl_launch(expand_intt_a4096_row_kernel, dim3((unsigned)(GM * ctx->L)), dim3(kT4), 0, st, ia);
         return cudaGetLastError() == cudaSuccess ? PIR_OK : PIR_ERR_CUDA;
     }
     for (uint64_t b = 0; b < GM / per; ++b)   // one strided copy of the c1 rows per block of `per`

@@ -284,6 +284,30 @@ __device__ __forceinline__ void inv_round16x2(uint32_t (&x)[16], uint32_t (&y)[1
     }
 }
 
+// The three inverse rounds of a 4096-point transform on one row whose
+// first-round inputs (16 consecutive values per thread, in [0, 2q)) are in
+// x; the results (natural order, times N^-1, canonical) go to dst.
+__device__ __forceinline__ void inv4096_rounds(uint32_t (&x)[16], uint32_t *sm, const uint2 *__restrict__ T,
+                                               uint32_t q, uint32_t ni, uint32_t nis, uint32_t *dst) {
+    const uint32_t t = threadIdx.x;
+    const Swz4096 z(t);
+    inv_round16(x, 11, t, T, q);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) sm[z.row(k)] = x[k];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x[k] = sm[z.mid(k)];
+    inv_round16(x, 7, t >> 4, T, q);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) sm[z.mid(k)] = x[k];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x[k] = sm[z.col(k)];
+    inv_round16(x, 3, 0, T, q);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) dst[t + 256 * k] = inv_final(x[k], ni, nis, q);
+}
+
 // The three inverse rounds of a 4096-point transform on two rows of one
 // prime whose first-round inputs (16 consecutive values per thread, in
 // [0, 2q)) are already in x and y; the results (natural order, times N^-1,
